@@ -1,0 +1,470 @@
+"""Benchmark of the DSA sparse-MLA forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 1..5]
+
+A step is one sparse_mla_fwd call (one pass of the whole hot path) over the
+mid-prefill workload of "feat: add XTuner TileLang sparse MLA backend"
+(Performance, Isolated sparse MLA forward): s_q = s_kv = 2119, 8 TP-local
+query heads, d_qk = 576, d_v = 512, topk = 2048, BF16 Q/KV, causal index
+lists padded with -1.  Inputs are seeded synthetic (mla_inputs.config(2)).
+
+Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier
+and a device synchronise.  Before every timed step a 256 MB buffer is
+written so the step starts with a cold L2 (the inputs are smaller than L2);
+each step's kernel is timed with CUDA events on the launching stream and the
+sum over the K steps is the device time (max over ranks).  `value` is the
+nominal-FLOP throughput 2*s_q*h_q*topk*(576+512) summed over ranks; the
+line also carries us/call, gathered-KV GB/s and % of the per-shape roofline.
+With N > 1 (torchrun, one process per GPU) every rank runs its own replica
+of the workload: weak scaling, no collective on the data path.
+
+--impl reference times the float64 CPU oracle (test infrastructure) on the
+host cores instead, on the same workload, as the baseline arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KV_ROW_BYTES = 576 * 2
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("fwd_kernel.cuh", "ptx.cuh", "sparse_mla_api.cu"):
+        with open(os.path.join(ROOT, "serving_sparse_mla_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"fwd_kernel_config{config}_ncu.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def max_over_ranks(vals, dist, device=None):
+    """Elementwise max of per-rank timings (identity with one rank)."""
+    if dist is None:
+        return [float(v) for v in vals]
+    import torch
+    dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_total_ms: float) -> float:
+    """Units processed by all ranks (each runs its own replica) / slowest rank's time."""
+    return flops_per_step * steps * world / (max_total_ms * 1e-3) / 1e12
+
+
+def workload(config: int):
+    import mla_inputs as mi
+    return mi.config(config)
+
+
+def valid_entries(case) -> int:
+    return int((case.indices >= 0).sum())
+
+
+def step_flops(case) -> float:
+    import mla_inputs as mi
+    if hasattr(case, "kv_cache"):
+        n_tok, h = case.batch * case.s_next, case.h_q
+    else:
+        n_tok, h = case.q.shape[0], case.q.shape[1]
+    return mi.nominal_flops(n_tok, h, case.indices.shape[-1])
+
+
+def workload_name(case, config: int) -> str:
+    names = {1: "tiny prefill s_q=s_kv=64 h_q=8",
+             2: "mid prefill s_q=s_kv=2119 h_q=8",
+             3: "wide-head prefill s_q=s_kv=8192 h_q=64",
+             4: "packed varlen prefill 16384 tokens (8192,4096,2048,1024,1024) h_q=64",
+             5: "paged decode batch=16 x 6 MTP tokens, contexts U[4096,32768], page 64, h_q=8"}
+    return names[config] + " d_qk=576 d_v=512 topk=2048 bf16"
+
+
+# ----------------------------------------------------------------------------- oracle on host cores
+
+def _oracle_worker_init(config: int):
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    global _W_CASE
+    _W_CASE = workload(config)
+
+
+def _oracle_worker(tokens):
+    from oracle import sparse_mla_oracle as orc
+    c = _W_CASE
+    t0 = time.perf_counter()
+    if hasattr(c, "kv_cache"):
+        toks = [(t // c.s_next, t % c.s_next) for t in tokens]
+        orc.sparse_mla_decode(c.q, c.kv_cache, c.block_table, c.cache_seqlens, c.indices, c.sm_scale,
+                              c.page_size, tokens=toks)
+    elif hasattr(c, "cu_seqlens_q"):
+        orc.sparse_mla_fwd_varlen(c.q, c.kv, c.indices, c.cu_seqlens_q, c.cu_seqlens_kv, c.sm_scale,
+                                  tokens=tokens)
+    else:
+        orc.sparse_mla_fwd(c.q, c.kv, c.indices, c.sm_scale, tokens=tokens)
+    return time.perf_counter() - t0
+
+
+class OraclePool:
+    """The oracle, unchanged, sharded by token over a spawn process pool with
+    one single-threaded worker per host core."""
+
+    def __init__(self, config: int, cores: int):
+        import multiprocessing as mp
+        self.cores = cores
+        ctx = mp.get_context("spawn")
+        self.pool = ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(config,))
+        self.pool.map(_oracle_worker, [[] for _ in range(cores)])   # wait for every worker
+
+    def run(self, tokens):
+        shards = [tokens[i::self.cores] for i in range(self.cores)]
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_worker, shards)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def oracle_sample(case, config: int):
+    """Token sample for one oracle step: the whole workload for configs 1, 2
+    and 5; for the 8192/16384-token configs a seeded 1/16 sample."""
+    import numpy as np
+    n = case.batch * case.s_next if hasattr(case, "kv_cache") else case.q.shape[0]
+    if config in (1, 2, 5):
+        return list(range(n)), f"all {n} tokens of the workload"
+    rng = np.random.default_rng(config)
+    toks = sorted(rng.choice(n, n // 16, replace=False).tolist())
+    return toks, f"seeded sample of {len(toks)} of {n} tokens (1/16), scaled by FLOPs"
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    case = workload(args.config)
+    cores = os.cpu_count() or 1
+    pool = OraclePool(args.config, cores)
+    toks, sample = oracle_sample(case, args.config)
+    n_tok = case.batch * case.s_next if hasattr(case, "kv_cache") else case.q.shape[0]
+    flops = step_flops(case) * len(toks) / n_tok
+    for _ in range(args.warmup):
+        pool.run(toks)
+    times = [pool.run(toks) for _ in range(args.steps)]
+    pool.close()
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(case, args.config), "sample": sample,
+                   "l2": "n/a (CPU)", "seed": 1000 + args.config},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import serving_sparse_mla_gb300 as smla
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = smla.load()   # raises if the CUDA library is missing: no fallback
+
+    # The oracle pool (spawn) starts before the first GPU work.
+    pool = None
+    if rank == 0 and not args.no_cpu_baseline:
+        pool = OraclePool(args.config, os.cpu_count() or 1)
+
+    case = workload(args.config)
+    stream = torch.cuda.current_stream(dev)
+    is_decode = hasattr(case, "kv_cache")
+    is_varlen = hasattr(case, "cu_seqlens_q")
+    n_tok = case.batch * case.s_next if is_decode else case.q.shape[0]
+    flops = step_flops(case)
+    valid = valid_entries(case)
+    kv_bytes = valid * KV_ROW_BYTES
+
+    # device-resident inputs
+    d = lambda t: t.to(dev)
+    if is_decode:
+        inputs = dict(q=d(case.q), kv=d(case.kv_cache), bt=d(case.block_table), sl=d(case.cache_seqlens),
+                      idx=d(case.indices))
+        ws = torch.empty(max(1, smla.decode_workspace_size(case.batch, case.s_next, case.h_q, 2048)),
+                         dtype=torch.uint8, device=dev)
+    elif is_varlen:
+        inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices), cuq=d(case.cu_seqlens_q),
+                      cuk=d(case.cu_seqlens_kv))
+    else:
+        inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices))
+    h_q = case.h_q if is_decode else case.q.shape[1]
+    out = torch.empty((n_tok, h_q, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((n_tok, h_q), dtype=torch.float32, device=dev)
+
+    def call(inp):
+        if is_decode:
+            smla.sparse_mla_decode(inp["q"], inp["kv"], inp["bt"], inp["sl"], inp["idx"], case.sm_scale,
+                                   case.page_size, workspace=ws, out=out.view(case.batch, case.s_next, h_q, 512),
+                                   lse=lse.view(case.batch, case.s_next, h_q), stream=stream)
+        elif is_varlen:
+            smla.sparse_mla_fwd_varlen(inp["q"], inp["kv"], inp["idx"], inp["cuq"], inp["cuk"], case.sm_scale,
+                                       out=out, lse=lse, stream=stream)
+        else:
+            smla.sparse_mla_fwd(inp["q"], inp["kv"], inp["idx"], case.sm_scale, out=out, lse=lse, stream=stream)
+
+    launches_per_step = 1
+    if is_decode and smla.decode_workspace_size(case.batch, case.s_next, case.h_q, 2048) > 0:
+        launches_per_step = 2
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def timed_loop(k, body, flush_l2=True):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+        for i in range(k):
+            if flush_l2:
+                flush.zero_()
+            starts[i].record(stream)
+            body()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    for _ in range(max(3, args.warmup)):
+        call(inputs)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    times = timed_loop(args.steps, lambda: call(inputs))
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    # secondary: warm L2 (the pages' method has no flush)
+    warm = timed_loop(max(args.steps, 20), lambda: call(inputs), flush_l2=False)
+
+    # end to end through the C ABI with host buffers: pinned H2D of the inputs,
+    # the call, D2H of out and lse, all inside the timed region
+    host = {k: v.cpu().pin_memory() for k, v in inputs.items()}
+    dev2 = {k: torch.empty_like(v) for k, v in inputs.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev2[k].copy_(host[k], non_blocking=True)
+        call(dev2)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e2e_times = timed_loop(args.steps, e2e_step)
+    barrier()
+
+    total_ms, e2e_ms = max_over_ranks([sum(times), sum(e2e_times)], dist, dev)
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_kind = load_peaks()
+    ms = total_ms / args.steps
+    us = ms * 1e3
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    p_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    p_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    roof_us = max(flops / (p_tf * 1e12), kv_bytes / (p_bw * 1e9)) * 1e6
+    bound = "hbm" if kv_bytes / (p_bw * 1e9) >= flops / (p_tf * 1e12) else "tensor"
+    fwd_ms = ms  # one fwd launch per step (plus a combine launch for split decode)
+    if bound == "hbm":
+        achieved = kv_bytes / (fwd_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": p_bw, "unit": "GB/s",
+                    "frac": achieved / p_bw, "traffic": profiled_traffic(args.config),
+                    "peak_kind": f"{peak_kind} copy bandwidth (burst)",
+                    "algorithmic_bytes_per_launch": kv_bytes,
+                    "note": "achieved = valid entries x 1152 B / mean launch time (cold L2)"}
+    else:
+        achieved = flops / (fwd_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": p_tf, "unit": "TFLOP/s",
+                    "frac": achieved / p_tf, "traffic": profiled_traffic(args.config),
+                    "peak_kind": f"{peak_kind} bf16 (burst)", "algorithmic_flops_per_launch": flops}
+
+    cpu = None
+    if pool is not None:
+        toks, sample = oracle_sample(case, args.config)
+        wall = pool.run(toks)
+        cpu = {"value": flops * len(toks) / n_tok / wall / 1e12, "unit": "TFLOP/s", "cores": pool.cores,
+               "kind": "oracle", "sample": sample, "seconds": wall}
+        pool.close()
+
+    line = {
+        "metric": "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)",
+        "value": whole_job_tflops(flops, args.steps, world, total_ms), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(case, args.config), "seed": 1000 + args.config,
+                   "l2": "256 MB buffer written before every timed step (cold L2)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": us, "tflops_per_gpu": tflops, "gathered_kv_GBps": gbs,
+        "roofline_us": roof_us, "roofline_pct": 100.0 * roof_us / us,
+        "warm_l2": {"us_per_call": statistics.median(warm) * 1e3,
+                    "roofline_pct": 100.0 * roof_us / (statistics.median(warm) * 1e3)},
+        "valid_entries": valid, "nominal_flops": flops,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops * world / (e2e_ms / args.steps * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        tdist.init_process_group(backend=backend)
+        dist = tdist
+    try:
+        return run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,169 @@
+/*
+ * sparse_mla.h -- C ABI of the GB300 (sm_103a) DSA sparse-MLA attention forward.
+ *
+ * The operation (all three entry points).  For every query token t and
+ * query head h, over the token's list of top-k KV indices:
+ *
+ *   valid entries  j : index != -1 and inside the token's KV range
+ *   s_j      = sm_scale * sum_{d<576} q[t,h,d] * kv[row_j, d]
+ *   lse[t,h] = ln sum_j exp(s_j)                  (natural log, fp32)
+ *   out[t,h] = sum_j exp(s_j - lse[t,h]) * kv[row_j, 0:512]   (bf16)
+ *
+ * One latent KV head of 576 bf16 values per token is shared by every query
+ * head; its first 512 values are the value ("[Feature] Add optional FlashMLA
+ * backend for DSA Sparse MLA", Runtime constraints: kv_group=1,
+ * value_dim=512).  The shapes d_qk=576, d_v=512, topk=2048 at 8 TP-local
+ * heads are the isolated-forward workload of "feat: add XTuner TileLang
+ * sparse MLA backend" (Performance), whose Validation section covers
+ * -1-padded index lists; the same page's Summary has one kernel serve
+ * packed prefill and zero-copy BF16 paged-cache decode.  Output and LSE are
+ * the two results the FlashMLA page aligns across implementations
+ * (Motivation).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library never frees or retains them.  Tensors are dense row-major.
+ *   - q, kv / kv_cache and out must be 16-byte aligned; index, length and
+ *     lse arrays 4-byte aligned.
+ *   - Entries are taken with multiplicity (a repeated index counts once per
+ *     occurrence).  Index VALUES are never an error: -1, any other negative
+ *     value and anything at or past the token's KV length is masked and the
+ *     masked row is never read.  A token with no valid entry gets out = 0
+ *     and lse = -inf.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream): no host synchronisation, no allocation.  The first
+ *     call on a device performs one-time set-up (kernel attributes, the
+ *     driver entry point for tensor maps) and should not be made during
+ *     stream capture.
+ *   - Errors: arguments are checked on the host before any launch and a
+ *     non-OK status means nothing was launched, except SPARSE_MLA_ERR_CUDA
+ *     after a failed launch.  No exception or abort crosses the ABI.
+ *   - Supported device: compute capability 10.3 (GB300); other devices get
+ *     SPARSE_MLA_ERR_UNSUPPORTED_ARCH.  d_qk must be 576 and d_v 512
+ *     (SPARSE_MLA_ERR_UNSUPPORTED_SHAPE otherwise).  Any h_q >= 1 and
+ *     topk >= 1 are accepted.
+ *   - Device-side waits are bounded.  A kernel whose wait expires records a
+ *     code in a per-device error word (sparse_mla_get_device_error), leaves
+ *     its outputs undefined and returns; later launches on that device do no
+ *     work until the word is cleared.
+ */
+#ifndef SPARSE_MLA_H
+#define SPARSE_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPARSE_MLA_OK = 0,
+  SPARSE_MLA_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, negative size, bad count */
+  SPARSE_MLA_ERR_UNSUPPORTED_SHAPE = 2,  /* d_qk != 576 or d_v != 512 */
+  SPARSE_MLA_ERR_UNSUPPORTED_ARCH = 3,   /* current device is not sm_103 */
+  SPARSE_MLA_ERR_CUDA = 4,               /* a CUDA runtime/driver call or launch failed */
+  SPARSE_MLA_ERR_DEVICE_TIMEOUT = 5,     /* reported by sparse_mla_get_device_error */
+  SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL = 6 /* decode workspace below sparse_mla_decode_workspace_size */
+} sparse_mla_status_t;
+
+/*
+ * Dense-layout forward (prefill over one sequence or any token batch).
+ *
+ *   q        bf16 [s_q, h_q, d_qk]
+ *   kv       bf16 [s_kv, d_qk]      (the [s_kv, 1, d_qk] single-head layout)
+ *   indices  int32 [s_q, topk]      (the [s_q, 1, topk] layout); row index
+ *                                   into kv, -1 padded; valid iff 0 <= i < s_kv
+ *   sm_scale score scale (1/sqrt(576) for the pages' workloads)
+ *   out      bf16 [s_q, h_q, d_v]   written
+ *   lse      fp32 [s_q, h_q]        written, natural log
+ *
+ * s_q == 0 is a no-op.  s_kv == 0 masks everything.
+ */
+sparse_mla_status_t sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices, float sm_scale,
+                                   void* out, float* lse, int s_q, int s_kv, int h_q, int d_qk, int d_v,
+                                   int topk, void* stream);
+
+/*
+ * Packed (varlen) prefill: `batch` sequences concatenated along the token
+ * axis.  Token t belongs to the sequence b with cu_seqlens_q[b] <= t <
+ * cu_seqlens_q[b+1]; its indices are LOCAL to that sequence: entry i reads
+ * kv row cu_seqlens_kv[b] + i and is valid iff
+ * 0 <= i < cu_seqlens_kv[b+1] - cu_seqlens_kv[b].
+ *
+ *   q             bf16 [total_q, h_q, d_qk]
+ *   kv            bf16 [total_kv, d_qk]
+ *   indices       int32 [total_q, topk]
+ *   cu_seqlens_q  int32 [batch+1] device, non-decreasing, cu_seqlens_q[0] = 0,
+ *                 cu_seqlens_q[batch] = total_q
+ *   cu_seqlens_kv int32 [batch+1] device, same rules against total_kv
+ *   out / lse     as sparse_mla_fwd with s_q = total_q
+ *
+ * Rows computed from malformed cu_seqlens_kv that fall outside [0, total_kv)
+ * are masked, never read.
+ */
+sparse_mla_status_t sparse_mla_fwd_varlen(const void* q, const void* kv, const int32_t* indices,
+                                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv,
+                                          int batch, float sm_scale, void* out, float* lse, int total_q,
+                                          int total_kv, int h_q, int d_qk, int d_v, int topk,
+                                          void* stream);
+
+/*
+ * Bytes of device workspace sparse_mla_decode needs for this shape on the
+ * current device (0 when it needs none).  The value depends on the device's
+ * SM count; query it on the device that will run the call.
+ */
+size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v, int topk);
+
+/*
+ * Decode over a paged BF16 KV cache, read in place.
+ *
+ *   q             bf16 [batch, s_next, h_q, d_qk]   s_next query tokens per request
+ *                 (the speculative tokens of a request, e.g. 6 for MTP5)
+ *   kv_cache      bf16 [num_blocks, page_size, d_qk]
+ *   block_table   int32 [batch, max_blocks]: page of logical block k of request b
+ *   cache_seqlens int32 [batch]: tokens in request b's cache
+ *   indices       int32 [batch, s_next, topk]: LOGICAL positions in the request;
+ *                 entry i is valid iff 0 <= i < cache_seqlens[b], i / page_size <
+ *                 max_blocks and the page entry lies in [0, num_blocks); it reads
+ *                 cache slot block_table[b][i / page_size] * page_size + i % page_size
+ *   out           bf16 [batch, s_next, h_q, d_v]
+ *   lse           fp32 [batch, s_next, h_q]
+ *   workspace     device buffer of at least sparse_mla_decode_workspace_size(...)
+ *                 bytes (may be NULL when that size is 0); the library writes
+ *                 per-split partial results there during the call.  Two calls
+ *                 that may run concurrently need separate workspaces.
+ *
+ * num_blocks * page_size must fit in int32.
+ */
+sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                                      const int32_t* cache_seqlens, const int32_t* indices, float sm_scale,
+                                      void* out, float* lse, int batch, int s_next, int h_q, int d_qk,
+                                      int d_v, int topk, int page_size, int max_blocks, int num_blocks,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* sparse_mla_status_string(sparse_mla_status_t status);
+
+/*
+ * Device error word of the current device: 0 when no kernel has timed out,
+ * otherwise the code the first timed-out kernel recorded (its role in bits
+ * 8..11).  Synchronises with the device.  Returns SPARSE_MLA_OK, or
+ * SPARSE_MLA_ERR_CUDA if the read fails.
+ */
+sparse_mla_status_t sparse_mla_get_device_error(int* code);
+
+/* Clear the current device's error word (synchronous). */
+sparse_mla_status_t sparse_mla_clear_device_error(void);
+
+/*
+ * Set the bound on every device-side wait, in nanoseconds, for launches made
+ * after the call (process-wide; default 1 s; 0 restores the default).
+ */
+void sparse_mla_set_wait_timeout_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MLA_H */

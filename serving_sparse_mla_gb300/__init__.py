@@ -1,0 +1,13 @@
+"""GB300 (sm_103a) DSA sparse-MLA attention forward: a C-ABI CUDA library
+(csrc/, include/sparse_mla.h) and its thin Python binding."""
+from .binding import (  # noqa: F401
+    SparseMLAError,
+    clear_device_error,
+    decode_workspace_size,
+    get_device_error,
+    load,
+    set_wait_timeout_ns,
+    sparse_mla_decode,
+    sparse_mla_fwd,
+    sparse_mla_fwd_varlen,
+)

@@ -1,0 +1,185 @@
+"""Thin ctypes binding over the C ABI in include/sparse_mla.h.
+
+Argument marshalling only: shape/dtype/device checks, raw pointers and sizes,
+output allocation through torch.  Every step of the attention runs in the
+CUDA library; there is no fallback.  Loading fails loudly when the library
+has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+_LIB: Optional[ctypes.CDLL] = None
+
+c_int, c_float, c_void_p, c_size_t = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+STATUS = {0: "SPARSE_MLA_OK", 1: "SPARSE_MLA_ERR_INVALID_ARG", 2: "SPARSE_MLA_ERR_UNSUPPORTED_SHAPE",
+          3: "SPARSE_MLA_ERR_UNSUPPORTED_ARCH", 4: "SPARSE_MLA_ERR_CUDA", 5: "SPARSE_MLA_ERR_DEVICE_TIMEOUT",
+          6: "SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL"}
+
+# name -> (restype, argtypes); the exported surface of include/sparse_mla.h
+SIGNATURES = {
+    "sparse_mla_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_float, c_void_p, c_void_p,
+                               c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "sparse_mla_fwd_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_float,
+                                      c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "sparse_mla_decode_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "sparse_mla_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_void_p,
+                                  c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                  c_void_p, c_size_t, c_void_p]),
+    "sparse_mla_status_string": (ctypes.c_char_p, [c_int]),
+    "sparse_mla_get_device_error": (c_int, [ctypes.POINTER(c_int)]),
+    "sparse_mla_clear_device_error": (c_int, []),
+    "sparse_mla_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
+}
+
+
+class SparseMLAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the built library (raises if it is missing)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or lib_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built ({p}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise SparseMLAError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_scale: float,
+                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """q [s_q,h_q,576] bf16, kv [s_kv,576] or [s_kv,1,576] bf16,
+    indices [s_q,topk] or [s_q,1,topk] int32 -> (out [s_q,h_q,512] bf16,
+    lse [s_q,h_q] fp32)."""
+    lib = load()
+    s_q, h_q, d_qk = q.shape
+    s_kv = kv.shape[0]
+    topk = indices.shape[-1]
+    for t, dt, n in ((q, torch.bfloat16, "q"), (kv, torch.bfloat16, "kv"), (indices, torch.int32, "indices")):
+        _need(t, dt, n)
+    d_v = 512
+    if out is None:
+        out = torch.empty((s_q, h_q, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=q.device)
+    st = lib.sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), float(sm_scale), _ptr(out), _ptr(lse),
+                            s_q, s_kv, h_q, d_qk, d_v, topk, _stream(stream))
+    _check(st, "sparse_mla_fwd")
+    return out, lse
+
+
+def sparse_mla_fwd_varlen(q, kv, indices, cu_seqlens_q, cu_seqlens_kv, sm_scale, out=None, lse=None,
+                          stream=None):
+    """Packed prefill; indices are local to each token's sequence."""
+    lib = load()
+    total_q, h_q, d_qk = q.shape
+    total_kv = kv.shape[0]
+    topk = indices.shape[-1]
+    batch = cu_seqlens_q.numel() - 1
+    for t, dt, n in ((q, torch.bfloat16, "q"), (kv, torch.bfloat16, "kv"), (indices, torch.int32, "indices"),
+                     (cu_seqlens_q, torch.int32, "cu_seqlens_q"), (cu_seqlens_kv, torch.int32, "cu_seqlens_kv")):
+        _need(t, dt, n)
+    if out is None:
+        out = torch.empty((total_q, h_q, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((total_q, h_q), dtype=torch.float32, device=q.device)
+    st = lib.sparse_mla_fwd_varlen(_ptr(q), _ptr(kv), _ptr(indices), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+                                   batch, float(sm_scale), _ptr(out), _ptr(lse), total_q, total_kv, h_q, d_qk,
+                                   512, topk, _stream(stream))
+    _check(st, "sparse_mla_fwd_varlen")
+    return out, lse
+
+
+def decode_workspace_size(batch: int, s_next: int, h_q: int, topk: int, d_v: int = 512) -> int:
+    return int(load().sparse_mla_decode_workspace_size(batch, s_next, h_q, d_v, topk))
+
+
+def sparse_mla_decode(q, kv_cache, block_table, cache_seqlens, indices, sm_scale, page_size=None,
+                      workspace: Optional[torch.Tensor] = None, out=None, lse=None, stream=None):
+    """Paged decode.  q [b,s_next,h_q,576]; kv_cache [num_blocks,page,576]
+    (or [num_blocks,page,1,576]); block_table [b,max_blocks];
+    cache_seqlens [b]; indices [b,s_next,topk] logical positions."""
+    lib = load()
+    batch, s_next, h_q, d_qk = q.shape
+    num_blocks = kv_cache.shape[0]
+    page = kv_cache.shape[1] if page_size is None else page_size
+    max_blocks = block_table.shape[1]
+    topk = indices.shape[-1]
+    for t, dt, n in ((q, torch.bfloat16, "q"), (kv_cache, torch.bfloat16, "kv_cache"),
+                     (block_table, torch.int32, "block_table"), (cache_seqlens, torch.int32, "cache_seqlens"),
+                     (indices, torch.int32, "indices")):
+        _need(t, dt, n)
+    if out is None:
+        out = torch.empty((batch, s_next, h_q, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((batch, s_next, h_q), dtype=torch.float32, device=q.device)
+    need = lib.sparse_mla_decode_workspace_size(batch, s_next, h_q, 512, topk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.sparse_mla_decode(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(cache_seqlens), _ptr(indices),
+                               float(sm_scale), _ptr(out), _ptr(lse), batch, s_next, h_q, d_qk, 512, topk, page,
+                               max_blocks, num_blocks, _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "sparse_mla_decode")
+    return out, lse
+
+
+def get_device_error() -> int:
+    code = c_int(0)
+    _check(load().sparse_mla_get_device_error(ctypes.byref(code)), "sparse_mla_get_device_error")
+    return code.value
+
+
+def clear_device_error():
+    _check(load().sparse_mla_clear_device_error(), "sparse_mla_clear_device_error")
+
+
+def set_wait_timeout_ns(ns: int):
+    load().sparse_mla_set_wait_timeout_ns(int(ns))

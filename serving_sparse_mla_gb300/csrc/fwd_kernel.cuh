@@ -1,0 +1,662 @@
+// DSA sparse-MLA attention forward for sm_103a (tcgen05 + TMA gather4).
+//
+// Computes, per query token t and head h over the token's top-k index list
+// ("feat: add XTuner TileLang sparse MLA backend", Performance, Isolated
+// sparse MLA forward: dqk=576, dv=512, topk=2048, BF16 Q/KV):
+//
+//   s_j   = sm_scale * q[t,h,:] . kv[r_j,:]              (576-wide latent rows)
+//   LSE   = ln sum_j exp(s_j)                             (fp32, natural log)
+//   out   = sum_j exp(s_j - LSE) * kv[r_j, 0:512]         (bf16)
+//
+// over the valid entries j (not -1 and inside the token's KV range; the
+// TileLang page's Validation covers -1 padded lists).  A list with no valid
+// entry gives out = 0 and LSE = -inf.  One latent KV head is shared by all
+// query heads and its first 512 columns are the value ("[Feature] Add
+// optional FlashMLA backend for DSA Sparse MLA", Runtime constraints:
+// kv_group=1, value_dim=512).  The same kernel serves dense prefill, packed
+// (cu_seqlens) prefill and the paged BF16 cache (TileLang page, Summary);
+// only the index -> row mapping differs.
+//
+// Work decomposition: one CTA per (token, top-k split, head group).  The
+// index list is walked in blocks of 128 entries; a block with no valid
+// entry is skipped.  Per block:
+//
+//   warp 0 (producer)  maps the 128 indices to KV rows and gathers the rows
+//                      with TMA tile::gather4 (4 rows x 64 columns per
+//                      instruction, 128B swizzle) into shared memory:
+//                      four 128x128 "pair" tiles for columns 0..511 (the
+//                      value part) and one 128x64 tile for the rope columns.
+//                      Masked rows use an out-of-range row coordinate, which
+//                      TMA fills with zeros; they are never read from HBM.
+//   warp 1 (MMA)       one thread issues tcgen05.mma:
+//                        S^T[128 x N]  = K_blk[128 x 576] . Q^T[576 x N]
+//                        O^T[512 x N] += V^T[512 x 128]  . P^T[128 x N]
+//                      (swap-AB: the kv rows fill M=128, the heads are N, so
+//                      8 heads cost N=16 instead of a 64-row pad).  V^T is
+//                      the same gathered tile read through an MN-major
+//                      descriptor; no second copy.  Accumulators live in TMEM.
+//   warps 2..5         thread r owns TMEM lane r = kv row r of the block:
+//   (softmax)          loads its S^T row, masks, reduces the per-head block
+//                      max across the 128 rows (warp transpose-reduce plus a
+//                      shared-memory step), keeps a lazily updated running
+//                      max (the O accumulator is rescaled only when a head's
+//                      max grows by more than 2^8), writes P^T = exp2(s - m)
+//                      as bf16 into shared memory, and at the end normalises
+//                      O^T and writes out / LSE.
+//
+// All waits are bounded (see ptx.cuh); a timed-out CTA records an error in
+// the device error word, drains its in-flight copies and MMAs, frees TMEM
+// and returns.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace smla {
+
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kBlk = 128;                    // index entries (kv rows) per block
+constexpr int kChunkBytes = kBlk * 128;      // 128 rows x 64 bf16 columns
+constexpr int kPairBytes = 2 * kChunkBytes;  // 128 rows x 128 columns
+constexpr int kInfoDepth = 4;
+constexpr int kThreads = 192;
+constexpr float kLazyRescale = 8.0f;         // log2 units
+constexpr int kMaxSmem = 232448;
+
+enum Mode : int { kDense = 0, kVarlen = 1, kPaged = 2 };
+
+enum ErrCode : int { kErrProducerWait = 0x101, kErrMmaWait = 0x201, kErrSoftmaxWait = 0x301 };
+
+struct FwdParams {
+  const __nv_bfloat16* q;   // [n_tok, h_q, 576]
+  const int32_t* indices;   // [n_tok, topk]
+  __nv_bfloat16* out;       // [n_tok, h_q, 512]
+  float* lse;               // [n_tok, h_q]
+  float* part_o;            // [splits, n_tok, h_q, 512]  (splits > 1)
+  float* part_lse;          // [splits, n_tok, h_q]
+  const int32_t* cu_q;      // varlen: [batch+1]
+  const int32_t* cu_kv;     // varlen: [batch+1]
+  const int32_t* block_table;  // paged: [batch, max_blocks]
+  const int32_t* seqlens;      // paged: [batch]
+  int n_tok, h_q, topk, mode;
+  int n_rows;               // rows of the KV tensor map
+  int s_kv, batch, s_next, page_size, max_blocks, num_blocks;
+  int splits;
+  float scale_log2;         // sm_scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+__device__ int g_device_error;
+
+template <int N>
+struct Layout {
+  static_assert(N == 16 || N == 32 || N == 64, "head group width");
+  static constexpr int kNV = (N == 64) ? 4 : 5;       // value pair-tile ring
+  static constexpr int kNR = (N == 16) ? 2 : 1;       // rope / P^T ring
+  static constexpr int kPRow = N * 2;                 // bytes of one P^T row
+  static constexpr uint32_t kPSwz = N == 64 ? SWZ_128B : (N == 32 ? SWZ_64B : SWZ_32B);
+  static constexpr int kTmemCols = N == 64 ? 512 : (N == 32 ? 256 : 128);
+  static constexpr int kQOff = 0;
+  static constexpr int kVOff = 9 * N * 128;
+  static constexpr int kROff = kVOff + kNV * kPairBytes;
+  static constexpr int kMiscOff = kROff + kNR * kChunkBytes;
+};
+
+struct __align__(16) Misc {
+  uint64_t v_full[5], v_empty[5], rp_full[2], rp_empty[2];
+  uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
+  uint64_t q_full, s_full, p_full, o_full, drain;
+  int32_t info_blk[kInfoDepth];
+  uint32_t info_mask[kInfoDepth][4];
+  float red[4][64];
+  float mrun[64];
+  float alpha[64];
+  float fin[64];
+  uint32_t tmem_base;
+  int abort_flag;
+  int prior_error;
+};
+
+template <int N>
+constexpr int smem_bytes() {
+  return Layout<N>::kMiscOff + static_cast<int>(sizeof(Misc)) + 1024;
+}
+static_assert(smem_bytes<64>() <= kMaxSmem, "smem budget (64 heads)");
+static_assert(smem_bytes<32>() <= kMaxSmem, "smem budget (32 heads)");
+static_assert(smem_bytes<16>() <= kMaxSmem, "smem budget (16 heads)");
+
+// ------------------------------------------------------------------ helpers
+
+struct TokCtx {
+  int kv_lo;
+  int kv_len;
+  const int32_t* table;
+};
+
+__device__ __forceinline__ TokCtx token_context(const FwdParams& p, int tok) {
+  TokCtx c;
+  c.table = nullptr;
+  if (p.mode == kDense) {
+    c.kv_lo = 0;
+    c.kv_len = p.s_kv;
+  } else if (p.mode == kVarlen) {
+    int lo = 0, hi = p.batch;  // largest b with cu_q[b] <= tok
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.cu_q + mid) <= tok) lo = mid; else hi = mid;
+    }
+    c.kv_lo = __ldg(p.cu_kv + lo);
+    c.kv_len = __ldg(p.cu_kv + lo + 1) - c.kv_lo;
+  } else {
+    const int b = tok / p.s_next;
+    c.kv_lo = 0;
+    c.kv_len = __ldg(p.seqlens + b);
+    c.table = p.block_table + static_cast<size_t>(b) * p.max_blocks;
+  }
+  return c;
+}
+
+// KV tensor-map row read by one index entry, or -1 when the entry is masked.
+__device__ __forceinline__ int map_entry(const FwdParams& p, const TokCtx& c, int idx) {
+  if (idx < 0 || idx >= c.kv_len) return -1;
+  int row;
+  if (p.mode == kPaged) {
+    const int pg = idx / p.page_size;
+    if (pg >= p.max_blocks) return -1;
+    const int blk = __ldg(c.table + pg);
+    if (blk < 0 || blk >= p.num_blocks) return -1;
+    row = blk * p.page_size + (idx - pg * p.page_size);
+  } else {
+    row = c.kv_lo + idx;
+  }
+  return (row >= 0 && row < p.n_rows) ? row : -1;
+}
+
+__device__ __forceinline__ void raise_error(Misc& m, int code) {
+  *reinterpret_cast<volatile int*>(&m.abort_flag) = 1;
+  atomicCAS(&g_device_error, 0, code);
+}
+
+// Transposing butterfly over the warp: lane l ends with the reduction (over
+// the 32 lanes) of a contiguous run of heads and writes it to dst[head].
+template <int N, bool kMax>
+__device__ __forceinline__ void warp_xreduce(float (&v)[N], int lane, float* dst) {
+  int cnt = N;
+  int base = 0;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (cnt > 1) {
+      const int half = cnt >> 1;
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+          v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+      }
+      if (upper) base += half;
+      cnt = half;
+    } else {
+      const float recv = __shfl_xor_sync(0xffffffffu, v[0], off);
+      v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if (i < cnt) dst[base + i] = v[i];
+}
+
+// bar.sync over the 128 softmax threads, returning the OR of `pred`.
+__device__ __forceinline__ bool bar_red_or_128(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+// ------------------------------------------------------------------ roles
+
+template <int N>
+__device__ bool run_producer(const CUtensorMap* tmap, const FwdParams& p, Misc& m, uint8_t* sbase,
+                             int tok, int jb, int je, uint64_t deadline, uint32_t (&vfills)[5],
+                             uint32_t (&rfills)[2]) {
+  using L = Layout<N>;
+  const int lane = static_cast<int>(lane_id());
+  const volatile int* ab = &m.abort_flag;
+  const TokCtx ctx = token_context(p, tok);
+  const int32_t* irow = p.indices + static_cast<size_t>(tok) * p.topk;
+  const uint32_t vbase = smem_u32(sbase + L::kVOff);
+  const uint32_t rbase = smem_u32(sbase + L::kROff);
+  uint32_t vuse = 0;
+  int n = 0;
+  for (int j = jb; j < je; ++j) {
+    int rows[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = j * kBlk + lane * 4 + i;
+      const int idx = e < p.topk ? __ldg(irow + e) : -1;
+      rows[i] = map_entry(p, ctx, idx);
+    }
+    uint32_t bal[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bal[i] = __ballot_sync(0xffffffffu, rows[i] >= 0);
+    if ((bal[0] | bal[1] | bal[2] | bal[3]) == 0u) continue;
+
+    const int k = n % kInfoDepth;
+    if (!mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab)) return false;
+    if (lane == 0) {
+      m.info_blk[k] = j;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m.info_mask[k][i] = bal[i];
+      mbar_arrive(smem_u32(&m.info_full[k]));
+    }
+#pragma unroll
+    for (int pr = 0; pr < 4; ++pr) {
+      const uint32_t s = (vuse + pr) % L::kNV;
+      const uint32_t ph = ((vuse + pr) / L::kNV) & 1u;
+      if (!mbar_wait(smem_u32(&m.v_empty[s]), ph ^ 1u, deadline, ab)) return false;
+      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&m.v_full[s]), kPairBytes);
+      __syncwarp();
+      const uint32_t dst = vbase + s * kPairBytes + lane * 512;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        tma_gather4(dst + c * kChunkBytes, tmap, (2 * pr + c) * 64, rows[0], rows[1], rows[2], rows[3],
+                    smem_u32(&m.v_full[s]));
+      vfills[s] += 1;
+    }
+    vuse += 4;
+    const uint32_t rs = n % L::kNR;
+    const uint32_t rph = (n / L::kNR) & 1u;
+    if (!mbar_wait(smem_u32(&m.rp_empty[rs]), rph ^ 1u, deadline, ab)) return false;
+    if (lane == 0) mbar_arrive_expect_tx(smem_u32(&m.rp_full[rs]), kChunkBytes);
+    __syncwarp();
+    tma_gather4(rbase + rs * kChunkBytes + lane * 512, tmap, 512, rows[0], rows[1], rows[2], rows[3],
+                smem_u32(&m.rp_full[rs]));
+    rfills[rs] += 1;
+    ++n;
+  }
+  const int k = n % kInfoDepth;
+  if (!mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab)) return false;
+  if (lane == 0) {
+    m.info_blk[k] = -1;
+    mbar_arrive(smem_u32(&m.info_full[k]));
+  }
+  return true;
+}
+
+template <int N>
+__device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline) {
+  using L = Layout<N>;
+  const volatile int* ab = &m.abort_flag;
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(128, N, false, false);
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
+  const uint32_t qbase = smem_u32(sbase + L::kQOff);
+  const uint32_t vbase = smem_u32(sbase + L::kVOff);
+  const uint32_t rbase = smem_u32(sbase + L::kROff);
+  const uint32_t tS = tmem;
+  const uint32_t tO = tmem + N;
+  if (!mbar_wait(smem_u32(&m.q_full), 0, deadline, ab)) return false;
+  tc_fence_after();
+  uint32_t vuse = 0;
+  int n = 0;
+  for (;;) {
+    const int k = n % kInfoDepth;
+    if (!mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab)) return false;
+    const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
+    mbar_arrive(smem_u32(&m.info_empty[k]));
+    if (blk < 0) break;
+    // S^T = K_blk . Q^T over the 9 column chunks (value pairs, then rope).
+#pragma unroll 1
+    for (int pr = 0; pr < 4; ++pr) {
+      const uint32_t s = (vuse + pr) % L::kNV;
+      if (!mbar_wait(smem_u32(&m.v_full[s]), ((vuse + pr) / L::kNV) & 1u, deadline, ab)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = smem_desc(vbase + s * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
+          const uint64_t b = smem_desc(qbase + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+          mma_bf16_ss(tS, a, b, kIdescQK, (pr | c | kk) != 0 ? 1u : 0u);
+        }
+      }
+    }
+    const uint32_t rs = n % L::kNR;
+    if (!mbar_wait(smem_u32(&m.rp_full[rs]), (n / L::kNR) & 1u, deadline, ab)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
+      const uint64_t b = smem_desc(qbase + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+      mma_bf16_ss(tS, a, b, kIdescQK, 1u);
+    }
+    mma_commit(smem_u32(&m.s_full));
+    // O^T += V^T . P^T once the softmax has written P^T into the rope slot.
+    if (!mbar_wait(smem_u32(&m.p_full), n & 1, deadline, ab)) return false;
+    tc_fence_after();
+#pragma unroll 1
+    for (int mt = 0; mt < 4; ++mt) {
+      const uint32_t s = (vuse + mt) % L::kNV;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
+        const uint64_t b = smem_desc(rbase + rs * kChunkBytes + ks * 16 * L::kPRow, 16 * L::kPRow * 8,
+                                     8 * L::kPRow, L::kPSwz);
+        mma_bf16_ss(tO + mt * N, a, b, kIdescPV, (n > 0 || ks > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&m.v_empty[s]));
+    }
+    mma_commit(smem_u32(&m.rp_empty[rs]));
+    vuse += 4;
+    ++n;
+  }
+  if (n > 0) mma_commit(smem_u32(&m.o_full));
+  else mbar_arrive(smem_u32(&m.o_full));
+  return true;
+}
+
+template <int N>
+__device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int tok,
+                            int split, int h0, int hv, uint64_t deadline) {
+  using L = Layout<N>;
+  const volatile int* ab = &m.abort_flag;
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(lane_id());
+  const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..127
+  const int q4 = warp & 3;                             // TMEM lane quarter of this warp
+  const int row = q4 * 32 + lane;                      // kv row of the block == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+  const uint32_t tS = tmem + lane_off;
+  const uint32_t tO = tmem + lane_off + N;
+  const uint32_t qbase = smem_u32(sbase + L::kQOff);
+  const uint32_t rbase = smem_u32(sbase + L::kROff);
+
+  // Q for heads [h0, h0+N) -> shared memory, K-major with the 128B swizzle;
+  // heads past h_q are zero.
+  {
+    const __nv_bfloat16* qt = p.q + (static_cast<size_t>(tok) * p.h_q + h0) * kDqk;
+    for (int x = tid; x < N * 72; x += 128) {
+      const int h = x / 72, rem = x - h * 72, c = rem >> 3, piece = rem & 7;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (h < hv) v = __ldg(reinterpret_cast<const uint4*>(qt + static_cast<size_t>(h) * kDqk + c * 64 + piece * 8));
+      st_shared_v4(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4), v.x, v.y, v.z, v.w);
+    }
+    fence_proxy_async_smem();
+    if (tid < N) m.mrun[tid] = -INFINITY;
+    named_bar_sync(1, 128);
+    if (tid == 0) mbar_arrive(smem_u32(&m.q_full));
+  }
+
+  float lpart[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) lpart[i] = 0.f;
+
+  int n = 0;
+  for (;;) {
+    const int k = n % kInfoDepth;
+    if (!mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab)) return false;
+    const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
+    const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&m.info_mask[k][row & 3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
+    if (blk < 0) break;
+    const bool valid = ((bits >> (row >> 2)) & 1u) != 0u;
+
+    if (!mbar_wait(smem_u32(&m.s_full), n & 1, deadline, ab)) return false;
+    tc_fence_after();
+    float s[N];
+#pragma unroll
+    for (int g = 0; g < N / 16; ++g) tmem_ld16(tS + g * 16, s + g * 16);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < N; ++i) s[i] = valid ? s[i] * p.scale_log2 : -INFINITY;
+
+    {
+      float t[N];
+#pragma unroll
+      for (int i = 0; i < N; ++i) t[i] = s[i];
+      warp_xreduce<N, true>(t, lane, m.red[q4]);
+    }
+    named_bar_sync(1, 128);
+    bool grew = false;
+    if (tid < N) {
+      const float bm = fmaxf(fmaxf(m.red[0][tid], m.red[1][tid]), fmaxf(m.red[2][tid], m.red[3][tid]));
+      const float mo = m.mrun[tid];
+      const float mn = (bm > mo + kLazyRescale) ? bm : mo;
+      const float al = fast_exp2(mo - mn);
+      m.alpha[tid] = al;
+      m.mrun[tid] = mn;
+      grew = (mn != mo);
+    }
+    const bool rescale = bar_red_or_128(grew);
+    if (rescale) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) lpart[i] *= m.alpha[i];
+      if (n > 0) {
+        // O^T holds the sum through the previous block (its PV completed
+        // before S of this block was committed): rescale each head column.
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int g = 0; g < N / 16; ++g) {
+            float o[16];
+            tmem_ld16(tO + mt * N + g * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= m.alpha[g * 16 + i];
+            tmem_st16(tO + mt * N + g * 16, o);
+          }
+        }
+        tmem_wait_st();
+      }
+    }
+    // P^T row (bf16) into the rope slot of this block, MN-major swizzled.
+    const uint32_t prow = rbase + (n % L::kNR) * kChunkBytes + row * L::kPRow;
+    const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+      float pv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        pv[i] = fast_exp2(s[c * 8 + i] - m.mrun[c * 8 + i]);
+        lpart[c * 8 + i] += pv[i];
+      }
+      st_shared_v4(prow + ((static_cast<uint32_t>(c) ^ sw) << 4), pack_bf16x2(pv[0], pv[1]),
+                   pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&m.p_full));
+    ++n;
+  }
+
+  // ---------------------------------------------------------- epilogue
+  if (!mbar_wait(smem_u32(&m.o_full), 0, deadline, ab)) return false;
+  tc_fence_after();
+  warp_xreduce<N, false>(lpart, lane, m.red[q4]);
+  named_bar_sync(1, 128);
+  const size_t tok_h = static_cast<size_t>(tok) * p.h_q + h0;
+  if (tid < N) {
+    const float l = m.red[0][tid] + m.red[1][tid] + m.red[2][tid] + m.red[3][tid];
+    float lse;
+    if (n > 0) {
+      lse = (m.mrun[tid] + log2f(l)) * 0.69314718055994530942f;
+      m.fin[tid] = 1.0f / l;
+    } else {
+      lse = -INFINITY;
+      m.fin[tid] = 0.f;
+    }
+    if (tid < hv) {
+      if (p.splits > 1) p.part_lse[static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + tid] = lse;
+      else p.lse[tok_h + tid] = lse;
+    }
+  }
+  named_bar_sync(1, 128);
+#pragma unroll 1
+  for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+    for (int g = 0; g < N / 16; ++g) {
+      float o[16];
+      if (n > 0) {
+        tmem_ld16(tO + mt * N + g * 16, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = 0.f;
+      }
+      const int dv = mt * 128 + row;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int h = g * 16 + i;
+        if (h < hv) {
+          const float val = o[i] * m.fin[h];
+          if (p.splits > 1)
+            p.part_o[(static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + h) * kDv + dv] = val;
+          else
+            p.out[(tok_h + h) * kDv + dv] = __float2bfloat16_rn(val);
+        }
+      }
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_fwd_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ FwdParams p) {
+  using L = Layout<N>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Misc& m = *reinterpret_cast<Misc*>(sbase + L::kMiscOff);
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(lane_id());
+  const int tok = static_cast<int>(blockIdx.x) / p.splits;
+  const int split = static_cast<int>(blockIdx.x) % p.splits;
+  const int h0 = static_cast<int>(blockIdx.y) * 64;
+  const int hv = min(N, p.h_q - h0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 5; ++i) { mbar_init(smem_u32(&m.v_full[i]), 1); mbar_init(smem_u32(&m.v_empty[i]), 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(smem_u32(&m.rp_full[i]), 1); mbar_init(smem_u32(&m.rp_empty[i]), 1); }
+    for (int i = 0; i < kInfoDepth; ++i) {
+      mbar_init(smem_u32(&m.info_full[i]), 1);
+      mbar_init(smem_u32(&m.info_empty[i]), 5);
+    }
+    mbar_init(smem_u32(&m.q_full), 1);
+    mbar_init(smem_u32(&m.s_full), 1);
+    mbar_init(smem_u32(&m.p_full), 128);
+    mbar_init(smem_u32(&m.o_full), 1);
+    mbar_init(smem_u32(&m.drain), 1);
+    m.abort_flag = 0;
+    m.prior_error = *reinterpret_cast<volatile int*>(&g_device_error);
+    fence_mbar_init();
+  }
+  if (warp == 0) prefetch_tmap(&tmap_kv);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&m.tmem_base), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (m.prior_error == 0) {
+    const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+    const int nb = (p.topk + kBlk - 1) / kBlk;
+    const int jb = static_cast<int>((static_cast<long long>(split) * nb) / p.splits);
+    const int je = static_cast<int>((static_cast<long long>(split + 1) * nb) / p.splits);
+    if (warp == 0) {
+      uint32_t vfills[5] = {0, 0, 0, 0, 0};
+      uint32_t rfills[2] = {0, 0};
+      if (!run_producer<N>(&tmap_kv, p, m, sbase, tok, jb, je, deadline, vfills, rfills) && lane == 0)
+        raise_error(m, kErrProducerWait);
+      // Drain: wait (bounded) until every gather this warp issued has landed,
+      // whether or not the consumers got to it.
+      const uint64_t dl2 = global_timer_ns() + 100000000ull;
+      const int never = 0;
+      for (int s = 0; s < L::kNV; ++s)
+        if (vfills[s]) mbar_wait(smem_u32(&m.v_full[s]), (vfills[s] - 1) & 1u, dl2, &never);
+      for (int s = 0; s < L::kNR; ++s)
+        if (rfills[s]) mbar_wait(smem_u32(&m.rp_full[s]), (rfills[s] - 1) & 1u, dl2, &never);
+    } else if (warp == 1) {
+      if (lane == 0) {
+        if (!run_mma<N>(m, sbase, tmem, deadline)) raise_error(m, kErrMmaWait);
+        // Drain: every MMA this thread issued completes before TMEM is freed.
+        const int never = 0;
+        mma_commit(smem_u32(&m.drain));
+        mbar_wait(smem_u32(&m.drain), 0, global_timer_ns() + 100000000ull, &never);
+      }
+      __syncwarp();
+    } else {
+      if (!run_softmax<N>(p, m, sbase, tmem, tok, split, h0, hv, deadline)) raise_error(m, kErrSoftmaxWait);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
+}
+
+// ------------------------------------------------------------------ helpers kernels
+
+// Merge per-split partial results: LSE = ln sum_s exp(LSE_s),
+// out = sum_s exp(LSE_s - LSE) * O_s (each O_s already normalised).
+__global__ void __launch_bounds__(128) combine_splits_kernel(const float* __restrict__ part_o,
+                                                             const float* __restrict__ part_lse,
+                                                             __nv_bfloat16* __restrict__ out,
+                                                             float* __restrict__ lse, int n_rows_th,
+                                                             int splits) {
+  const int th = static_cast<int>(blockIdx.x);
+  if (th >= n_rows_th) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[static_cast<size_t>(s) * n_rows_th + th]);
+  const int d = static_cast<int>(threadIdx.x) * 4;
+  if (mx == -INFINITY) {
+    if (threadIdx.x == 0) lse[th] = -INFINITY;
+    __nv_bfloat162 z = __floats2bfloat162_rn(0.f, 0.f);
+    reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(th) * kDv + d)[0] = z;
+    reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(th) * kDv + d)[1] = z;
+    return;
+  }
+  float sum = 0.f;
+  for (int s = 0; s < splits; ++s) sum += expf(part_lse[static_cast<size_t>(s) * n_rows_th + th] - mx);
+  const float tot = mx + logf(sum);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < splits; ++s) {
+    const float ls = part_lse[static_cast<size_t>(s) * n_rows_th + th];
+    if (ls == -INFINITY) continue;
+    const float w = expf(ls - tot);
+    const float4 v = *reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(s) * n_rows_th + th) * kDv + d);
+    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  }
+  if (threadIdx.x == 0) lse[th] = tot;
+  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(th) * kDv + d);
+  o2[0] = __floats2bfloat162_rn(acc.x, acc.y);
+  o2[1] = __floats2bfloat162_rn(acc.z, acc.w);
+}
+
+// Every entry masked (no KV rows at all): out = 0, LSE = -inf.
+__global__ void fill_masked_kernel(__nv_bfloat16* __restrict__ out, float* __restrict__ lse, long long n_th) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n_th) lse[i] = -INFINITY;
+  const long long n_el = n_th * kDv;
+  for (long long e = i; e < n_el; e += static_cast<long long>(gridDim.x) * blockDim.x)
+    out[e] = __float2bfloat16_rn(0.f);
+}
+
+}  // namespace smla

@@ -1,0 +1,306 @@
+// C-ABI entry points: host-side validation, tensor-map encoding, launch
+// planning (head-group width, top-k splits) and launches on the caller's
+// stream.  See include/sparse_mla.h for the contract of each call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fwd_kernel.cuh"
+#include "sparse_mla.h"
+
+namespace {
+
+using smla::FwdParams;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceState {
+  bool probed = false;
+  bool supported = false;
+  int sm_count = 0;
+  bool attrs_set = false;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+sparse_mla_status_t device_setup(int* sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPARSE_MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SPARSE_MLA_ERR_CUDA;
+    st.supported = (major == 10 && minor == 3);
+    st.sm_count = sms;
+    st.probed = true;
+  }
+  if (!st.supported) return SPARSE_MLA_ERR_UNSUPPORTED_ARCH;
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return SPARSE_MLA_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  if (!st.attrs_set) {
+    if (cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::smem_bytes<16>()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::smem_bytes<32>()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::smem_bytes<64>()) != cudaSuccess)
+      return SPARSE_MLA_ERR_CUDA;
+    st.attrs_set = true;
+  }
+  *sm_count = st.sm_count;
+  return SPARSE_MLA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Head-group width N (the MMA's N): 16, 32 or 64; more heads use several
+// 64-wide groups (one CTA per group).
+int head_width(int h_q) { return h_q <= 16 ? 16 : (h_q <= 32 ? 32 : 64); }
+int head_groups(int h_q) { return (h_q + 63) / 64; }
+
+// Number of top-k splits per token: enough CTAs for two per SM, never more
+// than the number of 128-entry blocks.
+int plan_splits(long long n_tok, int h_q, int topk, int sm_count) {
+  const long long units = n_tok * head_groups(h_q);
+  const int nb = (topk + smla::kBlk - 1) / smla::kBlk;
+  if (units <= 0) return 1;
+  long long s = (2LL * sm_count + units - 1) / units;
+  if (s < 1) s = 1;
+  if (s > nb) s = nb;
+  if (s > 32) s = 32;
+  return static_cast<int>(s);
+}
+
+sparse_mla_status_t encode_kv_map(CUtensorMap* map, const void* kv, long long n_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(smla::kDqk), static_cast<cuuint64_t>(n_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(smla::kDqk) * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SPARSE_MLA_OK : SPARSE_MLA_ERR_INVALID_ARG;
+}
+
+sparse_mla_status_t launch_fwd(const CUtensorMap& map, const FwdParams& p, cudaStream_t stream) {
+  const int N = head_width(p.h_q);
+  dim3 grid(static_cast<unsigned>(p.n_tok) * static_cast<unsigned>(p.splits), static_cast<unsigned>(head_groups(p.h_q)));
+  dim3 block(smla::kThreads);
+  if (N == 16)
+    smla::sparse_mla_fwd_kernel<16><<<grid, block, smla::smem_bytes<16>(), stream>>>(map, p);
+  else if (N == 32)
+    smla::sparse_mla_fwd_kernel<32><<<grid, block, smla::smem_bytes<32>(), stream>>>(map, p);
+  else
+    smla::sparse_mla_fwd_kernel<64><<<grid, block, smla::smem_bytes<64>(), stream>>>(map, p);
+  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+}
+
+sparse_mla_status_t launch_fill(void* out, float* lse, long long n_th, cudaStream_t stream) {
+  if (n_th <= 0) return SPARSE_MLA_OK;
+  const long long blocks = (n_th + 255) / 256;
+  smla::fill_masked_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(
+      static_cast<__nv_bfloat16*>(out), lse, n_th);
+  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+}
+
+FwdParams base_params(const void* q, const int32_t* indices, float sm_scale, void* out, float* lse, int n_tok,
+                      int h_q, int topk) {
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.indices = indices;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.n_tok = n_tok;
+  p.h_q = h_q;
+  p.topk = topk;
+  p.splits = 1;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  unsigned long long t = g_timeout_ns.load();
+  p.timeout_ns = t ? t : kDefaultTimeoutNs;
+  return p;
+}
+
+sparse_mla_status_t check_common(const void* q, const int32_t* indices, const void* out, const float* lse,
+                                 long long n_tok, int h_q, int d_qk, int d_v, int topk) {
+  if (n_tok < 0 || h_q < 1 || topk < 1) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (d_qk != smla::kDqk || d_v != smla::kDv) return SPARSE_MLA_ERR_UNSUPPORTED_SHAPE;
+  if (n_tok > INT_MAX / 2 || static_cast<long long>(h_q) * 64 > INT_MAX) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_tok == 0) return SPARSE_MLA_OK;
+  if (!q || !indices || !out || !lse) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(indices, 4) || !aligned(lse, 4))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  return SPARSE_MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sparse_mla_status_t sparse_mla_fwd(const void* q, const void* kv, const int32_t* indices, float sm_scale, void* out,
+                                   float* lse, int s_q, int s_kv, int h_q, int d_qk, int d_v, int topk,
+                                   void* stream) {
+  sparse_mla_status_t st = check_common(q, indices, out, lse, s_q, h_q, d_qk, d_v, topk);
+  if (st != SPARSE_MLA_OK) return st;
+  if (s_kv < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (s_q == 0) return SPARSE_MLA_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (s_kv == 0) return launch_fill(out, lse, static_cast<long long>(s_q) * h_q, cs);
+  if (!kv || !aligned(kv, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  CUtensorMap map;
+  if ((st = encode_kv_map(&map, kv, s_kv)) != SPARSE_MLA_OK) return st;
+  FwdParams p = base_params(q, indices, sm_scale, out, lse, s_q, h_q, topk);
+  p.mode = smla::kDense;
+  p.n_rows = s_kv;
+  p.s_kv = s_kv;
+  return launch_fwd(map, p, cs);
+}
+
+sparse_mla_status_t sparse_mla_fwd_varlen(const void* q, const void* kv, const int32_t* indices,
+                                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                                          float sm_scale, void* out, float* lse, int total_q, int total_kv,
+                                          int h_q, int d_qk, int d_v, int topk, void* stream) {
+  sparse_mla_status_t st = check_common(q, indices, out, lse, total_q, h_q, d_qk, d_v, topk);
+  if (st != SPARSE_MLA_OK) return st;
+  if (total_kv < 0 || batch < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (total_q > 0 && (batch < 1 || !cu_seqlens_q || !cu_seqlens_kv || !aligned(cu_seqlens_q, 4) ||
+                      !aligned(cu_seqlens_kv, 4)))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (total_q == 0) return SPARSE_MLA_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (total_kv == 0) return launch_fill(out, lse, static_cast<long long>(total_q) * h_q, cs);
+  if (!kv || !aligned(kv, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  CUtensorMap map;
+  if ((st = encode_kv_map(&map, kv, total_kv)) != SPARSE_MLA_OK) return st;
+  FwdParams p = base_params(q, indices, sm_scale, out, lse, total_q, h_q, topk);
+  p.mode = smla::kVarlen;
+  p.n_rows = total_kv;
+  p.batch = batch;
+  p.cu_q = cu_seqlens_q;
+  p.cu_kv = cu_seqlens_kv;
+  return launch_fwd(map, p, cs);
+}
+
+size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v, int topk) {
+  if (batch < 1 || s_next < 1 || h_q < 1 || topk < 1 || d_v != smla::kDv) return 0;
+  int sms = 0;
+  if (device_setup(&sms) != SPARSE_MLA_OK) return 0;
+  const long long n_tok = static_cast<long long>(batch) * s_next;
+  const int splits = plan_splits(n_tok, h_q, topk, sms);
+  if (splits <= 1) return 0;
+  return static_cast<size_t>(splits) * static_cast<size_t>(n_tok) * static_cast<size_t>(h_q) *
+         (static_cast<size_t>(smla::kDv) + 1) * sizeof(float);
+}
+
+sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                                      const int32_t* cache_seqlens, const int32_t* indices, float sm_scale, void* out,
+                                      float* lse, int batch, int s_next, int h_q, int d_qk, int d_v, int topk,
+                                      int page_size, int max_blocks, int num_blocks, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (batch < 0 || s_next < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  const long long n_tok = static_cast<long long>(batch) * s_next;
+  sparse_mla_status_t st = check_common(q, indices, out, lse, n_tok, h_q, d_qk, d_v, topk);
+  if (st != SPARSE_MLA_OK) return st;
+  if (page_size < 1 || max_blocks < 0 || num_blocks < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * page_size > INT_MAX) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_tok > 0 && (!block_table || !cache_seqlens || !aligned(block_table, 4) || !aligned(cache_seqlens, 4)))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (n_tok == 0) return SPARSE_MLA_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (num_blocks == 0 || max_blocks == 0) return launch_fill(out, lse, n_tok * h_q, cs);
+  if (!kv_cache || !aligned(kv_cache, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  const int splits = plan_splits(n_tok, h_q, topk, sms);
+  const size_t need = sparse_mla_decode_workspace_size(batch, s_next, h_q, d_v, topk);
+  if (splits > 1 && (workspace_bytes < need || !workspace)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (splits > 1 && !aligned(workspace, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  CUtensorMap map;
+  if ((st = encode_kv_map(&map, kv_cache, static_cast<long long>(num_blocks) * page_size)) != SPARSE_MLA_OK)
+    return st;
+  FwdParams p = base_params(q, indices, sm_scale, out, lse, static_cast<int>(n_tok), h_q, topk);
+  p.mode = smla::kPaged;
+  p.n_rows = num_blocks * page_size;
+  p.batch = batch;
+  p.s_next = s_next;
+  p.page_size = page_size;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
+  p.block_table = block_table;
+  p.seqlens = cache_seqlens;
+  p.splits = splits;
+  if (splits > 1) {
+    float* ws = static_cast<float*>(workspace);
+    p.part_o = ws;
+    p.part_lse = ws + static_cast<size_t>(splits) * n_tok * h_q * smla::kDv;
+  }
+  if ((st = launch_fwd(map, p, cs)) != SPARSE_MLA_OK) return st;
+  if (splits > 1) {
+    const int n_th = static_cast<int>(n_tok * h_q);
+    smla::combine_splits_kernel<<<n_th, 128, 0, cs>>>(p.part_o, p.part_lse, static_cast<__nv_bfloat16*>(out), lse,
+                                                      n_th, splits);
+    if (cudaGetLastError() != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
+  }
+  return SPARSE_MLA_OK;
+}
+
+const char* sparse_mla_status_string(sparse_mla_status_t s) {
+  switch (s) {
+    case SPARSE_MLA_OK: return "SPARSE_MLA_OK";
+    case SPARSE_MLA_ERR_INVALID_ARG: return "SPARSE_MLA_ERR_INVALID_ARG";
+    case SPARSE_MLA_ERR_UNSUPPORTED_SHAPE: return "SPARSE_MLA_ERR_UNSUPPORTED_SHAPE";
+    case SPARSE_MLA_ERR_UNSUPPORTED_ARCH: return "SPARSE_MLA_ERR_UNSUPPORTED_ARCH";
+    case SPARSE_MLA_ERR_CUDA: return "SPARSE_MLA_ERR_CUDA";
+    case SPARSE_MLA_ERR_DEVICE_TIMEOUT: return "SPARSE_MLA_ERR_DEVICE_TIMEOUT";
+    case SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL: return "SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL";
+  }
+  return "SPARSE_MLA_UNKNOWN_STATUS";
+}
+
+sparse_mla_status_t sparse_mla_get_device_error(int* code) {
+  if (!code) return SPARSE_MLA_ERR_INVALID_ARG;
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, smla::g_device_error, sizeof(int)) != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
+  *code = v;
+  return SPARSE_MLA_OK;
+}
+
+sparse_mla_status_t sparse_mla_clear_device_error(void) {
+  const int zero = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(smla::g_device_error, &zero, sizeof(int)) != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
+  return SPARSE_MLA_OK;
+}
+
+void sparse_mla_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
+
+}  // extern "C"

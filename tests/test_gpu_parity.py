@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on
+the same seeded inputs (tolerances in tests/parity.py)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+from oracle import sparse_mla_oracle as orc
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def _run_fwd(smla, case, kv=None, indices=None):
+    kv = case.kv if kv is None else kv
+    idx = case.indices if indices is None else indices
+    out, lse = smla.sparse_mla_fwd(case.q.to(DEV), kv.to(DEV), idx.to(DEV), case.sm_scale)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _check_fwd(smla, case, kv=None, indices=None, tokens=None, what=""):
+    kv = case.kv if kv is None else kv
+    idx = case.indices if indices is None else indices
+    o, l = _run_fwd(smla, case, kv, idx)
+    if tokens is not None:
+        o, l = o[tokens], l[tokens]
+    ref_o, ref_l = orc.sparse_mla_fwd(case.q, kv, idx, case.sm_scale, tokens=tokens)
+    return compare(o, l, ref_o, ref_l, what or case.name)
+
+
+@pytest.fixture(scope="module")
+def smla(cuda_lib):
+    import serving_sparse_mla_gb300 as pkg
+    pkg.clear_device_error()
+    yield pkg
+    assert pkg.get_device_error() == 0
+
+
+# ---------------------------------------------------------------- dense prefill
+
+def test_tiny_prefill_config(smla):
+    """s_q = s_kv = 64, h = 8, topk = 2048: every causal position listed."""
+    _check_fwd(smla, mi.config(1))
+
+
+@pytest.mark.parametrize("h_q", [1, 8, 16, 24, 64, 100, 128])
+def test_head_counts(smla, h_q):
+    case = mi.prefill_case(200 + h_q, s_q=37, s_kv=420, h_q=h_q, topk=384)
+    _check_fwd(smla, case)
+
+
+@pytest.mark.parametrize("topk", [1, 64, 128, 192, 300, 2048])
+def test_topk_values(smla, topk):
+    case = mi.prefill_case(300 + topk, s_q=160, s_kv=700, h_q=8, topk=topk)
+    _check_fwd(smla, case)
+
+
+def test_scattered_padding_and_poisoned_rows(smla):
+    """-1 anywhere in the list; every KV row no list references is NaN."""
+    case = mi.prefill_case(401, s_q=200, s_kv=900, h_q=8, topk=512)
+    idx = mi.scatter_padding(mi._gen(402), case.indices)
+    kv = mi.poison_unreferenced(case.kv, case.referenced)
+    _check_fwd(smla, case, kv=kv, indices=idx)
+
+
+def test_masking_edge_cases(smla):
+    s_q, s_kv, topk = 8, 50, 256
+    case = mi.prefill_case(403, s_q=s_q, s_kv=s_kv, h_q=16, topk=topk)
+    idx = torch.full((s_q, topk), -1, dtype=torch.int32)
+    idx[1, 200] = 7                                   # single valid entry, late block
+    idx[2, :] = torch.randint(-9, -1, (topk,), dtype=torch.int32)    # all negative
+    idx[3, :] = torch.randint(s_kv, s_kv + 1000, (topk,), dtype=torch.int32)  # all past the end
+    idx[4, :5] = torch.tensor([3, 3, 3, 9, 9])       # duplicates
+    idx[5, 0::2] = torch.arange(0, topk // 2, dtype=torch.int32) % s_kv   # every other entry
+    idx[6, :] = torch.arange(topk, dtype=torch.int32) % s_kv            # all valid, repeats
+    idx[7, 127:129] = torch.tensor([11, 12])          # straddles a 128-entry block edge
+    kv = mi.poison_unreferenced(case.kv, torch.unique(idx[(idx >= 0) & (idx < s_kv)]))
+    o, l = _run_fwd(smla, case, kv, idx)
+    ref_o, ref_l = orc.sparse_mla_fwd(case.q, kv, idx, case.sm_scale)
+    compare(o, l, ref_o, ref_l, "masking")
+    # rows 0, 2, 3: nothing valid -> exactly +0 and -inf
+    for t in (0, 2, 3):
+        assert np.all(o[t] == 0.0) and np.all(np.isneginf(l[t]))
+    # row 1: a single valid entry returns that value row (bf16-exact)
+    assert np.array_equal(o[1], np.broadcast_to(case.kv[7, :512].float().numpy(), o[1].shape))
+
+
+def test_s_kv_zero_and_empty_batch(smla):
+    q = torch.randn(3, 8, 576, device=DEV).to(torch.bfloat16)
+    kv = torch.empty(0, 576, device=DEV, dtype=torch.bfloat16)
+    idx = torch.zeros(3, 64, dtype=torch.int32, device=DEV)
+    out, lse = smla.sparse_mla_fwd(q, kv, idx, 0.1)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+    out, lse = smla.sparse_mla_fwd(q[:0], kv, idx[:0], 0.1)
+    assert out.shape == (0, 8, 512)
+
+
+def test_mid_prefill_config_all_tokens(smla):
+    """s_q = s_kv = 2119, h = 8, topk = 2048 (the pages' SWE-like shape)."""
+    case = mi.config(2)
+    _check_fwd(smla, case)
+
+
+def test_wide_head_config_sampled(smla):
+    """s_q = s_kv = 8192, h = 64, topk = 2048 at the launch the bench times;
+    sampled tokens (edges, the 2047/2048 boundary and a seeded spread)."""
+    case = mi.config(3)
+    g = np.random.default_rng(3)
+    toks = sorted(set([0, 1, 2, 127, 128, 2046, 2047, 2048, 4095, 8190, 8191]
+                      + g.choice(8192, 53, replace=False).tolist()))
+    _check_fwd(smla, case, tokens=toks)
+
+
+# ---------------------------------------------------------------- packed prefill
+
+def _check_varlen(smla, case, tokens=None, what=""):
+    d = lambda t: t.to(DEV)
+    out, lse = smla.sparse_mla_fwd_varlen(d(case.q), d(case.kv), d(case.indices), d(case.cu_seqlens_q),
+                                          d(case.cu_seqlens_kv), case.sm_scale)
+    torch.cuda.synchronize()
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    if tokens is not None:
+        o, l = o[tokens], l[tokens]
+    ref_o, ref_l = orc.sparse_mla_fwd_varlen(case.q, case.kv, case.indices, case.cu_seqlens_q,
+                                             case.cu_seqlens_kv, case.sm_scale, tokens=tokens)
+    return compare(o, l, ref_o, ref_l, what or case.name)
+
+
+@pytest.mark.parametrize("h_q", [8, 64])
+def test_varlen_small(smla, h_q):
+    case = mi.varlen_case(500 + h_q, [130, 1, 257, 64, 300], h_q, topk=256)
+    case.kv = mi.poison_unreferenced(case.kv, case.referenced)
+    _check_varlen(smla, case)
+
+
+def test_varlen_config_sampled(smla):
+    """16384 packed tokens (8192, 4096, 2048, 1024, 1024), h = 64."""
+    case = mi.config(4)
+    cu = case.cu_seqlens_q.tolist()
+    g = np.random.default_rng(4)
+    toks = set(g.choice(cu[-1], 40, replace=False).tolist())
+    for a, b in zip(cu[:-1], cu[1:]):
+        toks.update([a, a + 1, b - 1, min(a + 2047, b - 1), min(a + 2048, b - 1)])
+    _check_varlen(smla, case, tokens=sorted(toks))
+
+
+# ---------------------------------------------------------------- paged decode
+
+def _check_decode(smla, case, tokens=None):
+    d = lambda t: t.to(DEV)
+    out, lse = smla.sparse_mla_decode(d(case.q), d(case.kv_cache), d(case.block_table), d(case.cache_seqlens),
+                                      d(case.indices), case.sm_scale, case.page_size)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy().reshape(-1, case.h_q, 512)
+    l = lse.cpu().numpy().reshape(-1, case.h_q)
+    ref_o, ref_l = orc.sparse_mla_decode(case.q, case.kv_cache, case.block_table, case.cache_seqlens,
+                                         case.indices, case.sm_scale, case.page_size)
+    return compare(o, l, ref_o, ref_l, case.name)
+
+
+def test_decode_small(smla):
+    case = mi.decode_case(601, batch=3, s_next=2, h_q=8, lo=100, hi=900, topk=256, page=64, spare_pages=4)
+    _check_decode(smla, case)
+
+
+def test_decode_page16_wide_heads(smla):
+    case = mi.decode_case(602, batch=2, s_next=3, h_q=64, lo=50, hi=400, topk=192, page=16, spare_pages=3)
+    _check_decode(smla, case)
+
+
+def test_decode_config_all_tokens(smla):
+    """batch 16 x 6 MTP tokens, contexts U[4096, 32768], 64-token pages in a
+    shuffled pool with every unread slot NaN, h = 8, topk = 2048."""
+    _check_decode(smla, mi.config(5))
+
+
+# ---------------------------------------------------------------- failure detection
+
+def test_device_wait_timeout_reports_and_recovers(smla):
+    """A 1 ns bound on device waits makes the kernel give up: it records a
+    code, drains, frees TMEM and returns; the host reads the code, clears it
+    and the next call is correct."""
+    case = mi.prefill_case(701, s_q=16, s_kv=600, h_q=8, topk=512)
+    try:
+        smla.set_wait_timeout_ns(1)
+        _run_fwd(smla, case)
+        code = smla.get_device_error()
+    finally:
+        smla.set_wait_timeout_ns(0)
+    assert code != 0 and (code & 0xff) == 1
+    smla.clear_device_error()
+    assert smla.get_device_error() == 0
+    _check_fwd(smla, case)

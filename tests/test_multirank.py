@@ -1,0 +1,51 @@
+"""N>1 host logic of bench.py on CPU: two gloo ranks, each timing its own
+replica; the job takes the slowest rank's time and counts every rank's units."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    mine = [10.0 + 5.0 * rank, 20.0 - 3.0 * rank]
+    got = bench.max_over_ranks(mine, dist)
+    dist.barrier()
+    q.put((rank, got))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0] == res[1] == [15.0, 20.0]
+
+
+def test_whole_job_value_counts_every_replica():
+    import bench
+    one = bench.whole_job_tflops(75.5e9, 10, 1, 5.0)
+    two = bench.whole_job_tflops(75.5e9, 10, 2, 5.0)
+    assert two == pytest.approx(2 * one)
+    assert one == pytest.approx(75.5e9 * 10 / 5e-3 / 1e12)
+    assert bench.max_over_ranks([1.0, 2.0], None) == [1.0, 2.0]

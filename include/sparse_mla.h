@@ -142,6 +142,41 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
                                       int d_v, int topk, int page_size, int max_blocks, int num_blocks,
                                       void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * sparse_mla_decode without a caller workspace, for callers that cannot
+ * allocate device memory at the point of the call: code running inside a
+ * serving engine whose allocator owns every byte of the device (a KV-cache
+ * pool sized to fill HBM, with allocation forbidden after start-up), plug-ins
+ * that receive device pointers from a host runtime but have no allocator of
+ * their own, and hot paths that must not call cudaMalloc because it can
+ * synchronise the device.  The pages describe no counterpart of this entry
+ * point; it exists for such callers only.
+ *
+ * Arguments, layouts and results are those of sparse_mla_decode, minus the
+ * workspace.  The per-split partial results go to one scratch array of
+ * sparse_mla_decode_noalloc_max_scratch_bytes() bytes (8 MiB) that the
+ * library holds in device memory on every GPU that loads it, until the
+ * process exits.  A shape whose sparse_mla_decode_workspace_size exceeds that
+ * maximum is rejected with SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL before any
+ * launch (use sparse_mla_decode with a workspace for it).  The call makes no
+ * cudaMalloc, cudaFree or other allocating call.
+ *
+ * Every call shares the one scratch array, which keeps the last call's
+ * contents; each call overwrites every entry it later reads, so nothing has
+ * to be cleared.  Calls whose kernels overlap on the GPU (different streams,
+ * or different host threads) race on the array: serialise them.  The first
+ * call on a device looks up the array's device address once (with that device
+ * current); make that first call before any stream capture.
+ */
+sparse_mla_status_t sparse_mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t* block_table,
+                                              const int32_t* cache_seqlens, const int32_t* indices, float sm_scale,
+                                              void* out, float* lse, int batch, int s_next, int h_q, int d_qk,
+                                              int d_v, int topk, int page_size, int max_blocks, int num_blocks,
+                                              void* stream);
+
+/* Size in bytes of the scratch array sparse_mla_decode_noalloc uses. */
+size_t sparse_mla_decode_noalloc_max_scratch_bytes(void);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* sparse_mla_status_string(sparse_mla_status_t status);
 

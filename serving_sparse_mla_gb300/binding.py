@@ -33,6 +33,10 @@ SIGNATURES = {
     "sparse_mla_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_void_p,
                                   c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                   c_void_p, c_size_t, c_void_p]),
+    "sparse_mla_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_void_p,
+                                          c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                          c_void_p]),
+    "sparse_mla_decode_noalloc_max_scratch_bytes": (c_size_t, []),
     "sparse_mla_status_string": (ctypes.c_char_p, [c_int]),
     "sparse_mla_get_device_error": (c_int, [ctypes.POINTER(c_int)]),
     "sparse_mla_clear_device_error": (c_int, []),

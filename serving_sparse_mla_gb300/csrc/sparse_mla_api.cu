@@ -272,6 +272,55 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
   return SPARSE_MLA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Scratch of sparse_mla_decode_noalloc: a file-scope device array, so the
+// entry point needs no allocation.  Every GPU that loads this library holds
+// it until the process exits.  In host code the symbol is only a host-side
+// stand-in; its device address comes from cudaGetSymbolAddress, taken once
+// per device with that device current.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+sparse_mla_status_t noalloc_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPARSE_MLA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SPARSE_MLA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return SPARSE_MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sparse_mla_decode_noalloc_max_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+sparse_mla_status_t sparse_mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t* block_table,
+                                              const int32_t* cache_seqlens, const int32_t* indices, float sm_scale,
+                                              void* out, float* lse, int batch, int s_next, int h_q, int d_qk,
+                                              int d_v, int topk, int page_size, int max_blocks, int num_blocks,
+                                              void* stream) {
+  const size_t need = sparse_mla_decode_workspace_size(batch, s_next, h_q, d_v, topk);
+  if (need > kNoAllocScratchBytes) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  if (need > 0) {
+    sparse_mla_status_t st = noalloc_scratch(&ws);
+    if (st != SPARSE_MLA_OK) return st;
+  }
+  return sparse_mla_decode(q, kv_cache, block_table, cache_seqlens, indices, sm_scale, out, lse, batch, s_next,
+                           h_q, d_qk, d_v, topk, page_size, max_blocks, num_blocks, ws,
+                           need > 0 ? kNoAllocScratchBytes : 0, stream);
+}
+
 const char* sparse_mla_status_string(sparse_mla_status_t s) {
   switch (s) {
     case SPARSE_MLA_OK: return "SPARSE_MLA_OK";

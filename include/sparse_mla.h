@@ -32,9 +32,8 @@
  *     and lse = -inf.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream): no host synchronisation, no allocation.  The first
- *     call on a device performs one-time set-up (kernel attributes, the
- *     driver entry point for tensor maps) and should not be made during
- *     stream capture.
+ *     call on a device performs one-time set-up (device query, kernel
+ *     attributes) and should not be made during stream capture.
  *   - Errors: arguments are checked on the host before any launch and a
  *     non-OK status means nothing was launched, except SPARSE_MLA_ERR_CUDA
  *     after a failed launch.  No exception or abort crosses the ABI.

@@ -21,21 +21,29 @@
 // index list is walked in blocks of 128 entries; a block with no valid
 // entry is skipped.  Per block:
 //
-//   warp 0 (producer)  maps the 128 indices to KV rows and gathers the rows
-//                      with TMA tile::gather4 (4 rows x 64 columns per
-//                      instruction, 128B swizzle) into shared memory:
-//                      four 128x128 "pair" tiles for columns 0..511 (the
-//                      value part) and one 128x64 tile for the rope columns.
-//                      Masked rows use an out-of-range row coordinate, which
-//                      TMA fills with zeros; they are never read from HBM.
-//   warp 1 (MMA)       one thread issues tcgen05.mma:
+//   warps 0..3         map the block's indices to KV rows (every warp maps
+//   (producers)        all 128 entries, so all agree on the block-skip and
+//                      the validity mask without a barrier) and copy the rows
+//                      into shared memory with 16-byte cp.async, 128B-swizzled:
+//                      four 128x128 "pair" tiles for columns 0..511 (the value
+//                      part) and one 128x64 tile for the rope columns; each
+//                      warp copies its 32 rows of every tile.  Masked rows are
+//                      zero-filled (source size 0) and never read.  Issue never
+//                      waits on the thread's own copies: the hardware arrives
+//                      on a per-tile "landed" barrier, and each thread forwards
+//                      landed tiles to the MMA (fence.proxy.async, then arrive
+//                      on "full") as it goes, and all of them before it blocks.
+//                      On GB300 this gathers random 1152-B rows ~6x faster than
+//                      TMA tile::gather4 (13.9 vs 2.2 TB/s from L2, 5.3 vs 2.2
+//                      TB/s from HBM).
+//   warp 4 (MMA)       one thread issues tcgen05.mma:
 //                        S^T[128 x N]  = K_blk[128 x 576] . Q^T[576 x N]
 //                        O^T[512 x N] += V^T[512 x 128]  . P^T[128 x N]
 //                      (swap-AB: the kv rows fill M=128, the heads are N, so
 //                      8 heads cost N=16 instead of a 64-row pad).  V^T is
 //                      the same gathered tile read through an MN-major
 //                      descriptor; no second copy.  Accumulators live in TMEM.
-//   warps 2..5         thread r owns TMEM lane r = kv row r of the block:
+//   warps 5..8         thread r owns TMEM lane r = kv row r of the block:
 //   (softmax)          loads its S^T row, masks, reduces the per-head block
 //                      max across the 128 rows (warp transpose-reduce plus a
 //                      shared-memory step), keeps a lazily updated running
@@ -48,7 +56,6 @@
 // the device error word, drains its in-flight copies and MMAs, frees TMEM
 // and returns.
 #pragma once
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -62,7 +69,10 @@ constexpr int kBlk = 128;                    // index entries (kv rows) per bloc
 constexpr int kChunkBytes = kBlk * 128;      // 128 rows x 64 bf16 columns
 constexpr int kPairBytes = 2 * kChunkBytes;  // 128 rows x 128 columns
 constexpr int kInfoDepth = 4;
-constexpr int kThreads = 192;
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kSoftmaxWarp0 = 5;
+constexpr int kThreads = 288;
 constexpr float kLazyRescale = 8.0f;         // log2 units
 constexpr int kMaxSmem = 232448;
 
@@ -72,6 +82,7 @@ enum ErrCode : int { kErrProducerWait = 0x101, kErrMmaWait = 0x201, kErrSoftmaxW
 
 struct FwdParams {
   const __nv_bfloat16* q;   // [n_tok, h_q, 576]
+  const __nv_bfloat16* kv;  // [n_rows, 576] (paged: [num_blocks * page_size, 576])
   const int32_t* indices;   // [n_tok, topk]
   __nv_bfloat16* out;       // [n_tok, h_q, 512]
   float* lse;               // [n_tok, h_q]
@@ -82,7 +93,7 @@ struct FwdParams {
   const int32_t* block_table;  // paged: [batch, max_blocks]
   const int32_t* seqlens;      // paged: [batch]
   int n_tok, h_q, topk, mode;
-  int n_rows;               // rows of the KV tensor map
+  int n_rows;               // rows of kv
   int s_kv, batch, s_next, page_size, max_blocks, num_blocks;
   int splits;
   float scale_log2;         // sm_scale * log2(e)
@@ -106,12 +117,13 @@ struct Layout {
 };
 
 struct __align__(16) Misc {
-  uint64_t v_full[5], v_empty[5], rp_full[2], rp_empty[2];
+  uint64_t v_full[5], v_empty[5], rp_full[2], rp_empty[2], v_land[5], rp_land[2];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   uint64_t q_full, s_full, p_full, o_full, drain;
   int32_t info_blk[kInfoDepth];
   uint32_t info_mask[kInfoDepth][4];
   float red[4][64];
+  float rsum[4][64];
   float mrun[64];
   float alpha[64];
   float fin[64];
@@ -159,7 +171,7 @@ __device__ __forceinline__ TokCtx token_context(const FwdParams& p, int tok) {
   return c;
 }
 
-// KV tensor-map row read by one index entry, or -1 when the entry is masked.
+// KV row read by one index entry, or -1 when the entry is masked.
 __device__ __forceinline__ int map_entry(const FwdParams& p, const TokCtx& c, int idx) {
   if (idx < 0 || idx >= c.kv_len) return -1;
   int row;
@@ -228,70 +240,188 @@ __device__ __forceinline__ bool bar_red_or_128(bool pred) {
 
 // ------------------------------------------------------------------ roles
 
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async_arrive_on(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Tiles are numbered in issue order: tile t is part u = t % 5 of the
+// (t / 5)-th processed block (parts 0..3: value pairs, 4: rope).  Each tile
+// has a "landed" barrier (the hardware arrives for each producer thread
+// once that thread's copies of it have completed) and a "full" barrier (each
+// producer thread arrives after it has seen the tile land and fenced its
+// copies for the async proxy, the tensor core's view of shared memory).
 template <int N>
-__device__ bool run_producer(const CUtensorMap* tmap, const FwdParams& p, Misc& m, uint8_t* sbase,
-                             int tok, int jb, int je, uint64_t deadline, uint32_t (&vfills)[5],
-                             uint32_t (&rfills)[2]) {
+struct TileRing {
   using L = Layout<N>;
+  Misc& m;
+  uint32_t iss = 0;   // tiles this thread has issued
+  uint32_t fwd = 0;   // tiles this thread has forwarded to the MMA
+  __device__ TileRing(Misc& mm) : m(mm) {}
+
+  __device__ __forceinline__ void where(uint32_t t, uint32_t& landed, uint32_t& full, uint32_t& par) const {
+    const uint32_t b = t / 5u, u = t % 5u;
+    if (u < 4u) {
+      const uint32_t vi = 4u * b + u;
+      landed = smem_u32(&m.v_land[vi % L::kNV]);
+      full = smem_u32(&m.v_full[vi % L::kNV]);
+      par = (vi / L::kNV) & 1u;
+    } else {
+      landed = smem_u32(&m.rp_land[b % L::kNR]);
+      full = smem_u32(&m.rp_full[b % L::kNR]);
+      par = (b / L::kNR) & 1u;
+    }
+  }
+  __device__ __forceinline__ void forward_ready() {
+    while (fwd < iss) {
+      uint32_t landed, full, par;
+      where(fwd, landed, full, par);
+      if (!mbar_test_wait(landed, par)) return;
+      fence_proxy_async_smem();
+      mbar_arrive(full);
+      ++fwd;
+    }
+  }
+  __device__ __forceinline__ bool forward_oldest(uint64_t deadline, const volatile int* ab) {
+    uint32_t landed, full, par;
+    where(fwd, landed, full, par);
+    if (!mbar_wait(landed, par, deadline, ab)) return false;
+    fence_proxy_async_smem();
+    mbar_arrive(full);
+    ++fwd;
+    return true;
+  }
+  // Wait for a barrier phase the consumers complete.  Before blocking, every
+  // tile this thread issued is forwarded, so the consumers never wait on this
+  // thread while it waits on them.
+  __device__ __forceinline__ bool wait_consumer(uint32_t bar, uint32_t par, uint64_t deadline, const volatile int* ab) {
+    while (!mbar_test_wait(bar, par)) {
+      if (fwd < iss) {
+        if (!forward_oldest(deadline, ab)) return false;
+      } else {
+        return mbar_wait(bar, par, deadline, ab);
+      }
+    }
+    return true;
+  }
+  __device__ __forceinline__ bool drain(uint64_t deadline, const volatile int* ab) {
+    while (fwd < iss)
+      if (!forward_oldest(deadline, ab)) return false;
+    return true;
+  }
+};
+
+template <int N>
+__device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int tok, int jb, int je,
+                             uint64_t deadline, TileRing<N>& ring) {
+  using L = Layout<N>;
+  const int warp = static_cast<int>(threadIdx.x >> 5);   // 0..3
   const int lane = static_cast<int>(lane_id());
   const volatile int* ab = &m.abort_flag;
   const TokCtx ctx = token_context(p, tok);
   const int32_t* irow = p.indices + static_cast<size_t>(tok) * p.topk;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
-  uint32_t vuse = 0;
+  const int piece = lane & 7;
+  // Every warp maps the whole block (entries 4*lane .. 4*lane+3) so all
+  // agree on the skip decision and on ring positions without a barrier; each
+  // warp then copies its own 32 rows of every tile.
+  int idx_next[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = jb * kBlk + lane * 4 + i;
+    idx_next[i] = (jb < je && e < p.topk) ? __ldg(irow + e) : -1;
+  }
   int n = 0;
   for (int j = jb; j < je; ++j) {
     int rows[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = j * kBlk + lane * 4 + i;
-      const int idx = e < p.topk ? __ldg(irow + e) : -1;
-      rows[i] = map_entry(p, ctx, idx);
+    for (int i = 0; i < 4; ++i) rows[i] = map_entry(p, ctx, idx_next[i]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {   // prefetch the next block's indices
+      const int e = (j + 1) * kBlk + lane * 4 + i;
+      idx_next[i] = (j + 1 < je && e < p.topk) ? __ldg(irow + e) : -1;
     }
     uint32_t bal[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) bal[i] = __ballot_sync(0xffffffffu, rows[i] >= 0);
     if ((bal[0] | bal[1] | bal[2] | bal[3]) == 0u) continue;
 
-    const int k = n % kInfoDepth;
-    if (!mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab)) return false;
-    if (lane == 0) {
-      m.info_blk[k] = j;
+    if (warp == 0) {
+      const int k = n % kInfoDepth;
+      const bool ok = ring.wait_consumer(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      if (lane == 0) {
+        m.info_blk[k] = j;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) m.info_mask[k][i] = bal[i];
-      mbar_arrive(smem_u32(&m.info_full[k]));
+        for (int i = 0; i < 4; ++i) m.info_mask[k][i] = bal[i];
+        mbar_arrive(smem_u32(&m.info_full[k]));
+      }
     }
+    // This warp copies block rows 32*warp + 4*it + (lane >> 3); entry r of
+    // the block sits in lane r / 4 as rows[r % 4].
+    int myrow[8];
 #pragma unroll
-    for (int pr = 0; pr < 4; ++pr) {
-      const uint32_t s = (vuse + pr) % L::kNV;
-      const uint32_t ph = ((vuse + pr) / L::kNV) & 1u;
-      if (!mbar_wait(smem_u32(&m.v_empty[s]), ph ^ 1u, deadline, ab)) return false;
-      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&m.v_full[s]), kPairBytes);
-      __syncwarp();
-      const uint32_t dst = vbase + s * kPairBytes + lane * 512;
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-        tma_gather4(dst + c * kChunkBytes, tmap, (2 * pr + c) * 64, rows[0], rows[1], rows[2], rows[3],
-                    smem_u32(&m.v_full[s]));
-      vfills[s] += 1;
+    for (int it = 0; it < 8; ++it) {
+      const int src = warp * 8 + it;
+      const int r0 = __shfl_sync(0xffffffffu, rows[0], src);
+      const int r1 = __shfl_sync(0xffffffffu, rows[1], src);
+      const int r2 = __shfl_sync(0xffffffffu, rows[2], src);
+      const int r3 = __shfl_sync(0xffffffffu, rows[3], src);
+      const int sel = lane >> 3;
+      myrow[it] = sel == 0 ? r0 : (sel == 1 ? r1 : (sel == 2 ? r2 : r3));
     }
-    vuse += 4;
-    const uint32_t rs = n % L::kNR;
-    const uint32_t rph = (n / L::kNR) & 1u;
-    if (!mbar_wait(smem_u32(&m.rp_empty[rs]), rph ^ 1u, deadline, ab)) return false;
-    if (lane == 0) mbar_arrive_expect_tx(smem_u32(&m.rp_full[rs]), kChunkBytes);
-    __syncwarp();
-    tma_gather4(rbase + rs * kChunkBytes + lane * 512, tmap, 512, rows[0], rows[1], rows[2], rows[3],
-                smem_u32(&m.rp_full[rs]));
-    rfills[rs] += 1;
+#pragma unroll 1
+    for (int u = 0; u < 5; ++u) {
+      uint32_t landed, full, par;
+      ring.where(ring.iss, landed, full, par);
+      uint32_t empty, dst;
+      int first_chunk, n_chunks;
+      if (u < 4) {
+        const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u)) % L::kNV;
+        empty = smem_u32(&m.v_empty[s]);
+        dst = vbase + s * kPairBytes;
+        first_chunk = 2 * u;
+        n_chunks = 2;
+      } else {
+        const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
+        empty = smem_u32(&m.rp_empty[rs]);
+        dst = rbase + rs * kChunkBytes;
+        first_chunk = 8;
+        n_chunks = 1;
+      }
+      const bool ok = ring.wait_consumer(empty, par ^ 1u, deadline, ab);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      for (int c = 0; c < n_chunks; ++c) {
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = warp * 32 + it * 4 + (lane >> 3);
+          const int src_row = myrow[it];
+          const __nv_bfloat16* src =
+              p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
+          cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
+        }
+      }
+      cp_async_arrive_on(landed);
+      ring.iss += 1;
+      ring.forward_ready();
+    }
     ++n;
   }
-  const int k = n % kInfoDepth;
-  if (!mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab)) return false;
-  if (lane == 0) {
-    m.info_blk[k] = -1;
-    mbar_arrive(smem_u32(&m.info_full[k]));
+  const bool dok = ring.drain(deadline, ab);
+  if (!__all_sync(0xffffffffu, dok)) return false;
+  if (warp == 0) {
+    const int k = n % kInfoDepth;
+    const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    if (lane == 0) {
+      m.info_blk[k] = -1;
+      mbar_arrive(smem_u32(&m.info_full[k]));
+    }
   }
   return true;
 }
@@ -368,13 +498,14 @@ __device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadlin
 }
 
 template <int N>
-__device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int tok,
-                            int split, int h0, int hv, uint64_t deadline) {
+__device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int tok, int split, int h0,
+                            int hv, uint64_t deadline) {
   using L = Layout<N>;
+  constexpr int H = N > 32 ? 32 : N;   // heads per register pass
   const volatile int* ab = &m.abort_flag;
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
-  const int tid = static_cast<int>(threadIdx.x) - 64;  // 0..127
+  const int tid = static_cast<int>(threadIdx.x) - kSoftmaxWarp0 * 32;  // 0..127
   const int q4 = warp & 3;                             // TMEM lane quarter of this warp
   const int row = q4 * 32 + lane;                      // kv row of the block == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
@@ -399,14 +530,16 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     if (tid == 0) mbar_arrive(smem_u32(&m.q_full));
   }
 
-  float lpart[N];
-#pragma unroll
-  for (int i = 0; i < N; ++i) lpart[i] = 0.f;
-
+  // Head tid's running sum of exp2(s - m) (owner threads tid < N); the
+  // per-block sums arrive through m.rsum, reduced over the 128 rows.
+  float lrun = 0.f;
   int n = 0;
   for (;;) {
     const int k = n % kInfoDepth;
-    if (!mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab)) return false;
+    // Every wait is followed by a barrier that ORs the failures of the 128
+    // softmax threads, so they all continue or all return together.
+    const bool iok = mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab);
+    if (bar_red_or_128(!iok)) return false;
     const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
     const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&m.info_mask[k][row & 3]);
     __syncwarp();
@@ -414,67 +547,73 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     if (blk < 0) break;
     const bool valid = ((bits >> (row >> 2)) & 1u) != 0u;
 
-    if (!mbar_wait(smem_u32(&m.s_full), n & 1, deadline, ab)) return false;
+    const bool sok = mbar_wait(smem_u32(&m.s_full), n & 1, deadline, ab);
     tc_fence_after();
-    float s[N];
+    // Block max per head: butterfly over the warp, then over the 4 warps.
 #pragma unroll
-    for (int g = 0; g < N / 16; ++g) tmem_ld16(tS + g * 16, s + g * 16);
-    tmem_wait_ld();
+    for (int ps = 0; ps < N / H; ++ps) {
+      float s[H];
 #pragma unroll
-    for (int i = 0; i < N; ++i) s[i] = valid ? s[i] * p.scale_log2 : -INFINITY;
-
-    {
-      float t[N];
+      for (int g = 0; g < H / 16; ++g) tmem_ld16(tS + ps * H + g * 16, s + g * 16);
+      tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < N; ++i) t[i] = s[i];
-      warp_xreduce<N, true>(t, lane, m.red[q4]);
+      for (int i = 0; i < H; ++i) s[i] = valid ? s[i] * p.scale_log2 : -INFINITY;
+      warp_xreduce<H, true>(s, lane, m.red[q4] + ps * H);
     }
-    named_bar_sync(1, 128);
+    if (bar_red_or_128(!sok)) return false;
     bool grew = false;
     if (tid < N) {
+      if (n > 0) lrun += (m.rsum[0][tid] + m.rsum[1][tid]) + (m.rsum[2][tid] + m.rsum[3][tid]);
       const float bm = fmaxf(fmaxf(m.red[0][tid], m.red[1][tid]), fmaxf(m.red[2][tid], m.red[3][tid]));
       const float mo = m.mrun[tid];
       const float mn = (bm > mo + kLazyRescale) ? bm : mo;
       const float al = fast_exp2(mo - mn);
+      lrun *= al;
       m.alpha[tid] = al;
       m.mrun[tid] = mn;
       grew = (mn != mo);
     }
     const bool rescale = bar_red_or_128(grew);
-    if (rescale) {
-#pragma unroll
-      for (int i = 0; i < N; ++i) lpart[i] *= m.alpha[i];
-      if (n > 0) {
-        // O^T holds the sum through the previous block (its PV completed
-        // before S of this block was committed): rescale each head column.
+    if (rescale && n > 0) {
+      // O^T holds the sum through the previous block (its PV completed
+      // before S of this block was committed): rescale each head column.
 #pragma unroll 1
-        for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-          for (int g = 0; g < N / 16; ++g) {
-            float o[16];
-            tmem_ld16(tO + mt * N + g * 16, o);
-            tmem_wait_ld();
+        for (int g = 0; g < N / 16; ++g) {
+          float o[16];
+          tmem_ld16(tO + mt * N + g * 16, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= m.alpha[g * 16 + i];
-            tmem_st16(tO + mt * N + g * 16, o);
-          }
+          for (int i = 0; i < 16; ++i) o[i] *= m.alpha[g * 16 + i];
+          tmem_st16(tO + mt * N + g * 16, o);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
     }
-    // P^T row (bf16) into the rope slot of this block, MN-major swizzled.
+    // P^T row (bf16) into the rope slot of this block, MN-major swizzled,
+    // and the block's per-head sums of P.
     const uint32_t prow = rbase + (n % L::kNR) * kChunkBytes + row * L::kPRow;
     const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
 #pragma unroll
-    for (int c = 0; c < N / 8; ++c) {
-      float pv[8];
+    for (int ps = 0; ps < N / H; ++ps) {
+      float s[H];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        pv[i] = fast_exp2(s[c * 8 + i] - m.mrun[c * 8 + i]);
-        lpart[c * 8 + i] += pv[i];
+      for (int g = 0; g < H / 16; ++g) tmem_ld16(tS + ps * H + g * 16, s + g * 16);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < H / 8; ++c) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int h = ps * H + c * 8 + i;
+          s[c * 8 + i] = valid ? fast_exp2(s[c * 8 + i] * p.scale_log2 - m.mrun[h]) : 0.f;
+        }
+        const uint32_t chunk = static_cast<uint32_t>(ps * H / 8 + c);
+        st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
+                     pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
+                     pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
       }
-      st_shared_v4(prow + ((static_cast<uint32_t>(c) ^ sw) << 4), pack_bf16x2(pv[0], pv[1]),
-                   pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
+      warp_xreduce<H, false>(s, lane, m.rsum[q4] + ps * H);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -483,17 +622,16 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   }
 
   // ---------------------------------------------------------- epilogue
-  if (!mbar_wait(smem_u32(&m.o_full), 0, deadline, ab)) return false;
+  const bool ook = mbar_wait(smem_u32(&m.o_full), 0, deadline, ab);
   tc_fence_after();
-  warp_xreduce<N, false>(lpart, lane, m.red[q4]);
-  named_bar_sync(1, 128);
+  if (bar_red_or_128(!ook)) return false;
   const size_t tok_h = static_cast<size_t>(tok) * p.h_q + h0;
   if (tid < N) {
-    const float l = m.red[0][tid] + m.red[1][tid] + m.red[2][tid] + m.red[3][tid];
+    if (n > 0) lrun += (m.rsum[0][tid] + m.rsum[1][tid]) + (m.rsum[2][tid] + m.rsum[3][tid]);
     float lse;
     if (n > 0) {
-      lse = (m.mrun[tid] + log2f(l)) * 0.69314718055994530942f;
-      m.fin[tid] = 1.0f / l;
+      lse = (m.mrun[tid] + log2f(lrun)) * 0.69314718055994530942f;
+      m.fin[tid] = 1.0f / lrun;
     } else {
       lse = -INFINITY;
       m.fin[tid] = 0.f;
@@ -536,8 +674,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 // ------------------------------------------------------------------ kernel
 
 template <int N>
-__global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_fwd_kernel(const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Layout<N>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -550,8 +687,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hv = min(N, p.h_q - h0);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 5; ++i) { mbar_init(smem_u32(&m.v_full[i]), 1); mbar_init(smem_u32(&m.v_empty[i]), 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(smem_u32(&m.rp_full[i]), 1); mbar_init(smem_u32(&m.rp_empty[i]), 1); }
+    for (int i = 0; i < 5; ++i) {
+      mbar_init(smem_u32(&m.v_full[i]), kProducerWarps * 32);
+      mbar_init(smem_u32(&m.v_land[i]), kProducerWarps * 32);
+      mbar_init(smem_u32(&m.v_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&m.rp_full[i]), kProducerWarps * 32);
+      mbar_init(smem_u32(&m.rp_land[i]), kProducerWarps * 32);
+      mbar_init(smem_u32(&m.rp_empty[i]), 1);
+    }
     for (int i = 0; i < kInfoDepth; ++i) {
       mbar_init(smem_u32(&m.info_full[i]), 1);
       mbar_init(smem_u32(&m.info_empty[i]), 5);
@@ -565,8 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     m.prior_error = *reinterpret_cast<volatile int*>(&g_device_error);
     fence_mbar_init();
   }
-  if (warp == 0) prefetch_tmap(&tmap_kv);
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&m.tmem_base), L::kTmemCols);
     tmem_relinquish();
   }
@@ -580,20 +724,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nb = (p.topk + kBlk - 1) / kBlk;
     const int jb = static_cast<int>((static_cast<long long>(split) * nb) / p.splits);
     const int je = static_cast<int>((static_cast<long long>(split + 1) * nb) / p.splits);
-    if (warp == 0) {
-      uint32_t vfills[5] = {0, 0, 0, 0, 0};
-      uint32_t rfills[2] = {0, 0};
-      if (!run_producer<N>(&tmap_kv, p, m, sbase, tok, jb, je, deadline, vfills, rfills) && lane == 0)
-        raise_error(m, kErrProducerWait);
-      // Drain: wait (bounded) until every gather this warp issued has landed,
-      // whether or not the consumers got to it.
-      const uint64_t dl2 = global_timer_ns() + 100000000ull;
-      const int never = 0;
-      for (int s = 0; s < L::kNV; ++s)
-        if (vfills[s]) mbar_wait(smem_u32(&m.v_full[s]), (vfills[s] - 1) & 1u, dl2, &never);
-      for (int s = 0; s < L::kNR; ++s)
-        if (rfills[s]) mbar_wait(smem_u32(&m.rp_full[s]), (rfills[s] - 1) & 1u, dl2, &never);
-    } else if (warp == 1) {
+    if (warp < kProducerWarps) {
+      TileRing<N> ring(m);
+      if (!run_producer<N>(p, m, sbase, tok, jb, je, deadline, ring)) raise_error(m, kErrProducerWait);
+      // Drain: every copy this thread issued has landed before the CTA can
+      // exit, whether or not the consumers got to it.
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp == kMmaWarp) {
       if (lane == 0) {
         if (!run_mma<N>(m, sbase, tmem, deadline)) raise_error(m, kErrMmaWait);
         // Drain: every MMA this thread issued completes before TMEM is freed.
@@ -609,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, L::kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
 }
 
 // ------------------------------------------------------------------ helpers kernels

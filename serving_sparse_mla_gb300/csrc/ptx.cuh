@@ -1,4 +1,4 @@
-// Inline-PTX building blocks for sm_103a: mbarriers, TMA tile::gather4,
+// Inline-PTX building blocks for sm_103a: mbarriers, proxy fences,
 // tcgen05 (TMEM allocation, MMA, commit, TMEM loads/stores) and the shared
 // memory / instruction descriptors the MMAs take.
 //
@@ -59,39 +59,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or `hint_ns` passes, so waiting warps issue nothing meanwhile
+// (a tight poll loop competes with the copies for the memory pipe).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait on the phase with the given parity.  Returns false when the
-// deadline passes or another thread of the CTA raised the abort flag.
+// deadline passes or another thread of the CTA raised the abort flag (both
+// checked before each suspension period).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline_ns,
                                           const volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   for (;;) {
     if (*abort_flag) return false;
     if (global_timer_ns() > deadline_ns) return false;
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
   }
 }
 
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- TMA
-// Four rows of a 2-D tensor map (box = {cols, 1}) into shared memory; the
-// rows land one after another with the map's swizzle.  Row coordinates out
-// of the tensor's range read the fill value (zero).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t col, int32_t r0,
-                                            int32_t r1, int32_t r2, int32_t r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-        "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -1,7 +1,6 @@
-// C-ABI entry points: host-side validation, tensor-map encoding, launch
+// C-ABI entry points: host-side validation, launch
 // planning (head-group width, top-k splits) and launches on the caller's
 // stream.  See include/sparse_mla.h for the contract of each call.
-#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -21,10 +20,6 @@ constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 struct DeviceState {
   bool probed = false;
   bool supported = false;
@@ -34,7 +29,6 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
-EncodeTiledFn g_encode = nullptr;
 
 sparse_mla_status_t device_setup(int* sm_count) {
   int dev = 0;
@@ -52,15 +46,6 @@ sparse_mla_status_t device_setup(int* sm_count) {
     st.probed = true;
   }
   if (!st.supported) return SPARSE_MLA_ERR_UNSUPPORTED_ARCH;
-  if (!g_encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || fn == nullptr)
-      return SPARSE_MLA_ERR_CUDA;
-    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
-  }
   if (!st.attrs_set) {
     if (cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::smem_bytes<16>()) != cudaSuccess ||
@@ -95,27 +80,16 @@ int plan_splits(long long n_tok, int h_q, int topk, int sm_count) {
   return static_cast<int>(s);
 }
 
-sparse_mla_status_t encode_kv_map(CUtensorMap* map, const void* kv, long long n_rows) {
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(smla::kDqk), static_cast<cuuint64_t>(n_rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(smla::kDqk) * 2};
-  cuuint32_t box[2] = {64, 1};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? SPARSE_MLA_OK : SPARSE_MLA_ERR_INVALID_ARG;
-}
-
-sparse_mla_status_t launch_fwd(const CUtensorMap& map, const FwdParams& p, cudaStream_t stream) {
+sparse_mla_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
   const int N = head_width(p.h_q);
   dim3 grid(static_cast<unsigned>(p.n_tok) * static_cast<unsigned>(p.splits), static_cast<unsigned>(head_groups(p.h_q)));
   dim3 block(smla::kThreads);
   if (N == 16)
-    smla::sparse_mla_fwd_kernel<16><<<grid, block, smla::smem_bytes<16>(), stream>>>(map, p);
+    smla::sparse_mla_fwd_kernel<16><<<grid, block, smla::smem_bytes<16>(), stream>>>(p);
   else if (N == 32)
-    smla::sparse_mla_fwd_kernel<32><<<grid, block, smla::smem_bytes<32>(), stream>>>(map, p);
+    smla::sparse_mla_fwd_kernel<32><<<grid, block, smla::smem_bytes<32>(), stream>>>(p);
   else
-    smla::sparse_mla_fwd_kernel<64><<<grid, block, smla::smem_bytes<64>(), stream>>>(map, p);
+    smla::sparse_mla_fwd_kernel<64><<<grid, block, smla::smem_bytes<64>(), stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
 }
 
@@ -173,13 +147,12 @@ sparse_mla_status_t sparse_mla_fwd(const void* q, const void* kv, const int32_t*
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (s_kv == 0) return launch_fill(out, lse, static_cast<long long>(s_q) * h_q, cs);
   if (!kv || !aligned(kv, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
-  CUtensorMap map;
-  if ((st = encode_kv_map(&map, kv, s_kv)) != SPARSE_MLA_OK) return st;
   FwdParams p = base_params(q, indices, sm_scale, out, lse, s_q, h_q, topk);
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
   p.mode = smla::kDense;
   p.n_rows = s_kv;
   p.s_kv = s_kv;
-  return launch_fwd(map, p, cs);
+  return launch_fwd(p, cs);
 }
 
 sparse_mla_status_t sparse_mla_fwd_varlen(const void* q, const void* kv, const int32_t* indices,
@@ -198,15 +171,14 @@ sparse_mla_status_t sparse_mla_fwd_varlen(const void* q, const void* kv, const i
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (total_kv == 0) return launch_fill(out, lse, static_cast<long long>(total_q) * h_q, cs);
   if (!kv || !aligned(kv, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
-  CUtensorMap map;
-  if ((st = encode_kv_map(&map, kv, total_kv)) != SPARSE_MLA_OK) return st;
   FwdParams p = base_params(q, indices, sm_scale, out, lse, total_q, h_q, topk);
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
   p.mode = smla::kVarlen;
   p.n_rows = total_kv;
   p.batch = batch;
   p.cu_q = cu_seqlens_q;
   p.cu_kv = cu_seqlens_kv;
-  return launch_fwd(map, p, cs);
+  return launch_fwd(p, cs);
 }
 
 size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v, int topk) {
@@ -243,10 +215,8 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
   const size_t need = sparse_mla_decode_workspace_size(batch, s_next, h_q, d_v, topk);
   if (splits > 1 && (workspace_bytes < need || !workspace)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
   if (splits > 1 && !aligned(workspace, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
-  CUtensorMap map;
-  if ((st = encode_kv_map(&map, kv_cache, static_cast<long long>(num_blocks) * page_size)) != SPARSE_MLA_OK)
-    return st;
   FwdParams p = base_params(q, indices, sm_scale, out, lse, static_cast<int>(n_tok), h_q, topk);
+  p.kv = static_cast<const __nv_bfloat16*>(kv_cache);
   p.mode = smla::kPaged;
   p.n_rows = num_blocks * page_size;
   p.batch = batch;
@@ -262,7 +232,7 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
     p.part_o = ws;
     p.part_lse = ws + static_cast<size_t>(splits) * n_tok * h_q * smla::kDv;
   }
-  if ((st = launch_fwd(map, p, cs)) != SPARSE_MLA_OK) return st;
+  if ((st = launch_fwd(p, cs)) != SPARSE_MLA_OK) return st;
   if (splits > 1) {
     const int n_th = static_cast<int>(n_tok * h_q);
     smla::combine_splits_kernel<<<n_th, 128, 0, cs>>>(p.part_o, p.part_lse, static_cast<__nv_bfloat16*>(out), lse,

@@ -1,4 +1,4 @@
-// DSA sparse-MLA attention forward for sm_103a (tcgen05 + TMA gather4).
+// DSA sparse-MLA attention forward for sm_103a (cp.async gather + tcgen05).
 //
 // Computes, per query token t and head h over the token's top-k index list
 // ("feat: add XTuner TileLang sparse MLA backend", Performance, Isolated
@@ -18,39 +18,44 @@
 // only the index -> row mapping differs.
 //
 // Work decomposition: one CTA per (token, top-k split, head group).  The
-// index list is walked in blocks of 128 entries; a block with no valid
-// entry is skipped.  Per block:
+// index list is walked in blocks of 64 entries (64 gathered rows = 72 KB, so
+// two to three blocks fit in shared memory and the gather of the next blocks
+// overlaps the math of the current one); a block with no valid entry is
+// skipped.  Per block:
 //
 //   warps 0..3         map the block's indices to KV rows (every warp maps
-//   (producers)        all 128 entries, so all agree on the block-skip and
-//                      the validity mask without a barrier) and copy the rows
+//   (producers)        all 64 entries, so all agree on the block-skip and the
+//                      validity mask without a barrier) and copy the rows
 //                      into shared memory with 16-byte cp.async, 128B-swizzled:
-//                      four 128x128 "pair" tiles for columns 0..511 (the value
-//                      part) and one 128x64 tile for the rope columns; each
-//                      warp copies its 32 rows of every tile.  Masked rows are
-//                      zero-filled (source size 0) and never read.  Issue never
-//                      waits on the thread's own copies: the hardware arrives
-//                      on a per-tile "landed" barrier, and each thread forwards
-//                      landed tiles to the MMA (fence.proxy.async, then arrive
-//                      on "full") as it goes, and all of them before it blocks.
-//                      On GB300 this gathers random 1152-B rows ~6x faster than
-//                      TMA tile::gather4 (13.9 vs 2.2 TB/s from L2, 5.3 vs 2.2
-//                      TB/s from HBM).
-//   warp 4 (MMA)       one thread issues tcgen05.mma:
-//                        S^T[128 x N]  = K_blk[128 x 576] . Q^T[576 x N]
-//                        O^T[512 x N] += V^T[512 x 128]  . P^T[128 x N]
-//                      (swap-AB: the kv rows fill M=128, the heads are N, so
-//                      8 heads cost N=16 instead of a 64-row pad).  V^T is
-//                      the same gathered tile read through an MN-major
-//                      descriptor; no second copy.  Accumulators live in TMEM.
-//   warps 5..8         thread r owns TMEM lane r = kv row r of the block:
-//   (softmax)          loads its S^T row, masks, reduces the per-head block
-//                      max across the 128 rows (warp transpose-reduce plus a
-//                      shared-memory step), keeps a lazily updated running
-//                      max (the O accumulator is rescaled only when a head's
-//                      max grows by more than 2^8), writes P^T = exp2(s - m)
-//                      as bf16 into shared memory, and at the end normalises
-//                      O^T and writes out / LSE.
+//                      four 64x128 "pair" tiles for columns 0..511 (the value
+//                      part) and one 64x64 tile for the rope columns; each
+//                      warp copies its 16 rows of every tile.  Masked rows are
+//                      zero-filled (source size 0) and never read.  Producers
+//                      never wait on their own copies: the hardware arrives on
+//                      the tile's full barrier when a thread's copies have
+//                      landed, and the MMA thread, after acquiring the tile,
+//                      issues fence.proxy.async before the tensor core reads
+//                      it.  On GB300 this gathers random 1152-B rows ~6x
+//                      faster than TMA tile::gather4 (13.9 vs 2.2 TB/s from
+//                      L2, 5.3 vs 2.2 TB/s from HBM).
+//   warp 4 (MMA)       one thread issues tcgen05.mma (kind::f16, fp32 in TMEM):
+//                        S^T[64 x N]   = K_blk[64 x 576] . Q^T[576 x N]   (M=64)
+//                        O^T[512 x N] += V^T[512 x 64]  . P^T[64 x N]    (M=128)
+//                      (swap-AB: kv rows are M and heads are N, so 8 heads
+//                      cost N=16 instead of a 64-row pad).  V^T is the same
+//                      gathered tile read through an MN-major descriptor.  The
+//                      order is QK(0), QK(1), PV(0), QK(2), PV(1), ... with S
+//                      double-buffered, so QK of the next block runs while the
+//                      softmax works on the current one.
+//   warps 5..8         the M=64 result sits in lanes 32*(i/16) + i%16, so
+//   (softmax)          lanes 0..15 of each warp own one kv row each: load the
+//                      S^T row, mask, reduce the per-head block max across the
+//                      64 rows (warp transpose-reduce plus a shared-memory
+//                      step), keep a lazily updated running max (O is rescaled
+//                      only when a head's max grows by more than 2^8, after the
+//                      previous P.V has completed), write P^T = exp2(s - m) as
+//                      bf16 into the block's rope slot, and at the end
+//                      normalise O^T and write out / LSE.
 //
 // All waits are bounded (see ptx.cuh); a timed-out CTA records an error in
 // the device error word, drains its in-flight copies and MMAs, frees TMEM
@@ -65,10 +70,10 @@ namespace smla {
 
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
-constexpr int kBlk = 128;                    // index entries (kv rows) per block
-constexpr int kChunkBytes = kBlk * 128;      // 128 rows x 64 bf16 columns
-constexpr int kPairBytes = 2 * kChunkBytes;  // 128 rows x 128 columns
-constexpr int kInfoDepth = 4;
+constexpr int kBlk = 64;                     // index entries (kv rows) per block
+constexpr int kChunkBytes = kBlk * 128;      // 64 rows x 64 bf16 columns
+constexpr int kPairBytes = 2 * kChunkBytes;  // 64 rows x 128 columns
+constexpr int kInfoDepth = 8;
 constexpr int kProducerWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kSoftmaxWarp0 = 5;
@@ -105,23 +110,25 @@ __device__ int g_device_error;
 template <int N>
 struct Layout {
   static_assert(N == 16 || N == 32 || N == 64, "head group width");
-  static constexpr int kNV = (N == 64) ? 4 : 5;       // value pair-tile ring
-  static constexpr int kNR = (N == 16) ? 2 : 1;       // rope / P^T ring
-  static constexpr int kPRow = N * 2;                 // bytes of one P^T row
+  static constexpr int kNV = N == 64 ? 8 : (N == 32 ? 10 : 11);   // value pair-tile ring
+  static constexpr int kNR = N == 64 ? 2 : 3;                     // rope / P^T ring
+  static constexpr int kPRow = N * 2;                             // bytes of one P^T row
   static constexpr uint32_t kPSwz = N == 64 ? SWZ_128B : (N == 32 ? SWZ_64B : SWZ_32B);
   static constexpr int kTmemCols = N == 64 ? 512 : (N == 32 ? 256 : 128);
   static constexpr int kQOff = 0;
   static constexpr int kVOff = 9 * N * 128;
   static constexpr int kROff = kVOff + kNV * kPairBytes;
   static constexpr int kMiscOff = kROff + kNR * kChunkBytes;
+  static_assert(kBlk * kPRow <= kChunkBytes, "P^T fits in a rope slot");
 };
 
 struct __align__(16) Misc {
-  uint64_t v_full[5], v_empty[5], rp_full[2], rp_empty[2], v_land[5], rp_land[2];
+  uint64_t v_full[12], v_empty[12];
+  uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
-  uint64_t q_full, s_full, p_full, o_full, drain;
+  uint64_t q_full, s_full[2], p_full[2], o_full, drain;
   int32_t info_blk[kInfoDepth];
-  uint32_t info_mask[kInfoDepth][4];
+  uint32_t info_mask[kInfoDepth][2];
   float red[4][64];
   float rsum[4][64];
   float mrun[64];
@@ -238,86 +245,19 @@ __device__ __forceinline__ bool bar_red_or_128(bool pred) {
   return r != 0;
 }
 
-// ------------------------------------------------------------------ roles
-
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void cp_async_arrive_on(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Tiles are numbered in issue order: tile t is part u = t % 5 of the
-// (t / 5)-th processed block (parts 0..3: value pairs, 4: rope).  Each tile
-// has a "landed" barrier (the hardware arrives for each producer thread
-// once that thread's copies of it have completed) and a "full" barrier (each
-// producer thread arrives after it has seen the tile land and fenced its
-// copies for the async proxy, the tensor core's view of shared memory).
-template <int N>
-struct TileRing {
-  using L = Layout<N>;
-  Misc& m;
-  uint32_t iss = 0;   // tiles this thread has issued
-  uint32_t fwd = 0;   // tiles this thread has forwarded to the MMA
-  __device__ TileRing(Misc& mm) : m(mm) {}
-
-  __device__ __forceinline__ void where(uint32_t t, uint32_t& landed, uint32_t& full, uint32_t& par) const {
-    const uint32_t b = t / 5u, u = t % 5u;
-    if (u < 4u) {
-      const uint32_t vi = 4u * b + u;
-      landed = smem_u32(&m.v_land[vi % L::kNV]);
-      full = smem_u32(&m.v_full[vi % L::kNV]);
-      par = (vi / L::kNV) & 1u;
-    } else {
-      landed = smem_u32(&m.rp_land[b % L::kNR]);
-      full = smem_u32(&m.rp_full[b % L::kNR]);
-      par = (b / L::kNR) & 1u;
-    }
-  }
-  __device__ __forceinline__ void forward_ready() {
-    while (fwd < iss) {
-      uint32_t landed, full, par;
-      where(fwd, landed, full, par);
-      if (!mbar_test_wait(landed, par)) return;
-      fence_proxy_async_smem();
-      mbar_arrive(full);
-      ++fwd;
-    }
-  }
-  __device__ __forceinline__ bool forward_oldest(uint64_t deadline, const volatile int* ab) {
-    uint32_t landed, full, par;
-    where(fwd, landed, full, par);
-    if (!mbar_wait(landed, par, deadline, ab)) return false;
-    fence_proxy_async_smem();
-    mbar_arrive(full);
-    ++fwd;
-    return true;
-  }
-  // Wait for a barrier phase the consumers complete.  Before blocking, every
-  // tile this thread issued is forwarded, so the consumers never wait on this
-  // thread while it waits on them.
-  __device__ __forceinline__ bool wait_consumer(uint32_t bar, uint32_t par, uint64_t deadline, const volatile int* ab) {
-    while (!mbar_test_wait(bar, par)) {
-      if (fwd < iss) {
-        if (!forward_oldest(deadline, ab)) return false;
-      } else {
-        return mbar_wait(bar, par, deadline, ab);
-      }
-    }
-    return true;
-  }
-  __device__ __forceinline__ bool drain(uint64_t deadline, const volatile int* ab) {
-    while (fwd < iss)
-      if (!forward_oldest(deadline, ab)) return false;
-    return true;
-  }
-};
+// ------------------------------------------------------------------ producer
 
 template <int N>
 __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int tok, int jb, int je,
-                             uint64_t deadline, TileRing<N>& ring) {
+                             uint64_t deadline) {
   using L = Layout<N>;
   const int warp = static_cast<int>(threadIdx.x >> 5);   // 0..3
   const int lane = static_cast<int>(lane_id());
@@ -327,93 +267,92 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int to
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
   const int piece = lane & 7;
-  // Every warp maps the whole block (entries 4*lane .. 4*lane+3) so all
-  // agree on the skip decision and on ring positions without a barrier; each
-  // warp then copies its own 32 rows of every tile.
-  int idx_next[4];
+  const int sel = lane >> 3;
+  // Every warp maps the whole block (entries 2*lane, 2*lane+1) so all agree
+  // on the skip decision and on ring positions without a barrier; each warp
+  // then copies its own 16 rows of every tile.
+  int idx_next[2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int e = jb * kBlk + lane * 4 + i;
+  for (int i = 0; i < 2; ++i) {
+    const int e = jb * kBlk + lane * 2 + i;
     idx_next[i] = (jb < je && e < p.topk) ? __ldg(irow + e) : -1;
   }
   int n = 0;
   for (int j = jb; j < je; ++j) {
-    int rows[4];
+    int rows[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) rows[i] = map_entry(p, ctx, idx_next[i]);
+    for (int i = 0; i < 2; ++i) rows[i] = map_entry(p, ctx, idx_next[i]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {   // prefetch the next block's indices
-      const int e = (j + 1) * kBlk + lane * 4 + i;
+    for (int i = 0; i < 2; ++i) {   // prefetch the next block's indices
+      const int e = (j + 1) * kBlk + lane * 2 + i;
       idx_next[i] = (j + 1 < je && e < p.topk) ? __ldg(irow + e) : -1;
     }
-    uint32_t bal[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) bal[i] = __ballot_sync(0xffffffffu, rows[i] >= 0);
-    if ((bal[0] | bal[1] | bal[2] | bal[3]) == 0u) continue;
+    const uint32_t bal0 = __ballot_sync(0xffffffffu, rows[0] >= 0);
+    const uint32_t bal1 = __ballot_sync(0xffffffffu, rows[1] >= 0);
+    if ((bal0 | bal1) == 0u) continue;
 
     if (warp == 0) {
       const int k = n % kInfoDepth;
-      const bool ok = ring.wait_consumer(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
+      const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
       if (!__all_sync(0xffffffffu, ok)) return false;
       if (lane == 0) {
         m.info_blk[k] = j;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) m.info_mask[k][i] = bal[i];
+        m.info_mask[k][0] = bal0;
+        m.info_mask[k][1] = bal1;
         mbar_arrive(smem_u32(&m.info_full[k]));
       }
     }
-    // This warp copies block rows 32*warp + 4*it + (lane >> 3); entry r of
-    // the block sits in lane r / 4 as rows[r % 4].
-    int myrow[8];
+    // This warp copies block rows 16*warp + 4*it + sel; entry r of the block
+    // sits in lane r / 2 as rows[r % 2].
+    int myrow[4];
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int src = warp * 8 + it;
-      const int r0 = __shfl_sync(0xffffffffu, rows[0], src);
-      const int r1 = __shfl_sync(0xffffffffu, rows[1], src);
-      const int r2 = __shfl_sync(0xffffffffu, rows[2], src);
-      const int r3 = __shfl_sync(0xffffffffu, rows[3], src);
-      const int sel = lane >> 3;
-      myrow[it] = sel == 0 ? r0 : (sel == 1 ? r1 : (sel == 2 ? r2 : r3));
+    for (int it = 0; it < 4; ++it) {
+      const int r = warp * 16 + it * 4 + sel;
+      const int r0 = __shfl_sync(0xffffffffu, rows[0], r >> 1);
+      const int r1 = __shfl_sync(0xffffffffu, rows[1], r >> 1);
+      myrow[it] = (r & 1) ? r1 : r0;
     }
 #pragma unroll 1
     for (int u = 0; u < 5; ++u) {
-      uint32_t landed, full, par;
-      ring.where(ring.iss, landed, full, par);
-      uint32_t empty, dst;
+      uint32_t empty, full, par, dst;
       int first_chunk, n_chunks;
       if (u < 4) {
-        const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u)) % L::kNV;
+        const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+        const uint32_t s = vi % L::kNV;
         empty = smem_u32(&m.v_empty[s]);
+        full = smem_u32(&m.v_full[s]);
+        par = (vi / L::kNV) & 1u;
         dst = vbase + s * kPairBytes;
         first_chunk = 2 * u;
         n_chunks = 2;
       } else {
         const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
         empty = smem_u32(&m.rp_empty[rs]);
+        full = smem_u32(&m.rp_full[rs]);
+        par = (static_cast<uint32_t>(n) / L::kNR) & 1u;
         dst = rbase + rs * kChunkBytes;
         first_chunk = 8;
         n_chunks = 1;
       }
-      const bool ok = ring.wait_consumer(empty, par ^ 1u, deadline, ab);
+      const bool ok = mbar_wait(empty, par ^ 1u, deadline, ab);
       if (!__all_sync(0xffffffffu, ok)) return false;
       for (int c = 0; c < n_chunks; ++c) {
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int r = warp * 32 + it * 4 + (lane >> 3);
+        for (int it = 0; it < 4; ++it) {
+          const int r = warp * 16 + it * 4 + sel;
           const int src_row = myrow[it];
           const __nv_bfloat16* src =
               p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
           cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
         }
       }
-      cp_async_arrive_on(landed);
-      ring.iss += 1;
-      ring.forward_ready();
+      // The hardware arrives on the tile's full barrier for this thread once
+      // all of this thread's copies so far have landed; the thread itself
+      // never waits on them.
+      cp_async_arrive_on(full);
     }
     ++n;
   }
-  const bool dok = ring.drain(deadline, ab);
-  if (!__all_sync(0xffffffffu, dok)) return false;
   if (warp == 0) {
     const int k = n % kInfoDepth;
     const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
@@ -426,20 +365,84 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int to
   return true;
 }
 
+// ------------------------------------------------------------------ MMA issuer
+
+template <int N>
+__device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase, uint32_t rbase, uint32_t tmem,
+                                         int n, uint64_t deadline, const volatile int* ab) {
+  using L = Layout<N>;
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(64, N, false, false);
+  const uint32_t tS = tmem + static_cast<uint32_t>(n & 1) * N;
+  // Acquire all five tiles of the block, then one proxy fence: the tiles were
+  // written by cp.async (generic proxy) and are read by the tensor core
+  // (async proxy).
+  uint32_t slot[4];
+#pragma unroll
+  for (int pr = 0; pr < 4; ++pr) {
+    const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(pr);
+    slot[pr] = vi % L::kNV;
+    if (!mbar_wait(smem_u32(&m.v_full[slot[pr]]), (vi / L::kNV) & 1u, deadline, ab)) return false;
+  }
+  const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
+  if (!mbar_wait(smem_u32(&m.rp_full[rs]), (static_cast<uint32_t>(n) / L::kNR) & 1u, deadline, ab)) return false;
+  fence_proxy_async_smem();
+  tc_fence_after();
+#pragma unroll
+  for (int pr = 0; pr < 4; ++pr) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t a = smem_desc(vbase + slot[pr] * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
+        const uint64_t b = smem_desc(qbase + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+        mma_bf16_ss(tS, a, b, kIdescQK, (pr | c | kk) != 0 ? 1u : 0u);
+      }
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
+    const uint64_t b = smem_desc(qbase + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+    mma_bf16_ss(tS, a, b, kIdescQK, 1u);
+  }
+  mma_commit(smem_u32(&m.s_full[n & 1]));
+  return true;
+}
+
+template <int N>
+__device__ __forceinline__ bool issue_pv(Misc& m, uint32_t vbase, uint32_t rbase, uint32_t tmem, int n,
+                                         uint64_t deadline, const volatile int* ab) {
+  using L = Layout<N>;
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
+  const uint32_t tO = tmem + 2 * N;
+  if (!mbar_wait(smem_u32(&m.p_full[n & 1]), (n >> 1) & 1, deadline, ab)) return false;
+  tc_fence_after();
+  const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
+#pragma unroll 1
+  for (int mt = 0; mt < 4; ++mt) {
+    const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(mt)) % L::kNV;
+#pragma unroll
+    for (int ks = 0; ks < kBlk / 16; ++ks) {
+      const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
+      const uint64_t b = smem_desc(rbase + rs * kChunkBytes + ks * 16 * L::kPRow, 16 * L::kPRow * 8,
+                                   8 * L::kPRow, L::kPSwz);
+      mma_bf16_ss(tO + mt * N, a, b, kIdescPV, (n > 0 || ks > 0) ? 1u : 0u);
+    }
+    mma_commit(smem_u32(&m.v_empty[s]));
+  }
+  mma_commit(smem_u32(&m.rp_empty[rs]));
+  return true;
+}
+
 template <int N>
 __device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline) {
   using L = Layout<N>;
   const volatile int* ab = &m.abort_flag;
-  constexpr uint32_t kIdescQK = idesc_bf16_f32(128, N, false, false);
-  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
-  const uint32_t tS = tmem;
-  const uint32_t tO = tmem + N;
   if (!mbar_wait(smem_u32(&m.q_full), 0, deadline, ab)) return false;
   tc_fence_after();
-  uint32_t vuse = 0;
   int n = 0;
   for (;;) {
     const int k = n % kInfoDepth;
@@ -447,55 +450,22 @@ __device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadlin
     const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
     mbar_arrive(smem_u32(&m.info_empty[k]));
     if (blk < 0) break;
-    // S^T = K_blk . Q^T over the 9 column chunks (value pairs, then rope).
-#pragma unroll 1
-    for (int pr = 0; pr < 4; ++pr) {
-      const uint32_t s = (vuse + pr) % L::kNV;
-      if (!mbar_wait(smem_u32(&m.v_full[s]), ((vuse + pr) / L::kNV) & 1u, deadline, ab)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc(vbase + s * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
-          const uint64_t b = smem_desc(qbase + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
-          mma_bf16_ss(tS, a, b, kIdescQK, (pr | c | kk) != 0 ? 1u : 0u);
-        }
-      }
-    }
-    const uint32_t rs = n % L::kNR;
-    if (!mbar_wait(smem_u32(&m.rp_full[rs]), (n / L::kNR) & 1u, deadline, ab)) return false;
-    tc_fence_after();
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
-      const uint64_t b = smem_desc(qbase + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
-      mma_bf16_ss(tS, a, b, kIdescQK, 1u);
-    }
-    mma_commit(smem_u32(&m.s_full));
-    // O^T += V^T . P^T once the softmax has written P^T into the rope slot.
-    if (!mbar_wait(smem_u32(&m.p_full), n & 1, deadline, ab)) return false;
-    tc_fence_after();
-#pragma unroll 1
-    for (int mt = 0; mt < 4; ++mt) {
-      const uint32_t s = (vuse + mt) % L::kNV;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-        const uint64_t b = smem_desc(rbase + rs * kChunkBytes + ks * 16 * L::kPRow, 16 * L::kPRow * 8,
-                                     8 * L::kPRow, L::kPSwz);
-        mma_bf16_ss(tO + mt * N, a, b, kIdescPV, (n > 0 || ks > 0) ? 1u : 0u);
-      }
-      mma_commit(smem_u32(&m.v_empty[s]));
-    }
-    mma_commit(smem_u32(&m.rp_empty[rs]));
-    vuse += 4;
+    // QK of this block goes ahead of PV of the previous one, so the tensor
+    // core has work while the softmax runs.
+    if (!issue_qk<N>(m, qbase, vbase, rbase, tmem, n, deadline, ab)) return false;
+    if (n > 0 && !issue_pv<N>(m, vbase, rbase, tmem, n - 1, deadline, ab)) return false;
     ++n;
   }
-  if (n > 0) mma_commit(smem_u32(&m.o_full));
-  else mbar_arrive(smem_u32(&m.o_full));
+  if (n > 0) {
+    if (!issue_pv<N>(m, vbase, rbase, tmem, n - 1, deadline, ab)) return false;
+    mma_commit(smem_u32(&m.o_full));
+  } else {
+    mbar_arrive(smem_u32(&m.o_full));
+  }
   return true;
 }
+
+// ------------------------------------------------------------------ softmax + epilogue
 
 template <int N>
 __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int tok, int split, int h0,
@@ -507,10 +477,10 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   const int lane = static_cast<int>(lane_id());
   const int tid = static_cast<int>(threadIdx.x) - kSoftmaxWarp0 * 32;  // 0..127
   const int q4 = warp & 3;                             // TMEM lane quarter of this warp
-  const int row = q4 * 32 + lane;                      // kv row of the block == TMEM lane
+  const bool has_row = lane < 16;                      // M=64 result: 16 lanes per quarter
+  const int row = q4 * 16 + (lane & 15);               // kv row of the block (when has_row)
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-  const uint32_t tS = tmem + lane_off;
-  const uint32_t tO = tmem + lane_off + N;
+  const uint32_t tO = tmem + lane_off + 2 * N;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
 
@@ -531,7 +501,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   }
 
   // Head tid's running sum of exp2(s - m) (owner threads tid < N); the
-  // per-block sums arrive through m.rsum, reduced over the 128 rows.
+  // per-block sums arrive through m.rsum, reduced over the 64 rows.
   float lrun = 0.f;
   int n = 0;
   for (;;) {
@@ -541,13 +511,14 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     const bool iok = mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab);
     if (bar_red_or_128(!iok)) return false;
     const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
-    const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&m.info_mask[k][row & 3]);
+    const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&m.info_mask[k][row & 1]);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
     if (blk < 0) break;
-    const bool valid = ((bits >> (row >> 2)) & 1u) != 0u;
+    const bool valid = has_row && ((bits >> (row >> 1)) & 1u) != 0u;
+    const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(n & 1) * N;
 
-    const bool sok = mbar_wait(smem_u32(&m.s_full), n & 1, deadline, ab);
+    const bool sok = mbar_wait(smem_u32(&m.s_full[n & 1]), (n >> 1) & 1, deadline, ab);
     tc_fence_after();
     // Block max per head: butterfly over the warp, then over the 4 warps.
 #pragma unroll
@@ -575,8 +546,13 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     }
     const bool rescale = bar_red_or_128(grew);
     if (rescale && n > 0) {
-      // O^T holds the sum through the previous block (its PV completed
-      // before S of this block was committed): rescale each head column.
+      // O^T must hold exactly the blocks before this one: wait for the
+      // previous block's P.V (its last commit releases that block's rope /
+      // P^T slot), then rescale each head column.
+      const int pb = n - 1;
+      const bool pok = mbar_wait(smem_u32(&m.rp_empty[pb % L::kNR]), (pb / L::kNR) & 1, deadline, ab);
+      tc_fence_after();
+      if (bar_red_or_128(!pok)) return false;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -608,16 +584,18 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
           const int h = ps * H + c * 8 + i;
           s[c * 8 + i] = valid ? fast_exp2(s[c * 8 + i] * p.scale_log2 - m.mrun[h]) : 0.f;
         }
-        const uint32_t chunk = static_cast<uint32_t>(ps * H / 8 + c);
-        st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
-                     pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
-                     pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
+        if (has_row) {
+          const uint32_t chunk = static_cast<uint32_t>(ps * H / 8 + c);
+          st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
+                       pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
+                       pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
+        }
       }
       warp_xreduce<H, false>(s, lane, m.rsum[q4] + ps * H);
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    mbar_arrive(smem_u32(&m.p_full));
+    mbar_arrive(smem_u32(&m.p_full[n & 1]));
     ++n;
   }
 
@@ -642,6 +620,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     }
   }
   named_bar_sync(1, 128);
+  const int dvrow = q4 * 32 + lane;   // O^T (M=128) lane of this thread
 #pragma unroll 1
   for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -654,7 +633,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[i] = 0.f;
       }
-      const int dv = mt * 128 + row;
+      const int dv = mt * 128 + dvrow;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int h = g * 16 + i;
@@ -687,14 +666,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_kernel(const __gri
   const int hv = min(N, p.h_q - h0);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < L::kNV; ++i) {
       mbar_init(smem_u32(&m.v_full[i]), kProducerWarps * 32);
-      mbar_init(smem_u32(&m.v_land[i]), kProducerWarps * 32);
       mbar_init(smem_u32(&m.v_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < L::kNR; ++i) {
       mbar_init(smem_u32(&m.rp_full[i]), kProducerWarps * 32);
-      mbar_init(smem_u32(&m.rp_land[i]), kProducerWarps * 32);
       mbar_init(smem_u32(&m.rp_empty[i]), 1);
     }
     for (int i = 0; i < kInfoDepth; ++i) {
@@ -702,8 +679,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_kernel(const __gri
       mbar_init(smem_u32(&m.info_empty[i]), 5);
     }
     mbar_init(smem_u32(&m.q_full), 1);
-    mbar_init(smem_u32(&m.s_full), 1);
-    mbar_init(smem_u32(&m.p_full), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&m.s_full[i]), 1);
+      mbar_init(smem_u32(&m.p_full[i]), 128);
+    }
     mbar_init(smem_u32(&m.o_full), 1);
     mbar_init(smem_u32(&m.drain), 1);
     m.abort_flag = 0;
@@ -725,8 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_kernel(const __gri
     const int jb = static_cast<int>((static_cast<long long>(split) * nb) / p.splits);
     const int je = static_cast<int>((static_cast<long long>(split + 1) * nb) / p.splits);
     if (warp < kProducerWarps) {
-      TileRing<N> ring(m);
-      if (!run_producer<N>(p, m, sbase, tok, jb, je, deadline, ring)) raise_error(m, kErrProducerWait);
+      if (!run_producer<N>(p, m, sbase, tok, jb, je, deadline)) raise_error(m, kErrProducerWait);
       // Drain: every copy this thread issued has landed before the CTA can
       // exit, whether or not the consumers got to it.
       asm volatile("cp.async.wait_all;" ::: "memory");
@@ -749,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_kernel(const __gri
   if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
 }
 
-// ------------------------------------------------------------------ helpers kernels
+// ------------------------------------------------------------------ helper kernels
 
 // Merge per-split partial results: LSE = ln sum_s exp(LSE_s),
 // out = sum_s exp(LSE_s - LSE) * O_s (each O_s already normalised).

@@ -180,6 +180,31 @@ def test_decode_config_all_tokens(smla):
     _check_decode(smla, mi.config(5))
 
 
+# ---------------------------------------------------------------- determinism
+
+def test_repeated_runs_are_bit_identical(smla):
+    """The kernel's reduction order is fixed, so repeated calls on the same
+    inputs must agree bit for bit; a copy read by the tensor core before it
+    became visible would show up here as run-to-run differences.  Runs are
+    interleaved with L2 flushes and decode calls to vary the timing."""
+    case = mi.config(2)
+    d = lambda t: t.to(DEV)
+    q, kv, idx = d(case.q), d(case.kv), d(case.indices)
+    dec = mi.decode_case(901, batch=4, s_next=6, h_q=8, lo=3000, hi=9000, topk=2048, spare_pages=4)
+    dq, dc, dbt, dsl, di = (d(dec.q), d(dec.kv_cache), d(dec.block_table), d(dec.cache_seqlens), d(dec.indices))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=DEV)
+    ref_o, ref_l = smla.sparse_mla_fwd(q, kv, idx, case.sm_scale)
+    ref_do, ref_dl = smla.sparse_mla_decode(dq, dc, dbt, dsl, di, dec.sm_scale, dec.page_size)
+    for it in range(12):
+        if it % 3 == 0:
+            flush.zero_()
+        o, l = smla.sparse_mla_fwd(q, kv, idx, case.sm_scale)
+        do, dl = smla.sparse_mla_decode(dq, dc, dbt, dsl, di, dec.sm_scale, dec.page_size)
+        assert torch.equal(o, ref_o) and torch.equal(l, ref_l), f"prefill run {it} differs"
+        assert torch.equal(do, ref_do) and torch.equal(dl, ref_dl), f"decode run {it} differs"
+    torch.cuda.synchronize()
+
+
 # ---------------------------------------------------------------- failure detection
 
 def test_device_wait_timeout_reports_and_recovers(smla):

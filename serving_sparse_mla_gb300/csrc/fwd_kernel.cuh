@@ -38,7 +38,11 @@
 //                      it.  On GB300 this gathers random 1152-B rows ~6x
 //                      faster than TMA tile::gather4 (13.9 vs 2.2 TB/s from
 //                      L2, 5.3 vs 2.2 TB/s from HBM).
-//   warp 4 (MMA)       one thread issues tcgen05.mma (kind::f16, fp32 in TMEM):
+//   warps 4, 9 (MMA)   two threads issue tcgen05.mma (kind::f16, fp32 in TMEM),
+//                      each for half of every block (value pairs 0,1 + rope /
+//                      pairs 2,3 of QK^T into two partial S^T, dv 0..255 /
+//                      256..511 of P.V); one issuer sustains ~59 cycles per
+//                      MMA on GB300, two ~39 in aggregate:
 //                        S^T[64 x N]   = K_blk[64 x 576] . Q^T[576 x N]   (M=64)
 //                        O^T[512 x N] += V^T[512 x 64]  . P^T[64 x N]    (M=128)
 //                      (swap-AB: kv rows are M and heads are N, so 8 heads
@@ -48,14 +52,16 @@
 //                      double-buffered, so QK of the next block runs while the
 //                      softmax works on the current one.
 //   warps 5..8         the M=64 result sits in lanes 32*(i/16) + i%16, so
-//   (softmax)          lanes 0..15 of each warp own one kv row each: load the
-//                      S^T row, mask, reduce the per-head block max across the
-//                      64 rows (warp transpose-reduce plus a shared-memory
-//                      step), keep a lazily updated running max (O is rescaled
-//                      only when a head's max grows by more than 2^8, after the
-//                      previous P.V has completed), write P^T = exp2(s - m) as
-//                      bf16 into the block's rope slot, and at the end
-//                      normalise O^T and write out / LSE.
+//   (+ 10..13 for      lanes 0..15 of each warp own one kv row each; a group
+//   64 heads;          of 4 warps owns up to 32 heads (two groups for 64 heads,
+//   softmax)           each with its own named barrier).  Per row: add the
+//                      two partial S^T rows, mask, reduce the per-head block
+//                      max across the 64 rows (warp transpose-reduce plus a
+//                      shared-memory step), keep a lazily updated running max
+//                      (O is rescaled only when a head's max grows by more
+//                      than 2^8, after the previous P.V has completed), write
+//                      P^T = exp2(s - m) as bf16 into the block's rope slot,
+//                      and at the end normalise O^T and write out / LSE.
 //
 // All waits are bounded (see ptx.cuh); a timed-out CTA records an error in
 // the device error word, drains its in-flight copies and MMAs, frees TMEM
@@ -75,9 +81,11 @@ constexpr int kChunkBytes = kBlk * 128;      // 64 rows x 64 bf16 columns
 constexpr int kPairBytes = 2 * kChunkBytes;  // 64 rows x 128 columns
 constexpr int kInfoDepth = 8;
 constexpr int kProducerWarps = 4;
-constexpr int kMmaWarp = 4;
-constexpr int kSoftmaxWarp0 = 5;
-constexpr int kThreads = 288;
+constexpr int kMmaWarp = 4;                  // MMA issuer A (also owns the TMEM allocation)
+constexpr int kMmaWarpB = 9;                 // MMA issuer B
+// Softmax group g (4 warps, one per TMEM lane quarter) owns heads
+// [32 g, 32 g + 32): warps 5..8 for g = 0, warps 10..13 for g = 1.
+__host__ __device__ constexpr int softmax_warp0(int g) { return g == 0 ? 5 : 10; }
 constexpr float kLazyRescale = 8.0f;         // log2 units
 constexpr int kMaxSmem = 232448;
 
@@ -115,6 +123,9 @@ struct Layout {
   static constexpr int kPRow = N * 2;                             // bytes of one P^T row
   static constexpr uint32_t kPSwz = N == 64 ? SWZ_128B : (N == 32 ? SWZ_64B : SWZ_32B);
   static constexpr int kTmemCols = N == 64 ? 512 : (N == 32 ? 256 : 128);
+  static constexpr int kGroups = N == 64 ? 2 : 1;                 // softmax groups
+  static constexpr int kHG = N / kGroups;                         // heads per group (<= 32)
+  static constexpr int kThreads = (6 + 4 * kGroups) * 32;
   static constexpr int kQOff = 0;
   static constexpr int kVOff = 9 * N * 128;
   static constexpr int kROff = kVOff + kNV * kPairBytes;
@@ -126,7 +137,7 @@ struct __align__(16) Misc {
   uint64_t v_full[12], v_empty[12];
   uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
-  uint64_t q_full, s_full[2], p_full[2], o_full, drain;
+  uint64_t q_full, s_full[2][2], p_full[2], o_full, drain[2];
   int32_t info_blk[kInfoDepth];
   uint32_t info_mask[kInfoDepth][2];
   float red[4][64];
@@ -231,16 +242,17 @@ __device__ __forceinline__ void warp_xreduce(float (&v)[N], int lane, float* dst
     if (i < cnt) dst[base + i] = v[i];
 }
 
-// bar.sync over the 128 softmax threads, returning the OR of `pred`.
-__device__ __forceinline__ bool bar_red_or_128(bool pred) {
+// bar.sync over the 128 threads of one softmax group (named barrier `id`),
+// returning the OR of `pred`.
+__device__ __forceinline__ bool bar_red_or_128(uint32_t id, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(pred ? 1u : 0u)
+      : "r"(pred ? 1u : 0u), "r"(id)
       : "memory");
   return r != 0;
 }
@@ -367,59 +379,69 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int to
 
 // ------------------------------------------------------------------ MMA issuer
 
-template <int N>
+// The MMA work of a block is split between two issuing threads (one tcgen05
+// issuer sustains ~59 cycles per MMA here, two ~39 in aggregate):
+//   part 0: QK^T over value pairs 0,1 and the rope columns, P.V for dv 0..255
+//   part 1: QK^T over value pairs 2,3,                   P.V for dv 256..511
+// Each part accumulates its own partial S^T; the softmax adds the two.
+template <int N, int PART>
 __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase, uint32_t rbase, uint32_t tmem,
                                          int n, uint64_t deadline, const volatile int* ab) {
   using L = Layout<N>;
   constexpr uint32_t kIdescQK = idesc_bf16_f32(64, N, false, false);
-  const uint32_t tS = tmem + static_cast<uint32_t>(n & 1) * N;
-  // Acquire all five tiles of the block, then one proxy fence: the tiles were
-  // written by cp.async (generic proxy) and are read by the tensor core
-  // (async proxy).
-  uint32_t slot[4];
+  const uint32_t tS = tmem + static_cast<uint32_t>(PART * 2 + (n & 1)) * N;
+  // Acquire this part's tiles, then one proxy fence: the tiles were written
+  // by cp.async (generic proxy) and are read by the tensor core (async proxy).
+  uint32_t slot[2];
 #pragma unroll
-  for (int pr = 0; pr < 4; ++pr) {
-    const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(pr);
-    slot[pr] = vi % L::kNV;
-    if (!mbar_wait(smem_u32(&m.v_full[slot[pr]]), (vi / L::kNV) & 1u, deadline, ab)) return false;
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(2 * PART + i);
+    slot[i] = vi % L::kNV;
+    if (!mbar_wait(smem_u32(&m.v_full[slot[i]]), (vi / L::kNV) & 1u, deadline, ab)) return false;
   }
   const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
-  if (!mbar_wait(smem_u32(&m.rp_full[rs]), (static_cast<uint32_t>(n) / L::kNR) & 1u, deadline, ab)) return false;
+  if (PART == 0 &&
+      !mbar_wait(smem_u32(&m.rp_full[rs]), (static_cast<uint32_t>(n) / L::kNR) & 1u, deadline, ab))
+    return false;
   fence_proxy_async_smem();
   tc_fence_after();
 #pragma unroll
-  for (int pr = 0; pr < 4; ++pr) {
+  for (int i = 0; i < 2; ++i) {
+    const int pr = 2 * PART + i;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t a = smem_desc(vbase + slot[pr] * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
+        const uint64_t a = smem_desc(vbase + slot[i] * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
         const uint64_t b = smem_desc(qbase + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
-        mma_bf16_ss(tS, a, b, kIdescQK, (pr | c | kk) != 0 ? 1u : 0u);
+        mma_bf16_ss(tS, a, b, kIdescQK, (i | c | kk) != 0 ? 1u : 0u);
       }
     }
   }
+  if (PART == 0) {
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
-    const uint64_t b = smem_desc(qbase + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
-    mma_bf16_ss(tS, a, b, kIdescQK, 1u);
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
+      const uint64_t b = smem_desc(qbase + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+      mma_bf16_ss(tS, a, b, kIdescQK, 1u);
+    }
   }
-  mma_commit(smem_u32(&m.s_full[n & 1]));
+  mma_commit(smem_u32(&m.s_full[PART][n & 1]));
   return true;
 }
 
-template <int N>
+template <int N, int PART>
 __device__ __forceinline__ bool issue_pv(Misc& m, uint32_t vbase, uint32_t rbase, uint32_t tmem, int n,
                                          uint64_t deadline, const volatile int* ab) {
   using L = Layout<N>;
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
-  const uint32_t tO = tmem + 2 * N;
+  const uint32_t tO = tmem + 4 * N;
   if (!mbar_wait(smem_u32(&m.p_full[n & 1]), (n >> 1) & 1, deadline, ab)) return false;
   tc_fence_after();
   const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
-#pragma unroll 1
-  for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int mt = 2 * PART + i;
     const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(mt)) % L::kNV;
 #pragma unroll
     for (int ks = 0; ks < kBlk / 16; ++ks) {
@@ -430,11 +452,11 @@ __device__ __forceinline__ bool issue_pv(Misc& m, uint32_t vbase, uint32_t rbase
     }
     mma_commit(smem_u32(&m.v_empty[s]));
   }
-  mma_commit(smem_u32(&m.rp_empty[rs]));
+  mma_commit(smem_u32(&m.rp_empty[rs]));   // two arrivals (one per part) release the P^T / rope slot
   return true;
 }
 
-template <int N>
+template <int N, int PART>
 __device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline) {
   using L = Layout<N>;
   const volatile int* ab = &m.abort_flag;
@@ -451,13 +473,14 @@ __device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadlin
     mbar_arrive(smem_u32(&m.info_empty[k]));
     if (blk < 0) break;
     // QK of this block goes ahead of PV of the previous one, so the tensor
-    // core has work while the softmax runs.
-    if (!issue_qk<N>(m, qbase, vbase, rbase, tmem, n, deadline, ab)) return false;
-    if (n > 0 && !issue_pv<N>(m, vbase, rbase, tmem, n - 1, deadline, ab)) return false;
+    // core has work while the softmax runs.  (S buffer n&1 is free: PV(n-2),
+    // issued before by this thread, waited for the softmax of block n-2.)
+    if (!issue_qk<N, PART>(m, qbase, vbase, rbase, tmem, n, deadline, ab)) return false;
+    if (n > 0 && !issue_pv<N, PART>(m, vbase, rbase, tmem, n - 1, deadline, ab)) return false;
     ++n;
   }
   if (n > 0) {
-    if (!issue_pv<N>(m, vbase, rbase, tmem, n - 1, deadline, ab)) return false;
+    if (!issue_pv<N, PART>(m, vbase, rbase, tmem, n - 1, deadline, ab)) return false;
     mma_commit(smem_u32(&m.o_full));
   } else {
     mbar_arrive(smem_u32(&m.o_full));
@@ -469,99 +492,106 @@ __device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadlin
 
 template <int N>
 __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int tok, int split, int h0,
-                            int hv, uint64_t deadline) {
+                            int hv, int grp, uint64_t deadline) {
   using L = Layout<N>;
-  constexpr int H = N > 32 ? 32 : N;   // heads per register pass
+  constexpr int H = L::kHG;            // heads this group owns (16 or 32)
   const volatile int* ab = &m.abort_flag;
+  const uint32_t bar_id = 1u + static_cast<uint32_t>(grp);
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
-  const int tid = static_cast<int>(threadIdx.x) - kSoftmaxWarp0 * 32;  // 0..127
+  const int tid = static_cast<int>(threadIdx.x) - softmax_warp0(grp) * 32;  // 0..127 within the group
+  const int hb = grp * H;                              // first head of the group
   const int q4 = warp & 3;                             // TMEM lane quarter of this warp
   const bool has_row = lane < 16;                      // M=64 result: 16 lanes per quarter
   const int row = q4 * 16 + (lane & 15);               // kv row of the block (when has_row)
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-  const uint32_t tO = tmem + lane_off + 2 * N;
+  const uint32_t tO = tmem + lane_off + 4 * N + hb;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
 
-  // Q for heads [h0, h0+N) -> shared memory, K-major with the 128B swizzle;
-  // heads past h_q are zero.
+  // Q rows of this group's heads -> shared memory, K-major with the 128B
+  // swizzle; heads past h_q are zero.
   {
     const __nv_bfloat16* qt = p.q + (static_cast<size_t>(tok) * p.h_q + h0) * kDqk;
-    for (int x = tid; x < N * 72; x += 128) {
-      const int h = x / 72, rem = x - h * 72, c = rem >> 3, piece = rem & 7;
+    for (int x = tid; x < H * 72; x += 128) {
+      const int h = hb + x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (h < hv) v = __ldg(reinterpret_cast<const uint4*>(qt + static_cast<size_t>(h) * kDqk + c * 64 + piece * 8));
       st_shared_v4(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4), v.x, v.y, v.z, v.w);
     }
     fence_proxy_async_smem();
-    if (tid < N) m.mrun[tid] = -INFINITY;
-    named_bar_sync(1, 128);
+    if (tid < H) m.mrun[hb + tid] = -INFINITY;
+    named_bar_sync(bar_id, 128);
     if (tid == 0) mbar_arrive(smem_u32(&m.q_full));
   }
 
-  // Head tid's running sum of exp2(s - m) (owner threads tid < N); the
+  // Head hb+tid's running sum of exp2(s - m) (owner threads tid < H); the
   // per-block sums arrive through m.rsum, reduced over the 64 rows.
   float lrun = 0.f;
   int n = 0;
   for (;;) {
     const int k = n % kInfoDepth;
-    // Every wait is followed by a barrier that ORs the failures of the 128
-    // softmax threads, so they all continue or all return together.
+    // Every wait is followed by a barrier that ORs the failures of the
+    // group's 128 threads, so they all continue or all return together.
     const bool iok = mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab);
-    if (bar_red_or_128(!iok)) return false;
+    if (bar_red_or_128(bar_id, !iok)) return false;
     const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
     const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&m.info_mask[k][row & 1]);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
     if (blk < 0) break;
     const bool valid = has_row && ((bits >> (row >> 1)) & 1u) != 0u;
-    const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(n & 1) * N;
+    const uint32_t tSa = tmem + lane_off + static_cast<uint32_t>(n & 1) * N + hb;        // part 0
+    const uint32_t tSb = tmem + lane_off + static_cast<uint32_t>(2 + (n & 1)) * N + hb;  // part 1
 
-    const bool sok = mbar_wait(smem_u32(&m.s_full[n & 1]), (n >> 1) & 1, deadline, ab);
+    const bool sok = mbar_wait(smem_u32(&m.s_full[0][n & 1]), (n >> 1) & 1, deadline, ab) &&
+                     mbar_wait(smem_u32(&m.s_full[1][n & 1]), (n >> 1) & 1, deadline, ab);
     tc_fence_after();
     // Block max per head: butterfly over the warp, then over the 4 warps.
+    {
+      float s[H], t[H];
 #pragma unroll
-    for (int ps = 0; ps < N / H; ++ps) {
-      float s[H];
-#pragma unroll
-      for (int g = 0; g < H / 16; ++g) tmem_ld16(tS + ps * H + g * 16, s + g * 16);
+      for (int g = 0; g < H / 16; ++g) {
+        tmem_ld16(tSa + g * 16, s + g * 16);
+        tmem_ld16(tSb + g * 16, t + g * 16);
+      }
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < H; ++i) s[i] = valid ? s[i] * p.scale_log2 : -INFINITY;
-      warp_xreduce<H, true>(s, lane, m.red[q4] + ps * H);
+      for (int i = 0; i < H; ++i) s[i] = valid ? (s[i] + t[i]) * p.scale_log2 : -INFINITY;
+      warp_xreduce<H, true>(s, lane, m.red[q4] + hb);
     }
-    if (bar_red_or_128(!sok)) return false;
+    if (bar_red_or_128(bar_id, !sok)) return false;
     bool grew = false;
-    if (tid < N) {
-      if (n > 0) lrun += (m.rsum[0][tid] + m.rsum[1][tid]) + (m.rsum[2][tid] + m.rsum[3][tid]);
-      const float bm = fmaxf(fmaxf(m.red[0][tid], m.red[1][tid]), fmaxf(m.red[2][tid], m.red[3][tid]));
-      const float mo = m.mrun[tid];
+    if (tid < H) {
+      const int h = hb + tid;
+      if (n > 0) lrun += (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]);
+      const float bm = fmaxf(fmaxf(m.red[0][h], m.red[1][h]), fmaxf(m.red[2][h], m.red[3][h]));
+      const float mo = m.mrun[h];
       const float mn = (bm > mo + kLazyRescale) ? bm : mo;
       const float al = fast_exp2(mo - mn);
       lrun *= al;
-      m.alpha[tid] = al;
-      m.mrun[tid] = mn;
+      m.alpha[h] = al;
+      m.mrun[h] = mn;
       grew = (mn != mo);
     }
-    const bool rescale = bar_red_or_128(grew);
+    const bool rescale = bar_red_or_128(bar_id, grew);
     if (rescale && n > 0) {
       // O^T must hold exactly the blocks before this one: wait for the
-      // previous block's P.V (its last commit releases that block's rope /
-      // P^T slot), then rescale each head column.
+      // previous block's P.V (its last commits release that block's rope /
+      // P^T slot), then rescale this group's head columns.
       const int pb = n - 1;
       const bool pok = mbar_wait(smem_u32(&m.rp_empty[pb % L::kNR]), (pb / L::kNR) & 1, deadline, ab);
       tc_fence_after();
-      if (bar_red_or_128(!pok)) return false;
+      if (bar_red_or_128(bar_id, !pok)) return false;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-        for (int g = 0; g < N / 16; ++g) {
+        for (int g = 0; g < H / 16; ++g) {
           float o[16];
           tmem_ld16(tO + mt * N + g * 16, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] *= m.alpha[g * 16 + i];
+          for (int i = 0; i < 16; ++i) o[i] *= m.alpha[hb + g * 16 + i];
           tmem_st16(tO + mt * N + g * 16, o);
         }
       }
@@ -569,29 +599,31 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     }
     // P^T row (bf16) into the rope slot of this block, MN-major swizzled,
     // and the block's per-head sums of P.
-    const uint32_t prow = rbase + (n % L::kNR) * kChunkBytes + row * L::kPRow;
-    const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
+    {
+      const uint32_t prow = rbase + (n % L::kNR) * kChunkBytes + row * L::kPRow;
+      const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
+      float s[H], t[H];
 #pragma unroll
-    for (int ps = 0; ps < N / H; ++ps) {
-      float s[H];
-#pragma unroll
-      for (int g = 0; g < H / 16; ++g) tmem_ld16(tS + ps * H + g * 16, s + g * 16);
+      for (int g = 0; g < H / 16; ++g) {
+        tmem_ld16(tSa + g * 16, s + g * 16);
+        tmem_ld16(tSb + g * 16, t + g * 16);
+      }
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < H / 8; ++c) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int h = ps * H + c * 8 + i;
-          s[c * 8 + i] = valid ? fast_exp2(s[c * 8 + i] * p.scale_log2 - m.mrun[h]) : 0.f;
+          const int h = hb + c * 8 + i;
+          s[c * 8 + i] = valid ? fast_exp2((s[c * 8 + i] + t[c * 8 + i]) * p.scale_log2 - m.mrun[h]) : 0.f;
         }
         if (has_row) {
-          const uint32_t chunk = static_cast<uint32_t>(ps * H / 8 + c);
+          const uint32_t chunk = static_cast<uint32_t>(hb / 8 + c);
           st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
                        pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
                        pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
         }
       }
-      warp_xreduce<H, false>(s, lane, m.rsum[q4] + ps * H);
+      warp_xreduce<H, false>(s, lane, m.rsum[q4] + hb);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -602,29 +634,30 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   // ---------------------------------------------------------- epilogue
   const bool ook = mbar_wait(smem_u32(&m.o_full), 0, deadline, ab);
   tc_fence_after();
-  if (bar_red_or_128(!ook)) return false;
+  if (bar_red_or_128(bar_id, !ook)) return false;
   const size_t tok_h = static_cast<size_t>(tok) * p.h_q + h0;
-  if (tid < N) {
-    if (n > 0) lrun += (m.rsum[0][tid] + m.rsum[1][tid]) + (m.rsum[2][tid] + m.rsum[3][tid]);
+  if (tid < H) {
+    const int h = hb + tid;
+    if (n > 0) lrun += (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]);
     float lse;
     if (n > 0) {
-      lse = (m.mrun[tid] + log2f(lrun)) * 0.69314718055994530942f;
-      m.fin[tid] = 1.0f / lrun;
+      lse = (m.mrun[h] + log2f(lrun)) * 0.69314718055994530942f;
+      m.fin[h] = 1.0f / lrun;
     } else {
       lse = -INFINITY;
-      m.fin[tid] = 0.f;
+      m.fin[h] = 0.f;
     }
-    if (tid < hv) {
-      if (p.splits > 1) p.part_lse[static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + tid] = lse;
-      else p.lse[tok_h + tid] = lse;
+    if (h < hv) {
+      if (p.splits > 1) p.part_lse[static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + h] = lse;
+      else p.lse[tok_h + h] = lse;
     }
   }
-  named_bar_sync(1, 128);
+  named_bar_sync(bar_id, 128);
   const int dvrow = q4 * 32 + lane;   // O^T (M=128) lane of this thread
 #pragma unroll 1
   for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-    for (int g = 0; g < N / 16; ++g) {
+    for (int g = 0; g < H / 16; ++g) {
       float o[16];
       if (n > 0) {
         tmem_ld16(tO + mt * N + g * 16, o);
@@ -636,7 +669,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
       const int dv = mt * 128 + dvrow;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int h = g * 16 + i;
+        const int h = hb + g * 16 + i;
         if (h < hv) {
           const float val = o[i] * m.fin[h];
           if (p.splits > 1)
@@ -653,7 +686,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 // ------------------------------------------------------------------ kernel
 
 template <int N>
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Layout<N>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -672,19 +705,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_kernel(const __gri
     }
     for (int i = 0; i < L::kNR; ++i) {
       mbar_init(smem_u32(&m.rp_full[i]), kProducerWarps * 32);
-      mbar_init(smem_u32(&m.rp_empty[i]), 1);
+      mbar_init(smem_u32(&m.rp_empty[i]), 2);
     }
     for (int i = 0; i < kInfoDepth; ++i) {
       mbar_init(smem_u32(&m.info_full[i]), 1);
-      mbar_init(smem_u32(&m.info_empty[i]), 5);
+      mbar_init(smem_u32(&m.info_empty[i]), 2 + 4 * L::kGroups);
     }
-    mbar_init(smem_u32(&m.q_full), 1);
+    mbar_init(smem_u32(&m.q_full), L::kGroups);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&m.s_full[i]), 1);
-      mbar_init(smem_u32(&m.p_full[i]), 128);
+      mbar_init(smem_u32(&m.s_full[0][i]), 1);
+      mbar_init(smem_u32(&m.s_full[1][i]), 1);
+      mbar_init(smem_u32(&m.p_full[i]), 128 * L::kGroups);
+      mbar_init(smem_u32(&m.drain[i]), 1);
     }
-    mbar_init(smem_u32(&m.o_full), 1);
-    mbar_init(smem_u32(&m.drain), 1);
+    mbar_init(smem_u32(&m.o_full), 2);
     m.abort_flag = 0;
     m.prior_error = *reinterpret_cast<volatile int*>(&g_device_error);
     fence_mbar_init();
@@ -708,17 +742,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_kernel(const __gri
       // Drain: every copy this thread issued has landed before the CTA can
       // exit, whether or not the consumers got to it.
       asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || warp == kMmaWarpB) {
       if (lane == 0) {
-        if (!run_mma<N>(m, sbase, tmem, deadline)) raise_error(m, kErrMmaWait);
+        const int part = warp == kMmaWarp ? 0 : 1;
+        const bool ok = part == 0 ? run_mma<N, 0>(m, sbase, tmem, deadline) : run_mma<N, 1>(m, sbase, tmem, deadline);
+        if (!ok) raise_error(m, kErrMmaWait);
         // Drain: every MMA this thread issued completes before TMEM is freed.
         const int never = 0;
-        mma_commit(smem_u32(&m.drain));
-        mbar_wait(smem_u32(&m.drain), 0, global_timer_ns() + 100000000ull, &never);
+        mma_commit(smem_u32(&m.drain[part]));
+        mbar_wait(smem_u32(&m.drain[part]), 0, global_timer_ns() + 100000000ull, &never);
       }
       __syncwarp();
     } else {
-      if (!run_softmax<N>(p, m, sbase, tmem, tok, split, h0, hv, deadline)) raise_error(m, kErrSoftmaxWait);
+      const int grp = warp >= softmax_warp0(1) ? 1 : 0;
+      if (!run_softmax<N>(p, m, sbase, tmem, tok, split, h0, hv, grp, deadline)) raise_error(m, kErrSoftmaxWait);
     }
   }
   tc_fence_before();

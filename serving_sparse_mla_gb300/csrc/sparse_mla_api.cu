@@ -83,13 +83,12 @@ int plan_splits(long long n_tok, int h_q, int topk, int sm_count) {
 sparse_mla_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
   const int N = head_width(p.h_q);
   dim3 grid(static_cast<unsigned>(p.n_tok) * static_cast<unsigned>(p.splits), static_cast<unsigned>(head_groups(p.h_q)));
-  dim3 block(smla::kThreads);
   if (N == 16)
-    smla::sparse_mla_fwd_kernel<16><<<grid, block, smla::smem_bytes<16>(), stream>>>(p);
+    smla::sparse_mla_fwd_kernel<16><<<grid, smla::Layout<16>::kThreads, smla::smem_bytes<16>(), stream>>>(p);
   else if (N == 32)
-    smla::sparse_mla_fwd_kernel<32><<<grid, block, smla::smem_bytes<32>(), stream>>>(p);
+    smla::sparse_mla_fwd_kernel<32><<<grid, smla::Layout<32>::kThreads, smla::smem_bytes<32>(), stream>>>(p);
   else
-    smla::sparse_mla_fwd_kernel<64><<<grid, block, smla::smem_bytes<64>(), stream>>>(p);
+    smla::sparse_mla_fwd_kernel<64><<<grid, smla::Layout<64>::kThreads, smla::smem_bytes<64>(), stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
 }
 

@@ -510,15 +510,17 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   const uint32_t rbase = smem_u32(sbase + L::kROff);
 
   // Q rows of this group's heads -> shared memory, K-major with the 128B
-  // swizzle; heads past h_q are zero.
+  // swizzle, by cp.async so all loads are in flight at once; heads past h_q
+  // are zero-filled.
   {
     const __nv_bfloat16* qt = p.q + (static_cast<size_t>(tok) * p.h_q + h0) * kDqk;
     for (int x = tid; x < H * 72; x += 128) {
       const int h = hb + x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (h < hv) v = __ldg(reinterpret_cast<const uint4*>(qt + static_cast<size_t>(h) * kDqk + c * 64 + piece * 8));
-      st_shared_v4(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4), v.x, v.y, v.z, v.w);
+      const bool live = h < hv;
+      const __nv_bfloat16* src = qt + static_cast<size_t>(live ? h : 0) * kDqk + c * 64 + piece * 8;
+      cp_async_16(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4), src, live ? 16u : 0u);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     fence_proxy_async_smem();
     if (tid < H) m.mrun[hb + tid] = -INFINITY;
     named_bar_sync(bar_id, 128);
@@ -654,6 +656,35 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   }
   named_bar_sync(bar_id, 128);
   const int dvrow = q4 * 32 + lane;   // O^T (M=128) lane of this thread
+  if (p.splits > 1) {
+    // fp32 partials: 32 consecutive dv per warp store (128 B), already coalesced.
+#pragma unroll 1
+    for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+      for (int g = 0; g < H / 16; ++g) {
+        float o[16];
+        if (n > 0) {
+          tmem_ld16(tO + mt * N + g * 16, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int h = hb + g * 16 + i;
+          if (h < hv)
+            p.part_o[(static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + h) * kDv + mt * 128 + dvrow] =
+                o[i] * m.fin[h];
+        }
+      }
+    }
+    return true;
+  }
+  // bf16 output: O^T rows (one dv per thread) are transposed through shared
+  // memory -- the value ring is idle once the last P.V has completed -- into
+  // [head][dv] rows, then written with 16-byte coalesced stores.
+  const uint32_t stage = smem_u32(sbase + L::kVOff) + static_cast<uint32_t>(hb) * (kDv * 2);
 #pragma unroll 1
   for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -666,18 +697,25 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 #pragma unroll
         for (int i = 0; i < 16; ++i) o[i] = 0.f;
       }
-      const int dv = mt * 128 + dvrow;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int h = hb + g * 16 + i;
-        if (h < hv) {
-          const float val = o[i] * m.fin[h];
-          if (p.splits > 1)
-            p.part_o[(static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + h) * kDv + dv] = val;
-          else
-            p.out[(tok_h + h) * kDv + dv] = __float2bfloat16_rn(val);
-        }
+        const int hl = g * 16 + i;
+        const __nv_bfloat16 v = __float2bfloat16_rn(o[i] * m.fin[hb + hl]);
+        const uint32_t addr = stage + static_cast<uint32_t>(hl * kDv + mt * 128 + dvrow) * 2u;
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&v))
+                     : "memory");
       }
+    }
+  }
+  named_bar_sync(bar_id, 128);
+  for (int x = tid; x < H * (kDv / 8); x += 128) {
+    const int hl = x / (kDv / 8), c8 = x % (kDv / 8);
+    if (hb + hl < hv) {
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(stage + static_cast<uint32_t>(hl * kDv + c8 * 8) * 2u));
+      *reinterpret_cast<uint4*>(p.out + (tok_h + hb + hl) * kDv + c8 * 8) = v;
     }
   }
   return true;

@@ -38,19 +38,18 @@
 //                      it.  On GB300 this gathers random 1152-B rows ~6x
 //                      faster than TMA tile::gather4 (13.9 vs 2.2 TB/s from
 //                      L2, 5.3 vs 2.2 TB/s from HBM).
-//   warps 4, 9 (MMA)   two threads issue tcgen05.mma (kind::f16, fp32 in TMEM),
-//                      each for half of every block (value pairs 0,1 + rope /
-//                      pairs 2,3 of QK^T into two partial S^T, dv 0..255 /
-//                      256..511 of P.V); one issuer sustains ~59 cycles per
-//                      MMA on GB300, two ~39 in aggregate:
+//   warps 4, 9 and    three threads issue tcgen05.mma (kind::f16, fp32 in
+//   the last warp      TMEM): two split QK^T (value pairs 0,1 + rope / pairs
+//   (MMA)              2,3, into two partial S^T) and one issues P.V as soon as
+//                      P^T is ready; one issuer sustains ~59 cycles per MMA on
+//                      GB300, several more in aggregate:
 //                        S^T[64 x N]   = K_blk[64 x 576] . Q^T[576 x N]   (M=64)
 //                        O^T[512 x N] += V^T[512 x 64]  . P^T[64 x N]    (M=128)
 //                      (swap-AB: kv rows are M and heads are N, so 8 heads
 //                      cost N=16 instead of a 64-row pad).  V^T is the same
-//                      gathered tile read through an MN-major descriptor.  The
-//                      order is QK(0), QK(1), PV(0), QK(2), PV(1), ... with S
-//                      double-buffered, so QK of the next block runs while the
-//                      softmax works on the current one.
+//                      gathered tile read through an MN-major descriptor.  S
+//                      is double-buffered, so QK of the next block runs while
+//                      the softmax works on the current one.
 //   warps 5..8         the M=64 result sits in lanes 32*(i/16) + i%16, so
 //   (+ 10..13 for      lanes 0..15 of each warp own one kv row each; a group
 //   64 heads;          of 4 warps owns up to 32 heads (two groups for 64 heads,
@@ -81,8 +80,9 @@ constexpr int kChunkBytes = kBlk * 128;      // 64 rows x 64 bf16 columns
 constexpr int kPairBytes = 2 * kChunkBytes;  // 64 rows x 128 columns
 constexpr int kInfoDepth = 8;
 constexpr int kProducerWarps = 4;
-constexpr int kMmaWarp = 4;                  // MMA issuer A (also owns the TMEM allocation)
-constexpr int kMmaWarpB = 9;                 // MMA issuer B
+constexpr int kMmaWarp = 4;                  // QK^T issuer, part 0 (also owns the TMEM allocation)
+constexpr int kMmaWarpB = 9;                 // QK^T issuer, part 1
+// P.V issuer: the warp after the softmax groups (10 or 14).
 // Softmax group g (4 warps, one per TMEM lane quarter) owns heads
 // [32 g, 32 g + 32): warps 5..8 for g = 0, warps 10..13 for g = 1.
 __host__ __device__ constexpr int softmax_warp0(int g) { return g == 0 ? 5 : 10; }
@@ -125,19 +125,25 @@ struct Layout {
   static constexpr int kTmemCols = N == 64 ? 512 : (N == 32 ? 256 : 128);
   static constexpr int kGroups = N == 64 ? 2 : 1;                 // softmax groups
   static constexpr int kHG = N / kGroups;                         // heads per group (<= 32)
-  static constexpr int kThreads = (6 + 4 * kGroups) * 32;
+  static constexpr int kPvWarp = 6 + 4 * kGroups;
+  static constexpr int kThreads = (kPvWarp + 1) * 32;
   static constexpr int kQOff = 0;
   static constexpr int kVOff = 9 * N * 128;
   static constexpr int kROff = kVOff + kNV * kPairBytes;
   static constexpr int kMiscOff = kROff + kNR * kChunkBytes;
   static_assert(kBlk * kPRow <= kChunkBytes, "P^T fits in a rope slot");
+  // Block n+2's last value tile reuses a slot that P.V of block n frees, so
+  // the softmax of block n+2 cannot finish before P.V(n) has started; that
+  // keeps every double-buffered phase wait (p_full, s_full) within one phase.
+  static_assert(kNV >= 8 && kNV <= 11, "value ring must span 2 to 2.75 blocks");
+  static_assert(kNR >= 2, "P^T of the next block needs its own rope slot");
 };
 
 struct __align__(16) Misc {
   uint64_t v_full[12], v_empty[12];
   uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
-  uint64_t q_full, s_full[2][2], p_full[2], o_full, drain[2];
+  uint64_t q_full, s_full[2][2], p_full[2], o_full, drain[3];
   int32_t info_blk[kInfoDepth];
   uint32_t info_mask[kInfoDepth][2];
   float red[4][64];
@@ -324,8 +330,11 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int to
       const int r1 = __shfl_sync(0xffffffffu, rows[1], r >> 1);
       myrow[it] = (r & 1) ? r1 : r0;
     }
+    // Tile order: value pairs 0 and 1, the rope tile, pairs 2 and 3 -- the
+    // QK^T part that needs pairs 0,1 and the rope can start after 3 tiles.
 #pragma unroll 1
-    for (int u = 0; u < 5; ++u) {
+    for (int step = 0; step < 5; ++step) {
+      const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
       uint32_t empty, full, par, dst;
       int first_chunk, n_chunks;
       if (u < 4) {
@@ -379,11 +388,13 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int to
 
 // ------------------------------------------------------------------ MMA issuer
 
-// The MMA work of a block is split between two issuing threads (one tcgen05
-// issuer sustains ~59 cycles per MMA here, two ~39 in aggregate):
-//   part 0: QK^T over value pairs 0,1 and the rope columns, P.V for dv 0..255
-//   part 1: QK^T over value pairs 2,3,                   P.V for dv 256..511
-// Each part accumulates its own partial S^T; the softmax adds the two.
+// The MMA work of a block is split between three issuing threads (one
+// tcgen05 issuer sustains ~59 cycles per MMA here, several issuers more in
+// aggregate), each with its own dependencies so none waits behind another:
+//   QK part 0: QK^T over value pairs 0,1 and the rope columns
+//   QK part 1: QK^T over value pairs 2,3
+//   PV:        P.V for all of dv, as soon as the softmax has written P^T
+// Each QK part accumulates its own partial S^T; the softmax adds the two.
 template <int N, int PART>
 __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase, uint32_t rbase, uint32_t tmem,
                                          int n, uint64_t deadline, const volatile int* ab) {
@@ -431,33 +442,7 @@ __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase
 }
 
 template <int N, int PART>
-__device__ __forceinline__ bool issue_pv(Misc& m, uint32_t vbase, uint32_t rbase, uint32_t tmem, int n,
-                                         uint64_t deadline, const volatile int* ab) {
-  using L = Layout<N>;
-  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
-  const uint32_t tO = tmem + 4 * N;
-  if (!mbar_wait(smem_u32(&m.p_full[n & 1]), (n >> 1) & 1, deadline, ab)) return false;
-  tc_fence_after();
-  const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int mt = 2 * PART + i;
-    const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(mt)) % L::kNV;
-#pragma unroll
-    for (int ks = 0; ks < kBlk / 16; ++ks) {
-      const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-      const uint64_t b = smem_desc(rbase + rs * kChunkBytes + ks * 16 * L::kPRow, 16 * L::kPRow * 8,
-                                   8 * L::kPRow, L::kPSwz);
-      mma_bf16_ss(tO + mt * N, a, b, kIdescPV, (n > 0 || ks > 0) ? 1u : 0u);
-    }
-    mma_commit(smem_u32(&m.v_empty[s]));
-  }
-  mma_commit(smem_u32(&m.rp_empty[rs]));   // two arrivals (one per part) release the P^T / rope slot
-  return true;
-}
-
-template <int N, int PART>
-__device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline) {
+__device__ bool run_qk(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline) {
   using L = Layout<N>;
   const volatile int* ab = &m.abort_flag;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
@@ -465,26 +450,53 @@ __device__ bool run_mma(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadlin
   const uint32_t rbase = smem_u32(sbase + L::kROff);
   if (!mbar_wait(smem_u32(&m.q_full), 0, deadline, ab)) return false;
   tc_fence_after();
-  int n = 0;
-  for (;;) {
+  for (int n = 0;; ++n) {
     const int k = n % kInfoDepth;
     if (!mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab)) return false;
     const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
     mbar_arrive(smem_u32(&m.info_empty[k]));
     if (blk < 0) break;
-    // QK of this block goes ahead of PV of the previous one, so the tensor
-    // core has work while the softmax runs.  (S buffer n&1 is free: PV(n-2),
-    // issued before by this thread, waited for the softmax of block n-2.)
+    // S buffer n&1 was last read by the softmax of block n-2.
+    if (n >= 2 && !mbar_wait(smem_u32(&m.p_full[n & 1]), ((n - 2) >> 1) & 1, deadline, ab)) return false;
     if (!issue_qk<N, PART>(m, qbase, vbase, rbase, tmem, n, deadline, ab)) return false;
-    if (n > 0 && !issue_pv<N, PART>(m, vbase, rbase, tmem, n - 1, deadline, ab)) return false;
-    ++n;
   }
-  if (n > 0) {
-    if (!issue_pv<N, PART>(m, vbase, rbase, tmem, n - 1, deadline, ab)) return false;
-    mma_commit(smem_u32(&m.o_full));
-  } else {
-    mbar_arrive(smem_u32(&m.o_full));
+  return true;
+}
+
+template <int N>
+__device__ bool run_pv(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline) {
+  using L = Layout<N>;
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
+  const volatile int* ab = &m.abort_flag;
+  const uint32_t vbase = smem_u32(sbase + L::kVOff);
+  const uint32_t rbase = smem_u32(sbase + L::kROff);
+  const uint32_t tO = tmem + 4 * N;
+  int n = 0;
+  for (;; ++n) {
+    const int k = n % kInfoDepth;
+    if (!mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab)) return false;
+    const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
+    mbar_arrive(smem_u32(&m.info_empty[k]));
+    if (blk < 0) break;
+    if (!mbar_wait(smem_u32(&m.p_full[n & 1]), (n >> 1) & 1, deadline, ab)) return false;
+    tc_fence_after();
+    const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
+#pragma unroll 1
+    for (int mt = 0; mt < 4; ++mt) {
+      const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(mt)) % L::kNV;
+#pragma unroll
+      for (int ks = 0; ks < kBlk / 16; ++ks) {
+        const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
+        const uint64_t b = smem_desc(rbase + rs * kChunkBytes + ks * 16 * L::kPRow, 16 * L::kPRow * 8,
+                                     8 * L::kPRow, L::kPSwz);
+        mma_bf16_ss(tO + mt * N, a, b, kIdescPV, (n > 0 || ks > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&m.v_empty[s]));
+    }
+    mma_commit(smem_u32(&m.rp_empty[rs]));
   }
+  if (n > 0) mma_commit(smem_u32(&m.o_full));
+  else mbar_arrive(smem_u32(&m.o_full));
   return true;
 }
 
@@ -743,20 +755,20 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
     }
     for (int i = 0; i < L::kNR; ++i) {
       mbar_init(smem_u32(&m.rp_full[i]), kProducerWarps * 32);
-      mbar_init(smem_u32(&m.rp_empty[i]), 2);
+      mbar_init(smem_u32(&m.rp_empty[i]), 1);
     }
     for (int i = 0; i < kInfoDepth; ++i) {
       mbar_init(smem_u32(&m.info_full[i]), 1);
-      mbar_init(smem_u32(&m.info_empty[i]), 2 + 4 * L::kGroups);
+      mbar_init(smem_u32(&m.info_empty[i]), 3 + 4 * L::kGroups);
     }
     mbar_init(smem_u32(&m.q_full), L::kGroups);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&m.s_full[0][i]), 1);
       mbar_init(smem_u32(&m.s_full[1][i]), 1);
       mbar_init(smem_u32(&m.p_full[i]), 128 * L::kGroups);
-      mbar_init(smem_u32(&m.drain[i]), 1);
     }
-    mbar_init(smem_u32(&m.o_full), 2);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&m.drain[i]), 1);
+    mbar_init(smem_u32(&m.o_full), 1);
     m.abort_flag = 0;
     m.prior_error = *reinterpret_cast<volatile int*>(&g_device_error);
     fence_mbar_init();
@@ -780,15 +792,17 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
       // Drain: every copy this thread issued has landed before the CTA can
       // exit, whether or not the consumers got to it.
       asm volatile("cp.async.wait_all;" ::: "memory");
-    } else if (warp == kMmaWarp || warp == kMmaWarpB) {
+    } else if (warp == kMmaWarp || warp == kMmaWarpB || warp == L::kPvWarp) {
       if (lane == 0) {
-        const int part = warp == kMmaWarp ? 0 : 1;
-        const bool ok = part == 0 ? run_mma<N, 0>(m, sbase, tmem, deadline) : run_mma<N, 1>(m, sbase, tmem, deadline);
+        const int role = warp == kMmaWarp ? 0 : (warp == kMmaWarpB ? 1 : 2);
+        const bool ok = role == 0 ? run_qk<N, 0>(m, sbase, tmem, deadline)
+                                  : (role == 1 ? run_qk<N, 1>(m, sbase, tmem, deadline)
+                                               : run_pv<N>(m, sbase, tmem, deadline));
         if (!ok) raise_error(m, kErrMmaWait);
         // Drain: every MMA this thread issued completes before TMEM is freed.
         const int never = 0;
-        mma_commit(smem_u32(&m.drain[part]));
-        mbar_wait(smem_u32(&m.drain[part]), 0, global_timer_ns() + 100000000ull, &never);
+        mma_commit(smem_u32(&m.drain[role]));
+        mbar_wait(smem_u32(&m.drain[role]), 0, global_timer_ns() + 100000000ull, &never);
       }
       __syncwarp();
     } else {

@@ -67,17 +67,26 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int head_width(int h_q) { return h_q <= 16 ? 16 : (h_q <= 32 ? 32 : 64); }
 int head_groups(int h_q) { return (h_q + 63) / 64; }
 
-// Number of top-k splits per token: enough CTAs for two per SM, never more
-// than the number of 128-entry blocks.
+// Number of top-k splits per token (decode).  One CTA runs per SM, so the
+// time is about (waves of CTAs) x (blocks per split + per-CTA start-up and
+// tail, ~1.5 blocks); pick the split count that minimises it, never more
+// than the number of blocks or 32.
 int plan_splits(long long n_tok, int h_q, int topk, int sm_count) {
   const long long units = n_tok * head_groups(h_q);
   const int nb = (topk + smla::kBlk - 1) / smla::kBlk;
-  if (units <= 0) return 1;
-  long long s = (2LL * sm_count + units - 1) / units;
-  if (s < 1) s = 1;
-  if (s > nb) s = nb;
-  if (s > 32) s = 32;
-  return static_cast<int>(s);
+  if (units <= 0 || sm_count <= 0) return 1;
+  int best = 1;
+  double best_cost = 0.0;
+  for (int s = 1; s <= nb && s <= 32; ++s) {
+    const long long ctas = units * s;
+    const long long waves = (ctas + sm_count - 1) / sm_count;
+    const double cost = static_cast<double>(waves) * (static_cast<double>((nb + s - 1) / s) + 1.5);
+    if (s == 1 || cost < best_cost - 1e-9) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 sparse_mla_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {

@@ -248,6 +248,38 @@ __device__ __forceinline__ void warp_xreduce(float (&v)[N], int lane, float* dst
     if (i < cnt) dst[base + i] = v[i];
 }
 
+// The same butterfly within each 16-lane half of the warp (the halves hold
+// different heads of the same rows); dst is the half's first head.
+template <int V, bool kMax>
+__device__ __forceinline__ void half_xreduce(float (&v)[V], int lane, float* dst) {
+  int cnt = V;
+  int base = 0;
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) {
+    if (cnt > 1) {
+      const int half = cnt >> 1;
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < V / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+          v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+      }
+      if (upper) base += half;
+      cnt = half;
+    } else {
+      const float recv = __shfl_xor_sync(0xffffffffu, v[0], off);
+      v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+    if (i < cnt) dst[base + i] = v[i];
+}
+
 // bar.sync over the 128 threads of one softmax group (named barrier `id`),
 // returning the OR of `pred`.
 __device__ __forceinline__ bool bar_red_or_128(uint32_t id, bool pred) {
@@ -502,6 +534,14 @@ __device__ bool run_pv(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline
 
 // ------------------------------------------------------------------ softmax + epilogue
 
+// S^T row of this thread's half: HH consecutive heads starting at the
+// half's first head (16x32bx2 read, upper half offset by HH columns).
+template <int HH>
+__device__ __forceinline__ void load_s_half(uint32_t taddr, float* v) {
+  if constexpr (HH == 16) tmem_ld16x2_x16<16>(taddr, v);
+  else tmem_ld16x2_x8<8>(taddr, v);
+}
+
 template <int N>
 __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int tok, int split, int h0,
                             int hv, int grp, uint64_t deadline) {
@@ -514,8 +554,12 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   const int tid = static_cast<int>(threadIdx.x) - softmax_warp0(grp) * 32;  // 0..127 within the group
   const int hb = grp * H;                              // first head of the group
   const int q4 = warp & 3;                             // TMEM lane quarter of this warp
-  const bool has_row = lane < 16;                      // M=64 result: 16 lanes per quarter
-  const int row = q4 * 16 + (lane & 15);               // kv row of the block (when has_row)
+  // The M=64 result sits in 16 lanes per quarter: both half-warps work on
+  // the same 16 rows, the lower half on heads [hb, hb+H/2), the upper half on
+  // [hb+H/2, hb+H).
+  constexpr int HH = H / 2;
+  const int hsub = (lane >> 4) * HH;                   // first head of this half, within the group
+  const int row = q4 * 16 + (lane & 15);               // kv row of the block
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
   const uint32_t tO = tmem + lane_off + 4 * N + hb;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
@@ -554,25 +598,22 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
     if (blk < 0) break;
-    const bool valid = has_row && ((bits >> (row >> 1)) & 1u) != 0u;
+    const bool valid = ((bits >> (row >> 1)) & 1u) != 0u;
     const uint32_t tSa = tmem + lane_off + static_cast<uint32_t>(n & 1) * N + hb;        // part 0
     const uint32_t tSb = tmem + lane_off + static_cast<uint32_t>(2 + (n & 1)) * N + hb;  // part 1
 
     const bool sok = mbar_wait(smem_u32(&m.s_full[0][n & 1]), (n >> 1) & 1, deadline, ab) &&
                      mbar_wait(smem_u32(&m.s_full[1][n & 1]), (n >> 1) & 1, deadline, ab);
     tc_fence_after();
-    // Block max per head: butterfly over the warp, then over the 4 warps.
+    // Block max per head: butterfly over the half-warp, then over the 4 warps.
     {
-      float s[H], t[H];
-#pragma unroll
-      for (int g = 0; g < H / 16; ++g) {
-        tmem_ld16(tSa + g * 16, s + g * 16);
-        tmem_ld16(tSb + g * 16, t + g * 16);
-      }
+      float s[HH], t[HH];
+      load_s_half<HH>(tSa, s);
+      load_s_half<HH>(tSb, t);
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < H; ++i) s[i] = valid ? (s[i] + t[i]) * p.scale_log2 : -INFINITY;
-      warp_xreduce<H, true>(s, lane, m.red[q4] + hb);
+      for (int i = 0; i < HH; ++i) s[i] = valid ? (s[i] + t[i]) * p.scale_log2 : -INFINITY;
+      half_xreduce<HH, true>(s, lane, m.red[q4] + hb + hsub);
     }
     if (bar_red_or_128(bar_id, !sok)) return false;
     bool grew = false;
@@ -616,28 +657,23 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     {
       const uint32_t prow = rbase + (n % L::kNR) * kChunkBytes + row * L::kPRow;
       const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
-      float s[H], t[H];
-#pragma unroll
-      for (int g = 0; g < H / 16; ++g) {
-        tmem_ld16(tSa + g * 16, s + g * 16);
-        tmem_ld16(tSb + g * 16, t + g * 16);
-      }
+      float s[HH], t[HH];
+      load_s_half<HH>(tSa, s);
+      load_s_half<HH>(tSb, t);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < H / 8; ++c) {
+      for (int c = 0; c < HH / 8; ++c) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int h = hb + c * 8 + i;
+          const int h = hb + hsub + c * 8 + i;
           s[c * 8 + i] = valid ? fast_exp2((s[c * 8 + i] + t[c * 8 + i]) * p.scale_log2 - m.mrun[h]) : 0.f;
         }
-        if (has_row) {
-          const uint32_t chunk = static_cast<uint32_t>(hb / 8 + c);
-          st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
-                       pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
-                       pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
-        }
+        const uint32_t chunk = static_cast<uint32_t>((hb + hsub) / 8 + c);
+        st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
+                     pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
+                     pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
       }
-      warp_xreduce<H, false>(s, lane, m.rsum[q4] + hb);
+      half_xreduce<HH, false>(s, lane, m.rsum[q4] + hb + hsub);
     }
     fence_proxy_async_smem();
     tc_fence_before();

@@ -143,9 +143,10 @@ struct __align__(16) Misc {
   uint64_t v_full[12], v_empty[12];
   uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
-  uint64_t q_full, s_full[2][2], p_full[2], o_full, drain[3];
+  uint64_t q_full, s_full[2][2], p_full[2], o_full, drain[3], cand_full;
   int32_t info_blk[kInfoDepth];
   uint32_t info_mask[kInfoDepth][2];
+  uint32_t cand[2][kProducerWarps];
   float red[4][64];
   float rsum[4][64];
   float mrun[64];
@@ -321,90 +322,190 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int to
   // Every warp maps the whole block (entries 2*lane, 2*lane+1) so all agree
   // on the skip decision and on ring positions without a barrier; each warp
   // then copies its own 16 rows of every tile.
-  int idx_next[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int e = jb * kBlk + lane * 2 + i;
-    idx_next[i] = (jb < je && e < p.topk) ? __ldg(irow + e) : -1;
-  }
   int n = 0;
-  for (int j = jb; j < je; ++j) {
-    int rows[2];
+  int win = 0;
+  for (int wb = jb; wb < je; wb += 32, ++win) {
+    // Candidate blocks of this window of up to 32: a block none of whose
+    // entries lies in [0, kv_len) is skipped without mapping its rows (a
+    // causal list is mostly -1 padding for early tokens).  Each warp scans 8
+    // blocks with 16 coalesced loads in flight per lane; the four masks meet
+    // in shared memory.  The loads also bring the list into L1 for the row
+    // mapping below.
+    const int we = min(je, wb + 32);
+    uint32_t cand;
+    {
+      const int b0 = wb + warp * 8;
+      int v[16];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) rows[i] = map_entry(p, ctx, idx_next[i]);
+      for (int i = 0; i < 16; ++i) {
+        const int blk = b0 + (i >> 1);
+        const int e = blk * kBlk + (i & 1) * 32 + lane;
+        v[i] = (blk < we && e < p.topk) ? __ldg(irow + e) : -1;
+      }
+      uint32_t bits = 0;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {   // prefetch the next block's indices
-      const int e = (j + 1) * kBlk + lane * 2 + i;
-      idx_next[i] = (j + 1 < je && e < p.topk) ? __ldg(irow + e) : -1;
-    }
-    const uint32_t bal0 = __ballot_sync(0xffffffffu, rows[0] >= 0);
-    const uint32_t bal1 = __ballot_sync(0xffffffffu, rows[1] >= 0);
-    if ((bal0 | bal1) == 0u) continue;
-
-    if (warp == 0) {
-      const int k = n % kInfoDepth;
-      const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
-      if (!__all_sync(0xffffffffu, ok)) return false;
+      for (int i = 0; i < 16; i += 2) {
+        const bool c = (v[i] >= 0 && v[i] < ctx.kv_len) || (v[i + 1] >= 0 && v[i + 1] < ctx.kv_len);
+        if (__ballot_sync(0xffffffffu, c) != 0u) bits |= 1u << (i >> 1);
+      }
       if (lane == 0) {
-        m.info_blk[k] = j;
-        m.info_mask[k][0] = bal0;
-        m.info_mask[k][1] = bal1;
-        mbar_arrive(smem_u32(&m.info_full[k]));
+        m.cand[win & 1][warp] = bits << (warp * 8);
+        mbar_arrive(smem_u32(&m.cand_full));
       }
-    }
-    // This warp copies block rows 16*warp + 4*it + sel; entry r of the block
-    // sits in lane r / 2 as rows[r % 2].
-    int myrow[4];
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int r = warp * 16 + it * 4 + sel;
-      const int r0 = __shfl_sync(0xffffffffu, rows[0], r >> 1);
-      const int r1 = __shfl_sync(0xffffffffu, rows[1], r >> 1);
-      myrow[it] = (r & 1) ? r1 : r0;
-    }
-    // Tile order: value pairs 0 and 1, the rope tile, pairs 2 and 3 -- the
-    // QK^T part that needs pairs 0,1 and the rope can start after 3 tiles.
-#pragma unroll 1
-    for (int step = 0; step < 5; ++step) {
-      const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
-      uint32_t empty, full, par, dst;
-      int first_chunk, n_chunks;
-      if (u < 4) {
-        const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
-        const uint32_t s = vi % L::kNV;
-        empty = smem_u32(&m.v_empty[s]);
-        full = smem_u32(&m.v_full[s]);
-        par = (vi / L::kNV) & 1u;
-        dst = vbase + s * kPairBytes;
-        first_chunk = 2 * u;
-        n_chunks = 2;
-      } else {
-        const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
-        empty = smem_u32(&m.rp_empty[rs]);
-        full = smem_u32(&m.rp_full[rs]);
-        par = (static_cast<uint32_t>(n) / L::kNR) & 1u;
-        dst = rbase + rs * kChunkBytes;
-        first_chunk = 8;
-        n_chunks = 1;
-      }
-      const bool ok = mbar_wait(empty, par ^ 1u, deadline, ab);
+      const bool ok = mbar_wait(smem_u32(&m.cand_full), static_cast<uint32_t>(win) & 1u, deadline, ab);
       if (!__all_sync(0xffffffffu, ok)) return false;
-      for (int c = 0; c < n_chunks; ++c) {
+      cand = 0;
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int r = warp * 16 + it * 4 + sel;
-          const int src_row = myrow[it];
-          const __nv_bfloat16* src =
-              p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
-          cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
+      for (int w = 0; w < kProducerWarps; ++w) cand |= *reinterpret_cast<volatile uint32_t*>(&m.cand[win & 1][w]);
+    }
+    int j_next = cand != 0u ? wb + __ffs(static_cast<int>(cand)) - 1 : -1;
+    int idx_next[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = j_next * kBlk + lane * 2 + i;
+      idx_next[i] = (j_next >= 0 && e < p.topk) ? __ldg(irow + e) : -1;
+    }
+    while (j_next >= 0) {
+      const int j = j_next;
+      cand &= cand - 1u;
+      j_next = cand != 0u ? wb + __ffs(static_cast<int>(cand)) - 1 : -1;
+      int rows[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) rows[i] = map_entry(p, ctx, idx_next[i]);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {   // prefetch the next candidate's indices
+        const int e = j_next * kBlk + lane * 2 + i;
+        idx_next[i] = (j_next >= 0 && e < p.topk) ? __ldg(irow + e) : -1;
+      }
+      const uint32_t bal0 = __ballot_sync(0xffffffffu, rows[0] >= 0);
+      const uint32_t bal1 = __ballot_sync(0xffffffffu, rows[1] >= 0);
+      if ((bal0 | bal1) == 0u) continue;
+
+      if (warp == 0) {
+        const int k = n % kInfoDepth;
+        const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        if (lane == 0) {
+          m.info_blk[k] = j;
+          m.info_mask[k][0] = bal0;
+          m.info_mask[k][1] = bal1;
+          mbar_arrive(smem_u32(&m.info_full[k]));
         }
       }
-      // The hardware arrives on the tile's full barrier for this thread once
-      // all of this thread's copies so far have landed; the thread itself
-      // never waits on them.
-      cp_async_arrive_on(full);
+      // This warp copies block rows 16*warp + 4*it + sel; entry r of the block
+      // sits in lane r / 2 as rows[r % 2].
+      int myrow[4];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int r = warp * 16 + it * 4 + sel;
+        const int r0 = __shfl_sync(0xffffffffu, rows[0], r >> 1);
+        const int r1 = __shfl_sync(0xffffffffu, rows[1], r >> 1);
+        myrow[it] = (r & 1) ? r1 : r0;
+      }
+      // Tile order: value pairs 0 and 1, the rope tile, pairs 2 and 3 -- the
+      // QK^T part that needs pairs 0,1 and the rope can start after 3 tiles.
+      auto tile = [&](int step, uint32_t& empty, uint32_t& full, uint32_t& par, uint32_t& dst, int& first_chunk,
+                      int& n_chunks) {
+        const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
+        if (u < 4) {
+          const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+          const uint32_t s = vi % L::kNV;
+          empty = smem_u32(&m.v_empty[s]);
+          full = smem_u32(&m.v_full[s]);
+          par = (vi / L::kNV) & 1u;
+          dst = vbase + s * kPairBytes;
+          first_chunk = 2 * u;
+          n_chunks = 2;
+        } else {
+          const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
+          empty = smem_u32(&m.rp_empty[rs]);
+          full = smem_u32(&m.rp_full[rs]);
+          par = (static_cast<uint32_t>(n) / L::kNR) & 1u;
+          dst = rbase + rs * kChunkBytes;
+          first_chunk = 8;
+          n_chunks = 1;
+        }
+      };
+      // A barrier test sits in the memory pipe behind this warp's earlier
+      // copies, so every wait costs about one drain of that queue.  With a
+      // ring deeper than two blocks (N <= 32) the slots of a block are usually
+      // all free already: test them together and issue every free tile back
+      // to back, blocking only when none is free.  With the two-block ring of
+      // N = 64 the slots free one by one behind P.V; there, waiting for each
+      // tile in turn measures faster.
+      if constexpr (N != 64) {
+        uint32_t done = 0;
+        while (done != 0x1fu) {
+          uint32_t ready = 0;
+#pragma unroll
+          for (int step = 0; step < 5; ++step) {
+            if (!((done >> step) & 1u)) {
+              uint32_t empty, full, par, dst;
+              int fc, nc;
+              tile(step, empty, full, par, dst, fc, nc);
+              if (mbar_test_wait(empty, par ^ 1u)) ready |= 1u << step;
+            }
+          }
+          ready = __shfl_sync(0xffffffffu, ready, 0);
+          if (ready == 0u) {
+            const int step = __ffs(static_cast<int>(~done & 0x1fu)) - 1;
+            uint32_t empty, full, par, dst;
+            int fc, nc;
+            tile(step, empty, full, par, dst, fc, nc);
+            const bool ok = mbar_wait(empty, par ^ 1u, deadline, ab);
+            if (!__all_sync(0xffffffffu, ok)) return false;
+            ready = 1u << step;
+          }
+#pragma unroll
+          for (int step = 0; step < 5; ++step) {
+            if ((ready >> step) & 1u) {
+              uint32_t empty, full, par, dst;
+              int first_chunk, n_chunks;
+              tile(step, empty, full, par, dst, first_chunk, n_chunks);
+            for (int c = 0; c < n_chunks; ++c) {
+#pragma unroll
+              for (int it = 0; it < 4; ++it) {
+                const int r = warp * 16 + it * 4 + sel;
+                const int src_row = myrow[it];
+                const __nv_bfloat16* src =
+                    p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
+                cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
+              }
+            }
+            // The hardware arrives on the tile's full barrier for this thread
+            // once all of this thread's copies so far have landed; the thread
+            // itself never waits on them.
+            cp_async_arrive_on(full);
+            }
+          }
+          done |= ready;
+        }
+      } else {
+#pragma unroll 1
+        for (int step = 0; step < 5; ++step) {
+          uint32_t empty, full, par, dst;
+          int first_chunk, n_chunks;
+          tile(step, empty, full, par, dst, first_chunk, n_chunks);
+          const bool ok = mbar_wait(empty, par ^ 1u, deadline, ab);
+          if (!__all_sync(0xffffffffu, ok)) return false;
+          for (int c = 0; c < n_chunks; ++c) {
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+              const int r = warp * 16 + it * 4 + sel;
+              const int src_row = myrow[it];
+              const __nv_bfloat16* src =
+                  p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
+              cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
+            }
+          }
+          // The hardware arrives on the tile's full barrier for this thread
+          // once all of this thread's copies so far have landed; the thread
+          // itself never waits on them.
+          cp_async_arrive_on(full);
+        }
+      }
+      ++n;
     }
-    ++n;
   }
   if (warp == 0) {
     const int k = n % kInfoDepth;
@@ -704,8 +805,14 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   }
   named_bar_sync(bar_id, 128);
   const int dvrow = q4 * 32 + lane;   // O^T (M=128) lane of this thread
+  // The group's normalisers in registers: read once here, not after every
+  // store (which the compiler must assume may alias them).
+  float fin[H];
+#pragma unroll
+  for (int i = 0; i < H; ++i) fin[i] = m.fin[hb + i];
   if (p.splits > 1) {
     // fp32 partials: 32 consecutive dv per warp store (128 B), already coalesced.
+    float* dst = p.part_o + (static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + hb) * kDv + dvrow;
 #pragma unroll 1
     for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -720,10 +827,8 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int h = hb + g * 16 + i;
-          if (h < hv)
-            p.part_o[(static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + h) * kDv + mt * 128 + dvrow] =
-                o[i] * m.fin[h];
+          const int hl = g * 16 + i;
+          if (hb + hl < hv) dst[static_cast<size_t>(hl) * kDv + mt * 128] = o[i] * fin[hl];
         }
       }
     }
@@ -748,22 +853,32 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int hl = g * 16 + i;
-        const __nv_bfloat16 v = __float2bfloat16_rn(o[i] * m.fin[hb + hl]);
+        const __nv_bfloat16 v = __float2bfloat16_rn(o[i] * fin[hl]);
         const uint32_t addr = stage + static_cast<uint32_t>(hl * kDv + mt * 128 + dvrow) * 2u;
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&v))
-                     : "memory");
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&v)));
       }
     }
   }
   named_bar_sync(bar_id, 128);
-  for (int x = tid; x < H * (kDv / 8); x += 128) {
-    const int hl = x / (kDv / 8), c8 = x % (kDv / 8);
-    if (hb + hl < hv) {
-      uint4 v;
+  // Rows of 512 dv, 16 bytes per thread: four shared loads in flight, then
+  // four global stores.
+  constexpr int kRounds = H * (kDv / 8) / 128;
+  static_assert(kRounds % 4 == 0, "store rounds");
+#pragma unroll 1
+  for (int r0 = 0; r0 < kRounds; r0 += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = tid + (r0 + j) * 128;
       asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                   : "r"(stage + static_cast<uint32_t>(hl * kDv + c8 * 8) * 2u));
-      *reinterpret_cast<uint4*>(p.out + (tok_h + hb + hl) * kDv + c8 * 8) = v;
+                   : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
+                   : "r"(stage + static_cast<uint32_t>(x) * 16u));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = tid + (r0 + j) * 128;
+      const int hl = x / (kDv / 8), c8 = x % (kDv / 8);
+      if (hb + hl < hv) *reinterpret_cast<uint4*>(p.out + (tok_h + hb + hl) * kDv + c8 * 8) = v[j];
     }
   }
   return true;
@@ -804,6 +919,7 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
       mbar_init(smem_u32(&m.p_full[i]), 128 * L::kGroups);
     }
     for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&m.drain[i]), 1);
+    mbar_init(smem_u32(&m.cand_full), kProducerWarps);
     mbar_init(smem_u32(&m.o_full), 1);
     m.abort_flag = 0;
     m.prior_error = *reinterpret_cast<volatile int*>(&g_device_error);

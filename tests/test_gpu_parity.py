@@ -90,6 +90,28 @@ def test_masking_edge_cases(smla):
     assert np.array_equal(o[1], np.broadcast_to(case.kv[7, :512].float().numpy(), o[1].shape))
 
 
+def test_long_lists_span_several_windows(smla):
+    """top-k lists longer than 32 blocks of 64 (the producer scans them 32
+    blocks at a time), a ragged last block, and lists whose only valid
+    entries sit late: in the second window, or in one block after -1s."""
+    s_q, s_kv, topk = 24, 6000, 3100
+    case = mi.prefill_case(404, s_q=s_q, s_kv=s_kv, h_q=8, topk=topk)
+    idx = case.indices.clone()
+    g = torch.Generator().manual_seed(405)
+    idx[0, :] = -1
+    idx[0, 3000:3003] = torch.tensor([5, 4000, 5999], dtype=torch.int32)   # second window, ragged block
+    idx[1, :2500] = -1                                                        # first window empty
+    idx[1, 2500:] = torch.randint(0, s_kv, (topk - 2500,), generator=g, dtype=torch.int32)
+    idx[2, :] = -1
+    idx[2, 1500:1564] = torch.randint(0, s_kv, (64,), generator=g, dtype=torch.int32)  # one block, mid window
+    idx[3, :] = torch.randint(0, s_kv, (topk,), generator=g, dtype=torch.int32)        # every block valid
+    idx[3, 64:2048] = -1
+    kv = mi.poison_unreferenced(case.kv, torch.unique(idx[(idx >= 0) & (idx < s_kv)]))
+    o, l = _run_fwd(smla, case, kv, idx)
+    ref_o, ref_l = orc.sparse_mla_fwd(case.q, kv, idx, case.sm_scale)
+    compare(o, l, ref_o, ref_l, "long lists")
+
+
 def test_s_kv_zero_and_empty_batch(smla):
     q = torch.randn(3, 8, 576, device=DEV).to(torch.bfloat16)
     kv = torch.empty(0, 576, device=DEV, dtype=torch.bfloat16)

@@ -47,7 +47,7 @@ KV_ROW_BYTES = 576 * 2
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
@@ -91,8 +91,90 @@ def profiled_traffic(config: int):
         return None
 
 
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons of this process's GPU, read
+    through NVML (read-only queries) every ~2 ms by a thread that samples only
+    while the timed region runs.  The NVML device is found by PCI bus id, so
+    CUDA_VISIBLE_DEVICES remapping does not matter."""
+    NVML_CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device):
+        import ctypes
+        import threading
+        import torch
+        self.ok = False
+        self.samples = []
+        self._run = threading.Event()
+        self._stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            pr = torch.cuda.get_device_properties(device)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                uuid = f"GPU-{pr.uuid}".encode()
+                if lib.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid), ctypes.byref(h)) != 0:
+                    return
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) != 0:
+                return
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            return
+        self.lib, self.h, self.max_mhz, self.reasons_fn = lib, h, mx.value, reasons_fn
+        self.ctypes = ctypes
+        self.ok = True
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        c = self.ctypes
+        clk, mw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, c.byref(clk)) != 0:
+            return None
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw))
+        self.reasons_fn(self.h, c.byref(rs))
+        return clk.value, mw.value / 1000.0, rs.value
+
+    def _loop(self):
+        while not self._stop.is_set():
+            if not self._run.wait(timeout=0.05):
+                continue
+            r = self._read()
+            if r is not None and self._run.is_set():
+                self.samples.append(r)
+            time.sleep(0.002)
+
+    def start(self):
+        if self.ok:
+            self._run.set()
+
+    def stop(self):
+        if not self.ok:
+            return None
+        self._run.clear()
+        self._stop.set()
+        self.thread.join(timeout=2)
+        if not self.samples:
+            return None
+        reasons = set()
+        for _, _, bits in self.samples:
+            for b, name in self.REASONS.items():
+                if bits & b:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[0] for x in self.samples), "sm_max_mhz": self.max_mhz,
+                "power_w_median": round(statistics.median(x[1] for x in self.samples), 1),
+                "samples": len(self.samples), "source": "nvml, 2 ms", "reasons": sorted(reasons)}
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks / throttle reasons every 200 ms into a CSV beside the
+    run (a record of the whole run; the NVML sampler covers the timed region)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -140,7 +222,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "source": "nvidia-smi, 200 ms", "reasons": sorted(reasons)}
 
 
 def max_over_ranks(vals, dist, device=None):
@@ -353,13 +435,17 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(local)
+    nvml = NvmlClockSampler(dev)
+    sampler.start()
     barrier()
     torch.cuda.synchronize(dev)
-    sampler.start()
+    nvml.start()
     times = timed_loop(args.steps, lambda: call(inputs))
     torch.cuda.synchronize(dev)
+    nvml_clocks = nvml.stop()
     barrier()
-    clocks = sampler.stop()
+    smi_clocks = sampler.stop()
+    clocks = nvml_clocks or smi_clocks
     # secondary: warm L2 (the pages' method has no flush)
     warm = timed_loop(max(args.steps, 20), lambda: call(inputs), flush_l2=False)
 

@@ -971,39 +971,64 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
 // ------------------------------------------------------------------ helper kernels
 
 // Merge per-split partial results: LSE = ln sum_s exp(LSE_s),
-// out = sum_s exp(LSE_s - LSE) * O_s (each O_s already normalised).
-__global__ void __launch_bounds__(128) combine_splits_kernel(const float* __restrict__ part_o,
-                                                             const float* __restrict__ part_lse,
-                                                             __nv_bfloat16* __restrict__ out,
-                                                             float* __restrict__ lse, int n_rows_th,
-                                                             int splits) {
-  const int th = static_cast<int>(blockIdx.x);
-  if (th >= n_rows_th) return;
+// out = sum_s exp(LSE_s - LSE) * O_s (each O_s already normalised over its
+// split; the LSE merge of the TileLang page's split-KV decode).  One warp per
+// (token, head) row: lane s holds split s's LSE (splits <= 32), and every lane
+// owns the float4 columns lane + 32 k of the 512-wide row, so each load
+// instruction reads 512 contiguous bytes.  The sums run over s in order, so
+// the result does not depend on the launch shape.
+constexpr int kCombineRows = 8;   // rows (warps) per 256-thread block
+__global__ void __launch_bounds__(32 * kCombineRows) combine_splits_kernel(const float* __restrict__ part_o,
+                                                                          const float* __restrict__ part_lse,
+                                                                          __nv_bfloat16* __restrict__ out,
+                                                                          float* __restrict__ lse, int n_rows_th,
+                                                                          int splits) {
+  const int row = static_cast<int>(blockIdx.x) * kCombineRows + static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  if (row >= n_rows_th) return;
+  constexpr int kF4 = kDv / 4;                                   // float4 per row
+  const float4* src = reinterpret_cast<const float4*>(part_o) + static_cast<size_t>(row) * kF4 + lane;
+  const size_t split_stride = static_cast<size_t>(n_rows_th) * kF4;
+  // Split 0's partial is read while the LSEs arrive (one round trip saved).
+  float4 v0[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v0[k] = __ldcg(src + 32 * k);
+  const float my_ls = lane < splits ? __ldcg(part_lse + static_cast<size_t>(lane) * n_rows_th + row) : -INFINITY;
   float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[static_cast<size_t>(s) * n_rows_th + th]);
-  const int d = static_cast<int>(threadIdx.x) * 4;
+  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, __shfl_sync(0xffffffffu, my_ls, s));
+  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(row) * kDv) + 2 * lane;
   if (mx == -INFINITY) {
-    if (threadIdx.x == 0) lse[th] = -INFINITY;
-    __nv_bfloat162 z = __floats2bfloat162_rn(0.f, 0.f);
-    reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(th) * kDv + d)[0] = z;
-    reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(th) * kDv + d)[1] = z;
+    if (lane == 0) lse[row] = -INFINITY;
+    const __nv_bfloat162 z = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      o2[64 * k] = z;
+      o2[64 * k + 1] = z;
+    }
     return;
   }
   float sum = 0.f;
-  for (int s = 0; s < splits; ++s) sum += expf(part_lse[static_cast<size_t>(s) * n_rows_th + th] - mx);
+  for (int s = 0; s < splits; ++s) sum += expf(__shfl_sync(0xffffffffu, my_ls, s) - mx);
   const float tot = mx + logf(sum);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s = 0; s < splits; ++s) {
-    const float ls = part_lse[static_cast<size_t>(s) * n_rows_th + th];
+    const float ls = __shfl_sync(0xffffffffu, my_ls, s);
     if (ls == -INFINITY) continue;
     const float w = expf(ls - tot);
-    const float4 v = *reinterpret_cast<const float4*>(part_o + (static_cast<size_t>(s) * n_rows_th + th) * kDv + d);
-    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v = s == 0 ? v0[k] : __ldcg(src + s * split_stride + 32 * k);
+      acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
+    }
   }
-  if (threadIdx.x == 0) lse[th] = tot;
-  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(th) * kDv + d);
-  o2[0] = __floats2bfloat162_rn(acc.x, acc.y);
-  o2[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  if (lane == 0) lse[row] = tot;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    o2[64 * k] = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+    o2[64 * k + 1] = __floats2bfloat162_rn(acc[k].z, acc[k].w);
+  }
 }
 
 // Every entry masked (no KV rows at all): out = 0, LSE = -inf.

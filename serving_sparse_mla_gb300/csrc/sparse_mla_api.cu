@@ -243,8 +243,9 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
   if ((st = launch_fwd(p, cs)) != SPARSE_MLA_OK) return st;
   if (splits > 1) {
     const int n_th = static_cast<int>(n_tok * h_q);
-    smla::combine_splits_kernel<<<n_th, 128, 0, cs>>>(p.part_o, p.part_lse, static_cast<__nv_bfloat16*>(out), lse,
-                                                      n_th, splits);
+    const int blocks = (n_th + smla::kCombineRows - 1) / smla::kCombineRows;
+    smla::combine_splits_kernel<<<blocks, 32 * smla::kCombineRows, 0, cs>>>(
+        p.part_o, p.part_lse, static_cast<__nv_bfloat16*>(out), lse, n_th, splits);
     if (cudaGetLastError() != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
   }
   return SPARSE_MLA_OK;

@@ -196,6 +196,27 @@ def test_decode_page16_wide_heads(smla):
     _check_decode(smla, case)
 
 
+def test_decode_dirty_workspace(smla):
+    """The workspace arrives with arbitrary contents (here every byte 0xFF):
+    a call may read nothing from it that it did not write itself.  Run twice
+    on the same buffer."""
+    case = mi.decode_case(603, batch=16, s_next=6, h_q=8, lo=4096, hi=9000, topk=2048, spare_pages=4)
+    need = smla.decode_workspace_size(case.batch, case.s_next, case.h_q, case.indices.shape[-1])
+    assert need > 0, "this shape is expected to split the top-k list"
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)
+    d = lambda t: t.to(DEV)
+    args = (d(case.q), d(case.kv_cache), d(case.block_table), d(case.cache_seqlens), d(case.indices),
+            case.sm_scale, case.page_size)
+    ref_o, ref_l = orc.sparse_mla_decode(case.q, case.kv_cache, case.block_table, case.cache_seqlens,
+                                         case.indices, case.sm_scale, case.page_size)
+    for _ in range(2):
+        out, lse = smla.sparse_mla_decode(*args, workspace=ws)
+        torch.cuda.synchronize()
+        o = out.float().cpu().numpy().reshape(-1, case.h_q, 512)
+        l = lse.cpu().numpy().reshape(-1, case.h_q)
+        compare(o, l, ref_o, ref_l, "dirty workspace")
+
+
 def test_decode_config_all_tokens(smla):
     """batch 16 x 6 MTP tokens, contexts U[4096, 32768], 64-token pages in a
     shuffled pool with every unread slot NaN, h = 8, topk = 2048."""

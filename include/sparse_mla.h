@@ -191,8 +191,11 @@ sparse_mla_status_t sparse_mla_get_device_error(int* code);
 sparse_mla_status_t sparse_mla_clear_device_error(void);
 
 /*
- * Set the bound on every device-side wait, in nanoseconds, for launches made
- * after the call (process-wide; default 1 s; 0 restores the default).
+ * Set the bound on device-side waits, in nanoseconds, for launches made after
+ * the call (process-wide; default 1 s; 0 restores the default).  Each CTA
+ * restarts the clock at every unit of work it takes up (one token's head
+ * group, or a CTA's share of one), so the bound applies per unit, not to the
+ * whole launch.
  */
 void sparse_mla_set_wait_timeout_ns(unsigned long long ns);
 

@@ -17,7 +17,13 @@
 // (cu_seqlens) prefill and the paged BF16 cache (TileLang page, Summary);
 // only the index -> row mapping differs.
 //
-// Work decomposition: one CTA per (token, top-k split, head group).  The
+// Work decomposition: a persistent grid of at most one CTA per SM (each
+// takes ~225 KB of shared memory).  A unit of work is one token's list for
+// one group of up to 64 heads; prefill deals whole units round-robin to the
+// CTAs, decode cuts the units' lists, laid end to end, into one equal range
+// per CTA and merges the pieces of cut units afterwards (combine kernel).
+// Every role of a CTA walks the same sequence of items, so the producers
+// gather the next item while the consumers finish the current one.  The
 // index list is walked in blocks of 64 entries (64 gathered rows = 72 KB, so
 // two to three blocks fit in shared memory and the gather of the next blocks
 // overlaps the math of the current one); a block with no valid entry is
@@ -91,6 +97,15 @@ constexpr int kMaxSmem = 232448;
 
 enum Mode : int { kDense = 0, kVarlen = 1, kPaged = 2 };
 
+// How units (token x head group) are dealt to the persistent CTAs:
+//   kWholeUnits   CTA c runs units c, c + G, c + 2G, ... whole (prefill).
+//   kBlockRanges  the units' index lists, laid end to end as T = units x nb
+//                 blocks of 64 entries, are cut into G equal ranges, one per
+//                 CTA (decode: a few long lists spread over every SM).  A unit
+//                 cut between CTAs leaves a partial result per piece, merged
+//                 by combine_splits_kernel.
+enum Sched : int { kWholeUnits = 0, kBlockRanges = 1 };
+
 enum ErrCode : int { kErrProducerWait = 0x101, kErrMmaWait = 0x201, kErrSoftmaxWait = 0x301 };
 
 struct FwdParams {
@@ -99,8 +114,8 @@ struct FwdParams {
   const int32_t* indices;   // [n_tok, topk]
   __nv_bfloat16* out;       // [n_tok, h_q, 512]
   float* lse;               // [n_tok, h_q]
-  float* part_o;            // [splits, n_tok, h_q, 512]  (splits > 1)
-  float* part_lse;          // [splits, n_tok, h_q]
+  float* part_o;            // [2 * ctas, part_rows, 512]  (kBlockRanges)
+  float* part_lse;          // [2 * ctas, part_rows]
   const int32_t* cu_q;      // varlen: [batch+1]
   const int32_t* cu_kv;     // varlen: [batch+1]
   const int32_t* block_table;  // paged: [batch, max_blocks]
@@ -108,12 +123,75 @@ struct FwdParams {
   int n_tok, h_q, topk, mode;
   int n_rows;               // rows of kv
   int s_kv, batch, s_next, page_size, max_blocks, num_blocks;
-  int splits;
+  int sched;                // kWholeUnits or kBlockRanges
+  int groups;               // head groups of up to 64 (a unit is one token x one group)
+  int nb;                   // 64-entry blocks per index list
+  int ctas;                 // CTAs of the (persistent) grid
+  int part_rows;            // head rows per partial slot: min(h_q, 64)
   float scale_log2;         // sm_scale * log2(e)
   unsigned long long timeout_ns;
 };
 
 __device__ int g_device_error;
+
+// kBlockRanges: CTA c covers flattened blocks [range_start(c), range_start(c+1)).
+__host__ __device__ inline long long range_start(int c, long long total, int ctas) {
+  return static_cast<long long>(c) * total / ctas;
+}
+// The CTA whose range holds flattened block x (0 <= x < total).
+__host__ __device__ inline int range_cta(long long x, long long total, int ctas) {
+  return static_cast<int>(((x + 1) * ctas - 1) / total);
+}
+
+// One piece of work: blocks [jb, je) of a unit's index list.  slot < 0: the
+// CTA runs the whole unit and writes out / LSE; else it writes a partial
+// result to slot 2c (its first item) or 2c + 1 (its last item).
+struct Item {
+  int unit, jb, je, slot;
+};
+
+struct ItemIter {
+  long long x;   // kBlockRanges: next flattened block of this CTA
+  int k;         // items handed out so far
+};
+
+__device__ __forceinline__ ItemIter items_begin(const FwdParams& p) {
+  ItemIter it;
+  it.k = 0;
+  it.x = p.sched == kBlockRanges
+             ? range_start(static_cast<int>(blockIdx.x), static_cast<long long>(p.n_tok) * p.groups * p.nb, p.ctas)
+             : 0;
+  return it;
+}
+
+// Every role of a CTA walks the same item sequence with its own iterator.
+__device__ __forceinline__ bool next_item(const FwdParams& p, ItemIter& it, Item& out) {
+  const int c = static_cast<int>(blockIdx.x);
+  const long long units = static_cast<long long>(p.n_tok) * p.groups;
+  if (p.sched == kWholeUnits) {
+    const long long u = c + static_cast<long long>(it.k) * p.ctas;
+    if (u >= units) return false;
+    out.unit = static_cast<int>(u);
+    out.jb = 0;
+    out.je = p.nb;
+    out.slot = -1;
+    ++it.k;
+    return true;
+  }
+  const long long total = units * p.nb;
+  const long long end = range_start(c + 1, total, p.ctas);
+  if (it.x >= end) return false;
+  const long long u = it.x / p.nb;
+  const long long ub = u * p.nb;
+  out.unit = static_cast<int>(u);
+  out.jb = static_cast<int>(it.x - ub);
+  out.je = static_cast<int>(min(static_cast<long long>(p.nb), end - ub));
+  const bool whole = range_cta(ub, total, p.ctas) == range_cta(ub + p.nb - 1, total, p.ctas);
+  out.slot = whole ? -1 : 2 * c + (it.k == 0 ? 0 : 1);
+  it.x = ub + out.je;
+  ++it.k;
+  return true;
+}
 
 template <int N>
 struct Layout {
@@ -143,7 +221,7 @@ struct __align__(16) Misc {
   uint64_t v_full[12], v_empty[12];
   uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
-  uint64_t q_full, s_full[2][2], p_full[2], o_full, drain[3], cand_full;
+  uint64_t q_full, q_empty, s_full[2][2], p_full[2], o_full, drain[3], cand_full, stage_free;
   int32_t info_blk[kInfoDepth];
   uint32_t info_mask[kInfoDepth][2];
   uint32_t cand[2][kProducerWarps];
@@ -307,14 +385,11 @@ __device__ __forceinline__ void cp_async_arrive_on(uint32_t bar) {
 // ------------------------------------------------------------------ producer
 
 template <int N>
-__device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int tok, int jb, int je,
-                             uint64_t deadline) {
+__device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
   using L = Layout<N>;
   const int warp = static_cast<int>(threadIdx.x >> 5);   // 0..3
   const int lane = static_cast<int>(lane_id());
   const volatile int* ab = &m.abort_flag;
-  const TokCtx ctx = token_context(p, tok);
-  const int32_t* irow = p.indices + static_cast<size_t>(tok) * p.topk;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
   const int piece = lane & 7;
@@ -322,146 +397,182 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int to
   // Every warp maps the whole block (entries 2*lane, 2*lane+1) so all agree
   // on the skip decision and on ring positions without a barrier; each warp
   // then copies its own 16 rows of every tile.
-  int n = 0;
-  int win = 0;
-  for (int wb = jb; wb < je; wb += 32, ++win) {
-    // Candidate blocks of this window of up to 32: a block none of whose
-    // entries lies in [0, kv_len) is skipped without mapping its rows (a
-    // causal list is mostly -1 padding for early tokens).  Each warp scans 8
-    // blocks with 16 coalesced loads in flight per lane; the four masks meet
-    // in shared memory.  The loads also bring the list into L1 for the row
-    // mapping below.
-    const int we = min(je, wb + 32);
-    uint32_t cand;
-    {
-      const int b0 = wb + warp * 8;
-      int v[16];
+  int n = 0;     // blocks issued: position in the tile rings
+  int ni = 0;    // info entries published: blocks and per-item end markers
+  int win = 0;   // index windows scanned (phase of cand_full)
+  ItemIter iter = items_begin(p);
+  Item item;
+  uint64_t deadline = 0;
+  while (next_item(p, iter, item)) {
+    deadline = global_timer_ns() + p.timeout_ns;   // every wait of this item is bounded from here
+    const int tok = item.unit / p.groups;
+    const int jb = item.jb, je = item.je;
+    const TokCtx ctx = token_context(p, tok);
+    const int32_t* irow = p.indices + static_cast<size_t>(tok) * p.topk;
+    for (int wb = jb; wb < je; wb += 32, ++win) {
+      // Candidate blocks of this window of up to 32: a block none of whose
+      // entries lies in [0, kv_len) is skipped without mapping its rows (a
+      // causal list is mostly -1 padding for early tokens).  Each warp scans 8
+      // blocks with 16 coalesced loads in flight per lane; the four masks meet
+      // in shared memory.  The loads also bring the list into L1 for the row
+      // mapping below.
+      const int we = min(je, wb + 32);
+      uint32_t cand;
+      {
+        const int b0 = wb + warp * 8;
+        int v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int blk = b0 + (i >> 1);
-        const int e = blk * kBlk + (i & 1) * 32 + lane;
-        v[i] = (blk < we && e < p.topk) ? __ldg(irow + e) : -1;
+        for (int i = 0; i < 16; ++i) {
+          const int blk = b0 + (i >> 1);
+          const int e = blk * kBlk + (i & 1) * 32 + lane;
+          v[i] = (blk < we && e < p.topk) ? __ldg(irow + e) : -1;
+        }
+        uint32_t bits = 0;
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const bool c = (v[i] >= 0 && v[i] < ctx.kv_len) || (v[i + 1] >= 0 && v[i + 1] < ctx.kv_len);
+          if (__ballot_sync(0xffffffffu, c) != 0u) bits |= 1u << (i >> 1);
+        }
+        if (lane == 0) {
+          m.cand[win & 1][warp] = bits << (warp * 8);
+          mbar_arrive(smem_u32(&m.cand_full));
+        }
+        const bool ok = mbar_wait(smem_u32(&m.cand_full), static_cast<uint32_t>(win) & 1u, deadline, ab);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        cand = 0;
+#pragma unroll
+        for (int w = 0; w < kProducerWarps; ++w) cand |= *reinterpret_cast<volatile uint32_t*>(&m.cand[win & 1][w]);
       }
-      uint32_t bits = 0;
+      int j_next = cand != 0u ? wb + __ffs(static_cast<int>(cand)) - 1 : -1;
+      int idx_next[2];
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        const bool c = (v[i] >= 0 && v[i] < ctx.kv_len) || (v[i + 1] >= 0 && v[i + 1] < ctx.kv_len);
-        if (__ballot_sync(0xffffffffu, c) != 0u) bits |= 1u << (i >> 1);
-      }
-      if (lane == 0) {
-        m.cand[win & 1][warp] = bits << (warp * 8);
-        mbar_arrive(smem_u32(&m.cand_full));
-      }
-      const bool ok = mbar_wait(smem_u32(&m.cand_full), static_cast<uint32_t>(win) & 1u, deadline, ab);
-      if (!__all_sync(0xffffffffu, ok)) return false;
-      cand = 0;
-#pragma unroll
-      for (int w = 0; w < kProducerWarps; ++w) cand |= *reinterpret_cast<volatile uint32_t*>(&m.cand[win & 1][w]);
-    }
-    int j_next = cand != 0u ? wb + __ffs(static_cast<int>(cand)) - 1 : -1;
-    int idx_next[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int e = j_next * kBlk + lane * 2 + i;
-      idx_next[i] = (j_next >= 0 && e < p.topk) ? __ldg(irow + e) : -1;
-    }
-    while (j_next >= 0) {
-      const int j = j_next;
-      cand &= cand - 1u;
-      j_next = cand != 0u ? wb + __ffs(static_cast<int>(cand)) - 1 : -1;
-      int rows[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) rows[i] = map_entry(p, ctx, idx_next[i]);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {   // prefetch the next candidate's indices
+      for (int i = 0; i < 2; ++i) {
         const int e = j_next * kBlk + lane * 2 + i;
         idx_next[i] = (j_next >= 0 && e < p.topk) ? __ldg(irow + e) : -1;
       }
-      const uint32_t bal0 = __ballot_sync(0xffffffffu, rows[0] >= 0);
-      const uint32_t bal1 = __ballot_sync(0xffffffffu, rows[1] >= 0);
-      if ((bal0 | bal1) == 0u) continue;
+      while (j_next >= 0) {
+        const int j = j_next;
+        cand &= cand - 1u;
+        j_next = cand != 0u ? wb + __ffs(static_cast<int>(cand)) - 1 : -1;
+        int rows[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) rows[i] = map_entry(p, ctx, idx_next[i]);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {   // prefetch the next candidate's indices
+          const int e = j_next * kBlk + lane * 2 + i;
+          idx_next[i] = (j_next >= 0 && e < p.topk) ? __ldg(irow + e) : -1;
+        }
+        const uint32_t bal0 = __ballot_sync(0xffffffffu, rows[0] >= 0);
+        const uint32_t bal1 = __ballot_sync(0xffffffffu, rows[1] >= 0);
+        if ((bal0 | bal1) == 0u) continue;
 
-      if (warp == 0) {
-        const int k = n % kInfoDepth;
-        const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
-        if (!__all_sync(0xffffffffu, ok)) return false;
-        if (lane == 0) {
-          m.info_blk[k] = j;
-          m.info_mask[k][0] = bal0;
-          m.info_mask[k][1] = bal1;
-          mbar_arrive(smem_u32(&m.info_full[k]));
+        if (warp == 0) {
+          const int k = ni % kInfoDepth;
+          const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((ni / kInfoDepth) & 1) ^ 1, deadline, ab);
+          if (!__all_sync(0xffffffffu, ok)) return false;
+          if (lane == 0) {
+            m.info_blk[k] = j;
+            m.info_mask[k][0] = bal0;
+            m.info_mask[k][1] = bal1;
+            mbar_arrive(smem_u32(&m.info_full[k]));
+          }
         }
-      }
-      // This warp copies block rows 16*warp + 4*it + sel; entry r of the block
-      // sits in lane r / 2 as rows[r % 2].
-      int myrow[4];
+        // This warp copies block rows 16*warp + 4*it + sel; entry r of the block
+        // sits in lane r / 2 as rows[r % 2].
+        int myrow[4];
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int r = warp * 16 + it * 4 + sel;
-        const int r0 = __shfl_sync(0xffffffffu, rows[0], r >> 1);
-        const int r1 = __shfl_sync(0xffffffffu, rows[1], r >> 1);
-        myrow[it] = (r & 1) ? r1 : r0;
-      }
-      // Tile order: value pairs 0 and 1, the rope tile, pairs 2 and 3 -- the
-      // QK^T part that needs pairs 0,1 and the rope can start after 3 tiles.
-      auto tile = [&](int step, uint32_t& empty, uint32_t& full, uint32_t& par, uint32_t& dst, int& first_chunk,
-                      int& n_chunks) {
-        const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
-        if (u < 4) {
-          const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
-          const uint32_t s = vi % L::kNV;
-          empty = smem_u32(&m.v_empty[s]);
-          full = smem_u32(&m.v_full[s]);
-          par = (vi / L::kNV) & 1u;
-          dst = vbase + s * kPairBytes;
-          first_chunk = 2 * u;
-          n_chunks = 2;
-        } else {
-          const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
-          empty = smem_u32(&m.rp_empty[rs]);
-          full = smem_u32(&m.rp_full[rs]);
-          par = (static_cast<uint32_t>(n) / L::kNR) & 1u;
-          dst = rbase + rs * kChunkBytes;
-          first_chunk = 8;
-          n_chunks = 1;
+        for (int it = 0; it < 4; ++it) {
+          const int r = warp * 16 + it * 4 + sel;
+          const int r0 = __shfl_sync(0xffffffffu, rows[0], r >> 1);
+          const int r1 = __shfl_sync(0xffffffffu, rows[1], r >> 1);
+          myrow[it] = (r & 1) ? r1 : r0;
         }
-      };
-      // A barrier test sits in the memory pipe behind this warp's earlier
-      // copies, so every wait costs about one drain of that queue.  With a
-      // ring deeper than two blocks (N <= 32) the slots of a block are usually
-      // all free already: test them together and issue every free tile back
-      // to back, blocking only when none is free.  With the two-block ring of
-      // N = 64 the slots free one by one behind P.V; there, waiting for each
-      // tile in turn measures faster.
-      if constexpr (N != 64) {
-        uint32_t done = 0;
-        while (done != 0x1fu) {
-          uint32_t ready = 0;
+        // Tile order: value pairs 0 and 1, the rope tile, pairs 2 and 3 -- the
+        // QK^T part that needs pairs 0,1 and the rope can start after 3 tiles.
+        auto tile = [&](int step, uint32_t& empty, uint32_t& full, uint32_t& par, uint32_t& dst, int& first_chunk,
+                        int& n_chunks) {
+          const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
+          if (u < 4) {
+            const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+            const uint32_t s = vi % L::kNV;
+            empty = smem_u32(&m.v_empty[s]);
+            full = smem_u32(&m.v_full[s]);
+            par = (vi / L::kNV) & 1u;
+            dst = vbase + s * kPairBytes;
+            first_chunk = 2 * u;
+            n_chunks = 2;
+          } else {
+            const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
+            empty = smem_u32(&m.rp_empty[rs]);
+            full = smem_u32(&m.rp_full[rs]);
+            par = (static_cast<uint32_t>(n) / L::kNR) & 1u;
+            dst = rbase + rs * kChunkBytes;
+            first_chunk = 8;
+            n_chunks = 1;
+          }
+        };
+        // A barrier test sits in the memory pipe behind this warp's earlier
+        // copies, so every wait costs about one drain of that queue.  With a
+        // ring deeper than two blocks (N <= 32) the slots of a block are usually
+        // all free already: test them together and issue every free tile back
+        // to back, blocking only when none is free.  With the two-block ring of
+        // N = 64 the slots free one by one behind P.V; there, waiting for each
+        // tile in turn measures faster.
+        if constexpr (N != 64) {
+          uint32_t done = 0;
+          while (done != 0x1fu) {
+            uint32_t ready = 0;
 #pragma unroll
-          for (int step = 0; step < 5; ++step) {
-            if (!((done >> step) & 1u)) {
+            for (int step = 0; step < 5; ++step) {
+              if (!((done >> step) & 1u)) {
+                uint32_t empty, full, par, dst;
+                int fc, nc;
+                tile(step, empty, full, par, dst, fc, nc);
+                if (mbar_test_wait(empty, par ^ 1u)) ready |= 1u << step;
+              }
+            }
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            if (ready == 0u) {
+              const int step = __ffs(static_cast<int>(~done & 0x1fu)) - 1;
               uint32_t empty, full, par, dst;
               int fc, nc;
               tile(step, empty, full, par, dst, fc, nc);
-              if (mbar_test_wait(empty, par ^ 1u)) ready |= 1u << step;
+              const bool ok = mbar_wait(empty, par ^ 1u, deadline, ab);
+              if (!__all_sync(0xffffffffu, ok)) return false;
+              ready = 1u << step;
             }
+#pragma unroll
+            for (int step = 0; step < 5; ++step) {
+              if ((ready >> step) & 1u) {
+                uint32_t empty, full, par, dst;
+                int first_chunk, n_chunks;
+                tile(step, empty, full, par, dst, first_chunk, n_chunks);
+              for (int c = 0; c < n_chunks; ++c) {
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                  const int r = warp * 16 + it * 4 + sel;
+                  const int src_row = myrow[it];
+                  const __nv_bfloat16* src =
+                      p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
+                  cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
+                }
+              }
+              // The hardware arrives on the tile's full barrier for this thread
+              // once all of this thread's copies so far have landed; the thread
+              // itself never waits on them.
+              cp_async_arrive_on(full);
+              }
+            }
+            done |= ready;
           }
-          ready = __shfl_sync(0xffffffffu, ready, 0);
-          if (ready == 0u) {
-            const int step = __ffs(static_cast<int>(~done & 0x1fu)) - 1;
+        } else {
+#pragma unroll 1
+          for (int step = 0; step < 5; ++step) {
             uint32_t empty, full, par, dst;
-            int fc, nc;
-            tile(step, empty, full, par, dst, fc, nc);
+            int first_chunk, n_chunks;
+            tile(step, empty, full, par, dst, first_chunk, n_chunks);
             const bool ok = mbar_wait(empty, par ^ 1u, deadline, ab);
             if (!__all_sync(0xffffffffu, ok)) return false;
-            ready = 1u << step;
-          }
-#pragma unroll
-          for (int step = 0; step < 5; ++step) {
-            if ((ready >> step) & 1u) {
-              uint32_t empty, full, par, dst;
-              int first_chunk, n_chunks;
-              tile(step, empty, full, par, dst, first_chunk, n_chunks);
             for (int c = 0; c < n_chunks; ++c) {
 #pragma unroll
               for (int it = 0; it < 4; ++it) {
@@ -476,45 +587,23 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase, int to
             // once all of this thread's copies so far have landed; the thread
             // itself never waits on them.
             cp_async_arrive_on(full);
-            }
           }
-          done |= ready;
         }
-      } else {
-#pragma unroll 1
-        for (int step = 0; step < 5; ++step) {
-          uint32_t empty, full, par, dst;
-          int first_chunk, n_chunks;
-          tile(step, empty, full, par, dst, first_chunk, n_chunks);
-          const bool ok = mbar_wait(empty, par ^ 1u, deadline, ab);
-          if (!__all_sync(0xffffffffu, ok)) return false;
-          for (int c = 0; c < n_chunks; ++c) {
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-              const int r = warp * 16 + it * 4 + sel;
-              const int src_row = myrow[it];
-              const __nv_bfloat16* src =
-                  p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
-              cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
-            }
-          }
-          // The hardware arrives on the tile's full barrier for this thread
-          // once all of this thread's copies so far have landed; the thread
-          // itself never waits on them.
-          cp_async_arrive_on(full);
-        }
+        ++n;
+        ++ni;
       }
-      ++n;
     }
-  }
-  if (warp == 0) {
-    const int k = n % kInfoDepth;
-    const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((n / kInfoDepth) & 1) ^ 1, deadline, ab);
-    if (!__all_sync(0xffffffffu, ok)) return false;
-    if (lane == 0) {
-      m.info_blk[k] = -1;
-      mbar_arrive(smem_u32(&m.info_full[k]));
+    // End of the item: a marker the consumers take as "finish this unit".
+    if (warp == 0) {
+      const int k = ni % kInfoDepth;
+      const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((ni / kInfoDepth) & 1) ^ 1, deadline, ab);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      if (lane == 0) {
+        m.info_blk[k] = -1;
+        mbar_arrive(smem_u32(&m.info_full[k]));
+      }
     }
+    ++ni;
   }
   return true;
 }
@@ -575,61 +664,83 @@ __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase
 }
 
 template <int N, int PART>
-__device__ bool run_qk(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline) {
+__device__ bool run_qk(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem) {
   using L = Layout<N>;
   const volatile int* ab = &m.abort_flag;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
-  if (!mbar_wait(smem_u32(&m.q_full), 0, deadline, ab)) return false;
-  tc_fence_after();
-  for (int n = 0;; ++n) {
-    const int k = n % kInfoDepth;
-    if (!mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab)) return false;
-    const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
-    mbar_arrive(smem_u32(&m.info_empty[k]));
-    if (blk < 0) break;
-    // S buffer n&1 was last read by the softmax of block n-2.
-    if (n >= 2 && !mbar_wait(smem_u32(&m.p_full[n & 1]), ((n - 2) >> 1) & 1, deadline, ab)) return false;
-    if (!issue_qk<N, PART>(m, qbase, vbase, rbase, tmem, n, deadline, ab)) return false;
+  int n = 0, ni = 0, items = 0;   // blocks (S buffer parity), info entries, items
+  ItemIter iter = items_begin(p);
+  Item item;
+  uint64_t deadline = 0;
+  while (next_item(p, iter, item)) {
+    deadline = global_timer_ns() + p.timeout_ns;   // every wait of this item is bounded from here
+      // Q of this item, loaded by the softmax warps.
+      if (!mbar_wait(smem_u32(&m.q_full), items & 1, deadline, ab)) return false;
+      tc_fence_after();
+      for (;;) {
+        const int k = ni % kInfoDepth;
+        if (!mbar_wait(smem_u32(&m.info_full[k]), (ni / kInfoDepth) & 1, deadline, ab)) return false;
+        const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
+        mbar_arrive(smem_u32(&m.info_empty[k]));
+        ++ni;
+        if (blk < 0) break;
+        // S buffer n&1 was last read by the softmax of block n-2.
+        if (n >= 2 && !mbar_wait(smem_u32(&m.p_full[n & 1]), ((n - 2) >> 1) & 1, deadline, ab)) return false;
+        if (!issue_qk<N, PART>(m, qbase, vbase, rbase, tmem, n, deadline, ab)) return false;
+        ++n;
+      }
+      // Q may be replaced once this thread's QK^T MMAs have completed.
+      mma_commit(smem_u32(&m.q_empty));
+      ++items;
   }
   return true;
 }
 
 template <int N>
-__device__ bool run_pv(Misc& m, uint8_t* sbase, uint32_t tmem, uint64_t deadline) {
+__device__ bool run_pv(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem) {
   using L = Layout<N>;
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
   const volatile int* ab = &m.abort_flag;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
   const uint32_t tO = tmem + 4 * N;
-  int n = 0;
-  for (;; ++n) {
-    const int k = n % kInfoDepth;
-    if (!mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab)) return false;
-    const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
-    mbar_arrive(smem_u32(&m.info_empty[k]));
-    if (blk < 0) break;
-    if (!mbar_wait(smem_u32(&m.p_full[n & 1]), (n >> 1) & 1, deadline, ab)) return false;
-    tc_fence_after();
-    const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
+  int n = 0, ni = 0;   // blocks (ring positions), info entries
+  ItemIter iter = items_begin(p);
+  Item item;
+  uint64_t deadline = 0;
+  while (next_item(p, iter, item)) {
+    deadline = global_timer_ns() + p.timeout_ns;   // every wait of this item is bounded from here
+    int nl = 0;          // blocks of this item: the first one starts O^T afresh
+    for (;; ++n, ++nl) {
+      const int k = ni % kInfoDepth;
+      if (!mbar_wait(smem_u32(&m.info_full[k]), (ni / kInfoDepth) & 1, deadline, ab)) return false;
+      const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
+      mbar_arrive(smem_u32(&m.info_empty[k]));
+      ++ni;
+      if (blk < 0) break;
+      if (!mbar_wait(smem_u32(&m.p_full[n & 1]), (n >> 1) & 1, deadline, ab)) return false;
+      tc_fence_after();
+      const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
 #pragma unroll 1
-    for (int mt = 0; mt < 4; ++mt) {
-      const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(mt)) % L::kNV;
+      for (int mt = 0; mt < 4; ++mt) {
+        const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(mt)) % L::kNV;
 #pragma unroll
-      for (int ks = 0; ks < kBlk / 16; ++ks) {
-        const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-        const uint64_t b = smem_desc(rbase + rs * kChunkBytes + ks * 16 * L::kPRow, 16 * L::kPRow * 8,
-                                     8 * L::kPRow, L::kPSwz);
-        mma_bf16_ss(tO + mt * N, a, b, kIdescPV, (n > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < kBlk / 16; ++ks) {
+          const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
+          const uint64_t b = smem_desc(rbase + rs * kChunkBytes + ks * 16 * L::kPRow, 16 * L::kPRow * 8,
+                                       8 * L::kPRow, L::kPSwz);
+          mma_bf16_ss(tO + mt * N, a, b, kIdescPV, (nl > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&m.v_empty[s]));
       }
-      mma_commit(smem_u32(&m.v_empty[s]));
+      mma_commit(smem_u32(&m.rp_empty[rs]));
     }
-    mma_commit(smem_u32(&m.rp_empty[rs]));
+    // O^T of an item that issued blocks is complete (the softmax waits on this
+    // only for such items, so the two sides count the same phases).
+    if (nl > 0) mma_commit(smem_u32(&m.o_full));
   }
-  if (n > 0) mma_commit(smem_u32(&m.o_full));
-  else mbar_arrive(smem_u32(&m.o_full));
   return true;
 }
 
@@ -644,8 +755,7 @@ __device__ __forceinline__ void load_s_half(uint32_t taddr, float* v) {
 }
 
 template <int N>
-__device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int tok, int split, int h0,
-                            int hv, int grp, uint64_t deadline) {
+__device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int grp) {
   using L = Layout<N>;
   constexpr int H = L::kHG;            // heads this group owns (16 or 32)
   const volatile int* ab = &m.abort_flag;
@@ -666,159 +776,216 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
 
-  // Q rows of this group's heads -> shared memory, K-major with the 128B
-  // swizzle, by cp.async so all loads are in flight at once; heads past h_q
-  // are zero-filled.
-  {
-    const __nv_bfloat16* qt = p.q + (static_cast<size_t>(tok) * p.h_q + h0) * kDqk;
-    for (int x = tid; x < H * 72; x += 128) {
-      const int h = hb + x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
-      const bool live = h < hv;
-      const __nv_bfloat16* src = qt + static_cast<size_t>(live ? h : 0) * kDqk + c * 64 + piece * 8;
-      cp_async_16(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4), src, live ? 16u : 0u);
+  int n = 0, ni = 0;        // blocks (buffer positions), info entries
+  int items = 0, filled = 0; // items, items that issued blocks (o_full phases)
+  ItemIter iter = items_begin(p);
+  Item item;
+  uint64_t deadline = 0;
+  while (next_item(p, iter, item)) {
+    deadline = global_timer_ns() + p.timeout_ns;   // every wait of this item is bounded from here
+    const int tok = item.unit / p.groups;
+    const int h0 = (item.unit % p.groups) * 64;
+    const int hv = min(N, p.h_q - h0);
+    if (items > 0) {
+      // Q is replaced once the previous item's QK^T MMAs have completed and
+      // every softmax thread has read its staged output back (the staging area
+      // is the Q region).
+      const bool ok = mbar_wait(smem_u32(&m.q_empty), (items - 1) & 1, deadline, ab) &&
+                      mbar_wait(smem_u32(&m.stage_free), (items - 1) & 1, deadline, ab);
+      if (bar_red_or_128(bar_id, !ok)) return false;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    fence_proxy_async_smem();
-    if (tid < H) m.mrun[hb + tid] = -INFINITY;
-    named_bar_sync(bar_id, 128);
-    if (tid == 0) mbar_arrive(smem_u32(&m.q_full));
-  }
-
-  // Head hb+tid's running sum of exp2(s - m) (owner threads tid < H); the
-  // per-block sums arrive through m.rsum, reduced over the 64 rows.
-  float lrun = 0.f;
-  int n = 0;
-  for (;;) {
-    const int k = n % kInfoDepth;
-    // Every wait is followed by a barrier that ORs the failures of the
-    // group's 128 threads, so they all continue or all return together.
-    const bool iok = mbar_wait(smem_u32(&m.info_full[k]), (n / kInfoDepth) & 1, deadline, ab);
-    if (bar_red_or_128(bar_id, !iok)) return false;
-    const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
-    const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&m.info_mask[k][row & 1]);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
-    if (blk < 0) break;
-    const bool valid = ((bits >> (row >> 1)) & 1u) != 0u;
-    const uint32_t tSa = tmem + lane_off + static_cast<uint32_t>(n & 1) * N + hb;        // part 0
-    const uint32_t tSb = tmem + lane_off + static_cast<uint32_t>(2 + (n & 1)) * N + hb;  // part 1
-
-    const bool sok = mbar_wait(smem_u32(&m.s_full[0][n & 1]), (n >> 1) & 1, deadline, ab) &&
-                     mbar_wait(smem_u32(&m.s_full[1][n & 1]), (n >> 1) & 1, deadline, ab);
-    tc_fence_after();
-    // Block max per head: butterfly over the half-warp, then over the 4 warps.
+    // Q rows of this group's heads -> shared memory, K-major with the 128B
+    // swizzle, by cp.async so all loads are in flight at once; heads past h_q
+    // are zero-filled.
     {
-      float s[HH], t[HH];
-      load_s_half<HH>(tSa, s);
-      load_s_half<HH>(tSb, t);
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < HH; ++i) s[i] = valid ? (s[i] + t[i]) * p.scale_log2 : -INFINITY;
-      half_xreduce<HH, true>(s, lane, m.red[q4] + hb + hsub);
+      const __nv_bfloat16* qt = p.q + (static_cast<size_t>(tok) * p.h_q + h0) * kDqk;
+      for (int x = tid; x < H * 72; x += 128) {
+        const int h = hb + x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
+        const bool live = h < hv;
+        const __nv_bfloat16* src = qt + static_cast<size_t>(live ? h : 0) * kDqk + c * 64 + piece * 8;
+        cp_async_16(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4), src, live ? 16u : 0u);
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      fence_proxy_async_smem();
+      if (tid < H) m.mrun[hb + tid] = -INFINITY;
+      named_bar_sync(bar_id, 128);
+      if (tid == 0) mbar_arrive(smem_u32(&m.q_full));
     }
-    if (bar_red_or_128(bar_id, !sok)) return false;
-    bool grew = false;
+
+    // Head hb+tid's running sum of exp2(s - m) (owner threads tid < H); the
+    // per-block sums arrive through m.rsum, reduced over the 64 rows.
+    float lrun = 0.f;
+    int nl = 0;   // blocks of this item
+    for (;;) {
+      const int k = ni % kInfoDepth;
+      // Every wait is followed by a barrier that ORs the failures of the
+      // group's 128 threads, so they all continue or all return together.
+      const bool iok = mbar_wait(smem_u32(&m.info_full[k]), (ni / kInfoDepth) & 1, deadline, ab);
+      ++ni;
+      if (bar_red_or_128(bar_id, !iok)) return false;
+      const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
+      const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&m.info_mask[k][row & 1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
+      if (blk < 0) break;
+      const bool valid = ((bits >> (row >> 1)) & 1u) != 0u;
+      const uint32_t tSa = tmem + lane_off + static_cast<uint32_t>(n & 1) * N + hb;        // part 0
+      const uint32_t tSb = tmem + lane_off + static_cast<uint32_t>(2 + (n & 1)) * N + hb;  // part 1
+
+      const bool sok = mbar_wait(smem_u32(&m.s_full[0][n & 1]), (n >> 1) & 1, deadline, ab) &&
+                       mbar_wait(smem_u32(&m.s_full[1][n & 1]), (n >> 1) & 1, deadline, ab);
+      tc_fence_after();
+      // Block max per head: butterfly over the half-warp, then over the 4 warps.
+      {
+        float s[HH], t[HH];
+        load_s_half<HH>(tSa, s);
+        load_s_half<HH>(tSb, t);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < HH; ++i) s[i] = valid ? (s[i] + t[i]) * p.scale_log2 : -INFINITY;
+        half_xreduce<HH, true>(s, lane, m.red[q4] + hb + hsub);
+      }
+      if (bar_red_or_128(bar_id, !sok)) return false;
+      bool grew = false;
+      if (tid < H) {
+        const int h = hb + tid;
+        if (nl > 0) lrun += (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]);
+        const float bm = fmaxf(fmaxf(m.red[0][h], m.red[1][h]), fmaxf(m.red[2][h], m.red[3][h]));
+        const float mo = m.mrun[h];
+        const float mn = (bm > mo + kLazyRescale) ? bm : mo;
+        const float al = fast_exp2(mo - mn);
+        lrun *= al;
+        m.alpha[h] = al;
+        m.mrun[h] = mn;
+        grew = (mn != mo);
+      }
+      const bool rescale = bar_red_or_128(bar_id, grew);
+      if (rescale && nl > 0) {
+        // O^T must hold exactly the blocks before this one: wait for the
+        // previous block's P.V (its last commits release that block's rope /
+        // P^T slot), then rescale this group's head columns.
+        const int pb = n - 1;
+        const bool pok = mbar_wait(smem_u32(&m.rp_empty[pb % L::kNR]), (pb / L::kNR) & 1, deadline, ab);
+        tc_fence_after();
+        if (bar_red_or_128(bar_id, !pok)) return false;
+#pragma unroll 1
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int g = 0; g < H / 16; ++g) {
+            float o[16];
+            tmem_ld16(tO + mt * N + g * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= m.alpha[hb + g * 16 + i];
+            tmem_st16(tO + mt * N + g * 16, o);
+          }
+        }
+        tmem_wait_st();
+      }
+      // P^T row (bf16) into the rope slot of this block, MN-major swizzled,
+      // and the block's per-head sums of P.
+      {
+        const uint32_t prow = rbase + (n % L::kNR) * kChunkBytes + row * L::kPRow;
+        const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
+        float s[HH], t[HH];
+        load_s_half<HH>(tSa, s);
+        load_s_half<HH>(tSb, t);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < HH / 8; ++c) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int h = hb + hsub + c * 8 + i;
+            s[c * 8 + i] = valid ? fast_exp2((s[c * 8 + i] + t[c * 8 + i]) * p.scale_log2 - m.mrun[h]) : 0.f;
+          }
+          const uint32_t chunk = static_cast<uint32_t>((hb + hsub) / 8 + c);
+          st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
+                       pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
+                       pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
+        }
+        half_xreduce<HH, false>(s, lane, m.rsum[q4] + hb + hsub);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&m.p_full[n & 1]));
+      ++n;
+      ++nl;
+    }
+
+    // ---------------------------------------------------------- epilogue
+    // O^T is complete once the P.V of the item's last block has; an item with
+    // no block issued none (and P.V signals nothing for it).
+    if (nl > 0) {
+      const bool ook = mbar_wait(smem_u32(&m.o_full), filled & 1, deadline, ab);
+      tc_fence_after();
+      if (bar_red_or_128(bar_id, !ook)) return false;
+      ++filled;
+    }
+    const size_t tok_h = static_cast<size_t>(tok) * p.h_q + h0;
     if (tid < H) {
       const int h = hb + tid;
-      if (n > 0) lrun += (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]);
-      const float bm = fmaxf(fmaxf(m.red[0][h], m.red[1][h]), fmaxf(m.red[2][h], m.red[3][h]));
-      const float mo = m.mrun[h];
-      const float mn = (bm > mo + kLazyRescale) ? bm : mo;
-      const float al = fast_exp2(mo - mn);
-      lrun *= al;
-      m.alpha[h] = al;
-      m.mrun[h] = mn;
-      grew = (mn != mo);
+      if (nl > 0) lrun += (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]);
+      float lse;
+      if (nl > 0) {
+        lse = (m.mrun[h] + log2f(lrun)) * 0.69314718055994530942f;
+        m.fin[h] = 1.0f / lrun;
+      } else {
+        lse = -INFINITY;
+        m.fin[h] = 0.f;
+      }
+      if (h < hv) {
+        if (item.slot >= 0) p.part_lse[static_cast<size_t>(item.slot) * p.part_rows + h] = lse;
+        else p.lse[tok_h + h] = lse;
+      }
     }
-    const bool rescale = bar_red_or_128(bar_id, grew);
-    if (rescale && n > 0) {
-      // O^T must hold exactly the blocks before this one: wait for the
-      // previous block's P.V (its last commits release that block's rope /
-      // P^T slot), then rescale this group's head columns.
-      const int pb = n - 1;
-      const bool pok = mbar_wait(smem_u32(&m.rp_empty[pb % L::kNR]), (pb / L::kNR) & 1, deadline, ab);
-      tc_fence_after();
-      if (bar_red_or_128(bar_id, !pok)) return false;
+    named_bar_sync(bar_id, 128);
+    const int dvrow = q4 * 32 + lane;   // O^T (M=128) lane of this thread
+    // The group's normalisers in registers: read once here, not after every
+    // store (which the compiler must assume may alias them).
+    float fin[H];
+#pragma unroll
+    for (int i = 0; i < H; ++i) fin[i] = m.fin[hb + i];
+    if (item.slot >= 0) {
+      // fp32 partials: 32 consecutive dv per warp store (128 B), already coalesced.
+      float* dst = p.part_o + (static_cast<size_t>(item.slot) * p.part_rows + hb) * kDv + dvrow;
 #pragma unroll 1
       for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
         for (int g = 0; g < H / 16; ++g) {
           float o[16];
-          tmem_ld16(tO + mt * N + g * 16, o);
-          tmem_wait_ld();
+          if (nl > 0) {
+            tmem_ld16(tO + mt * N + g * 16, o);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] *= m.alpha[hb + g * 16 + i];
-          tmem_st16(tO + mt * N + g * 16, o);
+            for (int i = 0; i < 16; ++i) o[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int hl = g * 16 + i;
+            if (hb + hl < hv) dst[static_cast<size_t>(hl) * kDv + mt * 128] = o[i] * fin[hl];
+          }
         }
       }
-      tmem_wait_st();
-    }
-    // P^T row (bf16) into the rope slot of this block, MN-major swizzled,
-    // and the block's per-head sums of P.
-    {
-      const uint32_t prow = rbase + (n % L::kNR) * kChunkBytes + row * L::kPRow;
-      const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
-      float s[HH], t[HH];
-      load_s_half<HH>(tSa, s);
-      load_s_half<HH>(tSb, t);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < HH / 8; ++c) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int h = hb + hsub + c * 8 + i;
-          s[c * 8 + i] = valid ? fast_exp2((s[c * 8 + i] + t[c * 8 + i]) * p.scale_log2 - m.mrun[h]) : 0.f;
-        }
-        const uint32_t chunk = static_cast<uint32_t>((hb + hsub) / 8 + c);
-        st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
-                     pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
-                     pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
-      }
-      half_xreduce<HH, false>(s, lane, m.rsum[q4] + hb + hsub);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    mbar_arrive(smem_u32(&m.p_full[n & 1]));
-    ++n;
-  }
-
-  // ---------------------------------------------------------- epilogue
-  const bool ook = mbar_wait(smem_u32(&m.o_full), 0, deadline, ab);
-  tc_fence_after();
-  if (bar_red_or_128(bar_id, !ook)) return false;
-  const size_t tok_h = static_cast<size_t>(tok) * p.h_q + h0;
-  if (tid < H) {
-    const int h = hb + tid;
-    if (n > 0) lrun += (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]);
-    float lse;
-    if (n > 0) {
-      lse = (m.mrun[h] + log2f(lrun)) * 0.69314718055994530942f;
-      m.fin[h] = 1.0f / lrun;
     } else {
-      lse = -INFINITY;
-      m.fin[h] = 0.f;
-    }
-    if (h < hv) {
-      if (p.splits > 1) p.part_lse[static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + h] = lse;
-      else p.lse[tok_h + h] = lse;
-    }
+    // bf16 output: O^T rows (one dv per thread) are transposed through shared
+    // memory into [head][dv] rows, then written with 16-byte coalesced stores.
+    // The staging area is the Q region: the item's QK^T MMAs are complete and
+    // the next item's Q is loaded only after every softmax thread arrives on
+    // stage_free (the value ring already holds the next item's tiles).
+    // Every group's Q load of this item has landed before any of it is
+  // overwritten (an item without blocks gets here without waiting on QK^T).
+  {
+    const bool qok = mbar_wait(smem_u32(&m.q_full), items & 1, deadline, ab);
+    if (bar_red_or_128(bar_id, !qok)) return false;
   }
-  named_bar_sync(bar_id, 128);
-  const int dvrow = q4 * 32 + lane;   // O^T (M=128) lane of this thread
-  // The group's normalisers in registers: read once here, not after every
-  // store (which the compiler must assume may alias them).
-  float fin[H];
-#pragma unroll
-  for (int i = 0; i < H; ++i) fin[i] = m.fin[hb + i];
-  if (p.splits > 1) {
-    // fp32 partials: 32 consecutive dv per warp store (128 B), already coalesced.
-    float* dst = p.part_o + (static_cast<size_t>(split) * p.n_tok * p.h_q + tok_h + hb) * kDv + dvrow;
+  const uint32_t stage = smem_u32(sbase + L::kQOff) + static_cast<uint32_t>(hb) * (kDv * 2);
 #pragma unroll 1
     for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
       for (int g = 0; g < H / 16; ++g) {
         float o[16];
-        if (n > 0) {
+        if (nl > 0) {
           tmem_ld16(tO + mt * N + g * 16, o);
           tmem_wait_ld();
         } else {
@@ -828,58 +995,37 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int hl = g * 16 + i;
-          if (hb + hl < hv) dst[static_cast<size_t>(hl) * kDv + mt * 128] = o[i] * fin[hl];
+          const __nv_bfloat16 v = __float2bfloat16_rn(o[i] * fin[hl]);
+          const uint32_t addr = stage + static_cast<uint32_t>(hl * kDv + mt * 128 + dvrow) * 2u;
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&v)));
         }
       }
     }
-    return true;
-  }
-  // bf16 output: O^T rows (one dv per thread) are transposed through shared
-  // memory -- the value ring is idle once the last P.V has completed -- into
-  // [head][dv] rows, then written with 16-byte coalesced stores.
-  const uint32_t stage = smem_u32(sbase + L::kVOff) + static_cast<uint32_t>(hb) * (kDv * 2);
+    named_bar_sync(bar_id, 128);
+    // Rows of 512 dv, 16 bytes per thread: four shared loads in flight, then
+    // four global stores.
+    constexpr int kRounds = H * (kDv / 8) / 128;
+    static_assert(kRounds % 4 == 0, "store rounds");
 #pragma unroll 1
-  for (int mt = 0; mt < 4; ++mt) {
+    for (int r0 = 0; r0 < kRounds; r0 += 4) {
+      uint4 v[4];
 #pragma unroll
-    for (int g = 0; g < H / 16; ++g) {
-      float o[16];
-      if (n > 0) {
-        tmem_ld16(tO + mt * N + g * 16, o);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = 0.f;
+      for (int j = 0; j < 4; ++j) {
+        const int x = tid + (r0 + j) * 128;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
+                     : "r"(stage + static_cast<uint32_t>(x) * 16u));
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int hl = g * 16 + i;
-        const __nv_bfloat16 v = __float2bfloat16_rn(o[i] * fin[hl]);
-        const uint32_t addr = stage + static_cast<uint32_t>(hl * kDv + mt * 128 + dvrow) * 2u;
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&v)));
+      for (int j = 0; j < 4; ++j) {
+        const int x = tid + (r0 + j) * 128;
+        const int hl = x / (kDv / 8), c8 = x % (kDv / 8);
+        if (hb + hl < hv) *reinterpret_cast<uint4*>(p.out + (tok_h + hb + hl) * kDv + c8 * 8) = v[j];
       }
     }
-  }
-  named_bar_sync(bar_id, 128);
-  // Rows of 512 dv, 16 bytes per thread: four shared loads in flight, then
-  // four global stores.
-  constexpr int kRounds = H * (kDv / 8) / 128;
-  static_assert(kRounds % 4 == 0, "store rounds");
-#pragma unroll 1
-  for (int r0 = 0; r0 < kRounds; r0 += 4) {
-    uint4 v[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int x = tid + (r0 + j) * 128;
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
-                   : "r"(stage + static_cast<uint32_t>(x) * 16u));
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int x = tid + (r0 + j) * 128;
-      const int hl = x / (kDv / 8), c8 = x % (kDv / 8);
-      if (hb + hl < hv) *reinterpret_cast<uint4*>(p.out + (tok_h + hb + hl) * kDv + c8 * 8) = v[j];
-    }
+    mbar_arrive(smem_u32(&m.stage_free));
+    ++items;
   }
   return true;
 }
@@ -894,10 +1040,6 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
   Misc& m = *reinterpret_cast<Misc*>(sbase + L::kMiscOff);
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
-  const int tok = static_cast<int>(blockIdx.x) / p.splits;
-  const int split = static_cast<int>(blockIdx.x) % p.splits;
-  const int h0 = static_cast<int>(blockIdx.y) * 64;
-  const int hv = min(N, p.h_q - h0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNV; ++i) {
@@ -913,6 +1055,8 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
       mbar_init(smem_u32(&m.info_empty[i]), 3 + 4 * L::kGroups);
     }
     mbar_init(smem_u32(&m.q_full), L::kGroups);
+    mbar_init(smem_u32(&m.q_empty), 2);                       // the two QK^T issuers
+    mbar_init(smem_u32(&m.stage_free), 128 * L::kGroups);     // every softmax thread
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&m.s_full[0][i]), 1);
       mbar_init(smem_u32(&m.s_full[1][i]), 1);
@@ -935,21 +1079,16 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
   const uint32_t tmem = m.tmem_base;
 
   if (m.prior_error == 0) {
-    const uint64_t deadline = global_timer_ns() + p.timeout_ns;
-    const int nb = (p.topk + kBlk - 1) / kBlk;
-    const int jb = static_cast<int>((static_cast<long long>(split) * nb) / p.splits);
-    const int je = static_cast<int>((static_cast<long long>(split + 1) * nb) / p.splits);
     if (warp < kProducerWarps) {
-      if (!run_producer<N>(p, m, sbase, tok, jb, je, deadline)) raise_error(m, kErrProducerWait);
+      if (!run_producer<N>(p, m, sbase)) raise_error(m, kErrProducerWait);
       // Drain: every copy this thread issued has landed before the CTA can
       // exit, whether or not the consumers got to it.
       asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == kMmaWarp || warp == kMmaWarpB || warp == L::kPvWarp) {
       if (lane == 0) {
         const int role = warp == kMmaWarp ? 0 : (warp == kMmaWarpB ? 1 : 2);
-        const bool ok = role == 0 ? run_qk<N, 0>(m, sbase, tmem, deadline)
-                                  : (role == 1 ? run_qk<N, 1>(m, sbase, tmem, deadline)
-                                               : run_pv<N>(m, sbase, tmem, deadline));
+        const bool ok = role == 0 ? run_qk<N, 0>(p, m, sbase, tmem)
+                                  : (role == 1 ? run_qk<N, 1>(p, m, sbase, tmem) : run_pv<N>(p, m, sbase, tmem));
         if (!ok) raise_error(m, kErrMmaWait);
         // Drain: every MMA this thread issued completes before TMEM is freed.
         const int never = 0;
@@ -959,7 +1098,7 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
       __syncwarp();
     } else {
       const int grp = warp >= softmax_warp0(1) ? 1 : 0;
-      if (!run_softmax<N>(p, m, sbase, tmem, tok, split, h0, hv, grp, deadline)) raise_error(m, kErrSoftmaxWait);
+      if (!run_softmax<N>(p, m, sbase, tmem, grp)) raise_error(m, kErrSoftmaxWait);
     }
   }
   tc_fence_before();
@@ -970,35 +1109,49 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
 
 // ------------------------------------------------------------------ helper kernels
 
-// Merge per-split partial results: LSE = ln sum_s exp(LSE_s),
-// out = sum_s exp(LSE_s - LSE) * O_s (each O_s already normalised over its
-// split; the LSE merge of the TileLang page's split-KV decode).  One warp per
-// (token, head) row: lane s holds split s's LSE (splits <= 32), and every lane
-// owns the float4 columns lane + 32 k of the 512-wide row, so each load
-// instruction reads 512 contiguous bytes.  The sums run over s in order, so
-// the result does not depend on the launch shape.
+// Merge the pieces of units that kBlockRanges cut between CTAs:
+// LSE = ln sum_s exp(LSE_s), out = sum_s exp(LSE_s - LSE) * O_s (each O_s
+// already normalised over its piece; the LSE merge of the TileLang page's
+// split-KV decode).  One warp per (token, head) row.  The pieces of unit u
+// are the CTAs c_first..c_last whose ranges meet its blocks; CTA c holds u in
+// slot 2c if u is its first item, else 2c + 1.  Lane s handles piece s's LSE
+// (at most 32 pieces), and every lane owns the float4 columns lane + 32 k of
+// the 512-wide row, so each load instruction reads 512 contiguous bytes.  The
+// sums run over the pieces in order.  Rows of units one CTA ran whole are
+// final already and skipped.
 constexpr int kCombineRows = 8;   // rows (warps) per 256-thread block
-__global__ void __launch_bounds__(32 * kCombineRows) combine_splits_kernel(const float* __restrict__ part_o,
-                                                                          const float* __restrict__ part_lse,
-                                                                          __nv_bfloat16* __restrict__ out,
-                                                                          float* __restrict__ lse, int n_rows_th,
-                                                                          int splits) {
+__global__ void __launch_bounds__(32 * kCombineRows) combine_splits_kernel(const __grid_constant__ FwdParams p) {
   const int row = static_cast<int>(blockIdx.x) * kCombineRows + static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
-  if (row >= n_rows_th) return;
-  constexpr int kF4 = kDv / 4;                                   // float4 per row
-  const float4* src = reinterpret_cast<const float4*>(part_o) + static_cast<size_t>(row) * kF4 + lane;
-  const size_t split_stride = static_cast<size_t>(n_rows_th) * kF4;
-  // Split 0's partial is read while the LSEs arrive (one round trip saved).
+  if (row >= p.n_tok * p.h_q) return;
+  const int tok = row / p.h_q, hg = row % p.h_q;
+  const long long u = static_cast<long long>(tok) * p.groups + hg / 64;
+  const int h = hg % 64;
+  const long long total = static_cast<long long>(p.n_tok) * p.groups * p.nb;
+  const long long ub = u * p.nb;
+  const int c_first = range_cta(ub, total, p.ctas);
+  const int pieces = range_cta(ub + p.nb - 1, total, p.ctas) - c_first + 1;
+  if (pieces == 1) return;
+  auto slot_of = [&](int s) {
+    const int c = c_first + s;
+    return 2 * c + (range_start(c, total, p.ctas) < ub ? 1 : 0);
+  };
+  constexpr int kF4 = kDv / 4;   // float4 per row
+  auto row_of = [&](int slot) {
+    return reinterpret_cast<const float4*>(p.part_o) + (static_cast<size_t>(slot) * p.part_rows + h) * kF4 + lane;
+  };
+  // Piece 0's partial is read while the LSEs arrive.
+  const float4* src0 = row_of(slot_of(0));
   float4 v0[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) v0[k] = __ldcg(src + 32 * k);
-  const float my_ls = lane < splits ? __ldcg(part_lse + static_cast<size_t>(lane) * n_rows_th + row) : -INFINITY;
+  for (int k = 0; k < 4; ++k) v0[k] = __ldcg(src0 + 32 * k);
+  const float my_ls =
+      lane < pieces ? __ldcg(p.part_lse + static_cast<size_t>(slot_of(lane)) * p.part_rows + h) : -INFINITY;
   float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, __shfl_sync(0xffffffffu, my_ls, s));
-  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(row) * kDv) + 2 * lane;
+  for (int s = 0; s < pieces; ++s) mx = fmaxf(mx, __shfl_sync(0xffffffffu, my_ls, s));
+  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(p.out + static_cast<size_t>(row) * kDv) + 2 * lane;
   if (mx == -INFINITY) {
-    if (lane == 0) lse[row] = -INFINITY;
+    if (lane == 0) p.lse[row] = -INFINITY;
     const __nv_bfloat162 z = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -1008,22 +1161,23 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_splits_kernel(const
     return;
   }
   float sum = 0.f;
-  for (int s = 0; s < splits; ++s) sum += expf(__shfl_sync(0xffffffffu, my_ls, s) - mx);
+  for (int s = 0; s < pieces; ++s) sum += expf(__shfl_sync(0xffffffffu, my_ls, s) - mx);
   const float tot = mx + logf(sum);
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < splits; ++s) {
+  for (int s = 0; s < pieces; ++s) {
     const float ls = __shfl_sync(0xffffffffu, my_ls, s);
     if (ls == -INFINITY) continue;
     const float w = expf(ls - tot);
+    const float4* src = s == 0 ? src0 : row_of(slot_of(s));
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float4 v = s == 0 ? v0[k] : __ldcg(src + s * split_stride + 32 * k);
+      const float4 v = s == 0 ? v0[k] : __ldcg(src + 32 * k);
       acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
     }
   }
-  if (lane == 0) lse[row] = tot;
+  if (lane == 0) p.lse[row] = tot;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     o2[64 * k] = __floats2bfloat162_rn(acc[k].x, acc[k].y);

@@ -1,6 +1,6 @@
 // C-ABI entry points: host-side validation, launch
-// planning (head-group width, top-k splits) and launches on the caller's
-// stream.  See include/sparse_mla.h for the contract of each call.
+// planning (head-group width, persistent grid size and schedule) and
+// launches on the caller's stream.  See include/sparse_mla.h for the contract of each call.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -67,31 +67,41 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int head_width(int h_q) { return h_q <= 16 ? 16 : (h_q <= 32 ? 32 : 64); }
 int head_groups(int h_q) { return (h_q + 63) / 64; }
 
-// Number of top-k splits per token (decode).  One CTA runs per SM, so the
-// time is about (waves of CTAs) x (blocks per split + per-CTA start-up and
-// tail, ~1.5 blocks); pick the split count that minimises it, never more
-// than the number of blocks or 32.
-int plan_splits(long long n_tok, int h_q, int topk, int sm_count) {
+// Persistent grids: each CTA takes ~225 KB of shared memory, so one runs per
+// SM, and every CTA works through a list of items (see Sched in the kernel).
+int blocks_per_list(int topk) { return (topk + smla::kBlk - 1) / smla::kBlk; }
+
+// Prefill: whole units (token x head group) over min(units, SMs) CTAs.
+int prefill_ctas(long long n_tok, int h_q, int sm_count) {
   const long long units = n_tok * head_groups(h_q);
-  const int nb = (topk + smla::kBlk - 1) / smla::kBlk;
-  if (units <= 0 || sm_count <= 0) return 1;
-  int best = 1;
-  double best_cost = 0.0;
-  for (int s = 1; s <= nb && s <= 32; ++s) {
-    const long long ctas = units * s;
-    const long long waves = (ctas + sm_count - 1) / sm_count;
-    const double cost = static_cast<double>(waves) * (static_cast<double>((nb + s - 1) / s) + 1.5);
-    if (s == 1 || cost < best_cost - 1e-9) {
-      best = s;
-      best_cost = cost;
-    }
-  }
-  return best;
+  return static_cast<int>(units < sm_count ? units : sm_count);
+}
+
+// Decode: the units' block lists laid end to end and cut into equal ranges,
+// one per CTA, at most one CTA per SM.  Every range holds at least
+// ceil(nb / 31) blocks, so no unit is cut into more than 32 pieces (the
+// merge keeps one piece per lane of a warp).
+int decode_ctas(long long n_tok, int h_q, int topk, int sm_count) {
+  const int nb = blocks_per_list(topk);
+  const long long total = n_tok * head_groups(h_q) * nb;
+  const long long min_blocks = (nb + 30) / 31;
+  long long g = total / min_blocks;
+  if (g > sm_count) g = sm_count;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+// Head rows of one partial slot (a slot holds one unit's heads).
+int part_rows(int h_q) { return h_q < 64 ? h_q : 64; }
+
+// Decode workspace: partial outputs [2 G][part_rows][d_v] fp32, then partial
+// LSEs [2 G][part_rows] (two slots per CTA: its first and last item).
+size_t decode_part_floats(int ctas, int h_q) {
+  return 2 * static_cast<size_t>(ctas) * static_cast<size_t>(part_rows(h_q)) * (static_cast<size_t>(smla::kDv) + 1);
 }
 
 sparse_mla_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
   const int N = head_width(p.h_q);
-  dim3 grid(static_cast<unsigned>(p.n_tok) * static_cast<unsigned>(p.splits), static_cast<unsigned>(head_groups(p.h_q)));
+  const dim3 grid(static_cast<unsigned>(p.ctas));
   if (N == 16)
     smla::sparse_mla_fwd_kernel<16><<<grid, smla::Layout<16>::kThreads, smla::smem_bytes<16>(), stream>>>(p);
   else if (N == 32)
@@ -120,8 +130,10 @@ FwdParams base_params(const void* q, const int32_t* indices, float sm_scale, voi
   p.n_tok = n_tok;
   p.h_q = h_q;
   p.topk = topk;
-  p.splits = 1;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.groups = head_groups(h_q);
+  p.nb = blocks_per_list(topk);
+  p.part_rows = part_rows(h_q);
   unsigned long long t = g_timeout_ns.load();
   p.timeout_ns = t ? t : kDefaultTimeoutNs;
   return p;
@@ -160,6 +172,8 @@ sparse_mla_status_t sparse_mla_fwd(const void* q, const void* kv, const int32_t*
   p.mode = smla::kDense;
   p.n_rows = s_kv;
   p.s_kv = s_kv;
+  p.sched = smla::kWholeUnits;
+  p.ctas = prefill_ctas(s_q, h_q, sms);
   return launch_fwd(p, cs);
 }
 
@@ -186,6 +200,8 @@ sparse_mla_status_t sparse_mla_fwd_varlen(const void* q, const void* kv, const i
   p.batch = batch;
   p.cu_q = cu_seqlens_q;
   p.cu_kv = cu_seqlens_kv;
+  p.sched = smla::kWholeUnits;
+  p.ctas = prefill_ctas(total_q, h_q, sms);
   return launch_fwd(p, cs);
 }
 
@@ -194,10 +210,9 @@ size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v,
   int sms = 0;
   if (device_setup(&sms) != SPARSE_MLA_OK) return 0;
   const long long n_tok = static_cast<long long>(batch) * s_next;
-  const int splits = plan_splits(n_tok, h_q, topk, sms);
-  if (splits <= 1) return 0;
-  return static_cast<size_t>(splits) * static_cast<size_t>(n_tok) * static_cast<size_t>(h_q) *
-         (static_cast<size_t>(smla::kDv) + 1) * sizeof(float);
+  const int ctas = decode_ctas(n_tok, h_q, topk, sms);
+  if (ctas <= 1) return 0;   // one CTA runs every unit whole
+  return decode_part_floats(ctas, h_q) * sizeof(float);
 }
 
 sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
@@ -219,10 +234,10 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (num_blocks == 0 || max_blocks == 0) return launch_fill(out, lse, n_tok * h_q, cs);
   if (!kv_cache || !aligned(kv_cache, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
-  const int splits = plan_splits(n_tok, h_q, topk, sms);
+  const int ctas = decode_ctas(n_tok, h_q, topk, sms);
   const size_t need = sparse_mla_decode_workspace_size(batch, s_next, h_q, d_v, topk);
-  if (splits > 1 && (workspace_bytes < need || !workspace)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
-  if (splits > 1 && !aligned(workspace, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (need > 0 && (workspace_bytes < need || !workspace)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !aligned(workspace, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
   FwdParams p = base_params(q, indices, sm_scale, out, lse, static_cast<int>(n_tok), h_q, topk);
   p.kv = static_cast<const __nv_bfloat16*>(kv_cache);
   p.mode = smla::kPaged;
@@ -234,18 +249,20 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
   p.num_blocks = num_blocks;
   p.block_table = block_table;
   p.seqlens = cache_seqlens;
-  p.splits = splits;
-  if (splits > 1) {
+  p.sched = smla::kBlockRanges;
+  p.ctas = ctas;
+  if (need > 0) {
     float* ws = static_cast<float*>(workspace);
     p.part_o = ws;
-    p.part_lse = ws + static_cast<size_t>(splits) * n_tok * h_q * smla::kDv;
+    p.part_lse = ws + 2 * static_cast<size_t>(ctas) * p.part_rows * smla::kDv;
   }
   if ((st = launch_fwd(p, cs)) != SPARSE_MLA_OK) return st;
-  if (splits > 1) {
+  if (need > 0) {
+    // Units cut between CTAs: merge their pieces (rows of whole units are
+    // final already and skipped).
     const int n_th = static_cast<int>(n_tok * h_q);
     const int blocks = (n_th + smla::kCombineRows - 1) / smla::kCombineRows;
-    smla::combine_splits_kernel<<<blocks, 32 * smla::kCombineRows, 0, cs>>>(
-        p.part_o, p.part_lse, static_cast<__nv_bfloat16*>(out), lse, n_th, splits);
+    smla::combine_splits_kernel<<<blocks, 32 * smla::kCombineRows, 0, cs>>>(p);
     if (cudaGetLastError() != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
   }
   return SPARSE_MLA_OK;

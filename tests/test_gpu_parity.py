@@ -196,6 +196,34 @@ def test_decode_page16_wide_heads(smla):
     _check_decode(smla, case)
 
 
+def test_decode_one_token_cut_over_many_ctas(smla):
+    """A single decode token: its 32 blocks are spread over many CTAs, each
+    leaving a partial result, and merged."""
+    case = mi.decode_case(604, batch=1, s_next=1, h_q=8, lo=9000, hi=9001, topk=2048, spare_pages=2)
+    _check_decode(smla, case)
+
+
+def test_decode_two_head_groups_mostly_empty_pieces(smla):
+    """h_q = 128 (two 64-head units per token) over short caches: most of
+    each list is -1, so most CTAs' pieces hold no valid entry (empty partials
+    with LSE = -inf) and a unit's pieces mix empty and full ones."""
+    case = mi.decode_case(605, batch=3, s_next=2, h_q=128, lo=2, hi=200, topk=2048, page=16, spare_pages=2)
+    _check_decode(smla, case)
+
+
+def test_prefill_several_units_per_cta_with_empty_lists(smla):
+    """More tokens than SMs, so each CTA runs several units back to back
+    (reusing Q and its output staging in turn); every third list is empty."""
+    case = mi.prefill_case(406, s_q=700, s_kv=900, h_q=64, topk=256)
+    idx = case.indices.clone()
+    idx[::3] = -1
+    kv = mi.poison_unreferenced(case.kv, torch.unique(idx[idx >= 0]))
+    o, l = _run_fwd(smla, case, kv, idx)
+    ref_o, ref_l = orc.sparse_mla_fwd(case.q, kv, idx, case.sm_scale)
+    compare(o, l, ref_o, ref_l, "several units per CTA")
+    assert np.all(o[::3] == 0.0) and np.all(np.isneginf(l[::3]))
+
+
 def test_decode_dirty_workspace(smla):
     """The workspace arrives with arbitrary contents (here every byte 0xFF):
     a call may read nothing from it that it did not write itself.  Run twice

@@ -1077,6 +1077,9 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = m.tmem_base;
+  // A dependent launch (the decode merge) may place its CTAs once every CTA
+  // of this grid has started.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (m.prior_error == 0) {
     if (warp < kProducerWarps) {
@@ -1121,6 +1124,10 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
 // final already and skipped.
 constexpr int kCombineRows = 8;   // rows (warps) per 256-thread block
 __global__ void __launch_bounds__(32 * kCombineRows) combine_splits_kernel(const __grid_constant__ FwdParams p) {
+  // Launched as a programmatic dependent of the forward grid: its CTAs may be
+  // placed early (they need no shared memory) and wait here until that grid
+  // has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int row = static_cast<int>(blockIdx.x) * kCombineRows + static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
   if (row >= p.n_tok * p.h_q) return;

@@ -234,6 +234,9 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (num_blocks == 0 || max_blocks == 0) return launch_fill(out, lse, n_tok * h_q, cs);
   if (!kv_cache || !aligned(kv_cache, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  // The kernel forms c * (units x blocks) in 64 bits for c up to the grid size.
+  if (n_tok * head_groups(h_q) * blocks_per_list(topk) > (1LL << 62) / (sms > 0 ? sms : 1))
+    return SPARSE_MLA_ERR_INVALID_ARG;
   const int ctas = decode_ctas(n_tok, h_q, topk, sms);
   const size_t need = sparse_mla_decode_workspace_size(batch, s_next, h_q, d_v, topk);
   if (need > 0 && (workspace_bytes < need || !workspace)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
@@ -261,9 +264,17 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
     // Units cut between CTAs: merge their pieces (rows of whole units are
     // final already and skipped).
     const int n_th = static_cast<int>(n_tok * h_q);
-    const int blocks = (n_th + smla::kCombineRows - 1) / smla::kCombineRows;
-    smla::combine_splits_kernel<<<blocks, 32 * smla::kCombineRows, 0, cs>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((n_th + smla::kCombineRows - 1) / smla::kCombineRows));
+    cfg.blockDim = dim3(32 * smla::kCombineRows);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = cs;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap its launch with the forward tail
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, smla::combine_splits_kernel, p) != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
   }
   return SPARSE_MLA_OK;
 }

@@ -31,6 +31,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -52,6 +53,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log", default=None,
+                    help="directory for the nvidia-smi clock CSV of the run (default: the system temp dir)")
     return ap.parse_args()
 
 
@@ -179,15 +182,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir: str):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.log_dir = log_dir
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            os.makedirs(self.log_dir, exist_ok=True)
+            self.path = os.path.join(self.log_dir, f"clocks_rank{self.gpu}.csv")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -434,7 +438,7 @@ def run_ours(args, rank, world, dist):
         call(inputs)
     torch.cuda.synchronize(dev)
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, args.clock_log or tempfile.gettempdir())
     nvml = NvmlClockSampler(dev)
     sampler.start()
     barrier()

@@ -42,7 +42,9 @@ invariance to index order and to -1 padding, closed forms (single valid
 entry, zero query, duplicated entry, all masked) and the logsumexp
 definition.  Packed and paged variants are pinned against dense causal
 attention per sequence and against the dense-layout oracle on a linearised
-cache.
+cache.  The indices-free causal mode is pinned against torch's
+scaled_dot_product_attention (causal, and with an explicit bottom-right mask
+when the queries are the last s_q of s_kv positions).
 """
 from __future__ import annotations
 
@@ -183,6 +185,29 @@ def sparse_mla_decode(q, kv_cache, block_table, cache_seqlens, indices, sm_scale
         outs.append(o)
         lses.append(l)
     return _stack(outs, lses, h, d_v)
+
+
+def causal_mla_fwd(q, kv, sm_scale: float, d_v: int = 512,
+                   tokens: Optional[Iterable[int]] = None):
+    """Indices-free causal forward, the short-prefill case where every causal
+    position is selected ("feat: add XTuner TileLang sparse MLA backend",
+    Summary: short prefill keeps DSA index production; with s <= topk the
+    top-k list of token t is all of positions 0..t).  q [s_q,h,576], kv
+    [s_kv,576].  Query t sits at position t + s_kv - s_q (the queries are the
+    last s_q positions) and attends to every KV row at or before it; a query
+    before position 0 attends to nothing.  Returns float64 (out, lse)."""
+    s_q = q.shape[0]
+    kv2 = kv.reshape(kv.shape[0], -1)
+    s_kv = kv2.shape[0]
+    toks = range(s_q) if tokens is None else list(tokens)
+    outs, lses = [], []
+    for t in toks:
+        last = t + s_kv - s_q
+        r = np.arange(0, max(0, min(last + 1, s_kv)), dtype=np.int64)
+        o, l = attend(_f64(q[t]), _gather(kv2, r), sm_scale, d_v)
+        outs.append(o)
+        lses.append(l)
+    return _stack(outs, lses, q.shape[1], d_v)
 
 
 def valid_count_dense(indices, s_kv: int) -> np.ndarray:

@@ -384,6 +384,126 @@ def test_pins_catch_planted_mistake(monkeypatch, name, fn):
     assert failed >= 1, f"no pin caught the planted mistake {fn.__name__}"
 
 
+# ---------------------------------------------------------------------------
+# indices-free causal mode
+# ---------------------------------------------------------------------------
+
+def _bottom_right_sdpa(q, kv, scale):
+    """float64 attention of the s_q queries, taken as the last s_q of s_kv
+    positions, over every KV position at or before their own, through
+    torch's scaled_dot_product_attention with an explicit mask; plus the LSE
+    from scipy's logsumexp over the same mask."""
+    s_q, h = q.shape[0], q.shape[1]
+    s_kv = kv.shape[0]
+    mask = np.arange(s_kv)[None, :] <= (np.arange(s_q) + s_kv - s_q)[:, None]      # [s_q, s_kv]
+    qq = q.double().permute(1, 0, 2)[None]
+    kk = kv.double()[None, None].expand(1, h, s_kv, D)
+    vv = kv.double()[:, :DV][None, None].expand(1, h, s_kv, DV)
+    ref = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=torch.from_numpy(mask), scale=scale)
+    sc = scale * np.einsum("thd,kd->thk", q.double().numpy(), kv.double().numpy())
+    sc = np.where(mask[:, None, :], sc, -np.inf)
+    return ref[0].permute(1, 0, 2).numpy(), sp_logsumexp(sc, axis=-1), mask
+
+
+def pin_causal_square():
+    s, h = 40, 4
+    q, kv = _qkv(31, s, s, h)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = orc.causal_mla_fwd(q, kv, scale, DV)
+    qq = q.double().permute(1, 0, 2)[None]
+    kk = kv.double()[None, None].expand(1, h, s, D)
+    vv = kv.double()[:, :DV][None, None].expand(1, h, s, DV)
+    ref = F.scaled_dot_product_attention(qq, kk, vv, is_causal=True, scale=scale)
+    _close(out, ref[0].permute(1, 0, 2).numpy(), rtol=1e-9, atol=1e-11)
+    ref_o, ref_l, _ = _bottom_right_sdpa(q, kv, scale)
+    _close(lse, ref_l, rtol=1e-11, atol=1e-11)
+
+
+def pin_causal_queries_are_the_last_positions():
+    s_q, s_kv, h = 13, 50, 3
+    q, kv = _qkv(32, s_q, s_kv, h)
+    scale = 0.05
+    out, lse = orc.causal_mla_fwd(q, kv, scale, DV)
+    ref_o, ref_l, _ = _bottom_right_sdpa(q, kv, scale)
+    _close(out, ref_o, rtol=1e-9, atol=1e-11)
+    _close(lse, ref_l, rtol=1e-11, atol=1e-11)
+
+
+def pin_causal_queries_before_the_first_position():
+    """More queries than KV rows: the first s_q - s_kv attend to nothing."""
+    s_q, s_kv, h = 10, 4, 2
+    q, kv = _qkv(33, s_q, s_kv, h)
+    out, lse = orc.causal_mla_fwd(q, kv, 0.07, DV)
+    assert np.all(out[:6] == 0.0) and np.all(np.isneginf(lse[:6]))
+    ref_o, ref_l, _ = _bottom_right_sdpa(q[6:], kv, 0.07)
+    _close(out[6:], ref_o, rtol=1e-9, atol=1e-11)
+    _close(lse[6:], ref_l, rtol=1e-11, atol=1e-11)
+
+
+def pin_causal_equals_full_causal_lists():
+    """The mode is the sparse forward given every causal position as its list."""
+    s_q, s_kv, h = 9, 20, 2
+    q, kv = _qkv(34, s_q, s_kv, h)
+    idx = torch.full((s_q, s_kv), -1, dtype=torch.int32)
+    for t in range(s_q):
+        idx[t, : t + s_kv - s_q + 1] = torch.arange(t + s_kv - s_q + 1, dtype=torch.int32)
+    o1, l1 = orc.causal_mla_fwd(q, kv, 0.04, DV)
+    o2, l2 = orc.sparse_mla_fwd(q, kv, idx, 0.04, DV)
+    _close(o1, o2, rtol=1e-13, atol=1e-14)
+    _close(l1, l2, rtol=1e-13, atol=1e-14)
+
+
+CAUSAL_PINS = [pin_causal_square, pin_causal_queries_are_the_last_positions,
+               pin_causal_queries_before_the_first_position, pin_causal_equals_full_causal_lists]
+
+
+@pytest.mark.parametrize("pin", CAUSAL_PINS, ids=[p.__name__ for p in CAUSAL_PINS])
+def test_causal_pin(pin):
+    pin()
+
+
+def _causal_off_by_one(q, kv, sm_scale, d_v=512, tokens=None):
+    s_q, s_kv = q.shape[0], kv.shape[0]
+    outs, lses = [], []
+    for t in range(s_q):
+        r = np.arange(0, max(0, min(t + s_kv - s_q, s_kv)), dtype=np.int64)    # position t itself left out
+        o, l = orc.attend(orc._f64(q[t]), orc._gather(kv, r), sm_scale, d_v)
+        outs.append(o)
+        lses.append(l)
+    return orc._stack(outs, lses, q.shape[1], d_v)
+
+
+def _causal_top_left(q, kv, sm_scale, d_v=512, tokens=None):
+    s_q, s_kv = q.shape[0], kv.shape[0]
+    outs, lses = [], []
+    for t in range(s_q):
+        r = np.arange(0, min(t + 1, s_kv), dtype=np.int64)                        # queries taken as the first positions
+        o, l = orc.attend(orc._f64(q[t]), orc._gather(kv, r), sm_scale, d_v)
+        outs.append(o)
+        lses.append(l)
+    return orc._stack(outs, lses, q.shape[1], d_v)
+
+
+_TRUE_CAUSAL = orc.causal_mla_fwd
+
+
+def _causal_unscaled(q, kv, sm_scale, d_v=512, tokens=None):
+    return _TRUE_CAUSAL(q, kv, 1.0, d_v, tokens)
+
+
+@pytest.mark.parametrize("fn", [_causal_off_by_one, _causal_top_left, _causal_unscaled],
+                         ids=lambda f: f.__name__)
+def test_causal_pins_catch_planted_mistake(monkeypatch, fn):
+    monkeypatch.setattr(orc, "causal_mla_fwd", fn)
+    failed = 0
+    for pin in CAUSAL_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1, f"no pin caught the planted mistake {fn.__name__}"
+
+
 def test_generator_valid_row_counts():
     """Valid-entry totals of the workloads equal their closed forms:
     sum_i min(i+1, 2048) per sequence; 96*2048 for the decode batch."""

@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--causal", action="store_true",
+                    help="time the indices-free causal entry point on the q/kv of a dense prefill config (1-3); "
+                         "FLOPs and bytes then count every causal position")
     ap.add_argument("--clock-log", default=None,
                     help="directory for the nvidia-smi clock CSV of the run (default: the system temp dir)")
     return ap.parse_args()
@@ -374,16 +377,22 @@ def run_ours(args, rank, world, dist):
 
     # The oracle pool (spawn) starts before the first GPU work.
     pool = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.causal:
         pool = OraclePool(args.config, os.cpu_count() or 1)
 
     case = workload(args.config)
     stream = torch.cuda.current_stream(dev)
     is_decode = hasattr(case, "kv_cache")
     is_varlen = hasattr(case, "cu_seqlens_q")
+    if args.causal and (is_decode or is_varlen):
+        raise SystemExit("--causal needs a dense prefill config (1-3)")
     n_tok = case.batch * case.s_next if is_decode else case.q.shape[0]
     flops = step_flops(case)
     valid = valid_entries(case)
+    if args.causal:
+        s_q, s_kv = case.q.shape[0], case.kv.shape[0]
+        valid = sum(max(0, min(s_kv, t + s_kv - s_q + 1)) for t in range(s_q))
+        flops = 2.0 * case.q.shape[1] * 1088 * valid
     kv_bytes = valid * KV_ROW_BYTES
 
     # device-resident inputs
@@ -396,6 +405,8 @@ def run_ours(args, rank, world, dist):
     elif is_varlen:
         inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices), cuq=d(case.cu_seqlens_q),
                       cuk=d(case.cu_seqlens_kv))
+    elif args.causal:
+        inputs = dict(q=d(case.q), kv=d(case.kv))
     else:
         inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices))
     h_q = case.h_q if is_decode else case.q.shape[1]
@@ -410,6 +421,8 @@ def run_ours(args, rank, world, dist):
         elif is_varlen:
             smla.sparse_mla_fwd_varlen(inp["q"], inp["kv"], inp["idx"], inp["cuq"], inp["cuk"], case.sm_scale,
                                        out=out, lse=lse, stream=stream)
+        elif args.causal:
+            smla.sparse_mla_fwd_causal(inp["q"], inp["kv"], case.sm_scale, out=out, lse=lse, stream=stream)
         else:
             smla.sparse_mla_fwd(inp["q"], inp["kv"], inp["idx"], case.sm_scale, out=out, lse=lse, stream=stream)
 
@@ -493,14 +506,14 @@ def run_ours(args, rank, world, dist):
     if bound == "hbm":
         achieved = kv_bytes / (fwd_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": p_bw, "unit": "GB/s",
-                    "frac": achieved / p_bw, "traffic": profiled_traffic(args.config),
+                    "frac": achieved / p_bw, "traffic": None if args.causal else profiled_traffic(args.config),
                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                     "algorithmic_bytes_per_launch": kv_bytes,
                     "note": "achieved = valid entries x 1152 B / mean launch time (cold L2)"}
     else:
         achieved = flops / (fwd_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": p_tf, "unit": "TFLOP/s",
-                    "frac": achieved / p_tf, "traffic": profiled_traffic(args.config),
+                    "frac": achieved / p_tf, "traffic": None if args.causal else profiled_traffic(args.config),
                     "peak_kind": f"{peak_kind} bf16 (burst)", "algorithmic_flops_per_launch": flops}
 
     cpu = None
@@ -512,11 +525,13 @@ def run_ours(args, rank, world, dist):
         pool.close()
 
     line = {
-        "metric": "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)",
+        "metric": ("indices-free causal MLA fwd TFLOP/s (every causal position)" if args.causal
+                   else "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)"),
         "value": whole_job_tflops(flops, args.steps, world, total_ms), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(case, args.config), "seed": 1000 + args.config,
+        "config": {"workload": workload_name(case, args.config) + (" (indices-free causal mode)" if args.causal else ""),
+                   "seed": 1000 + args.config,
                    "l2": "256 MB buffer written before every timed step (cold L2)",
                    "parallelism": f"replicas x{world}"},
         "us_per_call": us, "tflops_per_gpu": tflops, "gathered_kv_GBps": gbs,

@@ -84,6 +84,25 @@ sparse_mla_status_t sparse_mla_fwd(const void* q, const void* kv, const int32_t*
                                    int topk, void* stream);
 
 /*
+ * Indices-free causal forward for short prefill, where the top-k selection
+ * keeps every causal position ("feat: add XTuner TileLang sparse MLA
+ * backend", Summary: short prefill), so no index tensor is needed.  The s_q
+ * queries are the last s_q of the s_kv positions: query t attends to every
+ * kv row at or before position t + s_kv - s_q (a query before position 0
+ * attends to nothing: out = 0, LSE = -inf).  The result equals
+ * sparse_mla_fwd given those positions as each token's list.
+ *
+ *   q        bf16 [s_q, h_q, d_qk]
+ *   kv       bf16 [s_kv, d_qk]
+ *   out      bf16 [s_q, h_q, d_v]   written
+ *   lse      fp32 [s_q, h_q]        written, natural log
+ *
+ * s_q == 0 is a no-op.  s_kv == 0 masks everything.
+ */
+sparse_mla_status_t sparse_mla_fwd_causal(const void* q, const void* kv, float sm_scale, void* out, float* lse,
+                                          int s_q, int s_kv, int h_q, int d_qk, int d_v, void* stream);
+
+/*
  * Packed (varlen) prefill: `batch` sequences concatenated along the token
  * axis.  Token t belongs to the sequence b with cu_seqlens_q[b] <= t <
  * cu_seqlens_q[b+1]; its indices are LOCAL to that sequence: entry i reads

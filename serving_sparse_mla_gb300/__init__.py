@@ -9,5 +9,6 @@ from .binding import (  # noqa: F401
     set_wait_timeout_ns,
     sparse_mla_decode,
     sparse_mla_fwd,
+    sparse_mla_fwd_causal,
     sparse_mla_fwd_varlen,
 )

@@ -27,6 +27,8 @@ STATUS = {0: "SPARSE_MLA_OK", 1: "SPARSE_MLA_ERR_INVALID_ARG", 2: "SPARSE_MLA_ER
 SIGNATURES = {
     "sparse_mla_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_float, c_void_p, c_void_p,
                                c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "sparse_mla_fwd_causal": (c_int, [c_void_p, c_void_p, c_float, c_void_p, c_void_p,
+                                      c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "sparse_mla_fwd_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_float,
                                       c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "sparse_mla_decode_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
@@ -116,6 +118,28 @@ def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_
     st = lib.sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), float(sm_scale), _ptr(out), _ptr(lse),
                             s_q, s_kv, h_q, d_qk, d_v, topk, _stream(stream))
     _check(st, "sparse_mla_fwd")
+    return out, lse
+
+
+def sparse_mla_fwd_causal(q: torch.Tensor, kv: torch.Tensor, sm_scale: float,
+                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Indices-free causal forward: q [s_q,h_q,576] bf16 (the last s_q of the
+    s_kv positions), kv [s_kv,576] or [s_kv,1,576] bf16 -> (out [s_q,h_q,512]
+    bf16, lse [s_q,h_q] fp32)."""
+    lib = load()
+    s_q, h_q, d_qk = q.shape
+    s_kv = kv.shape[0]
+    for t, dt, n in ((q, torch.bfloat16, "q"), (kv, torch.bfloat16, "kv")):
+        _need(t, dt, n)
+    d_v = 512
+    if out is None:
+        out = torch.empty((s_q, h_q, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=q.device)
+    st = lib.sparse_mla_fwd_causal(_ptr(q), _ptr(kv), float(sm_scale), _ptr(out), _ptr(lse),
+                                   s_q, s_kv, h_q, d_qk, d_v, _stream(stream))
+    _check(st, "sparse_mla_fwd_causal")
     return out, lse
 
 

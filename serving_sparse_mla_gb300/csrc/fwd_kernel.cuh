@@ -95,7 +95,11 @@ __host__ __device__ constexpr int softmax_warp0(int g) { return g == 0 ? 5 : 10;
 constexpr float kLazyRescale = 8.0f;         // log2 units
 constexpr int kMaxSmem = 232448;
 
-enum Mode : int { kDense = 0, kVarlen = 1, kPaged = 2 };
+// kCausal: dense rows without an index tensor; entry e of token t's list is
+// position e while e <= t + causal_off (every causal position selected, the
+// short-prefill case of "feat: add XTuner TileLang sparse MLA backend",
+// Summary), else masked.
+enum Mode : int { kDense = 0, kVarlen = 1, kPaged = 2, kCausal = 3 };
 
 // How units (token x head group) are dealt to the persistent CTAs:
 //   kWholeUnits   CTA c runs units c, c + G, c + 2G, ... whole (prefill).
@@ -123,6 +127,7 @@ struct FwdParams {
   int n_tok, h_q, topk, mode;
   int n_rows;               // rows of kv
   int s_kv, batch, s_next, page_size, max_blocks, num_blocks;
+  int causal_off;           // kCausal: s_kv - s_q (query t sits at position t + causal_off)
   int sched;                // kWholeUnits or kBlockRanges
   int groups;               // head groups of up to 64 (a unit is one token x one group)
   int nb;                   // 64-entry blocks per index list
@@ -254,7 +259,7 @@ struct TokCtx {
 __device__ __forceinline__ TokCtx token_context(const FwdParams& p, int tok) {
   TokCtx c;
   c.table = nullptr;
-  if (p.mode == kDense) {
+  if (p.mode == kDense || p.mode == kCausal) {
     c.kv_lo = 0;
     c.kv_len = p.s_kv;
   } else if (p.mode == kVarlen) {
@@ -272,6 +277,13 @@ __device__ __forceinline__ TokCtx token_context(const FwdParams& p, int tok) {
     c.table = p.block_table + static_cast<size_t>(b) * p.max_blocks;
   }
   return c;
+}
+
+// Entry e (< topk) of a token's index list: read from the list, or in the
+// causal mode the position itself while it is at or before the token's own
+// position `last` (no memory read).
+__device__ __forceinline__ int index_at(const FwdParams& p, const int32_t* irow, int last, int e) {
+  return p.mode == kCausal ? (e <= last ? e : -1) : __ldg(irow + e);
 }
 
 // KV row read by one index entry, or -1 when the entry is masked.
@@ -408,7 +420,8 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
     const int tok = item.unit / p.groups;
     const int jb = item.jb, je = item.je;
     const TokCtx ctx = token_context(p, tok);
-    const int32_t* irow = p.indices + static_cast<size_t>(tok) * p.topk;
+    const int32_t* irow = p.mode == kCausal ? nullptr : p.indices + static_cast<size_t>(tok) * p.topk;
+    const int last = tok + p.causal_off;   // kCausal only
     for (int wb = jb; wb < je; wb += 32, ++win) {
       // Candidate blocks of this window of up to 32: a block none of whose
       // entries lies in [0, kv_len) is skipped without mapping its rows (a
@@ -425,7 +438,7 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
         for (int i = 0; i < 16; ++i) {
           const int blk = b0 + (i >> 1);
           const int e = blk * kBlk + (i & 1) * 32 + lane;
-          v[i] = (blk < we && e < p.topk) ? __ldg(irow + e) : -1;
+          v[i] = (blk < we && e < p.topk) ? index_at(p, irow, last, e) : -1;
         }
         uint32_t bits = 0;
 #pragma unroll
@@ -448,7 +461,7 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int e = j_next * kBlk + lane * 2 + i;
-        idx_next[i] = (j_next >= 0 && e < p.topk) ? __ldg(irow + e) : -1;
+        idx_next[i] = (j_next >= 0 && e < p.topk) ? index_at(p, irow, last, e) : -1;
       }
       while (j_next >= 0) {
         const int j = j_next;
@@ -460,7 +473,7 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {   // prefetch the next candidate's indices
           const int e = j_next * kBlk + lane * 2 + i;
-          idx_next[i] = (j_next >= 0 && e < p.topk) ? __ldg(irow + e) : -1;
+          idx_next[i] = (j_next >= 0 && e < p.topk) ? index_at(p, irow, last, e) : -1;
         }
         const uint32_t bal0 = __ballot_sync(0xffffffffu, rows[0] >= 0);
         const uint32_t bal1 = __ballot_sync(0xffffffffu, rows[1] >= 0);

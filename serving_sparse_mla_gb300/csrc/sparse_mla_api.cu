@@ -140,13 +140,13 @@ FwdParams base_params(const void* q, const int32_t* indices, float sm_scale, voi
 }
 
 sparse_mla_status_t check_common(const void* q, const int32_t* indices, const void* out, const float* lse,
-                                 long long n_tok, int h_q, int d_qk, int d_v, int topk) {
+                                 long long n_tok, int h_q, int d_qk, int d_v, int topk, bool need_indices = true) {
   if (n_tok < 0 || h_q < 1 || topk < 1) return SPARSE_MLA_ERR_INVALID_ARG;
   if (d_qk != smla::kDqk || d_v != smla::kDv) return SPARSE_MLA_ERR_UNSUPPORTED_SHAPE;
   if (n_tok > INT_MAX / 2 || static_cast<long long>(h_q) * 64 > INT_MAX) return SPARSE_MLA_ERR_INVALID_ARG;
   if (n_tok == 0) return SPARSE_MLA_OK;
-  if (!q || !indices || !out || !lse) return SPARSE_MLA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(indices, 4) || !aligned(lse, 4))
+  if (!q || (need_indices && !indices) || !out || !lse) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || (need_indices && !aligned(indices, 4)) || !aligned(lse, 4))
     return SPARSE_MLA_ERR_INVALID_ARG;
   return SPARSE_MLA_OK;
 }
@@ -202,6 +202,30 @@ sparse_mla_status_t sparse_mla_fwd_varlen(const void* q, const void* kv, const i
   p.cu_kv = cu_seqlens_kv;
   p.sched = smla::kWholeUnits;
   p.ctas = prefill_ctas(total_q, h_q, sms);
+  return launch_fwd(p, cs);
+}
+
+sparse_mla_status_t sparse_mla_fwd_causal(const void* q, const void* kv, float sm_scale, void* out, float* lse,
+                                          int s_q, int s_kv, int h_q, int d_qk, int d_v, void* stream) {
+  if (s_kv < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  // A token's list holds every KV position: topk = s_kv (at least 1 for the
+  // shape checks; s_kv = 0 is the all-masked case below).
+  sparse_mla_status_t st = check_common(q, nullptr, out, lse, s_q, h_q, d_qk, d_v, s_kv > 0 ? s_kv : 1, false);
+  if (st != SPARSE_MLA_OK) return st;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (s_q == 0) return SPARSE_MLA_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (s_kv == 0) return launch_fill(out, lse, static_cast<long long>(s_q) * h_q, cs);
+  if (!kv || !aligned(kv, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  FwdParams p = base_params(q, nullptr, sm_scale, out, lse, s_q, h_q, s_kv);
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
+  p.mode = smla::kCausal;
+  p.n_rows = s_kv;
+  p.s_kv = s_kv;
+  p.causal_off = s_kv - s_q;
+  p.sched = smla::kWholeUnits;
+  p.ctas = prefill_ctas(s_q, h_q, sms);
   return launch_fwd(p, cs);
 }
 

@@ -67,6 +67,22 @@ def test_host_validation_codes(lib):
     assert _fwd(lib, idx=18) == 1    # not 4-byte aligned
 
 
+def test_causal_validation(lib):
+    def causal(**kw):
+        a = dict(q=16, kv=16, scale=0.1, out=16, lse=16, s_q=4, s_kv=8, h_q=8, d_qk=576, d_v=512, stream=None)
+        a.update(kw)
+        return lib.sparse_mla_fwd_causal(a["q"], a["kv"], a["scale"], a["out"], a["lse"], a["s_q"], a["s_kv"],
+                                         a["h_q"], a["d_qk"], a["d_v"], a["stream"])
+    assert causal(d_qk=512) == 2
+    assert causal(d_v=256) == 2
+    assert causal(h_q=0) == 1
+    assert causal(s_q=-1) == 1
+    assert causal(s_kv=-1) == 1
+    assert causal(q=None) == 1
+    assert causal(out=None) == 1
+    assert causal(q=24) == 1      # not 16-byte aligned
+
+
 def test_varlen_and_decode_validation(lib):
     st = lib.sparse_mla_fwd_varlen(16, 16, 16, None, None, 1, 0.1, 16, 16, 4, 4, 8, 576, 512, 64, None)
     assert st == 1

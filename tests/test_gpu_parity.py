@@ -139,6 +139,35 @@ def test_wide_head_config_sampled(smla):
     _check_fwd(smla, case, tokens=toks)
 
 
+# ---------------------------------------------------------------- indices-free causal mode
+
+@pytest.mark.parametrize("s_q,s_kv,h_q", [(64, 64, 8), (300, 300, 8), (100, 700, 64), (37, 20, 16), (1, 2500, 8)])
+def test_causal_mode(smla, s_q, s_kv, h_q):
+    """Every query attends to all KV positions at or before its own (queries
+    are the last s_q positions; with s_q > s_kv the first ones see nothing);
+    one query over 2500 positions spans two scan windows."""
+    case = mi.prefill_case(800 + s_q, s_q=s_q, s_kv=s_kv, h_q=h_q, topk=64)
+    out, lse = smla.sparse_mla_fwd_causal(case.q.to(DEV), case.kv.to(DEV), case.sm_scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = orc.causal_mla_fwd(case.q, case.kv, case.sm_scale)
+    compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, f"causal {s_q}x{s_kv}")
+
+
+def test_causal_mode_equals_sparse_with_full_causal_lists(smla):
+    """The causal mode walks the same blocks as the sparse forward given each
+    token's causal positions in order, so the two agree bit for bit."""
+    s = 300
+    case = mi.prefill_case(810, s_q=s, s_kv=s, h_q=8, topk=64)
+    idx = torch.full((s, s), -1, dtype=torch.int32)
+    for t in range(s):
+        idx[t, : t + 1] = torch.arange(t + 1, dtype=torch.int32)
+    q, kv = case.q.to(DEV), case.kv.to(DEV)
+    o1, l1 = smla.sparse_mla_fwd_causal(q, kv, case.sm_scale)
+    o2, l2 = smla.sparse_mla_fwd(q, kv, idx.to(DEV), case.sm_scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 # ---------------------------------------------------------------- packed prefill
 
 def _check_varlen(smla, case, tokens=None, what=""):

@@ -44,7 +44,9 @@ definition.  Packed and paged variants are pinned against dense causal
 attention per sequence and against the dense-layout oracle on a linearised
 cache.  The indices-free causal mode is pinned against torch's
 scaled_dot_product_attention (causal, and with an explicit bottom-right mask
-when the queries are the last s_q of s_kv positions).
+when the queries are the last s_q of s_kv positions).  The backward is pinned
+against torch autograd through an independent dense formulation of the
+forward, and against central finite differences on a tiny case.
 """
 from __future__ import annotations
 
@@ -208,6 +210,53 @@ def causal_mla_fwd(q, kv, sm_scale: float, d_v: int = 512,
         outs.append(o)
         lses.append(l)
     return _stack(outs, lses, q.shape[1], d_v)
+
+
+def sparse_mla_bwd(q, kv, indices, sm_scale: float, dout, d_v: int = 512):
+    """Gradients of the dense-layout forward with respect to q and kv, given
+    the upstream gradient dout of out (the LSE output carries no gradient).
+
+    The backward the training users pair with the forward (prime-rl page:
+    forward and backward sparse attention timings).  Per token t, with its
+    valid rows K = kv[r] (V = K[:, :512], the same latent rows), from the
+    definition of the forward by the chain rule:
+
+        P  = softmax(sm_scale * q_t K^T)            [h, n]
+        dP = dout_t V^T                             [h, n]
+        D  = rowsum(dout_t * out_t) = rowsum(P * dP)
+        dS = P * (dP - D)
+        dq_t            = sm_scale * dS K
+        dkv[r]         += sm_scale * dS^T q_t       (all 576 columns)
+        dkv[r, :512]   += P^T dout_t
+
+    with multiplicity (a row listed twice receives both contributions).  O and
+    the LSE are recomputed here from q and kv.  Returns float64 dq [s_q,h,576]
+    and dkv [s_kv,576]."""
+    s_q, h = q.shape[0], q.shape[1]
+    kv2 = kv.reshape(kv.shape[0], -1)
+    s_kv, d_qk = kv2.shape
+    idx = _i64(indices).reshape(s_q, -1)
+    q64, do64 = _f64(q), _f64(dout)
+    dq = np.zeros((s_q, h, d_qk))
+    dkv = np.zeros((s_kv, d_qk))
+    for t in range(s_q):
+        r = rows_dense(idx[t], s_kv)
+        if r.size == 0:
+            continue
+        K = _gather(kv2, r)
+        V = K[:, :d_v]
+        s = sm_scale * (q64[t] @ K.T)
+        m = s.max(axis=1, keepdims=True)
+        P = np.exp(s - m)
+        P /= P.sum(axis=1, keepdims=True)
+        O = P @ V
+        dP = do64[t] @ V.T
+        D = (do64[t] * O).sum(axis=1, keepdims=True)
+        dS = P * (dP - D)
+        dq[t] = sm_scale * (dS @ K)
+        np.add.at(dkv, r, sm_scale * (dS.T @ q64[t]))
+        np.add.at(dkv[:, :d_v], r, P.T @ do64[t])
+    return dq, dkv
 
 
 def valid_count_dense(indices, s_kv: int) -> np.ndarray:

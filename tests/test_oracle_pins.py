@@ -504,6 +504,151 @@ def test_causal_pins_catch_planted_mistake(monkeypatch, fn):
     assert failed >= 1, f"no pin caught the planted mistake {fn.__name__}"
 
 
+# ---------------------------------------------------------------------------
+# backward
+# ---------------------------------------------------------------------------
+
+def _autograd_reference(q, kv, idx, scale, dout):
+    """dq, dkv by torch autograd (float64) through a dense formulation of the
+    forward: scores over every kv row plus log(multiplicity of the row in the
+    token's list), softmax, times kv[:, :512]; loss = sum(out * dout) over the
+    tokens that have a valid entry."""
+    s_q, h = q.shape[0], q.shape[1]
+    s_kv = kv.shape[0]
+    qv = q.double().clone().requires_grad_(True)
+    kvv = kv.double().clone().requires_grad_(True)
+    count = torch.zeros((s_q, s_kv), dtype=torch.float64)
+    for t in range(s_q):
+        for i in idx[t].tolist():
+            if 0 <= i < s_kv:
+                count[t, i] += 1
+    live = count.sum(1) > 0
+    scores = scale * torch.einsum("thd,kd->thk", qv, kvv) + torch.log(count)[:, None, :]
+    w = torch.softmax(scores[live], dim=-1)
+    out = w @ kvv[:, :DV]
+    (out * dout.double()[live]).sum().backward()
+    return qv.grad.numpy(), kvv.grad.numpy()
+
+
+def pin_bwd_autograd():
+    s_q, s_kv, h, topk = 9, 23, 3, 12
+    q, kv = _qkv(41, s_q, s_kv, h)
+    g = mi._gen(42)
+    idx = torch.randint(-2, s_kv + 2, (s_q, topk), generator=g, dtype=torch.int32)
+    idx[0] = -1                                   # no valid entry: zero gradient
+    idx[1, :4] = torch.tensor([5, 5, 5, 7], dtype=torch.int32)   # multiplicity
+    dout = torch.randn((s_q, h, DV), generator=g, dtype=torch.float64)
+    scale = 0.0417
+    dq, dkv = orc.sparse_mla_bwd(q, kv, idx, scale, dout, DV)
+    rq, rkv = _autograd_reference(q, kv, idx, scale, dout)
+    _close(dq, rq, rtol=1e-9, atol=1e-12)
+    _close(dkv, rkv, rtol=1e-9, atol=1e-12)
+    assert np.all(dq[0] == 0.0)
+
+
+def pin_bwd_finite_differences():
+    """Central differences of L = sum(out * dout) through the float64 forward
+    oracle, along random directions in q and in kv."""
+    s_q, s_kv, h, topk = 3, 7, 2, 6
+    q, kv = _qkv(43, s_q, s_kv, h)
+    q, kv = q.double(), kv.double()
+    g = mi._gen(44)
+    idx = torch.randint(0, s_kv, (s_q, topk), generator=g, dtype=torch.int32)
+    dout = torch.randn((s_q, h, DV), generator=g, dtype=torch.float64)
+    scale = 0.05
+    dq, dkv = orc.sparse_mla_bwd(q, kv, idx, scale, dout, DV)
+
+    def loss(qq, kk):
+        out, _ = orc.sparse_mla_fwd(qq, kk, idx, scale, DV)
+        return float((out * dout.numpy()).sum())
+    eps = 1e-5
+    for _ in range(3):
+        dqd = torch.randn(q.shape, generator=g, dtype=torch.float64)
+        fd = (loss(q + eps * dqd, kv) - loss(q - eps * dqd, kv)) / (2 * eps)
+        assert abs(fd - float((dq * dqd.numpy()).sum())) <= 1e-6 * (1 + abs(fd)), "dq vs finite differences"
+        dkd = torch.randn(kv.shape, generator=g, dtype=torch.float64)
+        fd = (loss(q, kv + eps * dkd) - loss(q, kv - eps * dkd)) / (2 * eps)
+        assert abs(fd - float((dkv * dkd.numpy()).sum())) <= 1e-6 * (1 + abs(fd)), "dkv vs finite differences"
+
+
+BWD_PINS = [pin_bwd_autograd, pin_bwd_finite_differences]
+
+
+@pytest.mark.parametrize("pin", BWD_PINS, ids=[p.__name__ for p in BWD_PINS])
+def test_bwd_pin(pin):
+    pin()
+
+
+_TRUE_BWD = orc.sparse_mla_bwd
+
+
+def _bwd_variant(drop_d=False, unscaled_dq=False, v_into_rope=False, no_multiplicity=False):
+    def f(q, kv, indices, sm_scale, dout, d_v=512):
+        s_q, h = q.shape[0], q.shape[1]
+        kv2 = kv.reshape(kv.shape[0], -1)
+        s_kv, d_qk = kv2.shape
+        idx = orc._i64(indices).reshape(s_q, -1)
+        q64, do64 = orc._f64(q), orc._f64(dout)
+        dq = np.zeros((s_q, h, d_qk))
+        dkv = np.zeros((s_kv, d_qk))
+        for t in range(s_q):
+            r = orc.rows_dense(idx[t], s_kv)
+            if r.size == 0:
+                continue
+            K = orc._gather(kv2, r)
+            V = K if v_into_rope else K[:, :d_v]
+            s = sm_scale * (q64[t] @ K.T)
+            P = np.exp(s - s.max(axis=1, keepdims=True))
+            P /= P.sum(axis=1, keepdims=True)
+            dP = do64[t] @ K[:, :d_v].T
+            D = 0.0 if drop_d else (do64[t] * (P @ K[:, :d_v])).sum(axis=1, keepdims=True)
+            dS = P * (dP - D)
+            dq[t] = (1.0 if unscaled_dq else sm_scale) * (dS @ K)
+            dk = sm_scale * (dS.T @ q64[t])
+            dv = P.T @ do64[t]
+            if v_into_rope:
+                dv = np.concatenate([dv, dv[:, :d_qk - d_v]], axis=1)
+                dk = dk + dv
+            else:
+                dk[:, :d_v] += dv
+            if no_multiplicity:
+                dkv[r] += dk
+            else:
+                np.add.at(dkv, r, dk)
+        return dq, dkv
+    return f
+
+
+BWD_MUTANTS = [("drop_d", _bwd_variant(drop_d=True)), ("unscaled_dq", _bwd_variant(unscaled_dq=True)),
+               ("v_into_rope", _bwd_variant(v_into_rope=True)), ("no_multiplicity", _bwd_variant(no_multiplicity=True))]
+
+
+@pytest.mark.parametrize("name,fn", BWD_MUTANTS, ids=[m[0] for m in BWD_MUTANTS])
+def test_bwd_pins_catch_planted_mistake(monkeypatch, name, fn):
+    monkeypatch.setattr(orc, "sparse_mla_bwd", fn)
+    failed = 0
+    for pin in BWD_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1, f"no pin caught the planted mistake {name}"
+
+
+def test_bwd_variant_without_mistakes_passes():
+    """The mutation harness itself is faithful: with no mistake planted it
+    reproduces the oracle."""
+    s_q, s_kv, h = 5, 11, 2
+    q, kv = _qkv(45, s_q, s_kv, h)
+    g = mi._gen(46)
+    idx = torch.randint(-1, s_kv, (s_q, 8), generator=g, dtype=torch.int32)
+    dout = torch.randn((s_q, h, DV), generator=g, dtype=torch.float64)
+    a = _TRUE_BWD(q, kv, idx, 0.03, dout, DV)
+    b = _bwd_variant()(q, kv, idx, 0.03, dout, DV)
+    _close(a[0], b[0], rtol=1e-12, atol=1e-14)
+    _close(a[1], b[1], rtol=1e-12, atol=1e-14)
+
+
 def test_generator_valid_row_counts():
     """Valid-entry totals of the workloads equal their closed forms:
     sum_i min(i+1, 2048) per sequence; 96*2048 for the decode batch."""

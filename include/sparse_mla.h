@@ -103,6 +103,29 @@ sparse_mla_status_t sparse_mla_fwd_causal(const void* q, const void* kv, float s
                                           int s_q, int s_kv, int h_q, int d_qk, int d_v, void* stream);
 
 /*
+ * Backward of sparse_mla_fwd: gradients with respect to q and kv for an
+ * upstream gradient dout of out (the LSE output carries no gradient), the
+ * pass the training users pair with the forward (prime-rl cudnn_flashmla
+ * page: sparse-attention forward and backward timings).  Per token, with P
+ * the attention weights over its valid rows K (V = K[:, :512]):
+ *   dS = P * (dout V^T - rowsum(dout * out)),  dq = sm_scale dS K,
+ *   dkv[row] += sm_scale dS^T q  (all 576 columns)  +  P^T dout (first 512).
+ *
+ *   q, kv, indices, sm_scale   as for sparse_mla_fwd
+ *   out      bf16 [s_q, h_q, d_v]   the forward's output
+ *   lse      fp32 [s_q, h_q]        the forward's LSE
+ *   dout     bf16 [s_q, h_q, d_v]
+ *   dq       fp32 [s_q, h_q, d_qk]  written
+ *   dkv      fp32 [s_kv, d_qk]      written (zeroed on the stream, then accumulated)
+ *
+ * Rows listed by several tokens accumulate every contribution (atomic adds:
+ * the summation order, hence the last bits of dkv, varies between calls).
+ */
+sparse_mla_status_t sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const void* out,
+                                   const float* lse, const void* dout, float sm_scale, float* dq, float* dkv,
+                                   int s_q, int s_kv, int h_q, int d_qk, int d_v, int topk, void* stream);
+
+/*
  * Packed (varlen) prefill: `batch` sequences concatenated along the token
  * axis.  Token t belongs to the sequence b with cu_seqlens_q[b] <= t <
  * cu_seqlens_q[b+1]; its indices are LOCAL to that sequence: entry i reads

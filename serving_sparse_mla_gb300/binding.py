@@ -27,6 +27,8 @@ STATUS = {0: "SPARSE_MLA_OK", 1: "SPARSE_MLA_ERR_INVALID_ARG", 2: "SPARSE_MLA_ER
 SIGNATURES = {
     "sparse_mla_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_float, c_void_p, c_void_p,
                                c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "sparse_mla_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float,
+                               c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "sparse_mla_fwd_causal": (c_int, [c_void_p, c_void_p, c_float, c_void_p, c_void_p,
                                       c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "sparse_mla_fwd_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_float,
@@ -119,6 +121,31 @@ def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_
                             s_q, s_kv, h_q, d_qk, d_v, topk, _stream(stream))
     _check(st, "sparse_mla_fwd")
     return out, lse
+
+
+def sparse_mla_bwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_scale: float,
+                   out: torch.Tensor, lse: torch.Tensor, dout: torch.Tensor,
+                   dq: Optional[torch.Tensor] = None, dkv: Optional[torch.Tensor] = None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Gradients of sparse_mla_fwd: q [s_q,h_q,576], kv [s_kv,576], indices
+    [s_q,topk], the forward's out [s_q,h_q,512] bf16 and lse [s_q,h_q] fp32,
+    dout [s_q,h_q,512] bf16 -> (dq [s_q,h_q,576] fp32, dkv [s_kv,576] fp32)."""
+    lib = load()
+    s_q, h_q, d_qk = q.shape
+    s_kv = kv.shape[0]
+    topk = indices.shape[-1]
+    for t, dt, n in ((q, torch.bfloat16, "q"), (kv, torch.bfloat16, "kv"), (indices, torch.int32, "indices"),
+                     (out, torch.bfloat16, "out"), (lse, torch.float32, "lse"), (dout, torch.bfloat16, "dout")):
+        _need(t, dt, n)
+    d_v = 512
+    if dq is None:
+        dq = torch.empty((s_q, h_q, d_qk), dtype=torch.float32, device=q.device)
+    if dkv is None:
+        dkv = torch.empty((s_kv, d_qk), dtype=torch.float32, device=q.device)
+    st = lib.sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(out), _ptr(lse), _ptr(dout), float(sm_scale),
+                            _ptr(dq), _ptr(dkv), s_q, s_kv, h_q, d_qk, d_v, topk, _stream(stream))
+    _check(st, "sparse_mla_bwd")
+    return dq, dkv
 
 
 def sparse_mla_fwd_causal(q: torch.Tensor, kv: torch.Tensor, sm_scale: float,

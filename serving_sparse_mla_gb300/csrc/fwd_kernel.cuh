@@ -134,6 +134,11 @@ struct FwdParams {
   int ctas;                 // CTAs of the (persistent) grid
   int part_rows;            // head rows per partial slot: min(h_q, 64)
   float scale_log2;         // sm_scale * log2(e)
+  float sm_scale;
+  // backward only: out and lse above are the forward's results (inputs)
+  const __nv_bfloat16* dout;  // [n_tok, h_q, 512]
+  float* dq;                  // [n_tok, h_q, 576]
+  float* dkv;                 // [n_rows, 576], accumulated
   unsigned long long timeout_ns;
 };
 
@@ -396,9 +401,12 @@ __device__ __forceinline__ void cp_async_arrive_on(uint32_t bar) {
 
 // ------------------------------------------------------------------ producer
 
-template <int N>
-__device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
-  using L = Layout<N>;
+// The gather producer, shared with the backward kernel: L gives the shared
+// memory layout (ring sizes and offsets), M the barrier block (same member
+// names), and kRows also publishes each block's 64 KV rows (entry r of the
+// block in info_rows[k][r], -1 when masked) for consumers that scatter by row.
+template <int N, class L, class M, bool kRows>
+__device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
   const int warp = static_cast<int>(threadIdx.x >> 5);   // 0..3
   const int lane = static_cast<int>(lane_id());
   const volatile int* ab = &m.abort_flag;
@@ -483,6 +491,11 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
           const int k = ni % kInfoDepth;
           const bool ok = mbar_wait(smem_u32(&m.info_empty[k]), ((ni / kInfoDepth) & 1) ^ 1, deadline, ab);
           if (!__all_sync(0xffffffffu, ok)) return false;
+          if constexpr (kRows) {
+            m.info_rows[k][2 * lane] = rows[0];
+            m.info_rows[k][2 * lane + 1] = rows[1];
+            __syncwarp();
+          }
           if (lane == 0) {
             m.info_blk[k] = j;
             m.info_mask[k][0] = bal0;
@@ -619,6 +632,11 @@ __device__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
     ++ni;
   }
   return true;
+}
+
+template <int N>
+__device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
+  return run_producer_t<N, Layout<N>, Misc, false>(p, m, sbase);
 }
 
 // ------------------------------------------------------------------ MMA issuer

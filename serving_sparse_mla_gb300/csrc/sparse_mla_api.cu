@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "bwd_kernel.cuh"
 #include "fwd_kernel.cuh"
 #include "sparse_mla.h"
 
@@ -52,7 +53,9 @@ sparse_mla_status_t device_setup(int* sm_count) {
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::smem_bytes<32>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smla::smem_bytes<64>()) != cudaSuccess)
+                             smla::smem_bytes<64>()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::sparse_mla_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::bwd_smem_bytes()) != cudaSuccess)
       return SPARSE_MLA_ERR_CUDA;
     st.attrs_set = true;
   }
@@ -131,6 +134,7 @@ FwdParams base_params(const void* q, const int32_t* indices, float sm_scale, voi
   p.h_q = h_q;
   p.topk = topk;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.sm_scale = sm_scale;
   p.groups = head_groups(h_q);
   p.nb = blocks_per_list(topk);
   p.part_rows = part_rows(h_q);
@@ -227,6 +231,43 @@ sparse_mla_status_t sparse_mla_fwd_causal(const void* q, const void* kv, float s
   p.sched = smla::kWholeUnits;
   p.ctas = prefill_ctas(s_q, h_q, sms);
   return launch_fwd(p, cs);
+}
+
+sparse_mla_status_t sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const void* out,
+                                   const float* lse, const void* dout, float sm_scale, float* dq, float* dkv,
+                                   int s_q, int s_kv, int h_q, int d_qk, int d_v, int topk, void* stream) {
+  sparse_mla_status_t st = check_common(q, indices, out, lse, s_q, h_q, d_qk, d_v, topk);
+  if (st != SPARSE_MLA_OK) return st;
+  if (s_kv < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (s_q > 0 && (!dout || !dq || !aligned(dout, 16) || !aligned(dq, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (s_kv > 0 && (!dkv || !aligned(dkv, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // dkv accumulates the contributions of every token that lists a row.
+  if (s_kv > 0 &&
+      cudaMemsetAsync(dkv, 0, static_cast<size_t>(s_kv) * smla::kDqk * sizeof(float), cs) != cudaSuccess)
+    return SPARSE_MLA_ERR_CUDA;
+  if (s_q == 0) return SPARSE_MLA_OK;
+  if (s_kv == 0)
+    return cudaMemsetAsync(dq, 0, static_cast<size_t>(s_q) * h_q * smla::kDqk * sizeof(float), cs) == cudaSuccess
+               ? SPARSE_MLA_OK
+               : SPARSE_MLA_ERR_CUDA;
+  if (!kv || !aligned(kv, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  FwdParams p = base_params(q, indices, sm_scale, const_cast<void*>(out), const_cast<float*>(lse), s_q, h_q, topk);
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
+  p.mode = smla::kDense;
+  p.n_rows = s_kv;
+  p.s_kv = s_kv;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.dq = dq;
+  p.dkv = dkv;
+  p.groups = (h_q + smla::kBwdHeads - 1) / smla::kBwdHeads;   // units of 16 heads
+  p.sched = smla::kWholeUnits;
+  const long long units = static_cast<long long>(s_q) * p.groups;
+  p.ctas = static_cast<int>(units < sms ? units : sms);
+  smla::sparse_mla_bwd_kernel<<<p.ctas, smla::BwdLayout::kThreads, smla::bwd_smem_bytes(), cs>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
 }
 
 size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v, int topk) {

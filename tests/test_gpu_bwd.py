@@ -1,0 +1,106 @@
+"""GPU parity of the backward (sparse_mla_bwd through the C ABI) against the
+float64 oracle's sparse_mla_bwd on the same seeded inputs.  The forward's
+out / lse fed to the backward come from the CUDA forward, as in training."""
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+from oracle import sparse_mla_oracle as orc
+from tests.parity import bf16_rounding_err, compare_grad, forward_parity_err, grad_term_bounds
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def smla(cuda_lib):
+    import serving_sparse_mla_gb300 as pkg
+    pkg.clear_device_error()
+    yield pkg
+    assert pkg.get_device_error() == 0
+
+
+def _dout(seed, shape):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(shape, generator=g).to(torch.bfloat16)
+
+
+def _check_bwd(smla, case, idx=None, kv=None, seed=0, what="", cuda_forward=False):
+    """The backward is given the oracle forward's out (rounded to bf16) and
+    LSE, or with cuda_forward the CUDA forward's, as in training."""
+    idx = case.indices if idx is None else idx
+    kv = case.kv if kv is None else kv
+    dout = _dout(seed, (case.q.shape[0], case.q.shape[1], 512))
+    q_d, kv_d, idx_d = case.q.to(DEV), kv.to(DEV), idx.to(DEV)
+    if cuda_forward:
+        out, lse = smla.sparse_mla_fwd(q_d, kv_d, idx_d, case.sm_scale)
+        out_err = forward_parity_err
+    else:
+        ro, rl = orc.sparse_mla_fwd(case.q, kv, idx, case.sm_scale)
+        out = torch.from_numpy(ro).to(torch.bfloat16).to(DEV)
+        lse = torch.from_numpy(rl).to(torch.float32).to(DEV)
+        out_err = bf16_rounding_err
+    dq, dkv = smla.sparse_mla_bwd(q_d, kv_d, idx_d, case.sm_scale, out, lse, dout.to(DEV))
+    torch.cuda.synchronize()
+    rq, rkv = orc.sparse_mla_bwd(case.q, kv, idx, case.sm_scale, dout)
+    bq, bkv = grad_term_bounds(case.q, kv, idx, case.sm_scale, dout, out_err)
+    compare_grad(dq.cpu().numpy(), rq, bq, f"{what} dq")
+    compare_grad(dkv.cpu().numpy(), rkv, bkv, f"{what} dkv")
+    return dq.cpu().numpy(), dkv.cpu().numpy(), rq, rkv
+
+
+def test_bwd_small(smla):
+    case = mi.prefill_case(1201, s_q=37, s_kv=420, h_q=8, topk=384)
+    _check_bwd(smla, case, seed=1, what="small")
+
+
+@pytest.mark.parametrize("h_q", [1, 16, 24, 64])
+def test_bwd_head_counts(smla, h_q):
+    """One 16-head unit per token, a ragged second unit (24), four units (64)."""
+    case = mi.prefill_case(1210 + h_q, s_q=29, s_kv=300, h_q=h_q, topk=256)
+    _check_bwd(smla, case, seed=h_q, what=f"h={h_q}")
+
+
+def test_bwd_masking_multiplicity_and_unlisted_rows(smla):
+    """-1 and out-of-range entries, a row listed several times by one token,
+    tokens with no valid entry (dq exactly 0) and rows no token lists (dkv
+    exactly 0)."""
+    s_q, s_kv, topk = 12, 90, 128
+    case = mi.prefill_case(1220, s_q=s_q, s_kv=s_kv, h_q=8, topk=topk)
+    g = torch.Generator().manual_seed(1221)
+    idx = torch.randint(0, 60, (s_q, topk), generator=g, dtype=torch.int32)   # rows 60.. never listed
+    idx[:, ::5] = -1
+    idx[:, 3::7] = s_kv + 5
+    idx[2, :] = -1                                   # no valid entry
+    idx[4, :10] = 7                                  # multiplicity
+    dq, dkv, rq, rkv = _check_bwd(smla, case, idx=idx, seed=2, what="masking")
+    assert np.all(dq[2] == 0.0)
+    assert np.all(dkv[60:] == 0.0)
+
+
+def test_bwd_full_topk_config1(smla):
+    """s_q = s_kv = 64, h = 8, topk = 2048: every causal position listed."""
+    _check_bwd(smla, mi.config(1), seed=3, what="config 1")
+
+
+def test_bwd_long_lists(smla):
+    """Lists of 3100 entries (two 32-block scan windows), ragged last block."""
+    case = mi.prefill_case(1230, s_q=6, s_kv=5000, h_q=8, topk=3100)
+    g = torch.Generator().manual_seed(1231)
+    idx = torch.randint(0, 5000, (6, 3100), generator=g, dtype=torch.int32)
+    _check_bwd(smla, case, idx=idx, seed=4, what="long lists")
+
+
+def test_bwd_many_units_per_cta(smla):
+    """More token units than SMs: each CTA runs several units in turn."""
+    case = mi.prefill_case(1240, s_q=400, s_kv=500, h_q=8, topk=128)
+    _check_bwd(smla, case, seed=5, what="several units per CTA")
+
+
+def test_bwd_after_cuda_forward(smla):
+    """Forward then backward on the GPU, as in training: D uses the CUDA
+    forward's output, so its error enters through the forward's own bar."""
+    case = mi.prefill_case(1250, s_q=60, s_kv=500, h_q=16, topk=256)
+    _check_bwd(smla, case, seed=6, what="after CUDA forward", cuda_forward=True)

@@ -53,6 +53,10 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward (dq, dkv) on a dense prefill config (1-3); nominal FLOPs "
+                         "2*(3*576 + 2*512) per (token, head, top-k entry), bytes per valid entry = "
+                         "1152 gathered + 2304 of fp32 dkv reduction")
     ap.add_argument("--causal", action="store_true",
                     help="time the indices-free causal entry point on the q/kv of a dense prefill config (1-3); "
                          "FLOPs and bytes then count every causal position")
@@ -377,15 +381,17 @@ def run_ours(args, rank, world, dist):
 
     # The oracle pool (spawn) starts before the first GPU work.
     pool = None
-    if rank == 0 and not args.no_cpu_baseline and not args.causal:
+    if rank == 0 and not args.no_cpu_baseline and not args.causal and not args.bwd:
         pool = OraclePool(args.config, os.cpu_count() or 1)
 
     case = workload(args.config)
     stream = torch.cuda.current_stream(dev)
     is_decode = hasattr(case, "kv_cache")
     is_varlen = hasattr(case, "cu_seqlens_q")
-    if args.causal and (is_decode or is_varlen):
-        raise SystemExit("--causal needs a dense prefill config (1-3)")
+    if (args.causal or args.bwd) and (is_decode or is_varlen):
+        raise SystemExit("--causal / --bwd need a dense prefill config (1-3)")
+    if args.causal and args.bwd:
+        raise SystemExit("--causal and --bwd are separate modes")
     n_tok = case.batch * case.s_next if is_decode else case.q.shape[0]
     flops = step_flops(case)
     valid = valid_entries(case)
@@ -393,7 +399,9 @@ def run_ours(args, rank, world, dist):
         s_q, s_kv = case.q.shape[0], case.kv.shape[0]
         valid = sum(max(0, min(s_kv, t + s_kv - s_q + 1)) for t in range(s_q))
         flops = 2.0 * case.q.shape[1] * 1088 * valid
-    kv_bytes = valid * KV_ROW_BYTES
+    if args.bwd:
+        flops = 2.0 * case.q.shape[0] * case.q.shape[1] * case.indices.shape[-1] * (3 * 576 + 2 * 512)
+    kv_bytes = valid * (KV_ROW_BYTES + (2304 if args.bwd else 0))
 
     # device-resident inputs
     d = lambda t: t.to(dev)
@@ -407,6 +415,14 @@ def run_ours(args, rank, world, dist):
                       cuk=d(case.cu_seqlens_kv))
     elif args.causal:
         inputs = dict(q=d(case.q), kv=d(case.kv))
+    elif args.bwd:
+        inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices))
+        o_fwd, l_fwd = smla.sparse_mla_fwd(inputs["q"], inputs["kv"], inputs["idx"], case.sm_scale)
+        g_do = torch.Generator().manual_seed(2000 + args.config)
+        inputs.update(out=o_fwd, lse=l_fwd,
+                      dout=torch.randn(o_fwd.shape, generator=g_do).to(torch.bfloat16).to(dev))
+        dq_buf = torch.empty(case.q.shape, dtype=torch.float32, device=dev)
+        dkv_buf = torch.empty((case.kv.shape[0], 576), dtype=torch.float32, device=dev)
     else:
         inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices))
     h_q = case.h_q if is_decode else case.q.shape[1]
@@ -423,6 +439,9 @@ def run_ours(args, rank, world, dist):
                                        out=out, lse=lse, stream=stream)
         elif args.causal:
             smla.sparse_mla_fwd_causal(inp["q"], inp["kv"], case.sm_scale, out=out, lse=lse, stream=stream)
+        elif args.bwd:
+            smla.sparse_mla_bwd(inp["q"], inp["kv"], inp["idx"], case.sm_scale, inp["out"], inp["lse"], inp["dout"],
+                                dq=dq_buf, dkv=dkv_buf, stream=stream)
         else:
             smla.sparse_mla_fwd(inp["q"], inp["kv"], inp["idx"], case.sm_scale, out=out, lse=lse, stream=stream)
 
@@ -467,20 +486,21 @@ def run_ours(args, rank, world, dist):
     warm = timed_loop(max(args.steps, 20), lambda: call(inputs), flush_l2=False)
 
     # end to end through the C ABI with host buffers: pinned H2D of the inputs,
-    # the call, D2H of out and lse, all inside the timed region
+    # the call, D2H of its results (out and lse; dq and dkv for the backward),
+    # all inside the timed region
     host = {k: v.cpu().pin_memory() for k, v in inputs.items()}
     dev2 = {k: torch.empty_like(v) for k, v in inputs.items()}
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    results = [dq_buf, dkv_buf] if args.bwd else [out, lse]
+    res_h = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in results]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    d2h = sum(r.numel() * r.element_size() for r in results)
 
     def e2e_step():
         for k in host:
             dev2[k].copy_(host[k], non_blocking=True)
         call(dev2)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        for rh, r in zip(res_h, results):
+            rh.copy_(r, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -506,14 +526,14 @@ def run_ours(args, rank, world, dist):
     if bound == "hbm":
         achieved = kv_bytes / (fwd_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": p_bw, "unit": "GB/s",
-                    "frac": achieved / p_bw, "traffic": None if args.causal else profiled_traffic(args.config),
+                    "frac": achieved / p_bw, "traffic": None if (args.causal or args.bwd) else profiled_traffic(args.config),
                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                     "algorithmic_bytes_per_launch": kv_bytes,
                     "note": "achieved = valid entries x 1152 B / mean launch time (cold L2)"}
     else:
         achieved = flops / (fwd_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": p_tf, "unit": "TFLOP/s",
-                    "frac": achieved / p_tf, "traffic": None if args.causal else profiled_traffic(args.config),
+                    "frac": achieved / p_tf, "traffic": None if (args.causal or args.bwd) else profiled_traffic(args.config),
                     "peak_kind": f"{peak_kind} bf16 (burst)", "algorithmic_flops_per_launch": flops}
 
     cpu = None
@@ -526,11 +546,13 @@ def run_ours(args, rank, world, dist):
 
     line = {
         "metric": ("indices-free causal MLA fwd TFLOP/s (every causal position)" if args.causal
+                   else "sparse-MLA bwd TFLOP/s at topk=2048 (nominal FLOPs)" if args.bwd
                    else "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)"),
         "value": whole_job_tflops(flops, args.steps, world, total_ms), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(case, args.config) + (" (indices-free causal mode)" if args.causal else ""),
+        "config": {"workload": workload_name(case, args.config) + (" (indices-free causal mode)" if args.causal else "")
+                   + (" (backward: dq, dkv)" if args.bwd else ""),
                    "seed": 1000 + args.config,
                    "l2": "256 MB buffer written before every timed step (cold L2)",
                    "parallelism": f"replicas x{world}"},

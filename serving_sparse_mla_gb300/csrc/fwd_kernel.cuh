@@ -287,8 +287,10 @@ __device__ __forceinline__ TokCtx token_context(const FwdParams& p, int tok) {
 // Entry e (< topk) of a token's index list: read from the list, or in the
 // causal mode the position itself while it is at or before the token's own
 // position `last` (no memory read).
-__device__ __forceinline__ int index_at(const FwdParams& p, const int32_t* irow, int last, int e) {
-  return p.mode == kCausal ? (e <= last ? e : -1) : __ldg(irow + e);
+template <bool kCausalList>
+__device__ __forceinline__ int index_at(const int32_t* irow, int last, int e) {
+  if constexpr (kCausalList) return e <= last ? e : -1;
+  else return __ldg(irow + e);
 }
 
 // KV row read by one index entry, or -1 when the entry is masked.
@@ -405,7 +407,7 @@ __device__ __forceinline__ void cp_async_arrive_on(uint32_t bar) {
 // memory layout (ring sizes and offsets), M the barrier block (same member
 // names), and kRows also publishes each block's 64 KV rows (entry r of the
 // block in info_rows[k][r], -1 when masked) for consumers that scatter by row.
-template <int N, class L, class M, bool kRows>
+template <int N, class L, class M, bool kRows, bool kCausalList = false>
 __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
   const int warp = static_cast<int>(threadIdx.x >> 5);   // 0..3
   const int lane = static_cast<int>(lane_id());
@@ -428,7 +430,7 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
     const int tok = item.unit / p.groups;
     const int jb = item.jb, je = item.je;
     const TokCtx ctx = token_context(p, tok);
-    const int32_t* irow = p.mode == kCausal ? nullptr : p.indices + static_cast<size_t>(tok) * p.topk;
+    const int32_t* irow = kCausalList ? nullptr : p.indices + static_cast<size_t>(tok) * p.topk;
     const int last = tok + p.causal_off;   // kCausal only
     for (int wb = jb; wb < je; wb += 32, ++win) {
       // Candidate blocks of this window of up to 32: a block none of whose
@@ -446,7 +448,7 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
         for (int i = 0; i < 16; ++i) {
           const int blk = b0 + (i >> 1);
           const int e = blk * kBlk + (i & 1) * 32 + lane;
-          v[i] = (blk < we && e < p.topk) ? index_at(p, irow, last, e) : -1;
+          v[i] = (blk < we && e < p.topk) ? index_at<kCausalList>(irow, last, e) : -1;
         }
         uint32_t bits = 0;
 #pragma unroll
@@ -469,7 +471,7 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int e = j_next * kBlk + lane * 2 + i;
-        idx_next[i] = (j_next >= 0 && e < p.topk) ? index_at(p, irow, last, e) : -1;
+        idx_next[i] = (j_next >= 0 && e < p.topk) ? index_at<kCausalList>(irow, last, e) : -1;
       }
       while (j_next >= 0) {
         const int j = j_next;
@@ -481,7 +483,7 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
 #pragma unroll
         for (int i = 0; i < 2; ++i) {   // prefetch the next candidate's indices
           const int e = j_next * kBlk + lane * 2 + i;
-          idx_next[i] = (j_next >= 0 && e < p.topk) ? index_at(p, irow, last, e) : -1;
+          idx_next[i] = (j_next >= 0 && e < p.topk) ? index_at<kCausalList>(irow, last, e) : -1;
         }
         const uint32_t bal0 = __ballot_sync(0xffffffffu, rows[0] >= 0);
         const uint32_t bal1 = __ballot_sync(0xffffffffu, rows[1] >= 0);
@@ -634,9 +636,12 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
   return true;
 }
 
+// The index list is read from memory, or formed in place in the causal mode
+// (decided once per launch, so the list walk carries no per-entry branch).
 template <int N>
 __device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
-  return run_producer_t<N, Layout<N>, Misc, false>(p, m, sbase);
+  return p.mode == kCausal ? run_producer_t<N, Layout<N>, Misc, false, true>(p, m, sbase)
+                           : run_producer_t<N, Layout<N>, Misc, false, false>(p, m, sbase);
 }
 
 // ------------------------------------------------------------------ MMA issuer

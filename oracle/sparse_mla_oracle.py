@@ -212,26 +212,41 @@ def causal_mla_fwd(q, kv, sm_scale: float, d_v: int = 512,
     return _stack(outs, lses, q.shape[1], d_v)
 
 
-def sparse_mla_bwd(q, kv, indices, sm_scale: float, dout, d_v: int = 512):
-    """Gradients of the dense-layout forward with respect to q and kv, given
-    the upstream gradient dout of out (the LSE output carries no gradient).
-
-    The backward the training users pair with the forward (prime-rl page:
-    forward and backward sparse attention timings).  Per token t, with its
-    valid rows K = kv[r] (V = K[:, :512], the same latent rows), from the
-    definition of the forward by the chain rule:
+def bwd_token(q_t: np.ndarray, K: np.ndarray, do_t: np.ndarray, sm_scale: float, d_v: int
+              ) -> Tuple[np.ndarray, np.ndarray]:
+    """One token's backward over its gathered rows K [n, 576] (V = K[:, :512],
+    the same latent rows), from the definition of the forward by the chain
+    rule (the LSE output carries no gradient):
 
         P  = softmax(sm_scale * q_t K^T)            [h, n]
         dP = dout_t V^T                             [h, n]
         D  = rowsum(dout_t * out_t) = rowsum(P * dP)
         dS = P * (dP - D)
-        dq_t            = sm_scale * dS K
-        dkv[r]         += sm_scale * dS^T q_t       (all 576 columns)
-        dkv[r, :512]   += P^T dout_t
+        dq_t  = sm_scale * dS K                     [h, 576]
+        dK    = sm_scale * dS^T q_t, plus P^T dout_t on the first 512 columns
 
-    with multiplicity (a row listed twice receives both contributions).  O and
-    the LSE are recomputed here from q and kv.  Returns float64 dq [s_q,h,576]
-    and dkv [s_kv,576]."""
+    Returns (dq_t, dK [n, 576]); the caller adds dK into the rows."""
+    V = K[:, :d_v]
+    s = sm_scale * (q_t @ K.T)
+    m = s.max(axis=1, keepdims=True)
+    P = np.exp(s - m)
+    P /= P.sum(axis=1, keepdims=True)
+    O = P @ V
+    dP = do_t @ V.T
+    D = (do_t * O).sum(axis=1, keepdims=True)
+    dS = P * (dP - D)
+    dK = sm_scale * (dS.T @ q_t)
+    dK[:, :d_v] += P.T @ do_t
+    return sm_scale * (dS @ K), dK
+
+
+def sparse_mla_bwd(q, kv, indices, sm_scale: float, dout, d_v: int = 512):
+    """Gradients of the dense-layout forward with respect to q and kv, given
+    the upstream gradient dout of out: the backward the training users pair
+    with the forward (prime-rl page: forward and backward sparse attention
+    timings).  Per token, bwd_token over its valid rows, with multiplicity (a
+    row listed twice receives both contributions).  O and the LSE are
+    recomputed from q and kv.  Returns float64 dq [s_q,h,576], dkv [s_kv,576]."""
     s_q, h = q.shape[0], q.shape[1]
     kv2 = kv.reshape(kv.shape[0], -1)
     s_kv, d_qk = kv2.shape
@@ -243,19 +258,31 @@ def sparse_mla_bwd(q, kv, indices, sm_scale: float, dout, d_v: int = 512):
         r = rows_dense(idx[t], s_kv)
         if r.size == 0:
             continue
-        K = _gather(kv2, r)
-        V = K[:, :d_v]
-        s = sm_scale * (q64[t] @ K.T)
-        m = s.max(axis=1, keepdims=True)
-        P = np.exp(s - m)
-        P /= P.sum(axis=1, keepdims=True)
-        O = P @ V
-        dP = do64[t] @ V.T
-        D = (do64[t] * O).sum(axis=1, keepdims=True)
-        dS = P * (dP - D)
-        dq[t] = sm_scale * (dS @ K)
-        np.add.at(dkv, r, sm_scale * (dS.T @ q64[t]))
-        np.add.at(dkv[:, :d_v], r, P.T @ do64[t])
+        dq[t], dK = bwd_token(q64[t], _gather(kv2, r), do64[t], sm_scale, d_v)
+        np.add.at(dkv, r, dK)
+    return dq, dkv
+
+
+def sparse_mla_bwd_varlen(q, kv, indices, cu_seqlens_q, cu_seqlens_kv, sm_scale: float, dout,
+                          d_v: int = 512):
+    """Packed-prefill backward: as sparse_mla_bwd with each token's local
+    indices mapped into its own sequence's KV rows (rows_varlen)."""
+    total = q.shape[0]
+    h = q.shape[1]
+    kv2 = kv.reshape(kv.shape[0], -1)
+    n_rows, d_qk = kv2.shape
+    idx = _i64(indices).reshape(total, -1)
+    cu_q, cu_k = _i64(cu_seqlens_q), _i64(cu_seqlens_kv)
+    q64, do64 = _f64(q), _f64(dout)
+    dq = np.zeros((total, h, d_qk))
+    dkv = np.zeros((n_rows, d_qk))
+    for t in range(total):
+        b = sequence_of(cu_q, t)
+        r = rows_varlen(idx[t], int(cu_k[b]), int(cu_k[b + 1] - cu_k[b]))
+        if r.size == 0:
+            continue
+        dq[t], dK = bwd_token(q64[t], _gather(kv2, r), do64[t], sm_scale, d_v)
+        np.add.at(dkv, r, dK)
     return dq, dkv
 
 

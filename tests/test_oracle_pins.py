@@ -635,6 +635,25 @@ def test_bwd_pins_catch_planted_mistake(monkeypatch, name, fn):
     assert failed >= 1, f"no pin caught the planted mistake {name}"
 
 
+def test_bwd_varlen_autograd_per_sequence():
+    """Packed backward: per sequence, torch autograd on the sequence's own
+    slice with its local indices; kv rows of other sequences get nothing
+    from it."""
+    seqlens, h, topk = [9, 3, 14], 2, 10
+    case = mi.varlen_case(47, seqlens, h, topk=topk)
+    g = mi._gen(48)
+    dout = torch.randn((sum(seqlens), h, DV), generator=g, dtype=torch.float64)
+    dq, dkv = orc.sparse_mla_bwd_varlen(case.q, case.kv, case.indices, case.cu_seqlens_q, case.cu_seqlens_kv,
+                                        case.sm_scale, dout, DV)
+    cu, ck = case.cu_seqlens_q.tolist(), case.cu_seqlens_kv.tolist()
+    for b in range(len(seqlens)):
+        a, e = cu[b], cu[b + 1]
+        rq, rkv = _autograd_reference(case.q[a:e], case.kv[ck[b]:ck[b + 1]], case.indices[a:e], case.sm_scale,
+                                      dout[a:e])
+        _close(dq[a:e], rq, rtol=1e-9, atol=1e-12)
+        _close(dkv[ck[b]:ck[b + 1]], rkv, rtol=1e-9, atol=1e-12)
+
+
 def test_bwd_variant_without_mistakes_passes():
     """The mutation harness itself is faithful: with no mistake planted it
     reproduces the oracle."""

@@ -84,6 +84,18 @@ sparse_mla_status_t sparse_mla_fwd(const void* q, const void* kv, const int32_t*
                                    int topk, void* stream);
 
 /*
+ * Backward of sparse_mla_fwd_varlen (packed sequences; indices local to each
+ * token's sequence, as there).  Arguments as for sparse_mla_bwd, with the
+ * packed layout of sparse_mla_fwd_varlen: dq fp32 [total_q, h_q, d_qk]
+ * written, dkv fp32 [total_kv, d_qk] zeroed then accumulated.
+ */
+sparse_mla_status_t sparse_mla_bwd_varlen(const void* q, const void* kv, const int32_t* indices,
+                                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                                          const void* out, const float* lse, const void* dout, float sm_scale,
+                                          float* dq, float* dkv, int total_q, int total_kv, int h_q, int d_qk,
+                                          int d_v, int topk, void* stream);
+
+/*
  * Indices-free causal forward for short prefill, where the top-k selection
  * keeps every causal position ("feat: add XTuner TileLang sparse MLA
  * backend", Summary: short prefill), so no index tensor is needed.  The s_q

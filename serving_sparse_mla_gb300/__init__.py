@@ -8,6 +8,7 @@ from .binding import (  # noqa: F401
     load,
     set_wait_timeout_ns,
     sparse_mla_bwd,
+    sparse_mla_bwd_varlen,
     sparse_mla_decode,
     sparse_mla_fwd,
     sparse_mla_fwd_causal,

@@ -29,6 +29,9 @@ SIGNATURES = {
                                c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "sparse_mla_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float,
                                c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "sparse_mla_bwd_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
+                                      c_void_p, c_void_p, c_float, c_void_p, c_void_p, c_int, c_int, c_int,
+                                      c_int, c_int, c_int, c_void_p]),
     "sparse_mla_fwd_causal": (c_int, [c_void_p, c_void_p, c_float, c_void_p, c_void_p,
                                       c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "sparse_mla_fwd_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_float,
@@ -145,6 +148,30 @@ def sparse_mla_bwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_
     st = lib.sparse_mla_bwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(out), _ptr(lse), _ptr(dout), float(sm_scale),
                             _ptr(dq), _ptr(dkv), s_q, s_kv, h_q, d_qk, d_v, topk, _stream(stream))
     _check(st, "sparse_mla_bwd")
+    return dq, dkv
+
+
+def sparse_mla_bwd_varlen(q, kv, indices, cu_seqlens_q, cu_seqlens_kv, sm_scale, out, lse, dout,
+                          dq=None, dkv=None, stream=None):
+    """Backward of sparse_mla_fwd_varlen -> (dq [total_q,h_q,576] fp32,
+    dkv [total_kv,576] fp32)."""
+    lib = load()
+    total_q, h_q, d_qk = q.shape
+    total_kv = kv.shape[0]
+    topk = indices.shape[-1]
+    batch = cu_seqlens_q.numel() - 1
+    for t, dt, n in ((q, torch.bfloat16, "q"), (kv, torch.bfloat16, "kv"), (indices, torch.int32, "indices"),
+                     (cu_seqlens_q, torch.int32, "cu_seqlens_q"), (cu_seqlens_kv, torch.int32, "cu_seqlens_kv"),
+                     (out, torch.bfloat16, "out"), (lse, torch.float32, "lse"), (dout, torch.bfloat16, "dout")):
+        _need(t, dt, n)
+    if dq is None:
+        dq = torch.empty((total_q, h_q, d_qk), dtype=torch.float32, device=q.device)
+    if dkv is None:
+        dkv = torch.empty((total_kv, d_qk), dtype=torch.float32, device=q.device)
+    st = lib.sparse_mla_bwd_varlen(_ptr(q), _ptr(kv), _ptr(indices), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+                                   batch, _ptr(out), _ptr(lse), _ptr(dout), float(sm_scale), _ptr(dq), _ptr(dkv),
+                                   total_q, total_kv, h_q, d_qk, 512, topk, _stream(stream))
+    _check(st, "sparse_mla_bwd_varlen")
     return dq, dkv
 
 

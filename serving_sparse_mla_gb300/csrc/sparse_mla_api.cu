@@ -233,41 +233,88 @@ sparse_mla_status_t sparse_mla_fwd_causal(const void* q, const void* kv, float s
   return launch_fwd(p, cs);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Shared tail of the two backward entry points: dkv zeroed on the stream,
+// then the persistent backward grid over units of one token x 16 heads.
+sparse_mla_status_t launch_bwd(FwdParams p, long long n_tok, int h_q, long long n_rows, float* dq, float* dkv,
+                               int sms, cudaStream_t cs) {
+  if (n_rows > 0 &&
+      cudaMemsetAsync(dkv, 0, static_cast<size_t>(n_rows) * smla::kDqk * sizeof(float), cs) != cudaSuccess)
+    return SPARSE_MLA_ERR_CUDA;
+  if (n_tok == 0) return SPARSE_MLA_OK;
+  if (n_rows == 0)
+    return cudaMemsetAsync(dq, 0, static_cast<size_t>(n_tok) * h_q * smla::kDqk * sizeof(float), cs) ==
+                   cudaSuccess
+               ? SPARSE_MLA_OK
+               : SPARSE_MLA_ERR_CUDA;
+  p.dq = dq;
+  p.dkv = dkv;
+  p.groups = (h_q + smla::kBwdHeads - 1) / smla::kBwdHeads;   // units of 16 heads
+  p.sched = smla::kWholeUnits;
+  const long long units = n_tok * p.groups;
+  p.ctas = static_cast<int>(units < sms ? units : sms);
+  smla::sparse_mla_bwd_kernel<<<p.ctas, smla::BwdLayout::kThreads, smla::bwd_smem_bytes(), cs>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+}
+
+sparse_mla_status_t check_bwd(const void* dout, const float* dq, const float* dkv, long long n_tok,
+                              long long n_rows) {
+  if (n_tok > 0 && (!dout || !dq || !aligned(dout, 16) || !aligned(dq, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_rows > 0 && (!dkv || !aligned(dkv, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
+  return SPARSE_MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 sparse_mla_status_t sparse_mla_bwd(const void* q, const void* kv, const int32_t* indices, const void* out,
                                    const float* lse, const void* dout, float sm_scale, float* dq, float* dkv,
                                    int s_q, int s_kv, int h_q, int d_qk, int d_v, int topk, void* stream) {
   sparse_mla_status_t st = check_common(q, indices, out, lse, s_q, h_q, d_qk, d_v, topk);
   if (st != SPARSE_MLA_OK) return st;
   if (s_kv < 0) return SPARSE_MLA_ERR_INVALID_ARG;
-  if (s_q > 0 && (!dout || !dq || !aligned(dout, 16) || !aligned(dq, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
-  if (s_kv > 0 && (!dkv || !aligned(dkv, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
+  if ((st = check_bwd(dout, dq, dkv, s_q, s_kv)) != SPARSE_MLA_OK) return st;
   int sms = 0;
   if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  // dkv accumulates the contributions of every token that lists a row.
-  if (s_kv > 0 &&
-      cudaMemsetAsync(dkv, 0, static_cast<size_t>(s_kv) * smla::kDqk * sizeof(float), cs) != cudaSuccess)
-    return SPARSE_MLA_ERR_CUDA;
-  if (s_q == 0) return SPARSE_MLA_OK;
-  if (s_kv == 0)
-    return cudaMemsetAsync(dq, 0, static_cast<size_t>(s_q) * h_q * smla::kDqk * sizeof(float), cs) == cudaSuccess
-               ? SPARSE_MLA_OK
-               : SPARSE_MLA_ERR_CUDA;
-  if (!kv || !aligned(kv, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (s_q > 0 && s_kv > 0 && (!kv || !aligned(kv, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
   FwdParams p = base_params(q, indices, sm_scale, const_cast<void*>(out), const_cast<float*>(lse), s_q, h_q, topk);
   p.kv = static_cast<const __nv_bfloat16*>(kv);
   p.mode = smla::kDense;
   p.n_rows = s_kv;
   p.s_kv = s_kv;
   p.dout = static_cast<const __nv_bfloat16*>(dout);
-  p.dq = dq;
-  p.dkv = dkv;
-  p.groups = (h_q + smla::kBwdHeads - 1) / smla::kBwdHeads;   // units of 16 heads
-  p.sched = smla::kWholeUnits;
-  const long long units = static_cast<long long>(s_q) * p.groups;
-  p.ctas = static_cast<int>(units < sms ? units : sms);
-  smla::sparse_mla_bwd_kernel<<<p.ctas, smla::BwdLayout::kThreads, smla::bwd_smem_bytes(), cs>>>(p);
-  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+  return launch_bwd(p, s_q, h_q, s_kv, dq, dkv, sms, static_cast<cudaStream_t>(stream));
+}
+
+sparse_mla_status_t sparse_mla_bwd_varlen(const void* q, const void* kv, const int32_t* indices,
+                                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                                          const void* out, const float* lse, const void* dout, float sm_scale,
+                                          float* dq, float* dkv, int total_q, int total_kv, int h_q, int d_qk,
+                                          int d_v, int topk, void* stream) {
+  sparse_mla_status_t st = check_common(q, indices, out, lse, total_q, h_q, d_qk, d_v, topk);
+  if (st != SPARSE_MLA_OK) return st;
+  if (total_kv < 0 || batch < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (total_q > 0 && (batch < 1 || !cu_seqlens_q || !cu_seqlens_kv || !aligned(cu_seqlens_q, 4) ||
+                      !aligned(cu_seqlens_kv, 4)))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  if ((st = check_bwd(dout, dq, dkv, total_q, total_kv)) != SPARSE_MLA_OK) return st;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (total_q > 0 && total_kv > 0 && (!kv || !aligned(kv, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
+  FwdParams p = base_params(q, indices, sm_scale, const_cast<void*>(out), const_cast<float*>(lse), total_q, h_q,
+                            topk);
+  p.kv = static_cast<const __nv_bfloat16*>(kv);
+  p.mode = smla::kVarlen;
+  p.n_rows = total_kv;
+  p.batch = batch;
+  p.cu_q = cu_seqlens_q;
+  p.cu_kv = cu_seqlens_kv;
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  return launch_bwd(p, total_q, h_q, total_kv, dq, dkv, sms, static_cast<cudaStream_t>(stream));
 }
 
 size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v, int topk) {

@@ -48,10 +48,11 @@ GRAD_RTOL = 2e-2
 GRAD_ATOL_RMS = 1e-3
 
 
-def grad_term_bounds(q, kv, indices, sm_scale, dout, out_err, d_v=512):
-    """Per-element error bounds of dq and dkv for the dense-layout backward
-    (see above).  out_err(O) gives the elementwise bound on |out - O| for the
-    forward output the backward was given, from the exact O."""
+def grad_term_bounds(q, kv, indices, sm_scale, dout, out_err, d_v=512, rows_of=None):
+    """Per-element error bounds of dq and dkv (see above).  out_err(O) gives
+    the elementwise bound on |out - O| for the forward output the backward
+    was given, from the exact O; rows_of(t, idx_t) maps a token's list to KV
+    rows (default: the dense layout)."""
     import torch
     f64 = lambda x: x.double().numpy() if isinstance(x, torch.Tensor) else np.asarray(x, np.float64)
     qf, kvf, dof = f64(q), f64(kv), f64(dout)
@@ -61,7 +62,10 @@ def grad_term_bounds(q, kv, indices, sm_scale, dout, out_err, d_v=512):
     bq = np.zeros_like(qf)
     bkv = np.zeros_like(kvf)
     for t in range(s_q):
-        r = idx[t][(idx[t] >= 0) & (idx[t] < s_kv)].astype(np.int64)
+        if rows_of is None:
+            r = idx[t][(idx[t] >= 0) & (idx[t] < s_kv)].astype(np.int64)
+        else:
+            r = np.asarray(rows_of(t, idx[t]), dtype=np.int64)
         if r.size == 0:
             continue
         K = kvf[r]

@@ -104,3 +104,32 @@ def test_bwd_after_cuda_forward(smla):
     forward's output, so its error enters through the forward's own bar."""
     case = mi.prefill_case(1250, s_q=60, s_kv=500, h_q=16, topk=256)
     _check_bwd(smla, case, seed=6, what="after CUDA forward", cuda_forward=True)
+
+
+@pytest.mark.parametrize("h_q", [8, 64])
+def test_bwd_varlen(smla, h_q):
+    """Packed sequences: local indices into each sequence's own rows; the
+    CUDA backward against the oracle's packed backward."""
+    case = mi.varlen_case(1260 + h_q, [130, 1, 257, 64, 40], h_q, topk=192)
+    d = lambda t: t.to(DEV)
+    dout = _dout(h_q, (case.q.shape[0], h_q, 512))
+    ro, rl = orc.sparse_mla_fwd_varlen(case.q, case.kv, case.indices, case.cu_seqlens_q, case.cu_seqlens_kv,
+                                       case.sm_scale)
+    out = torch.from_numpy(ro).to(torch.bfloat16).to(DEV)
+    lse = torch.from_numpy(rl).to(torch.float32).to(DEV)
+    dq, dkv = smla.sparse_mla_bwd_varlen(d(case.q), d(case.kv), d(case.indices), d(case.cu_seqlens_q),
+                                         d(case.cu_seqlens_kv), case.sm_scale, out, lse, d(dout))
+    torch.cuda.synchronize()
+    rq, rkv = orc.sparse_mla_bwd_varlen(case.q, case.kv, case.indices, case.cu_seqlens_q, case.cu_seqlens_kv,
+                                        case.sm_scale, dout)
+    cu_q = case.cu_seqlens_q.numpy()
+    cu_k = case.cu_seqlens_kv.numpy()
+
+    def rows_of(t, idx_t):
+        b = int(np.searchsorted(cu_q, t, side="right") - 1)
+        n = int(cu_k[b + 1] - cu_k[b])
+        return int(cu_k[b]) + idx_t[(idx_t >= 0) & (idx_t < n)]
+    bq, bkv = grad_term_bounds(case.q, case.kv, case.indices, case.sm_scale, dout, bf16_rounding_err,
+                               rows_of=rows_of)
+    compare_grad(dq.cpu().numpy(), rq, bq, f"varlen h={h_q} dq")
+    compare_grad(dkv.cpu().numpy(), rkv, bkv, f"varlen h={h_q} dkv")

@@ -15,12 +15,18 @@ Shapes and index structure follow the workloads of the pages:
   sparse MLA forward), with -1 padded index lists (same page, Validation);
 * packed prefill and a BF16 paged cache for decode (same page, Summary);
 * MTP5 speculative decode, six query tokens per request (same page,
-  End-to-end serving).
+  End-to-end serving);
+* the DSA indexer that produces the lists (the pages name it but print
+  neither its formula nor its sizes): 64 indexer heads of width 128, one
+  key per position and per-token head weights, the sizes of the DeepSeek-V3.2
+  lightning indexer.
 
 Recipe: Q and KV are float32 standard normal draws from a CPU
 ``torch.Generator`` seeded per case, rounded to bf16 (round to nearest
 even).  Index lists draw distinct causal positions with ``torch.randperm``
-from generators derived from the same seed.
+from generators derived from the same seed.  Indexer queries and keys are
+N(0,1) draws rounded to bf16; head weights are fp32 N(0,1) draws scaled by
+h_idx^-1/2 * d_idx^-1/2.
 """
 from __future__ import annotations
 
@@ -324,3 +330,75 @@ def config(n: int, seed: Optional[int] = None):
 def nominal_flops(s_q: int, h_q: int, topk: int = TOPK, d_qk: int = D_QK, d_v: int = D_V) -> float:
     """2*s_q*h_q*topk*(d_qk+d_v): the workload's nominal FLOP count."""
     return 2.0 * s_q * h_q * topk * (d_qk + d_v)
+
+
+# --------------------------------------------------------------------------
+# DSA indexer inputs (the step that produces the index lists)
+# --------------------------------------------------------------------------
+
+H_IDX = 64     # indexer heads
+D_IDX = 128    # indexer head width
+
+
+@dataclass
+class IndexerCase:
+    """Indexer queries q_idx [total_q, h_idx, d_idx] bf16, one key per KV
+    position k_idx [total_kv, d_idx] bf16 and per-token head weights
+    [total_q, h_idx] fp32.  cu_seqlens_q / cu_seqlens_kv (int32 [batch+1])
+    are None for a dense prefill (one sequence)."""
+    name: str
+    q_idx: torch.Tensor
+    k_idx: torch.Tensor
+    weights: torch.Tensor
+    topk: int
+    cu_seqlens_q: Optional[torch.Tensor] = None
+    cu_seqlens_kv: Optional[torch.Tensor] = None
+
+    @property
+    def max_seqlen_kv(self) -> int:
+        if self.cu_seqlens_kv is None:
+            return int(self.k_idx.shape[0])
+        return int((self.cu_seqlens_kv[1:] - self.cu_seqlens_kv[:-1]).max().item())
+
+
+def indexer_weights(g: torch.Generator, total_q: int, h_idx: int, d_idx: int) -> torch.Tensor:
+    """Head weights: N(0,1) draws times h_idx^-1/2 * d_idx^-1/2 (a projection
+    of the hidden state folded with the head-count and softmax scales), fp32."""
+    w = torch.randn((total_q, h_idx), generator=g, dtype=torch.float32)
+    return w * float(h_idx ** -0.5 * d_idx ** -0.5)
+
+
+def indexer_case(seed: int, s_q: int, s_kv: int, h_idx: int = H_IDX, d_idx: int = D_IDX,
+                 topk: int = TOPK, name: str = "") -> IndexerCase:
+    """Dense causal prefill: the s_q queries are the last s_q of s_kv
+    positions.  q_idx, k_idx N(0,1) rounded to bf16."""
+    g = _gen(seed * 104729 + 3)
+    q = randn_bf16(g, (s_q, h_idx, d_idx))
+    k = randn_bf16(g, (s_kv, d_idx))
+    w = indexer_weights(g, s_q, h_idx, d_idx)
+    return IndexerCase(name or f"indexer_s{s_q}_kv{s_kv}_h{h_idx}", q, k, w, topk)
+
+
+def indexer_varlen_case(seed: int, q_lens: List[int], kv_lens: List[int], h_idx: int = H_IDX,
+                        d_idx: int = D_IDX, topk: int = TOPK, name: str = "") -> IndexerCase:
+    """Packed prefill: sequence b has q_lens[b] new tokens at the end of
+    kv_lens[b] positions (kv_lens[b] - q_lens[b] cached before them)."""
+    assert len(q_lens) == len(kv_lens)
+    g = _gen(seed * 104729 + 5)
+    tq, tk = int(sum(q_lens)), int(sum(kv_lens))
+    q = randn_bf16(g, (tq, h_idx, d_idx))
+    k = randn_bf16(g, (tk, d_idx))
+    w = indexer_weights(g, tq, h_idx, d_idx)
+    cq = torch.tensor([0] + list(torch.cumsum(torch.tensor(q_lens), 0).tolist()), dtype=torch.int32)
+    ck = torch.tensor([0] + list(torch.cumsum(torch.tensor(kv_lens), 0).tolist()), dtype=torch.int32)
+    return IndexerCase(name or f"indexer_varlen_{tq}_{tk}_h{h_idx}", q, k, w, topk, cq, ck)
+
+
+def tied_scores(seed: int, rows: int, width: int, levels: int = 7) -> torch.Tensor:
+    """Scores fp32 [rows, width] drawn from a few integer levels (many exact
+    ties) with some -inf entries, for the selection step alone."""
+    g = _gen(seed * 7 + 11)
+    s = torch.randint(-levels, levels + 1, (rows, width), generator=g).to(torch.float32)
+    hole = torch.rand((rows, width), generator=g) < 0.02
+    s[hole] = float("-inf")
+    return s

@@ -60,6 +60,10 @@ def parse_args():
     ap.add_argument("--causal", action="store_true",
                     help="time the indices-free causal entry point on the q/kv of a dense prefill config (1-3); "
                          "FLOPs and bytes then count every causal position")
+    ap.add_argument("--indexer", action="store_true",
+                    help="time the DSA indexer + top-k (dsa_indexer_topk) that produces the index lists, on "
+                         "the token shape of config 1-4 with 64 indexer heads of width 128; FLOPs "
+                         "2*64*128 per scored (row, visible position)")
     ap.add_argument("--clock-log", default=None,
                     help="directory for the nvidia-smi clock CSV of the run (default: the system temp dir)")
     return ap.parse_args()
@@ -340,9 +344,41 @@ def oracle_sample(case, config: int):
 
 # ----------------------------------------------------------------------------- arms
 
+def run_reference_indexer(args):
+    case = indexer_workload(args.config)
+    info = indexer_rows(case)
+    flops, _, scored_pos, _ = indexer_costs(case, info)
+    cores = os.cpu_count() or 1
+    pool = IndexerOraclePool(args.config, cores)
+    rows, sample = indexer_oracle_sample(info, args.config)
+    part = sum(info[r][0] for r in rows) / max(1, scored_pos)
+    for _ in range(args.warmup):
+        pool.run(rows)
+    times = [pool.run(rows) for _ in range(args.steps)]
+    pool.close()
+    total = sum(times)
+    value = flops * part * args.steps / total / 1e12
+    line = {
+        "impl": "reference",
+        "metric": "DSA indexer scores + top-k TFLOP/s at topk=2048 (2*h_idx*d_idx per scored position)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"DSA indexer, token shape of config {args.config}", "sample": sample,
+                   "l2": "n/a (CPU)", "seed": 1000 + args.config},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
+    if args.indexer:
+        return run_reference_indexer(args)
     case = workload(args.config)
     cores = os.cpu_count() or 1
     pool = OraclePool(args.config, cores)
@@ -573,6 +609,256 @@ def run_ours(args, rank, world, dist):
     return 0
 
 
+# ----------------------------------------------------------------------------- DSA indexer
+
+IDX_TOPK = 2048
+
+
+def indexer_workload(config: int):
+    """The indexer inputs on the token shape of workload `config`."""
+    import mla_inputs as mi
+    seed = 1000 + config
+    if config == 1:
+        return mi.indexer_case(seed, 64, 64)
+    if config == 2:
+        return mi.indexer_case(seed, 2119, 2119)
+    if config == 3:
+        return mi.indexer_case(seed, 8192, 8192)
+    if config == 4:
+        return mi.indexer_varlen_case(seed, mi.VARLEN_C4, mi.VARLEN_C4)
+    raise SystemExit("--indexer: configs 1-4 (prefill shapes)")
+
+
+def indexer_rows(case):
+    """Per query row: (visible length, scored?)."""
+    from itertools import accumulate
+    s_q, s_kv = case.q_idx.shape[0], case.k_idx.shape[0]
+    if case.cu_seqlens_q is None:
+        seqs = [(0, s_q, s_kv)]
+    else:
+        cq, ck = case.cu_seqlens_q.tolist(), case.cu_seqlens_kv.tolist()
+        seqs = [(cq[b], cq[b + 1] - cq[b], ck[b + 1] - ck[b]) for b in range(len(cq) - 1)]
+    out = []
+    for _, lq, lk in seqs:
+        for t in range(lq):
+            v = max(0, min(lk, t + lk - lq + 1))
+            out.append((v, v > case.topk))
+    return out
+
+
+def _idx_oracle_init(config: int):
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    global _W_IDX
+    _W_IDX = indexer_workload(config)
+
+
+def _idx_oracle_worker(rows):
+    from oracle import dsa_indexer_oracle as ido
+    c = _W_IDX
+    t0 = time.perf_counter()
+    if rows:
+        if c.cu_seqlens_q is None:
+            ido.dsa_indices(c.q_idx, c.k_idx, c.weights, c.topk, rows=rows)
+        else:
+            ido.dsa_indices_varlen(c.q_idx, c.k_idx, c.weights, c.cu_seqlens_q, c.cu_seqlens_kv, c.topk, rows=rows)
+    return time.perf_counter() - t0
+
+
+class IndexerOraclePool(OraclePool):
+    """The indexer oracle, unchanged, sharded by query row over a spawn pool
+    of single-threaded workers (one per host core)."""
+
+    def __init__(self, config: int, cores: int):
+        import multiprocessing as mp
+        self.cores = cores
+        ctx = mp.get_context("spawn")
+        self.pool = ctx.Pool(cores, initializer=_idx_oracle_init, initargs=(config,))
+        self.pool.map(_idx_oracle_worker, [[] for _ in range(cores)])
+
+    def run(self, rows):
+        shards = [rows[i::self.cores] for i in range(self.cores)]
+        t0 = time.perf_counter()
+        self.pool.map(_idx_oracle_worker, shards)
+        return time.perf_counter() - t0
+
+
+def indexer_oracle_sample(rows_info, config: int):
+    """Scored rows for one oracle step: all for configs 1 and 2, a seeded
+    1/32 sample of the scored rows otherwise (FLOPs scaled by the sample's
+    share of the scored positions)."""
+    import numpy as np
+    scored = [i for i, (_, sc) in enumerate(rows_info) if sc]
+    if config in (1, 2) or len(scored) < 64:
+        return scored, f"all {len(scored)} scored rows of the workload"
+    rng = np.random.default_rng(config)
+    pick = sorted(rng.choice(len(scored), len(scored) // 32, replace=False).tolist())
+    rows = [scored[i] for i in pick]
+    return rows, f"seeded sample of {len(rows)} of {len(scored)} scored rows (1/32), scaled by FLOPs"
+
+
+def indexer_costs(case, rows_info):
+    """Algorithmic FLOPs and bytes of one indexer step: the score contraction
+    over scored (row, position) pairs, and the HBM bytes of Q, K and the
+    weights of scored rows, the logits written and read back once, and the
+    lists written."""
+    h, d = case.q_idx.shape[1], case.q_idx.shape[2]
+    scored_pos = sum(v for v, sc in rows_info if sc)
+    scored_rows = sum(1 for _, sc in rows_info if sc)
+    flops = 2.0 * h * d * scored_pos
+    byts = (scored_rows * h * (d * 2 + 4) + case.k_idx.shape[0] * d * 2 + scored_pos * 4 * 2
+            + len(rows_info) * case.topk * 4)
+    return flops, byts, scored_pos, scored_rows
+
+
+def run_indexer(args, rank, world, dist):
+    import torch
+    import serving_sparse_mla_gb300 as smla
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    smla.load()   # raises if the CUDA library is missing: no fallback
+    pool = None
+    if rank == 0 and not args.no_cpu_baseline:
+        pool = IndexerOraclePool(args.config, os.cpu_count() or 1)
+
+    case = indexer_workload(args.config)
+    info = indexer_rows(case)
+    flops, byts, scored_pos, scored_rows = indexer_costs(case, info)
+    total_q, total_kv = case.q_idx.shape[0], case.k_idx.shape[0]
+    longest = case.max_seqlen_kv
+    stream = torch.cuda.current_stream(dev)
+    inputs = {"q": case.q_idx.to(dev), "k": case.k_idx.to(dev), "w": case.weights.to(dev)}
+    if case.cu_seqlens_q is not None:
+        inputs.update(cq=case.cu_seqlens_q.to(dev), ck=case.cu_seqlens_kv.to(dev))
+    need = smla.dsa_indexer_workspace_size(total_q, longest, case.topk)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)     # one chunk: every row's logits
+    idx = torch.empty((total_q, case.topk), dtype=torch.int32, device=dev)
+    stride = (longest + 3) // 4 * 4
+    logits = ws[:max(need, 16)].view(torch.float32)[:max(need, 16) // 4]
+    first = 0 if case.cu_seqlens_q is not None else max(0, min(total_q, case.topk - (total_kv - total_q)))
+
+    def call(inp):
+        smla.dsa_indexer_topk(inp["q"], inp["k"], inp["w"], case.topk, inp.get("cq"), inp.get("ck"), longest,
+                              workspace=ws, indices=idx, stream=stream)
+
+    def scores_only(inp):
+        # the launch dsa_indexer_topk makes for the scores of its one chunk
+        smla.dsa_indexer_scores(inp["q"], inp["k"], inp["w"], inp.get("cq"), inp.get("ck"), row0=first,
+                                n_rows=total_q - first, skip_len=case.topk,
+                                scores=logits[:(total_q - first) * stride].view(total_q - first, stride),
+                                max_seqlen_kv=longest, stream=stream)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed_loop(k, body, flush_l2=True):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+        for i in range(k):
+            if flush_l2:
+                flush.zero_()
+            starts[i].record(stream)
+            body()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        call(inputs)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local, args.clock_log or tempfile.gettempdir())
+    nvml = NvmlClockSampler(dev)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    nvml.start()
+    times = timed_loop(args.steps, lambda: call(inputs))
+    torch.cuda.synchronize(dev)
+    nvml_clocks = nvml.stop()
+    barrier()
+    smi_clocks = sampler.stop()
+    clocks = nvml_clocks or smi_clocks
+    # the dominant kernel alone (scores), same launch, for the roofline
+    sc_times = timed_loop(args.steps, lambda: scores_only(inputs)) if scored_rows else []
+
+    host = {k: v.cpu().pin_memory() for k, v in inputs.items()}
+    dev2 = {k: torch.empty_like(v) for k, v in inputs.items()}
+    res_h = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = idx.numel() * idx.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev2[k].copy_(host[k], non_blocking=True)
+        call(dev2)
+        res_h.copy_(idx, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e2e_times = timed_loop(args.steps, e2e_step)
+    barrier()
+    total_ms, e2e_ms = max_over_ranks([sum(times), sum(e2e_times)], dist, dev)
+    if rank != 0:
+        return 0
+
+    peaks, peak_kind = load_peaks()
+    p_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    p_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ms = total_ms / args.steps
+    roof_us = max(flops / (p_tf * 1e12), byts / (p_bw * 1e9)) * 1e6
+    roofline = None
+    if sc_times:
+        sc_ms = statistics.mean(sc_times)
+        sc_flops = flops
+        sc_bytes = scored_rows * case.q_idx.shape[1] * (case.q_idx.shape[2] * 2 + 4) + total_kv * 256 + scored_pos * 4
+        if sc_flops / (p_tf * 1e12) >= sc_bytes / (p_bw * 1e9):
+            ach = sc_flops / (sc_ms * 1e-3) / 1e12
+            roofline = {"bound": "tensor", "achieved": ach, "peak": p_tf, "unit": "TFLOP/s", "frac": ach / p_tf,
+                        "traffic": None, "kernel": "dsa_scores_kernel", "peak_kind": f"{peak_kind} bf16 (burst)",
+                        "algorithmic_flops_per_launch": sc_flops, "us_per_launch": sc_ms * 1e3}
+        else:
+            ach = sc_bytes / (sc_ms * 1e-3) / 1e9
+            roofline = {"bound": "hbm", "achieved": ach, "peak": p_bw, "unit": "GB/s", "frac": ach / p_bw,
+                        "traffic": None, "kernel": "dsa_scores_kernel", "peak_kind": f"{peak_kind} copy bandwidth",
+                        "algorithmic_bytes_per_launch": sc_bytes, "us_per_launch": sc_ms * 1e3}
+    cpu = None
+    if pool is not None:
+        rows, sample = indexer_oracle_sample(info, args.config)
+        wall = pool.run(rows)
+        part = sum(info[r][0] for r in rows) / max(1, scored_pos)
+        cpu = {"value": flops * part / wall / 1e12 if rows else None, "unit": "TFLOP/s", "cores": pool.cores,
+               "kind": "oracle", "sample": sample, "seconds": wall}
+        pool.close()
+    name = {1: "tiny prefill s_q=s_kv=64", 2: "mid prefill s_q=s_kv=2119", 3: "prefill s_q=s_kv=8192",
+            4: "packed varlen prefill 16384 tokens (8192,4096,2048,1024,1024)"}[args.config]
+    launches = 2 if scored_rows else 1
+    line = {
+        "metric": "DSA indexer scores + top-k TFLOP/s at topk=2048 (2*h_idx*d_idx per scored position)",
+        "value": whole_job_tflops(flops, args.steps, world, total_ms), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"DSA indexer {name} h_idx=64 d_idx=128 topk=2048 (lists for the sparse-MLA "
+                               f"forward; one logits chunk)", "seed": 1000 + args.config,
+                   "l2": "256 MB buffer written before every timed step (cold L2)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": ms * 1e3, "roofline_us": roof_us, "roofline_pct": 100.0 * roof_us / (ms * 1e3),
+        "scored_rows": scored_rows, "scored_positions": scored_pos, "algorithmic_bytes": byts,
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": flops * world / (e2e_ms / args.steps * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -587,6 +873,8 @@ def main():
         tdist.init_process_group(backend=backend)
         dist = tdist
     try:
+        if args.indexer:
+            return run_indexer(args, rank, world, dist)
         return run_ours(args, rank, world, dist)
     finally:
         if dist is not None:

@@ -230,6 +230,90 @@ sparse_mla_status_t sparse_mla_decode_noalloc(const void* q, const void* kv_cach
 /* Size in bytes of the scratch array sparse_mla_decode_noalloc uses. */
 size_t sparse_mla_decode_noalloc_max_scratch_bytes(void);
 
+/* ------------------------------------------------------------------------
+ * DSA indexer: the step that produces the index lists above.
+ *
+ * The pages name the indexer and its top-k ("[Feature] Add optional FlashMLA
+ * backend for DSA Sparse MLA", Changes: the TileLang indexer; "feat: add
+ * XTuner TileLang sparse MLA backend", Summary: DSA index production for
+ * short prefill, Copilot overview: prefill scores in query-row chunks under a
+ * logits budget) without printing its formula.  It is read as the DSA
+ * lightning indexer published with DeepSeek-V3.2: for query row t with
+ * indexer heads j < h_idx and one key per KV position s,
+ *
+ *   I[t,s] = sum_j weights[t,j] * max(0, q_idx[t,j,:] . k_idx[s,:])
+ *
+ * computed from bf16 q_idx and k_idx with fp32 accumulation and fp32
+ * weights.  Visibility is causal with the queries of a sequence at its end:
+ * local row t of a sequence with lq query rows and lk KV positions sees
+ * positions 0 .. t + lk - lq, i.e. V(t) = clip(t + lk - lq + 1, 0, lk).  Its
+ * list holds the topk visible positions of largest score, equal scores
+ * ranked by position (smaller first), in increasing position order, padded
+ * with -1; a row with V(t) <= topk lists 0 .. V(t)-1 and is never scored.
+ * Positions are local to the row's sequence, the convention of
+ * sparse_mla_fwd_varlen.
+ *
+ * Layout (all device pointers, row-major):
+ *   q_idx    bf16 [total_q, h_idx, d_idx]       16-byte aligned
+ *   k_idx    bf16 [total_kv, d_idx]             16-byte aligned
+ *   weights  fp32 [total_q, h_idx]              16-byte aligned
+ *   cu_seqlens_q / cu_seqlens_kv  int32 [batch + 1] packed-sequence offsets,
+ *            or both NULL for one dense sequence (total_q queries at the end
+ *            of total_kv positions; batch is then ignored).
+ * h_idx must be 16, 32 or 64 and d_idx 128 (else
+ * SPARSE_MLA_ERR_UNSUPPORTED_SHAPE); batch may not exceed 2048.  Offsets
+ * are trusted; a sequence longer than the caller's row length is cut to it
+ * and the device error word records 0x611.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Indexer scores of query rows row0 .. row0 + n_rows - 1 (the product path of
+ * dsa_indexer_topk, exported for testing and for callers that keep the
+ * logits).  Row r's scores for its positions 0 .. V-1 go to
+ * scores[(r - row0) * row_stride + s] (fp32); entries past V, and every
+ * entry of a row with V <= skip_len, are left as they were.  row_stride must
+ * be at least the longest visible length (else see above).  Nothing is
+ * allocated; launches on `stream`.
+ */
+sparse_mla_status_t dsa_indexer_scores(const void* q_idx, const void* k_idx, const float* weights,
+                                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                                       int total_q, int total_kv, int h_idx, int d_idx, int row0, int n_rows,
+                                       int skip_len, float* scores, long long row_stride, void* stream);
+
+/*
+ * Selection alone: the lists of rows row0 .. row0 + n_rows - 1 from their
+ * scores (layout of dsa_indexer_scores), written to
+ * indices[r * topk .. r * topk + topk - 1] (int32).  Rows with V <= topk get
+ * the identity list and their scores are not read (scores may be NULL when
+ * no row is longer).  Scores are compared as fp32 with -inf allowed; a NaN
+ * ranks above +inf.
+ */
+sparse_mla_status_t dsa_topk(const float* scores, long long row_stride, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_kv, int batch, int total_q, int total_kv, int row0,
+                             int n_rows, int topk, int32_t* indices, void* stream);
+
+/*
+ * Bytes of logits scratch that lets dsa_indexer_topk score every row in one
+ * pass: total_q rows of max_seqlen_kv rounded up to 4 floats.  0 when no
+ * row needs scoring (max_seqlen_kv <= topk).
+ */
+size_t dsa_indexer_workspace_size(int total_q, int max_seqlen_kv, int topk);
+
+/*
+ * Index lists of every query row: indices int32 [total_q, topk], written.
+ * max_seqlen_kv is the longest KV sequence (total_kv for a dense sequence).
+ * workspace (16-byte aligned, contents ignored) holds the logits of a chunk
+ * of query rows: with less than dsa_indexer_workspace_size bytes the rows are
+ * scored and selected in chunks of workspace_bytes / (4 * row length) rows
+ * (the logits budget); less than one row gives
+ * SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL.  The result does not depend on the
+ * chunking.  Nothing is allocated; launches on `stream`.
+ */
+sparse_mla_status_t dsa_indexer_topk(const void* q_idx, const void* k_idx, const float* weights,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                                     int total_q, int total_kv, int max_seqlen_kv, int h_idx, int d_idx, int topk,
+                                     int32_t* indices, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* sparse_mla_status_string(sparse_mla_status_t status);
 

@@ -1,9 +1,14 @@
-"""GB300 (sm_103a) DSA sparse-MLA attention forward: a C-ABI CUDA library
-(csrc/, include/sparse_mla.h) and its thin Python binding."""
+"""GB300 (sm_103a) DSA sparse-MLA attention (forward, backward) and the DSA
+indexer that produces its index lists: a C-ABI CUDA library (csrc/,
+include/sparse_mla.h) and its thin Python binding."""
 from .binding import (  # noqa: F401
     SparseMLAError,
     clear_device_error,
     decode_workspace_size,
+    dsa_indexer_scores,
+    dsa_indexer_topk,
+    dsa_indexer_workspace_size,
+    dsa_topk,
     get_device_error,
     load,
     set_wait_timeout_ns,

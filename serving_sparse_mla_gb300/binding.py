@@ -44,6 +44,13 @@ SIGNATURES = {
                                           c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                           c_void_p]),
     "sparse_mla_decode_noalloc_max_scratch_bytes": (c_size_t, []),
+    "dsa_indexer_scores": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                   c_int, c_int, c_int, c_int, c_int, c_void_p, ctypes.c_longlong, c_void_p]),
+    "dsa_topk": (c_int, [c_void_p, ctypes.c_longlong, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                         c_int, c_void_p, c_void_p]),
+    "dsa_indexer_workspace_size": (c_size_t, [c_int, c_int, c_int]),
+    "dsa_indexer_topk": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                 c_int, c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
     "sparse_mla_status_string": (ctypes.c_char_p, [c_int]),
     "sparse_mla_get_device_error": (c_int, [ctypes.POINTER(c_int)]),
     "sparse_mla_clear_device_error": (c_int, []),
@@ -251,6 +258,110 @@ def sparse_mla_decode(q, kv_cache, block_table, cache_seqlens, indices, sm_scale
                                max_blocks, num_blocks, _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "sparse_mla_decode")
     return out, lse
+
+
+# ---------------------------------------------------------------- DSA indexer
+
+def _seq_args(cu_seqlens_q, cu_seqlens_kv):
+    if (cu_seqlens_q is None) != (cu_seqlens_kv is None):
+        raise ValueError("give both cu_seqlens_q and cu_seqlens_kv, or neither")
+    if cu_seqlens_q is None:
+        return 1
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_kv, torch.int32, "cu_seqlens_kv")
+    return cu_seqlens_q.numel() - 1
+
+
+def _longest_kv(k_idx_rows: int, cu_seqlens_kv, max_seqlen_kv):
+    if max_seqlen_kv is not None:
+        return int(max_seqlen_kv)
+    if cu_seqlens_kv is None:
+        return int(k_idx_rows)
+    if cu_seqlens_kv.numel() < 2:
+        return 0
+    return int((cu_seqlens_kv[1:] - cu_seqlens_kv[:-1]).max().item())   # a device read
+
+
+def dsa_indexer_scores(q_idx, k_idx, weights, cu_seqlens_q=None, cu_seqlens_kv=None, row0: int = 0,
+                       n_rows: Optional[int] = None, skip_len: int = 0, scores=None,
+                       max_seqlen_kv: Optional[int] = None, stream=None):
+    """Indexer scores of rows row0 .. row0+n_rows-1: q_idx [total_q,h_idx,128]
+    bf16, k_idx [total_kv,128] bf16, weights [total_q,h_idx] fp32 ->
+    scores [n_rows, row_stride] fp32 (row_stride = longest KV sequence
+    rounded up to 4); positions a row does not see, and rows seeing at most
+    skip_len positions, keep the given contents (-inf when allocated here)."""
+    lib = load()
+    total_q, h_idx, d_idx = q_idx.shape
+    total_kv = k_idx.shape[0]
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(k_idx, torch.bfloat16, "k_idx")
+    _need(weights, torch.float32, "weights")
+    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv)
+    n_rows = total_q - row0 if n_rows is None else n_rows
+    stride = (_longest_kv(total_kv, cu_seqlens_kv, max_seqlen_kv) + 3) // 4 * 4
+    if scores is None:
+        scores = torch.full((n_rows, max(stride, 4)), float("-inf"), dtype=torch.float32, device=q_idx.device)
+    else:
+        _need(scores, torch.float32, "scores")
+    st = lib.dsa_indexer_scores(_ptr(q_idx), _ptr(k_idx), _ptr(weights), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+                                batch, total_q, total_kv, h_idx, d_idx, row0, n_rows, skip_len, _ptr(scores),
+                                scores.shape[-1], _stream(stream))
+    _check(st, "dsa_indexer_scores")
+    return scores
+
+
+def dsa_topk(scores, topk: int, total_q: int, total_kv: int, cu_seqlens_q=None, cu_seqlens_kv=None,
+             row0: int = 0, n_rows: Optional[int] = None, indices=None, stream=None):
+    """Lists of rows row0 .. row0+n_rows-1 from scores [n_rows, row_stride]
+    fp32 -> indices [total_q, topk] int32 (only those rows written)."""
+    lib = load()
+    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv)
+    if scores is not None:
+        _need(scores, torch.float32, "scores")
+    n_rows = total_q - row0 if n_rows is None else n_rows
+    dev = scores.device if scores is not None else torch.device("cuda")
+    if indices is None:
+        indices = torch.full((total_q, topk), -2, dtype=torch.int32, device=dev)
+    else:
+        _need(indices, torch.int32, "indices")
+    stride = scores.shape[-1] if scores is not None else 1
+    st = lib.dsa_topk(_ptr(scores), stride, _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), batch, total_q, total_kv,
+                      row0, n_rows, topk, _ptr(indices), _stream(stream))
+    _check(st, "dsa_topk")
+    return indices
+
+
+def dsa_indexer_workspace_size(total_q: int, max_seqlen_kv: int, topk: int) -> int:
+    return int(load().dsa_indexer_workspace_size(total_q, max_seqlen_kv, topk))
+
+
+def dsa_indexer_topk(q_idx, k_idx, weights, topk: int, cu_seqlens_q=None, cu_seqlens_kv=None,
+                     max_seqlen_kv: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
+                     indices=None, stream=None):
+    """Index lists [total_q, topk] int32 of every query row (scores and
+    top-k in query-row chunks sized by the workspace; a full-size workspace
+    is allocated when none is given)."""
+    lib = load()
+    total_q, h_idx, d_idx = q_idx.shape
+    total_kv = k_idx.shape[0]
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(k_idx, torch.bfloat16, "k_idx")
+    _need(weights, torch.float32, "weights")
+    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv)
+    longest = _longest_kv(total_kv, cu_seqlens_kv, max_seqlen_kv)
+    if indices is None:
+        indices = torch.empty((total_q, topk), dtype=torch.int32, device=q_idx.device)
+    else:
+        _need(indices, torch.int32, "indices")
+    if workspace is None:
+        need = lib.dsa_indexer_workspace_size(total_q, longest, topk)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_idx.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.dsa_indexer_topk(_ptr(q_idx), _ptr(k_idx), _ptr(weights), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+                              batch, total_q, total_kv, longest, h_idx, d_idx, topk, _ptr(indices),
+                              _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "dsa_indexer_topk")
+    return indices
 
 
 def get_device_error() -> int:

@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libsparse_mla_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 SOURCES = ["sparse_mla_api.cu"]
-DEPS = ["sparse_mla_api.cu", "fwd_kernel.cuh", "ptx.cuh"]
+DEPS = ["sparse_mla_api.cu", "fwd_kernel.cuh", "bwd_kernel.cuh", "indexer_kernel.cuh", "ptx.cuh"]
 
 
 def nvcc_path() -> str:

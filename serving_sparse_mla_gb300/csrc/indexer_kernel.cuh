@@ -1,0 +1,648 @@
+// DSA indexer scores and top-k selection for sm_103a (TMA + tcgen05).
+//
+// The step upstream of the sparse-MLA forward that produces its index
+// lists.  The pages name the indexer and its top-k ("[Feature] Add optional
+// FlashMLA backend for DSA Sparse MLA", Changes; "feat: add XTuner TileLang
+// sparse MLA backend", Summary and Copilot overview) without printing the
+// score formula; it is taken here as the DSA lightning indexer published
+// with DeepSeek-V3.2:
+//
+//   I[t,s] = sum_j w[t,j] * relu(q[t,j,:] . k[s,:])       (j < H_I, width 128)
+//
+// over the positions s query t may see (the s_q queries of a sequence are
+// the last s_q of its s_kv positions).  A row's list holds the topk visible
+// positions of largest score, equal scores ranked by position (smaller
+// first), written in increasing position order and padded with -1; a row
+// that sees at most topk positions takes all of them and is never scored.
+//
+// dsa_scores_kernel<H_I>: a dense contraction, so it runs on the tensor
+// cores.  A work item is a group of G = 256 / H_I consecutive query rows
+// (N = 256 columns: every head of every row) against up to 16 tiles of 128
+// positions of their sequence (M = 128):
+//
+//   S^T[128 x 256] = K_tile[128 x 128] . Q_group^T[128 x 256]    (fp32, TMEM)
+//
+//   warp 0      TMA: per item the group's Q (two 32 KB boxes, 128B swizzle)
+//               and its head weights (1-D bulk copy), then the K tiles (two
+//               16 KB boxes each) through a 4-deep ring that runs ahead
+//               across items.
+//   warp 1      one thread issues a tile's 8 MMAs (K = 16 each) into one of
+//               two 256-column TMEM accumulators and commits.
+//   warps 2..9  epilogue, lane = position: a thread reads its position's H_I
+//               products for half of the group's rows, frees the
+//               accumulator, applies relu and the row's head weights and
+//               stores the fp32 score into the row's logits row (32 lanes
+//               store 128 contiguous bytes).
+//
+// A persistent grid (at most one CTA per SM, ~212 KB of shared memory each)
+// walks items c, c + G, ....  Rows that see at most `skip_len` positions
+// get no tiles.  A group that straddles sequences is run as one segment per
+// sequence, each against that sequence's keys.
+//
+// dsa_topk_kernel: one CTA per query row.  Radix select of the topk largest
+// scores on the order-preserving integer image of fp32 (digits of 11, 11
+// and 10 bits, warp-aggregated shared-memory histograms; it stops as soon
+// as the threshold class is taken whole), then an ordered compaction that
+// writes the selected positions in increasing order, taking equal scores
+// at the threshold by position.  A row that fits is staged in shared
+// memory first.
+//
+// All waits of the scores kernel are bounded like the forward's; a CTA that
+// times out records an error, waits (bounded) for its copies and MMAs in
+// flight, frees TMEM and returns.
+#pragma once
+#include <cuda.h>
+
+#include "fwd_kernel.cuh"
+
+namespace smla {
+
+constexpr int kIdxD = 128;            // indexer head width
+constexpr int kIdxTile = 128;         // positions per K tile (the MMA's M)
+constexpr int kIdxN = 256;            // (row, head) columns of a group (the MMA's N)
+constexpr int kIdxChunkTiles = 16;    // tiles per item: 2048 positions
+constexpr int kIdxStages = 4;
+constexpr int kIdxMaxBatch = 2048;    // sequences whose offsets sit in shared memory
+constexpr int kIdxEpiWarp0 = 2;
+constexpr int kIdxThreads = 10 * 32;
+constexpr int kIdxTmemCols = 512;
+
+constexpr int kIdxQHalf = kIdxN * 128;                        // 256 rows x 64 columns (bf16)
+constexpr int kIdxKHalf = kIdxTile * 128;                     // 128 rows x 64 columns
+constexpr int kIdxKStage = 2 * kIdxKHalf;
+constexpr int kIdxQOff = 0;
+constexpr int kIdxKOff = kIdxQOff + 2 * kIdxQHalf;
+constexpr int kIdxWOff = kIdxKOff + kIdxStages * kIdxKStage;  // head weights [2][256] fp32
+constexpr int kIdxCuOff = kIdxWOff + 2 * kIdxN * 4;           // cu_q, cu_kv [kIdxMaxBatch + 1] each
+constexpr int kIdxMiscOff = kIdxCuOff + ((2 * (kIdxMaxBatch + 1) * 4 + 15) / 16) * 16;
+
+struct __align__(16) IdxMisc {
+  uint64_t q_full, q_empty, k_full[kIdxStages], k_empty[kIdxStages], acc_full[2], acc_empty[2], w_full[2],
+      w_empty[2], drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int prior_error;
+};
+
+constexpr int idx_smem_bytes() { return kIdxMiscOff + static_cast<int>(sizeof(IdxMisc)) + 1024; }
+static_assert(idx_smem_bytes() <= kMaxSmem, "smem budget (indexer scores)");
+static_assert(kIdxKOff % 1024 == 0 && kIdxKStage % 1024 == 0 && kIdxQHalf % 1024 == 0, "swizzled tiles");
+
+enum IdxErrCode : int {
+  kErrIdxProducerWait = 0x601,
+  kErrIdxMmaWait = 0x602,
+  kErrIdxEpilogueWait = 0x603,
+  kErrIdxRowTooLong = 0x611,   // a sequence sees more positions than a logits row holds
+};
+
+struct IdxParams {
+  CUtensorMap map_q;          // bf16 [total_q * h_idx, 128]: box {64, 256}, 128B swizzle
+  CUtensorMap map_k;          // bf16 [total_kv, 128]: box {64, 128}, 128B swizzle
+  const float* weights;       // [total_q, h_idx]
+  const int32_t* cu_q;        // [batch + 1], null for one dense sequence
+  const int32_t* cu_kv;
+  float* scores;              // [n_rows, row_stride]: row r - row0 holds row r's positions
+  long long row_stride;
+  int total_q, total_kv, batch, h_idx;
+  int row0, n_rows;           // the query rows of this launch
+  int skip_len;               // rows seeing <= skip_len positions are not scored
+  int groups;                 // ceil(n_rows / G)
+  int kv_chunks;              // ceil(longest KV sequence / 2048)
+  unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void idx_raise(IdxMisc& m, int code) {
+  *reinterpret_cast<volatile int*>(&m.abort_flag) = 1;
+  atomicCAS(&g_device_error, 0, code);
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Positions row r of sequence b sees: the sequence's queries are the last
+// lq of its lk positions.
+__device__ __forceinline__ int idx_visible(const int32_t* cq, const int32_t* ck, int b, int r) {
+  const int lq = cq[b + 1] - cq[b], lk = ck[b + 1] - ck[b];
+  const int v = r - cq[b] + lk - lq + 1;
+  return v < 0 ? 0 : (v > lk ? lk : v);
+}
+
+// Last b in [0, batch) with cq[b] <= r.
+__device__ __forceinline__ int idx_seq_of(const int32_t* cq, int batch, int r) {
+  int lo = 0, hi = batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cq[mid] <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// One run of a group's rows inside one sequence, with the tiles of the
+// item's chunk it needs (t0 == t1: none).
+struct IdxSeg {
+  int b, r_begin, r_end, kv_begin, t0, t1;
+};
+
+// The segments of item (group g, chunk c), in row order.  Every role walks
+// the same sequence.
+struct IdxWalk {
+  int r_first, r_stop, r, b, c;
+  __device__ __forceinline__ void start(const IdxParams& p, const int32_t* cq, long long item) {
+    const int g = static_cast<int>(item / p.kv_chunks);
+    c = static_cast<int>(item % p.kv_chunks);
+    const int G = kIdxN / p.h_idx;
+    r_first = p.row0 + g * G;
+    const int end = p.row0 + p.n_rows;
+    r_stop = r_first + G < end ? r_first + G : end;
+    r = r_first;
+    b = idx_seq_of(cq, p.batch, r_first);
+  }
+  __device__ __forceinline__ bool next(const IdxParams& p, const int32_t* cq, const int32_t* ck, IdxSeg& s) {
+    while (r < r_stop && b < p.batch) {
+      const int e = r_stop < cq[b + 1] ? r_stop : cq[b + 1];
+      if (e > r) {
+        s.b = b;
+        s.r_begin = r;
+        s.r_end = e;
+        s.kv_begin = ck[b];
+        long long v = idx_visible(cq, ck, b, e - 1);   // the segment's longest row
+        if (v > p.row_stride) v = p.row_stride;
+        s.t0 = s.t1 = c * kIdxChunkTiles;
+        if (v > p.skip_len) {
+          const int nt = static_cast<int>((v + kIdxTile - 1) / kIdxTile);
+          s.t1 = nt < s.t0 + kIdxChunkTiles ? nt : s.t0 + kIdxChunkTiles;
+          if (s.t1 < s.t0) s.t1 = s.t0;
+        }
+        r = e;
+        ++b;
+        return true;
+      }
+      ++b;
+    }
+    return false;
+  }
+};
+
+// ------------------------------------------------------------------ roles
+
+__device__ __forceinline__ bool idx_producer(const IdxParams& p, IdxMisc& m, uint32_t sb, const int32_t* cq,
+                                             const int32_t* ck, uint32_t& kcount, uint32_t& qcount,
+                                             uint32_t& wcount) {
+  const volatile int* ab = &m.abort_flag;
+  const long long n_items = static_cast<long long>(p.groups) * p.kv_chunks;
+  for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+    IdxWalk w;
+    w.start(p, cq, it);
+    IdxSeg s;
+    bool first = true;
+    while (w.next(p, cq, ck, s)) {
+      for (int t = s.t0; t < s.t1; ++t) {
+        if (first) {
+          first = false;
+          // the group's Q, once the previous item's MMAs have read it
+          if (!mbar_wait(smem_u32(&m.q_empty), (qcount & 1u) ^ 1u, deadline, ab)) return false;
+          mbar_arrive_expect_tx(smem_u32(&m.q_full), 2 * kIdxQHalf);
+          const int y = w.r_first * p.h_idx;
+          tma_load_2d(sb + kIdxQOff, &p.map_q, 0, y, smem_u32(&m.q_full));
+          tma_load_2d(sb + kIdxQOff + kIdxQHalf, &p.map_q, 64, y, smem_u32(&m.q_full));
+          ++qcount;
+          // its head weights, into the buffer the epilogue released
+          const uint32_t wb = wcount & 1u;
+          if (!mbar_wait(smem_u32(&m.w_empty[wb]), ((wcount >> 1) & 1u) ^ 1u, deadline, ab)) return false;
+          const uint32_t bytes = static_cast<uint32_t>((w.r_stop - w.r_first) * p.h_idx) * 4u;
+          mbar_arrive_expect_tx(smem_u32(&m.w_full[wb]), bytes);
+          bulk_load(sb + kIdxWOff + wb * kIdxN * 4, p.weights + static_cast<long long>(w.r_first) * p.h_idx, bytes,
+                    smem_u32(&m.w_full[wb]));
+          ++wcount;
+        }
+        const uint32_t slot = kcount % kIdxStages;
+        if (!mbar_wait(smem_u32(&m.k_empty[slot]), ((kcount / kIdxStages) & 1u) ^ 1u, deadline, ab)) return false;
+        mbar_arrive_expect_tx(smem_u32(&m.k_full[slot]), kIdxKStage);
+        const int y = s.kv_begin + t * kIdxTile;
+        const uint32_t dst = sb + kIdxKOff + slot * kIdxKStage;
+        tma_load_2d(dst, &p.map_k, 0, y, smem_u32(&m.k_full[slot]));
+        tma_load_2d(dst + kIdxKHalf, &p.map_k, 64, y, smem_u32(&m.k_full[slot]));
+        ++kcount;
+      }
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool idx_mma(const IdxParams& p, IdxMisc& m, uint32_t sb, uint32_t tmem,
+                                        const int32_t* cq, const int32_t* ck) {
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kIdxTile, kIdxN, false, false);
+  const volatile int* ab = &m.abort_flag;
+  uint32_t kcount = 0, acount = 0, qcount = 0;
+  const long long n_items = static_cast<long long>(p.groups) * p.kv_chunks;
+  for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+    IdxWalk w;
+    w.start(p, cq, it);
+    IdxSeg s;
+    bool q_ready = false;
+    while (w.next(p, cq, ck, s)) {
+      for (int t = s.t0; t < s.t1; ++t) {
+        if (!q_ready) {
+          if (!mbar_wait(smem_u32(&m.q_full), qcount & 1u, deadline, ab)) return false;
+          q_ready = true;
+        }
+        const uint32_t slot = kcount % kIdxStages;
+        if (!mbar_wait(smem_u32(&m.k_full[slot]), (kcount / kIdxStages) & 1u, deadline, ab)) return false;
+        const uint32_t buf = acount & 1u;
+        if (!mbar_wait(smem_u32(&m.acc_empty[buf]), ((acount >> 1) & 1u) ^ 1u, deadline, ab)) return false;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * kIdxN;
+        const uint32_t ka = sb + kIdxKOff + slot * kIdxKStage;
+#pragma unroll
+        for (int kk = 0; kk < kIdxD / 16; ++kk) {
+          const uint32_t half = static_cast<uint32_t>(kk >> 2), off = static_cast<uint32_t>(kk & 3) * 32u;
+          const uint64_t a = smem_desc(ka + half * kIdxKHalf + off, 16, 1024, SWZ_128B);
+          const uint64_t b = smem_desc(sb + kIdxQOff + half * kIdxQHalf + off, 16, 1024, SWZ_128B);
+          mma_bf16_ss(d, a, b, kIdesc, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&m.k_empty[slot]));
+        mma_commit(smem_u32(&m.acc_full[buf]));
+        ++kcount;
+        ++acount;
+      }
+    }
+    if (q_ready) {
+      mma_commit(smem_u32(&m.q_empty));
+      ++qcount;
+    }
+  }
+  return true;
+}
+
+// Epilogue warp e (0..7): TMEM lane quarter = warp % 4, rows of the group's
+// half e / 4.
+template <int H>
+__device__ __forceinline__ bool idx_epilogue(const IdxParams& p, IdxMisc& m, const uint8_t* sbase, uint32_t tmem,
+                                             const int32_t* cq, const int32_t* ck, int e) {
+  constexpr int G = kIdxN / H;
+  constexpr int GH = G / 2;   // rows per half
+  const volatile int* ab = &m.abort_flag;
+  const int lane = static_cast<int>(lane_id());
+  const int quarter = static_cast<int>(threadIdx.x >> 5) & 3;
+  const int half = e >> 2;
+  const float* wsm = reinterpret_cast<const float*>(sbase + kIdxWOff);
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  uint32_t acount = 0, wcount = 0;
+  const long long n_items = static_cast<long long>(p.groups) * p.kv_chunks;
+  for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+    IdxWalk w;
+    w.start(p, cq, it);
+    IdxSeg s;
+    bool first = true;
+    const float* wb = wsm;
+    while (w.next(p, cq, ck, s)) {
+      if (s.t1 <= s.t0) continue;
+      if (first) {
+        first = false;
+        const uint32_t b = wcount & 1u;
+        if (!mbar_wait(smem_u32(&m.w_full[b]), (wcount >> 1) & 1u, deadline, ab)) return false;
+        wb = wsm + b * kIdxN;
+      }
+      // this half's rows in the segment and the positions each sees
+      int vis[GH];
+      bool on[GH];
+#pragma unroll
+      for (int jj = 0; jj < GH; ++jj) {
+        const int r = w.r_first + half * GH + jj;
+        on[jj] = r >= s.r_begin && r < s.r_end;
+        long long v = on[jj] ? idx_visible(cq, ck, s.b, r) : 0;
+        if (v > p.row_stride) {
+          if (lane == 0) atomicCAS(&g_device_error, 0, static_cast<int>(kErrIdxRowTooLong));
+          v = p.row_stride;
+        }
+        on[jj] = on[jj] && v > p.skip_len;
+        vis[jj] = static_cast<int>(v);
+      }
+      for (int t = s.t0; t < s.t1; ++t) {
+        const uint32_t buf = acount & 1u;
+        if (!mbar_wait(smem_u32(&m.acc_full[buf]), (acount >> 1) & 1u, deadline, ab)) return false;
+        tc_fence_after();
+        float x[GH][H];
+#pragma unroll
+        for (int jj = 0; jj < GH; ++jj) {
+          if (!on[jj]) continue;   // warp-uniform
+          const uint32_t col = buf * kIdxN + static_cast<uint32_t>((half * GH + jj) * H);
+          if constexpr (H == 16) {
+            tmem_ld16(lane_base + col, x[jj]);
+          } else {
+#pragma unroll
+            for (int h = 0; h < H; h += 32) tmem_ld32(lane_base + col + h, x[jj] + h);
+          }
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&m.acc_empty[buf]));
+        ++acount;
+        const int pos = t * kIdxTile + quarter * 32 + lane;
+#pragma unroll
+        for (int jj = 0; jj < GH; ++jj) {
+          if (!on[jj]) continue;
+          const float* wr = wb + (half * GH + jj) * H;
+          float sc = 0.0f;
+#pragma unroll
+          for (int h = 0; h < H; h += 4) {
+            const float4 wv = *reinterpret_cast<const float4*>(wr + h);
+            sc = fmaf(wv.x, fmaxf(x[jj][h + 0], 0.0f), sc);
+            sc = fmaf(wv.y, fmaxf(x[jj][h + 1], 0.0f), sc);
+            sc = fmaf(wv.z, fmaxf(x[jj][h + 2], 0.0f), sc);
+            sc = fmaf(wv.w, fmaxf(x[jj][h + 3], 0.0f), sc);
+          }
+          if (pos < vis[jj]) {
+            const int r = w.r_first + half * GH + jj;
+            p.scores[static_cast<long long>(r - p.row0) * p.row_stride + pos] = sc;
+          }
+        }
+      }
+    }
+    if (!first) {
+      // every read of this item's weights is done
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&m.w_empty[wcount & 1u]));
+      ++wcount;
+    }
+  }
+  return true;
+}
+
+template <int H>
+__global__ void __launch_bounds__(kIdxThreads, 1) dsa_scores_kernel(const __grid_constant__ IdxParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  IdxMisc& m = *reinterpret_cast<IdxMisc*>(sbase + kIdxMiscOff);
+  int32_t* cq = reinterpret_cast<int32_t*>(sbase + kIdxCuOff);
+  int32_t* ck = cq + (kIdxMaxBatch + 1);
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(lane_id());
+  const uint32_t sb = smem_u32(sbase);
+
+  if (p.cu_q != nullptr) {
+    for (int i = static_cast<int>(threadIdx.x); i <= p.batch; i += kIdxThreads) {
+      cq[i] = p.cu_q[i];
+      ck[i] = p.cu_kv[i];
+    }
+  } else if (threadIdx.x == 0) {
+    cq[0] = 0;
+    cq[1] = p.total_q;
+    ck[0] = 0;
+    ck[1] = p.total_kv;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&m.q_full), 1);
+    mbar_init(smem_u32(&m.q_empty), 1);
+    for (int i = 0; i < kIdxStages; ++i) {
+      mbar_init(smem_u32(&m.k_full[i]), 1);
+      mbar_init(smem_u32(&m.k_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&m.acc_full[i]), 1);
+      mbar_init(smem_u32(&m.acc_empty[i]), 8);   // one arrival per epilogue warp
+      mbar_init(smem_u32(&m.w_full[i]), 1);
+      mbar_init(smem_u32(&m.w_empty[i]), 8);
+    }
+    mbar_init(smem_u32(&m.drain), 1);
+    m.abort_flag = 0;
+    m.prior_error = *reinterpret_cast<volatile int*>(&g_device_error);
+    fence_mbar_init();
+    prefetch_tmap(&p.map_q);
+    prefetch_tmap(&p.map_k);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&m.tmem_base), kIdxTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = m.tmem_base;
+
+  if (m.prior_error == 0) {
+    if (warp == 0) {
+      if (lane == 0) {
+        uint32_t kcount = 0, qcount = 0, wcount = 0;
+        if (!idx_producer(p, m, sb, cq, ck, kcount, qcount, wcount)) idx_raise(m, kErrIdxProducerWait);
+        // Drain: the copies this thread issued have landed before the CTA
+        // exits, whether or not the consumers got to them (only the last
+        // fill of each buffer can still be in flight).
+        const int never = 0;
+        const uint64_t dl = global_timer_ns() + 100000000ull;
+        for (uint32_t i = kcount > kIdxStages ? kcount - kIdxStages : 0; i < kcount; ++i)
+          mbar_wait(smem_u32(&m.k_full[i % kIdxStages]), (i / kIdxStages) & 1u, dl, &never);
+        if (qcount > 0) mbar_wait(smem_u32(&m.q_full), (qcount - 1) & 1u, dl, &never);
+        for (uint32_t i = wcount > 2 ? wcount - 2 : 0; i < wcount; ++i)
+          mbar_wait(smem_u32(&m.w_full[i & 1u]), (i >> 1) & 1u, dl, &never);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) {
+        if (!idx_mma(p, m, sb, tmem, cq, ck)) idx_raise(m, kErrIdxMmaWait);
+        // Drain: every MMA issued completes before TMEM is freed.
+        const int never = 0;
+        mma_commit(smem_u32(&m.drain));
+        mbar_wait(smem_u32(&m.drain), 0, global_timer_ns() + 100000000ull, &never);
+      }
+      __syncwarp();
+    } else {
+      if (!idx_epilogue<H>(p, m, sbase, tmem, cq, ck, warp - kIdxEpiWarp0)) idx_raise(m, kErrIdxEpilogueWait);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kIdxTmemCols);
+}
+
+// ------------------------------------------------------------------ top-k
+
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkBins = 2048;
+
+struct TopkParams {
+  const float* scores;        // [n_rows, row_stride]
+  int32_t* indices;           // [total_q, topk]: rows row0 .. row0 + n_rows - 1 are written
+  const int32_t* cu_q;        // [batch + 1], null for one dense sequence
+  const int32_t* cu_kv;
+  long long row_stride;
+  int total_q, total_kv, batch;
+  int row0, n_rows, topk;
+  int stage_cap;              // rows of at most this many positions are staged in shared memory
+};
+
+// Order-preserving image of an fp32 score: a < b as floats iff key(a) <
+// key(b) as unsigned integers (NaN images sort by their bit pattern).
+__device__ __forceinline__ uint32_t topk_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive block-wide count of `flag` below this thread, and the total.
+__device__ __forceinline__ void topk_scan(bool flag, int* sh, int& excl, int& total) {
+  const uint32_t bal = __ballot_sync(0xffffffffu, flag);
+  const int lane = static_cast<int>(lane_id()), w = static_cast<int>(threadIdx.x >> 5);
+  if (lane == 0) sh[w] = __popc(bal);
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < kTopkWarps; ++i) {
+    const int c = sh[i];
+    before += i < w ? c : 0;
+    tot += c;
+  }
+  __syncthreads();
+  excl = before + __popc(bal & ((1u << lane) - 1u));
+  total = tot;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) dsa_topk_kernel(const __grid_constant__ TopkParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);          // [kTopkBins]
+  float* stage = reinterpret_cast<float*>(smem_raw + kTopkBins * 4);
+  __shared__ int sh_scan[kTopkWarps];
+  __shared__ int sh_seq;
+  __shared__ uint32_t sh_bin;
+  __shared__ int sh_krem;
+  const int tid = static_cast<int>(threadIdx.x);
+  const int r = p.row0 + static_cast<int>(blockIdx.x);
+
+  // the row's sequence and visible length
+  if (tid == 0) sh_seq = p.cu_q == nullptr ? 0 : -1;
+  __syncthreads();
+  if (p.cu_q != nullptr) {
+    for (int i = tid; i < p.batch; i += kTopkThreads)
+      if (p.cu_q[i] <= r && r < p.cu_q[i + 1]) sh_seq = i;
+  }
+  __syncthreads();
+  const int b = sh_seq;
+  long long v = 0;
+  if (b >= 0) {
+    int cq2[2] = {0, p.total_q}, ck2[2] = {0, p.total_kv};
+    if (p.cu_q != nullptr) {
+      cq2[0] = p.cu_q[b];
+      cq2[1] = p.cu_q[b + 1];
+      ck2[0] = p.cu_kv[b];
+      ck2[1] = p.cu_kv[b + 1];
+    }
+    v = idx_visible(cq2, ck2, 0, r);
+  }
+  int32_t* out = p.indices + static_cast<long long>(r) * p.topk;
+  if (v > p.topk && p.scores == nullptr) {   // called for short rows only, but this one is longer
+    if (tid == 0) atomicCAS(&g_device_error, 0, static_cast<int>(kErrIdxRowTooLong));
+    v = p.topk;
+  }
+  if (v <= p.topk) {
+    for (int i = tid; i < p.topk; i += kTopkThreads) out[i] = i < v ? i : -1;
+    return;
+  }
+  if (v > p.row_stride) {
+    if (tid == 0) atomicCAS(&g_device_error, 0, static_cast<int>(kErrIdxRowTooLong));
+    v = p.row_stride;
+  }
+  const int n = static_cast<int>(v);
+  const float* row = p.scores + static_cast<long long>(blockIdx.x) * p.row_stride;
+  const float* src = row;
+  if (n <= p.stage_cap) {
+    for (int i = tid; i < n; i += kTopkThreads) stage[i] = row[i];
+    src = stage;
+  }
+
+  // radix select: the class of keys that shares the threshold's top bits
+  uint32_t prefix = 0, pmask = 0;
+  int krem = p.topk;
+  const int lane = static_cast<int>(lane_id());
+  for (int d = 0; d < 3; ++d) {
+    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
+    const int nbins = d == 2 ? 1024 : 2048;
+    for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += kTopkThreads) {
+      const int s = base + tid;
+      uint32_t key = 0;
+      bool act = false;
+      if (s < n) {
+        key = topk_key(src[s]);
+        act = (key & pmask) == prefix;
+      }
+      const uint32_t am = __ballot_sync(0xffffffffu, act);
+      if (act) {
+        const uint32_t bin = (key >> shift) & static_cast<uint32_t>(nbins - 1);
+        const uint32_t peers = __match_any_sync(am, bin);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
+      }
+    }
+    __syncthreads();
+    // the bin holding the krem-th largest key of the class: each thread owns
+    // a run of bins; counts above a thread's run by a suffix scan
+    const int per = nbins / kTopkThreads;
+    int own = 0;
+    for (int i = 0; i < per; ++i) own += static_cast<int>(hist[tid * per + i]);
+    int incl = own;   // suffix sum within the warp (lanes above and this one)
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    const int w = tid >> 5;
+    if (lane == 0) sh_scan[w] = incl;   // the warp's total
+    __syncthreads();
+    int above_w = 0;
+#pragma unroll
+    for (int i = 0; i < kTopkWarps; ++i) above_w += i > w ? sh_scan[i] : 0;
+    const int above = above_w + incl - own;   // keys of the class in bins above this thread's run
+    if (above < krem && krem <= above + own) {
+      int acc = above;
+      for (int i = per - 1; i >= 0; --i) {
+        const int c = static_cast<int>(hist[tid * per + i]);
+        if (krem <= acc + c) {
+          sh_bin = static_cast<uint32_t>(tid * per + i);
+          sh_krem = krem - acc;
+          break;
+        }
+        acc += c;
+      }
+    }
+    __syncthreads();
+    const uint32_t bin = sh_bin;
+    krem = sh_krem;
+    prefix |= bin << shift;
+    pmask |= static_cast<uint32_t>(nbins - 1) << shift;
+    const bool whole = static_cast<int>(hist[bin]) == krem;
+    __syncthreads();   // hist and the scan slots are rewritten next
+    if (whole) break;
+  }
+
+  // ordered compaction: keys above the class, then the first krem of the
+  // class by position
+  int eq_before = 0, out_before = 0;
+  for (int base = 0; base < n && out_before < p.topk; base += kTopkThreads) {
+    const int s = base + tid;
+    bool gt = false, eq = false;
+    if (s < n) {
+      const uint32_t hi = topk_key(src[s]) & pmask;
+      gt = hi > prefix;
+      eq = hi == prefix;
+    }
+    int eq_excl, eq_tot;
+    topk_scan(eq, sh_scan, eq_excl, eq_tot);
+    const bool take = gt || (eq && eq_before + eq_excl < krem);
+    int t_excl, t_tot;
+    topk_scan(take, sh_scan, t_excl, t_tot);
+    if (take) out[out_before + t_excl] = s;
+    eq_before += eq_tot;
+    out_before += t_tot;
+  }
+}
+
+}  // namespace smla

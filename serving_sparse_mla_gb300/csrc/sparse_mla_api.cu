@@ -1,6 +1,7 @@
 // C-ABI entry points: host-side validation, launch
 // planning (head-group width, persistent grid size and schedule) and
 // launches on the caller's stream.  See include/sparse_mla.h for the contract of each call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -11,6 +12,7 @@
 
 #include "bwd_kernel.cuh"
 #include "fwd_kernel.cuh"
+#include "indexer_kernel.cuh"
 #include "sparse_mla.h"
 
 namespace {
@@ -30,6 +32,10 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// Top-k kernel: histogram plus a staged row of up to kTopkStageCap scores.
+constexpr int kTopkStageCap = 12288;
+constexpr int kTopkMaxSmem = smla::kTopkBins * 4 + kTopkStageCap * 4;
 
 sparse_mla_status_t device_setup(int* sm_count) {
   int dev = 0;
@@ -55,7 +61,15 @@ sparse_mla_status_t device_setup(int* sm_count) {
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::smem_bytes<64>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smla::bwd_smem_bytes()) != cudaSuccess)
+                             smla::bwd_smem_bytes()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::dsa_scores_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::idx_smem_bytes()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::dsa_scores_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::idx_smem_bytes()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::dsa_scores_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::idx_smem_bytes()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::dsa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTopkMaxSmem) != cudaSuccess)
       return SPARSE_MLA_ERR_CUDA;
     st.attrs_set = true;
   }
@@ -470,5 +484,232 @@ sparse_mla_status_t sparse_mla_clear_device_error(void) {
 }
 
 void sparse_mla_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs); }
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ DSA indexer
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+sparse_mla_status_t get_encode(EncodeTiledFn* fn) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || f == nullptr)
+      return SPARSE_MLA_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  *fn = g_encode;
+  return SPARSE_MLA_OK;
+}
+
+// A 2-D bf16 tensor [rows, 128] read in boxes of 64 columns x box_rows rows,
+// 128B-swizzled (the K-major layout the MMA descriptors expect); boxes past
+// the last row read zeros.
+sparse_mla_status_t encode_rows128(EncodeTiledFn enc, CUtensorMap* map, const void* base, long long rows,
+                                   int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(smla::kIdxD), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(smla::kIdxD) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SPARSE_MLA_OK : SPARSE_MLA_ERR_INVALID_ARG;
+}
+
+bool idx_heads_ok(int h_idx) { return h_idx == 16 || h_idx == 32 || h_idx == 64; }
+
+// Shape and pointer checks shared by the indexer entry points.
+sparse_mla_status_t check_indexer(const void* q_idx, const void* k_idx, const float* weights,
+                                  const int32_t* cu_q, const int32_t* cu_kv, int batch, int total_q, int total_kv,
+                                  int h_idx, int d_idx) {
+  if (total_q < 0 || total_kv < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (d_idx != smla::kIdxD || !idx_heads_ok(h_idx)) return SPARSE_MLA_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(total_q) * h_idx + smla::kIdxN > INT_MAX ||
+      static_cast<long long>(total_kv) + smla::kIdxTile * smla::kIdxChunkTiles > INT_MAX)
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  if ((cu_q == nullptr) != (cu_kv == nullptr)) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (cu_q != nullptr) {
+    if (batch < 1 || !aligned(cu_q, 4) || !aligned(cu_kv, 4)) return SPARSE_MLA_ERR_INVALID_ARG;
+    if (batch > smla::kIdxMaxBatch) return SPARSE_MLA_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (total_q > 0 && total_kv > 0) {
+    if (!q_idx || !k_idx || !weights) return SPARSE_MLA_ERR_INVALID_ARG;
+    if (!aligned(q_idx, 16) || !aligned(k_idx, 16) || !aligned(weights, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  }
+  return SPARSE_MLA_OK;
+}
+
+sparse_mla_status_t launch_scores(const void* q_idx, const void* k_idx, const float* weights, const int32_t* cu_q,
+                                  const int32_t* cu_kv, int batch, int total_q, int total_kv, int h_idx, int row0,
+                                  int n_rows, int skip_len, float* scores, long long row_stride, int sms,
+                                  cudaStream_t cs) {
+  if (n_rows <= 0 || total_kv <= 0) return SPARSE_MLA_OK;
+  EncodeTiledFn enc = nullptr;
+  sparse_mla_status_t st = get_encode(&enc);
+  if (st != SPARSE_MLA_OK) return st;
+  smla::IdxParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((st = encode_rows128(enc, &p.map_q, q_idx, static_cast<long long>(total_q) * h_idx, smla::kIdxN)) !=
+      SPARSE_MLA_OK)
+    return st;
+  if ((st = encode_rows128(enc, &p.map_k, k_idx, total_kv, smla::kIdxTile)) != SPARSE_MLA_OK) return st;
+  p.weights = weights;
+  p.cu_q = cu_q;
+  p.cu_kv = cu_kv;
+  p.scores = scores;
+  p.row_stride = row_stride;
+  p.total_q = total_q;
+  p.total_kv = total_kv;
+  p.batch = cu_q ? batch : 1;
+  p.h_idx = h_idx;
+  p.row0 = row0;
+  p.n_rows = n_rows;
+  p.skip_len = skip_len;
+  const int G = smla::kIdxN / h_idx;
+  p.groups = (n_rows + G - 1) / G;
+  const long long longest = row_stride < total_kv ? row_stride : total_kv;
+  const long long span = static_cast<long long>(smla::kIdxTile) * smla::kIdxChunkTiles;
+  p.kv_chunks = static_cast<int>((longest + span - 1) / span);
+  if (p.kv_chunks < 1) p.kv_chunks = 1;
+  unsigned long long t = g_timeout_ns.load();
+  p.timeout_ns = t ? t : kDefaultTimeoutNs;
+  const long long items = static_cast<long long>(p.groups) * p.kv_chunks;
+  const int ctas = static_cast<int>(items < sms ? items : sms);
+  if (h_idx == 16)
+    smla::dsa_scores_kernel<16><<<ctas, smla::kIdxThreads, smla::idx_smem_bytes(), cs>>>(p);
+  else if (h_idx == 32)
+    smla::dsa_scores_kernel<32><<<ctas, smla::kIdxThreads, smla::idx_smem_bytes(), cs>>>(p);
+  else
+    smla::dsa_scores_kernel<64><<<ctas, smla::kIdxThreads, smla::idx_smem_bytes(), cs>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+}
+
+sparse_mla_status_t launch_topk(const float* scores, long long row_stride, const int32_t* cu_q, const int32_t* cu_kv,
+                                int batch, int total_q, int total_kv, int row0, int n_rows, int topk,
+                                int32_t* indices, cudaStream_t cs) {
+  if (n_rows <= 0) return SPARSE_MLA_OK;
+  smla::TopkParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.scores = scores;
+  p.indices = indices;
+  p.cu_q = cu_q;
+  p.cu_kv = cu_kv;
+  p.row_stride = row_stride;
+  p.total_q = total_q;
+  p.total_kv = total_kv;
+  p.batch = cu_q ? batch : 1;
+  p.row0 = row0;
+  p.n_rows = n_rows;
+  p.topk = topk;
+  const long long longest = row_stride < total_kv ? row_stride : total_kv;
+  p.stage_cap = static_cast<int>(longest < kTopkStageCap ? longest : kTopkStageCap);
+  const int smem = smla::kTopkBins * 4 + p.stage_cap * 4;
+  smla::dsa_topk_kernel<<<n_rows, smla::kTopkThreads, smem, cs>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+}
+
+long long idx_row_stride(int max_seqlen_kv) { return (static_cast<long long>(max_seqlen_kv) + 3) / 4 * 4; }
+
+}  // namespace
+
+extern "C" {
+
+sparse_mla_status_t dsa_indexer_scores(const void* q_idx, const void* k_idx, const float* weights,
+                                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                                       int total_q, int total_kv, int h_idx, int d_idx, int row0, int n_rows,
+                                       int skip_len, float* scores, long long row_stride, void* stream) {
+  sparse_mla_status_t st = check_indexer(q_idx, k_idx, weights, cu_seqlens_q, cu_seqlens_kv, batch, total_q,
+                                         total_kv, h_idx, d_idx);
+  if (st != SPARSE_MLA_OK) return st;
+  if (row0 < 0 || n_rows < 0 || static_cast<long long>(row0) + n_rows > total_q || skip_len < 0 || row_stride < 1)
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_rows > 0 && total_kv > 0 && (!scores || !aligned(scores, 4))) return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  return launch_scores(q_idx, k_idx, weights, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, h_idx, row0,
+                       n_rows, skip_len, scores, row_stride, sms, static_cast<cudaStream_t>(stream));
+}
+
+sparse_mla_status_t dsa_topk(const float* scores, long long row_stride, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_kv, int batch, int total_q, int total_kv, int row0,
+                             int n_rows, int topk, int32_t* indices, void* stream) {
+  if (total_q < 0 || total_kv < 0 || topk < 1 || row0 < 0 || n_rows < 0 ||
+      static_cast<long long>(row0) + n_rows > total_q || row_stride < 1)
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  if ((cu_seqlens_q == nullptr) != (cu_seqlens_kv == nullptr)) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (cu_seqlens_q != nullptr && (batch < 1 || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_kv, 4)))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(total_q) * topk > (1LL << 62)) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_rows > 0 && (!indices || !aligned(indices, 4))) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_rows > 0 && total_kv > topk && (!scores || !aligned(scores, 4))) return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  sparse_mla_status_t st = device_setup(&sms);
+  if (st != SPARSE_MLA_OK) return st;
+  return launch_topk(scores, row_stride, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, row0, n_rows, topk,
+                     indices, static_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_indexer_workspace_size(int total_q, int max_seqlen_kv, int topk) {
+  if (total_q < 1 || max_seqlen_kv < 1 || topk < 1 || max_seqlen_kv <= topk) return 0;
+  return static_cast<size_t>(total_q) * static_cast<size_t>(idx_row_stride(max_seqlen_kv)) * sizeof(float);
+}
+
+sparse_mla_status_t dsa_indexer_topk(const void* q_idx, const void* k_idx, const float* weights,
+                                     const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, int batch,
+                                     int total_q, int total_kv, int max_seqlen_kv, int h_idx, int d_idx, int topk,
+                                     int32_t* indices, void* workspace, size_t workspace_bytes, void* stream) {
+  sparse_mla_status_t st = check_indexer(q_idx, k_idx, weights, cu_seqlens_q, cu_seqlens_kv, batch, total_q,
+                                         total_kv, h_idx, d_idx);
+  if (st != SPARSE_MLA_OK) return st;
+  if (topk < 1 || max_seqlen_kv < 0 || max_seqlen_kv > total_kv) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (cu_seqlens_q == nullptr && max_seqlen_kv != total_kv) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(total_q) * topk > (1LL << 62)) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (total_q > 0 && (!indices || !aligned(indices, 4))) return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (total_q == 0) return SPARSE_MLA_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (max_seqlen_kv <= topk)   // every row is short: identity lists, no scores
+    return launch_topk(nullptr, 1, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, 0, total_q, topk, indices,
+                       cs);
+  const long long stride = idx_row_stride(max_seqlen_kv);
+  if (!workspace || !aligned(workspace, 16)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
+  long long rows = static_cast<long long>(workspace_bytes / (static_cast<size_t>(stride) * sizeof(float)));
+  if (rows < 1) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (rows > total_q) rows = total_q;
+  // One dense sequence: rows before first_long see at most topk positions.
+  long long first_long = 0;
+  if (cu_seqlens_q == nullptr) {
+    first_long = static_cast<long long>(topk) - (total_kv - total_q);
+    if (first_long < 0) first_long = 0;
+    if (first_long > total_q) first_long = total_q;
+  }
+  float* ws = static_cast<float*>(workspace);
+  // Query rows in chunks whose logits fit the workspace (the logits budget).
+  for (long long r0 = 0; r0 < total_q; r0 += rows) {
+    const int n = static_cast<int>(total_q - r0 < rows ? total_q - r0 : rows);
+    if (r0 + n > first_long) {
+      const long long s0 = r0 > first_long ? r0 : first_long;   // scored rows of this chunk start here
+      if ((st = launch_scores(q_idx, k_idx, weights, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, h_idx,
+                              static_cast<int>(s0), static_cast<int>(r0 + n - s0), topk,
+                              ws + (s0 - r0) * stride, stride, sms, cs)) != SPARSE_MLA_OK)
+        return st;
+    }
+    if ((st = launch_topk(ws, stride, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, static_cast<int>(r0), n,
+                          topk, indices, cs)) != SPARSE_MLA_OK)
+      return st;
+  }
+  return SPARSE_MLA_OK;
+}
 
 }  // extern "C"

@@ -23,7 +23,7 @@ def declared_functions():
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names += re.findall(r"\b(sparse_mla_\w+)\s*\(", text)
+        names += re.findall(r"\b((?:sparse_mla|dsa)_\w+)\s*\(", text)
     return sorted(set(names))
 
 
@@ -100,3 +100,55 @@ def test_varlen_and_decode_validation(lib):
 def test_workspace_size_rejects_bad_shapes(lib):
     assert lib.sparse_mla_decode_workspace_size(0, 6, 8, 512, 2048) == 0
     assert lib.sparse_mla_decode_workspace_size(4, 6, 8, 256, 2048) == 0
+
+
+def test_indexer_validation(lib):
+    def scores(**kw):
+        a = dict(q=16, k=16, w=16, cq=None, ck=None, batch=1, tq=8, tk=40, h=64, d=128, row0=0, n=8, skip=0,
+                 out=16, stride=40, stream=None)
+        a.update(kw)
+        return lib.dsa_indexer_scores(a["q"], a["k"], a["w"], a["cq"], a["ck"], a["batch"], a["tq"], a["tk"],
+                                      a["h"], a["d"], a["row0"], a["n"], a["skip"], a["out"], a["stride"],
+                                      a["stream"])
+    assert scores(d=64) == 2
+    assert scores(h=48) == 2
+    assert scores(cq=16) == 1            # one offset array without the other
+    assert scores(cq=16, ck=16, batch=4096) == 2
+    assert scores(q=24) == 1             # not 16-byte aligned
+    assert scores(w=8) == 1
+    assert scores(row0=4, n=5) == 1      # past the last row
+    assert scores(skip=-1) == 1
+    assert scores(stride=0) == 1
+    assert scores(tq=-1) == 1
+
+    def topk(**kw):
+        a = dict(sc=16, stride=40, cq=None, ck=None, batch=1, tq=8, tk=40, row0=0, n=8, topk=16, idx=16,
+                 stream=None)
+        a.update(kw)
+        return lib.dsa_topk(a["sc"], a["stride"], a["cq"], a["ck"], a["batch"], a["tq"], a["tk"], a["row0"],
+                            a["n"], a["topk"], a["idx"], a["stream"])
+    assert topk(topk=0) == 1
+    assert topk(ck=16) == 1
+    assert topk(n=9) == 1
+    assert topk(idx=None) == 1
+    assert topk(idx=18) == 1
+    assert topk(sc=None) == 1            # rows longer than topk need scores
+
+    def fused(**kw):
+        a = dict(q=16, k=16, w=16, cq=None, ck=None, batch=1, tq=8, tk=40, ms=40, h=64, d=128, topk=16, idx=16,
+                 ws=16, wsb=4096, stream=None)
+        a.update(kw)
+        return lib.dsa_indexer_topk(a["q"], a["k"], a["w"], a["cq"], a["ck"], a["batch"], a["tq"], a["tk"],
+                                    a["ms"], a["h"], a["d"], a["topk"], a["idx"], a["ws"], a["wsb"], a["stream"])
+    assert fused(ms=41) == 1             # longer than the keys
+    assert fused(ms=20) == 1             # one dense sequence: its length is total_kv
+    assert fused(topk=0) == 1
+    assert fused(h=8) == 2
+    assert fused(idx=None) == 1
+
+
+def test_indexer_workspace_size(lib):
+    assert lib.dsa_indexer_workspace_size(10, 4097, 2048) == 10 * 4100 * 4
+    assert lib.dsa_indexer_workspace_size(10, 4096, 2048) == 10 * 4096 * 4
+    assert lib.dsa_indexer_workspace_size(10, 2048, 2048) == 0      # no row is scored
+    assert lib.dsa_indexer_workspace_size(0, 4096, 2048) == 0

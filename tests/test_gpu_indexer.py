@@ -1,0 +1,242 @@
+"""GPU parity of the DSA indexer (dsa_indexer_scores, dsa_topk,
+dsa_indexer_topk through the C ABI) against the float64 oracle on the same
+seeded inputs.
+
+* Selection alone is integer work: on fp32 scores given to both sides (tied
+  integer levels, -inf holes, distinct normal draws, rows past the
+  shared-memory staging size) the lists must be identical.
+* Scores: per element, |gpu - oracle| <= sum_j |w_j| (2^-16 sum_d |q_jd k_d|)
+  + 2^-18 sum_j |w_j| relu(q_j . k): the worst case of an fp32 sum of 128
+  bf16 products (each exact in fp32) in any order even with truncating
+  adders (128 * 2^-23), then the fp32 weighted sum of H_I terms.
+* Lists from GPU scores: valid lists (increasing, distinct, visible, the
+  right count; short rows the identity list), every selected position's
+  oracle score at least every unselected one's up to the two bounds, and
+  identical to the oracle's list wherever the oracle's gap at the top-k
+  boundary exceeds twice the row's largest bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+from oracle import dsa_indexer_oracle as ido
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+GAMMA_DOT = 2.0 ** -16
+GAMMA_SUM = 2.0 ** -18
+
+
+@pytest.fixture(scope="module")
+def smla(cuda_lib):
+    import serving_sparse_mla_gb300 as pkg
+    pkg.clear_device_error()
+    yield pkg
+    assert pkg.get_device_error() == 0
+
+
+def _dev(c):
+    cq = None if c.cu_seqlens_q is None else c.cu_seqlens_q.to(DEV)
+    ck = None if c.cu_seqlens_kv is None else c.cu_seqlens_kv.to(DEV)
+    return c.q_idx.to(DEV), c.k_idx.to(DEV), c.weights.to(DEV), cq, ck
+
+
+def _row_meta(c, r):
+    """(sequence KV start, visible length) of packed row r."""
+    if c.cu_seqlens_q is None:
+        return 0, ido.visible_len(r, c.q_idx.shape[0], c.k_idx.shape[0])
+    cq, ck = c.cu_seqlens_q.tolist(), c.cu_seqlens_kv.tolist()
+    b = int(np.searchsorted(cq, r, side="right")) - 1
+    return ck[b], ido.visible_len(r - cq[b], cq[b + 1] - cq[b], ck[b + 1] - ck[b])
+
+
+def _row_ref(c, r):
+    """Oracle scores of row r over its visible positions and their bounds."""
+    k0, v = _row_meta(c, r)
+    q = c.q_idx[r].double().numpy()
+    w = c.weights[r].double().numpy()
+    k = c.k_idx[k0:k0 + v].double().numpy()
+    ref = ido.token_scores(q, w, k)
+    dots = q @ k.T
+    bound = np.abs(w) @ (GAMMA_DOT * (np.abs(q) @ np.abs(k).T)) + GAMMA_SUM * (np.abs(w) @ np.maximum(dots, 0.0))
+    return ref, bound + 1e-30, v
+
+
+def _check_scores(c, got, rows, row0=0):
+    for r in rows:
+        ref, bound, v = _row_ref(c, r)
+        g = got[r - row0]
+        err = np.abs(g[:v].astype(np.float64) - ref)
+        bad = np.nonzero(err > bound)[0]
+        assert bad.size == 0, (f"row {r}: {bad.size} scores off, first pos {bad[0]}: gpu {g[bad[0]]} "
+                               f"oracle {ref[bad[0]]} bound {bound[bad[0]]}")
+        assert np.all(np.isneginf(g[v:])), f"row {r}: positions past {v} were written"
+
+
+def _check_list(c, lst, r, topk):
+    """Validity, ordering against the oracle scores, exactness when unique.
+    Returns True when the row was checked exactly."""
+    _, v = _row_meta(c, r)
+    lst = np.asarray(lst)
+    n = min(topk, v)
+    assert np.all(lst[n:] == -1), f"row {r}: padding"
+    sel = lst[:n]
+    assert np.all(sel >= 0) and np.all(sel < v), f"row {r}: out of range"
+    assert np.all(np.diff(sel) > 0), f"row {r}: not increasing"
+    if v <= topk:
+        np.testing.assert_array_equal(sel, np.arange(v))
+        return True
+    ref, bound, _ = _row_ref(c, r)
+    chosen = np.zeros(v, dtype=bool)
+    chosen[sel] = True
+    lo = (ref + bound)[chosen].min()
+    hi = (ref - bound)[~chosen].max()
+    assert lo >= hi, f"row {r}: a selected score falls below an unselected one beyond the bounds"
+    srt = np.sort(ref)[::-1]
+    if srt[topk - 1] - srt[topk] > 2.0 * bound.max():
+        np.testing.assert_array_equal(sel, ido.select_topk(ref, topk)[:n])
+        return True
+    return False
+
+
+# --------------------------------------------------------------------------- selection alone
+
+def _lens_dense(s_q, s_kv):
+    return [ido.visible_len(t, s_q, s_kv) for t in range(s_q)]
+
+
+@pytest.mark.parametrize("rows,width,topk", [(40, 300, 16), (64, 3000, 2048), (33, 2500, 1),
+                                             (20, 2049, 2048), (24, 700, 650)])
+def test_topk_tied_scores_exact(smla, rows, width, topk):
+    """Integer levels with many ties at the threshold and -inf holes."""
+    sc = mi.tied_scores(rows * 7 + width, rows, width)
+    got = smla.dsa_topk(sc.to(DEV), topk, rows, width).cpu().numpy()
+    ref = ido.topk_rows(sc.numpy(), _lens_dense(rows, width), topk)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_topk_distinct_and_unstaged_rows_exact(smla):
+    """Distinct normal scores; rows longer than the shared-memory staging
+    (12288 positions) are read from global memory on every pass."""
+    g = torch.Generator().manual_seed(501)
+    rows, width, topk = 12, 20000, 2048
+    sc = torch.randn((rows, width), generator=g)
+    got = smla.dsa_topk(sc.to(DEV), topk, rows, width).cpu().numpy()
+    ref = ido.topk_rows(sc.numpy(), _lens_dense(rows, width), topk)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_topk_constant_row_takes_first_positions(smla):
+    sc = torch.zeros((3, 5000))
+    sc[1] = float("-inf")
+    got = smla.dsa_topk(sc.to(DEV), 100, 3, 5000).cpu().numpy()
+    for i in range(3):
+        np.testing.assert_array_equal(got[i], np.arange(100))
+
+
+def test_topk_varlen_exact(smla):
+    q_lens, kv_lens = [3, 40, 1, 17, 60], [3, 900, 2100, 40, 60]
+    cq = torch.tensor(np.concatenate([[0], np.cumsum(q_lens)]), dtype=torch.int32)
+    ck = torch.tensor(np.concatenate([[0], np.cumsum(kv_lens)]), dtype=torch.int32)
+    total_q, total_kv, width = int(cq[-1]), int(ck[-1]), max(kv_lens)
+    sc = mi.tied_scores(502, total_q, width, levels=40)
+    lens = []
+    for b in range(5):
+        lens += [ido.visible_len(t, q_lens[b], kv_lens[b]) for t in range(q_lens[b])]
+    got = smla.dsa_topk(sc.to(DEV), 32, total_q, total_kv, cq.to(DEV), ck.to(DEV)).cpu().numpy()
+    np.testing.assert_array_equal(got, ido.topk_rows(sc.numpy(), lens, 32))
+
+
+def test_topk_row_range(smla):
+    """Only rows row0 .. row0 + n_rows - 1 are written."""
+    sc = mi.tied_scores(503, 10, 400)
+    out = torch.full((30, 64), -7, dtype=torch.int32, device=DEV)
+    smla.dsa_topk(sc.to(DEV), 64, 30, 400, row0=12, n_rows=10, indices=out)
+    o = out.cpu().numpy()
+    assert np.all(o[:12] == -7) and np.all(o[22:] == -7)
+    lens = [ido.visible_len(t, 30, 400) for t in range(12, 22)]
+    np.testing.assert_array_equal(o[12:22], ido.topk_rows(sc.numpy(), lens, 64))
+
+
+# --------------------------------------------------------------------------- scores
+
+@pytest.mark.parametrize("h_idx", [64, 32, 16])
+def test_scores_dense(smla, h_idx):
+    """Several 128-position tiles and chunks of 2048, ragged tails, a cached
+    prefix (s_kv > s_q), every row scored."""
+    c = mi.indexer_case(510 + h_idx, 37, 2300, h_idx=h_idx)
+    got = smla.dsa_indexer_scores(*_dev(c)).cpu().numpy()
+    _check_scores(c, got, range(37))
+
+
+def test_scores_square_causal_and_empty_rows(smla):
+    c = mi.indexer_case(520, 300, 260)    # 40 queries before position 0 see nothing
+    got = smla.dsa_indexer_scores(*_dev(c)).cpu().numpy()
+    _check_scores(c, got, list(range(0, 45)) + list(range(290, 300)))
+
+
+def test_scores_skip_len_and_row_range(smla):
+    c = mi.indexer_case(521, 200, 200)
+    got = smla.dsa_indexer_scores(*_dev(c), row0=50, n_rows=101, skip_len=100).cpu().numpy()
+    assert got.shape[0] == 101
+    assert np.all(np.isneginf(got[:50]))           # rows 50..99 see <= 100 positions: skipped
+    _check_scores(c, got, range(100, 151), row0=50)
+
+
+def test_scores_varlen_groups_straddle_sequences(smla):
+    c = mi.indexer_varlen_case(522, [5, 130, 3, 77, 1], [300, 130, 2100, 77, 9])
+    got = smla.dsa_indexer_scores(*_dev(c)).cpu().numpy()
+    _check_scores(c, got, range(int(c.cu_seqlens_q[-1])))
+
+
+# --------------------------------------------------------------------------- lists
+
+def test_indexer_topk_dense(smla):
+    c = mi.indexer_case(530, 600, 2600, topk=2048)     # rows 0..47 short, the rest scored
+    lst = smla.dsa_indexer_topk(*_dev(c)[:3], 2048).cpu().numpy()
+    exact = sum(_check_list(c, lst[r], r, 2048) for r in range(0, 600, 7))
+    assert exact >= 25
+
+
+def test_indexer_topk_chunked_equals_unchunked(smla):
+    c = mi.indexer_case(531, 300, 2400, topk=512)
+    q, k, w, _, _ = _dev(c)
+    full = smla.dsa_indexer_topk(q, k, w, 512)
+    ws = torch.empty(7 * 2400 * 4 + 5, dtype=torch.uint8, device=DEV)    # 7 rows of logits per chunk
+    part = smla.dsa_indexer_topk(q, k, w, 512, workspace=ws)
+    assert torch.equal(full, part)
+    for r in (0, 1, 150, 299):
+        _check_list(c, full[r].cpu().numpy(), r, 512)
+
+
+def test_indexer_topk_varlen(smla):
+    c = mi.indexer_varlen_case(532, [50, 300, 9, 200], [3000, 300, 2500, 200], topk=256)
+    q, k, w, cq, ck = _dev(c)
+    lst = smla.dsa_indexer_topk(q, k, w, 256, cq, ck).cpu().numpy()
+    exact = sum(_check_list(c, lst[r], r, 256) for r in range(0, 559, 3))
+    assert exact >= 120
+
+
+def test_indexer_topk_all_short(smla):
+    """Every row sees <= topk positions: identity lists, no workspace."""
+    c = mi.indexer_case(533, 100, 120, topk=2048)
+    lst = smla.dsa_indexer_topk(*_dev(c)[:3], 2048, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    lst = lst.cpu().numpy()
+    for r in range(100):
+        v = ido.visible_len(r, 100, 120)
+        np.testing.assert_array_equal(lst[r, :v], np.arange(v))
+        assert np.all(lst[r, v:] == -1)
+
+
+def test_indexer_topk_full_size_sampled(smla):
+    """The 8192-token prefill at topk 2048 with 64 indexer heads, in 1024-row
+    logits chunks; sampled rows against the oracle."""
+    c = mi.indexer_case(534, 8192, 8192, topk=2048)
+    q, k, w, _, _ = _dev(c)
+    ws = torch.empty(1024 * 8192 * 4, dtype=torch.uint8, device=DEV)
+    lst = smla.dsa_indexer_topk(q, k, w, 2048, workspace=ws).cpu().numpy()
+    rows = [0, 2047, 2048, 2049, 3000, 4095, 5555, 8191]
+    exact = sum(_check_list(c, lst[r], r, 2048) for r in rows)
+    assert exact >= 3

@@ -17,7 +17,7 @@
 //
 // dsa_scores_kernel<H_I>: a dense contraction, so it runs on the tensor
 // cores.  A work item is a group of G = 256 / H_I consecutive query rows
-// (N = 256 columns: every head of every row) against up to 16 tiles of 128
+// (N = 256 columns: every head of every row) against up to 32 tiles of 128
 // positions of their sequence (M = 128):
 //
 //   S^T[128 x 256] = K_tile[128 x 128] . Q_group^T[128 x 256]    (fp32, TMEM)
@@ -29,23 +29,25 @@
 //   warp 1      one thread issues a tile's 8 MMAs (K = 16 each) into one of
 //               two 256-column TMEM accumulators and commits.
 //   warps 2..9  epilogue, lane = position: a thread reads its position's H_I
-//               products for half of the group's rows, frees the
-//               accumulator, applies relu and the row's head weights and
-//               stores the fp32 score into the row's logits row (32 lanes
-//               store 128 contiguous bytes).
+//               products for half of the group's rows (64 columns at a
+//               time; the accumulator is freed once the last are read),
+//               applies relu and the row's head weights (packed fp32 FMAs)
+//               and stores the fp32 score into the row's logits row (32
+//               lanes store 128 contiguous bytes).
 //
 // A persistent grid (at most one CTA per SM, ~212 KB of shared memory each)
-// walks items c, c + G, ....  Rows that see at most `skip_len` positions
+// walks items c, c + G, ... (largest groups first); while an item runs, its
+// successor's Q is prefetched into L2.  Rows that see at most `skip_len` positions
 // get no tiles.  A group that straddles sequences is run as one segment per
 // sequence, each against that sequence's keys.
 //
-// dsa_topk_kernel: one CTA per query row.  Radix select of the topk largest
-// scores on the order-preserving integer image of fp32 (digits of 11, 11
-// and 10 bits, warp-aggregated shared-memory histograms; it stops as soon
-// as the threshold class is taken whole), then an ordered compaction that
-// writes the selected positions in increasing order, taking equal scores
-// at the threshold by position.  A row that fits is staged in shared
-// memory first.
+// dsa_topk_kernel: one CTA per query row.  The row's order-preserving
+// integer keys (the image of fp32) are staged in shared memory when they
+// fit; a radix select of the topk largest then counts digits of 11, 11 and
+// 10 bits in shared-memory histograms (each pass over the keys still in
+// the threshold class, stopping as soon as the class is taken whole), and
+// an ordered compaction writes the selected positions in increasing order,
+// taking equal scores at the threshold by position.
 //
 // All waits of the scores kernel are bounded like the forward's; a CTA that
 // times out records an error, waits (bounded) for its copies and MMAs in
@@ -60,7 +62,7 @@ namespace smla {
 constexpr int kIdxD = 128;            // indexer head width
 constexpr int kIdxTile = 128;         // positions per K tile (the MMA's M)
 constexpr int kIdxN = 256;            // (row, head) columns of a group (the MMA's N)
-constexpr int kIdxChunkTiles = 16;    // tiles per item: 2048 positions
+constexpr int kIdxChunkTiles = 32;    // tiles per item: 4096 positions
 constexpr int kIdxStages = 4;
 constexpr int kIdxMaxBatch = 2048;    // sequences whose offsets sit in shared memory
 constexpr int kIdxEpiWarp0 = 2;
@@ -107,7 +109,7 @@ struct IdxParams {
   int row0, n_rows;           // the query rows of this launch
   int skip_len;               // rows seeing <= skip_len positions are not scored
   int groups;                 // ceil(n_rows / G)
-  int kv_chunks;              // ceil(longest KV sequence / 2048)
+  int kv_chunks;              // ceil(longest KV sequence / 4096)
   unsigned long long timeout_ns;
 };
 
@@ -120,6 +122,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// (c0, c1) += (a0 * b0, a1 * b1): one packed fp32 FMA, each lane rounded
+// as fmaf.
+__device__ __forceinline__ void ffma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 pa, pb, pc;\n\t"
+      "mov.b64 pa, {%2, %3};\n\t"
+      "mov.b64 pb, {%4, %5};\n\t"
+      "mov.b64 pc, {%0, %1};\n\t"
+      "fma.rn.f32x2 pc, pa, pb, pc;\n\t"
+      "mov.b64 {%0, %1}, pc;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // Positions row r of sequence b sees: the sequence's queries are the last
@@ -151,9 +166,14 @@ struct IdxSeg {
 // the same sequence.
 struct IdxWalk {
   int r_first, r_stop, r, b, c;
+  // Items are dealt chunk by chunk (every group's first 4096 positions,
+  // then every group's next 4096, ...), and within a chunk the last groups
+  // first: with causal rows the later groups see more positions, so every
+  // CTA's share runs from large items to small and no CTA collects only
+  // the short chunks.
   __device__ __forceinline__ void start(const IdxParams& p, const int32_t* cq, long long item) {
-    const int g = static_cast<int>(item / p.kv_chunks);
-    c = static_cast<int>(item % p.kv_chunks);
+    const int g = p.groups - 1 - static_cast<int>(item % p.groups);
+    c = static_cast<int>(item / p.groups);
     const int G = kIdxN / p.h_idx;
     r_first = p.row0 + g * G;
     const int end = p.row0 + p.n_rows;
@@ -211,6 +231,15 @@ __device__ __forceinline__ bool idx_producer(const IdxParams& p, IdxMisc& m, uin
           tma_load_2d(sb + kIdxQOff, &p.map_q, 0, y, smem_u32(&m.q_full));
           tma_load_2d(sb + kIdxQOff + kIdxQHalf, &p.map_q, 64, y, smem_u32(&m.q_full));
           ++qcount;
+          // the next item's Q into L2, so its load after this item's MMAs is short
+          if (it + gridDim.x < n_items) {
+            IdxWalk nx;
+            nx.start(p, cq, it + gridDim.x);
+            if (nx.r_first != w.r_first) {
+              tma_prefetch_2d(&p.map_q, 0, nx.r_first * p.h_idx);
+              tma_prefetch_2d(&p.map_q, 64, nx.r_first * p.h_idx);
+            }
+          }
           // its head weights, into the buffer the epilogue released
           const uint32_t wb = wcount & 1u;
           if (!mbar_wait(smem_u32(&m.w_empty[wb]), ((wcount >> 1) & 1u) ^ 1u, deadline, ab)) return false;
@@ -329,42 +358,53 @@ __device__ __forceinline__ bool idx_epilogue(const IdxParams& p, IdxMisc& m, con
         const uint32_t buf = acount & 1u;
         if (!mbar_wait(smem_u32(&m.acc_full[buf]), (acount >> 1) & 1u, deadline, ab)) return false;
         tc_fence_after();
-        float x[GH][H];
-#pragma unroll
-        for (int jj = 0; jj < GH; ++jj) {
-          if (!on[jj]) continue;   // warp-uniform
-          const uint32_t col = buf * kIdxN + static_cast<uint32_t>((half * GH + jj) * H);
-          if constexpr (H == 16) {
-            tmem_ld16(lane_base + col, x[jj]);
-          } else {
-#pragma unroll
-            for (int h = 0; h < H; h += 32) tmem_ld32(lane_base + col + h, x[jj] + h);
-          }
-        }
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&m.acc_empty[buf]));
-        ++acount;
+        // Rows in batches of 64 columns (RB rows): load a batch from TMEM,
+        // reduce it, store; the accumulator is freed once the last batch is
+        // in registers.
+        constexpr int RB = H >= 64 ? 1 : 64 / H;
+        constexpr int NB = GH / RB;
         const int pos = t * kIdxTile + quarter * 32 + lane;
 #pragma unroll
-        for (int jj = 0; jj < GH; ++jj) {
-          if (!on[jj]) continue;
-          const float* wr = wb + (half * GH + jj) * H;
-          float sc = 0.0f;
+        for (int bt = 0; bt < NB; ++bt) {
+          float x[RB][H];
 #pragma unroll
-          for (int h = 0; h < H; h += 4) {
-            const float4 wv = *reinterpret_cast<const float4*>(wr + h);
-            sc = fmaf(wv.x, fmaxf(x[jj][h + 0], 0.0f), sc);
-            sc = fmaf(wv.y, fmaxf(x[jj][h + 1], 0.0f), sc);
-            sc = fmaf(wv.z, fmaxf(x[jj][h + 2], 0.0f), sc);
-            sc = fmaf(wv.w, fmaxf(x[jj][h + 3], 0.0f), sc);
+          for (int rr = 0; rr < RB; ++rr) {
+            const int jj = bt * RB + rr;
+            if (!on[jj]) continue;   // warp-uniform
+            const uint32_t col = buf * kIdxN + static_cast<uint32_t>((half * GH + jj) * H);
+            if constexpr (H == 16) {
+              tmem_ld16(lane_base + col, x[rr]);
+            } else {
+#pragma unroll
+              for (int h = 0; h < H; h += 32) tmem_ld32(lane_base + col + h, x[rr] + h);
+            }
           }
-          if (pos < vis[jj]) {
-            const int r = w.r_first + half * GH + jj;
-            p.scores[static_cast<long long>(r - p.row0) * p.row_stride + pos] = sc;
+          tmem_wait_ld();
+          if (bt == NB - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&m.acc_empty[buf]));
+          }
+#pragma unroll
+          for (int rr = 0; rr < RB; ++rr) {
+            const int jj = bt * RB + rr;
+            if (!on[jj]) continue;
+            const float* wr = wb + (half * GH + jj) * H;
+            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;   // four partial sums (two f32x2 pairs)
+#pragma unroll
+            for (int h = 0; h < H; h += 4) {
+              const float4 wv = *reinterpret_cast<const float4*>(wr + h);
+              ffma2(a0, a1, fmaxf(x[rr][h + 0], 0.0f), fmaxf(x[rr][h + 1], 0.0f), wv.x, wv.y);
+              ffma2(a2, a3, fmaxf(x[rr][h + 2], 0.0f), fmaxf(x[rr][h + 3], 0.0f), wv.z, wv.w);
+            }
+            const float sc = (a0 + a1) + (a2 + a3);
+            if (pos < vis[jj]) {
+              const int r = w.r_first + half * GH + jj;
+              p.scores[static_cast<long long>(r - p.row0) * p.row_stride + pos] = sc;
+            }
           }
         }
+        ++acount;
       }
     }
     if (!first) {
@@ -466,7 +506,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1) dsa_scores_kernel(const __grid
 
 // ------------------------------------------------------------------ top-k
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkBins = 2048;
 
@@ -478,54 +518,197 @@ struct TopkParams {
   long long row_stride;
   int total_q, total_kv, batch;
   int row0, n_rows, topk;
-  int stage_cap;              // rows of at most this many positions are staged in shared memory
+  int stage_cap;              // rows of at most this many positions are staged (a multiple of 4)
 };
 
 // Order-preserving image of an fp32 score: a < b as floats iff key(a) <
 // key(b) as unsigned integers (NaN images sort by their bit pattern).
 __device__ __forceinline__ uint32_t topk_key(float f) {
   const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return u ^ ((u & 0x80000000u) ? 0xFFFFFFFFu : 0x80000000u);
 }
 
-// Exclusive block-wide count of `flag` below this thread, and the total.
-__device__ __forceinline__ void topk_scan(bool flag, int* sh, int& excl, int& total) {
-  const uint32_t bal = __ballot_sync(0xffffffffu, flag);
-  const int lane = static_cast<int>(lane_id()), w = static_cast<int>(threadIdx.x >> 5);
-  if (lane == 0) sh[w] = __popc(bal);
-  __syncthreads();
-  int before = 0, tot = 0;
+// Shared state of one row's selection.
+struct TopkShared {
+  int scan[kTopkWarps];
+  int scan2[kTopkWarps];
+  int seq, krem;
+  uint32_t bin;
+};
+
+// The bin of `hist` (nbins bins, counts of the current class) that holds
+// the class's krem-th largest key, and krem's rank inside it.  Thread t
+// owns bins [t per, t per + per); the counts above come from a suffix scan.
+// Ends with the block synchronised and sh.bin / sh.krem set.
+__device__ __forceinline__ void topk_find_bin(const uint32_t* hist, int nbins, int krem, TopkShared& sh) {
+  const int tid = static_cast<int>(threadIdx.x), lane = static_cast<int>(lane_id()), w = tid >> 5;
+  const int per = nbins / kTopkThreads;
+  int own = 0;
+  for (int i = 0; i < per; ++i) own += static_cast<int>(hist[tid * per + i]);
+  int incl = own;   // over this lane and the lanes above it
 #pragma unroll
-  for (int i = 0; i < kTopkWarps; ++i) {
-    const int c = sh[i];
-    before += i < w ? c : 0;
-    tot += c;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  if (lane == 0) sh.scan[w] = incl;
+  __syncthreads();
+  int above = incl - own;
+#pragma unroll
+  for (int i = 0; i < kTopkWarps; ++i) above += i > w ? sh.scan[i] : 0;
+  if (above < krem && krem <= above + own) {
+    int acc = above;
+    for (int i = per - 1; i >= 0; --i) {
+      const int c = static_cast<int>(hist[tid * per + i]);
+      if (krem <= acc + c) {
+        sh.bin = static_cast<uint32_t>(tid * per + i);
+        sh.krem = krem - acc;
+        break;
+      }
+      acc += c;
+    }
   }
   __syncthreads();
-  excl = before + __popc(bal & ((1u << lane) - 1u));
-  total = tot;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) dsa_topk_kernel(const __grid_constant__ TopkParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);          // [kTopkBins]
-  float* stage = reinterpret_cast<float*>(smem_raw + kTopkBins * 4);
-  __shared__ int sh_scan[kTopkWarps];
-  __shared__ int sh_seq;
-  __shared__ uint32_t sh_bin;
-  __shared__ int sh_krem;
+// Four consecutive keys starting at position 4 q (q < ceil(n / 4)); keys at
+// or past n read as 0 and are masked by the callers.
+template <bool kStaged>
+__device__ __forceinline__ uint4 topk_keys4(const uint32_t* keys, const float* row, int q, int n) {
+  if constexpr (kStaged) {
+    return reinterpret_cast<const uint4*>(keys)[q];
+  } else {
+    uint4 k;
+    const int s = 4 * q;
+    k.x = s + 0 < n ? topk_key(row[s + 0]) : 0u;
+    k.y = s + 1 < n ? topk_key(row[s + 1]) : 0u;
+    k.z = s + 2 < n ? topk_key(row[s + 2]) : 0u;
+    k.w = s + 3 < n ? topk_key(row[s + 3]) : 0u;
+    return k;
+  }
+}
+
+// Exclusive prefix over the block (in thread order) of two per-thread
+// counts.  Ends with the block synchronised.
+__device__ __forceinline__ void topk_block_scan2(int a, int b, TopkShared& sh, int& a_ex, int& b_ex) {
+  const int lane = static_cast<int>(lane_id()), w = static_cast<int>(threadIdx.x >> 5);
+  int ai = a, bi = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, ai, o);
+    const int y = __shfl_up_sync(0xffffffffu, bi, o);
+    if (lane >= o) {
+      ai += x;
+      bi += y;
+    }
+  }
+  if (lane == 31) {
+    sh.scan[w] = ai;
+    sh.scan2[w] = bi;
+  }
+  __syncthreads();
+  int wa = 0, wb = 0;
+#pragma unroll
+  for (int i = 0; i < kTopkWarps; ++i) {
+    wa += i < w ? sh.scan[i] : 0;
+    wb += i < w ? sh.scan2[i] : 0;
+  }
+  a_ex = wa + ai - a;
+  b_ex = wb + bi - b;
+  __syncthreads();
+}
+
+// Selection of one row of n > topk positions (keys staged in shared memory
+// or read from the row in global memory on every pass).
+template <bool kStaged>
+__device__ __forceinline__ void topk_select(const float* row, int n, int topk, int32_t* out, uint32_t* hist,
+                                            const uint32_t* keys, TopkShared& sh) {
+  const int tid = static_cast<int>(threadIdx.x);
+  const int nq = (n + 3) >> 2;
+  // digits of 11, 11 and 10 bits; each pass counts the keys of the current
+  // class (those sharing the digits fixed so far)
+  uint32_t prefix = 0, pmask = 0;
+  int krem = topk;
+  for (int d = 0; d < 3; ++d) {
+    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
+    const uint32_t bmask = d == 2 ? 1023u : 2047u;
+    if (d > 0) {
+      for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0;
+      __syncthreads();
+    }
+    for (int q = tid; q < nq; q += kTopkThreads) {
+      const uint4 k = topk_keys4<kStaged>(keys, row, q, n);
+      const int s = 4 * q;
+      if ((k.x & pmask) == prefix) atomicAdd(&hist[(k.x >> shift) & bmask], 1u);
+      if (s + 1 < n && (k.y & pmask) == prefix) atomicAdd(&hist[(k.y >> shift) & bmask], 1u);
+      if (s + 2 < n && (k.z & pmask) == prefix) atomicAdd(&hist[(k.z >> shift) & bmask], 1u);
+      if (s + 3 < n && (k.w & pmask) == prefix) atomicAdd(&hist[(k.w >> shift) & bmask], 1u);
+    }
+    __syncthreads();
+    topk_find_bin(hist, static_cast<int>(bmask) + 1, krem, sh);
+    prefix |= sh.bin << shift;
+    pmask |= bmask << shift;
+    krem = sh.krem;
+    const bool whole = static_cast<int>(hist[sh.bin]) == krem;   // the class is taken whole
+    __syncthreads();
+    if (whole) break;
+  }
+
+  // Ordered compaction: keys above the class, then the first krem of the
+  // class by position.  Thread t owns the quads [t QL, t QL + QL) with QL
+  // odd (so the 16-byte reads of eight consecutive threads hit distinct
+  // banks): it counts both kinds, one block scan gives the counts before
+  // its run, and a second walk writes its picks in order.
+  const int QL = ((nq + kTopkThreads - 1) / kTopkThreads) | 1;
+  const int q0 = tid * QL < nq ? tid * QL : nq, q1 = q0 + QL < nq ? q0 + QL : nq;
+  int gt = 0, eq = 0;
+  for (int q = q0; q < q1; ++q) {
+    const uint4 k = topk_keys4<kStaged>(keys, row, q, n);
+    const int s = 4 * q;
+    const uint32_t h0 = k.x & pmask, h1 = k.y & pmask, h2 = k.z & pmask, h3 = k.w & pmask;
+    gt += (h0 > prefix) + (s + 1 < n && h1 > prefix) + (s + 2 < n && h2 > prefix) + (s + 3 < n && h3 > prefix);
+    eq += (h0 == prefix) + (s + 1 < n && h1 == prefix) + (s + 2 < n && h2 == prefix) +
+          (s + 3 < n && h3 == prefix);
+  }
+  int gt_ex, eq_ex;
+  topk_block_scan2(gt, eq, sh, gt_ex, eq_ex);
+  int pos = gt_ex + (eq_ex < krem ? eq_ex : krem);
+  int eq_seen = eq_ex;
+  for (int q = q0; q < q1; ++q) {
+    const uint4 k = topk_keys4<kStaged>(keys, row, q, n);
+    const int s = 4 * q;
+    const uint32_t kk[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t hi = kk[j] & pmask;
+      bool take = s + j < n && hi > prefix;
+      if (s + j < n && hi == prefix) {
+        take = eq_seen < krem;
+        ++eq_seen;
+      }
+      if (take) out[pos++] = s + j;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 4) dsa_topk_kernel(const __grid_constant__ TopkParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);      // [kTopkBins]
+  uint32_t* keys = hist + kTopkBins;                           // [stage_cap]
+  __shared__ TopkShared sh;
   const int tid = static_cast<int>(threadIdx.x);
   const int r = p.row0 + static_cast<int>(blockIdx.x);
 
   // the row's sequence and visible length
-  if (tid == 0) sh_seq = p.cu_q == nullptr ? 0 : -1;
+  if (tid == 0) sh.seq = p.cu_q == nullptr ? 0 : -1;
   __syncthreads();
   if (p.cu_q != nullptr) {
     for (int i = tid; i < p.batch; i += kTopkThreads)
-      if (p.cu_q[i] <= r && r < p.cu_q[i + 1]) sh_seq = i;
+      if (p.cu_q[i] <= r && r < p.cu_q[i + 1]) sh.seq = i;
   }
+  for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0;
   __syncthreads();
-  const int b = sh_seq;
+  const int b = sh.seq;
   long long v = 0;
   if (b >= 0) {
     int cq2[2] = {0, p.total_q}, ck2[2] = {0, p.total_kv};
@@ -552,97 +735,36 @@ __global__ void __launch_bounds__(kTopkThreads) dsa_topk_kernel(const __grid_con
   }
   const int n = static_cast<int>(v);
   const float* row = p.scores + static_cast<long long>(blockIdx.x) * p.row_stride;
-  const float* src = row;
-  if (n <= p.stage_cap) {
-    for (int i = tid; i < n; i += kTopkThreads) stage[i] = row[i];
-    src = stage;
+  if (n > p.stage_cap) {
+    topk_select<false>(row, n, p.topk, out, hist, keys, sh);
+    return;
   }
-
-  // radix select: the class of keys that shares the threshold's top bits
-  uint32_t prefix = 0, pmask = 0;
-  int krem = p.topk;
-  const int lane = static_cast<int>(lane_id());
-  for (int d = 0; d < 3; ++d) {
-    const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
-    const int nbins = d == 2 ? 1024 : 2048;
-    for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
-    for (int base = 0; base < n; base += kTopkThreads) {
-      const int s = base + tid;
-      uint32_t key = 0;
-      bool act = false;
-      if (s < n) {
-        key = topk_key(src[s]);
-        act = (key & pmask) == prefix;
-      }
-      const uint32_t am = __ballot_sync(0xffffffffu, act);
-      if (act) {
-        const uint32_t bin = (key >> shift) & static_cast<uint32_t>(nbins - 1);
-        const uint32_t peers = __match_any_sync(am, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
-      }
-    }
-    __syncthreads();
-    // the bin holding the krem-th largest key of the class: each thread owns
-    // a run of bins; counts above a thread's run by a suffix scan
-    const int per = nbins / kTopkThreads;
-    int own = 0;
-    for (int i = 0; i < per; ++i) own += static_cast<int>(hist[tid * per + i]);
-    int incl = own;   // suffix sum within the warp (lanes above and this one)
+  // Stage the row's keys (16-byte loads, four in flight per thread, when the
+  // row is 16-byte aligned); the tail of the last quad reads as 0.
+  const int nq = (n + 3) >> 2;
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    uint4* k4 = reinterpret_cast<uint4*>(keys);
+    const int full = n >> 2;
+    for (int base = 0; base < full; base += 4 * kTopkThreads) {
+      float4 t[4];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_down_sync(0xffffffffu, incl, o);
-      if (lane + o < 32) incl += y;
-    }
-    const int w = tid >> 5;
-    if (lane == 0) sh_scan[w] = incl;   // the warp's total
-    __syncthreads();
-    int above_w = 0;
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kTopkThreads + tid;
+        if (i < full) t[u] = __ldg(r4 + i);
+      }
 #pragma unroll
-    for (int i = 0; i < kTopkWarps; ++i) above_w += i > w ? sh_scan[i] : 0;
-    const int above = above_w + incl - own;   // keys of the class in bins above this thread's run
-    if (above < krem && krem <= above + own) {
-      int acc = above;
-      for (int i = per - 1; i >= 0; --i) {
-        const int c = static_cast<int>(hist[tid * per + i]);
-        if (krem <= acc + c) {
-          sh_bin = static_cast<uint32_t>(tid * per + i);
-          sh_krem = krem - acc;
-          break;
-        }
-        acc += c;
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kTopkThreads + tid;
+        if (i < full) k4[i] = make_uint4(topk_key(t[u].x), topk_key(t[u].y), topk_key(t[u].z), topk_key(t[u].w));
       }
     }
-    __syncthreads();
-    const uint32_t bin = sh_bin;
-    krem = sh_krem;
-    prefix |= bin << shift;
-    pmask |= static_cast<uint32_t>(nbins - 1) << shift;
-    const bool whole = static_cast<int>(hist[bin]) == krem;
-    __syncthreads();   // hist and the scan slots are rewritten next
-    if (whole) break;
+    for (int i = 4 * full + tid; i < 4 * nq; i += kTopkThreads) keys[i] = i < n ? topk_key(row[i]) : 0u;
+  } else {
+    for (int i = tid; i < 4 * nq; i += kTopkThreads) keys[i] = i < n ? topk_key(row[i]) : 0u;
   }
-
-  // ordered compaction: keys above the class, then the first krem of the
-  // class by position
-  int eq_before = 0, out_before = 0;
-  for (int base = 0; base < n && out_before < p.topk; base += kTopkThreads) {
-    const int s = base + tid;
-    bool gt = false, eq = false;
-    if (s < n) {
-      const uint32_t hi = topk_key(src[s]) & pmask;
-      gt = hi > prefix;
-      eq = hi == prefix;
-    }
-    int eq_excl, eq_tot;
-    topk_scan(eq, sh_scan, eq_excl, eq_tot);
-    const bool take = gt || (eq && eq_before + eq_excl < krem);
-    int t_excl, t_tot;
-    topk_scan(take, sh_scan, t_excl, t_tot);
-    if (take) out[out_before + t_excl] = s;
-    eq_before += eq_tot;
-    out_before += t_tot;
-  }
+  __syncthreads();
+  topk_select<true>(row, n, p.topk, out, hist, keys, sh);
 }
 
 }  // namespace smla

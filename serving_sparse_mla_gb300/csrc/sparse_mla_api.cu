@@ -33,7 +33,8 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-// Top-k kernel: histogram plus a staged row of up to kTopkStageCap scores.
+// Top-k kernel: histogram and the staged keys of a row of up to
+// kTopkStageCap positions.
 constexpr int kTopkStageCap = 12288;
 constexpr int kTopkMaxSmem = smla::kTopkBins * 4 + kTopkStageCap * 4;
 
@@ -612,7 +613,7 @@ sparse_mla_status_t launch_topk(const float* scores, long long row_stride, const
   p.n_rows = n_rows;
   p.topk = topk;
   const long long longest = row_stride < total_kv ? row_stride : total_kv;
-  p.stage_cap = static_cast<int>(longest < kTopkStageCap ? longest : kTopkStageCap);
+  p.stage_cap = static_cast<int>(longest < kTopkStageCap ? (longest + 3) / 4 * 4 : kTopkStageCap);
   const int smem = smla::kTopkBins * 4 + p.stage_cap * 4;
   smla::dsa_topk_kernel<<<n_rows, smla::kTopkThreads, smem, cs>>>(p);
   return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;

@@ -28,12 +28,13 @@
 //               across items.
 //   warp 1      one thread issues a tile's 8 MMAs (K = 16 each) into one of
 //               two 256-column TMEM accumulators and commits.
-//   warps 2..9  epilogue, lane = position: a thread reads its position's H_I
-//               products for half of the group's rows (64 columns at a
-//               time; the accumulator is freed once the last are read),
-//               applies relu and the row's head weights (packed fp32 FMAs)
-//               and stores the fp32 score into the row's logits row (32
-//               lanes store 128 contiguous bytes).
+//   warps 2..9  epilogue over half of the group's (row, head) columns each:
+//               four threads share a position, each with 16 heads of it
+//               (16x256b TMEM reads; the heads' weights stay in registers
+//               for the item), relu and weights in packed fp32 FMAs, a
+//               3-shuffle transpose-reduce to one score per thread, fp32
+//               stores into the rows' logits (32 lanes: 32 consecutive
+//               positions).  The accumulator is freed once read.
 //
 // A persistent grid (at most one CTA per SM, ~212 KB of shared memory each)
 // walks items c, c + G, ... (largest groups first); while an item runs, its
@@ -309,19 +310,32 @@ __device__ __forceinline__ bool idx_mma(const IdxParams& p, IdxMisc& m, uint32_t
   return true;
 }
 
-// Epilogue warp e (0..7): TMEM lane quarter = warp % 4, rows of the group's
-// half e / 4.
+// Epilogue warp e (0..7): TMEM lane quarter = warp % 4, and the group's
+// half e / 4 of its (row, head) columns (128 of the 256).  The columns are
+// read 64 at a time with the 16x256b shape: thread t holds 16 of them (the
+// same 16 on every tile, so their head weights stay in registers for the
+// whole item) for 4 positions of the quarter, t/4 + {0, 8, 16, 24}.  A
+// thread sums its 16 heads per position; a transpose-reduce over the 4
+// threads that share the positions (lane bits 0..1) leaves each thread the
+// full score of one position.
 template <int H>
 __device__ __forceinline__ bool idx_epilogue(const IdxParams& p, IdxMisc& m, const uint8_t* sbase, uint32_t tmem,
                                              const int32_t* cq, const int32_t* ck, int e) {
   constexpr int G = kIdxN / H;
-  constexpr int GH = G / 2;   // rows per half
+  constexpr int GH = G / 2;          // rows per half
+  constexpr int RB = 64 / H;         // rows per 64-column batch (H <= 64)
+  constexpr int NB = GH / RB;        // batches per half: 2
+  constexpr int JR = 8 / RB;         // 8-column repetitions per row
+  static_assert(GH * H == 128 && NB == 2, "epilogue batching");
   const volatile int* ab = &m.abort_flag;
   const int lane = static_cast<int>(lane_id());
   const int quarter = static_cast<int>(threadIdx.x >> 5) & 3;
   const int half = e >> 2;
+  const int li = lane & 3;
   const float* wsm = reinterpret_cast<const float*>(sbase + kIdxWOff);
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  // the position this thread's final score belongs to, within the quarter
+  const int my_pos = (lane >> 2) + 8 * li;
   uint32_t acount = 0, wcount = 0;
   const long long n_items = static_cast<long long>(p.groups) * p.kv_chunks;
   for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -330,14 +344,22 @@ __device__ __forceinline__ bool idx_epilogue(const IdxParams& p, IdxMisc& m, con
     w.start(p, cq, it);
     IdxSeg s;
     bool first = true;
-    const float* wb = wsm;
+    float wr[NB][16];   // head weights of this thread's 16 columns per batch
     while (w.next(p, cq, ck, s)) {
       if (s.t1 <= s.t0) continue;
       if (first) {
         first = false;
         const uint32_t b = wcount & 1u;
         if (!mbar_wait(smem_u32(&m.w_full[b]), (wcount >> 1) & 1u, deadline, ab)) return false;
-        wb = wsm + b * kIdxN;
+        const float* wb = wsm + b * kIdxN + half * 128;
+#pragma unroll
+        for (int bt = 0; bt < NB; ++bt)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float2 x = *reinterpret_cast<const float2*>(wb + bt * 64 + 8 * j + 2 * li);
+            wr[bt][2 * j] = x.x;
+            wr[bt][2 * j + 1] = x.y;
+          }
       }
       // this half's rows in the segment and the positions each sees
       int vis[GH];
@@ -358,26 +380,17 @@ __device__ __forceinline__ bool idx_epilogue(const IdxParams& p, IdxMisc& m, con
         const uint32_t buf = acount & 1u;
         if (!mbar_wait(smem_u32(&m.acc_full[buf]), (acount >> 1) & 1u, deadline, ab)) return false;
         tc_fence_after();
-        // Rows in batches of 64 columns (RB rows): load a batch from TMEM,
-        // reduce it, store; the accumulator is freed once the last batch is
-        // in registers.
-        constexpr int RB = H >= 64 ? 1 : 64 / H;
-        constexpr int NB = GH / RB;
-        const int pos = t * kIdxTile + quarter * 32 + lane;
+        const int pos = t * kIdxTile + quarter * 32 + my_pos;
 #pragma unroll
         for (int bt = 0; bt < NB; ++bt) {
-          float x[RB][H];
+          bool any = false;
 #pragma unroll
-          for (int rr = 0; rr < RB; ++rr) {
-            const int jj = bt * RB + rr;
-            if (!on[jj]) continue;   // warp-uniform
-            const uint32_t col = buf * kIdxN + static_cast<uint32_t>((half * GH + jj) * H);
-            if constexpr (H == 16) {
-              tmem_ld16(lane_base + col, x[rr]);
-            } else {
-#pragma unroll
-              for (int h = 0; h < H; h += 32) tmem_ld32(lane_base + col + h, x[rr] + h);
-            }
+          for (int rr = 0; rr < RB; ++rr) any = any || on[bt * RB + rr];
+          float xa[32], xb[32];   // positions +0/+8 and +16/+24 of the quarter
+          if (any) {   // warp-uniform
+            const uint32_t col = buf * kIdxN + static_cast<uint32_t>(half * 128 + bt * 64);
+            tmem_ld16x256_x8(lane_base + col, xa);
+            tmem_ld16x256_x8(lane_base + (16u << 16) + col, xb);
           }
           tmem_wait_ld();
           if (bt == NB - 1) {
@@ -388,16 +401,25 @@ __device__ __forceinline__ bool idx_epilogue(const IdxParams& p, IdxMisc& m, con
 #pragma unroll
           for (int rr = 0; rr < RB; ++rr) {
             const int jj = bt * RB + rr;
-            if (!on[jj]) continue;
-            const float* wr = wb + (half * GH + jj) * H;
-            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;   // four partial sums (two f32x2 pairs)
+            if (!on[jj]) continue;   // warp-uniform
+            // partial sums of this thread's heads of row jj at its 4 positions
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f, c0 = 0.f, c1 = 0.f, d0 = 0.f, d1 = 0.f;
 #pragma unroll
-            for (int h = 0; h < H; h += 4) {
-              const float4 wv = *reinterpret_cast<const float4*>(wr + h);
-              ffma2(a0, a1, fmaxf(x[rr][h + 0], 0.0f), fmaxf(x[rr][h + 1], 0.0f), wv.x, wv.y);
-              ffma2(a2, a3, fmaxf(x[rr][h + 2], 0.0f), fmaxf(x[rr][h + 3], 0.0f), wv.z, wv.w);
+            for (int j = rr * JR; j < (rr + 1) * JR; ++j) {
+              const float w0 = wr[bt][2 * j], w1 = wr[bt][2 * j + 1];
+              ffma2(a0, a1, fmaxf(xa[4 * j + 0], 0.f), fmaxf(xa[4 * j + 1], 0.f), w0, w1);
+              ffma2(b0, b1, fmaxf(xa[4 * j + 2], 0.f), fmaxf(xa[4 * j + 3], 0.f), w0, w1);
+              ffma2(c0, c1, fmaxf(xb[4 * j + 0], 0.f), fmaxf(xb[4 * j + 1], 0.f), w0, w1);
+              ffma2(d0, d1, fmaxf(xb[4 * j + 2], 0.f), fmaxf(xb[4 * j + 3], 0.f), w0, w1);
             }
-            const float sc = (a0 + a1) + (a2 + a3);
+            // positions +0, +8, +16, +24: transpose-reduce over lane bits 0..1
+            const float v0 = a0 + a1, v1 = b0 + b1, v2 = c0 + c1, v3 = d0 + d1;
+            float k0 = (li & 2) ? v2 : v0, k1 = (li & 2) ? v3 : v1;
+            const float s0 = (li & 2) ? v0 : v2, s1 = (li & 2) ? v1 : v3;
+            k0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+            k1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+            float sc = (li & 1) ? k1 : k0;
+            sc += __shfl_xor_sync(0xffffffffu, (li & 1) ? k0 : k1, 1);
             if (pos < vis[jj]) {
               const int r = w.r_first + half * GH + jj;
               p.scores[static_cast<long long>(r - p.row0) * p.row_stride + pos] = sc;

@@ -240,3 +240,84 @@ def test_indexer_topk_full_size_sampled(smla):
     rows = [0, 2047, 2048, 2049, 3000, 4095, 5555, 8191]
     exact = sum(_check_list(c, lst[r], r, 2048) for r in rows)
     assert exact >= 3
+
+
+# --------------------------------------------------------------------------- edge cases
+
+def test_indexer_varlen_edge_sequences(smla):
+    """Empty query runs, empty key runs, fewer keys than queries (the first
+    queries see nothing), single-token sequences, 16 indexer heads."""
+    q_lens = [0, 7, 3, 0, 40, 1, 9]
+    kv_lens = [5, 0, 2, 0, 700, 1, 300]
+    c = mi.indexer_varlen_case(540, q_lens, kv_lens, h_idx=16, topk=64)
+    q, k, w, cq, ck = _dev(c)
+    lst = smla.dsa_indexer_topk(q, k, w, 64, cq, ck).cpu().numpy()
+    for r in range(int(c.cu_seqlens_q[-1])):
+        _check_list(c, lst[r], r, 64)
+    got = smla.dsa_indexer_scores(q, k, w, cq, ck).cpu().numpy()
+    _check_scores(c, got, range(int(c.cu_seqlens_q[-1])))
+
+
+def test_indexer_many_short_sequences(smla):
+    """Hundreds of short sequences: most groups straddle several."""
+    g = torch.Generator().manual_seed(541)
+    q_lens = torch.randint(1, 12, (300,), generator=g).tolist()
+    kv_lens = [ql + int(x) for ql, x in zip(q_lens, torch.randint(0, 90, (300,), generator=g).tolist())]
+    c = mi.indexer_varlen_case(541, q_lens, kv_lens, h_idx=32, topk=40)
+    q, k, w, cq, ck = _dev(c)
+    lst = smla.dsa_indexer_topk(q, k, w, 40, cq, ck).cpu().numpy()
+    total = int(c.cu_seqlens_q[-1])
+    exact = sum(_check_list(c, lst[r], r, 40) for r in range(0, total, 5))
+    assert exact >= total // 5 // 2
+
+
+def test_indexer_varlen_chunked_and_long_stride(smla):
+    """A logits budget of a few rows, and a row length above the longest
+    sequence, give the lists of the one-chunk call."""
+    c = mi.indexer_varlen_case(542, [30, 200, 17], [2500, 200, 3100], topk=256)
+    q, k, w, cq, ck = _dev(c)
+    full = smla.dsa_indexer_topk(q, k, w, 256, cq, ck)
+    ws = torch.empty(5 * 3104 * 4, dtype=torch.uint8, device=DEV)
+    part = smla.dsa_indexer_topk(q, k, w, 256, cq, ck, workspace=ws)
+    wide = smla.dsa_indexer_topk(q, k, w, 256, cq, ck, max_seqlen_kv=3500)
+    assert torch.equal(full, part) and torch.equal(full, wide)
+    for r in (0, 29, 30, 100, 229, 230, 246):
+        _check_list(c, full[r].cpu().numpy(), r, 256)
+
+
+def test_indexer_row_length_too_small_is_reported(smla):
+    """A max_seqlen_kv below the longest sequence cuts rows to it (nothing is
+    written past a logits row) and records the error code 0x611."""
+    c = mi.indexer_varlen_case(543, [20, 20], [600, 3000], topk=128)
+    q, k, w, cq, ck = _dev(c)
+    smla.clear_device_error()
+    lst = smla.dsa_indexer_topk(q, k, w, 128, cq, ck, max_seqlen_kv=1000)
+    torch.cuda.synchronize()
+    assert smla.get_device_error() == 0x611
+    smla.clear_device_error()
+    lst = lst.cpu().numpy()
+    for r in range(20):             # the first sequence fits: exact rules
+        _check_list(c, lst[r], r, 128)
+    assert np.all((lst[20:] >= 0) & (lst[20:] < 1000))   # cut rows still list valid positions
+
+
+def test_indexer_lists_drive_the_forward(smla):
+    """The pipeline: GPU lists into the sparse forward equal the oracle's
+    forward over the oracle's lists on every row whose list is unique."""
+    from oracle import sparse_mla_oracle as orc
+    s, topk = 300, 128
+    c = mi.indexer_case(544, s, s, topk=topk)
+    lst = smla.dsa_indexer_topk(*_dev(c)[:3], topk)
+    ref_lst = ido.dsa_indices(c.q_idx, c.k_idx, c.weights, topk)
+    same = [r for r in range(s) if np.array_equal(lst[r].cpu().numpy(), ref_lst[r])]
+    assert len(same) >= s // 2
+    g = mi._gen(545)
+    q = mi.randn_bf16(g, (s, 8, mi.D_QK))
+    kv = mi.randn_bf16(g, (s, mi.D_QK))
+    out, lse = smla.sparse_mla_fwd(q.to(DEV), kv.to(DEV), lst, mi.default_sm_scale())
+    ro, rl = orc.sparse_mla_fwd(q, kv, torch.from_numpy(ref_lst).to(torch.int32), mi.default_sm_scale(),
+                                tokens=same)
+    o = out.float().cpu().numpy()[same]
+    l = lse.cpu().numpy()[same]
+    assert np.all(np.abs(o - ro) <= 2e-2 + 2e-2 * np.abs(ro))
+    assert np.all(np.abs(l - rl) <= 1e-3)

@@ -30,7 +30,8 @@
 //                dKV = (sm_scale dS)^T Q + P^T [dout, 0] (M = 64 rows, K = 16
 //                heads, Q and dout read as MN-major B operands).
 //   warps 11..14 drain each dKV chunk from TMEM and add it into dkv (fp32)
-//                with 16-byte reductions, by the block's row ids.
+//                with 16-byte reductions, by the block's row ids, two lanes
+//                per aligned 32-byte sector in each instruction.
 //
 // At the end of a unit the softmax warps write dq (fp32) from TMEM.  All
 // waits are bounded like the forward's.
@@ -275,16 +276,21 @@ __device__ bool run_bwd_grad(const FwdParams& p, BwdMisc& m, uint8_t* sbase, uin
 
 // ------------------------------------------------------------------ dKV drain
 
-// One 16x32bx2 read: threads 0..15 of the warp take row r = 16 q4 + lane at
-// columns [col, col + 16), threads 16..31 the same row at col + HALF.
-template <int HALF>
-__device__ __forceinline__ void drain_cols(uint32_t taddr, int col, float* dst_row, bool live) {
+// 32 columns of the block's rows: four 16x32bx2.x4 reads with the half
+// split at 4 columns, so threads l and l + 16 (the same row r = 16 q4 + l)
+// hold columns [c, c + 4) and [c + 4, c + 8) of each 8-column step.  Their
+// two 16-byte reductions then fill one aligned 32-byte sector in the same
+// instruction (16 full sectors per instruction rather than 32 half ones:
+// the L2 reduction traffic that bounds the backward is counted in sectors).
+__device__ __forceinline__ void drain_cols(uint32_t taddr, int col, float* dst_row, bool live, int half) {
   float v[16];
-  tmem_ld16x2_x16<HALF>(taddr + static_cast<uint32_t>(col), v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) tmem_ld16x2_x4<4>(taddr + static_cast<uint32_t>(col + 8 * k), v + 4 * k);
   tmem_wait_ld();
   if (live) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) red_add_v4(dst_row + col + 4 * j, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    for (int k = 0; k < 4; ++k)
+      red_add_v4(dst_row + col + 8 * k + 4 * half, v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
   }
 }
 
@@ -323,11 +329,10 @@ __device__ bool run_bwd_drain(const FwdParams& p, BwdMisc& m, uint32_t tmem) {
         tc_fence_after();
         if (c < 2) {
 #pragma unroll 1
-          for (int col = 0; col < 128; col += 16)
-            drain_cols<128>(tKV, col, dst + c * 256 + half * 128, row >= 0);
+          for (int col = 0; col < 256; col += 32) drain_cols(tKV, col, dst + c * 256, row >= 0, half);
         } else {
 #pragma unroll
-          for (int col = 0; col < 32; col += 16) drain_cols<32>(tKV, col, dst + 512 + half * 32, row >= 0);
+          for (int col = 0; col < 64; col += 32) drain_cols(tKV, col, dst + 512, row >= 0, half);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&m.dkv_empty));

@@ -214,6 +214,14 @@ __device__ __forceinline__ void tmem_ld16x2_x8(uint32_t taddr, float* v) {
 }
 
 template <int OFF>
+__device__ __forceinline__ void tmem_ld16x2_x4(uint32_t taddr, float* v) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x4.b32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr), "n"(OFF));
+}
+
+template <int OFF>
 __device__ __forceinline__ void tmem_ld16x2_x16(uint32_t taddr, float* v) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
   asm volatile(

@@ -14,21 +14,29 @@
 //   dkv[r, :512] += P^T dout_t
 //
 // Work decomposition: the forward's persistent grid and gather (the same
-// producer), with units of one token x up to 16 heads.  Per 64-row block:
+// producer), with units of one token x up to 16 heads (U = 1) or, above 16
+// heads, one token x up to 32 heads taken as two halves of 16 (U = 2): each
+// block's dKV then sums both halves before it is drained, so the gather and
+// the dkv reductions (the L2 traffic that bounds the backward) are paid once
+// per 32 heads.  Per 64-row block:
 //
 //   warps 0..3   producers: gather the block's rows (value pairs + rope tile)
 //                and publish its 64 row ids.
 //   warps 4, 9   S^T = K Q^T and dP^T = V dout^T (swap-AB, M = 64 kv rows,
-//                N = 16 heads), each for half of the value pairs (part 0 also
-//                the rope columns of S), into TMEM.
+//                N = 16 heads) into TMEM: with U = 1 each takes half of the
+//                value pairs (warp 4 also the rope columns of S); with U = 2
+//                each takes one half of the heads, all pairs and the rope.
 //   warps 5..8   P, dS from S, dP, the LSE and D; write P^T and
-//                (sm_scale dS)^T as bf16 rows into shared memory.
-//   warp 10      dQ^T += K^T (sm_scale dS)^T (K^T the MN-major view of the
-//                gathered tile, as V^T in the forward's P.V; accumulated in
-//                TMEM over the unit), which frees the block's tiles; then the
-//                block's dKV rows in three column chunks (256, 256, 64):
-//                dKV = (sm_scale dS)^T Q + P^T [dout, 0] (M = 64 rows, K = 16
-//                heads, Q and dout read as MN-major B operands).
+//                (sm_scale dS)^T of every half as bf16 rows into shared
+//                memory.
+//   warp 10      dQ^T += K^T (sm_scale dS)^T per half (K^T the MN-major view
+//                of the gathered tile, as V^T in the forward's P.V;
+//                accumulated in TMEM over the unit), which frees the block's
+//                tiles; then the block's dKV rows in three column chunks
+//                (256, 256, 64 with U = 1; 192 each with U = 2):
+//                dKV = sum over halves of (sm_scale dS)^T Q + P^T [dout, 0]
+//                (M = 64 rows, K = 16 heads per half, Q and dout read as
+//                MN-major B operands).
 //   warps 11..14 drain each dKV chunk from TMEM and add it into dkv (fp32)
 //                with 16-byte reductions, by the block's row ids, two lanes
 //                per aligned 32-byte sector in each instruction.
@@ -40,38 +48,47 @@
 
 namespace smla {
 
-constexpr int kBwdHeads = 16;   // heads per CTA: the N of the S / dP / dQ MMAs
+constexpr int kBwdHeads = 16;   // heads per half: the N of the S / dP / dQ MMAs
 
+template <int U>
 struct BwdLayout {
   static constexpr int N = kBwdHeads;
-  static constexpr int kNV = 9;                         // value ring: 2.25 blocks
-  static constexpr int kNR = 3;                         // rope ring
+  static constexpr int H = U * N;                       // heads per unit
+  static constexpr int kNV = U == 1 ? 9 : 6;            // value ring: 2.25 / 1.5 blocks
+  static constexpr int kNR = U == 1 ? 3 : 2;            // rope ring
   static constexpr int kPRow = N * 2;                   // bytes of one P^T / dS^T row
   static constexpr uint32_t kPSwz = SWZ_32B;
-  static constexpr int kPSBytes = kBlk * kPRow;         // one P^T or dS^T tile (2 KB)
-  static constexpr int kQOff = 0;                       // Q: 9 chunks x N heads x 128 B
-  static constexpr int kDOOff = kQOff + 9 * N * 128;    // dout: 8 chunks x N x 128 B
-  static constexpr int kVOff = kDOOff + 8 * N * 128;
+  static constexpr int kPSBytes = kBlk * kPRow;         // one P^T or dS^T tile of one half (2 KB)
+  static constexpr int kQHalf = 9 * N * 128;            // Q of one half: 9 chunks x N heads x 128 B
+  static constexpr int kDOHalf = 8 * N * 128;           // dout of one half: 8 chunks
+  static constexpr int kQOff = 0;
+  static constexpr int kDOOff = kQOff + U * kQHalf;
+  static constexpr int kVOff = kDOOff + U * kDOHalf;
   static constexpr int kROff = kVOff + kNV * kPairBytes;
-  static constexpr int kPSOff = kROff + kNR * kChunkBytes;   // [buffer][P^T, dS^T]
-  static constexpr int kMiscOff = kPSOff + 2 * 2 * kPSBytes;
+  static constexpr int kPSOff = kROff + kNR * kChunkBytes;   // [buffer][half][P^T, dS^T]
+  static constexpr int kMiscOff = kPSOff + 2 * U * 2 * kPSBytes;
   // TMEM columns
-  static constexpr int kTS = 0;          // S^T: [part][buffer], N columns each
-  static constexpr int kTdP = 4 * N;     // dP^T: [part][buffer]
-  static constexpr int kTdQ = 8 * N;     // dQ^T: four M=128 tiles of 128 dims, then the M=64 rope tile
-  static constexpr int kTdKV = 256;      // one dKV chunk: 64 rows x up to 256 columns (M=64)
+  static constexpr int kTS = 0;                         // S^T: [part or half][buffer], N columns each
+  static constexpr int kTdP = 4 * N;                    // dP^T: [part or half][buffer]
+  static constexpr int kTdQ = 8 * N;                    // dQ^T per half: four M=128 tiles of 128 dims, the M=64 rope tile
+  static constexpr int kTdKV = U == 1 ? 256 : kTdQ + U * 5 * N;   // one dKV chunk (M=64)
+  static constexpr int kKVChunk = U == 1 ? 256 : 192;   // dKV chunk width: three chunks cover 576
   static constexpr int kTmemCols = 512;
   // warp roles
   static constexpr int kQkWarp0 = 4, kSoftWarp0 = 5, kQkWarp1 = 9, kGradWarp = 10, kDrainWarp0 = 11;
   static constexpr int kThreads = 15 * 32;
 };
-static_assert(BwdLayout::kTdQ + 5 * BwdLayout::N <= BwdLayout::kTdKV, "TMEM map");
-static_assert(BwdLayout::kVOff % 1024 == 0 && BwdLayout::kROff % 1024 == 0 && BwdLayout::kPSOff % 1024 == 0,
+static_assert(BwdLayout<1>::kTdQ + 5 * BwdLayout<1>::N <= BwdLayout<1>::kTdKV, "TMEM map");
+static_assert(BwdLayout<2>::kTdKV + BwdLayout<2>::kKVChunk <= BwdLayout<2>::kTmemCols, "TMEM map");
+static_assert(BwdLayout<1>::kVOff % 1024 == 0 && BwdLayout<1>::kROff % 1024 == 0 && BwdLayout<1>::kPSOff % 1024 == 0,
+              "swizzled tiles start on 1024-byte boundaries");
+static_assert(BwdLayout<2>::kVOff % 1024 == 0 && BwdLayout<2>::kROff % 1024 == 0 && BwdLayout<2>::kPSOff % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
 
+template <int U>
 struct __align__(16) BwdMisc {
-  uint64_t v_full[BwdLayout::kNV], v_empty[BwdLayout::kNV];
-  uint64_t rp_full[BwdLayout::kNR], rp_empty[BwdLayout::kNR];
+  uint64_t v_full[BwdLayout<U>::kNV], v_empty[BwdLayout<U>::kNV];
+  uint64_t rp_full[BwdLayout<U>::kNR], rp_empty[BwdLayout<U>::kNR];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   uint64_t q_full, q_empty, s_full[2][2], pds_full[2], pds_empty[2], dkv_full, dkv_empty, dq_full, drain[3],
       cand_full;
@@ -79,15 +96,17 @@ struct __align__(16) BwdMisc {
   uint32_t info_mask[kInfoDepth][2];
   int32_t info_rows[kInfoDepth][kBlk];
   uint32_t cand[2][kProducerWarps];
-  float dsum[kBwdHeads];   // D = rowsum(dout * out) per head of the unit
-  float lse2[kBwdHeads];   // LSE * log2(e)
+  float dsum[U * kBwdHeads];   // D = rowsum(dout * out) per head of the unit
+  float lse2[U * kBwdHeads];   // LSE * log2(e)
   uint32_t tmem_base;
   int abort_flag;
   int prior_error;
 };
 
-constexpr int bwd_smem_bytes() { return BwdLayout::kMiscOff + static_cast<int>(sizeof(BwdMisc)) + 1024; }
-static_assert(bwd_smem_bytes() <= kMaxSmem, "smem budget (backward)");
+template <int U>
+constexpr int bwd_smem_bytes() { return BwdLayout<U>::kMiscOff + static_cast<int>(sizeof(BwdMisc<U>)) + 1024; }
+static_assert(bwd_smem_bytes<1>() <= kMaxSmem, "smem budget (backward)");
+static_assert(bwd_smem_bytes<2>() <= kMaxSmem, "smem budget (backward, 32-head units)");
 
 enum BwdErrCode : int { kErrBwdGradWait = 0x401, kErrBwdDrainWait = 0x501 };
 
@@ -96,59 +115,66 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
-__device__ __forceinline__ void bwd_raise(BwdMisc& m, int code) {
+template <int U>
+__device__ __forceinline__ void bwd_raise(BwdMisc<U>& m, int code) {
   *reinterpret_cast<volatile int*>(&m.abort_flag) = 1;
   atomicCAS(&g_device_error, 0, code);
 }
 
 // ------------------------------------------------------------------ S, dP issuers
 
-// S^T (QK^T) and dP^T of block n for one part: value pairs 2P, 2P+1 (and for
-// part 0 the rope columns of S).  The A operand (the gathered rows, K-major)
-// is shared by the two products; B is Q for S and dout for dP.
-template <int PART>
-__device__ __forceinline__ bool bwd_issue_s_dp(BwdMisc& m, uint32_t qbase, uint32_t dobase, uint32_t vbase,
+// S^T (QK^T) and dP^T of block n for one part.  U = 1: value pairs 2P and
+// 2P+1 (part 0 also the rope columns of S), the two parts summed by the
+// softmax.  U = 2: PART is the half of the heads, over every value pair and
+// the rope.  The A operand (the gathered rows, K-major) is shared by the two
+// products; B is Q for S and dout for dP.
+template <int U, int PART>
+__device__ __forceinline__ bool bwd_issue_s_dp(BwdMisc<U>& m, uint32_t qbase, uint32_t dobase, uint32_t vbase,
                                                uint32_t rbase, uint32_t tmem, int n, uint64_t deadline,
                                                const volatile int* ab) {
-  using L = BwdLayout;
+  using L = BwdLayout<U>;
   constexpr int N = L::N;
+  constexpr int kPairs = U == 1 ? 2 : 4;          // value pairs this issuer takes
+  constexpr int kPair0 = U == 1 ? 2 * PART : 0;
+  constexpr bool kRope = U == 2 || PART == 0;
   constexpr uint32_t kIdesc = idesc_bf16_f32(64, N, false, false);
   const uint32_t tS = tmem + static_cast<uint32_t>(L::kTS + (PART * 2 + (n & 1)) * N);
   const uint32_t tP = tmem + static_cast<uint32_t>(L::kTdP + (PART * 2 + (n & 1)) * N);
-  uint32_t slot[2];
+  const uint32_t qh = qbase + (U == 2 ? PART * L::kQHalf : 0);
+  const uint32_t dh = dobase + (U == 2 ? PART * L::kDOHalf : 0);
+  uint32_t slot[kPairs];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(2 * PART + i);
+  for (int i = 0; i < kPairs; ++i) {
+    const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(kPair0 + i);
     slot[i] = vi % L::kNV;
     if (!mbar_wait(smem_u32(&m.v_full[slot[i]]), (vi / L::kNV) & 1u, deadline, ab)) return false;
   }
   const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
-  if (PART == 0 &&
-      !mbar_wait(smem_u32(&m.rp_full[rs]), (static_cast<uint32_t>(n) / L::kNR) & 1u, deadline, ab))
+  if (kRope && !mbar_wait(smem_u32(&m.rp_full[rs]), (static_cast<uint32_t>(n) / L::kNR) & 1u, deadline, ab))
     return false;
   fence_proxy_async_smem();
   tc_fence_after();
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int pr = 2 * PART + i;
+  for (int i = 0; i < kPairs; ++i) {
+    const int pr = kPair0 + i;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t a = smem_desc(vbase + slot[i] * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
-        const uint64_t bq = smem_desc(qbase + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
-        const uint64_t bd = smem_desc(dobase + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+        const uint64_t bq = smem_desc(qh + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+        const uint64_t bd = smem_desc(dh + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
         const uint32_t acc = (i | c | kk) != 0 ? 1u : 0u;
         mma_bf16_ss(tS, a, bq, kIdesc, acc);
         mma_bf16_ss(tP, a, bd, kIdesc, acc);
       }
     }
   }
-  if (PART == 0) {
+  if (kRope) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
-      const uint64_t b = smem_desc(qbase + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+      const uint64_t b = smem_desc(qh + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
       mma_bf16_ss(tS, a, b, kIdesc, 1u);
     }
   }
@@ -156,9 +182,9 @@ __device__ __forceinline__ bool bwd_issue_s_dp(BwdMisc& m, uint32_t qbase, uint3
   return true;
 }
 
-template <int PART>
-__device__ bool run_bwd_s_dp(const FwdParams& p, BwdMisc& m, uint8_t* sbase, uint32_t tmem) {
-  using L = BwdLayout;
+template <int U, int PART>
+__device__ bool run_bwd_s_dp(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbase, uint32_t tmem) {
+  using L = BwdLayout<U>;
   const volatile int* ab = &m.abort_flag;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t dobase = smem_u32(sbase + L::kDOOff);
@@ -181,7 +207,7 @@ __device__ bool run_bwd_s_dp(const FwdParams& p, BwdMisc& m, uint8_t* sbase, uin
       if (blk < 0) break;
       // S / dP buffer n&1 was last read by the softmax of block n-2.
       if (n >= 2 && !mbar_wait(smem_u32(&m.pds_full[n & 1]), ((n - 2) >> 1) & 1, deadline, ab)) return false;
-      if (!bwd_issue_s_dp<PART>(m, qbase, dobase, vbase, rbase, tmem, n, deadline, ab)) return false;
+      if (!bwd_issue_s_dp<U, PART>(m, qbase, dobase, vbase, rbase, tmem, n, deadline, ab)) return false;
       ++n;
     }
     mma_commit(smem_u32(&m.q_empty));   // Q / dout may be replaced once these MMAs complete
@@ -192,13 +218,12 @@ __device__ bool run_bwd_s_dp(const FwdParams& p, BwdMisc& m, uint8_t* sbase, uin
 
 // ------------------------------------------------------------------ dQ, dKV issuer
 
-__device__ bool run_bwd_grad(const FwdParams& p, BwdMisc& m, uint8_t* sbase, uint32_t tmem) {
-  using L = BwdLayout;
+template <int U>
+__device__ bool run_bwd_grad(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbase, uint32_t tmem) {
+  using L = BwdLayout<U>;
   constexpr int N = L::N;
   constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, N, true, true);
   constexpr uint32_t kIdescDQr = idesc_bf16_f32(64, N, true, true);
-  constexpr uint32_t kIdescKV = idesc_bf16_f32(64, 256, false, true);
-  constexpr uint32_t kIdescKVr = idesc_bf16_f32(64, 64, false, true);
   const volatile int* ab = &m.abort_flag;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t dobase = smem_u32(sbase + L::kDOOff);
@@ -223,45 +248,64 @@ __device__ bool run_bwd_grad(const FwdParams& p, BwdMisc& m, uint8_t* sbase, uin
       if (blk < 0) break;
       if (!mbar_wait(smem_u32(&m.pds_full[n & 1]), (n >> 1) & 1, deadline, ab)) return false;
       tc_fence_after();
-      const uint32_t ps = psbase + static_cast<uint32_t>(n & 1) * 2u * L::kPSBytes;   // P^T, then dS^T
-      const uint32_t pds = ps + L::kPSBytes;
-      // dQ^T[576 x N] += K^T[576 x 64] dS^T[64 x N]: four 128-dim tiles of the
-      // value pairs, then the 64 rope dims (M = 64).  Each pair tile is free
-      // after its MMAs (dP already used it; dKV does not read it).
+      // this block's tiles: [half][P^T, dS^T]
+      const uint32_t ps = psbase + static_cast<uint32_t>(n & 1) * static_cast<uint32_t>(U * 2 * L::kPSBytes);
+      // dQ^T[576 x N] += K^T[576 x 64] dS^T[64 x N] per half: four 128-dim
+      // tiles of the value pairs, then the 64 rope dims (M = 64).  Each pair
+      // tile is free after its MMAs of every half (dP already used it; dKV
+      // does not read it).
 #pragma unroll 1
       for (int u = 0; u < 4; ++u) {
         const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u)) % L::kNV;
 #pragma unroll
-        for (int ks = 0; ks < kBlk / 16; ++ks) {
-          const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-          const uint64_t b = smem_desc(pds + ks * 16 * L::kPRow, 16 * L::kPRow * 8, 8 * L::kPRow, L::kPSwz);
-          mma_bf16_ss(tdQ + u * N, a, b, kIdescDQ, (nl > 0 || ks > 0) ? 1u : 0u);
+        for (int h = 0; h < U; ++h) {
+          const uint32_t pds = ps + static_cast<uint32_t>(h * 2 + 1) * L::kPSBytes;
+#pragma unroll
+          for (int ks = 0; ks < kBlk / 16; ++ks) {
+            const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
+            const uint64_t b = smem_desc(pds + ks * 16 * L::kPRow, 16 * L::kPRow * 8, 8 * L::kPRow, L::kPSwz);
+            mma_bf16_ss(tdQ + h * 5 * N + u * N, a, b, kIdescDQ, (nl > 0 || ks > 0) ? 1u : 0u);
+          }
         }
         mma_commit(smem_u32(&m.v_empty[s]));
       }
       const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
 #pragma unroll
-      for (int ks = 0; ks < kBlk / 16; ++ks) {
-        const uint64_t a = smem_desc(rbase + rs * kChunkBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-        const uint64_t b = smem_desc(pds + ks * 16 * L::kPRow, 16 * L::kPRow * 8, 8 * L::kPRow, L::kPSwz);
-        mma_bf16_ss(tdQ + 4 * N, a, b, kIdescDQr, (nl > 0 || ks > 0) ? 1u : 0u);
+      for (int h = 0; h < U; ++h) {
+        const uint32_t pds = ps + static_cast<uint32_t>(h * 2 + 1) * L::kPSBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBlk / 16; ++ks) {
+          const uint64_t a = smem_desc(rbase + rs * kChunkBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
+          const uint64_t b = smem_desc(pds + ks * 16 * L::kPRow, 16 * L::kPRow * 8, 8 * L::kPRow, L::kPSwz);
+          mma_bf16_ss(tdQ + h * 5 * N + 4 * N, a, b, kIdescDQr, (nl > 0 || ks > 0) ? 1u : 0u);
+        }
       }
       mma_commit(smem_u32(&m.rp_empty[rs]));
-      // dKV rows of the block, three column chunks: (sm_scale dS)^T Q plus
-      // P^T [dout, 0].  A: the P^T / dS^T tiles as K-major [64 rows x 16
-      // heads]; B: Q / dout as MN-major [16 heads x dims].
-      const uint64_t a_ds = smem_desc(pds, 16, 8 * L::kPRow, L::kPSwz);
-      const uint64_t a_p = smem_desc(ps, 16, 8 * L::kPRow, L::kPSwz);
+      // dKV rows of the block in three column chunks: the sum over halves of
+      // (sm_scale dS)^T Q plus P^T [dout, 0].  A: the P^T / dS^T tiles as
+      // K-major [64 rows x 16 heads]; B: Q / dout as MN-major [16 heads x
+      // dims] (their 64-dim chunks sit N * 128 bytes apart).
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
+        const int col0 = c * L::kKVChunk;
+        const int wq = 576 - col0 < L::kKVChunk ? 576 - col0 : L::kKVChunk;   // Q columns of the chunk
+        const int wd = 512 - col0 < wq ? 512 - col0 : wq;                     // dout columns (may be none)
         if (!mbar_wait(smem_u32(&m.dkv_empty), (static_cast<uint32_t>(chunks) & 1u) ^ 1u, deadline, ab))
           return false;
         tc_fence_after();
-        const uint64_t bq = smem_desc(qbase + 4 * c * N * 128, N * 128, 1024, SWZ_128B);
-        mma_bf16_ss(tKV, a_ds, bq, c < 2 ? kIdescKV : kIdescKVr, 0u);
-        if (c < 2) {
-          const uint64_t bd = smem_desc(dobase + 4 * c * N * 128, N * 128, 1024, SWZ_128B);
-          mma_bf16_ss(tKV, a_p, bd, kIdescKV, 1u);
+#pragma unroll
+        for (int h = 0; h < U; ++h) {
+          const uint32_t pt = ps + static_cast<uint32_t>(h * 2) * L::kPSBytes;
+          const uint64_t a_p = smem_desc(pt, 16, 8 * L::kPRow, L::kPSwz);
+          const uint64_t a_ds = smem_desc(pt + L::kPSBytes, 16, 8 * L::kPRow, L::kPSwz);
+          const uint64_t bq =
+              smem_desc(qbase + h * L::kQHalf + (col0 / 64) * N * 128, N * 128, 1024, SWZ_128B);
+          mma_bf16_ss(tKV, a_ds, bq, idesc_bf16_f32(64, wq, false, true), h > 0 ? 1u : 0u);
+          if (wd > 0) {
+            const uint64_t bd =
+                smem_desc(dobase + h * L::kDOHalf + (col0 / 64) * N * 128, N * 128, 1024, SWZ_128B);
+            mma_bf16_ss(tKV, a_p, bd, idesc_bf16_f32(64, wd, false, true), 1u);
+          }
         }
         mma_commit(smem_u32(&m.dkv_full));
         ++chunks;
@@ -294,8 +338,9 @@ __device__ __forceinline__ void drain_cols(uint32_t taddr, int col, float* dst_r
   }
 }
 
-__device__ bool run_bwd_drain(const FwdParams& p, BwdMisc& m, uint32_t tmem) {
-  using L = BwdLayout;
+template <int U>
+__device__ bool run_bwd_drain(const FwdParams& p, BwdMisc<U>& m, uint32_t tmem) {
+  using L = BwdLayout<U>;
   const volatile int* ab = &m.abort_flag;
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
@@ -327,13 +372,10 @@ __device__ bool run_bwd_drain(const FwdParams& p, BwdMisc& m, uint32_t tmem) {
         const bool ok = mbar_wait(smem_u32(&m.dkv_full), static_cast<uint32_t>(chunks) & 1u, deadline, ab);
         if (!__all_sync(0xffffffffu, ok)) return false;
         tc_fence_after();
-        if (c < 2) {
+        const int col0 = c * L::kKVChunk;
+        const int w = 576 - col0 < L::kKVChunk ? 576 - col0 : L::kKVChunk;
 #pragma unroll 1
-          for (int col = 0; col < 256; col += 32) drain_cols(tKV, col, dst + c * 256, row >= 0, half);
-        } else {
-#pragma unroll
-          for (int col = 0; col < 64; col += 32) drain_cols(tKV, col, dst + 512, row >= 0, half);
-        }
+        for (int col = 0; col < w; col += 32) drain_cols(tKV, col, dst + col0, row >= 0, half);
         tc_fence_before();
         mbar_arrive(smem_u32(&m.dkv_empty));
         ++chunks;
@@ -347,10 +389,12 @@ __device__ bool run_bwd_drain(const FwdParams& p, BwdMisc& m, uint32_t tmem) {
 
 // ------------------------------------------------------------------ P, dS and dq
 
-__device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc& m, uint8_t* sbase, uint32_t tmem) {
-  using L = BwdLayout;
+template <int U>
+__device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbase, uint32_t tmem) {
+  using L = BwdLayout<U>;
   constexpr int N = L::N;
-  constexpr int HH = N / 2;                            // heads per half-warp
+  constexpr int H = L::H;                              // heads per unit
+  constexpr int HH = N / 2;                            // heads per half-warp (of one half)
   const volatile int* ab = &m.abort_flag;
   constexpr uint32_t bar_id = 1u;
   const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -371,8 +415,8 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc& m, uint8_t* sbase, 
   while (next_item(p, iter, item)) {
     deadline = global_timer_ns() + p.timeout_ns;
     const int tok = item.unit / p.groups;
-    const int h0 = (item.unit % p.groups) * N;
-    const int hv = min(N, p.h_q - h0);
+    const int h0 = (item.unit % p.groups) * H;
+    const int hv = min(H, p.h_q - h0);
     const size_t tok_h = static_cast<size_t>(tok) * p.h_q + h0;
     if (items > 0) {
       // Q and dout are replaced once the previous unit's MMAs reading them
@@ -381,25 +425,27 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc& m, uint8_t* sbase, 
       if (bar_red_or_128(bar_id, !ok)) return false;
     }
     // Q (9 chunks) and dout (8 chunks) of the unit's heads -> shared memory,
-    // K-major with the 128B swizzle; heads past h_q are zero-filled.
+    // each half K-major with the 128B swizzle; heads past h_q are zero-filled.
     {
       const __nv_bfloat16* qt = p.q + tok_h * kDqk;
-      for (int x = tid; x < N * 72; x += 128) {
-        const int h = x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
-        const bool live = h < hv;
-        cp_async_16(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4),
-                    qt + static_cast<size_t>(live ? h : 0) * kDqk + c * 64 + piece * 8, live ? 16u : 0u);
+      for (int x = tid; x < H * 72; x += 128) {
+        const int hd = x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
+        const int hf = hd / N, hh = hd % N;
+        const bool live = hd < hv;
+        cp_async_16(qbase + hf * L::kQHalf + c * (N * 128) + hh * 128 + ((piece ^ (hh & 7)) << 4),
+                    qt + static_cast<size_t>(live ? hd : 0) * kDqk + c * 64 + piece * 8, live ? 16u : 0u);
       }
       const __nv_bfloat16* dt = p.dout + tok_h * kDv;
-      for (int x = tid; x < N * 64; x += 128) {
-        const int h = x / 64, rem = x % 64, c = rem >> 3, piece = rem & 7;
-        const bool live = h < hv;
-        cp_async_16(dobase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4),
-                    dt + static_cast<size_t>(live ? h : 0) * kDv + c * 64 + piece * 8, live ? 16u : 0u);
+      for (int x = tid; x < H * 64; x += 128) {
+        const int hd = x / 64, rem = x % 64, c = rem >> 3, piece = rem & 7;
+        const int hf = hd / N, hh = hd % N;
+        const bool live = hd < hv;
+        cp_async_16(dobase + hf * L::kDOHalf + c * (N * 128) + hh * 128 + ((piece ^ (hh & 7)) << 4),
+                    dt + static_cast<size_t>(live ? hd : 0) * kDv + c * 64 + piece * 8, live ? 16u : 0u);
       }
       // D = rowsum(dout * out) per head: eight threads per head, 64 columns each.
-      {
-        const int h = tid >> 3, part = tid & 7;
+      for (int h = tid >> 3; h < H; h += 16) {
+        const int part = tid & 7;
         float acc = 0.f;
         if (h < hv) {
           const uint4* o4 = reinterpret_cast<const uint4*>(p.out + (tok_h + h) * kDv + part * 64);
@@ -429,12 +475,14 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc& m, uint8_t* sbase, 
       named_bar_sync(bar_id, 128);
       if (tid == 0) mbar_arrive(smem_u32(&m.q_full));
     }
-    float dsum[HH], lse2[HH];
+    float dsum[U][HH], lse2[U][HH];
 #pragma unroll
-    for (int i = 0; i < HH; ++i) {
-      dsum[i] = m.dsum[hsub + i];
-      lse2[i] = m.lse2[hsub + i];
-    }
+    for (int hf = 0; hf < U; ++hf)
+#pragma unroll
+      for (int i = 0; i < HH; ++i) {
+        dsum[hf][i] = m.dsum[hf * N + hsub + i];
+        lse2[hf][i] = m.lse2[hf * N + hsub + i];
+      }
 
     int nl = 0;
     for (;;) {
@@ -454,26 +502,43 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc& m, uint8_t* sbase, 
            mbar_wait(smem_u32(&m.s_full[1][n & 1]), (n >> 1) & 1, deadline, ab);
       tc_fence_after();
       if (bar_red_or_128(bar_id, !ok)) return false;
-      float sa[HH], sb[HH], pa[HH], pb[HH];
       const uint32_t col = static_cast<uint32_t>(n & 1) * N;
-      tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTS + col, sa);
-      tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTS + 2 * N + col, sb);
-      tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTdP + col, pa);
-      tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTdP + 2 * N + col, pb);
-      tmem_wait_ld();
-      float pr[HH], ds[HH];
-#pragma unroll
-      for (int i = 0; i < HH; ++i) {
-        pr[i] = valid ? fast_exp2((sa[i] + sb[i]) * p.scale_log2 - lse2[i]) : 0.f;
-        ds[i] = pr[i] * ((pa[i] + pb[i]) - dsum[i]) * sm_scale;
-      }
-      const uint32_t ps = psbase + static_cast<uint32_t>(n & 1) * 2u * L::kPSBytes;
+      const uint32_t ps0 = psbase + static_cast<uint32_t>(n & 1) * static_cast<uint32_t>(U * 2 * L::kPSBytes);
       const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
       const uint32_t off = static_cast<uint32_t>(row * L::kPRow) + (((static_cast<uint32_t>(hsub / 8)) ^ sw) << 4);
-      st_shared_v4(ps + off, pack_bf16x2(pr[0], pr[1]), pack_bf16x2(pr[2], pr[3]), pack_bf16x2(pr[4], pr[5]),
-                   pack_bf16x2(pr[6], pr[7]));
-      st_shared_v4(ps + L::kPSBytes + off, pack_bf16x2(ds[0], ds[1]), pack_bf16x2(ds[2], ds[3]),
-                   pack_bf16x2(ds[4], ds[5]), pack_bf16x2(ds[6], ds[7]));
+#pragma unroll
+      for (int hf = 0; hf < U; ++hf) {
+        // U = 1: S and dP are the sums of the two parts; U = 2: half hf's own.
+        float s[HH], d[HH];
+        if constexpr (U == 1) {
+          float sb[HH], db[HH];
+          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTS + col, s);
+          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTS + 2 * N + col, sb);
+          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTdP + col, d);
+          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTdP + 2 * N + col, db);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < HH; ++i) {
+            s[i] += sb[i];
+            d[i] += db[i];
+          }
+        } else {
+          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTS + hf * 2 * N + col, s);
+          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTdP + hf * 2 * N + col, d);
+          tmem_wait_ld();
+        }
+        float pr[HH], ds[HH];
+#pragma unroll
+        for (int i = 0; i < HH; ++i) {
+          pr[i] = valid ? fast_exp2(s[i] * p.scale_log2 - lse2[hf][i]) : 0.f;
+          ds[i] = pr[i] * (d[i] - dsum[hf][i]) * sm_scale;
+        }
+        const uint32_t ps = ps0 + static_cast<uint32_t>(hf * 2) * L::kPSBytes;
+        st_shared_v4(ps + off, pack_bf16x2(pr[0], pr[1]), pack_bf16x2(pr[2], pr[3]), pack_bf16x2(pr[4], pr[5]),
+                     pack_bf16x2(pr[6], pr[7]));
+        st_shared_v4(ps + L::kPSBytes + off, pack_bf16x2(ds[0], ds[1]), pack_bf16x2(ds[2], ds[3]),
+                     pack_bf16x2(ds[4], ds[5]), pack_bf16x2(ds[6], ds[7]));
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&m.pds_full[n & 1]));
@@ -489,24 +554,28 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc& m, uint8_t* sbase, 
       if (bar_red_or_128(bar_id, !ok)) return false;
       ++filled;
     }
-    float* dq = p.dq + tok_h * kDqk;
 #pragma unroll 1
-    for (int mt = 0; mt < 5; ++mt) {
-      float o[16];
-      if (nl > 0) {
-        tmem_ld16(tmem + lane_off + L::kTdQ + mt * N, o);
-        tmem_wait_ld();
-      } else {
+    for (int hf = 0; hf < U; ++hf) {
+      float* dq = p.dq + (tok_h + hf * N) * kDqk;
+      const int hvf = hv - hf * N;   // live heads of this half (may be <= 0)
+#pragma unroll 1
+      for (int mt = 0; mt < 5; ++mt) {
+        float o[16];
+        if (nl > 0) {
+          tmem_ld16(tmem + lane_off + L::kTdQ + hf * 5 * N + mt * N, o);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = 0.f;
-      }
-      // tiles 0..3: lane = dim 128 mt + 32 q4 + lane; the rope tile (M=64):
-      // dims 512 + 16 q4 + lane for lanes 0..15.
-      const int dim = mt < 4 ? mt * 128 + q4 * 32 + lane : 512 + q4 * 16 + lane;
-      if (mt < 4 || lane < 16) {
+          for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        }
+        // tiles 0..3: lane = dim 128 mt + 32 q4 + lane; the rope tile (M=64):
+        // dims 512 + 16 q4 + lane for lanes 0..15.
+        const int dim = mt < 4 ? mt * 128 + q4 * 32 + lane : 512 + q4 * 16 + lane;
+        if (mt < 4 || lane < 16) {
 #pragma unroll
-        for (int h = 0; h < 16; ++h)
-          if (h < hv) dq[static_cast<size_t>(h) * kDqk + dim] = o[h];
+          for (int h = 0; h < 16; ++h)
+            if (h < hvf) dq[static_cast<size_t>(h) * kDqk + dim] = o[h];
+        }
       }
     }
     tc_fence_before();
@@ -517,11 +586,12 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc& m, uint8_t* sbase, 
 
 // ------------------------------------------------------------------ kernel
 
-__global__ void __launch_bounds__(BwdLayout::kThreads, 1) sparse_mla_bwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = BwdLayout;
+template <int U>
+__global__ void __launch_bounds__(BwdLayout<U>::kThreads, 1) sparse_mla_bwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = BwdLayout<U>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  BwdMisc& m = *reinterpret_cast<BwdMisc*>(sbase + L::kMiscOff);
+  BwdMisc<U>& m = *reinterpret_cast<BwdMisc<U>*>(sbase + L::kMiscOff);
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
 
@@ -566,13 +636,15 @@ __global__ void __launch_bounds__(BwdLayout::kThreads, 1) sparse_mla_bwd_kernel(
 
   if (m.prior_error == 0) {
     if (warp < kProducerWarps) {
-      if (!run_producer_t<kBwdHeads, BwdLayout, BwdMisc, true>(p, m, sbase)) bwd_raise(m, kErrProducerWait);
+      // The ring of U = 2 is 1.5 blocks deep: take its slots one by one (the
+      // producer's strategy for shallow rings).
+      if (!run_producer_t<U == 1 ? kBwdHeads : 64, L, BwdMisc<U>, true>(p, m, sbase)) bwd_raise(m, kErrProducerWait);
       asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp == L::kQkWarp0 || warp == L::kQkWarp1 || warp == L::kGradWarp) {
       if (lane == 0) {
         const int role = warp == L::kQkWarp0 ? 0 : (warp == L::kQkWarp1 ? 1 : 2);
-        const bool ok = role == 0 ? run_bwd_s_dp<0>(p, m, sbase, tmem)
-                                  : (role == 1 ? run_bwd_s_dp<1>(p, m, sbase, tmem) : run_bwd_grad(p, m, sbase, tmem));
+        const bool ok = role == 0 ? run_bwd_s_dp<U, 0>(p, m, sbase, tmem)
+                                  : (role == 1 ? run_bwd_s_dp<U, 1>(p, m, sbase, tmem) : run_bwd_grad<U>(p, m, sbase, tmem));
         if (!ok) bwd_raise(m, role == 2 ? kErrBwdGradWait : kErrMmaWait);
         const int never = 0;
         mma_commit(smem_u32(&m.drain[role]));
@@ -580,9 +652,9 @@ __global__ void __launch_bounds__(BwdLayout::kThreads, 1) sparse_mla_bwd_kernel(
       }
       __syncwarp();
     } else if (warp >= L::kDrainWarp0) {
-      if (!run_bwd_drain(p, m, tmem)) bwd_raise(m, kErrBwdDrainWait);
+      if (!run_bwd_drain<U>(p, m, tmem)) bwd_raise(m, kErrBwdDrainWait);
     } else {
-      if (!run_bwd_softmax(p, m, sbase, tmem)) bwd_raise(m, kErrSoftmaxWait);
+      if (!run_bwd_softmax<U>(p, m, sbase, tmem)) bwd_raise(m, kErrSoftmaxWait);
     }
   }
   tc_fence_before();

@@ -61,8 +61,10 @@ sparse_mla_status_t device_setup(int* sm_count) {
                              smla::smem_bytes<32>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::smem_bytes<64>()) != cudaSuccess ||
-        cudaFuncSetAttribute(smla::sparse_mla_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smla::bwd_smem_bytes()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::sparse_mla_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::bwd_smem_bytes<1>()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::sparse_mla_bwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::bwd_smem_bytes<2>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::dsa_scores_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::idx_smem_bytes()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::dsa_scores_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -253,7 +255,8 @@ sparse_mla_status_t sparse_mla_fwd_causal(const void* q, const void* kv, float s
 namespace {
 
 // Shared tail of the two backward entry points: dkv zeroed on the stream,
-// then the persistent backward grid over units of one token x 16 heads.
+// then the persistent backward grid over units of one token x 16 heads (x 32
+// heads above 16).
 sparse_mla_status_t launch_bwd(FwdParams p, long long n_tok, int h_q, long long n_rows, float* dq, float* dkv,
                                int sms, cudaStream_t cs) {
   if (n_rows > 0 &&
@@ -267,11 +270,17 @@ sparse_mla_status_t launch_bwd(FwdParams p, long long n_tok, int h_q, long long 
                : SPARSE_MLA_ERR_CUDA;
   p.dq = dq;
   p.dkv = dkv;
-  p.groups = (h_q + smla::kBwdHeads - 1) / smla::kBwdHeads;   // units of 16 heads
+  // Units of 16 heads up to 16 heads, else of 32 (two halves of 16 that
+  // share the gather and each block's dkv reduction).
+  const int unit_heads = h_q <= smla::kBwdHeads ? smla::kBwdHeads : 2 * smla::kBwdHeads;
+  p.groups = (h_q + unit_heads - 1) / unit_heads;
   p.sched = smla::kWholeUnits;
   const long long units = n_tok * p.groups;
   p.ctas = static_cast<int>(units < sms ? units : sms);
-  smla::sparse_mla_bwd_kernel<<<p.ctas, smla::BwdLayout::kThreads, smla::bwd_smem_bytes(), cs>>>(p);
+  if (unit_heads == smla::kBwdHeads)
+    smla::sparse_mla_bwd_kernel<1><<<p.ctas, smla::BwdLayout<1>::kThreads, smla::bwd_smem_bytes<1>(), cs>>>(p);
+  else
+    smla::sparse_mla_bwd_kernel<2><<<p.ctas, smla::BwdLayout<2>::kThreads, smla::bwd_smem_bytes<2>(), cs>>>(p);
   return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
 }
 

@@ -64,6 +64,9 @@ def parse_args():
                     help="time the DSA indexer + top-k (dsa_indexer_topk) that produces the index lists, on "
                          "the token shape of config 1-4 with 64 indexer heads of width 128; FLOPs "
                          "2*64*128 per scored (row, visible position)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="profiling aid for the dense prefill configs (1-3): s_q = s_kv = TOKENS with the "
+                         "config's heads, list pattern and seed (a smaller case of the same kernel)")
     ap.add_argument("--clock-log", default=None,
                     help="directory for the nvidia-smi clock CSV of the run (default: the system temp dir)")
     return ap.parse_args()
@@ -256,9 +259,17 @@ def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_total_ms
     return flops_per_step * steps * world / (max_total_ms * 1e-3) / 1e12
 
 
-def workload(config: int):
+def workload(config: int, tokens=None):
+    """Workload `config`; with `tokens`, a dense prefill config regenerated at
+    s_q = s_kv = tokens (same heads, list pattern and seed)."""
     import mla_inputs as mi
-    return mi.config(config)
+    if tokens is None:
+        return mi.config(config)
+    if config not in (1, 2, 3):
+        raise SystemExit("--tokens applies to the dense prefill configs 1-3")
+    h, pattern = (64, "recent") if config == 3 else (8, "causal")
+    return mi.prefill_case(1000 + config, tokens, tokens, h, pattern=pattern,
+                           name=f"c{config}_at_{tokens}_tokens")
 
 
 def valid_entries(case) -> int:
@@ -274,7 +285,14 @@ def step_flops(case) -> float:
     return mi.nominal_flops(n_tok, h, case.indices.shape[-1])
 
 
-def workload_name(case, config: int) -> str:
+def workload_name(case, config: int, tokens=None) -> str:
+    if tokens is not None:
+        return (f"{'wide-head' if config == 3 else 'dense'} prefill s_q=s_kv={tokens} h_q={case.q.shape[1]} "
+                f"d_qk=576 d_v=512 topk=2048 bf16 (profiling size)")
+    return _workload_name(config)
+
+
+def _workload_name(config: int) -> str:
     names = {1: "tiny prefill s_q=s_kv=64 h_q=8",
              2: "mid prefill s_q=s_kv=2119 h_q=8",
              3: "wide-head prefill s_q=s_kv=8192 h_q=64",
@@ -417,10 +435,10 @@ def run_ours(args, rank, world, dist):
 
     # The oracle pool (spawn) starts before the first GPU work.
     pool = None
-    if rank == 0 and not args.no_cpu_baseline and not args.causal and not args.bwd:
+    if rank == 0 and not args.no_cpu_baseline and not args.causal and not args.bwd and args.tokens is None:
         pool = OraclePool(args.config, os.cpu_count() or 1)
 
-    case = workload(args.config)
+    case = workload(args.config, args.tokens)
     stream = torch.cuda.current_stream(dev)
     is_decode = hasattr(case, "kv_cache")
     is_varlen = hasattr(case, "cu_seqlens_q")
@@ -587,7 +605,8 @@ def run_ours(args, rank, world, dist):
         "value": whole_job_tflops(flops, args.steps, world, total_ms), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(case, args.config) + (" (indices-free causal mode)" if args.causal else "")
+        "config": {"workload": workload_name(case, args.config, args.tokens)
+                   + (" (indices-free causal mode)" if args.causal else "")
                    + (" (backward: dq, dkv)" if args.bwd else ""),
                    "seed": 1000 + args.config,
                    "l2": "256 MB buffer written before every timed step (cold L2)",

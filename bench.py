@@ -82,18 +82,28 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {
+    "fwd": ("fwd_kernel.cuh", "ptx.cuh", "sparse_mla_api.cu"),
+    "bwd": ("bwd_kernel.cuh", "fwd_kernel.cuh", "ptx.cuh", "sparse_mla_api.cu"),
+    "idx": ("indexer_kernel.cuh", "fwd_kernel.cuh", "ptx.cuh", "sparse_mla_api.cu"),
+}
+
+
+def kernel_source_hash(kind: str = "fwd") -> str:
+    """Hash of the sources a kernel family is built from (fwd, bwd, idx)."""
     h = hashlib.sha256()
-    for name in ("fwd_kernel.cuh", "ptx.cuh", "sparse_mla_api.cu"):
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "serving_sparse_mla_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config: int):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"fwd_kernel_config{config}_ncu.txt")
+def profiled_traffic(config: int, kind: str = "fwd"):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel sources (else None)."""
+    name = {"fwd": f"fwd_kernel_config{config}_ncu.txt", "bwd": f"bwd_kernel_config{config}_ncu.txt",
+            "idx": f"dsa_indexer_config{config}_ncu.txt"}[kind]
+    path = os.path.join(ROOT, "profiles", name)
     try:
         kv = {}
         with open(path) as f:
@@ -101,7 +111,7 @@ def profiled_traffic(config: int):
                 if ":" in line:
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_sha") != kernel_source_hash():
+        if kv.get("kernel_source_sha") != kernel_source_hash(kind):
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -580,14 +590,14 @@ def run_ours(args, rank, world, dist):
     if bound == "hbm":
         achieved = kv_bytes / (fwd_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": p_bw, "unit": "GB/s",
-                    "frac": achieved / p_bw, "traffic": None if (args.causal or args.bwd) else profiled_traffic(args.config),
+                    "frac": achieved / p_bw, "traffic": None if args.causal else profiled_traffic(args.config, "bwd" if args.bwd else "fwd"),
                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                     "algorithmic_bytes_per_launch": kv_bytes,
                     "note": "achieved = valid entries x 1152 B / mean launch time (cold L2)"}
     else:
         achieved = flops / (fwd_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": p_tf, "unit": "TFLOP/s",
-                    "frac": achieved / p_tf, "traffic": None if (args.causal or args.bwd) else profiled_traffic(args.config),
+                    "frac": achieved / p_tf, "traffic": None if args.causal else profiled_traffic(args.config, "bwd" if args.bwd else "fwd"),
                     "peak_kind": f"{peak_kind} bf16 (burst)", "algorithmic_flops_per_launch": flops}
 
     cpu = None
@@ -833,12 +843,12 @@ def run_indexer(args, rank, world, dist):
         if sc_flops / (p_tf * 1e12) >= sc_bytes / (p_bw * 1e9):
             ach = sc_flops / (sc_ms * 1e-3) / 1e12
             roofline = {"bound": "tensor", "achieved": ach, "peak": p_tf, "unit": "TFLOP/s", "frac": ach / p_tf,
-                        "traffic": None, "kernel": "dsa_scores_kernel", "peak_kind": f"{peak_kind} bf16 (burst)",
+                        "traffic": profiled_traffic(args.config, "idx"), "kernel": "dsa_scores_kernel", "peak_kind": f"{peak_kind} bf16 (burst)",
                         "algorithmic_flops_per_launch": sc_flops, "us_per_launch": sc_ms * 1e3}
         else:
             ach = sc_bytes / (sc_ms * 1e-3) / 1e9
             roofline = {"bound": "hbm", "achieved": ach, "peak": p_bw, "unit": "GB/s", "frac": ach / p_bw,
-                        "traffic": None, "kernel": "dsa_scores_kernel", "peak_kind": f"{peak_kind} copy bandwidth",
+                        "traffic": profiled_traffic(args.config, "idx"), "kernel": "dsa_scores_kernel", "peak_kind": f"{peak_kind} copy bandwidth",
                         "algorithmic_bytes_per_launch": sc_bytes, "us_per_launch": sc_ms * 1e3}
     cpu = None
     if pool is not None:

@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bwd", action="store_true",
-                    help="time the backward (dq, dkv) on a dense prefill config (1-3); nominal FLOPs "
+                    help="time the backward (dq, dkv) on a prefill config (1-4); nominal FLOPs "
                          "2*(3*576 + 2*512) per (token, head, top-k entry), bytes per valid entry = "
                          "1152 gathered + 2304 of fp32 dkv reduction")
     ap.add_argument("--causal", action="store_true",
@@ -452,8 +452,10 @@ def run_ours(args, rank, world, dist):
     stream = torch.cuda.current_stream(dev)
     is_decode = hasattr(case, "kv_cache")
     is_varlen = hasattr(case, "cu_seqlens_q")
-    if (args.causal or args.bwd) and (is_decode or is_varlen):
-        raise SystemExit("--causal / --bwd need a dense prefill config (1-3)")
+    if args.causal and (is_decode or is_varlen):
+        raise SystemExit("--causal needs a dense prefill config (1-3)")
+    if args.bwd and is_decode:
+        raise SystemExit("--bwd needs a prefill config (1-4)")
     if args.causal and args.bwd:
         raise SystemExit("--causal and --bwd are separate modes")
     n_tok = case.batch * case.s_next if is_decode else case.q.shape[0]
@@ -474,6 +476,16 @@ def run_ours(args, rank, world, dist):
                       idx=d(case.indices))
         ws = torch.empty(max(1, smla.decode_workspace_size(case.batch, case.s_next, case.h_q, 2048)),
                          dtype=torch.uint8, device=dev)
+    elif is_varlen and args.bwd:
+        inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices), cuq=d(case.cu_seqlens_q),
+                      cuk=d(case.cu_seqlens_kv))
+        o_fwd, l_fwd = smla.sparse_mla_fwd_varlen(inputs["q"], inputs["kv"], inputs["idx"], inputs["cuq"],
+                                                  inputs["cuk"], case.sm_scale)
+        g_do = torch.Generator().manual_seed(2000 + args.config)
+        inputs.update(out=o_fwd, lse=l_fwd,
+                      dout=torch.randn(o_fwd.shape, generator=g_do).to(torch.bfloat16).to(dev))
+        dq_buf = torch.empty(case.q.shape, dtype=torch.float32, device=dev)
+        dkv_buf = torch.empty((case.kv.shape[0], 576), dtype=torch.float32, device=dev)
     elif is_varlen:
         inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices), cuq=d(case.cu_seqlens_q),
                       cuk=d(case.cu_seqlens_kv))
@@ -498,6 +510,9 @@ def run_ours(args, rank, world, dist):
             smla.sparse_mla_decode(inp["q"], inp["kv"], inp["bt"], inp["sl"], inp["idx"], case.sm_scale,
                                    case.page_size, workspace=ws, out=out.view(case.batch, case.s_next, h_q, 512),
                                    lse=lse.view(case.batch, case.s_next, h_q), stream=stream)
+        elif is_varlen and args.bwd:
+            smla.sparse_mla_bwd_varlen(inp["q"], inp["kv"], inp["idx"], inp["cuq"], inp["cuk"], case.sm_scale,
+                                       inp["out"], inp["lse"], inp["dout"], dq=dq_buf, dkv=dkv_buf, stream=stream)
         elif is_varlen:
             smla.sparse_mla_fwd_varlen(inp["q"], inp["kv"], inp["idx"], inp["cuq"], inp["cuk"], case.sm_scale,
                                        out=out, lse=lse, stream=stream)

@@ -402,3 +402,51 @@ def tied_scores(seed: int, rows: int, width: int, levels: int = 7) -> torch.Tens
     hole = torch.rand((rows, width), generator=g) < 0.02
     s[hole] = float("-inf")
     return s
+
+
+@dataclass
+class IndexerPagedCase:
+    """Decode indexer inputs: q_idx [batch, s_next, h_idx, d_idx] bf16, a
+    paged key cache k_cache [num_blocks, page, d_idx] bf16 with its
+    block_table [batch, max_blocks] int32 and cache_seqlens [batch] int32,
+    weights [batch, s_next, h_idx] fp32."""
+    name: str
+    q_idx: torch.Tensor
+    k_cache: torch.Tensor
+    block_table: torch.Tensor
+    cache_seqlens: torch.Tensor
+    weights: torch.Tensor
+    topk: int
+    page: int = PAGE
+
+
+def indexer_paged_case(seed: int, batch: int, s_next: int, lo: int, hi: int, h_idx: int = H_IDX,
+                       d_idx: int = D_IDX, topk: int = TOPK, page: int = PAGE, spare_pages: int = 16,
+                       poison: bool = True, name: str = "") -> IndexerPagedCase:
+    """Request b holds L_b ~ U[lo, hi] positions; its s_next MTP query rows
+    are the last s_next positions.  The page pool holds sum(ceil(L_b / page))
+    + spare_pages pages in a random order (the block table is a random
+    permutation); with ``poison`` every slot past a request's length, and
+    every spare page, is NaN."""
+    g = _gen(seed * 104729 + 7)
+    lens = torch.randint(lo, hi + 1, (batch,), generator=g, dtype=torch.int64)
+    n_pages = [max(1, int(math.ceil(int(L) / page))) for L in lens]
+    num_blocks = sum(n_pages) + spare_pages
+    max_blocks = max(n_pages)
+    perm = torch.randperm(num_blocks, generator=g).to(torch.int32)
+    block_table = torch.zeros((batch, max_blocks), dtype=torch.int32)
+    off = 0
+    for b in range(batch):
+        block_table[b, : n_pages[b]] = perm[off: off + n_pages[b]]
+        off += n_pages[b]
+    q = randn_bf16(g, (batch, s_next, h_idx, d_idx))
+    k_cache = randn_bf16(g, (num_blocks, page, d_idx))
+    w = indexer_weights(g, batch * s_next, h_idx, d_idx).view(batch, s_next, h_idx)
+    if poison:
+        keep = torch.zeros(num_blocks * page, dtype=torch.bool)
+        for b in range(batch):
+            pos = torch.arange(int(lens[b]), dtype=torch.int64)
+            keep[block_table[b, pos // page].to(torch.int64) * page + pos % page] = True
+        k_cache.view(-1, d_idx)[~keep] = float("nan")
+    return IndexerPagedCase(name or f"indexer_paged_b{batch}_s{s_next}", q, k_cache, block_table,
+                            lens.to(torch.int32), w, topk, page)

@@ -34,7 +34,10 @@ largest I[t,s].  Two points the pages leave open, read here as:
 With V(t) <= topk every visible position is selected, so the list is
 0 .. V(t)-1 then -1s, and no score is needed: the short-prefill rows of the
 TileLang page's Summary.  Packed (varlen) prefill applies the same rules per
-sequence with local positions, the convention of the packed forward.
+sequence with local positions, the convention of the packed forward; the
+paged decode form reads a request's keys through its block table, with the
+request's s_next MTP tokens at the end of its cache_seqlens positions (the
+forward's decode convention).
 
 Pins (tests/test_indexer_oracle_pins.py): a worked example with small integers
 whose scores and selection are computed by hand, positive homogeneity and
@@ -42,9 +45,11 @@ additivity in the weights, the ReLU's zero floor (a key anti-aligned with
 every query scores exactly 0), selection against brute-force properties
 (every selected score >= every unselected one, ties resolved to the smaller
 positions), agreement with torch.topk on distinct scores, the short-row
-identity lists, the packed form against the dense form per sequence, and the
-link to the forward: with every row short, the sparse forward over these
-lists equals the indices-free causal forward.
+identity lists, the packed form against the dense form per sequence, the
+paged (decode) form against the packed form on a linearised cache and under a
+shuffle of the physical pages, and the link to the forward: with every row
+short, the sparse forward over these lists equals the indices-free causal
+forward.
 """
 from __future__ import annotations
 
@@ -184,4 +189,43 @@ def topk_rows(scores: np.ndarray, lens: Sequence[int], topk: int) -> np.ndarray:
             out[i] = identity_list(v, topk)
         else:
             out[i] = select_topk(np.asarray(scores[i, :v], dtype=np.float64), topk)
+    return out
+
+
+def linearise_keys(k_cache, block_table, seqlen: int, page: int) -> np.ndarray:
+    """The keys of one request in position order: position s is row s % page
+    of physical block block_table[s // page] (a paged key cache laid out like
+    the forward's paged KV cache)."""
+    kc = _f64(k_cache)
+    bt = [int(x) for x in block_table]
+    rows = [kc[bt[s // page], s % page] for s in range(seqlen)]
+    return np.stack(rows) if rows else np.zeros((0, kc.shape[-1]))
+
+
+def dsa_indices_paged(q_idx, k_cache, weights, block_table, cache_seqlens, topk: int, page: int,
+                      rows: Optional[Sequence[int]] = None) -> np.ndarray:
+    """Decode: request b has s_next query rows b s_next .. b s_next + s_next - 1
+    at the end of its cache_seqlens[b] positions (MTP token j sits at
+    position L_b - s_next + j and sees positions 0 .. L_b - s_next + j), its
+    keys in the paged cache k_cache [num_blocks, page, D_I] through
+    block_table [batch, max_blocks].  The dense rules per request on its
+    linearised keys.  q_idx [batch, s_next, H_I, D_I], weights
+    [batch, s_next, H_I].  Returns int64 [len(rows), topk] over the flattened
+    rows b s_next + j."""
+    batch, s_next = q_idx.shape[0], q_idx.shape[1]
+    q2 = q_idx.reshape(batch * s_next, *q_idx.shape[2:])
+    w2 = weights.reshape(batch * s_next, -1)
+    toks = range(batch * s_next) if rows is None else list(rows)
+    out = np.full((len(toks), topk), -1, dtype=np.int64)
+    keys = {}
+    for i, r in enumerate(toks):
+        b, j = divmod(r, s_next)
+        lk = int(cache_seqlens[b])
+        v = visible_len(j, s_next, lk)
+        if v <= topk:
+            out[i] = identity_list(v, topk)
+            continue
+        if b not in keys:
+            keys[b] = linearise_keys(k_cache, block_table[b], lk, page)
+        out[i] = select_topk(token_scores(_f64(q2[r]), _f64(w2[r]), keys[b][:v]), topk)
     return out

@@ -189,11 +189,64 @@ def pin_short_rows_reproduce_causal_forward():
     np.testing.assert_allclose(l1, l2, rtol=1e-12, atol=1e-13)
 
 
+def _paged(seed, poison=True):
+    return mi.indexer_paged_case(seed, 3, 5, 60, 330, h_idx=8, d_idx=32, topk=48, poison=poison)
+
+
+def pin_paged_identity_table_is_dense():
+    """One request whose block table is the identity: the dense oracle on the
+    cache read as one row per position."""
+    c = mi.indexer_paged_case(81, 1, 4, 200, 200, h_idx=8, d_idx=32, topk=40, spare_pages=0, poison=False)
+    bt = torch.arange(c.block_table.shape[1], dtype=torch.int32)[None]
+    got = ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, bt, c.cache_seqlens, 40, c.page)
+    k_lin = c.k_cache.reshape(-1, c.k_cache.shape[-1])[:200]
+    ref = ido.dsa_indices(c.q_idx[0], k_lin, c.weights[0], 40)
+    np.testing.assert_array_equal(got, ref)
+
+
+def pin_paged_matches_packed_on_linearised_keys():
+    c = _paged(82)
+    b_n, s_next = c.q_idx.shape[0], c.q_idx.shape[1]
+    lens = [int(x) for x in c.cache_seqlens]
+    keys = torch.cat([torch.from_numpy(ido.linearise_keys(c.k_cache, c.block_table[b], lens[b], c.page))
+                      for b in range(b_n)])
+    cq = torch.arange(0, (b_n + 1) * s_next, s_next, dtype=torch.int32)
+    ck = torch.tensor([0] + np.cumsum(lens).tolist(), dtype=torch.int32)
+    ref = ido.dsa_indices_varlen(c.q_idx.reshape(b_n * s_next, *c.q_idx.shape[2:]), keys,
+                                 c.weights.reshape(b_n * s_next, -1), cq, ck, 48)
+    got = ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, c.block_table, c.cache_seqlens, 48, c.page)
+    np.testing.assert_array_equal(got, ref)
+
+
+def pin_paged_page_shuffle_invariance():
+    c = _paged(83)
+    perm = torch.randperm(c.k_cache.shape[0], generator=mi._gen(84))
+    k2 = torch.empty_like(c.k_cache)
+    k2[perm] = c.k_cache                      # physical page x moves to perm[x]
+    bt2 = perm[c.block_table.long()].to(torch.int32)
+    a = ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, c.block_table, c.cache_seqlens, 48, c.page)
+    b = ido.dsa_indices_paged(c.q_idx, k2, c.weights, bt2, c.cache_seqlens, 48, c.page)
+    np.testing.assert_array_equal(a, b)
+
+
+def pin_paged_unused_slots_never_read():
+    """NaN in every slot past a request's length and in the spare pages gives
+    the lists of the same cache with finite values there."""
+    a = _paged(85, poison=True)
+    b = _paged(85, poison=False)
+    la = ido.dsa_indices_paged(a.q_idx, a.k_cache, a.weights, a.block_table, a.cache_seqlens, 48, a.page)
+    lb = ido.dsa_indices_paged(b.q_idx, b.k_cache, b.weights, b.block_table, b.cache_seqlens, 48, b.page)
+    np.testing.assert_array_equal(la, lb)
+    assert (la >= 0).sum() > 0
+
+
 PINS = [pin_worked_example_scores, pin_worked_example_lists, pin_relu_floor,
         pin_weight_homogeneity_additivity, pin_selection_properties_with_ties,
         pin_selection_matches_torch_topk, pin_visibility_closed_forms,
         pin_scores_selection_consistent, pin_varlen_matches_dense_per_sequence,
-        pin_short_rows_reproduce_causal_forward]
+        pin_short_rows_reproduce_causal_forward, pin_paged_identity_table_is_dense,
+        pin_paged_matches_packed_on_linearised_keys, pin_paged_page_shuffle_invariance,
+        pin_paged_unused_slots_never_read]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -205,7 +258,18 @@ def test_indexer_pin(pin):
 # planted mistakes
 # ---------------------------------------------------------------------------
 
-_TS, _SEL, _VIS = ido.token_scores, ido.select_topk, ido.visible_len
+_TS, _SEL, _VIS, _LIN = ido.token_scores, ido.select_topk, ido.visible_len, ido.linearise_keys
+
+
+def _lin_ignores_table(k_cache, block_table, seqlen, page):
+    kc = ido._f64(k_cache)
+    return np.stack([kc[s // page, s % page] for s in range(seqlen)])
+
+
+def _lin_table_by_offset(k_cache, block_table, seqlen, page):
+    kc = ido._f64(k_cache)
+    bt = [int(x) for x in block_table]
+    return np.stack([kc[bt[(s % page) % len(bt)], s // page % page] for s in range(seqlen)])
 
 
 def _ts_no_relu(q_t, w_t, k):
@@ -274,6 +338,7 @@ MUTANTS = [("token_scores", _ts_no_relu), ("token_scores", _ts_relu_after_weight
            ("token_scores", _ts_head_transposed), ("select_topk", _sel_ties_to_larger),
            ("select_topk", _sel_smallest), ("select_topk", _sel_unsorted),
            ("identity_list", _short_pad_zero), ("identity_list", _short_from_one),
+           ("linearise_keys", _lin_ignores_table), ("linearise_keys", _lin_table_by_offset),
            ("visible_len", _vis_off_by_one),
            ("visible_len", _vis_top_left)]
 

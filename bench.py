@@ -61,8 +61,9 @@ def parse_args():
                     help="time the indices-free causal entry point on the q/kv of a dense prefill config (1-3); "
                          "FLOPs and bytes then count every causal position")
     ap.add_argument("--indexer", action="store_true",
-                    help="time the DSA indexer + top-k (dsa_indexer_topk) that produces the index lists, on "
-                         "the token shape of config 1-4 with 64 indexer heads of width 128; FLOPs "
+                    help="time the DSA indexer + top-k (dsa_indexer_topk; config 5: dsa_indexer_topk_paged) that "
+                         "produces the index lists, on the token shape of config 1-5 with 64 indexer heads of "
+                         "width 128; FLOPs "
                          "2*64*128 per scored (row, visible position)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="profiling aid for the dense prefill configs (1-3): s_q = s_kv = TOKENS with the "
@@ -670,12 +671,20 @@ def indexer_workload(config: int):
         return mi.indexer_case(seed, 8192, 8192)
     if config == 4:
         return mi.indexer_varlen_case(seed, mi.VARLEN_C4, mi.VARLEN_C4)
-    raise SystemExit("--indexer: configs 1-4 (prefill shapes)")
+    # decode: 16 requests x 6 MTP rows over a paged key cache, contexts U[4096, 32768]
+    return mi.indexer_paged_case(seed, 16, 6, 4096, 32768)
 
 
 def indexer_rows(case):
     """Per query row: (visible length, scored?)."""
-    from itertools import accumulate
+    if hasattr(case, "k_cache"):
+        s_next = case.q_idx.shape[1]
+        out = []
+        for lk in case.cache_seqlens.tolist():
+            for t in range(s_next):
+                v = max(0, min(lk, t + lk - s_next + 1))
+                out.append((v, v > case.topk))
+        return out
     s_q, s_kv = case.q_idx.shape[0], case.k_idx.shape[0]
     if case.cu_seqlens_q is None:
         seqs = [(0, s_q, s_kv)]
@@ -701,7 +710,10 @@ def _idx_oracle_worker(rows):
     from oracle import dsa_indexer_oracle as ido
     c = _W_IDX
     t0 = time.perf_counter()
-    if rows:
+    if rows and hasattr(c, "k_cache"):
+        ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, c.block_table, c.cache_seqlens, c.topk, c.page,
+                              rows=rows)
+    elif rows:
         if c.cu_seqlens_q is None:
             ido.dsa_indices(c.q_idx, c.k_idx, c.weights, c.topk, rows=rows)
         else:
@@ -740,11 +752,12 @@ def indexer_costs(case, rows_info):
     over scored (row, position) pairs, and the HBM bytes of Q, K and the
     weights of scored rows, the logits written and read back once, and the
     lists written."""
-    h, d = case.q_idx.shape[1], case.q_idx.shape[2]
+    h, d = case.q_idx.shape[-2], case.q_idx.shape[-1]
     scored_pos = sum(v for v, sc in rows_info if sc)
     scored_rows = sum(1 for _, sc in rows_info if sc)
     flops = 2.0 * h * d * scored_pos
-    byts = (scored_rows * h * (d * 2 + 4) + case.k_idx.shape[0] * d * 2 + scored_pos * 4 * 2
+    n_keys = int(case.cache_seqlens.sum()) if hasattr(case, "k_cache") else case.k_idx.shape[0]
+    byts = (scored_rows * h * (d * 2 + 4) + n_keys * d * 2 + scored_pos * 4 * 2
             + len(rows_info) * case.topk * 4)
     return flops, byts, scored_pos, scored_rows
 
@@ -764,29 +777,46 @@ def run_indexer(args, rank, world, dist):
     case = indexer_workload(args.config)
     info = indexer_rows(case)
     flops, byts, scored_pos, scored_rows = indexer_costs(case, info)
-    total_q, total_kv = case.q_idx.shape[0], case.k_idx.shape[0]
-    longest = case.max_seqlen_kv
+    paged = hasattr(case, "k_cache")
     stream = torch.cuda.current_stream(dev)
-    inputs = {"q": case.q_idx.to(dev), "k": case.k_idx.to(dev), "w": case.weights.to(dev)}
-    if case.cu_seqlens_q is not None:
-        inputs.update(cq=case.cu_seqlens_q.to(dev), ck=case.cu_seqlens_kv.to(dev))
+    if paged:
+        total_q = case.q_idx.shape[0] * case.q_idx.shape[1]
+        total_kv = int(case.cache_seqlens.sum())
+        longest = int(case.cache_seqlens.max())
+        inputs = {"q": case.q_idx.to(dev), "k": case.k_cache.to(dev), "w": case.weights.to(dev),
+                  "bt": case.block_table.to(dev), "sl": case.cache_seqlens.to(dev)}
+    else:
+        total_q, total_kv = case.q_idx.shape[0], case.k_idx.shape[0]
+        longest = case.max_seqlen_kv
+        inputs = {"q": case.q_idx.to(dev), "k": case.k_idx.to(dev), "w": case.weights.to(dev)}
+        if case.cu_seqlens_q is not None:
+            inputs.update(cq=case.cu_seqlens_q.to(dev), ck=case.cu_seqlens_kv.to(dev))
     need = smla.dsa_indexer_workspace_size(total_q, longest, case.topk)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)     # one chunk: every row's logits
     idx = torch.empty((total_q, case.topk), dtype=torch.int32, device=dev)
     stride = (longest + 3) // 4 * 4
     logits = ws[:max(need, 16)].view(torch.float32)[:max(need, 16) // 4]
-    first = 0 if case.cu_seqlens_q is not None else max(0, min(total_q, case.topk - (total_kv - total_q)))
+    first = 0 if paged or case.cu_seqlens_q is not None else max(0, min(total_q, case.topk - (total_kv - total_q)))
 
     def call(inp):
-        smla.dsa_indexer_topk(inp["q"], inp["k"], inp["w"], case.topk, inp.get("cq"), inp.get("ck"), longest,
-                              workspace=ws, indices=idx, stream=stream)
+        if paged:
+            smla.dsa_indexer_topk_paged(inp["q"], inp["k"], inp["w"], inp["bt"], inp["sl"], case.topk, longest,
+                                        workspace=ws, indices=idx.view(inp["q"].shape[0], -1, case.topk),
+                                        stream=stream)
+        else:
+            smla.dsa_indexer_topk(inp["q"], inp["k"], inp["w"], case.topk, inp.get("cq"), inp.get("ck"), longest,
+                                  workspace=ws, indices=idx, stream=stream)
 
     def scores_only(inp):
         # the launch dsa_indexer_topk makes for the scores of its one chunk
-        smla.dsa_indexer_scores(inp["q"], inp["k"], inp["w"], inp.get("cq"), inp.get("ck"), row0=first,
-                                n_rows=total_q - first, skip_len=case.topk,
-                                scores=logits[:(total_q - first) * stride].view(total_q - first, stride),
-                                max_seqlen_kv=longest, stream=stream)
+        view = logits[:(total_q - first) * stride].view(total_q - first, stride)
+        if paged:
+            smla.dsa_indexer_scores_paged(inp["q"], inp["k"], inp["w"], inp["bt"], inp["sl"], longest, row0=0,
+                                          n_rows=total_q, skip_len=case.topk, scores=view, stream=stream)
+        else:
+            smla.dsa_indexer_scores(inp["q"], inp["k"], inp["w"], inp.get("cq"), inp.get("ck"), row0=first,
+                                    n_rows=total_q - first, skip_len=case.topk, scores=view,
+                                    max_seqlen_kv=longest, stream=stream)
 
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -854,7 +884,7 @@ def run_indexer(args, rank, world, dist):
     if sc_times:
         sc_ms = statistics.mean(sc_times)
         sc_flops = flops
-        sc_bytes = scored_rows * case.q_idx.shape[1] * (case.q_idx.shape[2] * 2 + 4) + total_kv * 256 + scored_pos * 4
+        sc_bytes = scored_rows * case.q_idx.shape[-2] * (case.q_idx.shape[-1] * 2 + 4) + total_kv * 256 + scored_pos * 4
         if sc_flops / (p_tf * 1e12) >= sc_bytes / (p_bw * 1e9):
             ach = sc_flops / (sc_ms * 1e-3) / 1e12
             roofline = {"bound": "tensor", "achieved": ach, "peak": p_tf, "unit": "TFLOP/s", "frac": ach / p_tf,
@@ -874,7 +904,8 @@ def run_indexer(args, rank, world, dist):
                "kind": "oracle", "sample": sample, "seconds": wall}
         pool.close()
     name = {1: "tiny prefill s_q=s_kv=64", 2: "mid prefill s_q=s_kv=2119", 3: "prefill s_q=s_kv=8192",
-            4: "packed varlen prefill 16384 tokens (8192,4096,2048,1024,1024)"}[args.config]
+            4: "packed varlen prefill 16384 tokens (8192,4096,2048,1024,1024)",
+            5: "paged decode 16 requests x 6 MTP rows, contexts U[4096,32768], page 64"}[args.config]
     launches = 2 if scored_rows else 1
     line = {
         "metric": "DSA indexer scores + top-k TFLOP/s at topk=2048 (2*h_idx*d_idx per scored position)",

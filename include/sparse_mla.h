@@ -314,6 +314,34 @@ sparse_mla_status_t dsa_indexer_topk(const void* q_idx, const void* k_idx, const
                                      int total_q, int total_kv, int max_seqlen_kv, int h_idx, int d_idx, int topk,
                                      int32_t* indices, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Decode form of the indexer over a paged key cache.  Request b has s_next
+ * query rows, the last s_next of its cache_seqlens[b] positions (MTP token
+ * j sits at position L_b - s_next + j and sees positions 0 .. L_b - s_next
+ * + j, the convention of sparse_mla_decode); its keys live in
+ *   k_cache       bf16 [num_blocks, page_size, d_idx]   16-byte aligned
+ * position s of request b at row s % page_size of page
+ * block_table[b * max_blocks + s / page_size] (int32 [batch, max_blocks]);
+ * cache_seqlens int32 [batch].  q_idx bf16 [batch, s_next, h_idx, d_idx],
+ * weights fp32 [batch, s_next, h_idx]; rows are numbered b * s_next + j.
+ * page_size must be 64 (else SPARSE_MLA_ERR_UNSUPPORTED_SHAPE).  Pages past a
+ * request's length are never used in a score; a page id outside
+ * [0, num_blocks) reads as zeros.  Otherwise as dsa_indexer_scores /
+ * dsa_indexer_topk (row_stride / max_seqlen_kv: at least the longest
+ * cache_seqlens).
+ */
+sparse_mla_status_t dsa_indexer_scores_paged(const void* q_idx, const void* k_cache, const float* weights,
+                                             const int32_t* block_table, const int32_t* cache_seqlens, int batch,
+                                             int s_next, int h_idx, int d_idx, int page_size, int max_blocks,
+                                             int num_blocks, int row0, int n_rows, int skip_len, float* scores,
+                                             long long row_stride, void* stream);
+
+sparse_mla_status_t dsa_indexer_topk_paged(const void* q_idx, const void* k_cache, const float* weights,
+                                           const int32_t* block_table, const int32_t* cache_seqlens, int batch,
+                                           int s_next, int h_idx, int d_idx, int page_size, int max_blocks,
+                                           int num_blocks, int max_seqlen_kv, int topk, int32_t* indices,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* sparse_mla_status_string(sparse_mla_status_t status);
 

@@ -6,7 +6,9 @@ from .binding import (  # noqa: F401
     clear_device_error,
     decode_workspace_size,
     dsa_indexer_scores,
+    dsa_indexer_scores_paged,
     dsa_indexer_topk,
+    dsa_indexer_topk_paged,
     dsa_indexer_workspace_size,
     dsa_topk,
     get_device_error,

@@ -51,6 +51,12 @@ SIGNATURES = {
     "dsa_indexer_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "dsa_indexer_topk": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                  c_int, c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "dsa_indexer_scores_paged": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                         c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p,
+                                         ctypes.c_longlong, c_void_p]),
+    "dsa_indexer_topk_paged": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                       c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_size_t,
+                                       c_void_p]),
     "sparse_mla_status_string": (ctypes.c_char_p, [c_int]),
     "sparse_mla_get_device_error": (c_int, [ctypes.POINTER(c_int)]),
     "sparse_mla_clear_device_error": (c_int, []),
@@ -361,6 +367,64 @@ def dsa_indexer_topk(q_idx, k_idx, weights, topk: int, cu_seqlens_q=None, cu_seq
                               batch, total_q, total_kv, longest, h_idx, d_idx, topk, _ptr(indices),
                               _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "dsa_indexer_topk")
+    return indices
+
+
+def _paged_args(q_idx, k_cache, weights, block_table, cache_seqlens):
+    _need(q_idx, torch.bfloat16, "q_idx")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(weights, torch.float32, "weights")
+    _need(block_table, torch.int32, "block_table")
+    _need(cache_seqlens, torch.int32, "cache_seqlens")
+    batch, s_next, h_idx, d_idx = q_idx.shape
+    num_blocks, page = k_cache.shape[0], k_cache.shape[1]
+    return batch, s_next, h_idx, d_idx, page, block_table.shape[1], num_blocks
+
+
+def dsa_indexer_scores_paged(q_idx, k_cache, weights, block_table, cache_seqlens, max_seqlen_kv: int,
+                             row0: int = 0, n_rows: Optional[int] = None, skip_len: int = 0, scores=None,
+                             stream=None):
+    """Decode indexer scores over a paged key cache: q_idx [b,s_next,h_idx,128],
+    k_cache [num_blocks,64,128], weights [b,s_next,h_idx], block_table
+    [b,max_blocks], cache_seqlens [b] -> scores [n_rows, row_stride] fp32 over
+    the flattened rows b*s_next + j (-inf where not written)."""
+    lib = load()
+    batch, s_next, h_idx, d_idx, page, max_blocks, num_blocks = _paged_args(q_idx, k_cache, weights, block_table,
+                                                                            cache_seqlens)
+    n_rows = batch * s_next - row0 if n_rows is None else n_rows
+    stride = (int(max_seqlen_kv) + 3) // 4 * 4
+    if scores is None:
+        scores = torch.full((n_rows, max(stride, 4)), float("-inf"), dtype=torch.float32, device=q_idx.device)
+    st = lib.dsa_indexer_scores_paged(_ptr(q_idx), _ptr(k_cache), _ptr(weights), _ptr(block_table),
+                                      _ptr(cache_seqlens), batch, s_next, h_idx, d_idx, page, max_blocks, num_blocks,
+                                      row0, n_rows, skip_len, _ptr(scores), scores.shape[-1], _stream(stream))
+    _check(st, "dsa_indexer_scores_paged")
+    return scores
+
+
+def dsa_indexer_topk_paged(q_idx, k_cache, weights, block_table, cache_seqlens, topk: int,
+                           max_seqlen_kv: Optional[int] = None, workspace: Optional[torch.Tensor] = None,
+                           indices=None, stream=None):
+    """Decode index lists [b, s_next, topk] int32 over a paged key cache
+    (positions local to each request)."""
+    lib = load()
+    batch, s_next, h_idx, d_idx, page, max_blocks, num_blocks = _paged_args(q_idx, k_cache, weights, block_table,
+                                                                            cache_seqlens)
+    if max_seqlen_kv is None:
+        max_seqlen_kv = int(cache_seqlens.max().item()) if cache_seqlens.numel() else 0   # a device read
+    if indices is None:
+        indices = torch.empty((batch, s_next, topk), dtype=torch.int32, device=q_idx.device)
+    else:
+        _need(indices, torch.int32, "indices")
+    if workspace is None:
+        need = lib.dsa_indexer_workspace_size(batch * s_next, int(max_seqlen_kv), topk)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_idx.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.dsa_indexer_topk_paged(_ptr(q_idx), _ptr(k_cache), _ptr(weights), _ptr(block_table),
+                                    _ptr(cache_seqlens), batch, s_next, h_idx, d_idx, page, max_blocks, num_blocks,
+                                    int(max_seqlen_kv), topk, _ptr(indices), _ptr(workspace), ws_bytes,
+                                    _stream(stream))
+    _check(st, "dsa_indexer_topk_paged")
     return indices
 
 

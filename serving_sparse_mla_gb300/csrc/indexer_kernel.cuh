@@ -10,7 +10,9 @@
 //   I[t,s] = sum_j w[t,j] * relu(q[t,j,:] . k[s,:])       (j < H_I, width 128)
 //
 // over the positions s query t may see (the s_q queries of a sequence are
-// the last s_q of its s_kv positions).  A row's list holds the topk visible
+// the last s_q of its s_kv positions; for a paged decode cache, the s_next
+// MTP rows of a request are its last s_next positions and its keys are read
+// page by page through the block table).  A row's list holds the topk visible
 // positions of largest score, equal scores ranked by position (smaller
 // first), written in increasing position order and padded with -1; a row
 // that sees at most topk positions takes all of them and is never scored.
@@ -18,7 +20,8 @@
 // dsa_scores_kernel<H_I>: a dense contraction, so it runs on the tensor
 // cores.  A work item is a group of G = 256 / H_I consecutive query rows
 // (N = 256 columns: every head of every row) against up to 32 tiles of 128
-// positions of their sequence (M = 128):
+// positions of their sequence (M = 128; fewer per item when a launch has
+// few groups, so that every SM gets several items):
 //
 //   S^T[128 x 256] = K_tile[128 x 128] . Q_group^T[128 x 256]    (fp32, TMEM)
 //
@@ -63,7 +66,7 @@ namespace smla {
 constexpr int kIdxD = 128;            // indexer head width
 constexpr int kIdxTile = 128;         // positions per K tile (the MMA's M)
 constexpr int kIdxN = 256;            // (row, head) columns of a group (the MMA's N)
-constexpr int kIdxChunkTiles = 32;    // tiles per item: 4096 positions
+constexpr int kIdxChunkTiles = 32;    // most tiles per item (4096 positions); a launch may take fewer
 constexpr int kIdxStages = 4;
 constexpr int kIdxMaxBatch = 2048;    // sequences whose offsets sit in shared memory
 constexpr int kIdxEpiWarp0 = 2;
@@ -85,6 +88,7 @@ struct __align__(16) IdxMisc {
   uint32_t tmem_base;
   int abort_flag;
   int prior_error;
+  int32_t pages[2 * kIdxChunkTiles];   // paged cache: the producer's current segment's page ids
 };
 
 constexpr int idx_smem_bytes() { return kIdxMiscOff + static_cast<int>(sizeof(IdxMisc)) + 1024; }
@@ -98,19 +102,25 @@ enum IdxErrCode : int {
   kErrIdxRowTooLong = 0x611,   // a sequence sees more positions than a logits row holds
 };
 
+constexpr int kIdxPage = 64;          // positions per page of a paged key cache
+
 struct IdxParams {
   CUtensorMap map_q;          // bf16 [total_q * h_idx, 128]: box {64, 256}, 128B swizzle
-  CUtensorMap map_k;          // bf16 [total_kv, 128]: box {64, 128}, 128B swizzle
+  CUtensorMap map_k;          // bf16 [total_kv, 128]: box {64, 128}, 128B swizzle (paged: box {64, 64})
   const float* weights;       // [total_q, h_idx]
-  const int32_t* cu_q;        // [batch + 1], null for one dense sequence
+  const int32_t* cu_q;        // [batch + 1], null for one dense sequence or a paged cache
   const int32_t* cu_kv;
+  const int32_t* block_table; // paged cache: [batch, max_blocks] pages of kIdxPage positions, else null
+  const int32_t* seqlens;     // paged cache: [batch] positions per request
+  int s_next, max_blocks, num_blocks;   // paged cache: query rows per request (the last s_next positions)
   float* scores;              // [n_rows, row_stride]: row r - row0 holds row r's positions
   long long row_stride;
   int total_q, total_kv, batch, h_idx;
   int row0, n_rows;           // the query rows of this launch
   int skip_len;               // rows seeing <= skip_len positions are not scored
   int groups;                 // ceil(n_rows / G)
-  int kv_chunks;              // ceil(longest KV sequence / 4096)
+  int kv_chunks;              // ceil(longest KV sequence / (128 chunk_tiles))
+  int chunk_tiles;            // tiles per item, at most kIdxChunkTiles
   unsigned long long timeout_ns;
 };
 
@@ -136,6 +146,11 @@ __device__ __forceinline__ void ffma2(float& c0, float& c1, float a0, float a1, 
       "mov.b64 {%0, %1}, pc;\n\t}"
       : "+f"(c0), "+f"(c1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// 4-byte asynchronous copy global -> shared (zero-filled when src_bytes is 0).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
 // Positions row r of sequence b sees: the sequence's queries are the last
@@ -192,10 +207,10 @@ struct IdxWalk {
         s.kv_begin = ck[b];
         long long v = idx_visible(cq, ck, b, e - 1);   // the segment's longest row
         if (v > p.row_stride) v = p.row_stride;
-        s.t0 = s.t1 = c * kIdxChunkTiles;
+        s.t0 = s.t1 = c * p.chunk_tiles;
         if (v > p.skip_len) {
           const int nt = static_cast<int>((v + kIdxTile - 1) / kIdxTile);
-          s.t1 = nt < s.t0 + kIdxChunkTiles ? nt : s.t0 + kIdxChunkTiles;
+          s.t1 = nt < s.t0 + p.chunk_tiles ? nt : s.t0 + p.chunk_tiles;
           if (s.t1 < s.t0) s.t1 = s.t0;
         }
         r = e;
@@ -222,6 +237,17 @@ __device__ __forceinline__ bool idx_producer(const IdxParams& p, IdxMisc& m, uin
     IdxSeg s;
     bool first = true;
     while (w.next(p, cq, ck, s)) {
+      if (p.block_table != nullptr && s.t1 > s.t0) {
+        // The segment's page ids, all in flight at once (one round trip
+        // rather than one per tile); ids past the table read as -1.
+        const int32_t* bt = p.block_table + static_cast<size_t>(s.b) * p.max_blocks;
+        const int lp0 = 2 * s.t0, npg = 2 * (s.t1 - s.t0);
+        for (int i = 0; i < npg; ++i) {
+          if (lp0 + i < p.max_blocks) cp_async_4(smem_u32(&m.pages[i]), bt + lp0 + i, 4u);
+          else m.pages[i] = -1;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+      }
       for (int t = s.t0; t < s.t1; ++t) {
         if (first) {
           first = false;
@@ -253,10 +279,23 @@ __device__ __forceinline__ bool idx_producer(const IdxParams& p, IdxMisc& m, uin
         const uint32_t slot = kcount % kIdxStages;
         if (!mbar_wait(smem_u32(&m.k_empty[slot]), ((kcount / kIdxStages) & 1u) ^ 1u, deadline, ab)) return false;
         mbar_arrive_expect_tx(smem_u32(&m.k_full[slot]), kIdxKStage);
-        const int y = s.kv_begin + t * kIdxTile;
         const uint32_t dst = sb + kIdxKOff + slot * kIdxKStage;
-        tma_load_2d(dst, &p.map_k, 0, y, smem_u32(&m.k_full[slot]));
-        tma_load_2d(dst + kIdxKHalf, &p.map_k, 64, y, smem_u32(&m.k_full[slot]));
+        if (p.block_table == nullptr) {
+          const int y = s.kv_begin + t * kIdxTile;
+          tma_load_2d(dst, &p.map_k, 0, y, smem_u32(&m.k_full[slot]));
+          tma_load_2d(dst + kIdxKHalf, &p.map_k, 64, y, smem_u32(&m.k_full[slot]));
+        } else {
+          // Two pages per tile, each a 64-row box per column half; a page id
+          // outside the table or the pool reads as zeros.
+#pragma unroll
+          for (int pg = 0; pg < 2; ++pg) {
+            const int blk = m.pages[2 * (t - s.t0) + pg];
+            const int y = blk >= 0 && blk < p.num_blocks ? blk * kIdxPage : -kIdxPage;
+            const uint32_t d = dst + static_cast<uint32_t>(pg * kIdxPage * 128);
+            tma_load_2d(d, &p.map_k, 0, y, smem_u32(&m.k_full[slot]));
+            tma_load_2d(d + kIdxKHalf, &p.map_k, 64, y, smem_u32(&m.k_full[slot]));
+          }
+        }
         ++kcount;
       }
     }
@@ -450,7 +489,29 @@ __global__ void __launch_bounds__(kIdxThreads, 1) dsa_scores_kernel(const __grid
   const int lane = static_cast<int>(lane_id());
   const uint32_t sb = smem_u32(sbase);
 
-  if (p.cu_q != nullptr) {
+  if (p.block_table != nullptr) {
+    // Paged cache: request b owns query rows [b s_next, (b + 1) s_next) and
+    // seqlens[b] positions; ck holds their prefix sums, so that every
+    // visibility rule reads lengths as for packed sequences.
+    for (int i = static_cast<int>(threadIdx.x); i <= p.batch; i += kIdxThreads) cq[i] = i * p.s_next;
+    if (warp == 0) {
+      int base = 0;
+      if (lane == 0) ck[0] = 0;
+      for (int i0 = 0; i0 < p.batch; i0 += 32) {
+        const int i = i0 + lane;
+        int v = i < p.batch ? p.seqlens[i] : 0;
+        v = v < 0 ? 0 : v;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (i < p.batch) ck[i + 1] = base + incl;
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+  } else if (p.cu_q != nullptr) {
     for (int i = static_cast<int>(threadIdx.x); i <= p.batch; i += kIdxThreads) {
       cq[i] = p.cu_q[i];
       ck[i] = p.cu_kv[i];
@@ -528,15 +589,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1) dsa_scores_kernel(const __grid
 
 // ------------------------------------------------------------------ top-k
 
-constexpr int kTopkThreads = 256;
-constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkMaxWarps = 32;   // CTAs of 256 threads, or 1024 for long rows
 constexpr int kTopkBins = 2048;
 
 struct TopkParams {
   const float* scores;        // [n_rows, row_stride]
   int32_t* indices;           // [total_q, topk]: rows row0 .. row0 + n_rows - 1 are written
-  const int32_t* cu_q;        // [batch + 1], null for one dense sequence
+  const int32_t* cu_q;        // [batch + 1], null for one dense sequence or a paged cache
   const int32_t* cu_kv;
+  const int32_t* seqlens;     // paged cache: [batch] positions per request, else null
+  int s_next;                 // paged cache: query rows per request
   long long row_stride;
   int total_q, total_kv, batch;
   int row0, n_rows, topk;
@@ -552,8 +614,8 @@ __device__ __forceinline__ uint32_t topk_key(float f) {
 
 // Shared state of one row's selection.
 struct TopkShared {
-  int scan[kTopkWarps];
-  int scan2[kTopkWarps];
+  int scan[kTopkMaxWarps];
+  int scan2[kTopkMaxWarps];
   int seq, krem;
   uint32_t bin;
 };
@@ -562,9 +624,10 @@ struct TopkShared {
 // the class's krem-th largest key, and krem's rank inside it.  Thread t
 // owns bins [t per, t per + per); the counts above come from a suffix scan.
 // Ends with the block synchronised and sh.bin / sh.krem set.
+template <int T>
 __device__ __forceinline__ void topk_find_bin(const uint32_t* hist, int nbins, int krem, TopkShared& sh) {
   const int tid = static_cast<int>(threadIdx.x), lane = static_cast<int>(lane_id()), w = tid >> 5;
-  const int per = nbins / kTopkThreads;
+  const int per = nbins / T;
   int own = 0;
   for (int i = 0; i < per; ++i) own += static_cast<int>(hist[tid * per + i]);
   int incl = own;   // over this lane and the lanes above it
@@ -577,7 +640,7 @@ __device__ __forceinline__ void topk_find_bin(const uint32_t* hist, int nbins, i
   __syncthreads();
   int above = incl - own;
 #pragma unroll
-  for (int i = 0; i < kTopkWarps; ++i) above += i > w ? sh.scan[i] : 0;
+  for (int i = 0; i < (T / 32); ++i) above += i > w ? sh.scan[i] : 0;
   if (above < krem && krem <= above + own) {
     int acc = above;
     for (int i = per - 1; i >= 0; --i) {
@@ -612,6 +675,7 @@ __device__ __forceinline__ uint4 topk_keys4(const uint32_t* keys, const float* r
 
 // Exclusive prefix over the block (in thread order) of two per-thread
 // counts.  Ends with the block synchronised.
+template <int T>
 __device__ __forceinline__ void topk_block_scan2(int a, int b, TopkShared& sh, int& a_ex, int& b_ex) {
   const int lane = static_cast<int>(lane_id()), w = static_cast<int>(threadIdx.x >> 5);
   int ai = a, bi = b;
@@ -631,7 +695,7 @@ __device__ __forceinline__ void topk_block_scan2(int a, int b, TopkShared& sh, i
   __syncthreads();
   int wa = 0, wb = 0;
 #pragma unroll
-  for (int i = 0; i < kTopkWarps; ++i) {
+  for (int i = 0; i < (T / 32); ++i) {
     wa += i < w ? sh.scan[i] : 0;
     wb += i < w ? sh.scan2[i] : 0;
   }
@@ -642,7 +706,7 @@ __device__ __forceinline__ void topk_block_scan2(int a, int b, TopkShared& sh, i
 
 // Selection of one row of n > topk positions (keys staged in shared memory
 // or read from the row in global memory on every pass).
-template <bool kStaged>
+template <int T, bool kStaged>
 __device__ __forceinline__ void topk_select(const float* row, int n, int topk, int32_t* out, uint32_t* hist,
                                             const uint32_t* keys, TopkShared& sh) {
   const int tid = static_cast<int>(threadIdx.x);
@@ -655,10 +719,10 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
     const int shift = d == 0 ? 21 : (d == 1 ? 10 : 0);
     const uint32_t bmask = d == 2 ? 1023u : 2047u;
     if (d > 0) {
-      for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0;
+      for (int i = tid; i < kTopkBins; i += T) hist[i] = 0;
       __syncthreads();
     }
-    for (int q = tid; q < nq; q += kTopkThreads) {
+    for (int q = tid; q < nq; q += T) {
       const uint4 k = topk_keys4<kStaged>(keys, row, q, n);
       const int s = 4 * q;
       if ((k.x & pmask) == prefix) atomicAdd(&hist[(k.x >> shift) & bmask], 1u);
@@ -667,7 +731,7 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
       if (s + 3 < n && (k.w & pmask) == prefix) atomicAdd(&hist[(k.w >> shift) & bmask], 1u);
     }
     __syncthreads();
-    topk_find_bin(hist, static_cast<int>(bmask) + 1, krem, sh);
+    topk_find_bin<T>(hist, static_cast<int>(bmask) + 1, krem, sh);
     prefix |= sh.bin << shift;
     pmask |= bmask << shift;
     krem = sh.krem;
@@ -681,7 +745,7 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
   // odd (so the 16-byte reads of eight consecutive threads hit distinct
   // banks): it counts both kinds, one block scan gives the counts before
   // its run, and a second walk writes its picks in order.
-  const int QL = ((nq + kTopkThreads - 1) / kTopkThreads) | 1;
+  const int QL = ((nq + T - 1) / T) | 1;
   const int q0 = tid * QL < nq ? tid * QL : nq, q1 = q0 + QL < nq ? q0 + QL : nq;
   int gt = 0, eq = 0;
   for (int q = q0; q < q1; ++q) {
@@ -693,7 +757,7 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
           (s + 3 < n && h3 == prefix);
   }
   int gt_ex, eq_ex;
-  topk_block_scan2(gt, eq, sh, gt_ex, eq_ex);
+  topk_block_scan2<T>(gt, eq, sh, gt_ex, eq_ex);
   int pos = gt_ex + (eq_ex < krem ? eq_ex : krem);
   int eq_seen = eq_ex;
   for (int q = q0; q < q1; ++q) {
@@ -713,7 +777,8 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
   }
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 4) dsa_topk_kernel(const __grid_constant__ TopkParams p) {
+template <int T>
+__global__ void __launch_bounds__(T, T == 256 ? 4 : 1) dsa_topk_kernel(const __grid_constant__ TopkParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);      // [kTopkBins]
   uint32_t* keys = hist + kTopkBins;                           // [stage_cap]
@@ -725,14 +790,19 @@ __global__ void __launch_bounds__(kTopkThreads, 4) dsa_topk_kernel(const __grid_
   if (tid == 0) sh.seq = p.cu_q == nullptr ? 0 : -1;
   __syncthreads();
   if (p.cu_q != nullptr) {
-    for (int i = tid; i < p.batch; i += kTopkThreads)
+    for (int i = tid; i < p.batch; i += T)
       if (p.cu_q[i] <= r && r < p.cu_q[i + 1]) sh.seq = i;
   }
-  for (int i = tid; i < kTopkBins; i += kTopkThreads) hist[i] = 0;
+  for (int i = tid; i < kTopkBins; i += T) hist[i] = 0;
   __syncthreads();
   const int b = sh.seq;
   long long v = 0;
-  if (b >= 0) {
+  if (p.seqlens != nullptr) {   // paged cache: request r / s_next, its last s_next positions are the rows
+    const int rb = r / p.s_next;
+    const int lk = p.seqlens[rb];
+    int cq2[2] = {rb * p.s_next, (rb + 1) * p.s_next}, ck2[2] = {0, lk < 0 ? 0 : lk};
+    v = idx_visible(cq2, ck2, 0, r);
+  } else if (b >= 0) {
     int cq2[2] = {0, p.total_q}, ck2[2] = {0, p.total_kv};
     if (p.cu_q != nullptr) {
       cq2[0] = p.cu_q[b];
@@ -748,7 +818,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) dsa_topk_kernel(const __grid_
     v = p.topk;
   }
   if (v <= p.topk) {
-    for (int i = tid; i < p.topk; i += kTopkThreads) out[i] = i < v ? i : -1;
+    for (int i = tid; i < p.topk; i += T) out[i] = i < v ? i : -1;
     return;
   }
   if (v > p.row_stride) {
@@ -758,7 +828,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) dsa_topk_kernel(const __grid_
   const int n = static_cast<int>(v);
   const float* row = p.scores + static_cast<long long>(blockIdx.x) * p.row_stride;
   if (n > p.stage_cap) {
-    topk_select<false>(row, n, p.topk, out, hist, keys, sh);
+    topk_select<T, false>(row, n, p.topk, out, hist, keys, sh);
     return;
   }
   // Stage the row's keys (16-byte loads, four in flight per thread, when the
@@ -768,25 +838,25 @@ __global__ void __launch_bounds__(kTopkThreads, 4) dsa_topk_kernel(const __grid_
     const float4* r4 = reinterpret_cast<const float4*>(row);
     uint4* k4 = reinterpret_cast<uint4*>(keys);
     const int full = n >> 2;
-    for (int base = 0; base < full; base += 4 * kTopkThreads) {
+    for (int base = 0; base < full; base += 4 * T) {
       float4 t[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int i = base + u * kTopkThreads + tid;
+        const int i = base + u * T + tid;
         if (i < full) t[u] = __ldg(r4 + i);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int i = base + u * kTopkThreads + tid;
+        const int i = base + u * T + tid;
         if (i < full) k4[i] = make_uint4(topk_key(t[u].x), topk_key(t[u].y), topk_key(t[u].z), topk_key(t[u].w));
       }
     }
-    for (int i = 4 * full + tid; i < 4 * nq; i += kTopkThreads) keys[i] = i < n ? topk_key(row[i]) : 0u;
+    for (int i = 4 * full + tid; i < 4 * nq; i += T) keys[i] = i < n ? topk_key(row[i]) : 0u;
   } else {
-    for (int i = tid; i < 4 * nq; i += kTopkThreads) keys[i] = i < n ? topk_key(row[i]) : 0u;
+    for (int i = tid; i < 4 * nq; i += T) keys[i] = i < n ? topk_key(row[i]) : 0u;
   }
   __syncthreads();
-  topk_select<true>(row, n, p.topk, out, hist, keys, sh);
+  topk_select<T, true>(row, n, p.topk, out, hist, keys, sh);
 }
 
 }  // namespace smla

@@ -35,7 +35,7 @@ DeviceState g_dev[kMaxDevices];
 
 // Top-k kernel: histogram and the staged keys of a row of up to
 // kTopkStageCap positions.
-constexpr int kTopkStageCap = 12288;
+constexpr int kTopkStageCap = 49152;
 constexpr int kTopkMaxSmem = smla::kTopkBins * 4 + kTopkStageCap * 4;
 
 sparse_mla_status_t device_setup(int* sm_count) {
@@ -71,7 +71,9 @@ sparse_mla_status_t device_setup(int* sm_count) {
                              smla::idx_smem_bytes()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::dsa_scores_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::idx_smem_bytes()) != cudaSuccess ||
-        cudaFuncSetAttribute(smla::dsa_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(smla::dsa_topk_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTopkMaxSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::dsa_topk_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kTopkMaxSmem) != cudaSuccess)
       return SPARSE_MLA_ERR_CUDA;
     st.attrs_set = true;
@@ -559,10 +561,20 @@ sparse_mla_status_t check_indexer(const void* q_idx, const void* k_idx, const fl
   return SPARSE_MLA_OK;
 }
 
-sparse_mla_status_t launch_scores(const void* q_idx, const void* k_idx, const float* weights, const int32_t* cu_q,
-                                  const int32_t* cu_kv, int batch, int total_q, int total_kv, int h_idx, int row0,
-                                  int n_rows, int skip_len, float* scores, long long row_stride, int sms,
-                                  cudaStream_t cs) {
+// How a launch's query rows map to key sequences: one dense sequence (all
+// null), packed sequences (cu_q / cu_kv) or a paged decode cache
+// (block_table / seqlens, s_next rows per request).
+struct IdxSeqs {
+  const int32_t* cu_q = nullptr;
+  const int32_t* cu_kv = nullptr;
+  const int32_t* block_table = nullptr;
+  const int32_t* seqlens = nullptr;
+  int batch = 1, s_next = 0, max_blocks = 0, num_blocks = 0;
+};
+
+sparse_mla_status_t launch_scores(const void* q_idx, const void* k_idx, const float* weights, const IdxSeqs& sq,
+                                  int total_q, int total_kv, int h_idx, int row0, int n_rows, int skip_len,
+                                  float* scores, long long row_stride, int sms, cudaStream_t cs) {
   if (n_rows <= 0 || total_kv <= 0) return SPARSE_MLA_OK;
   EncodeTiledFn enc = nullptr;
   sparse_mla_status_t st = get_encode(&enc);
@@ -572,23 +584,36 @@ sparse_mla_status_t launch_scores(const void* q_idx, const void* k_idx, const fl
   if ((st = encode_rows128(enc, &p.map_q, q_idx, static_cast<long long>(total_q) * h_idx, smla::kIdxN)) !=
       SPARSE_MLA_OK)
     return st;
-  if ((st = encode_rows128(enc, &p.map_k, k_idx, total_kv, smla::kIdxTile)) != SPARSE_MLA_OK) return st;
+  const bool paged = sq.block_table != nullptr;
+  if ((st = encode_rows128(enc, &p.map_k, k_idx, total_kv, paged ? smla::kIdxPage : smla::kIdxTile)) != SPARSE_MLA_OK)
+    return st;
   p.weights = weights;
-  p.cu_q = cu_q;
-  p.cu_kv = cu_kv;
+  p.cu_q = sq.cu_q;
+  p.cu_kv = sq.cu_kv;
+  p.block_table = sq.block_table;
+  p.seqlens = sq.seqlens;
+  p.s_next = sq.s_next;
+  p.max_blocks = sq.max_blocks;
+  p.num_blocks = sq.num_blocks;
   p.scores = scores;
   p.row_stride = row_stride;
   p.total_q = total_q;
   p.total_kv = total_kv;
-  p.batch = cu_q ? batch : 1;
+  p.batch = (sq.cu_q || paged) ? sq.batch : 1;
   p.h_idx = h_idx;
   p.row0 = row0;
   p.n_rows = n_rows;
   p.skip_len = skip_len;
   const int G = smla::kIdxN / h_idx;
   p.groups = (n_rows + G - 1) / G;
-  const long long longest = row_stride < total_kv ? row_stride : total_kv;
-  const long long span = static_cast<long long>(smla::kIdxTile) * smla::kIdxChunkTiles;
+  const long long longest = row_stride < total_kv || paged ? row_stride : total_kv;
+  // Tiles per item: about four items per SM over the (at most) groups x
+  // tiles of the launch, between 4 and 32 tiles, a power of two.
+  const long long tiles = static_cast<long long>(p.groups) * ((longest + smla::kIdxTile - 1) / smla::kIdxTile);
+  int ct = smla::kIdxChunkTiles;
+  while (ct > 4 && tiles / ct < 4LL * sms) ct >>= 1;
+  p.chunk_tiles = ct;
+  const long long span = static_cast<long long>(smla::kIdxTile) * ct;
   p.kv_chunks = static_cast<int>((longest + span - 1) / span);
   if (p.kv_chunks < 1) p.kv_chunks = 1;
   unsigned long long t = g_timeout_ns.load();
@@ -604,31 +629,106 @@ sparse_mla_status_t launch_scores(const void* q_idx, const void* k_idx, const fl
   return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
 }
 
-sparse_mla_status_t launch_topk(const float* scores, long long row_stride, const int32_t* cu_q, const int32_t* cu_kv,
-                                int batch, int total_q, int total_kv, int row0, int n_rows, int topk,
-                                int32_t* indices, cudaStream_t cs) {
+sparse_mla_status_t launch_topk(const float* scores, long long row_stride, const IdxSeqs& sq, int total_q,
+                                int total_kv, int row0, int n_rows, int topk, int32_t* indices, cudaStream_t cs) {
   if (n_rows <= 0) return SPARSE_MLA_OK;
   smla::TopkParams p;
   std::memset(&p, 0, sizeof(p));
+  const bool paged = sq.block_table != nullptr;
   p.scores = scores;
   p.indices = indices;
-  p.cu_q = cu_q;
-  p.cu_kv = cu_kv;
+  p.cu_q = paged ? nullptr : sq.cu_q;
+  p.cu_kv = paged ? nullptr : sq.cu_kv;
+  p.seqlens = paged ? sq.seqlens : nullptr;
+  p.s_next = sq.s_next;
   p.row_stride = row_stride;
   p.total_q = total_q;
   p.total_kv = total_kv;
-  p.batch = cu_q ? batch : 1;
+  p.batch = (sq.cu_q || paged) ? sq.batch : 1;
   p.row0 = row0;
   p.n_rows = n_rows;
   p.topk = topk;
-  const long long longest = row_stride < total_kv ? row_stride : total_kv;
+  const long long longest = row_stride < total_kv || paged ? row_stride : total_kv;
   p.stage_cap = static_cast<int>(longest < kTopkStageCap ? (longest + 3) / 4 * 4 : kTopkStageCap);
   const int smem = smla::kTopkBins * 4 + p.stage_cap * 4;
-  smla::dsa_topk_kernel<<<n_rows, smla::kTopkThreads, smem, cs>>>(p);
+  // Rows beyond 8192 positions (decode over long contexts) take CTAs of 1024
+  // threads: few rows, each with more work.
+  if (longest > 8192)
+    smla::dsa_topk_kernel<1024><<<n_rows, 1024, smem, cs>>>(p);
+  else
+    smla::dsa_topk_kernel<256><<<n_rows, 256, smem, cs>>>(p);
   return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
 }
 
 long long idx_row_stride(int max_seqlen_kv) { return (static_cast<long long>(max_seqlen_kv) + 3) / 4 * 4; }
+
+IdxSeqs paged_seqs(const int32_t* block_table, const int32_t* seqlens, int batch, int s_next, int max_blocks,
+                   int num_blocks) {
+  IdxSeqs sq;
+  sq.block_table = block_table;
+  sq.seqlens = seqlens;
+  sq.batch = batch;
+  sq.s_next = s_next;
+  sq.max_blocks = max_blocks;
+  sq.num_blocks = num_blocks;
+  return sq;
+}
+
+sparse_mla_status_t check_paged_indexer(const void* q_idx, const void* k_cache, const float* weights,
+                                        const int32_t* block_table, const int32_t* seqlens, int batch, int s_next,
+                                        int h_idx, int d_idx, int page_size, int max_blocks, int num_blocks) {
+  if (batch < 0 || s_next < 1 || max_blocks < 0 || num_blocks < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (d_idx != smla::kIdxD || !idx_heads_ok(h_idx) || page_size != smla::kIdxPage)
+    return SPARSE_MLA_ERR_UNSUPPORTED_SHAPE;
+  if (batch > smla::kIdxMaxBatch) return SPARSE_MLA_ERR_UNSUPPORTED_SHAPE;
+  const long long total_q = static_cast<long long>(batch) * s_next;
+  if (total_q * h_idx + smla::kIdxN > INT_MAX ||
+      static_cast<long long>(num_blocks) * smla::kIdxPage + smla::kIdxTile * smla::kIdxChunkTiles > INT_MAX)
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  if (batch > 0) {
+    if (!q_idx || !weights || !block_table || !seqlens) return SPARSE_MLA_ERR_INVALID_ARG;
+    if (!aligned(q_idx, 16) || !aligned(weights, 16) || !aligned(block_table, 4) || !aligned(seqlens, 4))
+      return SPARSE_MLA_ERR_INVALID_ARG;
+    if (num_blocks > 0 && (!k_cache || !aligned(k_cache, 16))) return SPARSE_MLA_ERR_INVALID_ARG;
+  }
+  return SPARSE_MLA_OK;
+}
+
+// Scores and lists of every query row, in chunks of rows whose logits fit the
+// workspace (the logits budget); rows before first_long are known to be short.
+sparse_mla_status_t indexer_topk_chunks(const void* q_idx, const void* k_idx, const float* weights, const IdxSeqs& sq,
+                                        int total_q, int total_kv, int max_seqlen_kv, int h_idx, int topk,
+                                        long long first_long, int32_t* indices, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t cs) {
+  if (static_cast<long long>(total_q) * topk > (1LL << 62)) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (total_q > 0 && (!indices || !aligned(indices, 4))) return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  sparse_mla_status_t st = device_setup(&sms);
+  if (st != SPARSE_MLA_OK) return st;
+  if (total_q == 0) return SPARSE_MLA_OK;
+  if (max_seqlen_kv <= topk)   // every row is short: identity lists, no scores
+    return launch_topk(nullptr, 1, sq, total_q, total_kv, 0, total_q, topk, indices, cs);
+  const long long stride = idx_row_stride(max_seqlen_kv);
+  if (!workspace || !aligned(workspace, 16)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
+  long long rows = static_cast<long long>(workspace_bytes / (static_cast<size_t>(stride) * sizeof(float)));
+  if (rows < 1) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (rows > total_q) rows = total_q;
+  float* ws = static_cast<float*>(workspace);
+  for (long long r0 = 0; r0 < total_q; r0 += rows) {
+    const int n = static_cast<int>(total_q - r0 < rows ? total_q - r0 : rows);
+    if (r0 + n > first_long) {
+      const long long s0 = r0 > first_long ? r0 : first_long;   // scored rows of this chunk start here
+      if ((st = launch_scores(q_idx, k_idx, weights, sq, total_q, total_kv, h_idx, static_cast<int>(s0),
+                              static_cast<int>(r0 + n - s0), topk, ws + (s0 - r0) * stride, stride, sms, cs)) !=
+          SPARSE_MLA_OK)
+        return st;
+    }
+    if ((st = launch_topk(ws, stride, sq, total_q, total_kv, static_cast<int>(r0), n, topk, indices, cs)) !=
+        SPARSE_MLA_OK)
+      return st;
+  }
+  return SPARSE_MLA_OK;
+}
 
 }  // namespace
 
@@ -646,8 +746,12 @@ sparse_mla_status_t dsa_indexer_scores(const void* q_idx, const void* k_idx, con
   if (n_rows > 0 && total_kv > 0 && (!scores || !aligned(scores, 4))) return SPARSE_MLA_ERR_INVALID_ARG;
   int sms = 0;
   if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
-  return launch_scores(q_idx, k_idx, weights, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, h_idx, row0,
-                       n_rows, skip_len, scores, row_stride, sms, static_cast<cudaStream_t>(stream));
+  IdxSeqs sq;
+  sq.cu_q = cu_seqlens_q;
+  sq.cu_kv = cu_seqlens_kv;
+  sq.batch = batch;
+  return launch_scores(q_idx, k_idx, weights, sq, total_q, total_kv, h_idx, row0, n_rows, skip_len, scores,
+                       row_stride, sms, static_cast<cudaStream_t>(stream));
 }
 
 sparse_mla_status_t dsa_topk(const float* scores, long long row_stride, const int32_t* cu_seqlens_q,
@@ -665,8 +769,12 @@ sparse_mla_status_t dsa_topk(const float* scores, long long row_stride, const in
   int sms = 0;
   sparse_mla_status_t st = device_setup(&sms);
   if (st != SPARSE_MLA_OK) return st;
-  return launch_topk(scores, row_stride, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, row0, n_rows, topk,
-                     indices, static_cast<cudaStream_t>(stream));
+  IdxSeqs sq;
+  sq.cu_q = cu_seqlens_q;
+  sq.cu_kv = cu_seqlens_kv;
+  sq.batch = batch;
+  return launch_topk(scores, row_stride, sq, total_q, total_kv, row0, n_rows, topk, indices,
+                     static_cast<cudaStream_t>(stream));
 }
 
 size_t dsa_indexer_workspace_size(int total_q, int max_seqlen_kv, int topk) {
@@ -683,20 +791,10 @@ sparse_mla_status_t dsa_indexer_topk(const void* q_idx, const void* k_idx, const
   if (st != SPARSE_MLA_OK) return st;
   if (topk < 1 || max_seqlen_kv < 0 || max_seqlen_kv > total_kv) return SPARSE_MLA_ERR_INVALID_ARG;
   if (cu_seqlens_q == nullptr && max_seqlen_kv != total_kv) return SPARSE_MLA_ERR_INVALID_ARG;
-  if (static_cast<long long>(total_q) * topk > (1LL << 62)) return SPARSE_MLA_ERR_INVALID_ARG;
-  if (total_q > 0 && (!indices || !aligned(indices, 4))) return SPARSE_MLA_ERR_INVALID_ARG;
-  int sms = 0;
-  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
-  if (total_q == 0) return SPARSE_MLA_OK;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (max_seqlen_kv <= topk)   // every row is short: identity lists, no scores
-    return launch_topk(nullptr, 1, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, 0, total_q, topk, indices,
-                       cs);
-  const long long stride = idx_row_stride(max_seqlen_kv);
-  if (!workspace || !aligned(workspace, 16)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
-  long long rows = static_cast<long long>(workspace_bytes / (static_cast<size_t>(stride) * sizeof(float)));
-  if (rows < 1) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
-  if (rows > total_q) rows = total_q;
+  IdxSeqs sq;
+  sq.cu_q = cu_seqlens_q;
+  sq.cu_kv = cu_seqlens_kv;
+  sq.batch = batch;
   // One dense sequence: rows before first_long see at most topk positions.
   long long first_long = 0;
   if (cu_seqlens_q == nullptr) {
@@ -704,22 +802,43 @@ sparse_mla_status_t dsa_indexer_topk(const void* q_idx, const void* k_idx, const
     if (first_long < 0) first_long = 0;
     if (first_long > total_q) first_long = total_q;
   }
-  float* ws = static_cast<float*>(workspace);
-  // Query rows in chunks whose logits fit the workspace (the logits budget).
-  for (long long r0 = 0; r0 < total_q; r0 += rows) {
-    const int n = static_cast<int>(total_q - r0 < rows ? total_q - r0 : rows);
-    if (r0 + n > first_long) {
-      const long long s0 = r0 > first_long ? r0 : first_long;   // scored rows of this chunk start here
-      if ((st = launch_scores(q_idx, k_idx, weights, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, h_idx,
-                              static_cast<int>(s0), static_cast<int>(r0 + n - s0), topk,
-                              ws + (s0 - r0) * stride, stride, sms, cs)) != SPARSE_MLA_OK)
-        return st;
-    }
-    if ((st = launch_topk(ws, stride, cu_seqlens_q, cu_seqlens_kv, batch, total_q, total_kv, static_cast<int>(r0), n,
-                          topk, indices, cs)) != SPARSE_MLA_OK)
-      return st;
-  }
-  return SPARSE_MLA_OK;
+  return indexer_topk_chunks(q_idx, k_idx, weights, sq, total_q, total_kv, max_seqlen_kv, h_idx, topk, first_long,
+                             indices, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+sparse_mla_status_t dsa_indexer_scores_paged(const void* q_idx, const void* k_cache, const float* weights,
+                                             const int32_t* block_table, const int32_t* cache_seqlens, int batch,
+                                             int s_next, int h_idx, int d_idx, int page_size, int max_blocks,
+                                             int num_blocks, int row0, int n_rows, int skip_len, float* scores,
+                                             long long row_stride, void* stream) {
+  sparse_mla_status_t st = check_paged_indexer(q_idx, k_cache, weights, block_table, cache_seqlens, batch, s_next,
+                                               h_idx, d_idx, page_size, max_blocks, num_blocks);
+  if (st != SPARSE_MLA_OK) return st;
+  const long long total_q = static_cast<long long>(batch) * s_next;
+  if (row0 < 0 || n_rows < 0 || row0 + static_cast<long long>(n_rows) > total_q || skip_len < 0 || row_stride < 1)
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_rows > 0 && (!scores || !aligned(scores, 4))) return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  IdxSeqs sq = paged_seqs(block_table, cache_seqlens, batch, s_next, max_blocks, num_blocks);
+  return launch_scores(q_idx, k_cache, weights, sq, static_cast<int>(total_q), num_blocks * smla::kIdxPage, h_idx,
+                       row0, n_rows, skip_len, scores, row_stride, sms, static_cast<cudaStream_t>(stream));
+}
+
+sparse_mla_status_t dsa_indexer_topk_paged(const void* q_idx, const void* k_cache, const float* weights,
+                                           const int32_t* block_table, const int32_t* cache_seqlens, int batch,
+                                           int s_next, int h_idx, int d_idx, int page_size, int max_blocks,
+                                           int num_blocks, int max_seqlen_kv, int topk, int32_t* indices,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  sparse_mla_status_t st = check_paged_indexer(q_idx, k_cache, weights, block_table, cache_seqlens, batch, s_next,
+                                               h_idx, d_idx, page_size, max_blocks, num_blocks);
+  if (st != SPARSE_MLA_OK) return st;
+  if (topk < 1 || max_seqlen_kv < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  const long long total_q = static_cast<long long>(batch) * s_next;
+  IdxSeqs sq = paged_seqs(block_table, cache_seqlens, batch, s_next, max_blocks, num_blocks);
+  return indexer_topk_chunks(q_idx, k_cache, weights, sq, static_cast<int>(total_q), num_blocks * smla::kIdxPage,
+                             max_seqlen_kv, h_idx, topk, 0, indices, workspace, workspace_bytes,
+                             static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

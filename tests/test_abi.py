@@ -152,3 +152,24 @@ def test_indexer_workspace_size(lib):
     assert lib.dsa_indexer_workspace_size(10, 4096, 2048) == 10 * 4096 * 4
     assert lib.dsa_indexer_workspace_size(10, 2048, 2048) == 0      # no row is scored
     assert lib.dsa_indexer_workspace_size(0, 4096, 2048) == 0
+
+
+def test_paged_indexer_validation(lib):
+    def paged(**kw):
+        a = dict(q=16, k=16, w=16, bt=16, sl=16, batch=2, s_next=6, h=64, d=128, page=64, mb=8, nb=16, ms=500,
+                 topk=64, idx=16, ws=16, wsb=4096, stream=None)
+        a.update(kw)
+        return lib.dsa_indexer_topk_paged(a["q"], a["k"], a["w"], a["bt"], a["sl"], a["batch"], a["s_next"],
+                                          a["h"], a["d"], a["page"], a["mb"], a["nb"], a["ms"], a["topk"], a["idx"],
+                                          a["ws"], a["wsb"], a["stream"])
+    assert paged(page=32) == 2
+    assert paged(h=8) == 2
+    assert paged(batch=4096) == 2
+    assert paged(s_next=0) == 1
+    assert paged(bt=None) == 1
+    assert paged(sl=None) == 1
+    assert paged(k=24) == 1          # not 16-byte aligned
+    assert paged(topk=0) == 1
+    assert paged(idx=None) == 1
+    st = lib.dsa_indexer_scores_paged(16, 16, 16, 16, 16, 2, 6, 64, 128, 64, 8, 16, 10, 5, 0, 16, 500, None)
+    assert st == 1                   # rows past batch * s_next

@@ -117,11 +117,13 @@ def test_topk_tied_scores_exact(smla, rows, width, topk):
     np.testing.assert_array_equal(got, ref)
 
 
-def test_topk_distinct_and_unstaged_rows_exact(smla):
-    """Distinct normal scores; rows longer than the shared-memory staging
-    (12288 positions) are read from global memory on every pass."""
-    g = torch.Generator().manual_seed(501)
-    rows, width, topk = 12, 20000, 2048
+@pytest.mark.parametrize("rows,width", [(12, 20000), (4, 60000)])
+def test_topk_long_rows_exact(smla, rows, width):
+    """Distinct normal scores on rows past 8192 positions (1024-thread CTAs):
+    staged in shared memory up to 49152 positions, read from global memory
+    on every pass beyond."""
+    g = torch.Generator().manual_seed(501 + width)
+    topk = 2048
     sc = torch.randn((rows, width), generator=g)
     got = smla.dsa_topk(sc.to(DEV), topk, rows, width).cpu().numpy()
     ref = ido.topk_rows(sc.numpy(), _lens_dense(rows, width), topk)
@@ -321,3 +323,104 @@ def test_indexer_lists_drive_the_forward(smla):
     l = lse.cpu().numpy()[same]
     assert np.all(np.abs(o - ro) <= 2e-2 + 2e-2 * np.abs(ro))
     assert np.all(np.abs(l - rl) <= 1e-3)
+
+
+# --------------------------------------------------------------------------- paged (decode) cache
+
+def _pdev(c):
+    return (c.q_idx.to(DEV), c.k_cache.to(DEV), c.weights.to(DEV), c.block_table.to(DEV), c.cache_seqlens.to(DEV))
+
+
+def _paged_row_ref(c, r, keys_cache):
+    s_next = c.q_idx.shape[1]
+    b, j = divmod(r, s_next)
+    lk = int(c.cache_seqlens[b])
+    v = ido.visible_len(j, s_next, lk)
+    if b not in keys_cache:
+        keys_cache[b] = ido.linearise_keys(c.k_cache, c.block_table[b], lk, c.page)
+    k = keys_cache[b][:v]
+    q = c.q_idx[b, j].double().numpy()
+    w = c.weights[b, j].double().numpy()
+    ref = ido.token_scores(q, w, k)
+    bound = np.abs(w) @ (GAMMA_DOT * (np.abs(q) @ np.abs(k).T)) + GAMMA_SUM * (np.abs(w) @ np.maximum(q @ k.T, 0.0))
+    return ref, bound + 1e-30, v
+
+
+def _check_paged_list(c, lst, r, topk, keys_cache):
+    ref, bound, v = _paged_row_ref(c, r, keys_cache)
+    lst = np.asarray(lst)
+    n = min(topk, v)
+    assert np.all(lst[n:] == -1), f"row {r}: padding"
+    sel = lst[:n]
+    assert np.all(sel >= 0) and np.all(sel < v) and np.all(np.diff(sel) > 0), f"row {r}: invalid list"
+    if v <= topk:
+        np.testing.assert_array_equal(sel, np.arange(v))
+        return True
+    chosen = np.zeros(v, dtype=bool)
+    chosen[sel] = True
+    assert (ref + bound)[chosen].min() >= (ref - bound)[~chosen].max(), f"row {r}: order beyond the bounds"
+    srt = np.sort(ref)[::-1]
+    if srt[topk - 1] - srt[topk] > 2.0 * bound.max():
+        np.testing.assert_array_equal(sel, ido.select_topk(ref, topk)[:n])
+        return True
+    return False
+
+
+def test_paged_scores(smla):
+    """Every row scored over its pages (NaN in every unused slot and spare
+    page), positions past a row's length untouched."""
+    c = mi.indexer_paged_case(550, 5, 6, 300, 1500, topk=128)
+    max_len = int(c.cache_seqlens.max())
+    got = smla.dsa_indexer_scores_paged(*_pdev(c), max_len).cpu().numpy()
+    keys = {}
+    for r in range(30):
+        ref, bound, v = _paged_row_ref(c, r, keys)
+        err = np.abs(got[r, :v].astype(np.float64) - ref)
+        assert np.all(err <= bound), f"row {r}: max err {err.max()}"
+        assert np.all(np.isneginf(got[r, v:]))
+
+
+def test_paged_lists_and_page_shuffle(smla):
+    c = mi.indexer_paged_case(551, 7, 6, 700, 3000, topk=512)
+    q, k, w, bt, sl = _pdev(c)
+    lst = smla.dsa_indexer_topk_paged(q, k, w, bt, sl, 512).cpu().numpy().reshape(42, 512)
+    keys = {}
+    exact = sum(_check_paged_list(c, lst[r], r, 512, keys) for r in range(42))
+    assert exact >= 6   # the oracle's gaps make 8 of these rows unique
+    # a shuffle of the physical pages, the block table remapped: same lists
+    perm = torch.randperm(c.k_cache.shape[0], generator=mi._gen(552))
+    k2 = torch.empty_like(c.k_cache)
+    k2[perm] = c.k_cache
+    bt2 = perm[c.block_table.long()].to(torch.int32)
+    lst2 = smla.dsa_indexer_topk_paged(q, k2.to(DEV), w, bt2.to(DEV), sl, 512).cpu().numpy().reshape(42, 512)
+    np.testing.assert_array_equal(lst, lst2)
+
+
+def test_paged_short_requests_and_budget(smla):
+    """Requests shorter than topk (identity lists), one shorter than its MTP
+    rows (its first rows see nothing), and a logits budget of three rows."""
+    c = mi.indexer_paged_case(553, 4, 6, 3, 900, topk=256)
+    c.cache_seqlens[1] = 4          # rows 0, 1 of request 1 see no position
+    c.cache_seqlens[2] = 200        # short: identity lists
+    q, k, w, bt, sl = _pdev(c)
+    full = smla.dsa_indexer_topk_paged(q, k, w, bt, sl, 256)
+    ws = torch.empty(3 * 904 * 4, dtype=torch.uint8, device=DEV)
+    part = smla.dsa_indexer_topk_paged(q, k, w, bt, sl, 256, max_seqlen_kv=900, workspace=ws)
+    assert torch.equal(full, part)
+    lst = full.cpu().numpy().reshape(24, 256)
+    keys = {}
+    for r in range(24):
+        _check_paged_list(c, lst[r], r, 256, keys)
+    assert np.all(lst[6:8] == -1)
+
+
+def test_paged_decode_shape_sampled(smla):
+    """16 requests x 6 MTP tokens, contexts U[4096, 32768], topk 2048, 64
+    indexer heads (the decode workload's shape); sampled rows."""
+    c = mi.indexer_paged_case(554, 16, 6, 4096, 32768, topk=2048)
+    lst = smla.dsa_indexer_topk_paged(*_pdev(c), 2048).cpu().numpy().reshape(96, 2048)
+    keys = {}
+    # rows of ~4-33 K positions: the oracle's gap at the 2048th score is
+    # within the bounds, so each row is checked by its validity and ordering
+    for r in (0, 5, 17, 40, 63, 95):
+        _check_paged_list(c, lst[r], r, 2048, keys)

@@ -27,8 +27,8 @@
 //
 //   warp 0      TMA: per item the group's Q (two 32 KB boxes, 128B swizzle)
 //               and its head weights (1-D bulk copy), then the K tiles (two
-//               16 KB boxes each) through a 4-deep ring that runs ahead
-//               across items.
+//               16 KB boxes each; four 8 KB boxes, two pages, for a paged
+//               cache) through a 4-deep ring that runs ahead across items.
 //   warp 1      one thread issues a tile's 8 MMAs (K = 16 each) into one of
 //               two 256-column TMEM accumulators and commits.
 //   warps 2..9  epilogue over half of the group's (row, head) columns each:
@@ -40,12 +40,13 @@
 //               positions).  The accumulator is freed once read.
 //
 // A persistent grid (at most one CTA per SM, ~212 KB of shared memory each)
-// walks items c, c + G, ... (largest groups first); while an item runs, its
-// successor's Q is prefetched into L2.  Rows that see at most `skip_len` positions
+// walks items c, c + G, ... (dealt chunk by chunk, largest groups first);
+// while an item runs, its successor's Q is prefetched into L2.  Rows that see at most `skip_len` positions
 // get no tiles.  A group that straddles sequences is run as one segment per
 // sequence, each against that sequence's keys.
 //
-// dsa_topk_kernel: one CTA per query row.  The row's order-preserving
+// dsa_topk_kernel: one CTA per query row (256 threads; 1024 when rows pass
+// 8192 positions).  The row's order-preserving
 // integer keys (the image of fp32) are staged in shared memory when they
 // fit; a radix select of the topk largest then counts digits of 11, 11 and
 // 10 bits in shared-memory histograms (each pass over the keys still in

@@ -23,17 +23,21 @@
 //   warps 0..3   producers: gather the block's rows (value pairs + rope tile)
 //                and publish its 64 row ids.
 //   warps 4, 9   S^T = K Q^T and dP^T = V dout^T (swap-AB, M = 64 kv rows,
-//                N = 16 heads) into TMEM: with U = 1 each takes half of the
-//                value pairs (warp 4 also the rope columns of S); with U = 2
-//                each takes one half of the heads, all pairs and the rope.
+//                N = every head of the unit) into TMEM: with U = 1 each
+//                takes half of the value pairs (warp 4 also the rope columns
+//                of S); with U = 2 warp 4 issues S and warp 9 dP, each over
+//                all pairs at N = 32 (Q and dout of the 32 heads form one
+//                K-major tile per 64-dim chunk).
 //   warps 5..8   P, dS from S, dP, the LSE and D; write P^T and
 //                (sm_scale dS)^T of every half as bf16 rows into shared
 //                memory.
-//   warp 10      dQ^T += K^T (sm_scale dS)^T per half (K^T the MN-major view
-//                of the gathered tile, as V^T in the forward's P.V;
-//                accumulated in TMEM over the unit), which frees the block's
-//                tiles; then the block's dKV rows in three column chunks
-//                (256, 256, 64 with U = 1; 192 each with U = 2):
+//   warp 10      dQ^T += K^T (sm_scale dS)^T over all heads of the unit (K^T
+//                the MN-major view of the gathered tile, as V^T in the
+//                forward's P.V; accumulated in TMEM over the unit), which frees the block's
+//                tiles; then the block's dKV rows in column chunks
+//                (256, 256, 64 in one TMEM buffer with U = 1; with U = 2
+//                128, 64, 128, 64, 128, 64 alternating between two buffers,
+//                one chunk's MMAs overlapping the other's drain):
 //                dKV = sum over halves of (sm_scale dS)^T Q + P^T [dout, 0]
 //                (M = 64 rows, K = 16 heads per half, Q and dout read as
 //                MN-major B operands).
@@ -59,27 +63,39 @@ struct BwdLayout {
   static constexpr int kPRow = N * 2;                   // bytes of one P^T / dS^T row
   static constexpr uint32_t kPSwz = SWZ_32B;
   static constexpr int kPSBytes = kBlk * kPRow;         // one P^T or dS^T tile of one half (2 KB)
-  static constexpr int kQHalf = 9 * N * 128;            // Q of one half: 9 chunks x N heads x 128 B
-  static constexpr int kDOHalf = 8 * N * 128;           // dout of one half: 8 chunks
+  static constexpr int kPSLbo = 2 * kPSBytes;           // dS^T of half 1 from that of half 0 ([half][P^T, dS^T])
+  // Q and dout: 64-dim chunks of all H heads of the unit (128 B per head,
+  // K-major with the 128B swizzle), so that the S, dP and dQ MMAs take every
+  // head of the unit at once (N = H); half h is rows [16 h, 16 h + 16).
+  static constexpr int kQChunk = H * 128;
   static constexpr int kQOff = 0;
-  static constexpr int kDOOff = kQOff + U * kQHalf;
-  static constexpr int kVOff = kDOOff + U * kDOHalf;
+  static constexpr int kDOOff = kQOff + 9 * kQChunk;
+  static constexpr int kVOff = kDOOff + 8 * kQChunk;
   static constexpr int kROff = kVOff + kNV * kPairBytes;
   static constexpr int kPSOff = kROff + kNR * kChunkBytes;   // [buffer][half][P^T, dS^T]
   static constexpr int kMiscOff = kPSOff + 2 * U * 2 * kPSBytes;
   // TMEM columns
-  static constexpr int kTS = 0;                         // S^T: [part or half][buffer], N columns each
-  static constexpr int kTdP = 4 * N;                    // dP^T: [part or half][buffer]
-  static constexpr int kTdQ = 8 * N;                    // dQ^T per half: four M=128 tiles of 128 dims, the M=64 rope tile
-  static constexpr int kTdKV = U == 1 ? 256 : kTdQ + U * 5 * N;   // one dKV chunk (M=64)
-  static constexpr int kKVChunk = U == 1 ? 256 : 192;   // dKV chunk width: three chunks cover 576
+  static constexpr int kTS = 0;                         // S^T: U = 1 [part][buffer] x 16; U = 2 [buffer] x 32
+  static constexpr int kTdP = 4 * N;                    // dP^T: the same
+  static constexpr int kTdQ = 8 * N;                    // dQ^T: four M=128 tiles of 128 dims, the M=64 rope tile; H columns each
+  static constexpr int kTdKV = U == 1 ? 256 : kTdQ + 5 * H;   // dKV chunk buffers (M=64)
+  // dKV column chunks: U = 1, three (256, 256, 64) in one TMEM buffer; U = 2,
+  // six alternating between a 128- and a 64-column buffer (128, 64, 128, 64,
+  // 128, 64), so that one chunk's MMAs run while the other buffer drains.
+  // Chunks start on 64-dim boundaries (the MN-major Q / dout swizzle atoms).
+  static constexpr int kKVChunks = U == 1 ? 3 : 6;
+  static constexpr int kKVBufs = U == 1 ? 1 : 2;
+  __device__ static constexpr int kv_col0(int c) { return U == 1 ? c * 256 : (c >> 1) * 192 + (c & 1) * 128; }
+  __device__ static constexpr int kv_width(int c) { return U == 1 ? (c < 2 ? 256 : 64) : ((c & 1) ? 64 : 128); }
+  __device__ static constexpr int kv_tmem(int c) { return kTdKV + (U == 1 ? 0 : (c & 1) * 128); }
   static constexpr int kTmemCols = 512;
   // warp roles
   static constexpr int kQkWarp0 = 4, kSoftWarp0 = 5, kQkWarp1 = 9, kGradWarp = 10, kDrainWarp0 = 11;
   static constexpr int kThreads = 15 * 32;
 };
 static_assert(BwdLayout<1>::kTdQ + 5 * BwdLayout<1>::N <= BwdLayout<1>::kTdKV, "TMEM map");
-static_assert(BwdLayout<2>::kTdKV + BwdLayout<2>::kKVChunk <= BwdLayout<2>::kTmemCols, "TMEM map");
+static_assert(BwdLayout<1>::kTdKV + 256 <= BwdLayout<1>::kTmemCols, "TMEM map");
+static_assert(BwdLayout<2>::kTdKV + 128 + 64 <= BwdLayout<2>::kTmemCols, "TMEM map");
 static_assert(BwdLayout<1>::kVOff % 1024 == 0 && BwdLayout<1>::kROff % 1024 == 0 && BwdLayout<1>::kPSOff % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
 static_assert(BwdLayout<2>::kVOff % 1024 == 0 && BwdLayout<2>::kROff % 1024 == 0 && BwdLayout<2>::kPSOff % 1024 == 0,
@@ -90,7 +106,8 @@ struct __align__(16) BwdMisc {
   uint64_t v_full[BwdLayout<U>::kNV], v_empty[BwdLayout<U>::kNV];
   uint64_t rp_full[BwdLayout<U>::kNR], rp_empty[BwdLayout<U>::kNR];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
-  uint64_t q_full, q_empty, s_full[2][2], pds_full[2], pds_empty[2], dkv_full, dkv_empty, dq_full, drain[3],
+  uint64_t q_full, q_empty, s_full[2][2], pds_full[2], pds_empty[2], dkv_full[2], dkv_empty[2], dq_full,
+      drain[3],
       cand_full;
   int32_t info_blk[kInfoDepth];
   uint32_t info_mask[kInfoDepth][2];
@@ -125,23 +142,25 @@ __device__ __forceinline__ void bwd_raise(BwdMisc<U>& m, int code) {
 
 // S^T (QK^T) and dP^T of block n for one part.  U = 1: value pairs 2P and
 // 2P+1 (part 0 also the rope columns of S), the two parts summed by the
-// softmax.  U = 2: PART is the half of the heads, over every value pair and
-// the rope.  The A operand (the gathered rows, K-major) is shared by the two
-// products; B is Q for S and dout for dP.
+// softmax.  U = 2: part 0 issues S^T and part 1 dP^T, each over every value
+// pair (S also the rope) and all 32 heads in one N = 32 MMA per k-step.  The
+// A operand (the gathered rows, K-major) is shared by the two products; B is
+// Q for S and dout for dP.
 template <int U, int PART>
 __device__ __forceinline__ bool bwd_issue_s_dp(BwdMisc<U>& m, uint32_t qbase, uint32_t dobase, uint32_t vbase,
                                                uint32_t rbase, uint32_t tmem, int n, uint64_t deadline,
                                                const volatile int* ab) {
   using L = BwdLayout<U>;
-  constexpr int N = L::N;
+  constexpr int NM = L::H;                        // MMA N: every head of the unit
   constexpr int kPairs = U == 1 ? 2 : 4;          // value pairs this issuer takes
   constexpr int kPair0 = U == 1 ? 2 * PART : 0;
-  constexpr bool kRope = U == 2 || PART == 0;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(64, N, false, false);
-  const uint32_t tS = tmem + static_cast<uint32_t>(L::kTS + (PART * 2 + (n & 1)) * N);
-  const uint32_t tP = tmem + static_cast<uint32_t>(L::kTdP + (PART * 2 + (n & 1)) * N);
-  const uint32_t qh = qbase + (U == 2 ? PART * L::kQHalf : 0);
-  const uint32_t dh = dobase + (U == 2 ? PART * L::kDOHalf : 0);
+  constexpr bool kS = U == 1 || PART == 0;        // issues S^T
+  constexpr bool kDP = U == 1 || PART == 1;       // issues dP^T
+  constexpr bool kRope = PART == 0;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(64, NM, false, false);
+  const uint32_t buf = U == 1 ? static_cast<uint32_t>(PART * 2 + (n & 1)) : static_cast<uint32_t>(n & 1);
+  const uint32_t tS = tmem + static_cast<uint32_t>(L::kTS) + buf * NM;
+  const uint32_t tP = tmem + static_cast<uint32_t>(L::kTdP) + buf * NM;
   uint32_t slot[kPairs];
 #pragma unroll
   for (int i = 0; i < kPairs; ++i) {
@@ -162,11 +181,10 @@ __device__ __forceinline__ bool bwd_issue_s_dp(BwdMisc<U>& m, uint32_t qbase, ui
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t a = smem_desc(vbase + slot[i] * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
-        const uint64_t bq = smem_desc(qh + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
-        const uint64_t bd = smem_desc(dh + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
         const uint32_t acc = (i | c | kk) != 0 ? 1u : 0u;
-        mma_bf16_ss(tS, a, bq, kIdesc, acc);
-        mma_bf16_ss(tP, a, bd, kIdesc, acc);
+        if (kS) mma_bf16_ss(tS, a, smem_desc(qbase + (2 * pr + c) * L::kQChunk + kk * 32, 16, 1024, SWZ_128B), kIdesc, acc);
+        if (kDP)
+          mma_bf16_ss(tP, a, smem_desc(dobase + (2 * pr + c) * L::kQChunk + kk * 32, 16, 1024, SWZ_128B), kIdesc, acc);
       }
     }
   }
@@ -174,7 +192,7 @@ __device__ __forceinline__ bool bwd_issue_s_dp(BwdMisc<U>& m, uint32_t qbase, ui
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
-      const uint64_t b = smem_desc(qh + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
+      const uint64_t b = smem_desc(qbase + 8 * L::kQChunk + kk * 32, 16, 1024, SWZ_128B);
       mma_bf16_ss(tS, a, b, kIdesc, 1u);
     }
   }
@@ -222,8 +240,9 @@ template <int U>
 __device__ bool run_bwd_grad(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbase, uint32_t tmem) {
   using L = BwdLayout<U>;
   constexpr int N = L::N;
-  constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, N, true, true);
-  constexpr uint32_t kIdescDQr = idesc_bf16_f32(64, N, true, true);
+  constexpr int NM = L::H;                           // MMA N of dQ: every head of the unit
+  constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, NM, true, true);
+  constexpr uint32_t kIdescDQr = idesc_bf16_f32(64, NM, true, true);
   const volatile int* ab = &m.abort_flag;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t dobase = smem_u32(sbase + L::kDOOff);
@@ -231,7 +250,6 @@ __device__ bool run_bwd_grad(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbase, 
   const uint32_t rbase = smem_u32(sbase + L::kROff);
   const uint32_t psbase = smem_u32(sbase + L::kPSOff);
   const uint32_t tdQ = tmem + L::kTdQ;
-  const uint32_t tKV = tmem + L::kTdKV;
   int n = 0, ni = 0, chunks = 0;
   ItemIter iter = items_begin(p);
   Item item;
@@ -250,48 +268,45 @@ __device__ bool run_bwd_grad(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbase, 
       tc_fence_after();
       // this block's tiles: [half][P^T, dS^T]
       const uint32_t ps = psbase + static_cast<uint32_t>(n & 1) * static_cast<uint32_t>(U * 2 * L::kPSBytes);
-      // dQ^T[576 x N] += K^T[576 x 64] dS^T[64 x N] per half: four 128-dim
-      // tiles of the value pairs, then the 64 rope dims (M = 64).  Each pair
-      // tile is free after its MMAs of every half (dP already used it; dKV
-      // does not read it).
+      // dQ^T[576 x H] += K^T[576 x 64] dS^T[64 x H]: four 128-dim tiles of
+      // the value pairs, then the 64 rope dims (M = 64).  B is MN-major over
+      // the heads: with U = 2 the dS^T tiles of the two halves are its two
+      // 16-head swizzle atoms, kLBO apart.  Each pair tile is free after its
+      // MMAs (dP already used it; dKV does not read it).
+      const uint32_t pds = ps + static_cast<uint32_t>(L::kPSBytes);   // dS^T of half 0
 #pragma unroll 1
       for (int u = 0; u < 4; ++u) {
         const uint32_t s = (static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u)) % L::kNV;
 #pragma unroll
-        for (int h = 0; h < U; ++h) {
-          const uint32_t pds = ps + static_cast<uint32_t>(h * 2 + 1) * L::kPSBytes;
-#pragma unroll
-          for (int ks = 0; ks < kBlk / 16; ++ks) {
-            const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-            const uint64_t b = smem_desc(pds + ks * 16 * L::kPRow, 16 * L::kPRow * 8, 8 * L::kPRow, L::kPSwz);
-            mma_bf16_ss(tdQ + h * 5 * N + u * N, a, b, kIdescDQ, (nl > 0 || ks > 0) ? 1u : 0u);
-          }
+        for (int ks = 0; ks < kBlk / 16; ++ks) {
+          const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
+          const uint64_t b = smem_desc(pds + ks * 16 * L::kPRow, L::kPSLbo, 8 * L::kPRow, L::kPSwz);
+          mma_bf16_ss(tdQ + u * NM, a, b, kIdescDQ, (nl > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&m.v_empty[s]));
       }
       const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
 #pragma unroll
-      for (int h = 0; h < U; ++h) {
-        const uint32_t pds = ps + static_cast<uint32_t>(h * 2 + 1) * L::kPSBytes;
-#pragma unroll
-        for (int ks = 0; ks < kBlk / 16; ++ks) {
-          const uint64_t a = smem_desc(rbase + rs * kChunkBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-          const uint64_t b = smem_desc(pds + ks * 16 * L::kPRow, 16 * L::kPRow * 8, 8 * L::kPRow, L::kPSwz);
-          mma_bf16_ss(tdQ + h * 5 * N + 4 * N, a, b, kIdescDQr, (nl > 0 || ks > 0) ? 1u : 0u);
-        }
+      for (int ks = 0; ks < kBlk / 16; ++ks) {
+        const uint64_t a = smem_desc(rbase + rs * kChunkBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
+        const uint64_t b = smem_desc(pds + ks * 16 * L::kPRow, L::kPSLbo, 8 * L::kPRow, L::kPSwz);
+        mma_bf16_ss(tdQ + 4 * NM, a, b, kIdescDQr, (nl > 0 || ks > 0) ? 1u : 0u);
       }
       mma_commit(smem_u32(&m.rp_empty[rs]));
-      // dKV rows of the block in three column chunks: the sum over halves of
+      // dKV rows of the block in column chunks: the sum over halves of
       // (sm_scale dS)^T Q plus P^T [dout, 0].  A: the P^T / dS^T tiles as
-      // K-major [64 rows x 16 heads]; B: Q / dout as MN-major [16 heads x
-      // dims] (their 64-dim chunks sit N * 128 bytes apart).
+      // K-major [64 rows x 16 heads]; B: the half's 16 rows of Q / dout as
+      // MN-major [16 heads x dims] (their 64-dim chunks sit kQChunk bytes
+      // apart).
 #pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        const int col0 = c * L::kKVChunk;
-        const int wq = 576 - col0 < L::kKVChunk ? 576 - col0 : L::kKVChunk;   // Q columns of the chunk
-        const int wd = 512 - col0 < wq ? 512 - col0 : wq;                     // dout columns (may be none)
-        if (!mbar_wait(smem_u32(&m.dkv_empty), (static_cast<uint32_t>(chunks) & 1u) ^ 1u, deadline, ab))
-          return false;
+      for (int c = 0; c < L::kKVChunks; ++c) {
+        const int col0 = L::kv_col0(c);
+        const int wq = L::kv_width(c);                                    // Q columns of the chunk
+        const int wd = 512 - col0 < wq ? (512 - col0 > 0 ? 512 - col0 : 0) : wq;   // dout columns (may be none)
+        const int b = chunks % L::kKVBufs;
+        const uint32_t use = static_cast<uint32_t>(chunks / L::kKVBufs);
+        const uint32_t tKV = tmem + static_cast<uint32_t>(L::kv_tmem(c));
+        if (!mbar_wait(smem_u32(&m.dkv_empty[b]), (use & 1u) ^ 1u, deadline, ab)) return false;
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < U; ++h) {
@@ -299,15 +314,15 @@ __device__ bool run_bwd_grad(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbase, 
           const uint64_t a_p = smem_desc(pt, 16, 8 * L::kPRow, L::kPSwz);
           const uint64_t a_ds = smem_desc(pt + L::kPSBytes, 16, 8 * L::kPRow, L::kPSwz);
           const uint64_t bq =
-              smem_desc(qbase + h * L::kQHalf + (col0 / 64) * N * 128, N * 128, 1024, SWZ_128B);
+              smem_desc(qbase + h * N * 128 + (col0 / 64) * L::kQChunk, L::kQChunk, 1024, SWZ_128B);
           mma_bf16_ss(tKV, a_ds, bq, idesc_bf16_f32(64, wq, false, true), h > 0 ? 1u : 0u);
           if (wd > 0) {
             const uint64_t bd =
-                smem_desc(dobase + h * L::kDOHalf + (col0 / 64) * N * 128, N * 128, 1024, SWZ_128B);
+                smem_desc(dobase + h * N * 128 + (col0 / 64) * L::kQChunk, L::kQChunk, 1024, SWZ_128B);
             mma_bf16_ss(tKV, a_p, bd, idesc_bf16_f32(64, wd, false, true), 1u);
           }
         }
-        mma_commit(smem_u32(&m.dkv_full));
+        mma_commit(smem_u32(&m.dkv_full[b]));
         ++chunks;
       }
       mma_commit(smem_u32(&m.pds_empty[n & 1]));
@@ -384,7 +399,7 @@ __device__ bool run_bwd_drain(const FwdParams& p, BwdMisc<U>& m, uint32_t tmem) 
   const int q4 = warp & 3;
   const int r = q4 * 16 + (lane & 15);        // block row of this thread (M=64 layout)
   const int half = lane >> 4;
-  const uint32_t tKV = tmem + (static_cast<uint32_t>(q4 * 32) << 16) + L::kTdKV;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);   // this warp's TMEM lanes
   int ni = 0, chunks = 0;
   ItemIter iter = items_begin(p);
   Item item;
@@ -405,12 +420,15 @@ __device__ bool run_bwd_drain(const FwdParams& p, BwdMisc<U>& m, uint32_t tmem) 
       }
       float* dst = p.dkv + static_cast<size_t>(row < 0 ? 0 : row) * kDqk;
 #pragma unroll 1
-      for (int c = 0; c < 3; ++c) {
-        const bool ok = mbar_wait(smem_u32(&m.dkv_full), static_cast<uint32_t>(chunks) & 1u, deadline, ab);
+      for (int c = 0; c < L::kKVChunks; ++c) {
+        const int b = chunks % L::kKVBufs;
+        const uint32_t use = static_cast<uint32_t>(chunks / L::kKVBufs);
+        const bool ok = mbar_wait(smem_u32(&m.dkv_full[b]), use & 1u, deadline, ab);
         if (!__all_sync(0xffffffffu, ok)) return false;
         tc_fence_after();
-        const int col0 = c * L::kKVChunk;
-        const int w = 576 - col0 < L::kKVChunk ? 576 - col0 : L::kKVChunk;
+        const int col0 = L::kv_col0(c);
+        const int w = L::kv_width(c);
+        const uint32_t tKV = tl + static_cast<uint32_t>(L::kv_tmem(c));
         if constexpr (U == 1) {
           drain_chunk(tKV, w, dst + col0, row >= 0, half);
         } else {
@@ -418,7 +436,7 @@ __device__ bool run_bwd_drain(const FwdParams& p, BwdMisc<U>& m, uint32_t tmem) 
           for (int col = 0; col < w; col += 32) drain_cols32(tKV, col, dst + col0, row >= 0, half);
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&m.dkv_empty));
+        mbar_arrive(smem_u32(&m.dkv_empty[b]));
         ++chunks;
       }
       __syncwarp();
@@ -466,22 +484,21 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbas
       if (bar_red_or_128(bar_id, !ok)) return false;
     }
     // Q (9 chunks) and dout (8 chunks) of the unit's heads -> shared memory,
-    // each half K-major with the 128B swizzle; heads past h_q are zero-filled.
+    // K-major with the 128B swizzle, all H heads per chunk; heads past h_q
+    // are zero-filled.
     {
       const __nv_bfloat16* qt = p.q + tok_h * kDqk;
       for (int x = tid; x < H * 72; x += 128) {
         const int hd = x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
-        const int hf = hd / N, hh = hd % N;
         const bool live = hd < hv;
-        cp_async_16(qbase + hf * L::kQHalf + c * (N * 128) + hh * 128 + ((piece ^ (hh & 7)) << 4),
+        cp_async_16(qbase + c * L::kQChunk + hd * 128 + ((piece ^ (hd & 7)) << 4),
                     qt + static_cast<size_t>(live ? hd : 0) * kDqk + c * 64 + piece * 8, live ? 16u : 0u);
       }
       const __nv_bfloat16* dt = p.dout + tok_h * kDv;
       for (int x = tid; x < H * 64; x += 128) {
         const int hd = x / 64, rem = x % 64, c = rem >> 3, piece = rem & 7;
-        const int hf = hd / N, hh = hd % N;
         const bool live = hd < hv;
-        cp_async_16(dobase + hf * L::kDOHalf + c * (N * 128) + hh * 128 + ((piece ^ (hh & 7)) << 4),
+        cp_async_16(dobase + c * L::kQChunk + hd * 128 + ((piece ^ (hd & 7)) << 4),
                     dt + static_cast<size_t>(live ? hd : 0) * kDv + c * 64 + piece * 8, live ? 16u : 0u);
       }
       // D = rowsum(dout * out) per head: eight threads per head, 64 columns each.
@@ -564,8 +581,8 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbas
             d[i] += db[i];
           }
         } else {
-          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTS + hf * 2 * N + col, s);
-          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTdP + hf * 2 * N + col, d);
+          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTS + 2 * col + hf * N, s);
+          tmem_ld16x2_x8<HH>(tmem + lane_off + L::kTdP + 2 * col + hf * N, d);
           tmem_wait_ld();
         }
         float pr[HH], ds[HH];
@@ -603,7 +620,7 @@ __device__ bool run_bwd_softmax(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbas
       for (int mt = 0; mt < 5; ++mt) {
         float o[16];
         if (nl > 0) {
-          tmem_ld16(tmem + lane_off + L::kTdQ + hf * 5 * N + mt * N, o);
+          tmem_ld16(tmem + lane_off + L::kTdQ + mt * H + hf * N, o);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -657,8 +674,10 @@ __global__ void __launch_bounds__(BwdLayout<U>::kThreads, 1) sparse_mla_bwd_kern
       mbar_init(smem_u32(&m.pds_full[i]), 128);
       mbar_init(smem_u32(&m.pds_empty[i]), 1);
     }
-    mbar_init(smem_u32(&m.dkv_full), 1);
-    mbar_init(smem_u32(&m.dkv_empty), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&m.dkv_full[i]), 1);
+      mbar_init(smem_u32(&m.dkv_empty[i]), 128);
+    }
     mbar_init(smem_u32(&m.dq_full), 1);
     for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&m.drain[i]), 1);
     mbar_init(smem_u32(&m.cand_full), kProducerWarps);

@@ -34,10 +34,10 @@
 //   warp 10      dQ^T += K^T (sm_scale dS)^T over all heads of the unit (K^T
 //                the MN-major view of the gathered tile, as V^T in the
 //                forward's P.V; accumulated in TMEM over the unit), which frees the block's
-//                tiles; then the block's dKV rows in column chunks
-//                (256, 256, 64 in one TMEM buffer with U = 1; with U = 2
-//                128, 64, 128, 64, 128, 64 alternating between two buffers,
-//                one chunk's MMAs overlapping the other's drain):
+//                tiles; then the block's dKV rows in column chunks taken
+//                in turn by two TMEM buffers, one chunk's MMAs overlapping
+//                the other's drain (128 x 4 and 64 with U = 1; 128, 64, 128,
+//                64, 128, 64 with U = 2):
 //                dKV = sum over halves of (sm_scale dS)^T Q + P^T [dout, 0]
 //                (M = 64 rows, K = 16 heads per half, Q and dout read as
 //                MN-major B operands).
@@ -79,22 +79,24 @@ struct BwdLayout {
   static constexpr int kTdP = 4 * N;                    // dP^T: the same
   static constexpr int kTdQ = 8 * N;                    // dQ^T: four M=128 tiles of 128 dims, the M=64 rope tile; H columns each
   static constexpr int kTdKV = U == 1 ? 256 : kTdQ + 5 * H;   // dKV chunk buffers (M=64)
-  // dKV column chunks: U = 1, three (256, 256, 64) in one TMEM buffer; U = 2,
-  // six alternating between a 128- and a 64-column buffer (128, 64, 128, 64,
-  // 128, 64), so that one chunk's MMAs run while the other buffer drains.
-  // Chunks start on 64-dim boundaries (the MN-major Q / dout swizzle atoms).
-  static constexpr int kKVChunks = U == 1 ? 3 : 6;
-  static constexpr int kKVBufs = U == 1 ? 1 : 2;
-  __device__ static constexpr int kv_col0(int c) { return U == 1 ? c * 256 : (c >> 1) * 192 + (c & 1) * 128; }
-  __device__ static constexpr int kv_width(int c) { return U == 1 ? (c < 2 ? 256 : 64) : ((c & 1) ? 64 : 128); }
-  __device__ static constexpr int kv_tmem(int c) { return kTdKV + (U == 1 ? 0 : (c & 1) * 128); }
+  // dKV column chunks in two TMEM buffers taken in turn (buffer b of the
+  // CTA's chunk g is g % 2), so that one chunk's MMAs run while the other
+  // buffer drains.  U = 1: five chunks (128 x 4, 64), two 128-column
+  // buffers; U = 2: six chunks (128, 64, 128, 64, 128, 64), a 128- and a
+  // 64-column buffer.  Chunks start on 64-dim boundaries (the MN-major
+  // Q / dout swizzle atoms).
+  static constexpr int kKVChunks = U == 1 ? 5 : 6;
+  static constexpr int kKVBufs = 2;
+  __device__ static constexpr int kv_col0(int c) { return U == 1 ? c * 128 : (c >> 1) * 192 + (c & 1) * 128; }
+  __device__ static constexpr int kv_width(int c) { return U == 1 ? (c < 4 ? 128 : 64) : ((c & 1) ? 64 : 128); }
+  __device__ static constexpr int kv_tmem(int b) { return kTdKV + b * 128; }
   static constexpr int kTmemCols = 512;
   // warp roles
   static constexpr int kQkWarp0 = 4, kSoftWarp0 = 5, kQkWarp1 = 9, kGradWarp = 10, kDrainWarp0 = 11;
   static constexpr int kThreads = 15 * 32;
 };
 static_assert(BwdLayout<1>::kTdQ + 5 * BwdLayout<1>::N <= BwdLayout<1>::kTdKV, "TMEM map");
-static_assert(BwdLayout<1>::kTdKV + 256 <= BwdLayout<1>::kTmemCols, "TMEM map");
+static_assert(BwdLayout<1>::kTdKV + 128 + 128 <= BwdLayout<1>::kTmemCols, "TMEM map");
 static_assert(BwdLayout<2>::kTdKV + 128 + 64 <= BwdLayout<2>::kTmemCols, "TMEM map");
 static_assert(BwdLayout<1>::kVOff % 1024 == 0 && BwdLayout<1>::kROff % 1024 == 0 && BwdLayout<1>::kPSOff % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
@@ -305,7 +307,7 @@ __device__ bool run_bwd_grad(const FwdParams& p, BwdMisc<U>& m, uint8_t* sbase, 
         const int wd = 512 - col0 < wq ? (512 - col0 > 0 ? 512 - col0 : 0) : wq;   // dout columns (may be none)
         const int b = chunks % L::kKVBufs;
         const uint32_t use = static_cast<uint32_t>(chunks / L::kKVBufs);
-        const uint32_t tKV = tmem + static_cast<uint32_t>(L::kv_tmem(c));
+        const uint32_t tKV = tmem + static_cast<uint32_t>(L::kv_tmem(b));
         if (!mbar_wait(smem_u32(&m.dkv_empty[b]), (use & 1u) ^ 1u, deadline, ab)) return false;
         tc_fence_after();
 #pragma unroll
@@ -428,7 +430,7 @@ __device__ bool run_bwd_drain(const FwdParams& p, BwdMisc<U>& m, uint32_t tmem) 
         tc_fence_after();
         const int col0 = L::kv_col0(c);
         const int w = L::kv_width(c);
-        const uint32_t tKV = tl + static_cast<uint32_t>(L::kv_tmem(c));
+        const uint32_t tKV = tl + static_cast<uint32_t>(L::kv_tmem(b));
         if constexpr (U == 1) {
           drain_chunk(tKV, w, dst + col0, row >= 0, half);
         } else {

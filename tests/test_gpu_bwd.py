@@ -51,6 +51,37 @@ def _check_bwd(smla, case, idx=None, kv=None, seed=0, what="", cuda_forward=Fals
     return dq.cpu().numpy(), dkv.cpu().numpy(), rq, rkv
 
 
+def _check_bwd_sampled(smla, case, dq_tokens, kv_rows, seed, what):
+    """Full-size backward (the launch the bench times) checked on sampled
+    outputs the oracle computes on its own: dq of the sampled tokens, and dkv
+    of the sampled rows, each of which sums the contributions of exactly the
+    tokens whose lists hold it (the oracle's backward over those tokens gives
+    those rows' full-problem values).  The backward reads the CUDA forward's
+    out / LSE for every token, with the oracle's (out rounded to bf16) for the
+    tokens the sampled outputs depend on."""
+    s_q, h = case.q.shape[0], case.q.shape[1]
+    dout = _dout(seed, (s_q, h, 512))
+    idx_np = case.indices.numpy()
+    listers = np.nonzero(np.isin(idx_np, kv_rows).any(axis=1))[0].tolist()
+    need = sorted(set(dq_tokens) | set(listers))
+    q_d, kv_d, idx_d = case.q.to(DEV), case.kv.to(DEV), case.indices.to(DEV)
+    out, lse = smla.sparse_mla_fwd(q_d, kv_d, idx_d, case.sm_scale)
+    ro, rl = orc.sparse_mla_fwd(case.q[need], case.kv, case.indices[need], case.sm_scale)
+    sel = torch.tensor(need, dtype=torch.int64, device=DEV)
+    out[sel] = torch.from_numpy(ro).to(torch.bfloat16).to(DEV)
+    lse[sel] = torch.from_numpy(rl).to(torch.float32).to(DEV)
+    dq, dkv = smla.sparse_mla_bwd(q_d, kv_d, idx_d, case.sm_scale, out, lse, dout.to(DEV))
+    torch.cuda.synchronize()
+    rq, rkv = orc.sparse_mla_bwd(case.q[need], case.kv, case.indices[need], case.sm_scale, dout[need])
+    bq, bkv = grad_term_bounds(case.q[need], case.kv, case.indices[need], case.sm_scale, dout[need],
+                               bf16_rounding_err)
+    pos = {t: i for i, t in enumerate(need)}
+    qi = [pos[t] for t in dq_tokens]
+    compare_grad(dq[dq_tokens].cpu().numpy(), rq[qi], bq[qi], f"{what} dq (sampled tokens)")
+    compare_grad(dkv[kv_rows].cpu().numpy(), rkv[kv_rows], bkv[kv_rows], f"{what} dkv (sampled rows)")
+    assert np.all(np.isfinite(dq.cpu().numpy())) and np.all(np.isfinite(dkv.cpu().numpy()))
+
+
 def test_bwd_small(smla):
     case = mi.prefill_case(1201, s_q=37, s_kv=420, h_q=8, topk=384)
     _check_bwd(smla, case, seed=1, what="small")
@@ -133,3 +164,20 @@ def test_bwd_varlen(smla, h_q):
                                rows_of=rows_of)
     compare_grad(dq.cpu().numpy(), rq, bq, f"varlen h={h_q} dq")
     compare_grad(dkv.cpu().numpy(), rkv, bkv, f"varlen h={h_q} dkv")
+
+
+def test_bwd_mid_prefill_config_sampled(smla):
+    """s_q = s_kv = 2119, h = 8, topk = 2048 (16-head units): sampled dq
+    tokens and dkv rows listed by 1 to ~120 tokens."""
+    g = np.random.default_rng(21)
+    toks = sorted(set([0, 1, 127, 128, 2047, 2048, 2118] + g.choice(2119, 13, replace=False).tolist()))
+    _check_bwd_sampled(smla, mi.config(2), toks, [2118, 2100, 2030, 2000], seed=21, what="config 2")
+
+
+def test_bwd_wide_head_config_sampled(smla):
+    """s_q = s_kv = 8192, h = 64, topk = 2048 (two 32-head units per token):
+    sampled dq tokens and dkv rows listed by 1 to ~170 tokens (the recent
+    window and the random tail of the list pattern)."""
+    g = np.random.default_rng(31)
+    toks = sorted(set([0, 1, 127, 128, 2047, 2048, 4095, 8191] + g.choice(8192, 16, replace=False).tolist()))
+    _check_bwd_sampled(smla, mi.config(3), toks, [8191, 8150, 8064, 7900], seed=31, what="config 3")

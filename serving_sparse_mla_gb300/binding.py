@@ -4,6 +4,13 @@ Argument marshalling only: shape/dtype/device checks, raw pointers and sizes,
 output allocation through torch.  Every step of the attention runs in the
 CUDA library; there is no fallback.  Loading fails loudly when the library
 has not been built.
+
+The C ABI receives pointers and sizes only, so the extents are checked
+here: every tensor a call reads or writes (inputs, caller-supplied outputs
+and workspaces) must sit on the call's device and hold at least the
+elements the passed sizes address, and caller-supplied outputs must have
+the output's dtype and be contiguous; otherwise ValueError is raised before
+anything is launched.
 """
 from __future__ import annotations
 
@@ -107,13 +114,46 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _need(t: torch.Tensor, dtype, name: str):
+def _on_cuda(t: torch.Tensor, name: str):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    _on_cuda(t, name)
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _device_key(device):
+    d = torch.device(device)
+    if d.type == "cuda" and d.index is None:   # "cuda" means the current device
+        return ("cuda", torch.cuda.current_device())
+    return (d.type, d.index)
+
+
+def _fits(t: Optional[torch.Tensor], need: int, name: str, device) -> None:
+    """The kernels address t as a dense array of `need` elements on `device`.
+    The C ABI sees only pointers and sizes, so extents are checked here: a
+    tensor on another device, or with fewer elements than the sizes passed
+    to the library imply, is refused before anything is launched."""
+    if t is None:
+        return
+    if _device_key(t.device) != _device_key(device):
+        raise ValueError(f"{name} is on {t.device}; the call's tensors are on {device}")
+    if t.numel() < need:
+        raise ValueError(f"{name} holds {t.numel()} elements; the call addresses {need}")
+
+
+def _given(t: Optional[torch.Tensor], dtype, name: str, need: int, device) -> None:
+    """A caller-supplied output or workspace: CUDA, dtype, contiguous, large
+    enough and on the call's device."""
+    if t is None:
+        return
+    _need(t, dtype, name)
+    _fits(t, need, name, device)
 
 
 def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_scale: float,
@@ -129,6 +169,11 @@ def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_
     for t, dt, n in ((q, torch.bfloat16, "q"), (kv, torch.bfloat16, "kv"), (indices, torch.int32, "indices")):
         _need(t, dt, n)
     d_v = 512
+    dev = q.device
+    _fits(kv, s_kv * d_qk, "kv", dev)
+    _fits(indices, s_q * topk, "indices", dev)
+    _given(out, torch.bfloat16, "out", s_q * h_q * d_v, dev)
+    _given(lse, torch.float32, "lse", s_q * h_q, dev)
     if out is None:
         out = torch.empty((s_q, h_q, d_v), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -154,6 +199,14 @@ def sparse_mla_bwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_
                      (out, torch.bfloat16, "out"), (lse, torch.float32, "lse"), (dout, torch.bfloat16, "dout")):
         _need(t, dt, n)
     d_v = 512
+    dev = q.device
+    _fits(kv, s_kv * d_qk, "kv", dev)
+    _fits(indices, s_q * topk, "indices", dev)
+    _fits(out, s_q * h_q * d_v, "out", dev)
+    _fits(lse, s_q * h_q, "lse", dev)
+    _fits(dout, s_q * h_q * d_v, "dout", dev)
+    _given(dq, torch.float32, "dq", s_q * h_q * d_qk, dev)
+    _given(dkv, torch.float32, "dkv", s_kv * d_qk, dev)
     if dq is None:
         dq = torch.empty((s_q, h_q, d_qk), dtype=torch.float32, device=q.device)
     if dkv is None:
@@ -177,6 +230,16 @@ def sparse_mla_bwd_varlen(q, kv, indices, cu_seqlens_q, cu_seqlens_kv, sm_scale,
                      (cu_seqlens_q, torch.int32, "cu_seqlens_q"), (cu_seqlens_kv, torch.int32, "cu_seqlens_kv"),
                      (out, torch.bfloat16, "out"), (lse, torch.float32, "lse"), (dout, torch.bfloat16, "dout")):
         _need(t, dt, n)
+    dev = q.device
+    _fits(kv, total_kv * d_qk, "kv", dev)
+    _fits(indices, total_q * topk, "indices", dev)
+    _fits(cu_seqlens_q, batch + 1, "cu_seqlens_q", dev)
+    _fits(cu_seqlens_kv, batch + 1, "cu_seqlens_kv", dev)
+    _fits(out, total_q * h_q * 512, "out", dev)
+    _fits(lse, total_q * h_q, "lse", dev)
+    _fits(dout, total_q * h_q * 512, "dout", dev)
+    _given(dq, torch.float32, "dq", total_q * h_q * d_qk, dev)
+    _given(dkv, torch.float32, "dkv", total_kv * d_qk, dev)
     if dq is None:
         dq = torch.empty((total_q, h_q, d_qk), dtype=torch.float32, device=q.device)
     if dkv is None:
@@ -200,6 +263,10 @@ def sparse_mla_fwd_causal(q: torch.Tensor, kv: torch.Tensor, sm_scale: float,
     for t, dt, n in ((q, torch.bfloat16, "q"), (kv, torch.bfloat16, "kv")):
         _need(t, dt, n)
     d_v = 512
+    dev = q.device
+    _fits(kv, s_kv * d_qk, "kv", dev)
+    _given(out, torch.bfloat16, "out", s_q * h_q * d_v, dev)
+    _given(lse, torch.float32, "lse", s_q * h_q, dev)
     if out is None:
         out = torch.empty((s_q, h_q, d_v), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -221,6 +288,13 @@ def sparse_mla_fwd_varlen(q, kv, indices, cu_seqlens_q, cu_seqlens_kv, sm_scale,
     for t, dt, n in ((q, torch.bfloat16, "q"), (kv, torch.bfloat16, "kv"), (indices, torch.int32, "indices"),
                      (cu_seqlens_q, torch.int32, "cu_seqlens_q"), (cu_seqlens_kv, torch.int32, "cu_seqlens_kv")):
         _need(t, dt, n)
+    dev = q.device
+    _fits(kv, total_kv * d_qk, "kv", dev)
+    _fits(indices, total_q * topk, "indices", dev)
+    _fits(cu_seqlens_q, batch + 1, "cu_seqlens_q", dev)
+    _fits(cu_seqlens_kv, batch + 1, "cu_seqlens_kv", dev)
+    _given(out, torch.bfloat16, "out", total_q * h_q * 512, dev)
+    _given(lse, torch.float32, "lse", total_q * h_q, dev)
     if out is None:
         out = torch.empty((total_q, h_q, 512), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -251,6 +325,14 @@ def sparse_mla_decode(q, kv_cache, block_table, cache_seqlens, indices, sm_scale
                      (block_table, torch.int32, "block_table"), (cache_seqlens, torch.int32, "cache_seqlens"),
                      (indices, torch.int32, "indices")):
         _need(t, dt, n)
+    dev = q.device
+    _fits(kv_cache, num_blocks * page * d_qk, "kv_cache", dev)
+    _fits(block_table, batch * max_blocks, "block_table", dev)
+    _fits(cache_seqlens, batch, "cache_seqlens", dev)
+    _fits(indices, batch * s_next * topk, "indices", dev)
+    _given(out, torch.bfloat16, "out", batch * s_next * h_q * 512, dev)
+    _given(lse, torch.float32, "lse", batch * s_next * h_q, dev)
+    _workspace(workspace, dev)
     if out is None:
         out = torch.empty((batch, s_next, h_q, 512), dtype=torch.bfloat16, device=q.device)
     if lse is None:
@@ -268,14 +350,24 @@ def sparse_mla_decode(q, kv_cache, block_table, cache_seqlens, indices, sm_scale
 
 # ---------------------------------------------------------------- DSA indexer
 
-def _seq_args(cu_seqlens_q, cu_seqlens_kv):
+def _seq_args(cu_seqlens_q, cu_seqlens_kv, device=None):
     if (cu_seqlens_q is None) != (cu_seqlens_kv is None):
         raise ValueError("give both cu_seqlens_q and cu_seqlens_kv, or neither")
     if cu_seqlens_q is None:
         return 1
     _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
     _need(cu_seqlens_kv, torch.int32, "cu_seqlens_kv")
-    return cu_seqlens_q.numel() - 1
+    batch = cu_seqlens_q.numel() - 1
+    if device is not None:
+        _fits(cu_seqlens_q, batch + 1, "cu_seqlens_q", device)
+        _fits(cu_seqlens_kv, batch + 1, "cu_seqlens_kv", device)
+    return batch
+
+
+def _workspace(workspace: Optional[torch.Tensor], device) -> None:
+    if workspace is not None:
+        _need(workspace, workspace.dtype, "workspace")
+        _fits(workspace, 0, "workspace", device)
 
 
 def _longest_kv(k_idx_rows: int, cu_seqlens_kv, max_seqlen_kv):
@@ -302,13 +394,16 @@ def dsa_indexer_scores(q_idx, k_idx, weights, cu_seqlens_q=None, cu_seqlens_kv=N
     _need(q_idx, torch.bfloat16, "q_idx")
     _need(k_idx, torch.bfloat16, "k_idx")
     _need(weights, torch.float32, "weights")
-    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv)
+    dev = q_idx.device
+    _fits(k_idx, total_kv * d_idx, "k_idx", dev)
+    _fits(weights, total_q * h_idx, "weights", dev)
+    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv, dev)
     n_rows = total_q - row0 if n_rows is None else n_rows
     stride = (_longest_kv(total_kv, cu_seqlens_kv, max_seqlen_kv) + 3) // 4 * 4
     if scores is None:
         scores = torch.full((n_rows, max(stride, 4)), float("-inf"), dtype=torch.float32, device=q_idx.device)
     else:
-        _need(scores, torch.float32, "scores")
+        _given(scores, torch.float32, "scores", max(n_rows, 0) * scores.shape[-1], dev)
     st = lib.dsa_indexer_scores(_ptr(q_idx), _ptr(k_idx), _ptr(weights), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
                                 batch, total_q, total_kv, h_idx, d_idx, row0, n_rows, skip_len, _ptr(scores),
                                 scores.shape[-1], _stream(stream))
@@ -321,15 +416,17 @@ def dsa_topk(scores, topk: int, total_q: int, total_kv: int, cu_seqlens_q=None, 
     """Lists of rows row0 .. row0+n_rows-1 from scores [n_rows, row_stride]
     fp32 -> indices [total_q, topk] int32 (only those rows written)."""
     lib = load()
-    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv)
     if scores is not None:
         _need(scores, torch.float32, "scores")
     n_rows = total_q - row0 if n_rows is None else n_rows
-    dev = scores.device if scores is not None else torch.device("cuda")
+    dev = scores.device if scores is not None else (indices.device if indices is not None else torch.device("cuda"))
+    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv, dev)
+    if scores is not None:
+        _fits(scores, max(n_rows, 0) * scores.shape[-1], "scores", dev)
     if indices is None:
         indices = torch.full((total_q, topk), -2, dtype=torch.int32, device=dev)
     else:
-        _need(indices, torch.int32, "indices")
+        _given(indices, torch.int32, "indices", total_q * topk, dev)
     stride = scores.shape[-1] if scores is not None else 1
     st = lib.dsa_topk(_ptr(scores), stride, _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), batch, total_q, total_kv,
                       row0, n_rows, topk, _ptr(indices), _stream(stream))
@@ -353,12 +450,16 @@ def dsa_indexer_topk(q_idx, k_idx, weights, topk: int, cu_seqlens_q=None, cu_seq
     _need(q_idx, torch.bfloat16, "q_idx")
     _need(k_idx, torch.bfloat16, "k_idx")
     _need(weights, torch.float32, "weights")
-    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv)
+    dev = q_idx.device
+    _fits(k_idx, total_kv * d_idx, "k_idx", dev)
+    _fits(weights, total_q * h_idx, "weights", dev)
+    batch = _seq_args(cu_seqlens_q, cu_seqlens_kv, dev)
     longest = _longest_kv(total_kv, cu_seqlens_kv, max_seqlen_kv)
     if indices is None:
         indices = torch.empty((total_q, topk), dtype=torch.int32, device=q_idx.device)
     else:
-        _need(indices, torch.int32, "indices")
+        _given(indices, torch.int32, "indices", total_q * topk, dev)
+    _workspace(workspace, dev)
     if workspace is None:
         need = lib.dsa_indexer_workspace_size(total_q, longest, topk)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_idx.device)
@@ -378,7 +479,13 @@ def _paged_args(q_idx, k_cache, weights, block_table, cache_seqlens):
     _need(cache_seqlens, torch.int32, "cache_seqlens")
     batch, s_next, h_idx, d_idx = q_idx.shape
     num_blocks, page = k_cache.shape[0], k_cache.shape[1]
-    return batch, s_next, h_idx, d_idx, page, block_table.shape[1], num_blocks
+    max_blocks = block_table.shape[1]
+    dev = q_idx.device
+    _fits(k_cache, num_blocks * page * d_idx, "k_cache", dev)
+    _fits(weights, batch * s_next * h_idx, "weights", dev)
+    _fits(block_table, batch * max_blocks, "block_table", dev)
+    _fits(cache_seqlens, batch, "cache_seqlens", dev)
+    return batch, s_next, h_idx, d_idx, page, max_blocks, num_blocks
 
 
 def dsa_indexer_scores_paged(q_idx, k_cache, weights, block_table, cache_seqlens, max_seqlen_kv: int,
@@ -395,6 +502,8 @@ def dsa_indexer_scores_paged(q_idx, k_cache, weights, block_table, cache_seqlens
     stride = (int(max_seqlen_kv) + 3) // 4 * 4
     if scores is None:
         scores = torch.full((n_rows, max(stride, 4)), float("-inf"), dtype=torch.float32, device=q_idx.device)
+    else:
+        _given(scores, torch.float32, "scores", max(n_rows, 0) * scores.shape[-1], q_idx.device)
     st = lib.dsa_indexer_scores_paged(_ptr(q_idx), _ptr(k_cache), _ptr(weights), _ptr(block_table),
                                       _ptr(cache_seqlens), batch, s_next, h_idx, d_idx, page, max_blocks, num_blocks,
                                       row0, n_rows, skip_len, _ptr(scores), scores.shape[-1], _stream(stream))
@@ -415,7 +524,8 @@ def dsa_indexer_topk_paged(q_idx, k_cache, weights, block_table, cache_seqlens, 
     if indices is None:
         indices = torch.empty((batch, s_next, topk), dtype=torch.int32, device=q_idx.device)
     else:
-        _need(indices, torch.int32, "indices")
+        _given(indices, torch.int32, "indices", batch * s_next * topk, q_idx.device)
+    _workspace(workspace, q_idx.device)
     if workspace is None:
         need = lib.dsa_indexer_workspace_size(batch * s_next, int(max_seqlen_kv), topk)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_idx.device)

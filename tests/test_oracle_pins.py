@@ -314,6 +314,43 @@ def test_decode_poisoned_slots_never_read():
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
 
 
+def test_decode_invalid_pages_are_masked():
+    """Masking beyond -1 on the paged layout: an index whose page lies past
+    the block table's width, or whose table entry falls outside
+    [0, num_blocks), counts as masked.  Pinned against the plain forward over
+    each request's linearised cache with those entries replaced by -1 on the
+    host (placeholder rows of zeros where a page is missing)."""
+    c = _small_decode(107)
+    nb, page = c.kv_cache.shape[0], c.page_size
+    width = 6                                           # pages 0..5: positions >= 96 have no page
+    bt = c.block_table[:, :width].clone()
+    bt[0, 1] = -5                                       # outside the pool, below
+    bt[1, 2] = nb + 3                                   # outside the pool, above
+    out, lse = orc.sparse_mla_decode(c.q, c.kv_cache, bt, c.cache_seqlens, c.indices, c.sm_scale, page, DV)
+    out = out.reshape(c.batch, c.s_next, c.h_q, DV)
+    lse = lse.reshape(c.batch, c.s_next, c.h_q)
+    masked_any = False
+    for b in range(c.batch):
+        L = int(c.cache_seqlens[b])
+        lin = torch.zeros((L, D), dtype=c.kv_cache.dtype)
+        good = torch.zeros(L, dtype=torch.bool)
+        for pg in range(min(width, (L + page - 1) // page)):
+            e = int(bt[b, pg])
+            if 0 <= e < nb:
+                n = min(page, L - pg * page)
+                lin[pg * page: pg * page + n] = c.kv_cache[e, :n]
+                good[pg * page: pg * page + n] = True
+        idx = c.indices[b].clone()
+        inside = (idx >= 0) & (idx < L)
+        bad = inside & ~good[idx.clamp(0, L - 1).long()]
+        masked_any |= bool(bad.any())
+        idx[bad] = -1
+        o2, l2 = orc.sparse_mla_fwd(c.q[b], lin, idx, c.sm_scale, DV)
+        _close(out[b], o2)
+        _close(lse[b], l2)
+    assert masked_any
+
+
 def test_valid_count_bruteforce():
     idx = torch.tensor([[-1, 0, 3, 3, 9], [10, -2, -1, -1, 4]], dtype=torch.int32)
     assert orc.valid_count_dense(idx, 10).tolist() == [4, 1]

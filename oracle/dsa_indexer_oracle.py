@@ -195,10 +195,20 @@ def topk_rows(scores: np.ndarray, lens: Sequence[int], topk: int) -> np.ndarray:
 def linearise_keys(k_cache, block_table, seqlen: int, page: int) -> np.ndarray:
     """The keys of one request in position order: position s is row s % page
     of physical block block_table[s // page] (a paged key cache laid out like
-    the forward's paged KV cache)."""
+    the forward's paged KV cache).  A position whose page lies past the
+    table, or whose table entry is outside [0, num_blocks), has a zero key
+    (the library's stated convention for the paged indexer; such a cache is
+    a caller error the kernel must not read past)."""
     kc = _f64(k_cache)
     bt = [int(x) for x in block_table]
-    rows = [kc[bt[s // page], s % page] for s in range(seqlen)]
+    zero = np.zeros(kc.shape[-1])
+
+    def key(s):
+        pg = s // page
+        if pg >= len(bt) or not 0 <= bt[pg] < kc.shape[0]:
+            return zero
+        return kc[bt[pg], s % page]
+    rows = [key(s) for s in range(seqlen)]
     return np.stack(rows) if rows else np.zeros((0, kc.shape[-1]))
 
 

@@ -240,13 +240,35 @@ def pin_paged_unused_slots_never_read():
     assert (la >= 0).sum() > 0
 
 
+def pin_paged_invalid_pages_read_as_zero_keys():
+    """A page past the block table's width, or a table entry outside the
+    pool, gives zero keys at its positions: the dense oracle over keys built
+    by hand with zero rows there."""
+    c = mi.indexer_paged_case(86, 1, 4, 300, 300, h_idx=8, d_idx=32, topk=40, spare_pages=0, poison=False)
+    nb, page, L = c.k_cache.shape[0], c.page, 300
+    bt = c.block_table[:, :4].clone()          # positions 256 .. 299 have no page
+    bt[0, 1] = -2
+    bt[0, 2] = nb + 7
+    keys = torch.zeros((L, c.k_cache.shape[-1]))
+    for pg in range(4):
+        e = int(bt[0, pg])
+        if 0 <= e < nb:
+            n = min(page, L - pg * page)
+            keys[pg * page: pg * page + n] = c.k_cache[e, :n].float()
+    got = ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, bt, c.cache_seqlens, 40, c.page)
+    ref = ido.dsa_indices(c.q_idx[0], keys, c.weights[0], 40)
+    np.testing.assert_array_equal(got, ref)
+    assert not np.array_equal(got, ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, c.block_table,
+                                                          c.cache_seqlens, 40, c.page))
+
+
 PINS = [pin_worked_example_scores, pin_worked_example_lists, pin_relu_floor,
         pin_weight_homogeneity_additivity, pin_selection_properties_with_ties,
         pin_selection_matches_torch_topk, pin_visibility_closed_forms,
         pin_scores_selection_consistent, pin_varlen_matches_dense_per_sequence,
         pin_short_rows_reproduce_causal_forward, pin_paged_identity_table_is_dense,
         pin_paged_matches_packed_on_linearised_keys, pin_paged_page_shuffle_invariance,
-        pin_paged_unused_slots_never_read]
+        pin_paged_unused_slots_never_read, pin_paged_invalid_pages_read_as_zero_keys]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -350,6 +372,6 @@ def test_indexer_pins_catch_planted_mistake(monkeypatch, name, fn):
     for pin in PINS:
         try:
             pin()
-        except AssertionError:
+        except (AssertionError, IndexError):     # a pin the mistake breaks, or one it crashes
             failed += 1
     assert failed >= 1, f"no pin caught the planted mistake {fn.__name__}"

@@ -325,8 +325,9 @@ sparse_mla_status_t dsa_indexer_topk(const void* q_idx, const void* k_idx, const
  * cache_seqlens int32 [batch].  q_idx bf16 [batch, s_next, h_idx, d_idx],
  * weights fp32 [batch, s_next, h_idx]; rows are numbered b * s_next + j.
  * page_size must be 64 (else SPARSE_MLA_ERR_UNSUPPORTED_SHAPE).  Pages past a
- * request's length are never used in a score; a page id outside
- * [0, num_blocks) reads as zeros.  Otherwise as dsa_indexer_scores /
+ * request's length are never used in a score; a visible position whose page
+ * index is at or past max_blocks, or whose page id is outside
+ * [0, num_blocks), has a zero key (score 0).  Otherwise as dsa_indexer_scores /
  * dsa_indexer_topk (row_stride / max_seqlen_kv: at least the longest
  * cache_seqlens).
  */

@@ -296,6 +296,43 @@ def step_flops(case) -> float:
     return mi.nominal_flops(n_tok, h, case.indices.shape[-1])
 
 
+METRICS = {"fwd": "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)",
+           "bwd": "sparse-MLA bwd TFLOP/s at topk=2048 (nominal FLOPs)",
+           "causal": "indices-free causal MLA fwd TFLOP/s (every causal position)"}
+MODE_SUFFIX = {"fwd": "", "bwd": " (backward: dq, dkv)", "causal": " (indices-free causal mode)"}
+
+
+def attention_mode(args) -> str:
+    if args.causal and args.bwd:
+        raise SystemExit("--causal and --bwd are separate modes")
+    return "causal" if args.causal else ("bwd" if args.bwd else "fwd")
+
+
+def check_mode(case, mode: str) -> None:
+    if mode == "causal" and (hasattr(case, "kv_cache") or hasattr(case, "cu_seqlens_q")):
+        raise SystemExit("--causal needs a dense prefill config (1-3)")
+    if mode == "bwd" and hasattr(case, "kv_cache"):
+        raise SystemExit("--bwd needs a prefill config (1-4)")
+
+
+def causal_entries(case) -> int:
+    """Positions the indices-free causal mode attends to (queries are the last
+    s_q of the s_kv positions)."""
+    s_q, s_kv = case.q.shape[0], case.kv.shape[0]
+    return sum(max(0, min(s_kv, t + s_kv - s_q + 1)) for t in range(s_q))
+
+
+def mode_flops(case, mode: str) -> float:
+    """FLOPs of one step: nominal 2 s_q h topk (576 + 512) for the forward,
+    2 s_q h topk (3 576 + 2 512) for the backward (S recompute, dP, dQ, dK,
+    dV), 2 h (576 + 512) per attended position for the causal mode."""
+    if mode == "causal":
+        return 2.0 * case.q.shape[1] * 1088 * causal_entries(case)
+    if mode == "bwd":
+        return 2.0 * case.q.shape[0] * case.q.shape[1] * case.indices.shape[-1] * (3 * 576 + 2 * 512)
+    return step_flops(case)
+
+
 def workload_name(case, config: int, tokens=None) -> str:
     if tokens is not None:
         return (f"{'wide-head' if config == 3 else 'dense'} prefill s_q=s_kv={tokens} h_q={case.q.shape[1]} "
@@ -314,18 +351,49 @@ def _workload_name(config: int) -> str:
 
 # ----------------------------------------------------------------------------- oracle on host cores
 
-def _oracle_worker_init(config: int):
+def bwd_dout(case, config: int):
+    """The upstream gradient both arms use for the backward: seeded N(0,1)
+    rounded to bf16, shaped like the forward's output."""
+    import torch
+    g = torch.Generator().manual_seed(2000 + config)
+    return torch.randn((case.q.shape[0], case.q.shape[1], 512), generator=g).to(torch.bfloat16)
+
+
+def _oracle_worker_init(config: int, mode: str = "fwd"):
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[v] = "1"
-    global _W_CASE
+    global _W_CASE, _W_MODE, _W_DOUT
     _W_CASE = workload(config)
+    _W_MODE = mode
+    _W_DOUT = bwd_dout(_W_CASE, config) if mode == "bwd" else None
+
+
+def _oracle_bwd_sample(orc, c, dout, tokens):
+    """The oracle backward over a token sample: the sampled tokens' own
+    gradients (dkv gets their contributions only)."""
+    import torch
+    if len(tokens) == 0:
+        return
+    sel = torch.tensor(list(tokens), dtype=torch.int64)
+    if hasattr(c, "cu_seqlens_q"):
+        cu = c.cu_seqlens_q.tolist()
+        # the sample's sequences keep their order: count its tokens per sequence
+        cu_s = [sum(1 for t in tokens if t < end) for end in cu]
+        orc.sparse_mla_bwd_varlen(c.q[sel], c.kv, c.indices[sel], torch.tensor(cu_s, dtype=torch.int32),
+                                  c.cu_seqlens_kv, c.sm_scale, dout[sel])
+    else:
+        orc.sparse_mla_bwd(c.q[sel], c.kv, c.indices[sel], c.sm_scale, dout[sel])
 
 
 def _oracle_worker(tokens):
     from oracle import sparse_mla_oracle as orc
     c = _W_CASE
     t0 = time.perf_counter()
-    if hasattr(c, "kv_cache"):
+    if _W_MODE == "causal":
+        orc.causal_mla_fwd(c.q, c.kv, c.sm_scale, tokens=tokens)
+    elif _W_MODE == "bwd":
+        _oracle_bwd_sample(orc, c, _W_DOUT, tokens)
+    elif hasattr(c, "kv_cache"):
         toks = [(t // c.s_next, t % c.s_next) for t in tokens]
         orc.sparse_mla_decode(c.q, c.kv_cache, c.block_table, c.cache_seqlens, c.indices, c.sm_scale,
                               c.page_size, tokens=toks)
@@ -339,13 +407,15 @@ def _oracle_worker(tokens):
 
 class OraclePool:
     """The oracle, unchanged, sharded by token over a spawn process pool with
-    one single-threaded worker per host core."""
+    one single-threaded worker per host core.  mode: "fwd" (the forward of
+    the workload's layout), "causal" (the indices-free causal forward) or
+    "bwd" (the backward)."""
 
-    def __init__(self, config: int, cores: int):
+    def __init__(self, config: int, cores: int, mode: str = "fwd"):
         import multiprocessing as mp
         self.cores = cores
         ctx = mp.get_context("spawn")
-        self.pool = ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(config,))
+        self.pool = ctx.Pool(cores, initializer=_oracle_worker_init, initargs=(config, mode))
         self.pool.map(_oracle_worker, [[] for _ in range(cores)])   # wait for every worker
 
     def run(self, tokens):
@@ -408,12 +478,16 @@ def run_reference(args, rank, world):
         return 0
     if args.indexer:
         return run_reference_indexer(args)
+    if args.tokens is not None:
+        raise SystemExit("--tokens is a profiling size for the CUDA arm only")
+    mode = attention_mode(args)
     case = workload(args.config)
+    check_mode(case, mode)
     cores = os.cpu_count() or 1
-    pool = OraclePool(args.config, cores)
+    pool = OraclePool(args.config, cores, mode)
     toks, sample = oracle_sample(case, args.config)
     n_tok = case.batch * case.s_next if hasattr(case, "kv_cache") else case.q.shape[0]
-    flops = step_flops(case) * len(toks) / n_tok
+    flops = mode_flops(case, mode) * len(toks) / n_tok
     for _ in range(args.warmup):
         pool.run(toks)
     times = [pool.run(toks) for _ in range(args.steps)]
@@ -421,11 +495,11 @@ def run_reference(args, rank, world):
     total = sum(times)
     value = flops * args.steps / total / 1e12
     line = {
-        "impl": "reference", "metric": "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)",
+        "impl": "reference", "metric": METRICS[mode],
         "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_name(case, args.config), "sample": sample,
+        "config": {"workload": workload_name(case, args.config) + MODE_SUFFIX[mode], "sample": sample,
                    "l2": "n/a (CPU)", "seed": 1000 + args.config},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -446,28 +520,18 @@ def run_ours(args, rank, world, dist):
 
     # The oracle pool (spawn) starts before the first GPU work.
     pool = None
-    if rank == 0 and not args.no_cpu_baseline and not args.causal and not args.bwd and args.tokens is None:
-        pool = OraclePool(args.config, os.cpu_count() or 1)
+    if rank == 0 and not args.no_cpu_baseline and args.tokens is None:
+        pool = OraclePool(args.config, os.cpu_count() or 1, attention_mode(args))
 
     case = workload(args.config, args.tokens)
     stream = torch.cuda.current_stream(dev)
     is_decode = hasattr(case, "kv_cache")
     is_varlen = hasattr(case, "cu_seqlens_q")
-    if args.causal and (is_decode or is_varlen):
-        raise SystemExit("--causal needs a dense prefill config (1-3)")
-    if args.bwd and is_decode:
-        raise SystemExit("--bwd needs a prefill config (1-4)")
-    if args.causal and args.bwd:
-        raise SystemExit("--causal and --bwd are separate modes")
+    mode = attention_mode(args)
+    check_mode(case, mode)
     n_tok = case.batch * case.s_next if is_decode else case.q.shape[0]
-    flops = step_flops(case)
-    valid = valid_entries(case)
-    if args.causal:
-        s_q, s_kv = case.q.shape[0], case.kv.shape[0]
-        valid = sum(max(0, min(s_kv, t + s_kv - s_q + 1)) for t in range(s_q))
-        flops = 2.0 * case.q.shape[1] * 1088 * valid
-    if args.bwd:
-        flops = 2.0 * case.q.shape[0] * case.q.shape[1] * case.indices.shape[-1] * (3 * 576 + 2 * 512)
+    flops = mode_flops(case, mode)
+    valid = causal_entries(case) if args.causal else valid_entries(case)
     kv_bytes = valid * (KV_ROW_BYTES + (2304 if args.bwd else 0))
 
     # device-resident inputs
@@ -482,9 +546,7 @@ def run_ours(args, rank, world, dist):
                       cuk=d(case.cu_seqlens_kv))
         o_fwd, l_fwd = smla.sparse_mla_fwd_varlen(inputs["q"], inputs["kv"], inputs["idx"], inputs["cuq"],
                                                   inputs["cuk"], case.sm_scale)
-        g_do = torch.Generator().manual_seed(2000 + args.config)
-        inputs.update(out=o_fwd, lse=l_fwd,
-                      dout=torch.randn(o_fwd.shape, generator=g_do).to(torch.bfloat16).to(dev))
+        inputs.update(out=o_fwd, lse=l_fwd, dout=bwd_dout(case, args.config).to(dev))
         dq_buf = torch.empty(case.q.shape, dtype=torch.float32, device=dev)
         dkv_buf = torch.empty((case.kv.shape[0], 576), dtype=torch.float32, device=dev)
     elif is_varlen:
@@ -495,9 +557,7 @@ def run_ours(args, rank, world, dist):
     elif args.bwd:
         inputs = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices))
         o_fwd, l_fwd = smla.sparse_mla_fwd(inputs["q"], inputs["kv"], inputs["idx"], case.sm_scale)
-        g_do = torch.Generator().manual_seed(2000 + args.config)
-        inputs.update(out=o_fwd, lse=l_fwd,
-                      dout=torch.randn(o_fwd.shape, generator=g_do).to(torch.bfloat16).to(dev))
+        inputs.update(out=o_fwd, lse=l_fwd, dout=bwd_dout(case, args.config).to(dev))
         dq_buf = torch.empty(case.q.shape, dtype=torch.float32, device=dev)
         dkv_buf = torch.empty((case.kv.shape[0], 576), dtype=torch.float32, device=dev)
     else:
@@ -609,7 +669,9 @@ def run_ours(args, rank, world, dist):
                     "frac": achieved / p_bw, "traffic": None if args.causal else profiled_traffic(args.config, "bwd" if args.bwd else "fwd"),
                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                     "algorithmic_bytes_per_launch": kv_bytes,
-                    "note": "achieved = valid entries x 1152 B / mean launch time (cold L2)"}
+                    "note": ("achieved = valid entries x (1152 B gathered + 2304 B of fp32 dkv reduction) / mean "
+                             "launch time (cold L2)" if args.bwd else
+                             "achieved = valid entries x 1152 B / mean launch time (cold L2)")}
     else:
         achieved = flops / (fwd_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": p_tf, "unit": "TFLOP/s",
@@ -625,15 +687,11 @@ def run_ours(args, rank, world, dist):
         pool.close()
 
     line = {
-        "metric": ("indices-free causal MLA fwd TFLOP/s (every causal position)" if args.causal
-                   else "sparse-MLA bwd TFLOP/s at topk=2048 (nominal FLOPs)" if args.bwd
-                   else "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)"),
+        "metric": METRICS[mode],
         "value": whole_job_tflops(flops, args.steps, world, total_ms), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(case, args.config, args.tokens)
-                   + (" (indices-free causal mode)" if args.causal else "")
-                   + (" (backward: dq, dkv)" if args.bwd else ""),
+        "config": {"workload": workload_name(case, args.config, args.tokens) + MODE_SUFFIX[mode],
                    "seed": 1000 + args.config,
                    "l2": "256 MB buffer written before every timed step (cold L2)",
                    "parallelism": f"replicas x{world}"},

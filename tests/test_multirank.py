@@ -49,3 +49,24 @@ def test_whole_job_value_counts_every_replica():
     assert two == pytest.approx(2 * one)
     assert one == pytest.approx(75.5e9 * 10 / 5e-3 / 1e12)
     assert bench.max_over_ranks([1.0, 2.0], None) == [1.0, 2.0]
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """bench.py --impl reference launched as the N>1 bench is (torchrun, two
+    ranks): rank 0 alone times the oracle and prints one JSON line; the other
+    rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           "bench.py", "--impl", "reference", "--gpus", "2", "--config", "1", "--steps", "1", "--warmup", "3"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"

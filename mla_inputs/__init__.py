@@ -327,6 +327,47 @@ def config(n: int, seed: Optional[int] = None):
     raise ValueError(n)
 
 
+# --------------------------------------------------------------------------
+# FP8 KV cache (the cache writer's quantization; the decode reads it)
+# --------------------------------------------------------------------------
+
+FP8_SLOT_BYTES = 656   # 512 e4m3 codes, 4 fp32 tile scales, 64 bf16 rope values
+
+
+def quantize_fp8_slots(latent: torch.Tensor, pow2_scales: bool = False) -> torch.Tensor:
+    """Latent rows [..., 576] -> FP8 cache slots uint8 [..., 656] in the
+    layout of DeepSeek-V3.2's FP8 sparse-decode cache: the first 512 values
+    as float8 e4m3 codes in four tiles of 128, each with an fp32 scale
+    amax / 448 (rounded up to a power of two with ``pow2_scales``), then the
+    scales, then the last 64 values as bf16.  The codes come from torch's
+    float8_e4m3fn conversion (round to nearest even).  A row holding NaN
+    (a poisoned slot) gets NaN codes, scales and rope values."""
+    lead = latent.shape[:-1]
+    x = latent.float().reshape(-1, D_QK)
+    v = x[:, :512].reshape(-1, 4, 128)
+    amax = v.abs().amax(dim=-1)
+    scale = amax / 448.0
+    scale = torch.where(scale > 0, scale, torch.ones_like(scale))
+    if pow2_scales:
+        scale = torch.exp2(torch.ceil(torch.log2(scale)))
+    scale = torch.where(torch.isnan(amax), torch.full_like(scale, float("nan")), scale)
+    codes = (v / scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(-1, 512)
+    sc = scale.to(torch.float32).contiguous().view(torch.uint8).reshape(-1, 16)
+    rope = x[:, 512:].to(torch.bfloat16).contiguous().view(torch.uint8).reshape(-1, 128)
+    return torch.cat([codes, sc, rope], dim=1).reshape(*lead, FP8_SLOT_BYTES).contiguous()
+
+
+def decode_case_fp8(seed: int, batch: int, s_next: int, h_q: int, lo: int, hi: int, topk: int = TOPK,
+                    page: int = PAGE, spare_pages: int = 64, pow2_scales: bool = False, name: str = ""):
+    """A paged decode case whose cache is FP8: decode_case's structure
+    (contexts, shuffled pool, index lists, NaN in every slot no list picks),
+    its latent rows written as FP8 slots.  Returns (case, cache_u8 [num_blocks,
+    page, 656])."""
+    c = decode_case(seed, batch, s_next, h_q, lo, hi, topk=topk, page=page, spare_pages=spare_pages,
+                    name=name or f"decode_fp8_b{batch}_s{s_next}_h{h_q}")
+    return c, quantize_fp8_slots(c.kv_cache, pow2_scales=pow2_scales)
+
+
 def nominal_flops(s_q: int, h_q: int, topk: int = TOPK, d_qk: int = D_QK, d_v: int = D_V) -> float:
     """2*s_q*h_q*topk*(d_qk+d_v): the workload's nominal FLOP count."""
     return 2.0 * s_q * h_q * topk * (d_qk + d_v)

@@ -68,6 +68,9 @@ def parse_args():
     ap.add_argument("--tokens", type=int, default=None,
                     help="profiling aid for the dense prefill configs (1-3): s_q = s_kv = TOKENS with the "
                          "config's heads, list pattern and seed (a smaller case of the same kernel)")
+    ap.add_argument("--no-all-configs", action="store_true",
+                    help="skip the per-workload records of all five forward workloads that the default forward "
+                         "run adds under the key 'configs'")
     ap.add_argument("--clock-log", default=None,
                     help="directory for the nvidia-smi clock CSV of the run (default: the system temp dir)")
     return ap.parse_args()
@@ -349,6 +352,20 @@ def _workload_name(config: int) -> str:
     return names[config] + " d_qk=576 d_v=512 topk=2048 bf16"
 
 
+def h_q_of(case) -> int:
+    return case.h_q if hasattr(case, "kv_cache") else case.q.shape[1]
+
+
+def run_config(case, args, mode: str, world: int) -> dict:
+    """The `config` object of both arms' lines (identical for the same
+    workload and mode): the workload, its seed, the L2 rule of the GPU arm's
+    timing and the parallelism."""
+    return {"workload": workload_name(case, args.config, args.tokens) + MODE_SUFFIX[mode],
+            "seed": 1000 + args.config,
+            "l2": "256 MB buffer written before every timed step (cold L2)",
+            "parallelism": f"replicas x{world}"}
+
+
 # ----------------------------------------------------------------------------- oracle on host cores
 
 def bwd_dout(case, config: int):
@@ -443,7 +460,18 @@ def oracle_sample(case, config: int):
 
 # ----------------------------------------------------------------------------- arms
 
-def run_reference_indexer(args):
+def indexer_config(args, world: int) -> dict:
+    """The `config` object of both arms' indexer lines (identical)."""
+    name = {1: "tiny prefill s_q=s_kv=64", 2: "mid prefill s_q=s_kv=2119", 3: "prefill s_q=s_kv=8192",
+            4: "packed varlen prefill 16384 tokens (8192,4096,2048,1024,1024)",
+            5: "paged decode 16 requests x 6 MTP rows, contexts U[4096,32768], page 64"}[args.config]
+    return {"workload": f"DSA indexer {name} h_idx=64 d_idx=128 topk=2048 (lists for the sparse-MLA "
+                        f"forward; one logits chunk)", "seed": 1000 + args.config,
+            "l2": "256 MB buffer written before every timed step (cold L2)",
+            "parallelism": f"replicas x{world}"}
+
+
+def run_reference_indexer(args, world=1):
     case = indexer_workload(args.config)
     info = indexer_rows(case)
     flops, _, scored_pos, _ = indexer_costs(case, info)
@@ -463,8 +491,8 @@ def run_reference_indexer(args):
         "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"DSA indexer, token shape of config {args.config}", "sample": sample,
-                   "l2": "n/a (CPU)", "seed": 1000 + args.config},
+        "config": indexer_config(args, world),
+        "timing": "host wall clock of the oracle over the sample on the host cores (no L2 flush applies)",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -477,7 +505,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     if args.indexer:
-        return run_reference_indexer(args)
+        return run_reference_indexer(args, world)
     if args.tokens is not None:
         raise SystemExit("--tokens is a profiling size for the CUDA arm only")
     mode = attention_mode(args)
@@ -499,14 +527,131 @@ def run_reference(args, rank, world):
         "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_name(case, args.config) + MODE_SUFFIX[mode], "sample": sample,
-                   "l2": "n/a (CPU)", "seed": 1000 + args.config},
+        "config": run_config(case, args, mode, world),
+        "timing": "host wall clock of the oracle over the sample on the host cores (no L2 flush applies)",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def fwd_runner(smla, case, dev, stream):
+    """Device-resident inputs of one forward workload and a closure that runs
+    its forward once (dense, packed or paged, as the workload's layout is);
+    returns (closure, launches per call, device tensors to free)."""
+    d = lambda t: t.to(dev)
+    if hasattr(case, "kv_cache"):
+        inp = dict(q=d(case.q), kv=d(case.kv_cache), bt=d(case.block_table), sl=d(case.cache_seqlens),
+                   idx=d(case.indices))
+        need = smla.decode_workspace_size(case.batch, case.s_next, case.h_q, case.indices.shape[-1])
+        ws = torch_empty_bytes(max(1, need), dev)
+        out = torch_empty_out((case.batch, case.s_next, case.h_q), dev)
+
+        def call():
+            smla.sparse_mla_decode(inp["q"], inp["kv"], inp["bt"], inp["sl"], inp["idx"], case.sm_scale,
+                                   case.page_size, workspace=ws, out=out[0], lse=out[1], stream=stream)
+        return call, (2 if need > 0 else 1), [inp, ws, out]
+    inp = dict(q=d(case.q), kv=d(case.kv), idx=d(case.indices))
+    out = torch_empty_out((case.q.shape[0], case.q.shape[1]), dev)
+    if hasattr(case, "cu_seqlens_q"):
+        inp.update(cuq=d(case.cu_seqlens_q), cuk=d(case.cu_seqlens_kv))
+
+        def call():
+            smla.sparse_mla_fwd_varlen(inp["q"], inp["kv"], inp["idx"], inp["cuq"], inp["cuk"], case.sm_scale,
+                                       out=out[0], lse=out[1], stream=stream)
+    else:
+        def call():
+            smla.sparse_mla_fwd(inp["q"], inp["kv"], inp["idx"], case.sm_scale, out=out[0], lse=out[1],
+                                stream=stream)
+    return call, 1, [inp, out]
+
+
+def torch_empty_bytes(n, dev):
+    import torch
+    return torch.empty(n, dtype=torch.uint8, device=dev)
+
+
+def torch_empty_out(lead, dev):
+    """(out [*lead, 512] bf16, lse [*lead] fp32) on dev."""
+    import torch
+    return (torch.empty((*lead, 512), dtype=torch.bfloat16, device=dev),
+            torch.empty(lead, dtype=torch.float32, device=dev))
+
+
+FP8_SLOT_BYTES = 656
+
+
+def fp8_runner(smla, case, dev, stream):
+    """The paged-decode workload with its cache written as FP8 slots (the
+    656-byte layout of sparse_mla_decode_fp8): device inputs and a closure
+    that runs one FP8 decode."""
+    import mla_inputs as mi
+    d = lambda t: t.to(dev)
+    inp = dict(q=d(case.q), kv=d(mi.quantize_fp8_slots(case.kv_cache)), bt=d(case.block_table),
+               sl=d(case.cache_seqlens), idx=d(case.indices))
+    need = smla.decode_workspace_size(case.batch, case.s_next, case.h_q, case.indices.shape[-1])
+    ws = torch_empty_bytes(max(1, need), dev)
+    out = torch_empty_out((case.batch, case.s_next, case.h_q), dev)
+
+    def call():
+        smla.sparse_mla_decode_fp8(inp["q"], inp["kv"], inp["bt"], inp["sl"], inp["idx"], case.sm_scale,
+                                   case.page_size, workspace=ws, out=out[0], lse=out[1], stream=stream)
+    return call, (2 if need > 0 else 1), [inp, ws, out]
+
+
+def config_records(smla, dev, stream, steps: int, warmup: int, flush, peaks) -> dict:
+    """Per-workload forward records for all five workloads: the time per call
+    with a cold L2 (mean over `steps` calls, CUDA events on the launching
+    stream, a 256 MB buffer written before each) and with a warm L2 (median),
+    the per-shape roofline (max of the nominal-FLOP term at the measured bf16
+    peak and the valid gathered-KV bytes at the measured HBM copy bandwidth),
+    the fraction of it reached, the tensor-only fraction (FLOP term / time),
+    and the profiled DRAM traffic of the launch when the committed ncu summary
+    matches the current kernel sources."""
+    import torch
+    p_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    p_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    recs = {}
+    for c in (1, 2, 3, 4, 5, "5_fp8"):
+        fp8 = c == "5_fp8"
+        case = workload(5 if fp8 else c)
+        call, launches, keep = (fp8_runner if fp8 else fwd_runner)(smla, case, dev, stream)
+        row_bytes = FP8_SLOT_BYTES if fp8 else KV_ROW_BYTES
+        for _ in range(max(3, warmup)):
+            call()
+        torch.cuda.synchronize(dev)
+        cold, warm = [], []
+        for i in range(2 * steps):
+            if i < steps:
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            (cold if i < steps else warm).append((a, b))
+        torch.cuda.synchronize(dev)
+        us = statistics.mean(a.elapsed_time(b) for a, b in cold) * 1e3
+        us_warm = statistics.median(a.elapsed_time(b) for a, b in warm) * 1e3
+        valid = valid_entries(case)
+        flops = step_flops(case)
+        t_flop = flops / (p_tf * 1e12) * 1e6
+        t_byte = valid * row_bytes / (p_bw * 1e9) * 1e6
+        roof = max(t_flop, t_byte)
+        recs[str(c)] = {
+            "workload": (_workload_name(5) + ", FP8 cache (656-byte slots)") if fp8 else _workload_name(c),
+            "us_per_call": us, "us_per_call_warm_l2": us_warm,
+            "roofline_us": roof, "bound": "hbm" if t_byte >= t_flop else "tensor",
+            "roofline_frac": roof / us, "tensor_only_frac": t_flop / us,
+            "tflops": flops / (us * 1e-6) / 1e12, "gathered_kv_GBps": valid * row_bytes / (us * 1e-6) / 1e9,
+            "gathered_row_bytes": row_bytes,
+            "valid_entries": valid, "nominal_flops": flops, "launches_per_call": launches,
+            "traffic": profiled_traffic(c, "fwd"),
+        }
+        del keep, call
+        torch.cuda.empty_cache()
+    return recs
 
 
 def run_ours(args, rank, world, dist):
@@ -532,7 +677,11 @@ def run_ours(args, rank, world, dist):
     n_tok = case.batch * case.s_next if is_decode else case.q.shape[0]
     flops = mode_flops(case, mode)
     valid = causal_entries(case) if args.causal else valid_entries(case)
-    kv_bytes = valid * (KV_ROW_BYTES + (2304 if args.bwd else 0))
+    # The HBM roofline counts the gathered KV rows; the backward's fp32 dkv
+    # reductions (576 x 4 B per valid entry and 32-head unit, L2-resident
+    # red.global.add) are reported beside it, not as HBM bytes.
+    kv_bytes = valid * KV_ROW_BYTES
+    red_bytes = valid * 2304 * (2 if h_q_of(case) > 16 else 1) if args.bwd else 0
 
     # device-resident inputs
     d = lambda t: t.to(dev)
@@ -669,9 +818,7 @@ def run_ours(args, rank, world, dist):
                     "frac": achieved / p_bw, "traffic": None if args.causal else profiled_traffic(args.config, "bwd" if args.bwd else "fwd"),
                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                     "algorithmic_bytes_per_launch": kv_bytes,
-                    "note": ("achieved = valid entries x (1152 B gathered + 2304 B of fp32 dkv reduction) / mean "
-                             "launch time (cold L2)" if args.bwd else
-                             "achieved = valid entries x 1152 B / mean launch time (cold L2)")}
+                    "note": "achieved = valid entries x 1152 B gathered / mean launch time (cold L2)"}
     else:
         achieved = flops / (fwd_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": p_tf, "unit": "TFLOP/s",
@@ -691,10 +838,7 @@ def run_ours(args, rank, world, dist):
         "value": whole_job_tflops(flops, args.steps, world, total_ms), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(case, args.config, args.tokens) + MODE_SUFFIX[mode],
-                   "seed": 1000 + args.config,
-                   "l2": "256 MB buffer written before every timed step (cold L2)",
-                   "parallelism": f"replicas x{world}"},
+        "config": run_config(case, args, mode, world),
         "us_per_call": us, "tflops_per_gpu": tflops, "gathered_kv_GBps": gbs,
         "roofline_us": roof_us, "roofline_pct": 100.0 * roof_us / us,
         "warm_l2": {"us_per_call": statistics.median(warm) * 1e3,
@@ -708,6 +852,14 @@ def run_ours(args, rank, world, dist):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if args.bwd:
+        line["dkv_reduction"] = {
+            "bytes_per_launch": red_bytes, "GBps": red_bytes / (ms * 1e-3) / 1e9,
+            "note": "fp32 red.global.add of dK/dV rows into dkv (576 x 4 B per valid entry and 32-head unit); "
+                    "the rows stay in L2, so this is L2 traffic, not counted in the HBM roofline and not "
+                    "divided by any measured peak"}
+    if mode == "fwd" and args.tokens is None and not args.no_all_configs:
+        line["configs"] = config_records(smla, dev, stream, args.steps, args.warmup, flush, peaks)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -961,19 +1113,13 @@ def run_indexer(args, rank, world, dist):
         cpu = {"value": flops * part / wall / 1e12 if rows else None, "unit": "TFLOP/s", "cores": pool.cores,
                "kind": "oracle", "sample": sample, "seconds": wall}
         pool.close()
-    name = {1: "tiny prefill s_q=s_kv=64", 2: "mid prefill s_q=s_kv=2119", 3: "prefill s_q=s_kv=8192",
-            4: "packed varlen prefill 16384 tokens (8192,4096,2048,1024,1024)",
-            5: "paged decode 16 requests x 6 MTP rows, contexts U[4096,32768], page 64"}[args.config]
     launches = 2 if scored_rows else 1
     line = {
         "metric": "DSA indexer scores + top-k TFLOP/s at topk=2048 (2*h_idx*d_idx per scored position)",
         "value": whole_job_tflops(flops, args.steps, world, total_ms), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"DSA indexer {name} h_idx=64 d_idx=128 topk=2048 (lists for the sparse-MLA "
-                               f"forward; one logits chunk)", "seed": 1000 + args.config,
-                   "l2": "256 MB buffer written before every timed step (cold L2)",
-                   "parallelism": f"replicas x{world}"},
+        "config": indexer_config(args, world),
         "us_per_call": ms * 1e3, "roofline_us": roof_us, "roofline_pct": 100.0 * roof_us / (ms * 1e3),
         "scored_rows": scored_rows, "scored_positions": scored_pos, "algorithmic_bytes": byts,
         "roofline": roofline, "cpu_baseline": cpu,

@@ -196,6 +196,33 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sparse_mla_decode over an FP8 paged KV cache, read in place.  The pages
+ * name this path ("feat: add XTuner TileLang sparse MLA backend", Summary:
+ * the FP8 MLA KV-cache path; Pull request overview: BF16 and FP8 sparse
+ * decode tests for FlashMLA) without its format; the format is the FP8
+ * sparse-decode cache published with DeepSeek-V3.2's FlashMLA kernels.  One
+ * cache slot (one token's latent row) is 656 bytes:
+ *
+ *   bytes [0, 512)    512 float8 e4m3 codes (OCP E4M3, the variant without
+ *                     infinities) of the latent's first 512 values;
+ *   bytes [512, 528)  4 fp32 scales; scale k applies to codes 128k .. 128k+127;
+ *   bytes [528, 656)  the latent's last 64 values (rope), bf16.
+ *
+ * The row the attention uses is code * scale (d < 512) and the rope values;
+ * the kernel dequantizes each gathered row to bf16 (round to nearest even)
+ * in shared memory and then computes as sparse_mla_decode does.
+ *
+ *   kv_cache      uint8 [num_blocks, page_size, 656], 16-byte aligned
+ *   everything else, including the workspace (sparse_mla_decode_workspace_size),
+ *   as sparse_mla_decode.
+ */
+sparse_mla_status_t sparse_mla_decode_fp8(const void* q, const void* kv_cache, const int32_t* block_table,
+                                          const int32_t* cache_seqlens, const int32_t* indices, float sm_scale,
+                                          void* out, float* lse, int batch, int s_next, int h_q, int d_qk, int d_v,
+                                          int topk, int page_size, int max_blocks, int num_blocks, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/*
  * sparse_mla_decode without a caller workspace, for callers that cannot
  * allocate device memory at the point of the call: code running inside a
  * serving engine whose allocator owns every byte of the device (a KV-cache
@@ -209,10 +236,16 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
  * workspace.  The per-split partial results go to one scratch array of
  * sparse_mla_decode_noalloc_max_scratch_bytes() bytes (8 MiB) that the
  * library holds in device memory on every GPU that loads it, until the
- * process exits.  A shape whose sparse_mla_decode_workspace_size exceeds that
- * maximum is rejected with SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL before any
- * launch (use sparse_mla_decode with a workspace for it).  The call makes no
- * cudaMalloc, cudaFree or other allocating call.
+ * process exits.  The arguments are checked first, exactly as
+ * sparse_mla_decode checks them (same status codes); then a shape whose
+ * sparse_mla_decode_workspace_size exceeds that maximum is rejected with
+ * SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL before any launch (use
+ * sparse_mla_decode with a workspace for it).  The partials take
+ * 2 x CTAs x min(h_q, 64) x 513 x 4 bytes: on a 152-SM GB300 with a full
+ * grid (any batch x s_next >= 10 at topk 2048) h_q <= 13 fits, so the
+ * 8-head MTP decode does, while h_q >= 14 fits only for grids small enough
+ * (few tokens, short lists).  The call makes no cudaMalloc, cudaFree or
+ * other allocating call.
  *
  * Every call shares the one scratch array, which keeps the last call's
  * contents; each call overwrites every entry it later reads, so nothing has
@@ -229,6 +262,29 @@ sparse_mla_status_t sparse_mla_decode_noalloc(const void* q, const void* kv_cach
 
 /* Size in bytes of the scratch array sparse_mla_decode_noalloc uses. */
 size_t sparse_mla_decode_noalloc_max_scratch_bytes(void);
+
+/*
+ * Debug exports of "which entries are masked": counts[t] (int32, written) is
+ * the number of valid entries of token t's list, with multiplicity, as the
+ * forward gathers them.  Each call runs the forward's own gather walk (its
+ * item schedule, 64-entry block scan and skip, index -> row mapping and
+ * validity test) with the copies and the arithmetic left out, so the count is
+ * that of the rows the forward reads, to be compared exactly with the
+ * definition's count of valid entries ("feat: add XTuner TileLang sparse
+ * MLA backend", Validation: -1-padded index lists).  Arguments are
+ * those of the matching forward (sparse_mla_fwd, sparse_mla_fwd_varlen,
+ * sparse_mla_decode); counts int32 [tokens], 4-byte aligned, device.  Nothing
+ * is allocated; launches on `stream`.
+ */
+sparse_mla_status_t sparse_mla_debug_valid_count(const int32_t* indices, int s_q, int s_kv, int topk,
+                                                 int32_t* counts, void* stream);
+sparse_mla_status_t sparse_mla_debug_valid_count_varlen(const int32_t* indices, const int32_t* cu_seqlens_q,
+                                                        const int32_t* cu_seqlens_kv, int batch, int total_q,
+                                                        int total_kv, int topk, int32_t* counts, void* stream);
+sparse_mla_status_t sparse_mla_debug_valid_count_paged(const int32_t* indices, const int32_t* block_table,
+                                                       const int32_t* cache_seqlens, int batch, int s_next, int topk,
+                                                       int page_size, int max_blocks, int num_blocks,
+                                                       int32_t* counts, void* stream);
 
 /* ------------------------------------------------------------------------
  * DSA indexer: the step that produces the index lists above.

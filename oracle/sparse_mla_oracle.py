@@ -287,8 +287,30 @@ def sparse_mla_bwd_varlen(q, kv, indices, cu_seqlens_q, cu_seqlens_kv, sm_scale:
 
 
 def valid_count_dense(indices, s_kv: int) -> np.ndarray:
+    """|V_t| per token: the number of valid entries, with multiplicity."""
     idx = _i64(indices).reshape(indices.shape[0], -1)
     return np.array([rows_dense(r, s_kv).size for r in idx], dtype=np.int64)
+
+
+def valid_count_varlen(indices, cu_seqlens_q, cu_seqlens_kv) -> np.ndarray:
+    """|V_t| per packed token (entries local to the token's sequence)."""
+    idx = _i64(indices).reshape(indices.shape[0], -1)
+    cu_q, cu_k = _i64(cu_seqlens_q), _i64(cu_seqlens_kv)
+    out = np.zeros(idx.shape[0], dtype=np.int64)
+    for t in range(idx.shape[0]):
+        b = int(np.searchsorted(cu_q, t, side="right") - 1)
+        out[t] = rows_varlen(idx[t], int(cu_k[b]), int(cu_k[b + 1] - cu_k[b])).size
+    return out
+
+
+def valid_count_paged(indices, block_table, cache_seqlens, page_size: int, num_blocks: int) -> np.ndarray:
+    """|V_t| per decode token, flattened as [batch * s_next]."""
+    table = _i64(block_table)
+    lens = _i64(cache_seqlens)
+    batch = table.shape[0]
+    idx = _i64(indices).reshape(batch, -1, indices.shape[-1])
+    return np.array([rows_paged(idx[b, j], table[b], int(lens[b]), page_size, num_blocks).size
+                     for b in range(batch) for j in range(idx.shape[1])], dtype=np.int64)
 
 
 def _stack(outs, lses, h, d_v):

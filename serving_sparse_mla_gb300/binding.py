@@ -47,10 +47,18 @@ SIGNATURES = {
     "sparse_mla_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_void_p,
                                   c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                   c_void_p, c_size_t, c_void_p]),
+    "sparse_mla_decode_fp8": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_void_p,
+                                      c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                      c_void_p, c_size_t, c_void_p]),
     "sparse_mla_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_void_p,
                                           c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                                           c_void_p]),
     "sparse_mla_decode_noalloc_max_scratch_bytes": (c_size_t, []),
+    "sparse_mla_debug_valid_count": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "sparse_mla_debug_valid_count_varlen": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                                    c_void_p, c_void_p]),
+    "sparse_mla_debug_valid_count_paged": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                                   c_int, c_int, c_void_p, c_void_p]),
     "dsa_indexer_scores": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                    c_int, c_int, c_int, c_int, c_int, c_void_p, ctypes.c_longlong, c_void_p]),
     "dsa_topk": (c_int, [c_void_p, ctypes.c_longlong, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
@@ -346,6 +354,100 @@ def sparse_mla_decode(q, kv_cache, block_table, cache_seqlens, indices, sm_scale
                                max_blocks, num_blocks, _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "sparse_mla_decode")
     return out, lse
+
+
+FP8_SLOT_BYTES = 656
+
+
+def sparse_mla_decode_fp8(q, kv_cache, block_table, cache_seqlens, indices, sm_scale, page_size=None,
+                          workspace: Optional[torch.Tensor] = None, out=None, lse=None, stream=None):
+    """Paged decode over an FP8 cache: kv_cache uint8 [num_blocks, page, 656]
+    (512 e4m3 codes, 4 fp32 tile scales, 64 bf16 rope values per slot);
+    everything else as sparse_mla_decode."""
+    lib = load()
+    batch, s_next, h_q, d_qk = q.shape
+    num_blocks = kv_cache.shape[0]
+    page = kv_cache.shape[1] if page_size is None else page_size
+    max_blocks = block_table.shape[1]
+    topk = indices.shape[-1]
+    for t, dt, n in ((q, torch.bfloat16, "q"), (kv_cache, torch.uint8, "kv_cache"),
+                     (block_table, torch.int32, "block_table"), (cache_seqlens, torch.int32, "cache_seqlens"),
+                     (indices, torch.int32, "indices")):
+        _need(t, dt, n)
+    if kv_cache.shape[-1] != FP8_SLOT_BYTES:
+        raise ValueError(f"kv_cache slots must be {FP8_SLOT_BYTES} bytes, got {kv_cache.shape[-1]}")
+    dev = q.device
+    _fits(kv_cache, num_blocks * page * FP8_SLOT_BYTES, "kv_cache", dev)
+    _fits(block_table, batch * max_blocks, "block_table", dev)
+    _fits(cache_seqlens, batch, "cache_seqlens", dev)
+    _fits(indices, batch * s_next * topk, "indices", dev)
+    _given(out, torch.bfloat16, "out", batch * s_next * h_q * 512, dev)
+    _given(lse, torch.float32, "lse", batch * s_next * h_q, dev)
+    _workspace(workspace, dev)
+    if out is None:
+        out = torch.empty((batch, s_next, h_q, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((batch, s_next, h_q), dtype=torch.float32, device=q.device)
+    need = lib.sparse_mla_decode_workspace_size(batch, s_next, h_q, 512, topk)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.sparse_mla_decode_fp8(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(cache_seqlens), _ptr(indices),
+                                   float(sm_scale), _ptr(out), _ptr(lse), batch, s_next, h_q, d_qk, 512, topk, page,
+                                   max_blocks, num_blocks, _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "sparse_mla_decode_fp8")
+    return out, lse
+
+
+# ---------------------------------------------------------------- debug: valid entries per token
+
+def debug_valid_count(indices, s_kv: int, stream=None) -> torch.Tensor:
+    """Valid entries of each token's list as the dense forward gathers them:
+    indices [s_q, topk] int32 -> counts [s_q] int32."""
+    lib = load()
+    _need(indices, torch.int32, "indices")
+    s_q, topk = indices.shape[0], indices.shape[-1]
+    counts = torch.empty(s_q, dtype=torch.int32, device=indices.device)
+    _check(lib.sparse_mla_debug_valid_count(_ptr(indices), s_q, int(s_kv), topk, _ptr(counts), _stream(stream)),
+           "sparse_mla_debug_valid_count")
+    return counts
+
+
+def debug_valid_count_varlen(indices, cu_seqlens_q, cu_seqlens_kv, total_kv: int, stream=None) -> torch.Tensor:
+    """As debug_valid_count for the packed layout of sparse_mla_fwd_varlen."""
+    lib = load()
+    for t, n in ((indices, "indices"), (cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_kv, "cu_seqlens_kv")):
+        _need(t, torch.int32, n)
+    total_q, topk = indices.shape[0], indices.shape[-1]
+    batch = cu_seqlens_q.numel() - 1
+    dev = indices.device
+    _fits(cu_seqlens_q, batch + 1, "cu_seqlens_q", dev)
+    _fits(cu_seqlens_kv, batch + 1, "cu_seqlens_kv", dev)
+    counts = torch.empty(total_q, dtype=torch.int32, device=dev)
+    _check(lib.sparse_mla_debug_valid_count_varlen(_ptr(indices), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), batch,
+                                                   total_q, int(total_kv), topk, _ptr(counts), _stream(stream)),
+           "sparse_mla_debug_valid_count_varlen")
+    return counts
+
+
+def debug_valid_count_paged(indices, block_table, cache_seqlens, page_size: int, num_blocks: int,
+                            stream=None) -> torch.Tensor:
+    """As debug_valid_count for the paged layout of sparse_mla_decode:
+    indices [b, s_next, topk] -> counts [b * s_next] int32."""
+    lib = load()
+    for t, n in ((indices, "indices"), (block_table, "block_table"), (cache_seqlens, "cache_seqlens")):
+        _need(t, torch.int32, n)
+    batch, s_next, topk = indices.shape
+    max_blocks = block_table.shape[1]
+    dev = indices.device
+    _fits(block_table, batch * max_blocks, "block_table", dev)
+    _fits(cache_seqlens, batch, "cache_seqlens", dev)
+    counts = torch.empty(batch * s_next, dtype=torch.int32, device=dev)
+    _check(lib.sparse_mla_debug_valid_count_paged(_ptr(indices), _ptr(block_table), _ptr(cache_seqlens), batch,
+                                                  s_next, topk, int(page_size), max_blocks, int(num_blocks),
+                                                  _ptr(counts), _stream(stream)),
+           "sparse_mla_debug_valid_count_paged")
+    return counts
 
 
 # ---------------------------------------------------------------- DSA indexer

@@ -73,6 +73,7 @@
 // and returns.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -99,7 +100,16 @@ constexpr int kMaxSmem = 232448;
 // position e while e <= t + causal_off (every causal position selected, the
 // short-prefill case of "feat: add XTuner TileLang sparse MLA backend",
 // Summary), else masked.
-enum Mode : int { kDense = 0, kVarlen = 1, kPaged = 2, kCausal = 3 };
+// kPagedFp8: the paged layout over an FP8 cache (656-byte slots: 512 e4m3
+// codes, four fp32 tile scales, 64 bf16 rope values), dequantized to bf16 as
+// the rows are gathered.
+enum Mode : int { kDense = 0, kVarlen = 1, kPaged = 2, kCausal = 3, kPagedFp8 = 4 };
+
+// FP8 cache slot layout (the FP8 sparse-decode cache published with
+// DeepSeek-V3.2's FlashMLA kernels; the pages name the path, not its format).
+constexpr int kFp8SlotBytes = 656;
+constexpr int kFp8ScaleOff = 512;
+constexpr int kFp8RopeOff = 528;
 
 // How units (token x head group) are dealt to the persistent CTAs:
 //   kWholeUnits   CTA c runs units c, c + G, c + 2G, ... whole (prefill).
@@ -139,6 +149,7 @@ struct FwdParams {
   const __nv_bfloat16* dout;  // [n_tok, h_q, 512]
   float* dq;                  // [n_tok, h_q, 576]
   float* dkv;                 // [n_rows, 576], accumulated
+  int32_t* valid_count;       // debug count export: [n_tok], zeroed, accumulated
   unsigned long long timeout_ns;
 };
 
@@ -275,7 +286,7 @@ __device__ __forceinline__ TokCtx token_context(const FwdParams& p, int tok) {
     }
     c.kv_lo = __ldg(p.cu_kv + lo);
     c.kv_len = __ldg(p.cu_kv + lo + 1) - c.kv_lo;
-  } else {
+  } else {   // kPaged, kPagedFp8
     const int b = tok / p.s_next;
     c.kv_lo = 0;
     c.kv_len = __ldg(p.seqlens + b);
@@ -293,16 +304,26 @@ __device__ __forceinline__ int index_at(const int32_t* irow, int last, int e) {
   else return __ldg(irow + e);
 }
 
-// KV row read by one index entry, or -1 when the entry is masked.
-__device__ __forceinline__ int map_entry(const FwdParams& p, const TokCtx& c, int idx) {
+// The paged layouts' block-table entry of an index entry's page (-1 when the
+// entry is outside the token's range or its page past the table's width);
+// 0 for the other layouts.  Split from map_entry so that the producer can
+// load the next block's entries while it issues the current block's copies.
+__device__ __forceinline__ int table_entry(const FwdParams& p, const TokCtx& c, int idx) {
+  if (!(p.mode == kPaged || p.mode == kPagedFp8)) return 0;
+  if (idx < 0 || idx >= c.kv_len) return -1;
+  const int pg = idx / p.page_size;
+  if (pg >= p.max_blocks) return -1;
+  return __ldg(c.table + pg);
+}
+
+// KV row read by one index entry (blk: its table_entry), or -1 when the
+// entry is masked.
+__device__ __forceinline__ int map_entry(const FwdParams& p, const TokCtx& c, int idx, int blk) {
   if (idx < 0 || idx >= c.kv_len) return -1;
   int row;
-  if (p.mode == kPaged) {
-    const int pg = idx / p.page_size;
-    if (pg >= p.max_blocks) return -1;
-    const int blk = __ldg(c.table + pg);
+  if (p.mode == kPaged || p.mode == kPagedFp8) {
     if (blk < 0 || blk >= p.num_blocks) return -1;
-    row = blk * p.page_size + (idx - pg * p.page_size);
+    row = blk * p.page_size + idx % p.page_size;
   } else {
     row = c.kv_lo + idx;
   }
@@ -401,13 +422,42 @@ __device__ __forceinline__ void cp_async_arrive_on(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// 16 bytes from global memory through the non-coherent path, not kept in L1
+// (gathered cache rows are read once).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float4 ldg_stream_f4(const void* p) {
+  const uint4 v = ldg_stream_v4(p);
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
+
+// Two e4m3 codes (the low byte first) times a scale -> bf16x2 (round to
+// nearest even): e4m3 -> f16 is exact, the product is formed in fp32.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_codes, float scale) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two_codes)));
+  const __half2 h = *reinterpret_cast<const __half2*>(&h2);
+  const float2 f = __half22float2(h);
+  return pack_bf16x2(f.x * scale, f.y * scale);
+}
+
 // ------------------------------------------------------------------ producer
 
 // The gather producer, shared with the backward kernel: L gives the shared
 // memory layout (ring sizes and offsets), M the barrier block (same member
 // names), and kRows also publishes each block's 64 KV rows (entry r of the
 // block in info_rows[k][r], -1 when masked) for consumers that scatter by row.
-template <int N, class L, class M, bool kRows, bool kCausalList = false>
+// kCount walks the same windows, block skips, row mapping and validity
+// ballots but copies and publishes nothing: it adds each item's number of
+// valid entries to p.valid_count[token] (the debug count export).
+// kFp8 gathers FP8 cache slots (kPagedFp8) and dequantizes them to bf16.
+template <int N, class L, class M, bool kRows, bool kCausalList = false, bool kCount = false, bool kFp8 = false>
 __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
   const int warp = static_cast<int>(threadIdx.x >> 5);   // 0..3
   const int lane = static_cast<int>(lane_id());
@@ -422,6 +472,7 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
   int n = 0;     // blocks issued: position in the tile rings
   int ni = 0;    // info entries published: blocks and per-item end markers
   int win = 0;   // index windows scanned (phase of cand_full)
+  int counted = 0;   // kCount: valid entries of the current item
   ItemIter iter = items_begin(p);
   Item item;
   uint64_t deadline = 0;
@@ -467,11 +518,12 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
         for (int w = 0; w < kProducerWarps; ++w) cand |= *reinterpret_cast<volatile uint32_t*>(&m.cand[win & 1][w]);
       }
       int j_next = cand != 0u ? wb + __ffs(static_cast<int>(cand)) - 1 : -1;
-      int idx_next[2];
+      int idx_next[2], tbl_next[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int e = j_next * kBlk + lane * 2 + i;
         idx_next[i] = (j_next >= 0 && e < p.topk) ? index_at<kCausalList>(irow, last, e) : -1;
+        tbl_next[i] = table_entry(p, ctx, idx_next[i]);
       }
       while (j_next >= 0) {
         const int j = j_next;
@@ -479,15 +531,22 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
         j_next = cand != 0u ? wb + __ffs(static_cast<int>(cand)) - 1 : -1;
         int rows[2];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) rows[i] = map_entry(p, ctx, idx_next[i]);
+        for (int i = 0; i < 2; ++i) rows[i] = map_entry(p, ctx, idx_next[i], tbl_next[i]);
+        // The next candidate's indices, and (paged) its table entries: their
+        // loads are in flight while this block's copies are issued.
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {   // prefetch the next candidate's indices
+        for (int i = 0; i < 2; ++i) {
           const int e = j_next * kBlk + lane * 2 + i;
           idx_next[i] = (j_next >= 0 && e < p.topk) ? index_at<kCausalList>(irow, last, e) : -1;
+          tbl_next[i] = table_entry(p, ctx, idx_next[i]);
         }
         const uint32_t bal0 = __ballot_sync(0xffffffffu, rows[0] >= 0);
         const uint32_t bal1 = __ballot_sync(0xffffffffu, rows[1] >= 0);
         if ((bal0 | bal1) == 0u) continue;
+        if constexpr (kCount) {
+          counted += __popc(bal0) + __popc(bal1);
+          continue;
+        }
 
         if (warp == 0) {
           const int k = ni % kInfoDepth;
@@ -539,6 +598,76 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
             n_chunks = 1;
           }
         };
+        // FP8 cache: the block's e4m3 codes (16 per lane, row and value tile)
+        // and its rows' tile scales go to registers first, all loads in flight
+        // together; each value tile is dequantized into its ring slot once the
+        // slot is free.  Masked rows keep codes and scales 0 (a zero row).
+        uint4 codes[4][4];
+        float scl[4][4];
+        if constexpr (kFp8) {
+          const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int row = myrow[it];
+            const uint8_t* base = kv8 + static_cast<size_t>(row < 0 ? 0 : row) * kFp8SlotBytes;
+            float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row >= 0) sc = ldg_stream_f4(base + kFp8ScaleOff);
+            scl[it][0] = sc.x;
+            scl[it][1] = sc.y;
+            scl[it][2] = sc.z;
+            scl[it][3] = sc.w;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              codes[u][it] = row >= 0 ? ldg_stream_v4(base + u * 128 + piece * 16) : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        // One tile's copies into its (free) slot, then the arrival on its full
+        // barrier: cp.async with a hardware arrival, or (FP8 value tiles)
+        // dequantize, store, fence for the tensor core's proxy and arrive.
+        auto copy_tile = [&](int step, uint32_t full, uint32_t dst, int first_chunk, int n_chunks) {
+          const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
+          if constexpr (kFp8) {
+            if (u < 4) {
+              // 16 codes of row r: columns 128 u + 16 piece .. + 15, i.e. 64-column
+              // chunk piece / 4, 8-column pieces 2 (piece % 4) and 2 (piece % 4) + 1.
+              const int ch = piece >> 2, pc = (piece & 3) * 2;
+#pragma unroll
+              for (int it = 0; it < 4; ++it) {
+                const int r = warp * 16 + it * 4 + sel;
+                const uint4 c = codes[u][it];
+                const float sc = scl[it][u];
+                const uint32_t at = dst + ch * kChunkBytes + r * 128;
+                st_shared_v4(at + ((pc ^ (r & 7)) << 4), e4m3x2_scaled_bf16x2(c.x, sc),
+                             e4m3x2_scaled_bf16x2(c.x >> 16, sc), e4m3x2_scaled_bf16x2(c.y, sc),
+                             e4m3x2_scaled_bf16x2(c.y >> 16, sc));
+                st_shared_v4(at + (((pc + 1) ^ (r & 7)) << 4), e4m3x2_scaled_bf16x2(c.z, sc),
+                             e4m3x2_scaled_bf16x2(c.z >> 16, sc), e4m3x2_scaled_bf16x2(c.w, sc),
+                             e4m3x2_scaled_bf16x2(c.w >> 16, sc));
+              }
+              fence_proxy_async_smem();
+              mbar_arrive(full);
+              return;
+            }
+          }
+          for (int c = 0; c < n_chunks; ++c) {
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+              const int r = warp * 16 + it * 4 + sel;
+              const int src_row = myrow[it];
+              const void* src;
+              if constexpr (kFp8)   // the rope tile: 64 bf16 values after the codes and scales
+                src = reinterpret_cast<const uint8_t*>(p.kv) +
+                      static_cast<size_t>(src_row < 0 ? 0 : src_row) * kFp8SlotBytes + kFp8RopeOff + piece * 16;
+              else
+                src = p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
+              cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
+            }
+          }
+          // The hardware arrives on the tile's full barrier for this thread
+          // once all of this thread's copies so far have landed; the thread
+          // itself never waits on them.
+          cp_async_arrive_on(full);
+        };
         // A barrier test sits in the memory pipe behind this warp's earlier
         // copies, so every wait costs about one drain of that queue.  With a
         // ring deeper than two blocks (N <= 32) the slots of a block are usually
@@ -575,51 +704,40 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
                 uint32_t empty, full, par, dst;
                 int first_chunk, n_chunks;
                 tile(step, empty, full, par, dst, first_chunk, n_chunks);
-              for (int c = 0; c < n_chunks; ++c) {
-#pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                  const int r = warp * 16 + it * 4 + sel;
-                  const int src_row = myrow[it];
-                  const __nv_bfloat16* src =
-                      p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
-                  cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
-                }
-              }
-              // The hardware arrives on the tile's full barrier for this thread
-              // once all of this thread's copies so far have landed; the thread
-              // itself never waits on them.
-              cp_async_arrive_on(full);
+                copy_tile(step, full, dst, first_chunk, n_chunks);
               }
             }
             done |= ready;
           }
         } else {
-#pragma unroll 1
-          for (int step = 0; step < 5; ++step) {
+          auto wait_and_copy = [&](int step) {
             uint32_t empty, full, par, dst;
             int first_chunk, n_chunks;
             tile(step, empty, full, par, dst, first_chunk, n_chunks);
             const bool ok = mbar_wait(empty, par ^ 1u, deadline, ab);
             if (!__all_sync(0xffffffffu, ok)) return false;
-            for (int c = 0; c < n_chunks; ++c) {
+            copy_tile(step, full, dst, first_chunk, n_chunks);
+            return true;
+          };
+          if constexpr (kFp8) {   // register-held codes: the step must be a constant
 #pragma unroll
-              for (int it = 0; it < 4; ++it) {
-                const int r = warp * 16 + it * 4 + sel;
-                const int src_row = myrow[it];
-                const __nv_bfloat16* src =
-                    p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
-                cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
-              }
-            }
-            // The hardware arrives on the tile's full barrier for this thread
-            // once all of this thread's copies so far have landed; the thread
-            // itself never waits on them.
-            cp_async_arrive_on(full);
+            for (int step = 0; step < 5; ++step)
+              if (!wait_and_copy(step)) return false;
+          } else {
+#pragma unroll 1
+            for (int step = 0; step < 5; ++step)
+              if (!wait_and_copy(step)) return false;
           }
         }
         ++n;
         ++ni;
       }
+    }
+    if constexpr (kCount) {
+      // One add per item and head group 0 only (pieces of a cut unit add up).
+      if (warp == 0 && lane == 0 && counted > 0 && item.unit % p.groups == 0) atomicAdd(p.valid_count + tok, counted);
+      counted = 0;
+      continue;
     }
     // End of the item: a marker the consumers take as "finish this unit".
     if (warp == 0) {
@@ -638,10 +756,12 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
 
 // The index list is read from memory, or formed in place in the causal mode
 // (decided once per launch, so the list walk carries no per-entry branch).
-template <int N>
+template <int N, bool kFp8>
 __device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
-  return p.mode == kCausal ? run_producer_t<N, Layout<N>, Misc, false, true>(p, m, sbase)
-                           : run_producer_t<N, Layout<N>, Misc, false, false>(p, m, sbase);
+  if constexpr (kFp8) return run_producer_t<N, Layout<N>, Misc, false, false, false, true>(p, m, sbase);
+  else
+    return p.mode == kCausal ? run_producer_t<N, Layout<N>, Misc, false, true>(p, m, sbase)
+                             : run_producer_t<N, Layout<N>, Misc, false, false>(p, m, sbase);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -1068,7 +1188,8 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 
 // ------------------------------------------------------------------ kernel
 
-template <int N>
+// kFp8: the FP8-cache instantiation (kPagedFp8); only the gather differs.
+template <int N, bool kFp8 = false>
 __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Layout<N>;
   extern __shared__ uint8_t smem_raw[];
@@ -1119,7 +1240,7 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
 
   if (m.prior_error == 0) {
     if (warp < kProducerWarps) {
-      if (!run_producer<N>(p, m, sbase)) raise_error(m, kErrProducerWait);
+      if (!run_producer<N, kFp8>(p, m, sbase)) raise_error(m, kErrProducerWait);
       // Drain: every copy this thread issued has landed before the CTA can
       // exit, whether or not the consumers got to it.
       asm volatile("cp.async.wait_all;" ::: "memory");
@@ -1226,6 +1347,22 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_splits_kernel(const
     o2[64 * k] = __floats2bfloat162_rn(acc[k].x, acc[k].y);
     o2[64 * k + 1] = __floats2bfloat162_rn(acc[k].z, acc[k].w);
   }
+}
+
+// Debug export of the number of valid entries per token: the forward's own
+// producer walk (its item schedule, window scan, block skips, row mapping and
+// validity ballots) with the copies left out.  Four producer warps per CTA,
+// the launch's item schedule; p.valid_count is zeroed before the launch.
+__global__ void __launch_bounds__(kProducerWarps * 32, 1) valid_count_kernel(const __grid_constant__ FwdParams p) {
+  __shared__ Misc m;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&m.cand_full), kProducerWarps);
+    m.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!run_producer_t<16, Layout<16>, Misc, false, false, true>(p, m, reinterpret_cast<uint8_t*>(&m)))
+    raise_error(m, kErrProducerWait);
 }
 
 // Every entry masked (no KV rows at all): out = 0, LSE = -inf.

@@ -61,6 +61,12 @@ sparse_mla_status_t device_setup(int* sm_count) {
                              smla::smem_bytes<32>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::smem_bytes<64>()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::smem_bytes<16>()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::smem_bytes<32>()) != cudaSuccess ||
+        cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smla::smem_bytes<64>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::bwd_smem_bytes<1>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_bwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -124,6 +130,15 @@ size_t decode_part_floats(int ctas, int h_q) {
 sparse_mla_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
   const int N = head_width(p.h_q);
   const dim3 grid(static_cast<unsigned>(p.ctas));
+  if (p.mode == smla::kPagedFp8) {
+    if (N == 16)
+      smla::sparse_mla_fwd_kernel<16, true><<<grid, smla::Layout<16>::kThreads, smla::smem_bytes<16>(), stream>>>(p);
+    else if (N == 32)
+      smla::sparse_mla_fwd_kernel<32, true><<<grid, smla::Layout<32>::kThreads, smla::smem_bytes<32>(), stream>>>(p);
+    else
+      smla::sparse_mla_fwd_kernel<64, true><<<grid, smla::Layout<64>::kThreads, smla::smem_bytes<64>(), stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+  }
   if (N == 16)
     smla::sparse_mla_fwd_kernel<16><<<grid, smla::Layout<16>::kThreads, smla::smem_bytes<16>(), stream>>>(p);
   else if (N == 32)
@@ -353,11 +368,16 @@ size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v,
   return decode_part_floats(ctas, h_q) * sizeof(float);
 }
 
-sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
-                                      const int32_t* cache_seqlens, const int32_t* indices, float sm_scale, void* out,
-                                      float* lse, int batch, int s_next, int h_q, int d_qk, int d_v, int topk,
-                                      int page_size, int max_blocks, int num_blocks, void* workspace,
-                                      size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks of the paged decode (every decode entry point runs them
+// first, in this order).  On OK, *sms holds the device's SM count.
+sparse_mla_status_t check_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                                 const int32_t* cache_seqlens, const int32_t* indices, const void* out,
+                                 const float* lse, int batch, int s_next, int h_q, int d_qk, int d_v, int topk,
+                                 int page_size, int max_blocks, int num_blocks, int* sms) {
   if (batch < 0 || s_next < 0) return SPARSE_MLA_ERR_INVALID_ARG;
   const long long n_tok = static_cast<long long>(batch) * s_next;
   sparse_mla_status_t st = check_common(q, indices, out, lse, n_tok, h_q, d_qk, d_v, topk);
@@ -366,22 +386,45 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
   if (static_cast<long long>(num_blocks) * page_size > INT_MAX) return SPARSE_MLA_ERR_INVALID_ARG;
   if (n_tok > 0 && (!block_table || !cache_seqlens || !aligned(block_table, 4) || !aligned(cache_seqlens, 4)))
     return SPARSE_MLA_ERR_INVALID_ARG;
+  if ((st = device_setup(sms)) != SPARSE_MLA_OK) return st;
+  if (n_tok == 0 || num_blocks == 0 || max_blocks == 0) return SPARSE_MLA_OK;
+  if (!kv_cache || !aligned(kv_cache, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
+  // The kernel forms c * (units x blocks) in 64 bits for c up to the grid size.
+  if (n_tok * head_groups(h_q) * blocks_per_list(topk) > (1LL << 62) / (*sms > 0 ? *sms : 1))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  return SPARSE_MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+}  // extern "C"
+
+namespace {
+
+// The paged decode launch of both cache formats (mode kPaged or kPagedFp8):
+// the forward grid over block ranges, then the merge of cut units.
+sparse_mla_status_t run_decode(int mode, const void* q, const void* kv_cache, const int32_t* block_table,
+                               const int32_t* cache_seqlens, const int32_t* indices, float sm_scale, void* out,
+                               float* lse, int batch, int s_next, int h_q, int d_qk, int d_v, int topk,
+                               int page_size, int max_blocks, int num_blocks, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   int sms = 0;
-  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  sparse_mla_status_t st = check_decode(q, kv_cache, block_table, cache_seqlens, indices, out, lse, batch, s_next,
+                                        h_q, d_qk, d_v, topk, page_size, max_blocks, num_blocks, &sms);
+  if (st != SPARSE_MLA_OK) return st;
+  const long long n_tok = static_cast<long long>(batch) * s_next;
   if (n_tok == 0) return SPARSE_MLA_OK;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (num_blocks == 0 || max_blocks == 0) return launch_fill(out, lse, n_tok * h_q, cs);
-  if (!kv_cache || !aligned(kv_cache, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
-  // The kernel forms c * (units x blocks) in 64 bits for c up to the grid size.
-  if (n_tok * head_groups(h_q) * blocks_per_list(topk) > (1LL << 62) / (sms > 0 ? sms : 1))
-    return SPARSE_MLA_ERR_INVALID_ARG;
   const int ctas = decode_ctas(n_tok, h_q, topk, sms);
   const size_t need = sparse_mla_decode_workspace_size(batch, s_next, h_q, d_v, topk);
   if (need > 0 && (workspace_bytes < need || !workspace)) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
   if (need > 0 && !aligned(workspace, 16)) return SPARSE_MLA_ERR_INVALID_ARG;
   FwdParams p = base_params(q, indices, sm_scale, out, lse, static_cast<int>(n_tok), h_q, topk);
-  p.kv = static_cast<const __nv_bfloat16*>(kv_cache);
-  p.mode = smla::kPaged;
+  p.kv = static_cast<const __nv_bfloat16*>(kv_cache);   // kPagedFp8: read as bytes
+  p.mode = mode;
   p.n_rows = num_blocks * page_size;
   p.batch = batch;
   p.s_next = s_next;
@@ -415,6 +458,32 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
     if (cudaLaunchKernelEx(&cfg, smla::combine_splits_kernel, p) != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
   }
   return SPARSE_MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                                      const int32_t* cache_seqlens, const int32_t* indices, float sm_scale, void* out,
+                                      float* lse, int batch, int s_next, int h_q, int d_qk, int d_v, int topk,
+                                      int page_size, int max_blocks, int num_blocks, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return run_decode(smla::kPaged, q, kv_cache, block_table, cache_seqlens, indices, sm_scale, out, lse, batch,
+                    s_next, h_q, d_qk, d_v, topk, page_size, max_blocks, num_blocks, workspace, workspace_bytes,
+                    stream);
+}
+
+sparse_mla_status_t sparse_mla_decode_fp8(const void* q, const void* kv_cache, const int32_t* block_table,
+                                          const int32_t* cache_seqlens, const int32_t* indices, float sm_scale,
+                                          void* out, float* lse, int batch, int s_next, int h_q, int d_qk, int d_v,
+                                          int topk, int page_size, int max_blocks, int num_blocks, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  // Slots are 656 bytes: the pool's byte size must fit the 64-bit offsets the
+  // gather forms (num_blocks * page_size fits int32, as for the bf16 cache).
+  return run_decode(smla::kPagedFp8, q, kv_cache, block_table, cache_seqlens, indices, sm_scale, out, lse, batch,
+                    s_next, h_q, d_qk, d_v, topk, page_size, max_blocks, num_blocks, workspace, workspace_bytes,
+                    stream);
 }
 
 }  // extern "C"
@@ -454,6 +523,11 @@ sparse_mla_status_t sparse_mla_decode_noalloc(const void* q, const void* kv_cach
                                               void* out, float* lse, int batch, int s_next, int h_q, int d_qk,
                                               int d_v, int topk, int page_size, int max_blocks, int num_blocks,
                                               void* stream) {
+  // The same argument checks as sparse_mla_decode, then the scratch size.
+  int sms = 0;
+  sparse_mla_status_t cst = check_decode(q, kv_cache, block_table, cache_seqlens, indices, out, lse, batch, s_next,
+                                         h_q, d_qk, d_v, topk, page_size, max_blocks, num_blocks, &sms);
+  if (cst != SPARSE_MLA_OK) return cst;
   const size_t need = sparse_mla_decode_workspace_size(batch, s_next, h_q, d_v, topk);
   if (need > kNoAllocScratchBytes) return SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
@@ -464,6 +538,102 @@ sparse_mla_status_t sparse_mla_decode_noalloc(const void* q, const void* kv_cach
   return sparse_mla_decode(q, kv_cache, block_table, cache_seqlens, indices, sm_scale, out, lse, batch, s_next,
                            h_q, d_qk, d_v, topk, page_size, max_blocks, num_blocks, ws,
                            need > 0 ? kNoAllocScratchBytes : 0, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+sparse_mla_status_t launch_valid_count(FwdParams& p, int32_t* counts, cudaStream_t cs) {
+  if (cudaMemsetAsync(counts, 0, static_cast<size_t>(p.n_tok) * sizeof(int32_t), cs) != cudaSuccess)
+    return SPARSE_MLA_ERR_CUDA;
+  p.valid_count = counts;
+  smla::valid_count_kernel<<<p.ctas, smla::kProducerWarps * 32, 0, cs>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+}
+
+sparse_mla_status_t check_count_args(const int32_t* indices, long long n_tok, int topk, const int32_t* counts) {
+  if (n_tok < 0 || topk < 1 || n_tok > INT_MAX / 2) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_tok > 0 && (!indices || !counts || !aligned(indices, 4) || !aligned(counts, 4)))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  return SPARSE_MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sparse_mla_status_t sparse_mla_debug_valid_count(const int32_t* indices, int s_q, int s_kv, int topk,
+                                                 int32_t* counts, void* stream) {
+  sparse_mla_status_t st = check_count_args(indices, s_q, topk, counts);
+  if (st != SPARSE_MLA_OK) return st;
+  if (s_kv < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (s_q == 0) return SPARSE_MLA_OK;
+  FwdParams p = base_params(nullptr, indices, 1.f, nullptr, nullptr, s_q, 1, topk);
+  p.mode = smla::kDense;
+  p.n_rows = s_kv;
+  p.s_kv = s_kv;
+  p.sched = smla::kWholeUnits;
+  p.ctas = prefill_ctas(s_q, 1, sms);
+  return launch_valid_count(p, counts, static_cast<cudaStream_t>(stream));
+}
+
+sparse_mla_status_t sparse_mla_debug_valid_count_varlen(const int32_t* indices, const int32_t* cu_seqlens_q,
+                                                        const int32_t* cu_seqlens_kv, int batch, int total_q,
+                                                        int total_kv, int topk, int32_t* counts, void* stream) {
+  sparse_mla_status_t st = check_count_args(indices, total_q, topk, counts);
+  if (st != SPARSE_MLA_OK) return st;
+  if (total_kv < 0 || batch < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (total_q > 0 && (batch < 1 || !cu_seqlens_q || !cu_seqlens_kv || !aligned(cu_seqlens_q, 4) ||
+                      !aligned(cu_seqlens_kv, 4)))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (total_q == 0) return SPARSE_MLA_OK;
+  FwdParams p = base_params(nullptr, indices, 1.f, nullptr, nullptr, total_q, 1, topk);
+  p.mode = smla::kVarlen;
+  p.n_rows = total_kv;
+  p.batch = batch;
+  p.cu_q = cu_seqlens_q;
+  p.cu_kv = cu_seqlens_kv;
+  p.sched = smla::kWholeUnits;
+  p.ctas = prefill_ctas(total_q, 1, sms);
+  return launch_valid_count(p, counts, static_cast<cudaStream_t>(stream));
+}
+
+sparse_mla_status_t sparse_mla_debug_valid_count_paged(const int32_t* indices, const int32_t* block_table,
+                                                       const int32_t* cache_seqlens, int batch, int s_next, int topk,
+                                                       int page_size, int max_blocks, int num_blocks,
+                                                       int32_t* counts, void* stream) {
+  if (batch < 0 || s_next < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  const long long n_tok = static_cast<long long>(batch) * s_next;
+  sparse_mla_status_t st = check_count_args(indices, n_tok, topk, counts);
+  if (st != SPARSE_MLA_OK) return st;
+  if (page_size < 1 || max_blocks < 0 || num_blocks < 0) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (static_cast<long long>(num_blocks) * page_size > INT_MAX) return SPARSE_MLA_ERR_INVALID_ARG;
+  if (n_tok > 0 && (!block_table || !cache_seqlens || !aligned(block_table, 4) || !aligned(cache_seqlens, 4)))
+    return SPARSE_MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_setup(&sms)) != SPARSE_MLA_OK) return st;
+  if (n_tok == 0) return SPARSE_MLA_OK;
+  if (n_tok * blocks_per_list(topk) > (1LL << 62) / (sms > 0 ? sms : 1)) return SPARSE_MLA_ERR_INVALID_ARG;
+  FwdParams p = base_params(nullptr, indices, 1.f, nullptr, nullptr, static_cast<int>(n_tok), 1, topk);
+  p.mode = smla::kPaged;
+  p.n_rows = num_blocks * page_size;
+  p.batch = batch;
+  p.s_next = s_next;
+  p.page_size = page_size;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
+  p.block_table = block_table;
+  p.seqlens = cache_seqlens;
+  // The block ranges of a decode launch (one head group), so the walk cuts
+  // the lists where the forward does.
+  p.sched = smla::kBlockRanges;
+  p.ctas = decode_ctas(n_tok, 1, topk, sms);
+  return launch_valid_count(p, counts, static_cast<cudaStream_t>(stream));
 }
 
 const char* sparse_mla_status_string(sparse_mla_status_t s) {

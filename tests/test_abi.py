@@ -173,3 +173,28 @@ def test_paged_indexer_validation(lib):
     assert paged(idx=None) == 1
     st = lib.dsa_indexer_scores_paged(16, 16, 16, 16, 16, 2, 6, 64, 128, 64, 8, 16, 10, 5, 0, 16, 500, None)
     assert st == 1                   # rows past batch * s_next
+
+
+def test_fp8_decode_and_debug_count_validation(lib):
+    """Argument errors of the FP8 decode and of the debug count exports come
+    back before any device work."""
+    def fp8(**kw):
+        a = dict(q=16, kv=16, bt=16, sl=16, idx=16, scale=0.1, out=16, lse=16, batch=2, s_next=3, h_q=8,
+                 d_qk=576, d_v=512, topk=64, page=64, max_blocks=4, num_blocks=8, ws=None, ws_bytes=0,
+                 stream=None)
+        a.update(kw)
+        return lib.sparse_mla_decode_fp8(a["q"], a["kv"], a["bt"], a["sl"], a["idx"], a["scale"], a["out"],
+                                         a["lse"], a["batch"], a["s_next"], a["h_q"], a["d_qk"], a["d_v"],
+                                         a["topk"], a["page"], a["max_blocks"], a["num_blocks"], a["ws"],
+                                         a["ws_bytes"], a["stream"])
+    assert fp8(d_qk=512) == 2
+    assert fp8(batch=-1) == 1
+    assert fp8(page=0) == 1
+    assert fp8(bt=None) == 1
+    assert fp8(q=24) == 1
+    assert lib.sparse_mla_debug_valid_count(None, 4, 10, 64, 16, None) == 1
+    assert lib.sparse_mla_debug_valid_count(16, 4, 10, 0, 16, None) == 1
+    assert lib.sparse_mla_debug_valid_count(16, 4, -1, 64, 16, None) == 1
+    assert lib.sparse_mla_debug_valid_count_varlen(16, None, 16, 2, 4, 10, 64, 16, None) == 1
+    assert lib.sparse_mla_debug_valid_count_paged(16, 16, 16, 2, 3, 64, 0, 4, 8, 16, None) == 1
+    assert lib.sparse_mla_debug_valid_count_paged(16, None, 16, 2, 3, 64, 64, 4, 8, 16, None) == 1

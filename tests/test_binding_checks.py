@@ -129,6 +129,28 @@ def test_decode_shapes_and_extents(b):
     _refused(b, f, *args, workspace=torch.empty(64, dtype=torch.uint8)[::2], match="contiguous")
 
 
+def test_fp8_decode_and_debug_count_extents(b):
+    c, u = mi.decode_case_fp8(704, 4, 6, 8, 500, 3000, topk=512)
+    f = b.sparse_mla_decode_fp8
+    args = (c.q, u, c.block_table, c.cache_seqlens, c.indices, c.sm_scale, c.page_size)
+    _ok(b, "sparse_mla_decode_fp8", f, *args)
+    _refused(b, f, c.q, c.kv_cache, c.block_table, c.cache_seqlens, c.indices, c.sm_scale, c.page_size,
+             match="uint8")                                                       # a bf16 cache
+    _refused(b, f, c.q, u[..., :576].contiguous(), c.block_table, c.cache_seqlens, c.indices, c.sm_scale, c.page_size,
+             match="656")
+    _refused(b, f, c.q, u, c.block_table, c.cache_seqlens, c.indices, c.sm_scale, 2 * c.page_size, match="kv_cache")
+    _refused(b, f, c.q, u, c.block_table[:-1], c.cache_seqlens, c.indices, c.sm_scale, c.page_size,
+             match="block_table")
+    _ok(b, "sparse_mla_debug_valid_count_paged", b.debug_valid_count_paged, c.indices, c.block_table,
+        c.cache_seqlens, c.page_size, c.kv_cache.shape[0])
+    _refused(b, b.debug_valid_count_paged, c.indices, c.block_table[:-1], c.cache_seqlens, c.page_size,
+             c.kv_cache.shape[0], match="block_table")
+    v = mi.varlen_case(706, [30, 1, 50], 8, topk=64)
+    _ok(b, "sparse_mla_debug_valid_count_varlen", b.debug_valid_count_varlen, v.indices, v.cu_seqlens_q,
+        v.cu_seqlens_kv, v.kv.shape[0])
+    _ok(b, "sparse_mla_debug_valid_count", b.debug_valid_count, v.indices, v.kv.shape[0])
+
+
 def test_indexer_shapes_and_extents(b):
     c = mi.indexer_case(705, 400, 2600, topk=512)
     q, k, w = c.q_idx, c.k_idx, c.weights

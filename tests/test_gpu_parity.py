@@ -8,7 +8,8 @@ import torch
 
 import mla_inputs as mi
 from oracle import sparse_mla_oracle as orc
-from tests.parity import compare
+from tests.oracle_pool import check_all_tokens
+from tests.parity import compare, pv_rounding_sigma, record, tight_ratio
 
 pytestmark = pytest.mark.gpu
 
@@ -123,20 +124,40 @@ def test_s_kv_zero_and_empty_batch(smla):
     assert out.shape == (0, 8, 512)
 
 
+def _check_whole(name, layout, q, kv, indices, out, lse, sm_scale, extra=None):
+    """Every token of a full-size workload against the oracle on the host
+    cores: the allclose bar on every element, and the tight check of
+    tests/parity.py (its worst ratio recorded, and required <= 1)."""
+    st = check_all_tokens(layout, q, kv, indices, out.cpu(), lse.cpu(), sm_scale, extra)
+    assert st["fail"] is None, st["fail"]
+    assert st["tokens"] == q.shape[0]
+    record(name, tokens=st["tokens"], max_dout=st["max_dout"], max_dlse=st["max_dlse"],
+           tight_ratio=st["tight"], tight_ratio_full_lists=st["tight_full"])
+    assert st["tight"] <= 1.0, f"{name}: tight check ratio {st['tight']:.3f}"
+    return st
+
+
+def test_tiny_prefill_config_tight(smla):
+    case = mi.config(1)
+    out, lse = smla.sparse_mla_fwd(case.q.to(DEV), case.kv.to(DEV), case.indices.to(DEV), case.sm_scale)
+    _check_whole("config 1 tiny prefill", "dense", case.q, case.kv, case.indices, out, lse, case.sm_scale)
+
+
 def test_mid_prefill_config_all_tokens(smla):
-    """s_q = s_kv = 2119, h = 8, topk = 2048 (the pages' SWE-like shape)."""
+    """s_q = s_kv = 2119, h = 8, topk = 2048 (the pages' SWE-like shape):
+    every token, with the tight check (72 tokens list 2048 valid entries)."""
     case = mi.config(2)
-    _check_fwd(smla, case)
+    out, lse = smla.sparse_mla_fwd(case.q.to(DEV), case.kv.to(DEV), case.indices.to(DEV), case.sm_scale)
+    st = _check_whole("config 2 mid prefill", "dense", case.q, case.kv, case.indices, out, lse, case.sm_scale)
+    assert st["tight_full"] > 0.0   # the full-list tokens were checked
 
 
-def test_wide_head_config_sampled(smla):
-    """s_q = s_kv = 8192, h = 64, topk = 2048 at the launch the bench times;
-    sampled tokens (edges, the 2047/2048 boundary and a seeded spread)."""
+def test_wide_head_config_all_tokens(smla):
+    """s_q = s_kv = 8192, h = 64, topk = 2048 at the launch the bench times:
+    every token against the oracle (host cores), with the tight check."""
     case = mi.config(3)
-    g = np.random.default_rng(3)
-    toks = sorted(set([0, 1, 2, 127, 128, 2046, 2047, 2048, 4095, 8190, 8191]
-                      + g.choice(8192, 53, replace=False).tolist()))
-    _check_fwd(smla, case, tokens=toks)
+    out, lse = smla.sparse_mla_fwd(case.q.to(DEV), case.kv.to(DEV), case.indices.to(DEV), case.sm_scale)
+    _check_whole("config 3 wide-head prefill", "dense", case.q, case.kv, case.indices, out, lse, case.sm_scale)
 
 
 # ---------------------------------------------------------------- indices-free causal mode
@@ -190,15 +211,62 @@ def test_varlen_small(smla, h_q):
     _check_varlen(smla, case)
 
 
-def test_varlen_config_sampled(smla):
-    """16384 packed tokens (8192, 4096, 2048, 1024, 1024), h = 64."""
+def test_varlen_config_all_tokens(smla):
+    """16384 packed tokens (8192, 4096, 2048, 1024, 1024), h = 64: every
+    token against the oracle (host cores), with the tight check."""
     case = mi.config(4)
-    cu = case.cu_seqlens_q.tolist()
-    g = np.random.default_rng(4)
-    toks = set(g.choice(cu[-1], 40, replace=False).tolist())
-    for a, b in zip(cu[:-1], cu[1:]):
-        toks.update([a, a + 1, b - 1, min(a + 2047, b - 1), min(a + 2048, b - 1)])
-    _check_varlen(smla, case, tokens=sorted(toks))
+    d = lambda t: t.to(DEV)
+    out, lse = smla.sparse_mla_fwd_varlen(d(case.q), d(case.kv), d(case.indices), d(case.cu_seqlens_q),
+                                          d(case.cu_seqlens_kv), case.sm_scale)
+    _check_whole("config 4 packed varlen prefill", "varlen", case.q, case.kv, case.indices, out, lse,
+                 case.sm_scale, extra={"cu_q": case.cu_seqlens_q, "cu_k": case.cu_seqlens_kv})
+
+
+def test_varlen_indices_outside_own_sequence(smla):
+    """Local indices past a sequence's end land, unmasked, in the next
+    sequence's first rows; negative ones other than -1 land in the previous
+    sequence's last rows.  Those rows are NaN (and no list of their own
+    sequence references them), the rows past the last sequence are NaN, so a
+    mapping that fails to mask reads NaN."""
+    lens = [300, 200, 257, 130]
+    case = mi.varlen_case(630, lens, 8, topk=256)
+    cu = [0] + np.cumsum(lens).tolist()
+    idx = case.indices.clone()
+    g = torch.Generator().manual_seed(631)
+    k = 5
+    poison = []
+    for b in range(len(lens)):
+        a, e = cu[b], cu[b + 1]
+        L = lens[b]
+        own = idx[a:e]
+        # no list of a sequence names its own first k or last k positions (poisoned below)
+        own[(own >= 0) & (own < k)] = -1
+        own[(own >= L - k) & (own < L)] = -1
+        # every 9th entry of every 3rd token: past the end (L .. L+k-1) or below -1 (-k-1 .. -2)
+        for t in range(0, e - a, 3):
+            cols = torch.arange(t % 9, idx.shape[1], 9)
+            far = L + torch.randint(0, k, (cols.numel(),), generator=g, dtype=torch.int32)
+            neg = -2 - torch.randint(0, k, (cols.numel(),), generator=g, dtype=torch.int32)
+            own[t, cols] = torch.where(torch.arange(cols.numel()) % 2 == 0, far, neg)
+        poison += list(range(a, a + k)) + list(range(e - k, e))
+    total, guard = cu[-1], 64
+    # NaN guard rows before the first and after the last sequence
+    kv_buf = torch.full((guard + total + guard, 576), float("nan")).to(torch.bfloat16)
+    kv = kv_buf[guard:guard + total]
+    kv[:] = case.kv
+    kv[torch.tensor(poison)] = float("nan")
+    d_kv = kv_buf.to(DEV)
+    d = lambda t: t.to(DEV)
+    out, lse = smla.sparse_mla_fwd_varlen(d(case.q), d_kv[guard:guard + total], d(idx), d(case.cu_seqlens_q),
+                                          d(case.cu_seqlens_kv), case.sm_scale)
+    counts = smla.debug_valid_count_varlen(d(idx), d(case.cu_seqlens_q), d(case.cu_seqlens_kv), total)
+    torch.cuda.synchronize()
+    ref_o, ref_l = orc.sparse_mla_fwd_varlen(case.q, kv, idx, case.cu_seqlens_q, case.cu_seqlens_kv,
+                                             case.sm_scale)
+    compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, "varlen outside own sequence")
+    ref_c = orc.valid_count_varlen(idx, case.cu_seqlens_q, case.cu_seqlens_kv)
+    assert np.array_equal(counts.cpu().numpy(), ref_c)
+    assert ref_c.sum() < int((idx >= 0).sum())   # some non-negative entries really are masked
 
 
 # ---------------------------------------------------------------- paged decode
@@ -276,8 +344,93 @@ def test_decode_dirty_workspace(smla):
 
 def test_decode_config_all_tokens(smla):
     """batch 16 x 6 MTP tokens, contexts U[4096, 32768], 64-token pages in a
-    shuffled pool with every unread slot NaN, h = 8, topk = 2048."""
-    _check_decode(smla, mi.config(5))
+    shuffled pool with every unread slot NaN, h = 8, topk = 2048; every
+    token, with the tight check (every list holds 2048 valid entries)."""
+    c = mi.config(5)
+    d = lambda t: t.to(DEV)
+    out, lse = smla.sparse_mla_decode(d(c.q), d(c.kv_cache), d(c.block_table), d(c.cache_seqlens),
+                                      d(c.indices), c.sm_scale, c.page_size)
+    n = c.batch * c.s_next
+    _check_whole("config 5 paged decode", "paged", c.q.reshape(n, c.h_q, 576),
+                 c.kv_cache.reshape(-1, 576), c.indices.reshape(n, -1), out.reshape(n, c.h_q, 512),
+                 lse.reshape(n, c.h_q), c.sm_scale,
+                 extra={"table": c.block_table, "lens": c.cache_seqlens, "page": c.page_size,
+                        "num_blocks": c.kv_cache.shape[0], "s_next": c.s_next})
+
+
+def test_decode_invalid_pages_short_table_and_lengths(smla):
+    """Entries the paged mapping must mask although they are non-negative:
+    positions past cache_seqlens, pages at or past the table's width
+    (max_blocks), table entries -1, -2, num_blocks + 1 and num_blocks + 3.
+    The pool sits inside a larger buffer whose pages before and after it are
+    NaN, and the table is followed in memory by entries that name a NaN page:
+    a mapping that failed to mask would read NaN (or, for a page past the
+    width of an earlier request, the next request's pages, which the exact
+    valid count catches)."""
+    c = mi.decode_case(620, batch=4, s_next=3, h_q=8, lo=400, hi=1000, topk=512, page=64, spare_pages=4)
+    nb, page = c.kv_cache.shape[0], c.page_size
+    W = 5
+    bt = c.block_table[:, :W].clone()
+    bt[0, 1] = -1
+    bt[1, 0] = -2
+    bt[2, 3] = nb + 1
+    bt[3, 2] = nb + 3
+    lens = c.cache_seqlens.clone()
+    lens[1] -= 50
+    pre, post = 2, 4
+    pool = torch.full((pre + nb + post, page, 576), float("nan")).to(torch.bfloat16)
+    pool[pre:pre + nb] = c.kv_cache
+    tb = torch.full((c.batch * W + 64,), nb + 1, dtype=torch.int32)
+    tb[: c.batch * W] = bt.flatten()
+    d_pool, d_tb = pool.to(DEV), tb.to(DEV)
+    kv_view = d_pool[pre:pre + nb]
+    bt_view = d_tb[: c.batch * W].view(c.batch, W)
+    d = lambda t: t.to(DEV)
+    out, lse = smla.sparse_mla_decode(d(c.q), kv_view, bt_view, d(lens), d(c.indices), c.sm_scale, page)
+    counts = smla.debug_valid_count_paged(d(c.indices), bt_view, d(lens), page, nb)
+    torch.cuda.synchronize()
+    ref_o, ref_l = orc.sparse_mla_decode(c.q, c.kv_cache, bt, lens, c.indices, c.sm_scale, page)
+    compare(out.float().cpu().numpy().reshape(-1, c.h_q, 512), lse.cpu().numpy().reshape(-1, c.h_q),
+            ref_o, ref_l, "decode invalid pages")
+    ref_c = orc.valid_count_paged(c.indices, bt, lens, page, nb)
+    assert np.array_equal(counts.cpu().numpy(), ref_c)
+    assert ref_c.sum() < int((c.indices >= 0).sum()) // 2   # most entries are masked here
+
+
+# ---------------------------------------------------------------- masked set: exact valid counts
+
+def test_debug_valid_count_configs(smla):
+    """The debug export (the forward's own gather walk, counting) equals the
+    oracle's |V_t| exactly for every token of all five workloads."""
+    d = lambda t: t.to(DEV)
+    for n in (1, 2, 3):
+        c = mi.config(n)
+        got = smla.debug_valid_count(d(c.indices), c.kv.shape[0]).cpu().numpy()
+        assert np.array_equal(got, orc.valid_count_dense(c.indices, c.kv.shape[0])), f"config {n}"
+    c = mi.config(4)
+    got = smla.debug_valid_count_varlen(d(c.indices), d(c.cu_seqlens_q), d(c.cu_seqlens_kv), c.kv.shape[0])
+    assert np.array_equal(got.cpu().numpy(), orc.valid_count_varlen(c.indices, c.cu_seqlens_q, c.cu_seqlens_kv))
+    c = mi.config(5)
+    got = smla.debug_valid_count_paged(d(c.indices), d(c.block_table), d(c.cache_seqlens), c.page_size,
+                                       c.kv_cache.shape[0])
+    ref = orc.valid_count_paged(c.indices, c.block_table, c.cache_seqlens, c.page_size, c.kv_cache.shape[0])
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_debug_valid_count_masking_entries(smla):
+    """Dense lists mixing -1, other negatives, values at and past s_kv,
+    duplicates, ragged list ends (topk not a multiple of 64) and lists longer
+    than one 32-block scan window."""
+    s_q, s_kv, topk = 40, 700, 2500
+    g = torch.Generator().manual_seed(640)
+    idx = torch.randint(-800, 1500, (s_q, topk), generator=g, dtype=torch.int32)
+    idx[0] = -1
+    idx[1, :] = 699
+    idx[2, : topk - 1] = -1
+    idx[3, ::7] = s_kv
+    got = smla.debug_valid_count(idx.to(DEV), s_kv).cpu().numpy()
+    ref = orc.valid_count_dense(idx, s_kv)
+    assert np.array_equal(got, ref) and ref[0] == 0 and ref[1] == topk
 
 
 # ---------------------------------------------------------------- determinism

@@ -70,3 +70,9 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the CUDA arm builds its `config` with the same function: the two arms' objects are identical
+    import argparse
+    sys.path.insert(0, root)
+    import bench
+    args = argparse.Namespace(config=1, tokens=None)
+    assert d["config"] == bench.run_config(bench.workload(1), args, "fwd", 2)

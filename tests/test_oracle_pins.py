@@ -356,6 +356,30 @@ def test_valid_count_bruteforce():
     assert orc.valid_count_dense(idx, 10).tolist() == [4, 1]
 
 
+def test_valid_count_varlen_by_hand():
+    """Two sequences of 3 and 5 positions; local indices only count inside
+    their own sequence (counts written out by hand)."""
+    cu_q = torch.tensor([0, 2, 4], dtype=torch.int32)
+    cu_k = torch.tensor([0, 3, 8], dtype=torch.int32)
+    idx = torch.tensor([[0, 2, 3, -1],      # seq 0: 3 is past its 3 positions -> 2
+                        [2, 2, -2, 1],      # seq 0: duplicates count twice -> 3
+                        [4, 5, 7, 0],       # seq 1 (5 positions): 5 and 7 past -> 2
+                        [-1, -1, -1, -1]], dtype=torch.int32)
+    assert orc.valid_count_varlen(idx, cu_q, cu_k).tolist() == [2, 3, 2, 0]
+
+
+def test_valid_count_paged_by_hand():
+    """Pages of 4 slots, a pool of 5 pages, two requests with a table two
+    pages wide: request 0 has pages [3, -1] and 7 tokens; request 1 has
+    pages [9, 0] (9 outside the pool) and 8 tokens."""
+    table = torch.tensor([[3, -1], [9, 0]], dtype=torch.int32)
+    lens = torch.tensor([7, 8], dtype=torch.int32)
+    idx = torch.tensor([[[0, 3, 4, 6], [6, 7, 8, -1]],      # r0: page 1 is -1 -> 2 ; 7, 8 past the length -> 0
+                        [[0, 4, 7, 8], [5, 5, -3, 3]]],     # r1: page 0 is 9 -> only 4, 7 -> 2 ; 5, 5 -> 2
+                       dtype=torch.int32)
+    assert orc.valid_count_paged(idx, table, lens, 4, 5).tolist() == [2, 0, 2, 2]
+
+
 # ---------------------------------------------------------------------------
 # mutation tests: each planted mistake must fail at least one pin
 # ---------------------------------------------------------------------------

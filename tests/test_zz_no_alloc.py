@@ -5,9 +5,9 @@ It keeps its per-split partial results in a fixed device array inside the
 library instead of a caller workspace.
 
 Called through the C ABI, twice in a row on different inputs, it must agree
-with sparse_mla_decode given a workspace, within the parity tolerances; a
-shape that needs more scratch than the array holds is refused before any
-launch.
+with sparse_mla_decode given a workspace, and with the float64 oracle, within
+the parity tolerances; a shape that needs more scratch than the array holds
+is refused before any launch.
 """
 import ctypes
 
@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import mla_inputs as mi
+from oracle import sparse_mla_oracle as orc
 from tests.parity import compare
 
 pytestmark = pytest.mark.gpu
@@ -57,6 +58,10 @@ def test_noalloc_decode_matches_workspace_decode_twice(cuda_lib):
         torch.cuda.synchronize()
         compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out.float().cpu().numpy(),
                 ref_lse.cpu().numpy(), f"noalloc seed {seed}")
+        ro, rl = orc.sparse_mla_decode(case.q, case.kv_cache, case.block_table, case.cache_seqlens,
+                                       case.indices, case.sm_scale, case.page_size)
+        compare(out.float().cpu().numpy().reshape(-1, case.h_q, 512), lse.cpu().numpy().reshape(-1, case.h_q),
+                ro, rl, f"noalloc seed {seed} vs oracle")
 
 
 def test_noalloc_decode_refuses_shapes_past_its_scratch(cuda_lib):
@@ -64,8 +69,23 @@ def test_noalloc_decode_refuses_shapes_past_its_scratch(cuda_lib):
     batch, s_next, h_q, topk = 1, 4, 64, 8192
     need = lib.sparse_mla_decode_workspace_size(batch, s_next, h_q, 512, topk)
     assert need > lib.sparse_mla_decode_noalloc_max_scratch_bytes()
-    st = lib.sparse_mla_decode_noalloc(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
-                                       ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_float(0.1),
-                                       ctypes.c_void_p(16), ctypes.c_void_p(16), batch, s_next, h_q, 576, 512, topk,
-                                       64, 8, 8, None)
+    # Real device buffers of the call's full extents (all -1 indices), so a
+    # call that were wrongly launched could only produce a wrong status or
+    # output, never touch memory it does not own.
+    q = torch.zeros((batch, s_next, h_q, 576), dtype=torch.bfloat16, device=DEV)
+    cache = torch.zeros((8, 64, 576), dtype=torch.bfloat16, device=DEV)
+    table = torch.zeros((batch, 8), dtype=torch.int32, device=DEV)
+    lens = torch.full((batch,), 64, dtype=torch.int32, device=DEV)
+    idx = torch.full((batch, s_next, topk), -1, dtype=torch.int32, device=DEV)
+    out = torch.empty((batch, s_next, h_q, 512), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((batch, s_next, h_q), dtype=torch.float32, device=DEV)
+    st = lib.sparse_mla_decode_noalloc(P(q), P(cache), P(table), P(lens), P(idx), ctypes.c_float(0.1), P(out),
+                                       P(lse), batch, s_next, h_q, 576, 512, topk, 64, 8, 8, None)
     assert st == 6   # SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL, nothing launched
+    # argument errors are reported first, with the codes sparse_mla_decode gives
+    st = lib.sparse_mla_decode_noalloc(P(q), P(cache), P(table), P(lens), P(idx), ctypes.c_float(0.1), P(out),
+                                       P(lse), batch, s_next, h_q, 512, 512, topk, 64, 8, 8, None)
+    assert st == 2   # SPARSE_MLA_ERR_UNSUPPORTED_SHAPE (d_qk)
+    st = lib.sparse_mla_decode_noalloc(None, P(cache), P(table), P(lens), P(idx), ctypes.c_float(0.1), P(out),
+                                       P(lse), batch, s_next, h_q, 576, 512, topk, 64, 8, 8, None)
+    assert st == 1   # SPARSE_MLA_ERR_INVALID_ARG (null q)

@@ -306,6 +306,8 @@ sparse_mla_status_t sparse_mla_debug_valid_count_paged(const int32_t* indices, c
  * list holds the topk visible positions of largest score, equal scores
  * ranked by position (smaller first), in increasing position order, padded
  * with -1; a row with V(t) <= topk lists 0 .. V(t)-1 and is never scored.
+ * A position scoring -inf is never selected (a row with fewer than topk
+ * other positions lists those and pads with -1).
  * Positions are local to the row's sequence, the convention of
  * sparse_mla_fwd_varlen.
  *
@@ -341,8 +343,10 @@ sparse_mla_status_t dsa_indexer_scores(const void* q_idx, const void* k_idx, con
  * scores (layout of dsa_indexer_scores), written to
  * indices[r * topk .. r * topk + topk - 1] (int32).  Rows with V <= topk get
  * the identity list and their scores are not read (scores may be NULL when
- * no row is longer).  Scores are compared as fp32 with -inf allowed; a NaN
- * ranks above +inf.
+ * no row is longer).  Scores are compared as fp32; a NaN with the sign bit
+ * clear ranks above +inf.  A score of -inf (or a NaN with the sign bit set)
+ * is never selected: a row with fewer selectable positions than topk lists
+ * them all and pads with -1.
  */
 sparse_mla_status_t dsa_topk(const float* scores, long long row_stride, const int32_t* cu_seqlens_q,
                              const int32_t* cu_seqlens_kv, int batch, int total_q, int total_kv, int row0,
@@ -381,11 +385,13 @@ sparse_mla_status_t dsa_indexer_topk(const void* q_idx, const void* k_idx, const
  * cache_seqlens int32 [batch].  q_idx bf16 [batch, s_next, h_idx, d_idx],
  * weights fp32 [batch, s_next, h_idx]; rows are numbered b * s_next + j.
  * page_size must be 64 (else SPARSE_MLA_ERR_UNSUPPORTED_SHAPE).  Pages past a
- * request's length are never used in a score; a visible position whose page
+ * request's length are never used in a score.  A visible position whose page
  * index is at or past max_blocks, or whose page id is outside
- * [0, num_blocks), has a zero key (score 0).  Otherwise as dsa_indexer_scores /
- * dsa_indexer_topk (row_stride / max_seqlen_kv: at least the longest
- * cache_seqlens).
+ * [0, num_blocks), has no key: it scores -inf and is never listed (short
+ * rows list only the positions that have a key).  Those are exactly the
+ * positions sparse_mla_decode masks, so no listed entry is dropped by the
+ * decode.  Otherwise as dsa_indexer_scores / dsa_indexer_topk (row_stride /
+ * max_seqlen_kv: at least the longest cache_seqlens).
  */
 sparse_mla_status_t dsa_indexer_scores_paged(const void* q_idx, const void* k_cache, const float* weights,
                                              const int32_t* block_table, const int32_t* cache_seqlens, int batch,

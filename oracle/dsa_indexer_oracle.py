@@ -25,19 +25,28 @@ token t sees positions 0 .. t + s_kv - s_q, i.e.
     V(t) = clip(t + s_kv - s_q + 1, 0, s_kv)   positions.
 
 Selection.  The index list of token t holds the topk visible positions of
-largest I[t,s].  Two points the pages leave open, read here as:
+largest I[t,s].  Three points the pages leave open, read here as:
   * equal scores are ranked by position, the smaller first (this makes the
     selected set unique);
   * the list is written in increasing position order and padded with -1 to
     topk entries (the forward is invariant to list order and reads -1 as
-    masked).
+    masked);
+  * a position whose score is -inf is not selectable: it is never listed,
+    and a row with fewer than topk selectable positions lists those and pads
+    with -1.  -inf is the mask of the attention's own score space (its
+    fully masked row has LSE -inf), so such a position is one the attention
+    could not use.
 With V(t) <= topk every visible position is selected, so the list is
 0 .. V(t)-1 then -1s, and no score is needed: the short-prefill rows of the
 TileLang page's Summary.  Packed (varlen) prefill applies the same rules per
 sequence with local positions, the convention of the packed forward; the
 paged decode form reads a request's keys through its block table, with the
 request's s_next MTP tokens at the end of its cache_seqlens positions (the
-forward's decode convention).
+forward's decode convention).  A visible position whose page lies past the
+block table's width, or whose table entry is outside [0, num_blocks), has no
+key: it scores -inf and is never listed, short rows included.  The paged
+forward masks exactly these positions (an index there reads no row), so the
+indexer never lists an entry the forward would drop.
 
 Pins (tests/test_indexer_oracle_pins.py): a worked example with small integers
 whose scores and selection are computed by hand, positive homogeneity and
@@ -83,13 +92,14 @@ def token_scores(q_t: np.ndarray, w_t: np.ndarray, k_rows: np.ndarray) -> np.nda
 def select_topk(scores: np.ndarray, topk: int) -> np.ndarray:
     """The topk positions of largest score, equal scores ranked by position
     (smaller first), listed in increasing position order and padded with -1.
-    scores [V]; position p is scores[p]."""
-    v = scores.shape[0]
+    Positions scoring -inf are not selectable.  scores [V]; position p is
+    scores[p]."""
     out = np.full(topk, -1, dtype=np.int64)
-    if v == 0:
+    cand = np.nonzero(~np.isneginf(scores))[0]
+    if cand.size == 0:
         return out
-    order = np.lexsort((np.arange(v), -scores))   # by score desc, then position asc
-    take = np.sort(order[:min(topk, v)])
+    order = np.lexsort((cand, -scores[cand]))     # by score desc, then position asc
+    take = np.sort(cand[order[:min(topk, cand.size)]])
     out[:take.shape[0]] = take
     return out
 
@@ -192,13 +202,20 @@ def topk_rows(scores: np.ndarray, lens: Sequence[int], topk: int) -> np.ndarray:
     return out
 
 
+def page_valid(block_table, seqlen: int, page: int, num_blocks: int) -> np.ndarray:
+    """bool [seqlen]: position s of the request has a key, i.e. its page
+    s // page lies inside the block table and the table entry inside
+    [0, num_blocks)."""
+    bt = [int(x) for x in block_table]
+    return np.array([s // page < len(bt) and 0 <= bt[s // page] < num_blocks for s in range(seqlen)],
+                    dtype=bool)
+
+
 def linearise_keys(k_cache, block_table, seqlen: int, page: int) -> np.ndarray:
     """The keys of one request in position order: position s is row s % page
     of physical block block_table[s // page] (a paged key cache laid out like
-    the forward's paged KV cache).  A position whose page lies past the
-    table, or whose table entry is outside [0, num_blocks), has a zero key
-    (the library's stated convention for the paged indexer; such a cache is
-    a caller error the kernel must not read past)."""
+    the forward's paged KV cache).  Positions without a key (page_valid
+    false) hold zeros here; their scores are -inf."""
     kc = _f64(k_cache)
     bt = [int(x) for x in block_table]
     zero = np.zeros(kc.shape[-1])
@@ -210,6 +227,15 @@ def linearise_keys(k_cache, block_table, seqlen: int, page: int) -> np.ndarray:
         return kc[bt[pg], s % page]
     rows = [key(s) for s in range(seqlen)]
     return np.stack(rows) if rows else np.zeros((0, kc.shape[-1]))
+
+
+def paged_row_scores(q_t, w_t, keys: np.ndarray, valid: np.ndarray) -> np.ndarray:
+    """Scores of one decode row over its visible positions (keys [v, D_I],
+    valid [v]): the indexer score where the position has a key, -inf
+    elsewhere."""
+    sc = token_scores(q_t, w_t, keys)
+    sc[~valid] = -np.inf
+    return sc
 
 
 def dsa_indices_paged(q_idx, k_cache, weights, block_table, cache_seqlens, topk: int, page: int,
@@ -228,14 +254,17 @@ def dsa_indices_paged(q_idx, k_cache, weights, block_table, cache_seqlens, topk:
     toks = range(batch * s_next) if rows is None else list(rows)
     out = np.full((len(toks), topk), -1, dtype=np.int64)
     keys = {}
+    num_blocks = k_cache.shape[0]
     for i, r in enumerate(toks):
         b, j = divmod(r, s_next)
         lk = int(cache_seqlens[b])
         v = visible_len(j, s_next, lk)
-        if v <= topk:
-            out[i] = identity_list(v, topk)
+        ok = page_valid(block_table[b], v, page, num_blocks)
+        if v <= topk:   # every position with a key, in order
+            pos = np.nonzero(ok)[0]
+            out[i, :pos.size] = pos
             continue
         if b not in keys:
             keys[b] = linearise_keys(k_cache, block_table[b], lk, page)
-        out[i] = select_topk(token_scores(_f64(q2[r]), _f64(w2[r]), keys[b][:v]), topk)
+        out[i] = select_topk(paged_row_scores(_f64(q2[r]), _f64(w2[r]), keys[b][:v], ok), topk)
     return out

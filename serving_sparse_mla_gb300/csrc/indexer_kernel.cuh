@@ -421,6 +421,14 @@ __device__ __forceinline__ bool idx_epilogue(const IdxParams& p, IdxMisc& m, con
         if (!mbar_wait(smem_u32(&m.acc_full[buf]), (acount >> 1) & 1u, deadline, ab)) return false;
         tc_fence_after();
         const int pos = t * kIdxTile + quarter * 32 + my_pos;
+        // Paged cache: the quarter's 32 positions share one page; a page past
+        // the table or outside the pool gives them no key, and score -inf.
+        bool has_key = true;
+        if (p.block_table != nullptr) {
+          const int pg = t * (kIdxTile / kIdxPage) + quarter * 32 / kIdxPage;
+          const int blk = pg < p.max_blocks ? __ldg(p.block_table + static_cast<size_t>(s.b) * p.max_blocks + pg) : -1;
+          has_key = blk >= 0 && blk < p.num_blocks;
+        }
 #pragma unroll
         for (int bt = 0; bt < NB; ++bt) {
           bool any = false;
@@ -462,7 +470,7 @@ __device__ __forceinline__ bool idx_epilogue(const IdxParams& p, IdxMisc& m, con
             sc += __shfl_xor_sync(0xffffffffu, (li & 1) ? k0 : k1, 1);
             if (pos < vis[jj]) {
               const int r = w.r_first + half * GH + jj;
-              p.scores[static_cast<long long>(r - p.row0) * p.row_stride + pos] = sc;
+              p.scores[static_cast<long long>(r - p.row0) * p.row_stride + pos] = has_key ? sc : -INFINITY;
             }
           }
         }
@@ -599,7 +607,9 @@ struct TopkParams {
   const int32_t* cu_q;        // [batch + 1], null for one dense sequence or a paged cache
   const int32_t* cu_kv;
   const int32_t* seqlens;     // paged cache: [batch] positions per request, else null
+  const int32_t* block_table; // paged cache: [batch, max_blocks] (short rows list keyed positions only)
   int s_next;                 // paged cache: query rows per request
+  int max_blocks, num_blocks; // paged cache
   long long row_stride;
   int total_q, total_kv, batch;
   int row0, n_rows, topk;
@@ -613,11 +623,15 @@ __device__ __forceinline__ uint32_t topk_key(float f) {
   return u ^ ((u & 0x80000000u) ? 0xFFFFFFFFu : 0x80000000u);
 }
 
+// Image of -inf: keys at or below it (-inf, and NaNs with the sign bit set)
+// are never selected.
+constexpr uint32_t kKeyNegInf = 0x007FFFFFu;
+
 // Shared state of one row's selection.
 struct TopkShared {
   int scan[kTopkMaxWarps];
   int scan2[kTopkMaxWarps];
-  int seq, krem;
+  int seq, krem, fin;
   uint32_t bin;
 };
 
@@ -712,6 +726,8 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
                                             const uint32_t* keys, TopkShared& sh) {
   const int tid = static_cast<int>(threadIdx.x);
   const int nq = (n + 3) >> 2;
+  if (tid == 0) sh.fin = 0;
+  __syncthreads();
   // digits of 11, 11 and 10 bits; each pass counts the keys of the current
   // class (those sharing the digits fixed so far)
   uint32_t prefix = 0, pmask = 0;
@@ -723,6 +739,7 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
       for (int i = tid; i < kTopkBins; i += T) hist[i] = 0;
       __syncthreads();
     }
+    int fin = 0;   // first pass: this thread's selectable keys (above -inf)
     for (int q = tid; q < nq; q += T) {
       const uint4 k = topk_keys4<kStaged>(keys, row, q, n);
       const int s = 4 * q;
@@ -730,8 +747,24 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
       if (s + 1 < n && (k.y & pmask) == prefix) atomicAdd(&hist[(k.y >> shift) & bmask], 1u);
       if (s + 2 < n && (k.z & pmask) == prefix) atomicAdd(&hist[(k.z >> shift) & bmask], 1u);
       if (s + 3 < n && (k.w & pmask) == prefix) atomicAdd(&hist[(k.w >> shift) & bmask], 1u);
+      if (d == 0)
+        fin += (k.x > kKeyNegInf) + (s + 1 < n && k.y > kKeyNegInf) + (s + 2 < n && k.z > kKeyNegInf) +
+               (s + 3 < n && k.w > kKeyNegInf);
+    }
+    if (d == 0) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) fin += __shfl_xor_sync(0xffffffffu, fin, o);
+      if ((tid & 31) == 0 && fin) atomicAdd(&sh.fin, fin);
     }
     __syncthreads();
+    if (d == 0 && sh.fin <= topk) {
+      // At most topk selectable keys: take every key above -inf (the
+      // compaction below with the class "above -inf" and none of it partial).
+      prefix = kKeyNegInf;
+      pmask = 0xFFFFFFFFu;
+      krem = 0;
+      break;
+    }
     topk_find_bin<T>(hist, static_cast<int>(bmask) + 1, krem, sh);
     prefix |= sh.bin << shift;
     pmask |= bmask << shift;
@@ -776,6 +809,9 @@ __device__ __forceinline__ void topk_select(const float* row, int n, int topk, i
       if (take) out[pos++] = s + j;
     }
   }
+  // fewer selectable keys than topk: pad with -1
+  const int picked = sh.fin < topk ? sh.fin : topk;
+  for (int i = picked + tid; i < topk; i += T) out[i] = -1;
 }
 
 template <int T>
@@ -819,7 +855,34 @@ __global__ void __launch_bounds__(T, T == 256 ? 4 : 1) dsa_topk_kernel(const __g
     v = p.topk;
   }
   if (v <= p.topk) {
-    for (int i = tid; i < p.topk; i += T) out[i] = i < v ? i : -1;
+    if (p.block_table == nullptr) {
+      for (int i = tid; i < p.topk; i += T) out[i] = i < v ? i : -1;
+      return;
+    }
+    // Paged cache: the positions that have a key, in order (a page past the
+    // table or outside the pool has none), padded with -1.  Thread t owns a
+    // run of pages; one block scan places its positions.
+    const int32_t* btr = p.block_table + static_cast<long long>(r / p.s_next) * p.max_blocks;
+    const int vv = static_cast<int>(v);
+    const int npg = (vv + kIdxPage - 1) / kIdxPage;
+    const int per = (npg + T - 1) / T;
+    const int g0 = tid * per < npg ? tid * per : npg, g1 = g0 + per < npg ? g0 + per : npg;
+    int cnt = 0;
+    for (int g = g0; g < g1; ++g) {
+      const int blk = g < p.max_blocks ? btr[g] : -1;
+      if (blk >= 0 && blk < p.num_blocks) cnt += (vv - g * kIdxPage < kIdxPage ? vv - g * kIdxPage : kIdxPage);
+    }
+    int before, unused;
+    topk_block_scan2<T>(cnt, 0, sh, before, unused);
+    if (tid == T - 1) sh.krem = before + cnt;
+    int o = before;
+    for (int g = g0; g < g1; ++g) {
+      const int blk = g < p.max_blocks ? btr[g] : -1;
+      if (blk >= 0 && blk < p.num_blocks)
+        for (int i = g * kIdxPage; i < vv && i < (g + 1) * kIdxPage; ++i) out[o++] = i;
+    }
+    __syncthreads();
+    for (int i = sh.krem + tid; i < p.topk; i += T) out[i] = -1;
     return;
   }
   if (v > p.row_stride) {

@@ -810,6 +810,9 @@ sparse_mla_status_t launch_topk(const float* scores, long long row_stride, const
   p.cu_q = paged ? nullptr : sq.cu_q;
   p.cu_kv = paged ? nullptr : sq.cu_kv;
   p.seqlens = paged ? sq.seqlens : nullptr;
+  p.block_table = paged ? sq.block_table : nullptr;
+  p.max_blocks = sq.max_blocks;
+  p.num_blocks = sq.num_blocks;
   p.s_next = sq.s_next;
   p.row_stride = row_stride;
   p.total_q = total_q;

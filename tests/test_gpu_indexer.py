@@ -131,11 +131,18 @@ def test_topk_long_rows_exact(smla, rows, width):
 
 
 def test_topk_constant_row_takes_first_positions(smla):
-    sc = torch.zeros((3, 5000))
+    """A constant row takes its first positions; a row of -inf selects
+    nothing (-inf is never selectable); a row with fewer finite scores than
+    topk lists those and pads with -1."""
+    sc = torch.zeros((4, 5000))
     sc[1] = float("-inf")
-    got = smla.dsa_topk(sc.to(DEV), 100, 3, 5000).cpu().numpy()
-    for i in range(3):
+    sc[3] = float("-inf")
+    sc[3, 4000:4030] = 1.0
+    got = smla.dsa_topk(sc.to(DEV), 100, 4, 5000).cpu().numpy()
+    for i in (0, 2):
         np.testing.assert_array_equal(got[i], np.arange(100))
+    assert np.all(got[1] == -1)
+    np.testing.assert_array_equal(got[3], np.concatenate([np.arange(4000, 4030), np.full(70, -1)]))
 
 
 def test_topk_varlen_exact(smla):
@@ -331,35 +338,44 @@ def _pdev(c):
     return (c.q_idx.to(DEV), c.k_cache.to(DEV), c.weights.to(DEV), c.block_table.to(DEV), c.cache_seqlens.to(DEV))
 
 
-def _paged_row_ref(c, r, keys_cache):
+def _paged_row_ref(c, r, keys_cache, block_table=None):
+    """Oracle scores of decode row r (-inf where a position has no key),
+    their per-element bounds and the row's visible length."""
+    bt = c.block_table if block_table is None else block_table
     s_next = c.q_idx.shape[1]
     b, j = divmod(r, s_next)
     lk = int(c.cache_seqlens[b])
     v = ido.visible_len(j, s_next, lk)
     if b not in keys_cache:
-        keys_cache[b] = ido.linearise_keys(c.k_cache, c.block_table[b], lk, c.page)
+        keys_cache[b] = ido.linearise_keys(c.k_cache, bt[b], lk, c.page)
     k = keys_cache[b][:v]
     q = c.q_idx[b, j].double().numpy()
     w = c.weights[b, j].double().numpy()
-    ref = ido.token_scores(q, w, k)
+    ref = ido.paged_row_scores(q, w, k, ido.page_valid(bt[b], v, c.page, c.k_cache.shape[0]))
     bound = np.abs(w) @ (GAMMA_DOT * (np.abs(q) @ np.abs(k).T)) + GAMMA_SUM * (np.abs(w) @ np.maximum(q @ k.T, 0.0))
     return ref, bound + 1e-30, v
 
 
-def _check_paged_list(c, lst, r, topk, keys_cache):
-    ref, bound, v = _paged_row_ref(c, r, keys_cache)
+def _check_paged_list(c, lst, r, topk, keys_cache, block_table=None):
+    """Validity of one decode row's list (only positions with a key, in
+    order, -1 padded), its order within the score bounds, and equality with
+    the oracle's list where the oracle's top-k boundary gap exceeds twice the
+    bound.  Returns whether the row was compared exactly."""
+    ref, bound, v = _paged_row_ref(c, r, keys_cache, block_table)
     lst = np.asarray(lst)
-    n = min(topk, v)
+    keyed = np.nonzero(~np.isneginf(ref))[0]
+    n = min(topk, keyed.size)
     assert np.all(lst[n:] == -1), f"row {r}: padding"
     sel = lst[:n]
-    assert np.all(sel >= 0) and np.all(sel < v) and np.all(np.diff(sel) > 0), f"row {r}: invalid list"
-    if v <= topk:
-        np.testing.assert_array_equal(sel, np.arange(v))
+    assert np.all(np.isin(sel, keyed)) and np.all(np.diff(sel) > 0), f"row {r}: invalid list"
+    if keyed.size <= topk:
+        np.testing.assert_array_equal(sel, keyed)
         return True
     chosen = np.zeros(v, dtype=bool)
     chosen[sel] = True
-    assert (ref + bound)[chosen].min() >= (ref - bound)[~chosen].max(), f"row {r}: order beyond the bounds"
-    srt = np.sort(ref)[::-1]
+    others = ~chosen & ~np.isneginf(ref)
+    assert (ref + bound)[chosen].min() >= (ref - bound)[others].max(), f"row {r}: order beyond the bounds"
+    srt = np.sort(ref[keyed])[::-1]
     if srt[topk - 1] - srt[topk] > 2.0 * bound.max():
         np.testing.assert_array_equal(sel, ido.select_topk(ref, topk)[:n])
         return True
@@ -375,9 +391,46 @@ def test_paged_scores(smla):
     keys = {}
     for r in range(30):
         ref, bound, v = _paged_row_ref(c, r, keys)
+        assert not np.isneginf(ref).any()
         err = np.abs(got[r, :v].astype(np.float64) - ref)
         assert np.all(err <= bound), f"row {r}: max err {err.max()}"
         assert np.all(np.isneginf(got[r, v:]))
+
+
+def test_paged_invalid_pages_score_minus_inf_and_are_never_listed(smla):
+    """A block table with entries -1 and num_blocks + 3 and a width below the
+    requests' lengths: the positions of those pages score exactly -inf, every
+    other visible position within the bound; the lists hold only keyed
+    positions (exactly the oracle's list where it is unique), and every
+    listed entry is one the paged forward counts as valid (the forward's
+    valid-count export equals the number of listed entries)."""
+    c = mi.indexer_paged_case(556, 4, 6, 300, 1600, topk=256)
+    nb = c.k_cache.shape[0]
+    W = 12                                            # positions >= 768 have no page
+    bt = c.block_table[:, :W].clone()
+    bt[0, 2] = -1
+    bt[1, 0] = nb + 3
+    bt[2, 5] = -1
+    bt[3, 1] = nb
+    max_len = int(c.cache_seqlens.max())
+    d = lambda t: t.to(DEV)
+    q, k, w, _, sl = _pdev(c)
+    got = smla.dsa_indexer_scores_paged(q, k, w, d(bt), sl, max_len).cpu().numpy()
+    keys = {}
+    for r in range(24):
+        ref, bound, v = _paged_row_ref(c, r, keys, bt)
+        none = np.isneginf(ref)
+        assert np.all(np.isneginf(got[r, :v][none])), f"row {r}: a position without a key scored"
+        err = np.abs(got[r, :v][~none].astype(np.float64) - ref[~none])
+        assert np.all(err <= bound[~none]), f"row {r}: max err {err.max()}"
+    for topk in (256, 2048):   # long rows, and rows with fewer keyed positions than topk
+        lst = smla.dsa_indexer_topk_paged(q, k, w, d(bt), sl, topk).cpu()
+        keys = {}
+        for r in range(24):
+            _check_paged_list(c, lst.reshape(24, topk)[r].numpy(), r, topk, keys, bt)
+        idx = lst.reshape(4, 6, topk).to(DEV)
+        counts = smla.debug_valid_count_paged(idx, d(bt), sl, c.page, nb).cpu().numpy()
+        np.testing.assert_array_equal(counts, (lst.reshape(24, topk).numpy() >= 0).sum(axis=1))
 
 
 def test_paged_lists_and_page_shuffle(smla):

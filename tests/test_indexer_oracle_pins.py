@@ -240,26 +240,64 @@ def pin_paged_unused_slots_never_read():
     assert (la >= 0).sum() > 0
 
 
-def pin_paged_invalid_pages_read_as_zero_keys():
+def pin_paged_invalid_pages_never_listed():
     """A page past the block table's width, or a table entry outside the
-    pool, gives zero keys at its positions: the dense oracle over keys built
-    by hand with zero rows there."""
+    pool, gives its positions no key: they are never listed.  Long rows are
+    checked against a brute force over the positions that have a key (the
+    score written out per head, ranked by score then position), including
+    rows with fewer such positions than topk (padded with -1); short rows
+    list exactly those positions, in order."""
     c = mi.indexer_paged_case(86, 1, 4, 300, 300, h_idx=8, d_idx=32, topk=40, spare_pages=0, poison=False)
     nb, page, L = c.k_cache.shape[0], c.page, 300
     bt = c.block_table[:, :4].clone()          # positions 256 .. 299 have no page
     bt[0, 1] = -2
     bt[0, 2] = nb + 7
-    keys = torch.zeros((L, c.k_cache.shape[-1]))
-    for pg in range(4):
-        e = int(bt[0, pg])
-        if 0 <= e < nb:
-            n = min(page, L - pg * page)
-            keys[pg * page: pg * page + n] = c.k_cache[e, :n].float()
-    got = ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, bt, c.cache_seqlens, 40, c.page)
-    ref = ido.dsa_indices(c.q_idx[0], keys, c.weights[0], 40)
-    np.testing.assert_array_equal(got, ref)
-    assert not np.array_equal(got, ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, c.block_table,
-                                                          c.cache_seqlens, 40, c.page))
+    for topk in (40, 200, 300):
+        got = ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, bt, c.cache_seqlens, topk, page)
+        for j in range(4):
+            v = L - 4 + j + 1
+            have = [s for s in range(v) if s // page < 4 and 0 <= int(bt[0, s // page]) < nb]
+            assert len(have) == 128
+            if v <= topk:
+                want = have
+            else:
+                q = c.q_idx[0, j].double().numpy()
+                w = c.weights[0, j].double().numpy()
+                sc = []
+                for s in have:
+                    k = c.k_cache[int(bt[0, s // page]), s % page].double().numpy()
+                    sc.append((sum(w[h] * max(0.0, float(q[h] @ k)) for h in range(8)), s))
+                want = sorted(s for _, s in sorted(sc, key=lambda x: (-x[0], x[1]))[:topk])
+            assert got[j].tolist() == want + [-1] * (topk - len(want)), (topk, j)
+
+
+def pin_selection_never_lists_minus_inf():
+    """Hand-worked: -inf positions are not selectable."""
+    sc = np.array([3.0, -np.inf, 5.0, -np.inf, 1.0])
+    assert ido.select_topk(sc, 2).tolist() == [0, 2]
+    assert ido.select_topk(sc, 4).tolist() == [0, 2, 4, -1]
+    assert ido.select_topk(np.full(3, -np.inf), 2).tolist() == [-1, -1]
+    assert ido.select_topk(np.array([-np.inf, 7.0, 7.0]), 1).tolist() == [1]
+
+
+def pin_paged_lists_are_never_masked_by_the_forward():
+    """The link to the attention's masking: every entry the paged indexer
+    lists is a valid entry of the paged forward (the forward oracle's count
+    of valid entries equals the number of listed positions), with invalid
+    pages in the table, for short and long rows."""
+    from oracle import sparse_mla_oracle as orc
+    c = mi.indexer_paged_case(87, 3, 4, 100, 400, h_idx=8, d_idx=32, topk=64, spare_pages=1, poison=False)
+    nb, page = c.k_cache.shape[0], c.page
+    bt = c.block_table[:, :5].clone()
+    bt[0, 0] = -1
+    bt[1, 3] = nb
+    bt[2, 1] = nb + 2
+    for topk in (64, 512):
+        lst = ido.dsa_indices_paged(c.q_idx, c.k_cache, c.weights, bt, c.cache_seqlens, topk, page)
+        idx = torch.from_numpy(lst).reshape(c.q_idx.shape[0], c.q_idx.shape[1], topk).to(torch.int32)
+        cnt = orc.valid_count_paged(idx, bt, c.cache_seqlens, page, nb)
+        np.testing.assert_array_equal(cnt, (lst >= 0).sum(axis=1))
+        assert (lst >= 0).sum() > 0
 
 
 PINS = [pin_worked_example_scores, pin_worked_example_lists, pin_relu_floor,
@@ -268,7 +306,8 @@ PINS = [pin_worked_example_scores, pin_worked_example_lists, pin_relu_floor,
         pin_scores_selection_consistent, pin_varlen_matches_dense_per_sequence,
         pin_short_rows_reproduce_causal_forward, pin_paged_identity_table_is_dense,
         pin_paged_matches_packed_on_linearised_keys, pin_paged_page_shuffle_invariance,
-        pin_paged_unused_slots_never_read, pin_paged_invalid_pages_read_as_zero_keys]
+        pin_paged_unused_slots_never_read, pin_paged_invalid_pages_never_listed,
+        pin_selection_never_lists_minus_inf, pin_paged_lists_are_never_masked_by_the_forward]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -280,7 +319,8 @@ def test_indexer_pin(pin):
 # planted mistakes
 # ---------------------------------------------------------------------------
 
-_TS, _SEL, _VIS, _LIN = ido.token_scores, ido.select_topk, ido.visible_len, ido.linearise_keys
+_TS, _SEL, _VIS, _LIN, _PV = (ido.token_scores, ido.select_topk, ido.visible_len, ido.linearise_keys,
+                              ido.page_valid)
 
 
 def _lin_ignores_table(k_cache, block_table, seqlen, page):
@@ -335,6 +375,25 @@ def _sel_unsorted(scores, topk):
     return out
 
 
+def _sel_lists_minus_inf(scores, topk):
+    """The previous rule: -inf positions selectable after every other one."""
+    v = scores.shape[0]
+    out = np.full(topk, -1, dtype=np.int64)
+    order = np.lexsort((np.arange(v), -scores))
+    take = np.sort(order[:min(topk, v)])
+    out[:take.shape[0]] = take
+    return out
+
+
+def _pv_ignores_pool(block_table, seqlen, page, num_blocks):
+    return _PV(block_table, seqlen, page, 1 << 30)
+
+
+def _pv_ignores_width(block_table, seqlen, page, num_blocks):
+    bt = [int(x) for x in block_table]
+    return np.array([0 <= bt[min(s // page, len(bt) - 1)] < num_blocks for s in range(seqlen)], dtype=bool)
+
+
 def _short_pad_zero(v, topk):
     out = np.zeros(topk, dtype=np.int64)
     out[:v] = np.arange(v)
@@ -361,6 +420,8 @@ MUTANTS = [("token_scores", _ts_no_relu), ("token_scores", _ts_relu_after_weight
            ("select_topk", _sel_smallest), ("select_topk", _sel_unsorted),
            ("identity_list", _short_pad_zero), ("identity_list", _short_from_one),
            ("linearise_keys", _lin_ignores_table), ("linearise_keys", _lin_table_by_offset),
+           ("select_topk", _sel_lists_minus_inf), ("page_valid", _pv_ignores_pool),
+           ("page_valid", _pv_ignores_width),
            ("visible_len", _vis_off_by_one),
            ("visible_len", _vis_top_left)]
 

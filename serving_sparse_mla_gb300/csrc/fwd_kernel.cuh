@@ -238,8 +238,17 @@ struct Layout {
   static_assert(kNR >= 2, "P^T of the next block needs its own rope slot");
 };
 
+// FP8 cache at 16 heads per CTA: four converter warps after the P.V warp
+// dequantize each value tile as its raw codes land (the other widths convert
+// in the producer warps, one block behind their copies).
+template <int N, bool kFp8>
+__host__ __device__ constexpr int conv_warps() { return (kFp8 && N == 16) ? 4 : 0; }
+template <int N, bool kFp8>
+__host__ __device__ constexpr int fwd_threads() { return Layout<N>::kThreads + 32 * conv_warps<N, kFp8>(); }
+
 struct __align__(16) Misc {
   uint64_t v_full[12], v_empty[12];
+  uint64_t raw_full[12];   // FP8 with converter warps: a value tile's raw codes have landed
   uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   uint64_t q_full, q_empty, s_full[2][2], p_full[2], o_full, drain[3], cand_full, stage_free;
@@ -422,21 +431,6 @@ __device__ __forceinline__ void cp_async_arrive_on(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// 16 bytes from global memory through the non-coherent path, not kept in L1
-// (gathered cache rows are read once).
-__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ float4 ldg_stream_f4(const void* p) {
-  const uint4 v = ldg_stream_v4(p);
-  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
-}
-
 // Two e4m3 codes (the low byte first) times a scale -> bf16x2 (round to
 // nearest even): e4m3 -> f16 is exact, the product is formed in fp32.
 __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_codes, float scale) {
@@ -449,6 +443,69 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_codes, flo
 
 // ------------------------------------------------------------------ producer
 
+// FP8 gather, second half: block nb's four value tiles, whose raw e4m3 codes
+// (in each slot's second chunk) and tile scales (in the first tile's first
+// chunk, two rows per row group of 16) have landed (wait_tile(u, slot)
+// returns once tile u's have, false on a timeout), are dequantized in place
+// into the 128B-swizzled bf16 layout the MMA descriptors read; then each
+// tile's full barrier gets this thread's arrival.  Row group `warp` (rows
+// 16 warp .. 16 warp + 15): a lane converts 16 codes of one row per value
+// tile, the bytes that the producer lane of the same position copied.  The
+// scales are read before any store (the first tile's stores overwrite them),
+// and every row group's codes are read before its stores (a row's bf16
+// second chunk overwrites its codes).
+template <class L, class M, class Wait>
+__device__ __forceinline__ bool fp8_convert_block(M& m, uint32_t vbase, int nb, int warp, int sel, int piece,
+                                                  Wait&& wait_tile) {
+  const int ch = piece >> 2, pc = (piece & 3) * 2;
+  const uint8_t* gbase = reinterpret_cast<const uint8_t*>(&m) - smem_u32(&m);   // generic address of shared offset 0
+  float sc[4][4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const uint32_t s = (static_cast<uint32_t>(nb) * 4u + static_cast<uint32_t>(u)) % L::kNV;
+    if (!wait_tile(u, s)) return false;
+    const uint32_t dst = vbase + s * kPairBytes;
+    const uint8_t* tile = gbase + dst;
+    if (u == 0) {
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const float4 f = *reinterpret_cast<const float4*>(tile + warp * 2048 + (it * 4 + sel) * 16);
+        sc[it][0] = f.x;
+        sc[it][1] = f.y;
+        sc[it][2] = f.z;
+        sc[it][3] = f.w;
+      }
+    }
+    // The row group's codes of this tile (all four row sets in flight), then
+    // the stores: the second chunk's bf16 rows overwrite the codes, and the
+    // first tile's first chunk the scales.
+    uint4 c[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it)
+      c[it] = *reinterpret_cast<const uint4*>(tile + kChunkBytes + (warp * 16 + it * 4 + sel) * 128 + piece * 16);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int r = warp * 16 + it * 4 + sel;
+      const float f = sc[it][u];
+      // 16 codes: columns 128 u + 16 piece .. + 15 = chunk piece / 4, 8-column
+      // pieces 2 (piece % 4) and 2 (piece % 4) + 1 of row r
+      const uint32_t at = dst + ch * kChunkBytes + r * 128;
+      st_shared_v4(at + ((pc ^ (r & 7)) << 4), e4m3x2_scaled_bf16x2(c[it].x, f),
+                   e4m3x2_scaled_bf16x2(c[it].x >> 16, f), e4m3x2_scaled_bf16x2(c[it].y, f),
+                   e4m3x2_scaled_bf16x2(c[it].y >> 16, f));
+      st_shared_v4(at + (((pc + 1) ^ (r & 7)) << 4), e4m3x2_scaled_bf16x2(c[it].z, f),
+                   e4m3x2_scaled_bf16x2(c[it].z >> 16, f), e4m3x2_scaled_bf16x2(c[it].w, f),
+                   e4m3x2_scaled_bf16x2(c[it].w >> 16, f));
+    }
+    // the tile's bf16 rows are written: order them before the tensor core's
+    // reads (async proxy) and arrive on its full barrier
+    fence_proxy_async_smem();
+    mbar_arrive(smem_u32(&m.v_full[s]));
+  }
+  return true;
+}
+
 // The gather producer, shared with the backward kernel: L gives the shared
 // memory layout (ring sizes and offsets), M the barrier block (same member
 // names), and kRows also publishes each block's 64 KV rows (entry r of the
@@ -457,7 +514,10 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_bf16x2(uint32_t two_codes, flo
 // ballots but copies and publishes nothing: it adds each item's number of
 // valid entries to p.valid_count[token] (the debug count export).
 // kFp8 gathers FP8 cache slots (kPagedFp8) and dequantizes them to bf16.
-template <int N, class L, class M, bool kRows, bool kCausalList = false, bool kCount = false, bool kFp8 = false>
+// kConv (with kFp8): converter warps dequantize the tiles; the producer only
+// copies, and each value tile's raw codes arrive on raw_full.
+template <int N, class L, class M, bool kRows, bool kCausalList = false, bool kCount = false, bool kFp8 = false,
+          bool kConv = false>
 __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
   const int warp = static_cast<int>(threadIdx.x >> 5);   // 0..3
   const int lane = static_cast<int>(lane_id());
@@ -598,29 +658,6 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
             n_chunks = 1;
           }
         };
-        // FP8 cache: the block's e4m3 codes (16 per lane, row and value tile)
-        // and its rows' tile scales go to registers first, all loads in flight
-        // together; each value tile is dequantized into its ring slot once the
-        // slot is free.  Masked rows keep codes and scales 0 (a zero row).
-        uint4 codes[4][4];
-        float scl[4][4];
-        if constexpr (kFp8) {
-          const uint8_t* kv8 = reinterpret_cast<const uint8_t*>(p.kv);
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int row = myrow[it];
-            const uint8_t* base = kv8 + static_cast<size_t>(row < 0 ? 0 : row) * kFp8SlotBytes;
-            float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (row >= 0) sc = ldg_stream_f4(base + kFp8ScaleOff);
-            scl[it][0] = sc.x;
-            scl[it][1] = sc.y;
-            scl[it][2] = sc.z;
-            scl[it][3] = sc.w;
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              codes[u][it] = row >= 0 ? ldg_stream_v4(base + u * 128 + piece * 16) : make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
         // One tile's copies into its (free) slot, then the arrival on its full
         // barrier: cp.async with a hardware arrival, or (FP8 value tiles)
         // dequantize, store, fence for the tensor core's proxy and arrive.
@@ -628,24 +665,28 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
           const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
           if constexpr (kFp8) {
             if (u < 4) {
-              // 16 codes of row r: columns 128 u + 16 piece .. + 15, i.e. 64-column
-              // chunk piece / 4, 8-column pieces 2 (piece % 4) and 2 (piece % 4) + 1.
-              const int ch = piece >> 2, pc = (piece & 3) * 2;
+              // Raw e4m3 codes of the tile's 128 columns into the slot's second
+              // 64-column chunk (row r at r * 128, unswizzled), and with the
+              // first value tile the rows' four tile scales into the first two
+              // rows of this row group in that slot's first chunk; both are
+              // converted in place (fp8_convert_block), by the converter warps
+              // once raw_full completes, or by this warp one block later.
+              // Masked rows are zero-filled (codes and scales 0: a zero row).
 #pragma unroll
               for (int it = 0; it < 4; ++it) {
                 const int r = warp * 16 + it * 4 + sel;
-                const uint4 c = codes[u][it];
-                const float sc = scl[it][u];
-                const uint32_t at = dst + ch * kChunkBytes + r * 128;
-                st_shared_v4(at + ((pc ^ (r & 7)) << 4), e4m3x2_scaled_bf16x2(c.x, sc),
-                             e4m3x2_scaled_bf16x2(c.x >> 16, sc), e4m3x2_scaled_bf16x2(c.y, sc),
-                             e4m3x2_scaled_bf16x2(c.y >> 16, sc));
-                st_shared_v4(at + (((pc + 1) ^ (r & 7)) << 4), e4m3x2_scaled_bf16x2(c.z, sc),
-                             e4m3x2_scaled_bf16x2(c.z >> 16, sc), e4m3x2_scaled_bf16x2(c.w, sc),
-                             e4m3x2_scaled_bf16x2(c.w >> 16, sc));
+                const int src_row = myrow[it];
+                const uint8_t* slot_src = reinterpret_cast<const uint8_t*>(p.kv) +
+                                          static_cast<size_t>(src_row < 0 ? 0 : src_row) * kFp8SlotBytes;
+                cp_async_16(dst + kChunkBytes + r * 128 + piece * 16, slot_src + u * 128 + piece * 16,
+                            src_row < 0 ? 0u : 16u);
+                if (u == 0 && piece == 0)
+                  cp_async_16(dst + warp * 2048 + (it * 4 + sel) * 16, slot_src + kFp8ScaleOff, src_row < 0 ? 0u : 16u);
               }
-              fence_proxy_async_smem();
-              mbar_arrive(full);
+              if constexpr (kConv) {
+                const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+                cp_async_arrive_on(smem_u32(&m.raw_full[vi % L::kNV]));
+              }
               return;
             }
           }
@@ -729,6 +770,15 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
               if (!wait_and_copy(step)) return false;
           }
         }
+        if constexpr (kFp8 && !kConv) {
+          // This block's copies form one group; the previous block's group has
+          // landed once at most this one is pending: convert that block.
+          asm volatile("cp.async.commit_group;" ::: "memory");
+          if (n > 0) {
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+            fp8_convert_block<L>(m, vbase, n - 1, warp, sel, piece, [](int, uint32_t) { return true; });
+          }
+        }
         ++n;
         ++ni;
       }
@@ -751,6 +801,12 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
     }
     ++ni;
   }
+  if constexpr (kFp8 && !kConv) {
+    if (n > 0) {   // the last block's copies
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      fp8_convert_block<L>(m, vbase, n - 1, warp, sel, piece, [](int, uint32_t) { return true; });
+    }
+  }
   return true;
 }
 
@@ -758,10 +814,52 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
 // (decided once per launch, so the list walk carries no per-entry branch).
 template <int N, bool kFp8>
 __device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
-  if constexpr (kFp8) return run_producer_t<N, Layout<N>, Misc, false, false, false, true>(p, m, sbase);
+  if constexpr (kFp8)
+    return run_producer_t<N, Layout<N>, Misc, false, false, false, true, (conv_warps<N, kFp8>() > 0)>(p, m, sbase);
   else
     return p.mode == kCausal ? run_producer_t<N, Layout<N>, Misc, false, true>(p, m, sbase)
                              : run_producer_t<N, Layout<N>, Misc, false, false>(p, m, sbase);
+}
+
+// ------------------------------------------------------------------ FP8 converters
+
+// Converter warp cw (0..3) of the FP8 decode at 16 heads: follows the block
+// sequence through the info ring like the consumers and, per block, waits
+// for its four value tiles' raw codes (raw_full) and dequantizes rows
+// 16 cw .. 16 cw + 15 of each into bf16, arriving on the tiles' full
+// barriers for the QK^T issuers.
+template <int N>
+__device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw) {
+  using L = Layout<N>;
+  const volatile int* ab = &m.abort_flag;
+  const uint32_t vbase = smem_u32(sbase + L::kVOff);
+  const int lane = static_cast<int>(lane_id());
+  int n = 0, ni = 0;
+  ItemIter iter = items_begin(p);
+  Item item;
+  while (next_item(p, iter, item)) {
+    const uint64_t deadline = global_timer_ns() + p.timeout_ns;   // every wait of this item is bounded from here
+    for (;;) {
+      const int k = ni % kInfoDepth;
+      const bool ok = mbar_wait(smem_u32(&m.info_full[k]), (ni / kInfoDepth) & 1, deadline, ab);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
+      ++ni;
+      if (blk < 0) break;
+      // each tile once its raw codes have landed
+      const int nb = n;
+      auto wait_raw = [&](int u, uint32_t slot) {
+        const uint32_t vi = static_cast<uint32_t>(nb) * 4u + static_cast<uint32_t>(u);
+        const bool rok = mbar_wait(smem_u32(&m.raw_full[slot]), (vi / L::kNV) & 1u, deadline, ab);
+        return __all_sync(0xffffffffu, rok);
+      };
+      if (!fp8_convert_block<L>(m, vbase, n, cw, lane >> 3, lane & 7, wait_raw)) return false;
+      ++n;
+    }
+  }
+  return true;
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -1190,8 +1288,9 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 
 // kFp8: the FP8-cache instantiation (kPagedFp8); only the gather differs.
 template <int N, bool kFp8 = false>
-__global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Layout<N>;
+  constexpr int kConvWarps = conv_warps<N, kFp8>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Misc& m = *reinterpret_cast<Misc*>(sbase + L::kMiscOff);
@@ -1200,8 +1299,9 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNV; ++i) {
-      mbar_init(smem_u32(&m.v_full[i]), kProducerWarps * 32);
+      mbar_init(smem_u32(&m.v_full[i]), kProducerWarps * 32);   // producer or converter threads
       mbar_init(smem_u32(&m.v_empty[i]), 1);
+      mbar_init(smem_u32(&m.raw_full[i]), kProducerWarps * 32);
     }
     for (int i = 0; i < L::kNR; ++i) {
       mbar_init(smem_u32(&m.rp_full[i]), kProducerWarps * 32);
@@ -1209,7 +1309,7 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
     }
     for (int i = 0; i < kInfoDepth; ++i) {
       mbar_init(smem_u32(&m.info_full[i]), 1);
-      mbar_init(smem_u32(&m.info_empty[i]), 3 + 4 * L::kGroups);
+      mbar_init(smem_u32(&m.info_empty[i]), 3 + 4 * L::kGroups + kConvWarps);
     }
     mbar_init(smem_u32(&m.q_full), L::kGroups);
     mbar_init(smem_u32(&m.q_empty), 2);                       // the two QK^T issuers
@@ -1256,6 +1356,8 @@ __global__ void __launch_bounds__(Layout<N>::kThreads, 1) sparse_mla_fwd_kernel(
         mbar_wait(smem_u32(&m.drain[role]), 0, global_timer_ns() + 100000000ull, &never);
       }
       __syncwarp();
+    } else if (kConvWarps > 0 && warp > L::kPvWarp) {
+      if (!run_convert<N>(p, m, sbase, warp - L::kPvWarp - 1)) raise_error(m, kErrProducerWait);
     } else {
       const int grp = warp >= softmax_warp0(1) ? 1 : 0;
       if (!run_softmax<N>(p, m, sbase, tmem, grp)) raise_error(m, kErrSoftmaxWait);

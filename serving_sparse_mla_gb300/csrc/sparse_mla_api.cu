@@ -132,11 +132,11 @@ sparse_mla_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(p.ctas));
   if (p.mode == smla::kPagedFp8) {
     if (N == 16)
-      smla::sparse_mla_fwd_kernel<16, true><<<grid, smla::Layout<16>::kThreads, smla::smem_bytes<16>(), stream>>>(p);
+      smla::sparse_mla_fwd_kernel<16, true><<<grid, smla::fwd_threads<16, true>(), smla::smem_bytes<16>(), stream>>>(p);
     else if (N == 32)
-      smla::sparse_mla_fwd_kernel<32, true><<<grid, smla::Layout<32>::kThreads, smla::smem_bytes<32>(), stream>>>(p);
+      smla::sparse_mla_fwd_kernel<32, true><<<grid, smla::fwd_threads<32, true>(), smla::smem_bytes<32>(), stream>>>(p);
     else
-      smla::sparse_mla_fwd_kernel<64, true><<<grid, smla::Layout<64>::kThreads, smla::smem_bytes<64>(), stream>>>(p);
+      smla::sparse_mla_fwd_kernel<64, true><<<grid, smla::fwd_threads<64, true>(), smla::smem_bytes<64>(), stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
   }
   if (N == 16)

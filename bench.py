@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--causal", action="store_true",
                     help="time the indices-free causal entry point on the q/kv of a dense prefill config (1-3); "
                          "FLOPs and bytes then count every causal position")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the paged decode (config 5) over its cache written as FP8 slots (512 e4m3 codes, four "
+                         "fp32 tile scales, 64 bf16 rope values: 656 B per row) through sparse_mla_decode_fp8")
     ap.add_argument("--indexer", action="store_true",
                     help="time the DSA indexer + top-k (dsa_indexer_topk; config 5: dsa_indexer_topk_paged) that "
                          "produces the index lists, on the token shape of config 1-5 with 64 indexer heads of "
@@ -301,14 +304,17 @@ def step_flops(case) -> float:
 
 METRICS = {"fwd": "sparse-MLA fwd TFLOP/s at topk=2048 (nominal FLOPs)",
            "bwd": "sparse-MLA bwd TFLOP/s at topk=2048 (nominal FLOPs)",
-           "causal": "indices-free causal MLA fwd TFLOP/s (every causal position)"}
-MODE_SUFFIX = {"fwd": "", "bwd": " (backward: dq, dkv)", "causal": " (indices-free causal mode)"}
+           "causal": "indices-free causal MLA fwd TFLOP/s (every causal position)",
+           "fp8": "sparse-MLA FP8-cache decode TFLOP/s at topk=2048 (nominal FLOPs)"}
+MODE_SUFFIX = {"fwd": "", "bwd": " (backward: dq, dkv)", "causal": " (indices-free causal mode)",
+               "fp8": ", FP8 cache (656-byte slots)"}
 
 
 def attention_mode(args) -> str:
-    if args.causal and args.bwd:
-        raise SystemExit("--causal and --bwd are separate modes")
-    return "causal" if args.causal else ("bwd" if args.bwd else "fwd")
+    fp8 = getattr(args, "fp8", False)
+    if int(args.causal) + int(args.bwd) + int(fp8) > 1:
+        raise SystemExit("--causal, --bwd and --fp8 are separate modes")
+    return "causal" if args.causal else ("bwd" if args.bwd else ("fp8" if fp8 else "fwd"))
 
 
 def check_mode(case, mode: str) -> None:
@@ -316,6 +322,8 @@ def check_mode(case, mode: str) -> None:
         raise SystemExit("--causal needs a dense prefill config (1-3)")
     if mode == "bwd" and hasattr(case, "kv_cache"):
         raise SystemExit("--bwd needs a prefill config (1-4)")
+    if mode == "fp8" and not hasattr(case, "kv_cache"):
+        raise SystemExit("--fp8 needs the paged decode config (5)")
 
 
 def causal_entries(case) -> int:
@@ -379,10 +387,13 @@ def bwd_dout(case, config: int):
 def _oracle_worker_init(config: int, mode: str = "fwd"):
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[v] = "1"
-    global _W_CASE, _W_MODE, _W_DOUT
+    global _W_CASE, _W_MODE, _W_DOUT, _W_CACHE8
     _W_CASE = workload(config)
     _W_MODE = mode
     _W_DOUT = bwd_dout(_W_CASE, config) if mode == "bwd" else None
+    if mode == "fp8":
+        import mla_inputs as mi
+        _W_CACHE8 = mi.quantize_fp8_slots(_W_CASE.kv_cache)
 
 
 def _oracle_bwd_sample(orc, c, dout, tokens):
@@ -410,6 +421,11 @@ def _oracle_worker(tokens):
         orc.causal_mla_fwd(c.q, c.kv, c.sm_scale, tokens=tokens)
     elif _W_MODE == "bwd":
         _oracle_bwd_sample(orc, c, _W_DOUT, tokens)
+    elif _W_MODE == "fp8":
+        from oracle import fp8_kv_oracle as f8
+        toks = [(t // c.s_next, t % c.s_next) for t in tokens]
+        f8.sparse_mla_decode_fp8(c.q, _W_CACHE8, c.block_table, c.cache_seqlens, c.indices, c.sm_scale,
+                                 c.page_size, tokens=toks)
     elif hasattr(c, "kv_cache"):
         toks = [(t // c.s_next, t % c.s_next) for t in tokens]
         orc.sparse_mla_decode(c.q, c.kv_cache, c.block_table, c.cache_seqlens, c.indices, c.sm_scale,
@@ -680,13 +696,17 @@ def run_ours(args, rank, world, dist):
     # The HBM roofline counts the gathered KV rows; the backward's fp32 dkv
     # reductions (576 x 4 B per valid entry and 32-head unit, L2-resident
     # red.global.add) are reported beside it, not as HBM bytes.
-    kv_bytes = valid * KV_ROW_BYTES
+    kv_bytes = valid * (FP8_SLOT_BYTES if mode == "fp8" else KV_ROW_BYTES)
     red_bytes = valid * 2304 * (2 if h_q_of(case) > 16 else 1) if args.bwd else 0
 
     # device-resident inputs
     d = lambda t: t.to(dev)
     if is_decode:
-        inputs = dict(q=d(case.q), kv=d(case.kv_cache), bt=d(case.block_table), sl=d(case.cache_seqlens),
+        kv_in = case.kv_cache
+        if mode == "fp8":
+            import mla_inputs as mi
+            kv_in = mi.quantize_fp8_slots(case.kv_cache)
+        inputs = dict(q=d(case.q), kv=d(kv_in), bt=d(case.block_table), sl=d(case.cache_seqlens),
                       idx=d(case.indices))
         ws = torch.empty(max(1, smla.decode_workspace_size(case.batch, case.s_next, case.h_q, 2048)),
                          dtype=torch.uint8, device=dev)
@@ -716,7 +736,11 @@ def run_ours(args, rank, world, dist):
     lse = torch.empty((n_tok, h_q), dtype=torch.float32, device=dev)
 
     def call(inp):
-        if is_decode:
+        if is_decode and mode == "fp8":
+            smla.sparse_mla_decode_fp8(inp["q"], inp["kv"], inp["bt"], inp["sl"], inp["idx"], case.sm_scale,
+                                       case.page_size, workspace=ws, out=out.view(case.batch, case.s_next, h_q, 512),
+                                       lse=lse.view(case.batch, case.s_next, h_q), stream=stream)
+        elif is_decode:
             smla.sparse_mla_decode(inp["q"], inp["kv"], inp["bt"], inp["sl"], inp["idx"], case.sm_scale,
                                    case.page_size, workspace=ws, out=out.view(case.batch, case.s_next, h_q, 512),
                                    lse=lse.view(case.batch, case.s_next, h_q), stream=stream)
@@ -815,10 +839,12 @@ def run_ours(args, rank, world, dist):
     if bound == "hbm":
         achieved = kv_bytes / (fwd_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": p_bw, "unit": "GB/s",
-                    "frac": achieved / p_bw, "traffic": None if args.causal else profiled_traffic(args.config, "bwd" if args.bwd else "fwd"),
+                    "frac": achieved / p_bw, "traffic": None if args.causal else profiled_traffic("5_fp8" if mode == "fp8" else args.config,
+                                                                                "bwd" if args.bwd else "fwd"),
                     "peak_kind": f"{peak_kind} copy bandwidth (burst)",
                     "algorithmic_bytes_per_launch": kv_bytes,
-                    "note": "achieved = valid entries x 1152 B gathered / mean launch time (cold L2)"}
+                    "note": f"achieved = valid entries x {kv_bytes // max(1, valid)} B gathered / mean launch time "
+                            "(cold L2)"}
     else:
         achieved = flops / (fwd_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": p_tf, "unit": "TFLOP/s",

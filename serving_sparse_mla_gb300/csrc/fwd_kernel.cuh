@@ -251,7 +251,7 @@ struct __align__(16) Misc {
   uint64_t raw_full[12];   // FP8 with converter warps: a value tile's raw codes have landed
   uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
-  uint64_t q_full, q_empty, s_full[2][2], p_full[2], o_full, drain[3], cand_full, stage_free;
+  uint64_t q_full, q_empty, s_full[2][2], p_full[2], o_full, drain[3], cand_full;
   int32_t info_blk[kInfoDepth];
   uint32_t info_mask[kInfoDepth][2];
   uint32_t cand[2][kProducerWarps];
@@ -930,8 +930,10 @@ __device__ bool run_qk(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tme
   uint64_t deadline = 0;
   while (next_item(p, iter, item)) {
     deadline = global_timer_ns() + p.timeout_ns;   // every wait of this item is bounded from here
-      // Q of this item, loaded by the softmax warps.
+      // Q of this item, copied by the softmax warps (cp.async, generic proxy;
+      // the tensor core reads it through the async proxy).
       if (!mbar_wait(smem_u32(&m.q_full), items & 1, deadline, ab)) return false;
+      fence_proxy_async_smem();
       tc_fence_after();
       for (;;) {
         const int k = ni % kInfoDepth;
@@ -1035,36 +1037,34 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   ItemIter iter = items_begin(p);
   Item item;
   uint64_t deadline = 0;
+  // Q rows of this group's heads for unit u -> shared memory, K-major with
+  // the 128B swizzle, by cp.async so all loads are in flight at once; heads
+  // past h_q are zero-filled.  The hardware arrives on q_full for this thread
+  // once its copies have landed (the QK^T issuers fence the async proxy
+  // after acquiring it), so no softmax thread waits on them.
+  auto issue_q = [&](int u) {
+    const int qtok = u / p.groups, qh0 = (u % p.groups) * 64;
+    const int qhv = min(N, p.h_q - qh0);
+    const __nv_bfloat16* qt = p.q + (static_cast<size_t>(qtok) * p.h_q + qh0) * kDqk;
+    for (int x = tid; x < H * 72; x += 128) {
+      const int h = hb + x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
+      const bool live = h < qhv;
+      const __nv_bfloat16* src = qt + static_cast<size_t>(live ? h : 0) * kDqk + c * 64 + piece * 8;
+      cp_async_16(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4), src, live ? 16u : 0u);
+    }
+    cp_async_arrive_on(smem_u32(&m.q_full));
+  };
+  bool q_issued = false;   // the current item's Q copies were issued during the previous item
   while (next_item(p, iter, item)) {
     deadline = global_timer_ns() + p.timeout_ns;   // every wait of this item is bounded from here
     const int tok = item.unit / p.groups;
     const int h0 = (item.unit % p.groups) * 64;
     const int hv = min(N, p.h_q - h0);
-    if (items > 0) {
-      // Q is replaced once the previous item's QK^T MMAs have completed and
-      // every softmax thread has read its staged output back (the staging area
-      // is the Q region).
-      const bool ok = mbar_wait(smem_u32(&m.q_empty), (items - 1) & 1, deadline, ab) &&
-                      mbar_wait(smem_u32(&m.stage_free), (items - 1) & 1, deadline, ab);
-      if (bar_red_or_128(bar_id, !ok)) return false;
-    }
-    // Q rows of this group's heads -> shared memory, K-major with the 128B
-    // swizzle, by cp.async so all loads are in flight at once; heads past h_q
-    // are zero-filled.
-    {
-      const __nv_bfloat16* qt = p.q + (static_cast<size_t>(tok) * p.h_q + h0) * kDqk;
-      for (int x = tid; x < H * 72; x += 128) {
-        const int h = hb + x / 72, rem = x % 72, c = rem >> 3, piece = rem & 7;
-        const bool live = h < hv;
-        const __nv_bfloat16* src = qt + static_cast<size_t>(live ? h : 0) * kDqk + c * 64 + piece * 8;
-        cp_async_16(qbase + c * (N * 128) + h * 128 + ((piece ^ (h & 7)) << 4), src, live ? 16u : 0u);
-      }
-      asm volatile("cp.async.wait_all;" ::: "memory");
-      fence_proxy_async_smem();
-      if (tid < H) m.mrun[hb + tid] = -INFINITY;
-      named_bar_sync(bar_id, 128);
-      if (tid == 0) mbar_arrive(smem_u32(&m.q_full));
-    }
+    if (!q_issued) issue_q(item.unit);   // the first item (later ones are issued ahead)
+    q_issued = false;
+    // (read after the first block's max barrier; the previous item's
+    // epilogue, the last reader, has finished on this thread's side)
+    if (tid < H) m.mrun[hb + tid] = -INFINITY;
 
     // Head hb+tid's running sum of exp2(s - m) (owner threads tid < H); the
     // per-block sums arrive through m.rsum, reduced over the 64 rows.
@@ -1166,6 +1166,21 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
       ++nl;
     }
 
+    // The next item's Q, once this item's QK^T MMAs (the readers of Q) have
+    // completed: its copies fly during this item's last P.V and epilogue,
+    // which no longer touch the Q region, and the next item's QK^T can start
+    // as soon as they land.
+    {
+      ItemIter peek = iter;
+      Item nx;
+      if (next_item(p, peek, nx)) {
+        const bool qok = mbar_wait(smem_u32(&m.q_empty), items & 1, deadline, ab);
+        if (bar_red_or_128(bar_id, !qok)) return false;
+        issue_q(nx.unit);
+        q_issued = true;
+      }
+    }
+
     // ---------------------------------------------------------- epilogue
     // O^T is complete once the P.V of the item's last block has; an item with
     // no block issued none (and P.V signals nothing for it).
@@ -1222,63 +1237,38 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
         }
       }
     } else {
-    // bf16 output: O^T rows (one dv per thread) are transposed through shared
-    // memory into [head][dv] rows, then written with 16-byte coalesced stores.
-    // The staging area is the Q region: the item's QK^T MMAs are complete and
-    // the next item's Q is loaded only after every softmax thread arrives on
-    // stage_free (the value ring already holds the next item's tiles).
-    // Every group's Q load of this item has landed before any of it is
-  // overwritten (an item without blocks gets here without waiting on QK^T).
-  {
-    const bool qok = mbar_wait(smem_u32(&m.q_full), items & 1, deadline, ab);
-    if (bar_red_or_128(bar_id, !qok)) return false;
-  }
-  const uint32_t stage = smem_u32(sbase + L::kQOff) + static_cast<uint32_t>(hb) * (kDv * 2);
+      // bf16 output straight from TMEM: thread (q4, lane) holds dv = 128 mt +
+      // 32 q4 + lane for each head; the lanes of an even/odd pair swap half
+      // their heads so that each stores bf16x2 pairs (dv, dv + 1): a warp
+      // store covers two 64-byte runs of two head rows.
+      const bool odd = (lane & 1) != 0;
+      __nv_bfloat16* orow = p.out + tok_h * kDv;
 #pragma unroll 1
-    for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-      for (int g = 0; g < H / 16; ++g) {
-        float o[16];
-        if (nl > 0) {
-          tmem_ld16(tO + mt * N + g * 16, o);
-          tmem_wait_ld();
-        } else {
+        for (int g = 0; g < H / 16; ++g) {
+          float o[16];
+          if (nl > 0) {
+            tmem_ld16(tO + mt * N + g * 16, o);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = 0.f;
+            for (int i = 0; i < 16; ++i) o[i] = 0.f;
+          }
+          const int dv0 = mt * 128 + q4 * 32 + (lane & ~1);
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            // even lane: head i with the odd lane's dv; odd lane: head i + 1 with the even lane's
+            const float mine = odd ? o[i + 1] * fin[g * 16 + i + 1] : o[i] * fin[g * 16 + i];
+            const float give = odd ? o[i] * fin[g * 16 + i] : o[i + 1] * fin[g * 16 + i + 1];
+            const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+            const int hl = g * 16 + i + (odd ? 1 : 0);
+            const uint32_t v = odd ? pack_bf16x2(got, mine) : pack_bf16x2(mine, got);
+            if (hb + hl < hv) *reinterpret_cast<uint32_t*>(orow + static_cast<size_t>(hb + hl) * kDv + dv0) = v;
+          }
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int hl = g * 16 + i;
-          const __nv_bfloat16 v = __float2bfloat16_rn(o[i] * fin[hl]);
-          const uint32_t addr = stage + static_cast<uint32_t>(hl * kDv + mt * 128 + dvrow) * 2u;
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&v)));
-        }
       }
     }
-    named_bar_sync(bar_id, 128);
-    // Rows of 512 dv, 16 bytes per thread: four shared loads in flight, then
-    // four global stores.
-    constexpr int kRounds = H * (kDv / 8) / 128;
-    static_assert(kRounds % 4 == 0, "store rounds");
-#pragma unroll 1
-    for (int r0 = 0; r0 < kRounds; r0 += 4) {
-      uint4 v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int x = tid + (r0 + j) * 128;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v[j].x), "=r"(v[j].y), "=r"(v[j].z), "=r"(v[j].w)
-                     : "r"(stage + static_cast<uint32_t>(x) * 16u));
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int x = tid + (r0 + j) * 128;
-        const int hl = x / (kDv / 8), c8 = x % (kDv / 8);
-        if (hb + hl < hv) *reinterpret_cast<uint4*>(p.out + (tok_h + hb + hl) * kDv + c8 * 8) = v[j];
-      }
-    }
-    }
-    mbar_arrive(smem_u32(&m.stage_free));
     ++items;
   }
   return true;
@@ -1311,9 +1301,8 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
       mbar_init(smem_u32(&m.info_full[i]), 1);
       mbar_init(smem_u32(&m.info_empty[i]), 3 + 4 * L::kGroups + kConvWarps);
     }
-    mbar_init(smem_u32(&m.q_full), L::kGroups);
+    mbar_init(smem_u32(&m.q_full), 128 * L::kGroups);         // every softmax thread's Q copies (noinc)
     mbar_init(smem_u32(&m.q_empty), 2);                       // the two QK^T issuers
-    mbar_init(smem_u32(&m.stage_free), 128 * L::kGroups);     // every softmax thread
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&m.s_full[0][i]), 1);
       mbar_init(smem_u32(&m.s_full[1][i]), 1);
@@ -1361,6 +1350,8 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
     } else {
       const int grp = warp >= softmax_warp0(1) ? 1 : 0;
       if (!run_softmax<N>(p, m, sbase, tmem, grp)) raise_error(m, kErrSoftmaxWait);
+      // Drain: this thread's Q copies have landed before the CTA can exit.
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
   }
   tc_fence_before();

@@ -140,3 +140,98 @@ def check_all_tokens(layout: str, q, kv, indices, gpu_out, gpu_lse, sm_scale: fl
             "tight": max(p["tight"] for p in parts),
             "tight_full": max(p["tight_full"] for p in parts),
             "fail": next((p["fail"] for p in parts if p["fail"]), None)}
+
+
+# ---------------------------------------------------------------------------
+# the backward's heavily shared dkv rows, over every token that lists them
+# ---------------------------------------------------------------------------
+
+def _bits_to_bf16(bits: np.ndarray):
+    import torch
+    return torch.from_numpy(np.array(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def _fwd_shard(payload):
+    """Oracle forward of a shard: out as bf16 bits (rounded once, as the
+    forward's output is) and the LSE as float32."""
+    import torch
+    from oracle import sparse_mla_oracle as orc
+    toks, q_bits, idx = payload
+    kv = _bits_to_bf16(np.asarray(_W["kv"]))
+    o, l = orc.sparse_mla_fwd(_bits_to_bf16(q_bits), kv, torch.from_numpy(idx), _W["sm_scale"])
+    return toks, _bits(torch.from_numpy(o).to(torch.bfloat16)), l.astype(np.float32)
+
+
+def _bwd_rows_shard(payload):
+    """The shard's tokens' contributions to dkv of the target rows, and of
+    the per-element bounds of tests/parity.py (the backward given the oracle
+    forward's out rounded to bf16)."""
+    import torch
+    from oracle import sparse_mla_oracle as orc
+    from tests.parity import bf16_rounding_err, grad_term_bounds
+    q_bits, idx, do_bits, rows = payload
+    kv = _bits_to_bf16(np.asarray(_W["kv"]))
+    q, dout, it = _bits_to_bf16(q_bits), _bits_to_bf16(do_bits), torch.from_numpy(idx)
+    _, dkv = orc.sparse_mla_bwd(q, kv, it, _W["sm_scale"], dout)
+    _, bkv = grad_term_bounds(q, kv, it, _W["sm_scale"], dout, bf16_rounding_err)
+    return dkv[rows], bkv[rows]
+
+
+def _dense_pool(kv, sm_scale, cores):
+    import multiprocessing as mp
+    tmp = tempfile.mkdtemp(prefix="oracle_pool_")
+    path = os.path.join(tmp, "kv.npy")
+    np.save(path, _bits(kv))
+    saved = {v: os.environ.get(v) for v in _THREAD_VARS}
+    os.environ.update({v: "1" for v in _THREAD_VARS})
+    try:
+        pool = mp.get_context("spawn").Pool(cores or (os.cpu_count() or 1), initializer=_init,
+                                            initargs=("dense", path, sm_scale, {}))
+    finally:
+        for v, old in saved.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+    return pool, tmp
+
+
+def oracle_fwd_dense_all(q, kv, indices, sm_scale: float, cores: int = 0, shard_tokens: int = 32):
+    """The oracle forward of every token of a dense-layout workload on the
+    host cores: (out bf16 [n, h, 512], lse float32 [n, h]) CPU tensors."""
+    import torch
+    n = q.shape[0]
+    qb, idx = _bits(q), indices.reshape(n, -1).numpy().astype(np.int64)
+    pool, tmp = _dense_pool(kv, sm_scale, cores)
+    try:
+        parts = pool.map(_fwd_shard, [(np.arange(a, min(n, a + shard_tokens)), qb[a:a + shard_tokens].copy(),
+                                       idx[a:a + shard_tokens]) for a in range(0, n, shard_tokens)], chunksize=1)
+    finally:
+        pool.close()
+        pool.join()
+        shutil.rmtree(tmp, ignore_errors=True)
+    out = np.concatenate([p[1] for p in parts])
+    lse = np.concatenate([p[2] for p in parts])
+    return _bits_to_bf16(out), torch.from_numpy(lse)
+
+
+def oracle_bwd_dense_rows(q, kv, indices, dout, sm_scale: float, rows, cores: int = 0, shard_tokens: int = 32):
+    """dkv of the given rows over every token of a dense-layout workload (the
+    oracle's backward summed over token shards on the host cores), with the
+    summed per-element bounds: (ref [R, 576], bound [R, 576]) float64."""
+    n = q.shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    qb, db = _bits(q), _bits(dout)
+    idx = indices.reshape(n, -1).numpy().astype(np.int64)
+    # only the tokens that list a target row contribute to it
+    toks = np.nonzero(np.isin(idx, rows).any(axis=1))[0]
+    pool, tmp = _dense_pool(kv, sm_scale, cores)
+    try:
+        parts = pool.map(_bwd_rows_shard, [(qb[toks[a:a + shard_tokens]], idx[toks[a:a + shard_tokens]],
+                                            db[toks[a:a + shard_tokens]], rows)
+                                           for a in range(0, toks.size, shard_tokens)], chunksize=1)
+    finally:
+        pool.close()
+        pool.join()
+        shutil.rmtree(tmp, ignore_errors=True)
+    return sum(p[0] for p in parts), sum(p[1] for p in parts), int(toks.size)

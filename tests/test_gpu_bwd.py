@@ -7,7 +7,8 @@ import torch
 
 import mla_inputs as mi
 from oracle import sparse_mla_oracle as orc
-from tests.parity import bf16_rounding_err, compare_grad, forward_parity_err, grad_term_bounds
+from tests.oracle_pool import oracle_bwd_dense_rows, oracle_fwd_dense_all
+from tests.parity import bf16_rounding_err, compare_grad, forward_parity_err, grad_term_bounds, record
 
 pytestmark = pytest.mark.gpu
 
@@ -181,3 +182,26 @@ def test_bwd_wide_head_config_sampled(smla):
     g = np.random.default_rng(31)
     toks = sorted(set([0, 1, 127, 128, 2047, 2048, 4095, 8191] + g.choice(8192, 16, replace=False).tolist()))
     _check_bwd_sampled(smla, mi.config(3), toks, [8191, 8150, 8064, 7900], seed=31, what="config 3")
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_bwd_heavily_listed_rows_full_size(smla, cfg):
+    """dkv rows 0 .. 127 at full size (configs 2 and 3, the launch the bench
+    times): almost every token lists them, so each sums ~2000-8000 fp32
+    atomic contributions.  The backward is given the oracle forward's out
+    (rounded to bf16) and LSE for every token, and its dkv rows are compared
+    with the oracle's backward summed over every listing token (host cores)."""
+    case = mi.config(cfg)
+    rows = list(range(128))
+    s_q, h = case.q.shape[0], case.q.shape[1]
+    dout = _dout(40 + cfg, (s_q, h, 512))
+    out, lse = oracle_fwd_dense_all(case.q, case.kv, case.indices, case.sm_scale)
+    dq, dkv = smla.sparse_mla_bwd(case.q.to(DEV), case.kv.to(DEV), case.indices.to(DEV), case.sm_scale,
+                                  out.to(DEV), lse.to(DEV), dout.to(DEV))
+    torch.cuda.synchronize()
+    ref, bound, listers = oracle_bwd_dense_rows(case.q, case.kv, case.indices, dout, case.sm_scale, rows)
+    assert listers > 0.9 * s_q
+    worst = compare_grad(dkv[rows].cpu().numpy(), ref, bound, f"config {cfg} dkv rows 0..127")
+    record(f"config {cfg} backward, dkv rows 0..127", listing_tokens=listers,
+           max_ddkv=float(np.abs(dkv[rows].cpu().numpy() - ref).max()), worst_bound_ratio=worst)
+    assert np.all(np.isfinite(dq.cpu().numpy()))

@@ -377,13 +377,15 @@ __device__ __forceinline__ void warp_xreduce(float (&v)[N], int lane, float* dst
 }
 
 // The same butterfly within each 16-lane half of the warp (the halves hold
-// different heads of the same rows); dst is the half's first head.
-template <int V, bool kMax>
+// different heads of the same rows); dst is the half's first head.  kOff0 < 8
+// continues a butterfly whose first levels were taken already (v then holds
+// the heads from dst on).
+template <int V, bool kMax, int kOff0 = 8>
 __device__ __forceinline__ void half_xreduce(float (&v)[V], int lane, float* dst) {
   int cnt = V;
   int base = 0;
 #pragma unroll
-  for (int off = 8; off >= 1; off >>= 1) {
+  for (int off = kOff0; off >= 1; off >>= 1) {
     if (cnt > 1) {
       const int half = cnt >> 1;
       const bool upper = (lane & off) != 0;
@@ -1066,9 +1068,17 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     // epilogue, the last reader, has finished on this thread's side)
     if (tid < H) m.mrun[hb + tid] = -INFINITY;
 
-    // Head hb+tid's running sum of exp2(s - m) (owner threads tid < H); the
-    // per-block sums arrive through m.rsum, reduced over the 64 rows.
-    float lrun = 0.f;
+    // Shares of the running sums of exp2(s - m), kept with the running max:
+    // each block's row values go through the first two levels of the
+    // half-warp butterfly (rows r, r ^ 4, r ^ 8, r ^ 12 of the quarter added),
+    // so this thread holds heads hl0 .. hl0 + HH/4 - 1 of its four rows; the
+    // rest of the butterfly runs once, at the end of the item.
+    constexpr int HQ = HH / 4;
+    const bool up8 = (lane & 8) != 0, up4 = (lane & 4) != 0;
+    const int hl0 = hb + hsub + (up8 ? 2 * HQ : 0) + (up4 ? HQ : 0);
+    float lpart[HQ];
+#pragma unroll
+    for (int i = 0; i < HQ; ++i) lpart[i] = 0.f;
     int nl = 0;   // blocks of this item
     for (;;) {
       const int k = ni % kInfoDepth;
@@ -1076,88 +1086,112 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
       // group's 128 threads, so they all continue or all return together.
       const bool iok = mbar_wait(smem_u32(&m.info_full[k]), (ni / kInfoDepth) & 1, deadline, ab);
       ++ni;
-      if (bar_red_or_128(bar_id, !iok)) return false;
-      const int blk = *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]);
+      const int blk = iok ? *reinterpret_cast<volatile int32_t*>(&m.info_blk[k]) : -1;
       const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(&m.info_mask[k][row & 1]);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
+      bool sok = true;
+      if (blk >= 0)
+        sok = mbar_wait(smem_u32(&m.s_full[0][n & 1]), (n >> 1) & 1, deadline, ab) &&
+              mbar_wait(smem_u32(&m.s_full[1][n & 1]), (n >> 1) & 1, deadline, ab);
+      if (bar_red_or_128(bar_id, !(iok && sok))) return false;
       if (blk < 0) break;
+      tc_fence_after();
       const bool valid = ((bits >> (row >> 1)) & 1u) != 0u;
       const uint32_t tSa = tmem + lane_off + static_cast<uint32_t>(n & 1) * N + hb;        // part 0
       const uint32_t tSb = tmem + lane_off + static_cast<uint32_t>(2 + (n & 1)) * N + hb;  // part 1
 
-      const bool sok = mbar_wait(smem_u32(&m.s_full[0][n & 1]), (n >> 1) & 1, deadline, ab) &&
-                       mbar_wait(smem_u32(&m.s_full[1][n & 1]), (n >> 1) & 1, deadline, ab);
-      tc_fence_after();
-      // Block max per head: butterfly over the half-warp, then over the 4 warps.
-      {
-        float s[HH], t[HH];
-        load_s_half<HH>(tSa, s);
+      // The row's scaled scores (log2 units), masked rows -inf.
+      auto load_scores = [&](float (&v)[HH]) {
+        float t[HH];
+        load_s_half<HH>(tSa, v);
         load_s_half<HH>(tSb, t);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < HH; ++i) s[i] = valid ? (s[i] + t[i]) * p.scale_log2 : -INFINITY;
+        for (int i = 0; i < HH; ++i) v[i] = valid ? (v[i] + t[i]) * p.scale_log2 : -INFINITY;
+      };
+      float s[HH];
+      load_scores(s);
+      // The running maxima move only when a head's block max passes them by
+      // more than 2^8 (lazy rescale), and always with the item's first block.
+      // Any row can see that on its own: only then does the group reduce the
+      // block max over the 64 rows and update the maxima.
+      bool need = nl == 0;
+#pragma unroll
+      for (int i = 0; i < HH; ++i) need |= s[i] > m.mrun[hb + hsub + i] + kLazyRescale;
+      if (bar_red_or_128(bar_id, need)) {
+        // (the reduction consumes s; the scores are read again below)
         half_xreduce<HH, true>(s, lane, m.red[q4] + hb + hsub);
-      }
-      if (bar_red_or_128(bar_id, !sok)) return false;
-      bool grew = false;
-      if (tid < H) {
-        const int h = hb + tid;
-        if (nl > 0) lrun += (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]);
-        const float bm = fmaxf(fmaxf(m.red[0][h], m.red[1][h]), fmaxf(m.red[2][h], m.red[3][h]));
-        const float mo = m.mrun[h];
-        const float mn = (bm > mo + kLazyRescale) ? bm : mo;
-        const float al = fast_exp2(mo - mn);
-        lrun *= al;
-        m.alpha[h] = al;
-        m.mrun[h] = mn;
-        grew = (mn != mo);
-      }
-      const bool rescale = bar_red_or_128(bar_id, grew);
-      if (rescale && nl > 0) {
-        // O^T must hold exactly the blocks before this one: wait for the
-        // previous block's P.V (its last commits release that block's rope /
-        // P^T slot), then rescale this group's head columns.
-        const int pb = n - 1;
-        const bool pok = mbar_wait(smem_u32(&m.rp_empty[pb % L::kNR]), (pb / L::kNR) & 1, deadline, ab);
-        tc_fence_after();
-        if (bar_red_or_128(bar_id, !pok)) return false;
-#pragma unroll 1
-        for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-          for (int g = 0; g < H / 16; ++g) {
-            float o[16];
-            tmem_ld16(tO + mt * N + g * 16, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] *= m.alpha[hb + g * 16 + i];
-            tmem_st16(tO + mt * N + g * 16, o);
-          }
+        named_bar_sync(bar_id, 128);
+        bool grew = false;
+        if (tid < H) {
+          const int h = hb + tid;
+          const float bm = fmaxf(fmaxf(m.red[0][h], m.red[1][h]), fmaxf(m.red[2][h], m.red[3][h]));
+          const float mo = m.mrun[h];
+          const float mn = (bm > mo + kLazyRescale) ? bm : mo;
+          m.alpha[h] = fast_exp2(mo - mn);
+          m.mrun[h] = mn;
+          grew = (mn != mo);
         }
-        tmem_wait_st();
+        const bool rescale = bar_red_or_128(bar_id, grew);
+        if (nl > 0) {
+#pragma unroll
+          for (int i = 0; i < HQ; ++i) lpart[i] *= m.alpha[hl0 + i];
+        }
+        if (rescale && nl > 0) {
+          // O^T must hold exactly the blocks before this one: wait for the
+          // previous block's P.V (its last commits release that block's rope /
+          // P^T slot), then rescale this group's head columns.
+          const int pb = n - 1;
+          const bool pok = mbar_wait(smem_u32(&m.rp_empty[pb % L::kNR]), (pb / L::kNR) & 1, deadline, ab);
+          tc_fence_after();
+          if (bar_red_or_128(bar_id, !pok)) return false;
+#pragma unroll 1
+          for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+            for (int g = 0; g < H / 16; ++g) {
+              float o[16];
+              tmem_ld16(tO + mt * N + g * 16, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] *= m.alpha[hb + g * 16 + i];
+              tmem_st16(tO + mt * N + g * 16, o);
+            }
+          }
+          tmem_wait_st();
+        }
+        load_scores(s);
       }
       // P^T row (bf16) into the rope slot of this block, MN-major swizzled,
-      // and the block's per-head sums of P.
+      // and the row's shares of the sums.
       {
         const uint32_t prow = rbase + (n % L::kNR) * kChunkBytes + row * L::kPRow;
         const uint32_t sw = (static_cast<uint32_t>(row * L::kPRow) >> 7) & static_cast<uint32_t>(L::kPRow / 16 - 1);
-        float s[HH], t[HH];
-        load_s_half<HH>(tSa, s);
-        load_s_half<HH>(tSb, t);
-        tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < HH / 8; ++c) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int h = hb + hsub + c * 8 + i;
-            s[c * 8 + i] = valid ? fast_exp2((s[c * 8 + i] + t[c * 8 + i]) * p.scale_log2 - m.mrun[h]) : 0.f;
+            s[c * 8 + i] = valid ? fast_exp2(s[c * 8 + i] - m.mrun[h]) : 0.f;
           }
           const uint32_t chunk = static_cast<uint32_t>((hb + hsub) / 8 + c);
           st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
                        pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
                        pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
         }
-        half_xreduce<HH, false>(s, lane, m.rsum[q4] + hb + hsub);
+        float h8[2 * HQ];
+#pragma unroll
+        for (int i = 0; i < 2 * HQ; ++i) {
+          const float send = up8 ? s[i] : s[i + 2 * HQ];
+          const float keep = up8 ? s[i + 2 * HQ] : s[i];
+          h8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int i = 0; i < HQ; ++i) {
+          const float send = up4 ? h8[i] : h8[i + HQ];
+          const float keep = up4 ? h8[i + HQ] : h8[i];
+          lpart[i] += keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -1165,6 +1199,9 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
       ++n;
       ++nl;
     }
+    // The item's sums over the 64 rows, per head (published by the barrier
+    // after the o_full wait below).
+    if (nl > 0) half_xreduce<HQ, false, 2>(lpart, lane, m.rsum[q4] + hl0);
 
     // The next item's Q, once this item's QK^T MMAs (the readers of Q) have
     // completed: its copies fly during this item's last P.V and epilogue,
@@ -1193,7 +1230,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
     const size_t tok_h = static_cast<size_t>(tok) * p.h_q + h0;
     if (tid < H) {
       const int h = hb + tid;
-      if (nl > 0) lrun += (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]);
+      const float lrun = nl > 0 ? (m.rsum[0][h] + m.rsum[1][h]) + (m.rsum[2][h] + m.rsum[3][h]) : 0.f;
       float lse;
       if (nl > 0) {
         lse = (m.mrun[h] + log2f(lrun)) * 0.69314718055994530942f;

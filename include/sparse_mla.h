@@ -183,9 +183,12 @@ size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v,
  *   out           bf16 [batch, s_next, h_q, d_v]
  *   lse           fp32 [batch, s_next, h_q]
  *   workspace     device buffer of at least sparse_mla_decode_workspace_size(...)
- *                 bytes (may be NULL when that size is 0); the library writes
- *                 per-split partial results there during the call.  Two calls
- *                 that may run concurrently need separate workspaces.
+ *                 bytes, 16-byte aligned (may be NULL when that size is 0);
+ *                 contents ignored on entry.  The library writes per-split
+ *                 partial results and one arrival counter per (token, 64-head
+ *                 group, softmax group) there during the call (the counters
+ *                 are zeroed on the call's stream before the kernel).  Two
+ *                 calls that may run concurrently need separate workspaces.
  *
  * num_blocks * page_size must fit in int32.
  */
@@ -241,10 +244,11 @@ sparse_mla_status_t sparse_mla_decode_fp8(const void* q, const void* kv_cache, c
  * sparse_mla_decode_workspace_size exceeds that maximum is rejected with
  * SPARSE_MLA_ERR_WORKSPACE_TOO_SMALL before any launch (use
  * sparse_mla_decode with a workspace for it).  The partials take
- * 2 x CTAs x min(h_q, 64) x 513 x 4 bytes: on a 152-SM GB300 with a full
- * grid (any batch x s_next >= 10 at topk 2048) h_q <= 13 fits, so the
- * 8-head MTP decode does, while h_q >= 14 fits only for grids small enough
- * (few tokens, short lists).  The call makes no cudaMalloc, cudaFree or
+ * 2 x CTAs x min(h_q, 64) x 513 x 4 bytes, rounded up to 16, and the merge
+ * counters 8 bytes per (token, 64-head group): on a 152-SM GB300 with a full
+ * grid (any batch x s_next >= 10 at topk 2048) h_q <= 13 fits for up to
+ * 34,000 tokens, so the 8-head MTP decode does, while h_q >= 14 fits only
+ * for grids small enough (few tokens, short lists).  The call makes no cudaMalloc, cudaFree or
  * other allocating call.
  *
  * Every call shares the one scratch array, which keeps the last call's

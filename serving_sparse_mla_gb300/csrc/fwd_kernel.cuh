@@ -116,8 +116,8 @@ constexpr int kFp8RopeOff = 528;
 //   kBlockRanges  the units' index lists, laid end to end as T = units x nb
 //                 blocks of 64 entries, are cut into G equal ranges, one per
 //                 CTA (decode: a few long lists spread over every SM).  A unit
-//                 cut between CTAs leaves a partial result per piece, merged
-//                 by combine_splits_kernel.
+//                 cut between CTAs leaves a partial result per piece; the CTA
+//                 that writes a unit's last piece merges them (merge_row).
 enum Sched : int { kWholeUnits = 0, kBlockRanges = 1 };
 
 enum ErrCode : int { kErrProducerWait = 0x101, kErrMmaWait = 0x201, kErrSoftmaxWait = 0x301 };
@@ -150,6 +150,7 @@ struct FwdParams {
   float* dq;                  // [n_tok, h_q, 576]
   float* dkv;                 // [n_rows, 576], accumulated
   int32_t* valid_count;       // debug count export: [n_tok], zeroed, accumulated
+  int32_t* merge_count;       // kBlockRanges: pieces written per (unit, softmax group), zeroed before the launch
   unsigned long long timeout_ns;
 };
 
@@ -263,6 +264,8 @@ struct __align__(16) Misc {
   uint32_t tmem_base;
   int abort_flag;
   int prior_error;
+  int merge_pieces[2];       // per softmax group: pieces of the unit to merge here (0: none)
+  int merge_slot[2][32];     // their partial slots
 };
 
 template <int N>
@@ -1006,6 +1009,64 @@ __device__ bool run_pv(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tme
 
 // S^T row of this thread's half: HH consecutive heads starting at the
 // half's first head (16x32bx2 read, upper half offset by HH columns).
+// Merge of a unit that kBlockRanges cut between CTAs, for the heads [h_lo,
+// h_hi) of one softmax group (128 threads): LSE = ln sum_s exp(LSE_s),
+// out = sum_s exp(LSE_s - LSE) * O_s, each O_s already normalised over its
+// piece (the LSE merge of the TileLang page's split-KV decode), taken in one
+// pass over the pieces in order with a running maximum.  Sixteen threads
+// share a (token, head) row, eight rows at a time; a thread owns the float4
+// columns c16 + 16 k of the 512-wide row, so sixteen threads read 256
+// contiguous bytes per load.  slots[s] is piece s's partial slot.  The
+// partials were written by other CTAs: they are read from L2 (__ldcg) after
+// the arrival count that made this the last piece.
+__device__ void merge_unit(const FwdParams& p, int u, int h_lo, int h_hi, int tid, const int* slots, int pieces) {
+  const int tok = u / p.groups;
+  const int g64 = (u % p.groups) * 64;
+  const int c16 = tid & 15;
+  constexpr int kF4 = kDv / 4;   // float4 per row
+  for (int h = h_lo + (tid >> 4); h < h_hi; h += 8) {
+    float mrun = -INFINITY, l = 0.f;
+    float4 acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+    for (int sp = 0; sp < pieces; ++sp) {
+      const int slot = slots[sp];
+      const float ls = __ldcg(p.part_lse + static_cast<size_t>(slot) * p.part_rows + h);
+      const float4* src = reinterpret_cast<const float4*>(p.part_o) + (static_cast<size_t>(slot) * p.part_rows + h) * kF4 + c16;
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __ldcg(src + 16 * k);
+      if (ls == -INFINITY) continue;   // an empty piece
+      const float mn = fmaxf(mrun, ls);
+      const float a = expf(mrun - mn), w = expf(ls - mn);
+      l = l * a + w;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc[k].x = acc[k].x * a + w * v[k].x;
+        acc[k].y = acc[k].y * a + w * v[k].y;
+        acc[k].z = acc[k].z * a + w * v[k].z;
+        acc[k].w = acc[k].w * a + w * v[k].w;
+      }
+      mrun = mn;
+    }
+    const int row = tok * p.h_q + g64 + h;
+    const float inv = mrun == -INFINITY ? 0.f : 1.0f / l;
+    if (c16 == 0) p.lse[row] = mrun == -INFINITY ? -INFINITY : mrun + logf(l);
+    uint2* o = reinterpret_cast<uint2*>(p.out + static_cast<size_t>(row) * kDv) + c16;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      o[16 * k] = make_uint2(pack_bf16x2(acc[k].x * inv, acc[k].y * inv), pack_bf16x2(acc[k].z * inv, acc[k].w * inv));
+  }
+}
+
+// Pieces of unit u under kBlockRanges (1 when one CTA runs it whole).
+__device__ __forceinline__ int unit_pieces(const FwdParams& p, int u) {
+  const long long total = static_cast<long long>(p.n_tok) * p.groups * p.nb;
+  const long long ub = static_cast<long long>(u) * p.nb;
+  return range_cta(ub + p.nb - 1, total, p.ctas) - range_cta(ub, total, p.ctas) + 1;
+}
+
 template <int HH>
 __device__ __forceinline__ void load_s_half(uint32_t taddr, float* v) {
   if constexpr (HH == 16) tmem_ld16x2_x16<16>(taddr, v);
@@ -1273,6 +1334,38 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
           }
         }
       }
+      // The piece is written (its LSEs by the owner threads above).  After
+      // the group's barrier one thread counts the piece with a release add,
+      // which publishes the group's writes; the group whose count completes
+      // the unit acquires the others' and merges every piece into out / LSE
+      // for its heads.
+      named_bar_sync(bar_id, 128);
+      if (tid < 32) {
+        // lane 0 counts the piece; if it completes the unit, the warp lists
+        // the pieces' slots (CTAs c_first .. c_last: slot 2c when the unit is
+        // that CTA's first item, else 2c + 1)
+        int last = 0;
+        if (lane == 0)
+          last = atomic_add_release_gpu(p.merge_count + item.unit * 2 + grp, 1) + 1 == unit_pieces(p, item.unit);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          fence_acquire_gpu();
+          const long long total = static_cast<long long>(p.n_tok) * p.groups * p.nb;
+          const long long ub = static_cast<long long>(item.unit) * p.nb;
+          const int c_first = range_cta(ub, total, p.ctas);
+          const int pieces = range_cta(ub + p.nb - 1, total, p.ctas) - c_first + 1;
+          if (lane < pieces) {
+            const int c = c_first + lane;
+            m.merge_slot[grp][lane] = 2 * c + (range_start(c, total, p.ctas) < ub ? 1 : 0);
+          }
+          if (lane == 0) m.merge_pieces[grp] = pieces;
+        } else if (lane == 0) {
+          m.merge_pieces[grp] = 0;
+        }
+      }
+      named_bar_sync(bar_id, 128);
+      if (m.merge_pieces[grp] > 0)
+        merge_unit(p, item.unit, hb, min(hb + H, hv), tid, m.merge_slot[grp], m.merge_pieces[grp]);
     } else {
       // bf16 output straight from TMEM: thread (q4, lane) holds dv = 128 mt +
       // 32 q4 + lane for each head; the lanes of an even/odd pair swap half
@@ -1360,9 +1453,6 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = m.tmem_base;
-  // A dependent launch (the decode merge) may place its CTAs once every CTA
-  // of this grid has started.
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (m.prior_error == 0) {
     if (warp < kProducerWarps) {
@@ -1398,86 +1488,6 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
 }
 
 // ------------------------------------------------------------------ helper kernels
-
-// Merge the pieces of units that kBlockRanges cut between CTAs:
-// LSE = ln sum_s exp(LSE_s), out = sum_s exp(LSE_s - LSE) * O_s (each O_s
-// already normalised over its piece; the LSE merge of the TileLang page's
-// split-KV decode).  One warp per (token, head) row.  The pieces of unit u
-// are the CTAs c_first..c_last whose ranges meet its blocks; CTA c holds u in
-// slot 2c if u is its first item, else 2c + 1.  Lane s handles piece s's LSE
-// (at most 32 pieces), and every lane owns the float4 columns lane + 32 k of
-// the 512-wide row, so each load instruction reads 512 contiguous bytes.  The
-// sums run over the pieces in order.  Rows of units one CTA ran whole are
-// final already and skipped.
-constexpr int kCombineRows = 8;   // rows (warps) per 256-thread block
-__global__ void __launch_bounds__(32 * kCombineRows) combine_splits_kernel(const __grid_constant__ FwdParams p) {
-  // Launched as a programmatic dependent of the forward grid: its CTAs may be
-  // placed early (they need no shared memory) and wait here until that grid
-  // has completed and its partials are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int row = static_cast<int>(blockIdx.x) * kCombineRows + static_cast<int>(threadIdx.x >> 5);
-  const int lane = static_cast<int>(threadIdx.x & 31);
-  if (row >= p.n_tok * p.h_q) return;
-  const int tok = row / p.h_q, hg = row % p.h_q;
-  const long long u = static_cast<long long>(tok) * p.groups + hg / 64;
-  const int h = hg % 64;
-  const long long total = static_cast<long long>(p.n_tok) * p.groups * p.nb;
-  const long long ub = u * p.nb;
-  const int c_first = range_cta(ub, total, p.ctas);
-  const int pieces = range_cta(ub + p.nb - 1, total, p.ctas) - c_first + 1;
-  if (pieces == 1) return;
-  auto slot_of = [&](int s) {
-    const int c = c_first + s;
-    return 2 * c + (range_start(c, total, p.ctas) < ub ? 1 : 0);
-  };
-  constexpr int kF4 = kDv / 4;   // float4 per row
-  auto row_of = [&](int slot) {
-    return reinterpret_cast<const float4*>(p.part_o) + (static_cast<size_t>(slot) * p.part_rows + h) * kF4 + lane;
-  };
-  // Piece 0's partial is read while the LSEs arrive.
-  const float4* src0 = row_of(slot_of(0));
-  float4 v0[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) v0[k] = __ldcg(src0 + 32 * k);
-  const float my_ls =
-      lane < pieces ? __ldcg(p.part_lse + static_cast<size_t>(slot_of(lane)) * p.part_rows + h) : -INFINITY;
-  float mx = -INFINITY;
-  for (int s = 0; s < pieces; ++s) mx = fmaxf(mx, __shfl_sync(0xffffffffu, my_ls, s));
-  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(p.out + static_cast<size_t>(row) * kDv) + 2 * lane;
-  if (mx == -INFINITY) {
-    if (lane == 0) p.lse[row] = -INFINITY;
-    const __nv_bfloat162 z = __floats2bfloat162_rn(0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      o2[64 * k] = z;
-      o2[64 * k + 1] = z;
-    }
-    return;
-  }
-  float sum = 0.f;
-  for (int s = 0; s < pieces; ++s) sum += expf(__shfl_sync(0xffffffffu, my_ls, s) - mx);
-  const float tot = mx + logf(sum);
-  float4 acc[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < pieces; ++s) {
-    const float ls = __shfl_sync(0xffffffffu, my_ls, s);
-    if (ls == -INFINITY) continue;
-    const float w = expf(ls - tot);
-    const float4* src = s == 0 ? src0 : row_of(slot_of(s));
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 v = s == 0 ? v0[k] : __ldcg(src + 32 * k);
-      acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
-    }
-  }
-  if (lane == 0) p.lse[row] = tot;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    o2[64 * k] = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-    o2[64 * k + 1] = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-  }
-}
 
 // Debug export of the number of valid entries per token: the forward's own
 // producer walk (its item schedule, window scan, block skips, row mapping and

@@ -100,6 +100,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// Device-scope atomic add with release semantics (returns the old value):
+// the writes ordered before it (this thread's, and other threads' through a
+// barrier) are visible to a thread that acquires the new value.
+__device__ __forceinline__ int atomic_add_release_gpu(int* addr, int v) {
+  int old;
+  asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
+// Device-scope acquire fence: later reads see what was released before an
+// atomic this thread has read.
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -127,25 +127,29 @@ size_t decode_part_floats(int ctas, int h_q) {
   return 2 * static_cast<size_t>(ctas) * static_cast<size_t>(part_rows(h_q)) * (static_cast<size_t>(smla::kDv) + 1);
 }
 
+// Decode workspace: the partials, then (16-byte aligned) one merge counter
+// per (unit, softmax group), units = tokens x 64-head groups.
+size_t decode_counter_offset(int ctas, int h_q) { return (decode_part_floats(ctas, h_q) * sizeof(float) + 15) & ~size_t(15); }
+size_t decode_counter_bytes(long long n_tok, int h_q) {
+  return static_cast<size_t>(n_tok) * static_cast<size_t>(head_groups(h_q)) * 2 * sizeof(int32_t);
+}
+
+// The forward grid (one persistent CTA per SM or fewer).
+template <int N, bool kFp8>
+cudaError_t launch_fwd_n(const FwdParams& p, cudaStream_t stream) {
+  smla::sparse_mla_fwd_kernel<N, kFp8><<<dim3(static_cast<unsigned>(p.ctas)), smla::fwd_threads<N, kFp8>(),
+                                         smla::smem_bytes<N>(), stream>>>(p);
+  return cudaGetLastError();
+}
+
 sparse_mla_status_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
   const int N = head_width(p.h_q);
-  const dim3 grid(static_cast<unsigned>(p.ctas));
-  if (p.mode == smla::kPagedFp8) {
-    if (N == 16)
-      smla::sparse_mla_fwd_kernel<16, true><<<grid, smla::fwd_threads<16, true>(), smla::smem_bytes<16>(), stream>>>(p);
-    else if (N == 32)
-      smla::sparse_mla_fwd_kernel<32, true><<<grid, smla::fwd_threads<32, true>(), smla::smem_bytes<32>(), stream>>>(p);
-    else
-      smla::sparse_mla_fwd_kernel<64, true><<<grid, smla::fwd_threads<64, true>(), smla::smem_bytes<64>(), stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
-  }
-  if (N == 16)
-    smla::sparse_mla_fwd_kernel<16><<<grid, smla::Layout<16>::kThreads, smla::smem_bytes<16>(), stream>>>(p);
-  else if (N == 32)
-    smla::sparse_mla_fwd_kernel<32><<<grid, smla::Layout<32>::kThreads, smla::smem_bytes<32>(), stream>>>(p);
-  else
-    smla::sparse_mla_fwd_kernel<64><<<grid, smla::Layout<64>::kThreads, smla::smem_bytes<64>(), stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
+  const bool fp8 = p.mode == smla::kPagedFp8;
+  cudaError_t e;
+  if (N == 16) e = fp8 ? launch_fwd_n<16, true>(p, stream) : launch_fwd_n<16, false>(p, stream);
+  else if (N == 32) e = fp8 ? launch_fwd_n<32, true>(p, stream) : launch_fwd_n<32, false>(p, stream);
+  else e = fp8 ? launch_fwd_n<64, true>(p, stream) : launch_fwd_n<64, false>(p, stream);
+  return e == cudaSuccess ? SPARSE_MLA_OK : SPARSE_MLA_ERR_CUDA;
 }
 
 sparse_mla_status_t launch_fill(void* out, float* lse, long long n_th, cudaStream_t stream) {
@@ -365,7 +369,7 @@ size_t sparse_mla_decode_workspace_size(int batch, int s_next, int h_q, int d_v,
   const long long n_tok = static_cast<long long>(batch) * s_next;
   const int ctas = decode_ctas(n_tok, h_q, topk, sms);
   if (ctas <= 1) return 0;   // one CTA runs every unit whole
-  return decode_part_floats(ctas, h_q) * sizeof(float);
+  return decode_counter_offset(ctas, h_q) + decode_counter_bytes(n_tok, h_q);
 }
 
 }  // extern "C"
@@ -439,25 +443,13 @@ sparse_mla_status_t run_decode(int mode, const void* q, const void* kv_cache, co
     float* ws = static_cast<float*>(workspace);
     p.part_o = ws;
     p.part_lse = ws + 2 * static_cast<size_t>(ctas) * p.part_rows * smla::kDv;
+    // Units cut between CTAs leave a partial per piece; the CTA that writes
+    // a unit's last piece (counted here, from zero) merges them.
+    p.merge_count = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + decode_counter_offset(ctas, h_q));
+    if (cudaMemsetAsync(p.merge_count, 0, decode_counter_bytes(n_tok, h_q), cs) != cudaSuccess)
+      return SPARSE_MLA_ERR_CUDA;
   }
-  if ((st = launch_fwd(p, cs)) != SPARSE_MLA_OK) return st;
-  if (need > 0) {
-    // Units cut between CTAs: merge their pieces (rows of whole units are
-    // final already and skipped).
-    const int n_th = static_cast<int>(n_tok * h_q);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((n_th + smla::kCombineRows - 1) / smla::kCombineRows));
-    cfg.blockDim = dim3(32 * smla::kCombineRows);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = cs;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap its launch with the forward tail
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, smla::combine_splits_kernel, p) != cudaSuccess) return SPARSE_MLA_ERR_CUDA;
-  }
-  return SPARSE_MLA_OK;
+  return launch_fwd(p, cs);
 }
 
 }  // namespace

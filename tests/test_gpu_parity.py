@@ -342,6 +342,41 @@ def test_decode_dirty_workspace(smla):
         compare(o, l, ref_o, ref_l, "dirty workspace")
 
 
+
+def test_decode_concurrent_streams_separate_workspaces(smla):
+    """Two decode calls in flight at once on two streams, each with its own
+    workspace (its own partials and merge counters): each result equals the
+    same call run alone, bit for bit."""
+    d = lambda t: t.to(DEV)
+    cases = [mi.decode_case(606 + i, batch=8, s_next=6, h_q=8, lo=3000, hi=9000, topk=2048, spare_pages=4)
+             for i in range(2)]
+    args, refs, wss, outs = [], [], [], []
+    for c in cases:
+        a = (d(c.q), d(c.kv_cache), d(c.block_table), d(c.cache_seqlens), d(c.indices), c.sm_scale, c.page_size)
+        need = smla.decode_workspace_size(c.batch, c.s_next, c.h_q, c.indices.shape[-1])
+        assert need > 0, "this shape is expected to split the top-k lists"
+        ws = torch.full((need,), 0xFF, dtype=torch.uint8, device=DEV)
+        refs.append(smla.sparse_mla_decode(*a, workspace=ws))
+        torch.cuda.synchronize()
+        args.append(a)
+        wss.append(ws)
+        outs.append((torch.empty_like(refs[-1][0]), torch.empty_like(refs[-1][1])))
+    streams = [torch.cuda.Stream(device=DEV) for _ in cases]
+    for rep in range(4):
+        for i, st in enumerate(streams):
+            smla.sparse_mla_decode(*args[i], workspace=wss[i], out=outs[i][0], lse=outs[i][1],
+                                   stream=st)
+        torch.cuda.synchronize()
+        for i in range(len(cases)):
+            assert torch.equal(outs[i][0], refs[i][0]) and torch.equal(outs[i][1], refs[i][1]), \
+                f"stream {i}, repetition {rep}: differs from the call run alone"
+    # and the first result against the oracle
+    c = cases[0]
+    ref_o, ref_l = orc.sparse_mla_decode(c.q, c.kv_cache, c.block_table, c.cache_seqlens, c.indices, c.sm_scale,
+                                         c.page_size)
+    compare(outs[0][0].float().cpu().numpy().reshape(-1, c.h_q, 512), outs[0][1].cpu().numpy().reshape(-1, c.h_q),
+            ref_o, ref_l, "concurrent decode")
+
 def test_decode_config_all_tokens(smla):
     """batch 16 x 6 MTP tokens, contexts U[4096, 32768], 64-token pages in a
     shuffled pool with every unread slot NaN, h = 8, topk = 2048; every

@@ -882,35 +882,33 @@ __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase
   using L = Layout<N>;
   constexpr uint32_t kIdescQK = idesc_bf16_f32(64, N, false, false);
   const uint32_t tS = tmem + static_cast<uint32_t>(PART * 2 + (n & 1)) * N;
-  // Acquire this part's tiles, then one proxy fence: the tiles were written
-  // by cp.async (generic proxy) and are read by the tensor core (async proxy).
-  uint32_t slot[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(2 * PART + i);
-    slot[i] = vi % L::kNV;
-    if (!mbar_wait(smem_u32(&m.v_full[slot[i]]), (vi / L::kNV) & 1u, deadline, ab)) return false;
-  }
-  const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
-  if (PART == 0 &&
-      !mbar_wait(smem_u32(&m.rp_full[rs]), (static_cast<uint32_t>(n) / L::kNR) & 1u, deadline, ab))
-    return false;
-  fence_proxy_async_smem();
-  tc_fence_after();
+  // Each tile's MMAs go as soon as that tile has landed (acquire, then a
+  // proxy fence: the tiles were written by cp.async, the generic proxy, and
+  // are read by the tensor core, the async proxy), so that only the last
+  // tile's MMAs remain once the block's last copies land.
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int pr = 2 * PART + i;
+    const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(pr);
+    const uint32_t slot = vi % L::kNV;
+    if (!mbar_wait(smem_u32(&m.v_full[slot]), (vi / L::kNV) & 1u, deadline, ab)) return false;
+    fence_proxy_async_smem();
+    tc_fence_after();
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t a = smem_desc(vbase + slot[i] * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
+        const uint64_t a = smem_desc(vbase + slot * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
         const uint64_t b = smem_desc(qbase + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
         mma_bf16_ss(tS, a, b, kIdescQK, (i | c | kk) != 0 ? 1u : 0u);
       }
     }
   }
   if (PART == 0) {
+    const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
+    if (!mbar_wait(smem_u32(&m.rp_full[rs]), (static_cast<uint32_t>(n) / L::kNR) & 1u, deadline, ab)) return false;
+    fence_proxy_async_smem();
+    tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);

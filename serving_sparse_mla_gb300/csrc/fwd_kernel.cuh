@@ -1415,6 +1415,27 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(lane_id());
 
+  // The producers' first reads (the first item's index window and, paged,
+  // its request's page-table row) head a chain of dependent round trips:
+  // start their lines into L2 while the CTA sets up.
+  if (warp < kProducerWarps && p.mode != kCausal) {
+    ItemIter it0 = items_begin(p);
+    Item first;
+    if (next_item(p, it0, first)) {
+      const int tok = first.unit / p.groups;
+      const int32_t* irow = p.indices + static_cast<size_t>(tok) * p.topk;
+      const int e0 = first.jb * kBlk;
+      const int e1 = min(p.topk, min(first.je, first.jb + 32) * kBlk);   // the first window of blocks
+      for (int e = e0 + static_cast<int>(threadIdx.x) * 32; e < e1; e += kProducerWarps * 32 * 32)
+        prefetch_line_l2(irow + e);
+      if ((p.mode == kPaged || p.mode == kPagedFp8) && p.max_blocks > 0) {
+        const int32_t* trow = p.block_table + static_cast<size_t>(tok / p.s_next) * p.max_blocks;
+        for (int e = static_cast<int>(threadIdx.x) * 32; e < p.max_blocks; e += kProducerWarps * 32 * 32)
+          prefetch_line_l2(trow + e);
+      }
+    }
+  }
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNV; ++i) {
       mbar_init(smem_u32(&m.v_full[i]), kProducerWarps * 32);   // producer or converter threads

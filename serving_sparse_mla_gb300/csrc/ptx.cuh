@@ -113,6 +113,12 @@ __device__ __forceinline__ int atomic_add_release_gpu(int* addr, int v) {
 // atomic this thread has read.
 __device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Start the 128-byte line holding `addr` on its way into L2 (no register
+// or shared memory is written; the instruction does not wait).
+__device__ __forceinline__ void prefetch_line_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr) : "memory");
+}
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

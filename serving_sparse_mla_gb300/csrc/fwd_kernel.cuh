@@ -215,10 +215,18 @@ __device__ __forceinline__ bool next_item(const FwdParams& p, ItemIter& it, Item
   return true;
 }
 
-template <int N>
+// kRaw: the FP8 cache at 16 heads, whose converter warps take raw e4m3 codes
+// from rings of their own (value-tile codes, 64 rows x 128 codes = 8 KB, and
+// per block the rows' tile scales, 1 KB) into the bf16 value ring, so that
+// the conversion can be spread over warps that write other rows than those
+// holding the codes and scales they read.
+template <int N, bool kRaw = false>
 struct Layout {
   static_assert(N == 16 || N == 32 || N == 64, "head group width");
-  static constexpr int kNV = N == 64 ? 8 : (N == 32 ? 10 : 11);   // value pair-tile ring
+  static_assert(!kRaw || N == 16, "raw-code rings: 16 heads only");
+  static constexpr int kNV = kRaw ? 8 : (N == 64 ? 8 : (N == 32 ? 10 : 11));   // value pair-tile ring
+  static constexpr int kNRaw = kRaw ? 6 : 0;                      // raw value-tile code ring
+  static constexpr int kNSc = kRaw ? 2 : 0;                       // per-block scale ring
   static constexpr int kNR = N == 64 ? 2 : 3;                     // rope / P^T ring
   static constexpr int kPRow = N * 2;                             // bytes of one P^T row
   static constexpr uint32_t kPSwz = N == 64 ? SWZ_128B : (N == 32 ? SWZ_64B : SWZ_32B);
@@ -230,7 +238,9 @@ struct Layout {
   static constexpr int kQOff = 0;
   static constexpr int kVOff = 9 * N * 128;
   static constexpr int kROff = kVOff + kNV * kPairBytes;
-  static constexpr int kMiscOff = kROff + kNR * kChunkBytes;
+  static constexpr int kRawOff = kROff + kNR * kChunkBytes;
+  static constexpr int kScOff = kRawOff + kNRaw * kChunkBytes;
+  static constexpr int kMiscOff = kScOff + kNSc * 1024;
   static_assert(kBlk * kPRow <= kChunkBytes, "P^T fits in a rope slot");
   // Block n+2's last value tile reuses a slot that P.V of block n frees, so
   // the softmax of block n+2 cannot finish before P.V(n) has started; that
@@ -239,17 +249,22 @@ struct Layout {
   static_assert(kNR >= 2, "P^T of the next block needs its own rope slot");
 };
 
-// FP8 cache at 16 heads per CTA: four converter warps after the P.V warp
-// dequantize each value tile as its raw codes land (the other widths convert
-// in the producer warps, one block behind their copies).
+// FP8 cache at 16 heads per CTA: eight converter warps after the P.V warp
+// dequantize each value tile from the raw rings as its codes land (the other
+// widths convert in the producer warps, one block behind their copies, in
+// place in the value slots).
 template <int N, bool kFp8>
-__host__ __device__ constexpr int conv_warps() { return (kFp8 && N == 16) ? 4 : 0; }
+__host__ __device__ constexpr int conv_warps() { return (kFp8 && N == 16) ? 8 : 0; }
 template <int N, bool kFp8>
 __host__ __device__ constexpr int fwd_threads() { return Layout<N>::kThreads + 32 * conv_warps<N, kFp8>(); }
+// The shared-memory layout of the kernel instantiation <N, kFp8>.
+template <int N, bool kFp8>
+using LayoutFor = Layout<N, kFp8 && N == 16>;
 
 struct __align__(16) Misc {
   uint64_t v_full[12], v_empty[12];
-  uint64_t raw_full[12];   // FP8 with converter warps: a value tile's raw codes have landed
+  uint64_t raw_full[12];   // FP8 with converter warps: a raw code slot's copies have landed
+  uint64_t raw_empty[12];  // ... and the converter warps have read it
   uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   uint64_t q_full, q_empty, s_full[2][2], p_full[2], o_full, drain[3], cand_full;
@@ -268,13 +283,14 @@ struct __align__(16) Misc {
   int merge_slot[2][32];     // their partial slots
 };
 
-template <int N>
+template <int N, bool kFp8 = false>
 constexpr int smem_bytes() {
-  return Layout<N>::kMiscOff + static_cast<int>(sizeof(Misc)) + 1024;
+  return LayoutFor<N, kFp8>::kMiscOff + static_cast<int>(sizeof(Misc)) + 1024;
 }
 static_assert(smem_bytes<64>() <= kMaxSmem, "smem budget (64 heads)");
 static_assert(smem_bytes<32>() <= kMaxSmem, "smem budget (32 heads)");
 static_assert(smem_bytes<16>() <= kMaxSmem, "smem budget (16 heads)");
+static_assert(smem_bytes<16, true>() <= kMaxSmem, "smem budget (16 heads, FP8 cache)");
 
 // ------------------------------------------------------------------ helpers
 
@@ -645,14 +661,26 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
                         int& n_chunks) {
           const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
           if (u < 4) {
-            const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
-            const uint32_t s = vi % L::kNV;
-            empty = smem_u32(&m.v_empty[s]);
-            full = smem_u32(&m.v_full[s]);
-            par = (vi / L::kNV) & 1u;
-            dst = vbase + s * kPairBytes;
-            first_chunk = 2 * u;
-            n_chunks = 2;
+            if constexpr (kConv) {
+              // FP8 with converter warps: the value tile's codes go to the raw ring
+              const uint32_t ri = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+              const uint32_t r = ri % L::kNRaw;
+              empty = smem_u32(&m.raw_empty[r]);
+              full = smem_u32(&m.raw_full[r]);
+              par = (ri / L::kNRaw) & 1u;
+              dst = smem_u32(sbase + L::kRawOff) + r * kChunkBytes;
+              first_chunk = 2 * u;
+              n_chunks = 1;
+            } else {
+              const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+              const uint32_t s = vi % L::kNV;
+              empty = smem_u32(&m.v_empty[s]);
+              full = smem_u32(&m.v_full[s]);
+              par = (vi / L::kNV) & 1u;
+              dst = vbase + s * kPairBytes;
+              first_chunk = 2 * u;
+              n_chunks = 2;
+            }
           } else {
             const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
             empty = smem_u32(&m.rp_empty[rs]);
@@ -670,28 +698,35 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
           const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
           if constexpr (kFp8) {
             if (u < 4) {
-              // Raw e4m3 codes of the tile's 128 columns into the slot's second
-              // 64-column chunk (row r at r * 128, unswizzled), and with the
-              // first value tile the rows' four tile scales into the first two
-              // rows of this row group in that slot's first chunk; both are
-              // converted in place (fp8_convert_block), by the converter warps
-              // once raw_full completes, or by this warp one block later.
-              // Masked rows are zero-filled (codes and scales 0: a zero row).
+              // Raw e4m3 codes of the tile's 128 columns (row r at r * 128,
+              // unswizzled) and, with the first value tile, the rows' four
+              // tile scales (16 bytes a row).  kConv: into the raw rings (the
+              // code slot dst, row r's scales at r * 16 in the block's scale
+              // slot) for the converter warps once raw_full completes.  Else
+              // into the value slot's second 64-column chunk and the first two
+              // rows of this row group in its first chunk, converted in place
+              // by this warp one block later (fp8_convert_block).  Masked rows
+              // are zero-filled (codes and scales 0: a zero row).
+              uint32_t code_dst, sc_dst;
+              if constexpr (kConv) {
+                code_dst = dst;
+                sc_dst = smem_u32(sbase + L::kScOff) + static_cast<uint32_t>(n % L::kNSc) * 1024u +
+                         static_cast<uint32_t>(warp * 16) * 16u;
+              } else {
+                code_dst = dst + kChunkBytes;
+                sc_dst = dst + static_cast<uint32_t>(warp) * 2048u;
+              }
 #pragma unroll
               for (int it = 0; it < 4; ++it) {
                 const int r = warp * 16 + it * 4 + sel;
                 const int src_row = myrow[it];
                 const uint8_t* slot_src = reinterpret_cast<const uint8_t*>(p.kv) +
                                           static_cast<size_t>(src_row < 0 ? 0 : src_row) * kFp8SlotBytes;
-                cp_async_16(dst + kChunkBytes + r * 128 + piece * 16, slot_src + u * 128 + piece * 16,
-                            src_row < 0 ? 0u : 16u);
+                cp_async_16(code_dst + r * 128 + piece * 16, slot_src + u * 128 + piece * 16, src_row < 0 ? 0u : 16u);
                 if (u == 0 && piece == 0)
-                  cp_async_16(dst + warp * 2048 + (it * 4 + sel) * 16, slot_src + kFp8ScaleOff, src_row < 0 ? 0u : 16u);
+                  cp_async_16(sc_dst + (it * 4 + sel) * 16, slot_src + kFp8ScaleOff, src_row < 0 ? 0u : 16u);
               }
-              if constexpr (kConv) {
-                const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
-                cp_async_arrive_on(smem_u32(&m.raw_full[vi % L::kNV]));
-              }
+              if constexpr (kConv) cp_async_arrive_on(full);
               return;
             }
           }
@@ -820,7 +855,7 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
 template <int N, bool kFp8>
 __device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_t* sbase) {
   if constexpr (kFp8)
-    return run_producer_t<N, Layout<N>, Misc, false, false, false, true, (conv_warps<N, kFp8>() > 0)>(p, m, sbase);
+    return run_producer_t<N, LayoutFor<N, kFp8>, Misc, false, false, false, true, (conv_warps<N, kFp8>() > 0)>(p, m, sbase);
   else
     return p.mode == kCausal ? run_producer_t<N, Layout<N>, Misc, false, true>(p, m, sbase)
                              : run_producer_t<N, Layout<N>, Misc, false, false>(p, m, sbase);
@@ -828,17 +863,27 @@ __device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_
 
 // ------------------------------------------------------------------ FP8 converters
 
-// Converter warp cw (0..3) of the FP8 decode at 16 heads: follows the block
-// sequence through the info ring like the consumers and, per block, waits
-// for its four value tiles' raw codes (raw_full) and dequantizes rows
-// 16 cw .. 16 cw + 15 of each into bf16, arriving on the tiles' full
-// barriers for the QK^T issuers.
+// Converter warp cw (0..7) of the FP8 decode at 16 heads: follows the block
+// sequence through the info ring like the consumers and, per block and value
+// tile, waits for the tile's raw codes (raw_full) and for a free bf16 slot
+// (v_empty), reads rows 8 cw .. 8 cw + 7 of the codes (and, with the first
+// tile, those rows' scales from the block's scale slot), releases the raw
+// slot (raw_empty), dequantizes into the 128B-swizzled bf16 layout the MMA
+// descriptors read and arrives on the bf16 slot's full barrier.  A lane
+// converts 16 codes of one row per tile.
 template <int N>
 __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw) {
-  using L = Layout<N>;
+  using L = Layout<N, true>;
+  constexpr int kRows = kBlk / conv_warps<N, true>();   // rows per converter warp
+  constexpr int kSets = kRows / 4;                      // row sets of 4 (8 lanes a row)
   const volatile int* ab = &m.abort_flag;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
+  const uint32_t rawbase = smem_u32(sbase + L::kRawOff);
+  const uint32_t scbase = smem_u32(sbase + L::kScOff);
+  const uint8_t* gbase = reinterpret_cast<const uint8_t*>(&m) - smem_u32(&m);   // generic address of shared offset 0
   const int lane = static_cast<int>(lane_id());
+  const int sel = lane >> 3, piece = lane & 7;
+  const int ch = piece >> 2, pc = (piece & 3) * 2;
   int n = 0, ni = 0;
   ItemIter iter = items_begin(p);
   Item item;
@@ -853,14 +898,52 @@ __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw)
       if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
       ++ni;
       if (blk < 0) break;
-      // each tile once its raw codes have landed
-      const int nb = n;
-      auto wait_raw = [&](int u, uint32_t slot) {
-        const uint32_t vi = static_cast<uint32_t>(nb) * 4u + static_cast<uint32_t>(u);
-        const bool rok = mbar_wait(smem_u32(&m.raw_full[slot]), (vi / L::kNV) & 1u, deadline, ab);
-        return __all_sync(0xffffffffu, rok);
-      };
-      if (!fp8_convert_block<L>(m, vbase, n, cw, lane >> 3, lane & 7, wait_raw)) return false;
+      float sc[kSets][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+        const uint32_t r = vi % L::kNRaw, sl = vi % L::kNV;
+        const bool tok = mbar_wait(smem_u32(&m.raw_full[r]), (vi / L::kNRaw) & 1u, deadline, ab) &&
+                         mbar_wait(smem_u32(&m.v_empty[sl]), ((vi / L::kNV) & 1u) ^ 1u, deadline, ab);
+        if (!__all_sync(0xffffffffu, tok)) return false;
+        if (u == 0) {
+          const uint8_t* scs = gbase + scbase + static_cast<uint32_t>(n % L::kNSc) * 1024u;
+#pragma unroll
+          for (int it = 0; it < kSets; ++it) {
+            const float4 f = *reinterpret_cast<const float4*>(scs + (cw * kRows + it * 4 + sel) * 16);
+            sc[it][0] = f.x;
+            sc[it][1] = f.y;
+            sc[it][2] = f.z;
+            sc[it][3] = f.w;
+          }
+        }
+        uint4 c[kSets];
+        const uint8_t* codes = gbase + rawbase + r * kChunkBytes;
+#pragma unroll
+        for (int it = 0; it < kSets; ++it)
+          c[it] = *reinterpret_cast<const uint4*>(codes + (cw * kRows + it * 4 + sel) * 128 + piece * 16);
+        // this thread's codes (and scales) are read: the raw slot may be refilled
+        mbar_arrive(smem_u32(&m.raw_empty[r]));
+        const uint32_t dst = vbase + sl * kPairBytes;
+#pragma unroll
+        for (int it = 0; it < kSets; ++it) {
+          const int row = cw * kRows + it * 4 + sel;
+          const float f = sc[it][u];
+          // 16 codes: columns 128 u + 16 piece .. + 15 = chunk piece / 4, 8-column
+          // pieces 2 (piece % 4) and 2 (piece % 4) + 1 of the row
+          const uint32_t at = dst + ch * kChunkBytes + row * 128;
+          st_shared_v4(at + ((pc ^ (row & 7)) << 4), e4m3x2_scaled_bf16x2(c[it].x, f),
+                       e4m3x2_scaled_bf16x2(c[it].x >> 16, f), e4m3x2_scaled_bf16x2(c[it].y, f),
+                       e4m3x2_scaled_bf16x2(c[it].y >> 16, f));
+          st_shared_v4(at + (((pc + 1) ^ (row & 7)) << 4), e4m3x2_scaled_bf16x2(c[it].z, f),
+                       e4m3x2_scaled_bf16x2(c[it].z >> 16, f), e4m3x2_scaled_bf16x2(c[it].w, f),
+                       e4m3x2_scaled_bf16x2(c[it].w >> 16, f));
+        }
+        // the tile's bf16 rows are written: order them before the tensor
+        // core's reads (async proxy) and arrive on the slot's full barrier
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&m.v_full[sl]));
+      }
       ++n;
     }
   }
@@ -876,10 +959,9 @@ __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw)
 //   QK part 1: QK^T over value pairs 2,3
 //   PV:        P.V for all of dv, as soon as the softmax has written P^T
 // Each QK part accumulates its own partial S^T; the softmax adds the two.
-template <int N, int PART>
+template <int N, int PART, class L>
 __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase, uint32_t rbase, uint32_t tmem,
                                          int n, uint64_t deadline, const volatile int* ab) {
-  using L = Layout<N>;
   constexpr uint32_t kIdescQK = idesc_bf16_f32(64, N, false, false);
   const uint32_t tS = tmem + static_cast<uint32_t>(PART * 2 + (n & 1)) * N;
   // Each tile's MMAs go as soon as that tile has landed (acquire, then a
@@ -920,9 +1002,8 @@ __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase
   return true;
 }
 
-template <int N, int PART>
+template <int N, int PART, class L>
 __device__ bool run_qk(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem) {
-  using L = Layout<N>;
   const volatile int* ab = &m.abort_flag;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
@@ -947,7 +1028,7 @@ __device__ bool run_qk(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tme
         if (blk < 0) break;
         // S buffer n&1 was last read by the softmax of block n-2.
         if (n >= 2 && !mbar_wait(smem_u32(&m.p_full[n & 1]), ((n - 2) >> 1) & 1, deadline, ab)) return false;
-        if (!issue_qk<N, PART>(m, qbase, vbase, rbase, tmem, n, deadline, ab)) return false;
+        if (!issue_qk<N, PART, L>(m, qbase, vbase, rbase, tmem, n, deadline, ab)) return false;
         ++n;
       }
       // Q may be replaced once this thread's QK^T MMAs have completed.
@@ -957,9 +1038,8 @@ __device__ bool run_qk(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tme
   return true;
 }
 
-template <int N>
+template <int N, class L>
 __device__ bool run_pv(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem) {
-  using L = Layout<N>;
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
   const volatile int* ab = &m.abort_flag;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
@@ -1071,9 +1151,8 @@ __device__ __forceinline__ void load_s_half(uint32_t taddr, float* v) {
   else tmem_ld16x2_x8<8>(taddr, v);
 }
 
-template <int N>
+template <int N, class L>
 __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem, int grp) {
-  using L = Layout<N>;
   constexpr int H = L::kHG;            // heads this group owns (16 or 32)
   const volatile int* ab = &m.abort_flag;
   const uint32_t bar_id = 1u + static_cast<uint32_t>(grp);
@@ -1407,7 +1486,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
 // kFp8: the FP8-cache instantiation (kPagedFp8); only the gather differs.
 template <int N, bool kFp8 = false>
 __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = Layout<N>;
+  using L = LayoutFor<N, kFp8>;
   constexpr int kConvWarps = conv_warps<N, kFp8>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1438,9 +1517,13 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNV; ++i) {
-      mbar_init(smem_u32(&m.v_full[i]), kProducerWarps * 32);   // producer or converter threads
+      // the producer threads, or with converter warps the converter threads
+      mbar_init(smem_u32(&m.v_full[i]), kConvWarps > 0 ? 32 * kConvWarps : kProducerWarps * 32);
       mbar_init(smem_u32(&m.v_empty[i]), 1);
-      mbar_init(smem_u32(&m.raw_full[i]), kProducerWarps * 32);
+    }
+    for (int i = 0; i < L::kNRaw; ++i) {
+      mbar_init(smem_u32(&m.raw_full[i]), kProducerWarps * 32);   // producer threads (cp.async)
+      mbar_init(smem_u32(&m.raw_empty[i]), 32 * kConvWarps);      // converter threads
     }
     for (int i = 0; i < L::kNR; ++i) {
       mbar_init(smem_u32(&m.rp_full[i]), kProducerWarps * 32);
@@ -1482,8 +1565,8 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
     } else if (warp == kMmaWarp || warp == kMmaWarpB || warp == L::kPvWarp) {
       if (lane == 0) {
         const int role = warp == kMmaWarp ? 0 : (warp == kMmaWarpB ? 1 : 2);
-        const bool ok = role == 0 ? run_qk<N, 0>(p, m, sbase, tmem)
-                                  : (role == 1 ? run_qk<N, 1>(p, m, sbase, tmem) : run_pv<N>(p, m, sbase, tmem));
+        const bool ok = role == 0 ? run_qk<N, 0, L>(p, m, sbase, tmem)
+                                  : (role == 1 ? run_qk<N, 1, L>(p, m, sbase, tmem) : run_pv<N, L>(p, m, sbase, tmem));
         if (!ok) raise_error(m, kErrMmaWait);
         // Drain: every MMA this thread issued completes before TMEM is freed.
         const int never = 0;
@@ -1492,10 +1575,12 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
       }
       __syncwarp();
     } else if (kConvWarps > 0 && warp > L::kPvWarp) {
-      if (!run_convert<N>(p, m, sbase, warp - L::kPvWarp - 1)) raise_error(m, kErrProducerWait);
+      if constexpr (kConvWarps > 0) {
+        if (!run_convert<N>(p, m, sbase, warp - L::kPvWarp - 1)) raise_error(m, kErrProducerWait);
+      }
     } else {
       const int grp = warp >= softmax_warp0(1) ? 1 : 0;
-      if (!run_softmax<N>(p, m, sbase, tmem, grp)) raise_error(m, kErrSoftmaxWait);
+      if (!run_softmax<N, L>(p, m, sbase, tmem, grp)) raise_error(m, kErrSoftmaxWait);
       // Drain: this thread's Q copies have landed before the CTA can exit.
       asm volatile("cp.async.wait_all;" ::: "memory");
     }

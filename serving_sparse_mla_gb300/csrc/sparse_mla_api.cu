@@ -62,7 +62,7 @@ sparse_mla_status_t device_setup(int* sm_count) {
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::smem_bytes<64>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smla::smem_bytes<16>()) != cudaSuccess ||
+                             smla::smem_bytes<16, true>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smla::smem_bytes<32>()) != cudaSuccess ||
         cudaFuncSetAttribute(smla::sparse_mla_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -138,7 +138,7 @@ size_t decode_counter_bytes(long long n_tok, int h_q) {
 template <int N, bool kFp8>
 cudaError_t launch_fwd_n(const FwdParams& p, cudaStream_t stream) {
   smla::sparse_mla_fwd_kernel<N, kFp8><<<dim3(static_cast<unsigned>(p.ctas)), smla::fwd_threads<N, kFp8>(),
-                                         smla::smem_bytes<N>(), stream>>>(p);
+                                         smla::smem_bytes<N, kFp8>(), stream>>>(p);
   return cudaGetLastError();
 }
 

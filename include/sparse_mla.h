@@ -211,9 +211,19 @@ sparse_mla_status_t sparse_mla_decode(const void* q, const void* kv_cache, const
  *   bytes [512, 528)  4 fp32 scales; scale k applies to codes 128k .. 128k+127;
  *   bytes [528, 656)  the latent's last 64 values (rope), bf16.
  *
- * The row the attention uses is code * scale (d < 512) and the rope values;
- * the kernel dequantizes each gathered row to bf16 (round to nearest even)
- * in shared memory and then computes as sparse_mla_decode does.
+ * The row the attention uses is code * scale (d < 512) and the rope values.
+ * Arithmetic:
+ *   h_q <= 16   the tensor cores contract the codes themselves, as bf16
+ *               values code * 2^-120 (exact; e4m3 subnormals become bf16
+ *               subnormals): each 128-column tile's partial score is taken
+ *               back by the row's tile scale (and 2^120) in fp32, and P.V
+ *               takes, per tile, P times the row's tile scale and 2^88
+ *               rounded to bf16 (its sum scaled back by 2^32).  Tile scales
+ *               below 2^32 keep these finite.  A NaN code (0x7F, 0xFF) under
+ *               a finite scale is read as +-480; a NaN scale gives NaN.
+ *   h_q > 16    each gathered row is dequantized to bf16 (code * scale in
+ *               fp32, round to nearest even) in shared memory, then computed
+ *               as sparse_mla_decode does.
  *
  *   kv_cache      uint8 [num_blocks, page_size, 656], 16-byte aligned
  *   everything else, including the workspace (sparse_mla_decode_workspace_size),

@@ -21,7 +21,7 @@
 // takes ~225 KB of shared memory).  A unit of work is one token's list for
 // one group of up to 64 heads; prefill deals whole units round-robin to the
 // CTAs, decode cuts the units' lists, laid end to end, into one equal range
-// per CTA and merges the pieces of cut units afterwards (combine kernel).
+// per CTA; the CTA that writes a cut unit's last piece merges its pieces.
 // Every role of a CTA walks the same sequence of items, so the producers
 // gather the next item while the consumers finish the current one.  The
 // index list is walked in blocks of 64 entries (64 gathered rows = 72 KB, so
@@ -101,8 +101,10 @@ constexpr int kMaxSmem = 232448;
 // short-prefill case of "feat: add XTuner TileLang sparse MLA backend",
 // Summary), else masked.
 // kPagedFp8: the paged layout over an FP8 cache (656-byte slots: 512 e4m3
-// codes, four fp32 tile scales, 64 bf16 rope values), dequantized to bf16 as
-// the rows are gathered.
+// codes, four fp32 tile scales, 64 bf16 rope values).  At 16 heads the
+// tensor cores contract the codes and the tile scales are applied to the
+// partial scores and to P (Layout kRaw); at 32 and 64 heads the rows are
+// dequantized to bf16 as they are gathered.
 enum Mode : int { kDense = 0, kVarlen = 1, kPaged = 2, kCausal = 3, kPagedFp8 = 4 };
 
 // FP8 cache slot layout (the FP8 sparse-decode cache published with
@@ -215,22 +217,34 @@ __device__ __forceinline__ bool next_item(const FwdParams& p, ItemIter& it, Item
   return true;
 }
 
-// kRaw: the FP8 cache at 16 heads, whose converter warps take raw e4m3 codes
-// from rings of their own (value-tile codes, 64 rows x 128 codes = 8 KB, and
-// per block the rows' tile scales, 1 KB) into the bf16 value ring, so that
-// the conversion can be spread over warps that write other rows than those
-// holding the codes and scales they read.
+// kRaw: the FP8 cache at 16 heads.  The producers copy each value tile's
+// raw e4m3 codes (64 rows x 128 codes) into the second 64-column chunk of its
+// value slot, and converter warps rewrite the slot in place as bf16 values
+// code * 2^-120 (exact, no scale applied), each warp its own rows, so the
+// conversion can be spread over more warps than the producers' row groups.
+// The tensor core then contracts the codes:
+// QK^T keeps one partial S^T per 128-column scale tile (and one for the
+// rope), which the softmax combines with the rows' tile scales, and P.V
+// takes, per value tile t, P^T scaled by the rows' scale of tile t and 2^88
+// (four bf16 tiles that fill the block's rope slot; O^T then holds the
+// output times 2^-32).  The rows' scales (1 KB per
+// block) ride with the rope tile into a scale ring indexed like the rope
+// ring, so the rope slot's release also releases them.
 template <int N, bool kRaw = false>
 struct Layout {
   static_assert(N == 16 || N == 32 || N == 64, "head group width");
   static_assert(!kRaw || N == 16, "raw-code rings: 16 heads only");
-  static constexpr int kNV = kRaw ? 8 : (N == 64 ? 8 : (N == 32 ? 10 : 11));   // value pair-tile ring
-  static constexpr int kNRaw = kRaw ? 6 : 0;                      // raw value-tile code ring
-  static constexpr int kNSc = kRaw ? 2 : 0;                       // per-block scale ring
+  static constexpr bool kRawCodes = kRaw;
+  static constexpr int kNV = N == 64 ? 8 : (N == 32 ? 10 : 11);  // value pair-tile ring
   static constexpr int kNR = N == 64 ? 2 : 3;                     // rope / P^T ring
+  static constexpr int kNSc = kRaw ? kNR : 0;                     // per-block scale ring (slot = rope slot)
   static constexpr int kPRow = N * 2;                             // bytes of one P^T row
   static constexpr uint32_t kPSwz = N == 64 ? SWZ_128B : (N == 32 ? SWZ_64B : SWZ_32B);
-  static constexpr int kTmemCols = N == 64 ? 512 : (N == 32 ? 256 : 128);
+  // TMEM: the partial S^T (2 parts, or kRaw 5 tiles, double-buffered), then O^T
+  static constexpr int kSParts = kRaw ? 5 : 2;
+  static constexpr int kOCol = 2 * kSParts * N;
+  static constexpr int kTmemCols = kRaw ? 256 : (N == 64 ? 512 : (N == 32 ? 256 : 128));
+  static_assert(kOCol + 4 * N <= kTmemCols, "TMEM columns");
   static constexpr int kGroups = N == 64 ? 2 : 1;                 // softmax groups
   static constexpr int kHG = N / kGroups;                         // heads per group (<= 32)
   static constexpr int kPvWarp = 6 + 4 * kGroups;
@@ -238,10 +252,9 @@ struct Layout {
   static constexpr int kQOff = 0;
   static constexpr int kVOff = 9 * N * 128;
   static constexpr int kROff = kVOff + kNV * kPairBytes;
-  static constexpr int kRawOff = kROff + kNR * kChunkBytes;
-  static constexpr int kScOff = kRawOff + kNRaw * kChunkBytes;
+  static constexpr int kScOff = kROff + kNR * kChunkBytes;
   static constexpr int kMiscOff = kScOff + kNSc * 1024;
-  static_assert(kBlk * kPRow <= kChunkBytes, "P^T fits in a rope slot");
+  static_assert(kBlk * kPRow * (kRaw ? 4 : 1) <= kChunkBytes, "P^T (kRaw: its four scaled tiles) fits in a rope slot");
   // Block n+2's last value tile reuses a slot that P.V of block n frees, so
   // the softmax of block n+2 cannot finish before P.V(n) has started; that
   // keeps every double-buffered phase wait (p_full, s_full) within one phase.
@@ -263,8 +276,7 @@ using LayoutFor = Layout<N, kFp8 && N == 16>;
 
 struct __align__(16) Misc {
   uint64_t v_full[12], v_empty[12];
-  uint64_t raw_full[12];   // FP8 with converter warps: a raw code slot's copies have landed
-  uint64_t raw_empty[12];  // ... and the converter warps have read it
+  uint64_t raw_full[12];   // FP8 with converter warps: a value slot's raw codes have landed
   uint64_t rp_full[3], rp_empty[3];
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   uint64_t q_full, q_empty, s_full[2][2], p_full[2], o_full, drain[3], cand_full;
@@ -450,6 +462,22 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
 
 __device__ __forceinline__ void cp_async_arrive_on(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Codes 2k and 2k + 1 of four e4m3 codes w (code i in byte i) as bf16x2
+// holding code * 2^-120 exactly: a bf16 whose exponent field is the e4m3's
+// exponent field and whose top three mantissa bits are the e4m3's mantissa
+// reads the e4m3 exponent bias 7 against 127, for subnormals (exponent field
+// 0) as well.  The byte permute places each code in the low byte of its
+// 16-bit lane with its sign replicated in the high byte; shifted left by four
+// bits, the lane holds the sign at bit 15 and exponent and mantissa at bits
+// 10..4, and the mask clears the rest (including what the shift carries from
+// the low lane into the high lane's bits 0..3).
+template <int K>
+__device__ __forceinline__ uint32_t e4m3x2_bf16x2_shifted(uint32_t w) {
+  uint32_t x;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(w), "n"(K == 0 ? 0x9180 : 0xB3A2));
+  return (x << 4) & 0x87F087F0u;
 }
 
 // Two e4m3 codes (the low byte first) times a scale -> bf16x2 (round to
@@ -661,26 +689,17 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
                         int& n_chunks) {
           const int u = step < 2 ? step : (step == 2 ? 4 : step - 1);
           if (u < 4) {
-            if constexpr (kConv) {
-              // FP8 with converter warps: the value tile's codes go to the raw ring
-              const uint32_t ri = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
-              const uint32_t r = ri % L::kNRaw;
-              empty = smem_u32(&m.raw_empty[r]);
-              full = smem_u32(&m.raw_full[r]);
-              par = (ri / L::kNRaw) & 1u;
-              dst = smem_u32(sbase + L::kRawOff) + r * kChunkBytes;
-              first_chunk = 2 * u;
-              n_chunks = 1;
-            } else {
-              const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
-              const uint32_t s = vi % L::kNV;
-              empty = smem_u32(&m.v_empty[s]);
-              full = smem_u32(&m.v_full[s]);
-              par = (vi / L::kNV) & 1u;
-              dst = vbase + s * kPairBytes;
-              first_chunk = 2 * u;
-              n_chunks = 2;
-            }
+            // (FP8 with converter warps: the raw codes' arrival goes to
+            // raw_full, the converters arrive on v_full)
+            const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+            const uint32_t s = vi % L::kNV;
+            empty = smem_u32(&m.v_empty[s]);
+            if constexpr (kConv) full = smem_u32(&m.raw_full[s]);
+            else full = smem_u32(&m.v_full[s]);
+            par = (vi / L::kNV) & 1u;
+            dst = vbase + s * kPairBytes;
+            first_chunk = 2 * u;
+            n_chunks = 2;
           } else {
             const uint32_t rs = static_cast<uint32_t>(n) % L::kNR;
             empty = smem_u32(&m.rp_empty[rs]);
@@ -699,23 +718,16 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
           if constexpr (kFp8) {
             if (u < 4) {
               // Raw e4m3 codes of the tile's 128 columns (row r at r * 128,
-              // unswizzled) and, with the first value tile, the rows' four
-              // tile scales (16 bytes a row).  kConv: into the raw rings (the
-              // code slot dst, row r's scales at r * 16 in the block's scale
-              // slot) for the converter warps once raw_full completes.  Else
-              // into the value slot's second 64-column chunk and the first two
-              // rows of this row group in its first chunk, converted in place
-              // by this warp one block later (fp8_convert_block).  Masked rows
-              // are zero-filled (codes and scales 0: a zero row).
-              uint32_t code_dst, sc_dst;
-              if constexpr (kConv) {
-                code_dst = dst;
-                sc_dst = smem_u32(sbase + L::kScOff) + static_cast<uint32_t>(n % L::kNSc) * 1024u +
-                         static_cast<uint32_t>(warp * 16) * 16u;
-              } else {
-                code_dst = dst + kChunkBytes;
-                sc_dst = dst + static_cast<uint32_t>(warp) * 2048u;
-              }
+              // unswizzled) into the value slot's second 64-column chunk.
+              // kConv: converted in place by the converter warps once raw_full
+              // completes (the rows' scales go with the rope tile).  Else with
+              // the first value tile the rows' four tile scales (16 bytes a
+              // row) in the first two rows of this row group in its first
+              // chunk, converted in place by this warp one block later
+              // (fp8_convert_block).  Masked rows are zero-filled (codes and
+              // scales 0: a zero row).
+              const uint32_t code_dst = dst + kChunkBytes;
+              const uint32_t sc_dst = dst + static_cast<uint32_t>(warp) * 2048u;
 #pragma unroll
               for (int it = 0; it < 4; ++it) {
                 const int r = warp * 16 + it * 4 + sel;
@@ -723,7 +735,7 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
                 const uint8_t* slot_src = reinterpret_cast<const uint8_t*>(p.kv) +
                                           static_cast<size_t>(src_row < 0 ? 0 : src_row) * kFp8SlotBytes;
                 cp_async_16(code_dst + r * 128 + piece * 16, slot_src + u * 128 + piece * 16, src_row < 0 ? 0u : 16u);
-                if (u == 0 && piece == 0)
+                if (!kConv && u == 0 && piece == 0)
                   cp_async_16(sc_dst + (it * 4 + sel) * 16, slot_src + kFp8ScaleOff, src_row < 0 ? 0u : 16u);
               }
               if constexpr (kConv) cp_async_arrive_on(full);
@@ -742,6 +754,22 @@ __device__ bool run_producer_t(const FwdParams& p, M& m, uint8_t* sbase) {
               else
                 src = p.kv + static_cast<size_t>(src_row < 0 ? 0 : src_row) * kDqk + (first_chunk + c) * 64 + piece * 8;
               cp_async_16(dst + c * kChunkBytes + r * 128 + ((piece ^ (r & 7)) << 4), src, src_row < 0 ? 0u : 16u);
+            }
+          }
+          if constexpr (kConv) {
+            // with the rope tile, the rows' four tile scales (16 bytes a row,
+            // row r at r * 16) into the scale slot of the block's rope slot
+            if (piece == 0) {
+              const uint32_t sc_dst = smem_u32(sbase + L::kScOff) + (static_cast<uint32_t>(n) % L::kNR) * 1024u;
+#pragma unroll
+              for (int it = 0; it < 4; ++it) {
+                const int r = warp * 16 + it * 4 + sel;
+                const int src_row = myrow[it];
+                cp_async_16(sc_dst + r * 16,
+                            reinterpret_cast<const uint8_t*>(p.kv) +
+                                static_cast<size_t>(src_row < 0 ? 0 : src_row) * kFp8SlotBytes + kFp8ScaleOff,
+                            src_row < 0 ? 0u : 16u);
+              }
             }
           }
           // The hardware arrives on the tile's full barrier for this thread
@@ -864,13 +892,14 @@ __device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_
 // ------------------------------------------------------------------ FP8 converters
 
 // Converter warp cw (0..7) of the FP8 decode at 16 heads: follows the block
-// sequence through the info ring like the consumers and, per block and value
-// tile, waits for the tile's raw codes (raw_full) and for a free bf16 slot
-// (v_empty), reads rows 8 cw .. 8 cw + 7 of the codes (and, with the first
-// tile, those rows' scales from the block's scale slot), releases the raw
-// slot (raw_empty), dequantizes into the 128B-swizzled bf16 layout the MMA
-// descriptors read and arrives on the bf16 slot's full barrier.  A lane
-// converts 16 codes of one row per tile.
+// sequence through the info ring like the consumers.  Per block and value
+// tile it waits for the tile's raw codes in its value slot (raw_full), reads
+// rows 8 cw .. 8 cw + 7 of the codes (the slot's second chunk), and once the
+// whole warp has read them rewrites those rows as bf16 code * 2^-120 (exact;
+// the tile scales are applied by the softmax) in the 128B-swizzled layout the
+// MMA descriptors read, then arrives on the slot's full barrier.  A lane
+// converts 16 codes of one row per tile; no other warp reads or writes these
+// rows of the slot.
 template <int N>
 __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw) {
   using L = Layout<N, true>;
@@ -878,8 +907,6 @@ __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw)
   constexpr int kSets = kRows / 4;                      // row sets of 4 (8 lanes a row)
   const volatile int* ab = &m.abort_flag;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
-  const uint32_t rawbase = smem_u32(sbase + L::kRawOff);
-  const uint32_t scbase = smem_u32(sbase + L::kScOff);
   const uint8_t* gbase = reinterpret_cast<const uint8_t*>(&m) - smem_u32(&m);   // generic address of shared offset 0
   const int lane = static_cast<int>(lane_id());
   const int sel = lane >> 3, piece = lane & 7;
@@ -898,46 +925,32 @@ __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw)
       if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
       ++ni;
       if (blk < 0) break;
-      float sc[kSets][4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
-        const uint32_t r = vi % L::kNRaw, sl = vi % L::kNV;
-        const bool tok = mbar_wait(smem_u32(&m.raw_full[r]), (vi / L::kNRaw) & 1u, deadline, ab) &&
-                         mbar_wait(smem_u32(&m.v_empty[sl]), ((vi / L::kNV) & 1u) ^ 1u, deadline, ab);
+        const uint32_t sl = vi % L::kNV;
+        const bool tok = mbar_wait(smem_u32(&m.raw_full[sl]), (vi / L::kNV) & 1u, deadline, ab);
         if (!__all_sync(0xffffffffu, tok)) return false;
-        if (u == 0) {
-          const uint8_t* scs = gbase + scbase + static_cast<uint32_t>(n % L::kNSc) * 1024u;
-#pragma unroll
-          for (int it = 0; it < kSets; ++it) {
-            const float4 f = *reinterpret_cast<const float4*>(scs + (cw * kRows + it * 4 + sel) * 16);
-            sc[it][0] = f.x;
-            sc[it][1] = f.y;
-            sc[it][2] = f.z;
-            sc[it][3] = f.w;
-          }
-        }
+        const uint32_t dst = vbase + sl * kPairBytes;
         uint4 c[kSets];
-        const uint8_t* codes = gbase + rawbase + r * kChunkBytes;
+        const uint8_t* codes = gbase + dst + kChunkBytes;
 #pragma unroll
         for (int it = 0; it < kSets; ++it)
           c[it] = *reinterpret_cast<const uint4*>(codes + (cw * kRows + it * 4 + sel) * 128 + piece * 16);
-        // this thread's codes (and scales) are read: the raw slot may be refilled
-        mbar_arrive(smem_u32(&m.raw_empty[r]));
-        const uint32_t dst = vbase + sl * kPairBytes;
+        // every lane has read its codes before any lane overwrites the rows
+        __syncwarp();
 #pragma unroll
         for (int it = 0; it < kSets; ++it) {
           const int row = cw * kRows + it * 4 + sel;
-          const float f = sc[it][u];
           // 16 codes: columns 128 u + 16 piece .. + 15 = chunk piece / 4, 8-column
           // pieces 2 (piece % 4) and 2 (piece % 4) + 1 of the row
           const uint32_t at = dst + ch * kChunkBytes + row * 128;
-          st_shared_v4(at + ((pc ^ (row & 7)) << 4), e4m3x2_scaled_bf16x2(c[it].x, f),
-                       e4m3x2_scaled_bf16x2(c[it].x >> 16, f), e4m3x2_scaled_bf16x2(c[it].y, f),
-                       e4m3x2_scaled_bf16x2(c[it].y >> 16, f));
-          st_shared_v4(at + (((pc + 1) ^ (row & 7)) << 4), e4m3x2_scaled_bf16x2(c[it].z, f),
-                       e4m3x2_scaled_bf16x2(c[it].z >> 16, f), e4m3x2_scaled_bf16x2(c[it].w, f),
-                       e4m3x2_scaled_bf16x2(c[it].w >> 16, f));
+          st_shared_v4(at + ((pc ^ (row & 7)) << 4), e4m3x2_bf16x2_shifted<0>(c[it].x),
+                       e4m3x2_bf16x2_shifted<1>(c[it].x), e4m3x2_bf16x2_shifted<0>(c[it].y),
+                       e4m3x2_bf16x2_shifted<1>(c[it].y));
+          st_shared_v4(at + (((pc + 1) ^ (row & 7)) << 4), e4m3x2_bf16x2_shifted<0>(c[it].z),
+                       e4m3x2_bf16x2_shifted<1>(c[it].z), e4m3x2_bf16x2_shifted<0>(c[it].w),
+                       e4m3x2_bf16x2_shifted<1>(c[it].w));
         }
         // the tile's bf16 rows are written: order them before the tensor
         // core's reads (async proxy) and arrive on the slot's full barrier
@@ -959,11 +972,15 @@ __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw)
 //   QK part 1: QK^T over value pairs 2,3
 //   PV:        P.V for all of dv, as soon as the softmax has written P^T
 // Each QK part accumulates its own partial S^T; the softmax adds the two.
+// kRawCodes (FP8 at 16 heads): the value pairs hold the codes (times
+// 2^-120); each pair (a 128-column scale tile) and the rope get a partial S^T
+// of their own, at TMEM columns (5 (n & 1) + tile) N, tile 4 the rope.
 template <int N, int PART, class L>
 __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase, uint32_t rbase, uint32_t tmem,
                                          int n, uint64_t deadline, const volatile int* ab) {
   constexpr uint32_t kIdescQK = idesc_bf16_f32(64, N, false, false);
   const uint32_t tS = tmem + static_cast<uint32_t>(PART * 2 + (n & 1)) * N;
+  auto tile_acc = [&](int t) { return tmem + static_cast<uint32_t>(5 * (n & 1) + t) * N; };
   // Each tile's MMAs go as soon as that tile has landed (acquire, then a
   // proxy fence: the tiles were written by cp.async, the generic proxy, and
   // are read by the tensor core, the async proxy), so that only the last
@@ -982,7 +999,10 @@ __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t a = smem_desc(vbase + slot * kPairBytes + c * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
         const uint64_t b = smem_desc(qbase + (2 * pr + c) * N * 128 + kk * 32, 16, 1024, SWZ_128B);
-        mma_bf16_ss(tS, a, b, kIdescQK, (i | c | kk) != 0 ? 1u : 0u);
+        if constexpr (L::kRawCodes)
+          mma_bf16_ss(tile_acc(pr), a, b, kIdescQK, (c | kk) != 0 ? 1u : 0u);
+        else
+          mma_bf16_ss(tS, a, b, kIdescQK, (i | c | kk) != 0 ? 1u : 0u);
       }
     }
   }
@@ -995,7 +1015,10 @@ __device__ __forceinline__ bool issue_qk(Misc& m, uint32_t qbase, uint32_t vbase
     for (int kk = 0; kk < 4; ++kk) {
       const uint64_t a = smem_desc(rbase + rs * kChunkBytes + kk * 32, 16, 1024, SWZ_128B);
       const uint64_t b = smem_desc(qbase + 8 * N * 128 + kk * 32, 16, 1024, SWZ_128B);
-      mma_bf16_ss(tS, a, b, kIdescQK, 1u);
+      if constexpr (L::kRawCodes)
+        mma_bf16_ss(tile_acc(4), a, b, kIdescQK, kk != 0 ? 1u : 0u);
+      else
+        mma_bf16_ss(tS, a, b, kIdescQK, 1u);
     }
   }
   mma_commit(smem_u32(&m.s_full[PART][n & 1]));
@@ -1038,13 +1061,16 @@ __device__ bool run_qk(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tme
   return true;
 }
 
+// kRawCodes: V^T holds the codes (times 2^-120), and value tile mt contracts
+// with its own scaled P^T tile (the rope slot's mt-th quarter).
 template <int N, class L>
 __device__ bool run_pv(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tmem) {
   constexpr uint32_t kIdescPV = idesc_bf16_f32(128, N, true, true);
+  constexpr uint32_t kPTile = L::kRawCodes ? kBlk * L::kPRow : 0;   // bytes between the scaled P^T tiles
   const volatile int* ab = &m.abort_flag;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
-  const uint32_t tO = tmem + 4 * N;
+  const uint32_t tO = tmem + L::kOCol;
   int n = 0, ni = 0;   // blocks (ring positions), info entries
   ItemIter iter = items_begin(p);
   Item item;
@@ -1068,8 +1094,8 @@ __device__ bool run_pv(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_t tme
 #pragma unroll
         for (int ks = 0; ks < kBlk / 16; ++ks) {
           const uint64_t a = smem_desc(vbase + s * kPairBytes + ks * 2048, kChunkBytes, 1024, SWZ_128B);
-          const uint64_t b = smem_desc(rbase + rs * kChunkBytes + ks * 16 * L::kPRow, 16 * L::kPRow * 8,
-                                       8 * L::kPRow, L::kPSwz);
+          const uint64_t b = smem_desc(rbase + rs * kChunkBytes + mt * kPTile + ks * 16 * L::kPRow,
+                                       16 * L::kPRow * 8, 8 * L::kPRow, L::kPSwz);
           mma_bf16_ss(tO + mt * N, a, b, kIdescPV, (nl > 0 || ks > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&m.v_empty[s]));
@@ -1168,7 +1194,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
   const int hsub = (lane >> 4) * HH;                   // first head of this half, within the group
   const int row = q4 * 16 + (lane & 15);               // kv row of the block
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-  const uint32_t tO = tmem + lane_off + 4 * N + hb;
+  const uint32_t tO = tmem + lane_off + L::kOCol + hb;
   const uint32_t qbase = smem_u32(sbase + L::kQOff);
   const uint32_t rbase = smem_u32(sbase + L::kROff);
 
@@ -1229,24 +1255,51 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
       bool sok = true;
-      if (blk >= 0)
+      if (blk >= 0) {
         sok = mbar_wait(smem_u32(&m.s_full[0][n & 1]), (n >> 1) & 1, deadline, ab) &&
               mbar_wait(smem_u32(&m.s_full[1][n & 1]), (n >> 1) & 1, deadline, ab);
+        // kRawCodes: the block's tile scales landed with its rope tile (the
+        // slot is not refilled before this block's P.V has completed)
+        if constexpr (L::kRawCodes)
+          sok = sok && mbar_wait(smem_u32(&m.rp_full[n % L::kNR]), (n / L::kNR) & 1, deadline, ab);
+      }
       if (bar_red_or_128(bar_id, !(iok && sok))) return false;
       if (blk < 0) break;
       tc_fence_after();
       const bool valid = ((bits >> (row >> 1)) & 1u) != 0u;
       const uint32_t tSa = tmem + lane_off + static_cast<uint32_t>(n & 1) * N + hb;        // part 0
       const uint32_t tSb = tmem + lane_off + static_cast<uint32_t>(2 + (n & 1)) * N + hb;  // part 1
+      // kRawCodes: the row's four tile scales
+      float4 tsc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (L::kRawCodes)
+        tsc = *reinterpret_cast<const float4*>(sbase + L::kScOff + (n % L::kNR) * 1024 + row * 16);
 
       // The row's scaled scores (log2 units), masked rows -inf.
       auto load_scores = [&](float (&v)[HH]) {
-        float t[HH];
-        load_s_half<HH>(tSa, v);
-        load_s_half<HH>(tSb, t);
-        tmem_wait_ld();
+        if constexpr (L::kRawCodes) {
+          // S = sum over the value tiles of scale_t * (codes_t . q_t) + rope;
+          // the partial sums hold codes_t . q_t times 2^-120 (taken back in
+          // two factors, 2^56 with the scales and 2^64 on their sum)
+          const uint32_t t0 = tmem + lane_off + static_cast<uint32_t>(5 * (n & 1)) * N + hb;
+          float t[4][HH];
 #pragma unroll
-        for (int i = 0; i < HH; ++i) v[i] = valid ? (v[i] + t[i]) * p.scale_log2 : -INFINITY;
+          for (int j = 0; j < 4; ++j) load_s_half<HH>(t0 + j * N, t[j]);
+          load_s_half<HH>(t0 + 4 * N, v);
+          tmem_wait_ld();
+          const float sl = p.scale_log2 * 0x1p56f;
+          const float a0 = tsc.x * sl, a1 = tsc.y * sl, a2 = tsc.z * sl, a3 = tsc.w * sl;
+#pragma unroll
+          for (int i = 0; i < HH; ++i)
+            v[i] = valid ? v[i] * p.scale_log2 + (t[0][i] * a0 + t[1][i] * a1 + t[2][i] * a2 + t[3][i] * a3) * 0x1p64f
+                         : -INFINITY;
+        } else {
+          float t[HH];
+          load_s_half<HH>(tSa, v);
+          load_s_half<HH>(tSb, t);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < HH; ++i) v[i] = valid ? (v[i] + t[i]) * p.scale_log2 : -INFINITY;
+        }
       };
       float s[HH];
       load_scores(s);
@@ -1313,9 +1366,21 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
             s[c * 8 + i] = valid ? fast_exp2(s[c * 8 + i] - m.mrun[h]) : 0.f;
           }
           const uint32_t chunk = static_cast<uint32_t>((hb + hsub) / 8 + c);
-          st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
-                       pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
-                       pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
+          if constexpr (L::kRawCodes) {
+            // value tile t's P^T: the row's P times its scale of tile t and
+            // 2^88, bf16 (against codes times 2^-120: O^T holds out * 2^-32)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float f = (t == 0 ? tsc.x : (t == 1 ? tsc.y : (t == 2 ? tsc.z : tsc.w))) * 0x1p88f;
+              st_shared_v4(prow + static_cast<uint32_t>(t * kBlk * L::kPRow) + ((chunk ^ sw) << 4),
+                           pack_bf16x2(s[c * 8 + 0] * f, s[c * 8 + 1] * f), pack_bf16x2(s[c * 8 + 2] * f, s[c * 8 + 3] * f),
+                           pack_bf16x2(s[c * 8 + 4] * f, s[c * 8 + 5] * f), pack_bf16x2(s[c * 8 + 6] * f, s[c * 8 + 7] * f));
+            }
+          } else {
+            st_shared_v4(prow + ((chunk ^ sw) << 4), pack_bf16x2(s[c * 8 + 0], s[c * 8 + 1]),
+                         pack_bf16x2(s[c * 8 + 2], s[c * 8 + 3]), pack_bf16x2(s[c * 8 + 4], s[c * 8 + 5]),
+                         pack_bf16x2(s[c * 8 + 6], s[c * 8 + 7]));
+          }
         }
         float h8[2 * HQ];
 #pragma unroll
@@ -1372,7 +1437,7 @@ __device__ bool run_softmax(const FwdParams& p, Misc& m, uint8_t* sbase, uint32_
       float lse;
       if (nl > 0) {
         lse = (m.mrun[h] + log2f(lrun)) * 0.69314718055994530942f;
-        m.fin[h] = 1.0f / lrun;
+        m.fin[h] = (L::kRawCodes ? 0x1p32f : 1.0f) / lrun;   // kRawCodes: O^T holds out * 2^-32
       } else {
         lse = -INFINITY;
         m.fin[h] = 0.f;
@@ -1521,10 +1586,8 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
       mbar_init(smem_u32(&m.v_full[i]), kConvWarps > 0 ? 32 * kConvWarps : kProducerWarps * 32);
       mbar_init(smem_u32(&m.v_empty[i]), 1);
     }
-    for (int i = 0; i < L::kNRaw; ++i) {
+    for (int i = 0; i < (kConvWarps > 0 ? L::kNV : 0); ++i)
       mbar_init(smem_u32(&m.raw_full[i]), kProducerWarps * 32);   // producer threads (cp.async)
-      mbar_init(smem_u32(&m.raw_empty[i]), 32 * kConvWarps);      // converter threads
-    }
     for (int i = 0; i < L::kNR; ++i) {
       mbar_init(smem_u32(&m.rp_full[i]), kProducerWarps * 32);
       mbar_init(smem_u32(&m.rp_empty[i]), 1);

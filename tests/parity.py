@@ -86,12 +86,15 @@ def pv_rounding_sigma(q_t, rows, sm_scale, d_v=512):
 
 
 def fp8_rounding_sigma(q_t, rows, sm_scale, d_v=512, d_quant=512):
-    """sigma_d for the FP8-cache decode, whose kernel also rounds every
-    dequantized cache value (the first d_quant columns) to bf16 (relative
-    eps_jd, |eps| <= 2^-9, variance <= 2^-16 / 12) before the products:
-    the score of row j moves by sm_scale * sum_d q_d k_jd eps_jd (standard
-    deviation sigma_s_j), the output by sum_j p_j [delta_s_j (v_jd - out_d)
-    + v_jd eps_jd], on top of the P rounding of pv_rounding_sigma."""
+    """sigma_d for the FP8-cache decode.  At 32 and 64 heads per CTA the
+    kernel also rounds every dequantized cache value (the first d_quant
+    columns) to bf16 (relative eps_jd, |eps| <= 2^-9, variance <= 2^-16 /
+    12) before the products: the score of row j moves by sm_scale * sum_d
+    q_d k_jd eps_jd (standard deviation sigma_s_j), the output by sum_j p_j
+    [delta_s_j (v_jd - out_d) + v_jd eps_jd], on top of the P rounding of
+    pv_rounding_sigma.  At 16 heads the codes enter the products exactly and
+    only P times each tile scale is rounded to bf16 (the size of the P
+    rounding), so this sigma bounds that arithmetic as well."""
     q_t = np.asarray(q_t, dtype=np.float64)
     rows = np.asarray(rows, dtype=np.float64)
     if rows.shape[0] == 0:

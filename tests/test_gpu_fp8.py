@@ -1,8 +1,10 @@
 """GPU parity of the FP8 KV-cache decode (sparse_mla_decode_fp8) against the
 float64 oracle of the dequantized cache (oracle/fp8_kv_oracle.py), on the
 same seeded inputs: the allclose bar of the pages on every element, and the
-tight bound of tests/parity.py with the FP8 terms (the kernel rounds each
-dequantized value to bf16 before the tensor-core products)."""
+tight bound of tests/parity.py with the FP8 terms (at 32 and 64 heads the
+kernel rounds each dequantized value to bf16 before the tensor-core
+products; at 16 heads it contracts the codes exactly and rounds P times each
+tile scale to bf16)."""
 import numpy as np
 import pytest
 import torch
@@ -73,12 +75,17 @@ def test_fp8_decode_long_lists_split_over_ctas(smla):
     _check(smla, c, u, "fp8 decode short lists")
 
 
-def test_fp8_equals_bf16_decode_when_exact(smla):
-    """With power-of-two tile scales every dequantized value is exact in
-    bf16, so the FP8 decode gathers the very tiles the bf16 decode gathers
-    from that bf16 cache: the two results agree bit for bit (this pins the
-    slot layout: code order, scale of each tile, rope offset)."""
-    c, u = mi.decode_case_fp8(713, batch=4, s_next=3, h_q=8, lo=500, hi=3000, topk=1024, page=64, spare_pages=2,
+@pytest.mark.parametrize("h_q", [24, 64])
+def test_fp8_equals_bf16_decode_when_exact(smla, h_q):
+    """At 32 and 64 heads per CTA the gather dequantizes each value to bf16
+    before the products.  With power-of-two tile scales every dequantized
+    value is exact in bf16, so the FP8 decode gathers the very tiles the bf16
+    decode gathers from that bf16 cache: the two results agree bit for bit
+    (this pins the slot layout: code order, scale of each tile, rope
+    offset).  At 16 heads the codes are contracted unscaled (the tile scales
+    applied to the partial scores and to P), a different rounding; its
+    layout is pinned by the tight bound against the oracle."""
+    c, u = mi.decode_case_fp8(713, batch=4, s_next=3, h_q=h_q, lo=500, hi=3000, topk=1024, page=64, spare_pages=2,
                               pow2_scales=True)
     xb = torch.from_numpy(f8.dequantize_slots(u)).to(torch.bfloat16)
     o8, l8 = _run(smla, c, u)
@@ -87,6 +94,46 @@ def test_fp8_equals_bf16_decode_when_exact(smla):
                                       c.sm_scale, c.page_size)
     torch.cuda.synchronize()
     assert torch.equal(o8, o16) and torch.equal(l8, l16)
+
+
+@pytest.mark.parametrize("h_q", [8, 24])
+@pytest.mark.parametrize("f", [2.0 ** -20, 2.0 ** 12])
+def test_fp8_decode_small_and_large_scales(smla, h_q, f):
+    """A cache whose latent values are scaled by a power of two f (tile
+    scales from ~1e-8 to ~1e2): the codes are those of the unscaled cache and
+    the scales carry f exactly.  The outputs, scaled back by 1/f, must meet
+    the tight bound scaled the same way (a relative check: the bound's
+    absolute floor would otherwise hide any error at small f), so no
+    intermediate of the kernel may under- or overflow at these scales."""
+    c, _ = mi.decode_case_fp8(720 + h_q, batch=2, s_next=2, h_q=h_q, lo=300, hi=2000, topk=512, page=64,
+                              spare_pages=2)
+    c.kv_cache = (c.kv_cache.float() * f).to(torch.bfloat16)
+    u = mi.quantize_fp8_slots(c.kv_cache)
+    out, lse = _run(smla, c, u)
+    n = c.batch * c.s_next
+    o = out.float().cpu().numpy().reshape(n, c.h_q, 512)
+    l = lse.cpu().numpy().reshape(n, c.h_q)
+    ro, rl = f8.sparse_mla_decode_fp8(c.q, u, c.block_table, c.cache_seqlens, c.indices, c.sm_scale, c.page_size)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+    X = f8.dequantize_slots(u).reshape(-1, 576)
+    idx = c.indices.numpy().astype(np.int64)
+    tab = c.block_table.numpy().astype(np.int64)
+    lens = c.cache_seqlens.numpy()
+    worst = 0.0
+    for t in range(n):
+        b, j = divmod(t, c.s_next)
+        r = orc.rows_paged(idx[b, j], tab[b], int(lens[b]), c.page_size, u.shape[0])
+        if r.size:
+            qt = c.q[b, j].double().numpy()
+            sig = fp8_rounding_sigma(qt, X[r], c.sm_scale)
+            worst = max(worst, tight_ratio(o[t] / f, ro[t] / f, sig / f))
+            # LSE: moves by at most the largest score error; a score carries
+            # at most 2^-9 relative rounding of each dequantized K value
+            # (bound taken at 2^-8): sm_scale * 2^-8 * max_j sum_d |q_d k_jd|
+            ds = c.sm_scale * 2.0 ** -8 * (np.abs(qt) @ np.abs(X[r]).T).max(axis=1)
+            assert np.all(np.abs(l[t] - rl[t]) <= ds + 2e-2), (t, np.abs(l[t] - rl[t]).max(), ds.max())
+    record(f"fp8 decode h={h_q}, cache x {f:g}", tight_ratio=worst)
+    assert worst <= 1.0, f"cache x {f:g}: relative tight ratio {worst:.3f}"
 
 
 def test_fp8_decode_config_shape_all_tokens(smla):

@@ -892,25 +892,29 @@ __device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_
 // ------------------------------------------------------------------ FP8 converters
 
 // Converter warp cw (0..7) of the FP8 decode at 16 heads: follows the block
-// sequence through the info ring like the consumers.  Per block and value
-// tile it waits for the tile's raw codes in its value slot (raw_full), reads
-// rows 8 cw .. 8 cw + 7 of the codes (the slot's second chunk), and once the
-// whole warp has read them rewrites those rows as bf16 code * 2^-120 (exact;
-// the tile scales are applied by the softmax) in the 128B-swizzled layout the
-// MMA descriptors read, then arrives on the slot's full barrier.  A lane
-// converts 16 codes of one row per tile; no other warp reads or writes these
-// rows of the slot.
+// sequence through the info ring like the consumers.  Warps 2u and 2u + 1
+// take value tile u of every block (rows 0..31 and 32..63), so a block's four
+// tiles are converted side by side as they land.  Per block a warp waits for
+// its tile's raw codes in the value slot (raw_full), and for each half of its
+// rows reads the codes (the slot's second chunk) and, once the whole warp
+// has read them, rewrites those rows as bf16 code * 2^-120 (exact; the tile
+// scales are applied by the softmax) in the 128B-swizzled layout the MMA
+// descriptors read; then it arrives on the slot's full barrier.  A lane
+// converts 16 codes of one row per row set; no other warp reads or writes
+// these rows of the slot.
 template <int N>
 __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw) {
   using L = Layout<N, true>;
-  constexpr int kRows = kBlk / conv_warps<N, true>();   // rows per converter warp
-  constexpr int kSets = kRows / 4;                      // row sets of 4 (8 lanes a row)
+  static_assert(conv_warps<N, true>() == 8, "two converter warps per value tile");
+  constexpr int kSets = 4;                              // row sets of 4 (8 lanes a row) per pass
   const volatile int* ab = &m.abort_flag;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint8_t* gbase = reinterpret_cast<const uint8_t*>(&m) - smem_u32(&m);   // generic address of shared offset 0
   const int lane = static_cast<int>(lane_id());
   const int sel = lane >> 3, piece = lane & 7;
   const int ch = piece >> 2, pc = (piece & 3) * 2;
+  const int u = cw >> 1;                                // this warp's value tile
+  const int row0 = (cw & 1) * 32;                       // and its rows
   int n = 0, ni = 0;
   ItemIter iter = items_begin(p);
   Item item;
@@ -925,23 +929,23 @@ __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw)
       if (lane == 0) mbar_arrive(smem_u32(&m.info_empty[k]));
       ++ni;
       if (blk < 0) break;
+      const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
+      const uint32_t sl = vi % L::kNV;
+      const bool tok = mbar_wait(smem_u32(&m.raw_full[sl]), (vi / L::kNV) & 1u, deadline, ab);
+      if (!__all_sync(0xffffffffu, tok)) return false;
+      const uint32_t dst = vbase + sl * kPairBytes;
+      const uint8_t* codes = gbase + dst + kChunkBytes;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t vi = static_cast<uint32_t>(n) * 4u + static_cast<uint32_t>(u);
-        const uint32_t sl = vi % L::kNV;
-        const bool tok = mbar_wait(smem_u32(&m.raw_full[sl]), (vi / L::kNV) & 1u, deadline, ab);
-        if (!__all_sync(0xffffffffu, tok)) return false;
-        const uint32_t dst = vbase + sl * kPairBytes;
+      for (int pass = 0; pass < 2; ++pass) {
         uint4 c[kSets];
-        const uint8_t* codes = gbase + dst + kChunkBytes;
 #pragma unroll
         for (int it = 0; it < kSets; ++it)
-          c[it] = *reinterpret_cast<const uint4*>(codes + (cw * kRows + it * 4 + sel) * 128 + piece * 16);
-        // every lane has read its codes before any lane overwrites the rows
+          c[it] = *reinterpret_cast<const uint4*>(codes + (row0 + pass * 16 + it * 4 + sel) * 128 + piece * 16);
+        // every lane has read these rows' codes before any lane overwrites them
         __syncwarp();
 #pragma unroll
         for (int it = 0; it < kSets; ++it) {
-          const int row = cw * kRows + it * 4 + sel;
+          const int row = row0 + pass * 16 + it * 4 + sel;
           // 16 codes: columns 128 u + 16 piece .. + 15 = chunk piece / 4, 8-column
           // pieces 2 (piece % 4) and 2 (piece % 4) + 1 of the row
           const uint32_t at = dst + ch * kChunkBytes + row * 128;
@@ -952,11 +956,11 @@ __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw)
                        e4m3x2_bf16x2_shifted<1>(c[it].z), e4m3x2_bf16x2_shifted<0>(c[it].w),
                        e4m3x2_bf16x2_shifted<1>(c[it].w));
         }
-        // the tile's bf16 rows are written: order them before the tensor
-        // core's reads (async proxy) and arrive on the slot's full barrier
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&m.v_full[sl]));
       }
+      // the tile's bf16 rows are written: order them before the tensor
+      // core's reads (async proxy) and arrive on the slot's full barrier
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&m.v_full[sl]));
       ++n;
     }
   }
@@ -1582,8 +1586,8 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNV; ++i) {
-      // the producer threads, or with converter warps the converter threads
-      mbar_init(smem_u32(&m.v_full[i]), kConvWarps > 0 ? 32 * kConvWarps : kProducerWarps * 32);
+      // the producer threads (cp.async), or the two converter warps of the tile
+      mbar_init(smem_u32(&m.v_full[i]), kConvWarps > 0 ? 64 : kProducerWarps * 32);   // converters: a tile's two warps
       mbar_init(smem_u32(&m.v_empty[i]), 1);
     }
     for (int i = 0; i < (kConvWarps > 0 ? L::kNV : 0); ++i)

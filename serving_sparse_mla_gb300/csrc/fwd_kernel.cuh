@@ -905,16 +905,18 @@ __device__ __forceinline__ bool run_producer(const FwdParams& p, Misc& m, uint8_
 template <int N>
 __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw) {
   using L = Layout<N, true>;
-  static_assert(conv_warps<N, true>() == 8, "two converter warps per value tile");
-  constexpr int kSets = 4;                              // row sets of 4 (8 lanes a row) per pass
+  constexpr int kPerTile = conv_warps<N, true>() / 4;   // converter warps per value tile
+  static_assert(kPerTile * 4 == conv_warps<N, true>(), "converter warps: a multiple of four");
+  constexpr int kPasses = kBlk / kPerTile / 16;          // passes of 16 rows per warp
+  constexpr int kSets = 4;                               // row sets of 4 (8 lanes a row) per pass
   const volatile int* ab = &m.abort_flag;
   const uint32_t vbase = smem_u32(sbase + L::kVOff);
   const uint8_t* gbase = reinterpret_cast<const uint8_t*>(&m) - smem_u32(&m);   // generic address of shared offset 0
   const int lane = static_cast<int>(lane_id());
   const int sel = lane >> 3, piece = lane & 7;
   const int ch = piece >> 2, pc = (piece & 3) * 2;
-  const int u = cw >> 1;                                // this warp's value tile
-  const int row0 = (cw & 1) * 32;                       // and its rows
+  const int u = cw / kPerTile;                          // this warp's value tile
+  const int row0 = (cw % kPerTile) * (kBlk / kPerTile); // and its rows
   int n = 0, ni = 0;
   ItemIter iter = items_begin(p);
   Item item;
@@ -936,7 +938,7 @@ __device__ bool run_convert(const FwdParams& p, Misc& m, uint8_t* sbase, int cw)
       const uint32_t dst = vbase + sl * kPairBytes;
       const uint8_t* codes = gbase + dst + kChunkBytes;
 #pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {
+      for (int pass = 0; pass < kPasses; ++pass) {
         uint4 c[kSets];
 #pragma unroll
         for (int it = 0; it < kSets; ++it)
@@ -1587,7 +1589,7 @@ __global__ void __launch_bounds__(fwd_threads<N, kFp8>(), 1) sparse_mla_fwd_kern
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::kNV; ++i) {
       // the producer threads (cp.async), or the two converter warps of the tile
-      mbar_init(smem_u32(&m.v_full[i]), kConvWarps > 0 ? 64 : kProducerWarps * 32);   // converters: a tile's two warps
+      mbar_init(smem_u32(&m.v_full[i]), kConvWarps > 0 ? 32 * kConvWarps / 4 : kProducerWarps * 32);   // converters: a tile's warps
       mbar_init(smem_u32(&m.v_empty[i]), 1);
     }
     for (int i = 0; i < (kConvWarps > 0 ? L::kNV : 0); ++i)

@@ -233,7 +233,7 @@ __device__ __forceinline__ bool next_item(const FwdParams& p, ItemIter& it, Item
 template <int N, bool kRaw = false>
 struct Layout {
   static_assert(N == 16 || N == 32 || N == 64, "head group width");
-  static_assert(!kRaw || N == 16, "raw-code rings: 16 heads only");
+  static_assert(!kRaw || N == 16, "codes contracted unscaled: 16 heads only");
   static constexpr bool kRawCodes = kRaw;
   static constexpr int kNV = N == 64 ? 8 : (N == 32 ? 10 : 11);  // value pair-tile ring
   static constexpr int kNR = N == 64 ? 2 : 3;                     // rope / P^T ring
@@ -262,10 +262,10 @@ struct Layout {
   static_assert(kNR >= 2, "P^T of the next block needs its own rope slot");
 };
 
-// FP8 cache at 16 heads per CTA: eight converter warps after the P.V warp
-// dequantize each value tile from the raw rings as its codes land (the other
-// widths convert in the producer warps, one block behind their copies, in
-// place in the value slots).
+// FP8 cache at 16 heads per CTA: eight converter warps after the P.V warp,
+// two per value tile, widen each tile's codes in place in its value slot as
+// they land (the other widths dequantize in the producer warps, one block
+// behind their copies, in place in the value slots).
 template <int N, bool kFp8>
 __host__ __device__ constexpr int conv_warps() { return (kFp8 && N == 16) ? 8 : 0; }
 template <int N, bool kFp8>

@@ -619,6 +619,7 @@ def fp8_runner(smla, case, dev, stream):
 
 PAGES_TRIALS = 5    # the pages' timing: interleaved trials ...
 PAGES_CALLS = 20    # ... each the median of this many warm calls
+PAGES_LEAD_CYCLES = 4_000_000   # ~2 ms of device-side wait ahead of a trial's timed calls
 
 
 def config_records(smla, dev, stream, steps: int, warmup: int, flush, peaks) -> dict:
@@ -680,6 +681,10 @@ def config_records(smla, dev, stream, steps: int, warmup: int, flush, peaks) -> 
         for c, (call, _, _, _, _) in alive.items():
             for _ in range(3):
                 call()
+            # a device-side wait first, so that the host has queued all the
+            # timed calls before the first runs: the events then time the
+            # GPU, not the host's launch gaps (the L2 stays warm)
+            torch.cuda._sleep(PAGES_LEAD_CYCLES)
             evs = []
             for _ in range(PAGES_CALLS):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -695,7 +700,8 @@ def config_records(smla, dev, stream, steps: int, warmup: int, flush, peaks) -> 
             "us_per_call": us_p, "trial_medians_us": trials[c], "roofline_frac": roof / us_p,
             "tflops": flops / (us_p * 1e-6) / 1e12, "gathered_kv_GBps": nbytes / (us_p * 1e-6) / 1e9,
             "method": f"{PAGES_TRIALS} trials, workloads rotated between trials, each the median of {PAGES_CALLS} "
-                      "warm-L2 calls after 3 warm-up calls; median of the trial medians (no L2 flush)"}
+                      "warm-L2 calls after 3 warm-up calls, queued behind a device-side wait so that the events "
+                      "time the GPU; median of the trial medians (no L2 flush)"}
     alive.clear()
     torch.cuda.empty_cache()
     return recs

@@ -66,6 +66,17 @@ def test_fp8_decode_small(smla, h_q):
     _check(smla, c, u, f"fp8 decode h={h_q}")
 
 
+@pytest.mark.parametrize("h_q,topk,page", [(1, 200, 16), (2, 72, 64), (16, 1000, 16), (128, 256, 64)])
+def test_fp8_decode_ragged_lists_small_pages(smla, h_q, topk, page):
+    """Lists whose last 64-entry block is partial (top-k not a multiple of
+    64), pages of 16 rows (a block's rows spread over several pages), one,
+    two or sixteen heads in the 16-head tile, and 128 heads (two 64-head
+    groups, dequantized in the gather)."""
+    c, u = mi.decode_case_fp8(730 + h_q, batch=3, s_next=2, h_q=h_q, lo=50, hi=1500, topk=topk, page=page,
+                              spare_pages=5)
+    _check(smla, c, u, f"fp8 decode h={h_q} topk={topk} page={page}")
+
+
 def test_fp8_decode_long_lists_split_over_ctas(smla):
     """One token whose 2048-entry list is cut over many CTAs, and a batch
     whose lists are short (mostly -1) so that many pieces are empty."""

@@ -293,6 +293,16 @@ def test_decode_page16_wide_heads(smla):
     _check_decode(smla, case)
 
 
+@pytest.mark.parametrize("h_q,topk,page", [(1, 200, 16), (2, 72, 64), (24, 1000, 16), (128, 136, 32)])
+def test_decode_ragged_lists_small_pages(smla, h_q, topk, page):
+    """Lists whose last 64-entry block is partial, pages smaller than a
+    block, and head counts at the edges of the 16-, 32- and 64-head tiles
+    (128: two head groups)."""
+    case = mi.decode_case(610 + h_q, batch=3, s_next=2, h_q=h_q, lo=50, hi=1500, topk=topk, page=page,
+                          spare_pages=5)
+    _check_decode(smla, case)
+
+
 def test_decode_one_token_cut_over_many_ctas(smla):
     """A single decode token: its 32 blocks are spread over many CTAs, each
     leaving a partial result, and merged."""

@@ -211,6 +211,40 @@ def test_varlen_small(smla, h_q):
     _check_varlen(smla, case)
 
 
+def test_varlen_chunked_lengths_and_empty_sequences(smla):
+    """Packed prefill with query and KV lengths that differ per sequence (a
+    chunk of queries over a longer KV history), a sequence with neither, one
+    with KV rows but no queries, and one with queries but no KV rows (every
+    entry masked: out 0, LSE -inf).  Lists hold distinct in-range local
+    positions, some past the sequence's KV end (masked), and -1 padding."""
+    lens_q = [100, 0, 0, 37, 10, 5]
+    lens_kv = [300, 0, 50, 0, 64, 700]
+    topk = 256
+    g = torch.Generator().manual_seed(640)
+    total_q, total_kv = sum(lens_q), sum(lens_kv)
+    q = torch.randn((total_q, 8, 576), generator=g).to(torch.bfloat16)
+    kv = torch.randn((total_kv, 576), generator=g).to(torch.bfloat16)
+    idx = torch.full((total_q, topk), -1, dtype=torch.int32)
+    t = 0
+    for lq, lk in zip(lens_q, lens_kv):
+        for _ in range(lq):
+            n = min(topk - 8, lk)
+            if n:
+                idx[t, :n] = torch.randperm(lk, generator=g)[:n].to(torch.int32)
+            idx[t, n:n + 8] = lk + torch.arange(8, dtype=torch.int32)   # past this sequence's KV end
+            t += 1
+    cu_q = torch.tensor([0] + np.cumsum(lens_q).tolist(), dtype=torch.int32)
+    cu_kv = torch.tensor([0] + np.cumsum(lens_kv).tolist(), dtype=torch.int32)
+    sm_scale = 1.0 / math.sqrt(576)
+    d = lambda x: x.to(DEV)
+    out, lse = smla.sparse_mla_fwd_varlen(d(q), d(kv), d(idx), d(cu_q), d(cu_kv), sm_scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = orc.sparse_mla_fwd_varlen(q, kv, idx, cu_q, cu_kv, sm_scale)
+    compare(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, "varlen chunked lengths")
+    masked = slice(int(cu_q[3]), int(cu_q[4]))             # queries with no KV rows
+    assert torch.all(lse[masked] == -float("inf")) and torch.all(out[masked] == 0)
+
+
 def test_varlen_config_all_tokens(smla):
     """16384 packed tokens (8192, 4096, 2048, 1024, 1024), h = 64: every
     token against the oracle (host cores), with the tight check."""

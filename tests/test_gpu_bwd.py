@@ -167,6 +167,50 @@ def test_bwd_varlen(smla, h_q):
     compare_grad(dkv.cpu().numpy(), rkv, bkv, f"varlen h={h_q} dkv")
 
 
+def test_bwd_varlen_chunked_lengths_and_empty_sequences(smla):
+    """The packed backward with query and KV lengths that differ per
+    sequence, an empty sequence, one with KV rows but no queries and one with
+    queries but no KV rows (their dq is 0), lists with entries past the
+    sequence's KV end (masked) and -1 padding."""
+    lens_q = [90, 0, 0, 23, 12, 6]
+    lens_kv = [260, 0, 40, 0, 64, 500]
+    topk = 192
+    g = torch.Generator().manual_seed(1280)
+    total_q, total_kv = sum(lens_q), sum(lens_kv)
+    q = torch.randn((total_q, 16, 576), generator=g).to(torch.bfloat16)
+    kv = torch.randn((total_kv, 576), generator=g).to(torch.bfloat16)
+    idx = torch.full((total_q, topk), -1, dtype=torch.int32)
+    t = 0
+    for lq, lk in zip(lens_q, lens_kv):
+        for _ in range(lq):
+            n = min(topk - 8, lk)
+            if n:
+                idx[t, :n] = torch.randperm(lk, generator=g)[:n].to(torch.int32)
+            idx[t, n:n + 8] = lk + torch.arange(8, dtype=torch.int32)
+            t += 1
+    cu_q = torch.tensor([0] + np.cumsum(lens_q).tolist(), dtype=torch.int32)
+    cu_kv = torch.tensor([0] + np.cumsum(lens_kv).tolist(), dtype=torch.int32)
+    sm_scale = 1.0 / 24.0
+    dout = _dout(1281, (total_q, 16, 512))
+    ro, rl = orc.sparse_mla_fwd_varlen(q, kv, idx, cu_q, cu_kv, sm_scale)
+    d = lambda x: x.to(DEV)
+    out = torch.from_numpy(ro).to(torch.bfloat16).to(DEV)
+    lse = torch.from_numpy(rl).to(torch.float32).to(DEV)
+    dq, dkv = smla.sparse_mla_bwd_varlen(d(q), d(kv), d(idx), d(cu_q), d(cu_kv), sm_scale, out, lse, d(dout))
+    torch.cuda.synchronize()
+    rq, rkv = orc.sparse_mla_bwd_varlen(q, kv, idx, cu_q, cu_kv, sm_scale, dout)
+    cq, ck = cu_q.numpy(), cu_kv.numpy()
+
+    def rows_of(t, idx_t):
+        b = int(np.searchsorted(cq, t, side="right") - 1)
+        n = int(ck[b + 1] - ck[b])
+        return int(ck[b]) + idx_t[(idx_t >= 0) & (idx_t < n)]
+    bq, bkv = grad_term_bounds(q, kv, idx, sm_scale, dout, bf16_rounding_err, rows_of=rows_of)
+    compare_grad(dq.cpu().numpy(), rq, bq, "varlen chunked dq")
+    compare_grad(dkv.cpu().numpy(), rkv, bkv, "varlen chunked dkv")
+    assert torch.all(dq[int(cq[3]):int(cq[4])] == 0)      # queries with no KV rows
+
+
 def test_bwd_mid_prefill_config_sampled(smla):
     """s_q = s_kv = 2119, h = 8, topk = 2048 (16-head units): sampled dq
     tokens and dkv rows listed by 1 to ~120 tokens."""

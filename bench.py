@@ -684,7 +684,8 @@ def config_records(smla, dev, stream, steps: int, warmup: int, flush, peaks) -> 
             # a device-side wait first, so that the host has queued all the
             # timed calls before the first runs: the events then time the
             # GPU, not the host's launch gaps (the L2 stays warm)
-            torch.cuda._sleep(PAGES_LEAD_CYCLES)
+            if hasattr(torch.cuda, "_sleep"):
+                torch.cuda._sleep(PAGES_LEAD_CYCLES)
             evs = []
             for _ in range(PAGES_CALLS):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
